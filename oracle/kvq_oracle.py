@@ -1,0 +1,416 @@
+"""Plain CPU oracle for compressed-KV decode attention.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check of
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import or run
+anything in this directory.  The GPU library never imports it and it imports
+nothing from the GPU library; the two share no code.  Inputs reach both sides
+from the seeded generators, which hold none of the method's arithmetic.
+
+Every function works on logical (unpaged) arrays: one sequence, one kv head,
+tokens in order.  Paging, packing bit order and GPU memory layout are
+implementation details of the GPU library and do not appear here.
+
+Sources (the pages this method is read from; a citation names the page and
+the section on it):
+
+* [TailorKV] "TailorKV" article, ijyty.com/news/1204784 -- §2.1 dense
+  preference score, §2.2 1-bit quantization of quantization-friendly layers
+  (the ``quant_1bit`` snippet), §2.3 dynamic loading of sparsity-friendly
+  layers (critical channels, approximate scores, top-K), §5.1 configuration
+  (sparse_ratio, critical_channels).
+* [KVSurvey] "大语言模型长上下文推理与KV Cache前沿压缩策略解析",
+  bbs.huaweicloud.com/blogs/490932 -- §一 PagedAttention (16-token blocks,
+  shared blocks), §三.1 StreamingLLM sinks + window, §三.2 H2O cumulative
+  attention scores.
+* [OnDevice] "端侧大模型KV缓存量化卸载协同：详解分层稀疏注意力与异构内存池动态迁移机制",
+  ufo.work/2026/495 -- §3.1 K per-channel asymmetric INT4/INT8, V grouped
+  (group 32/64), §3.2 fused dequant -> QK^T -> softmax -> PV.
+* [Meeting] "长上下文会议大模型推理KV缓存稀疏化与量化联合压缩：剖析重要性评分指标与异构内存分层调度策略",
+  ufo.work/2026/545 -- §3.2 softmax attention over retained tokens, §4.2
+  double-buffered prefetch, §8.1 block-sparse decode attention.
+
+Precision: the quantizer runs in IEEE fp32 (inputs are fp16 widened to fp32;
+round half to even), because its output is an integer code that both sides
+must decide in the same precision.  Attention, softmax and the dense
+preference score run in fp64.  The critical-channel score runs in fp32 in a
+fixed summation order (ascending channel), because it decides an integer
+(the top-K index set).
+
+Readings of points the pages leave open are marked READING below; the full
+list lives in the design notes of the repository.
+
+Parity pins: every function here is pinned by tests under ``tests/`` that
+check it against closed forms, invariants, brute force on tiny inputs and
+hand-worked fixtures in ``tests/golden/``.  No function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+HEAD_DIM = 128
+K_GROUP_TOKENS = 64
+
+
+# ---------------------------------------------------------------------------
+# a1: asymmetric min/max b-bit quantization   [TailorKV §2.2; OnDevice §3.1]
+# ---------------------------------------------------------------------------
+
+def quantize_groups(x16, bits):
+    """Quantize every group (the LAST axis of ``x16``) to ``bits``-bit codes.
+
+    [TailorKV §2.2] per group: scale = (max - min) / (2^b - 1), zero = min,
+    code = clamp(round((x - zero) / scale), 0, 2^b - 1); scale and zero are
+    stored as fp16.
+
+    READING: ``round`` is round-half-to-even (the snippet calls torch.round);
+    the code is computed with the unrounded fp32 scale and only the stored
+    scale is rounded to fp16 (the snippet divides first and converts the
+    scale to fp16 on return); a group with max == min gets scale 0 and all
+    codes 0 (the snippet would divide by zero).
+
+    Returns (codes int64, scale16 float16, zero16 float16, scale32 float32);
+    scale/zero have the group axis removed.
+    """
+    x = np.asarray(x16, dtype=np.float16).astype(np.float32)
+    levels = np.float32(2 ** bits - 1)
+    mn = x.min(axis=-1, keepdims=True)
+    mx = x.max(axis=-1, keepdims=True)
+    scale32 = (mx - mn) / levels                      # fp32, one rounding
+    ok = scale32 > 0
+    safe = np.where(ok, scale32, np.float32(1.0))
+    with np.errstate(over="ignore", invalid="ignore"):
+        u = (x - mn) / safe                           # fp32, two roundings
+    codes = np.clip(np.rint(u), np.float32(0), levels)
+    codes = np.where(ok, codes, np.float32(0)).astype(np.int64)
+    with np.errstate(over="ignore"):
+        scale16 = scale32[..., 0].astype(np.float16)
+    zero16 = mn[..., 0].astype(np.float16)            # exact: min of fp16 values
+    return codes, scale16, zero16, scale32[..., 0]
+
+
+def pack_k(k16, bits, group_tokens=K_GROUP_TOKENS):
+    """Quantize the keys of one (sequence, kv head): K is [T][d] fp16.
+
+    [TailorKV §2.2] keys are quantized per channel; [OnDevice §3.1] per
+    channel asymmetric with a zero point; the group runs over ``group_tokens``
+    consecutive tokens (64, [TailorKV §2.2 snippet and §5.2]).
+
+    READING: tokens past the last complete 64-token group (the "tail") stay
+    in fp16 and are attended exactly; they are quantized once the group fills.
+
+    Returns dict(codes [n_full*64][d] int64, scale16/zero16/scale32 [n_groups][d],
+    tail [T - n_full*64][d] fp16, n_packed).
+    """
+    k16 = np.asarray(k16, dtype=np.float16)
+    T, d = k16.shape
+    n_groups = T // group_tokens
+    n_packed = n_groups * group_tokens
+    g = k16[:n_packed].reshape(n_groups, group_tokens, d).transpose(0, 2, 1)  # [g][c][t]
+    codes, s16, z16, s32 = quantize_groups(g, bits)
+    codes = codes.transpose(0, 2, 1).reshape(n_packed, d)
+    return dict(codes=codes, scale16=s16, zero16=z16, scale32=s32,
+                tail=k16[n_packed:].copy(), n_packed=n_packed, bits=bits,
+                group_tokens=group_tokens)
+
+
+def pack_v(v16, bits, group_dims):
+    """Quantize the values of one (sequence, kv head): V is [T][d] fp16.
+
+    [TailorKV §2.2] values are quantized per token; [OnDevice §3.1] in groups
+    of ``group_dims`` (32 or 64) consecutive channels of head_dim.
+
+    Returns dict(codes [T][d] int64, scale16/zero16/scale32 [T][d/group_dims]).
+    """
+    v16 = np.asarray(v16, dtype=np.float16)
+    T, d = v16.shape
+    assert d % group_dims == 0
+    g = v16.reshape(T, d // group_dims, group_dims)
+    codes, s16, z16, s32 = quantize_groups(g, bits)
+    return dict(codes=codes.reshape(T, d), scale16=s16, zero16=z16, scale32=s32,
+                bits=bits, group_dims=group_dims)
+
+
+def dequant_k(pk):
+    """fp64 keys as the quantized cache represents them: zero + code * scale
+    for packed tokens (stored fp16 scale/zero), fp16 values for the tail."""
+    n_packed = pk["n_packed"]
+    gt = pk["group_tokens"]
+    d = pk["tail"].shape[1]
+    out = np.empty((n_packed + pk["tail"].shape[0], d), dtype=np.float64)
+    if n_packed:
+        grp = np.arange(n_packed) // gt
+        out[:n_packed] = (pk["zero16"].astype(np.float64)[grp]
+                          + pk["codes"].astype(np.float64) * pk["scale16"].astype(np.float64)[grp])
+    out[n_packed:] = pk["tail"].astype(np.float64)
+    return out
+
+
+def dequant_v(pv):
+    """fp64 values as the quantized cache represents them."""
+    T, d = pv["codes"].shape
+    gd = pv["group_dims"]
+    j = np.arange(d) // gd
+    return (pv["zero16"].astype(np.float64)[:, j]
+            + pv["codes"].astype(np.float64) * pv["scale16"].astype(np.float64)[:, j])
+
+
+# ---------------------------------------------------------------------------
+# exact softmax attention (shared definition used by a3, a6, a7, a8)
+# [Meeting §3.2: Softmax(Q K_ret^T / sqrt(d)) V_ret; OnDevice §3.2]
+# ---------------------------------------------------------------------------
+
+def softmax_attention(q, K, V):
+    """One query against n keys: s = K q / sqrt(d), p = softmax(s), o = p V.
+    fp64 throughout; the max is subtracted before exponentiation.
+    Returns (o [d], p [n])."""
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    s = (K @ q) / math.sqrt(q.shape[0])
+    e = np.exp(s - s.max())
+    p = e / e.sum()
+    return p @ V, p
+
+
+def kv_head_of(h, n_q_heads, n_kv_heads):
+    """GQA: q head h reads kv head floor(h * H_kv / H_q)."""
+    return (h * n_kv_heads) // n_q_heads
+
+
+# ---------------------------------------------------------------------------
+# a3: decode attention over the quantized cache   [OnDevice §3.2; TailorKV §2.2]
+# ---------------------------------------------------------------------------
+
+def decode_attn_quant(q16, packed_k, packed_v):
+    """Decode attention of every q head of one sequence over its quantized
+    cache.  ``q16`` is [H_q][d]; ``packed_k``/``packed_v`` are lists (one per
+    kv head) of ``pack_k``/``pack_v`` results.  Packed keys are dequantized,
+    tail keys are used as fp16, values are always dequantized.
+    Returns o [H_q][d] fp64."""
+    q16 = np.asarray(q16, dtype=np.float16)
+    Hq, d = q16.shape
+    Hkv = len(packed_k)
+    out = np.empty((Hq, d), dtype=np.float64)
+    cache = {}
+    for h in range(Hq):
+        g = kv_head_of(h, Hq, Hkv)
+        if g not in cache:
+            cache[g] = (dequant_k(packed_k[g]), dequant_v(packed_v[g]))
+        Kh, Vh = cache[g]
+        out[h], _ = softmax_attention(q16[h].astype(np.float64), Kh, Vh)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# a4: critical channels and approximate scores   [TailorKV §2.3]
+# ---------------------------------------------------------------------------
+
+def critical_channels(q16, absmax16, n_crit):
+    """[TailorKV §2.3] channel importance s_i = |q_i| * max_t |K_{t,i}|; the
+    n_crit most important channels (ties -> lower channel) are returned in
+    ascending channel order.  fp64 (exact for fp16 inputs)."""
+    q = np.abs(np.asarray(q16, dtype=np.float16).astype(np.float64))
+    a = np.asarray(absmax16, dtype=np.float64)
+    s = q * a
+    idx = np.arange(s.shape[0])
+    order = np.lexsort((idx, -s))        # primary: s descending, then index
+    return np.sort(order[:n_crit])
+
+
+def key_absmax(k16):
+    """max_t |K_{t,c}| over all cached tokens, per channel (fp16, exact)."""
+    return np.abs(np.asarray(k16, dtype=np.float16)).max(axis=0)
+
+
+def critical_scores(q16, k16, channels):
+    """[TailorKV §2.3] approximate attention score of every cached token from
+    the critical channels only: a_t = sum_{c in C} q_c K_{t,c}.
+    READING: fp32, summed over C in ascending channel order starting from +0.
+    Returns float32 [T]."""
+    q = np.asarray(q16, dtype=np.float16).astype(np.float32)
+    K = np.asarray(k16, dtype=np.float16)
+    acc = np.zeros(K.shape[0], dtype=np.float32)
+    for c in np.sort(np.asarray(channels)):
+        acc = acc + q[c] * K[:, c].astype(np.float32)
+    return acc
+
+
+# ---------------------------------------------------------------------------
+# a5: top-K selection with sinks and a recent window
+# [TailorKV §2.3 top-K, §5.1 sparse_ratio; KVSurvey §三.1 sinks + window]
+# ---------------------------------------------------------------------------
+
+def topk_select(scores, k, n_sink, window):
+    """Selected token ids (ascending) for one query head.
+
+    Tokens [0, n_sink) (attention sinks) and [T - window, T) (recent window)
+    are always kept; among the rest the k highest scores are added, ties ->
+    lower index.  If the sinks, window and k cover everything, all tokens are
+    selected."""
+    scores = np.asarray(scores, dtype=np.float32)
+    T = scores.shape[0]
+    if T <= n_sink + window + k:
+        return np.arange(T, dtype=np.int64)
+    cand = np.arange(n_sink, T - window)
+    order = np.lexsort((cand, -scores[cand].astype(np.float64)))
+    top = cand[order[:k]]
+    keep = np.concatenate([np.arange(n_sink), top, np.arange(T - window, T)])
+    return np.sort(keep).astype(np.int64)
+
+
+def topk_count(T, k, n_sink, window):
+    """Number of ids ``topk_select`` returns for a length-T sequence."""
+    return T if T <= n_sink + window + k else n_sink + window + k
+
+
+def ratio_k(T, ratio):
+    """K from a retention ratio: floor(ratio * T) ([TailorKV §5.1] sparse_ratio)."""
+    return int(math.floor(ratio * T))
+
+
+# ---------------------------------------------------------------------------
+# a6: exact attention over a selected token set   [Meeting §3.2, §8.1]
+# ---------------------------------------------------------------------------
+
+def sparse_attn(q16, k16, v16, ids):
+    """Exact softmax attention of one fp16 query over the fp16 K/V rows
+    ``ids``.  Returns (o [d] fp64, p [len(ids)] fp64) with p in ``ids`` order."""
+    ids = np.asarray(ids, dtype=np.int64)
+    K = np.asarray(k16, dtype=np.float16)[ids]
+    V = np.asarray(v16, dtype=np.float16)[ids]
+    return softmax_attention(np.asarray(q16, dtype=np.float16), K, V)
+
+
+# ---------------------------------------------------------------------------
+# a7: H2O cumulative attention accumulate / evict   [KVSurvey §三.2, §三.1]
+# ---------------------------------------------------------------------------
+
+def h2o_protected(pos, next_len, n_sink, window):
+    """A retained token is never evicted while it is a sink or sits in the
+    recent window of the next step (positions >= next_len - window)."""
+    pos = np.asarray(pos)
+    return (pos < n_sink) | (pos >= next_len - window)
+
+
+def h2o_evict(retained, cum, next_len, budget_after, n_sink, window):
+    """Evict unprotected tokens, lowest (cum, position) first, until at most
+    ``budget_after`` remain (or nothing unprotected is left).
+    READING: ties on the cumulative score evict the older token first.
+    Returns (kept positions, kept cum, evicted positions), keeping input order."""
+    retained = np.asarray(retained, dtype=np.int64)
+    cum = np.asarray(cum)
+    excess = retained.shape[0] - budget_after
+    if excess <= 0:
+        return retained, cum, np.empty(0, dtype=np.int64)
+    prot = h2o_protected(retained, next_len, n_sink, window)
+    cand = np.nonzero(~prot)[0]
+    order = np.lexsort((retained[cand], cum[cand].astype(np.float64)))
+    drop = cand[order[:excess]]
+    mask = np.ones(retained.shape[0], dtype=bool)
+    mask[drop] = False
+    return retained[mask], cum[mask], retained[drop]
+
+
+def h2o_accumulate32(probs32, retained, cum32, seq_len, budget, n_sink, window,
+                     new_pos):
+    """One accumulate/evict/admit update on fp32 state, for one (sequence, kv head).
+
+    ``probs32`` [G][n] fp32: this step's attention probability of every
+    retained token for each of the G query heads sharing the kv head.
+    cum += (((p_0 + p_1) + p_2) + ...) in fp32 (heads in ascending order, the
+    sum added to cum last).  Then unprotected tokens are evicted (lowest cum,
+    then lowest position) down to budget - 1 when a new token will be
+    admitted (``new_pos`` >= 0), else down to budget; the new token joins with
+    cum 0.  The window is taken relative to the next step's length
+    seq_len + 1.  Returns (retained, cum32, evicted)."""
+    probs32 = np.asarray(probs32, dtype=np.float32)
+    inc = probs32[0].copy()
+    for g in range(1, probs32.shape[0]):
+        inc = inc + probs32[g]
+    cum = np.asarray(cum32, dtype=np.float32) + inc
+    after = budget - 1 if new_pos >= 0 else budget
+    kept, kcum, ev = h2o_evict(retained, cum, seq_len + 1, after, n_sink, window)
+    if new_pos >= 0:
+        kept = np.concatenate([kept, [new_pos]])
+        kcum = np.concatenate([kcum, np.zeros(1, dtype=np.float32)])
+    return kept, kcum.astype(np.float32), ev
+
+
+def h2o_step(q16_group, k16, v16, retained, cum, seq_len, budget, n_sink, window,
+             admit_next=True):
+    """One H2O decode step in fp64 for one (sequence, kv head).
+
+    The G query heads of the group attend the retained tokens (positions
+    < seq_len; the newest token was admitted by the previous step); their
+    probabilities, summed over the group, are added to the cumulative scores
+    (a heavy-hitter score per kv head -- READING for GQA); then the lowest
+    unprotected tokens are evicted and position ``seq_len`` (the next token)
+    is admitted with score 0.  The first call, with every token retained and
+    cum 0, is the initial heavy-hitter selection over the prompt.
+    Returns (o [G][d], retained, cum, evicted)."""
+    q16_group = np.asarray(q16_group, dtype=np.float16)
+    G = q16_group.shape[0]
+    retained = np.asarray(retained, dtype=np.int64)
+    outs = []
+    inc = np.zeros(retained.shape[0], dtype=np.float64)
+    for g in range(G):
+        o, p = sparse_attn(q16_group[g], k16, v16, retained)
+        outs.append(o)
+        inc += p
+    cum = np.asarray(cum, dtype=np.float64) + inc
+    after = budget - 1 if admit_next else budget
+    kept, kcum, ev = h2o_evict(retained, cum, seq_len + 1, after, n_sink, window)
+    if admit_next:
+        kept = np.concatenate([kept, [seq_len]])
+        kcum = np.concatenate([kcum, [0.0]])
+    return np.stack(outs), kept, kcum, ev
+
+
+# ---------------------------------------------------------------------------
+# a8: dense-preference score and layer classification   [TailorKV §2.1]
+# ---------------------------------------------------------------------------
+
+def dense_pref_score(q16_recent, k16, topk):
+    """[TailorKV §2.1] P = n_q - sum over the top-k entries of every row of
+    A = softmax(Q K^T / sqrt(d_h)) for the n_q most recent queries of one head.
+
+    READING: the queries sit at the last n_q positions and attend causally
+    (query i at position T - n_q + i sees keys 0..T - n_q + i); a row shorter
+    than k contributes all of its entries.  fp64."""
+    Q = np.asarray(q16_recent, dtype=np.float16).astype(np.float64)
+    K = np.asarray(k16, dtype=np.float16).astype(np.float64)
+    n_q, d = Q.shape
+    T = K.shape[0]
+    total = 0.0
+    for i in range(n_q):
+        L = T - n_q + i + 1
+        s = (K[:L] @ Q[i]) / math.sqrt(d)
+        e = np.exp(s - s.max())
+        p = e / e.sum()
+        kk = min(topk, L)
+        total += np.sort(p)[L - kk:].sum()
+    return n_q - total
+
+
+def classify_layer(P_heads, n_q, tau):
+    """[TailorKV §2.1] READING of the comparison lost in the page text: a
+    layer is quantization-friendly when its dense-preference score, averaged
+    over heads and normalised by n_q, exceeds tau (dense attention -> large
+    P -> quantize; sparse attention -> small P -> top-K)."""
+    return float(np.mean(P_heads)) / n_q > tau
+
+
+# ---------------------------------------------------------------------------
+# a9: offload gather   [Meeting §4.2 double buffer; TailorKV §2.3, §3.1]
+# ---------------------------------------------------------------------------
+
+def offload_gather(rows16, ids):
+    """The rows ``ids`` of a host-resident fp16 [T][d] array, in ``ids`` order,
+    as raw bytes: what the host-link gather must deliver into HBM."""
+    rows16 = np.asarray(rows16, dtype=np.float16)
+    out = np.empty((len(ids), rows16.shape[1]), dtype=np.float16)
+    for i, t in enumerate(ids):
+        out[i] = rows16[int(t)]
+    return out

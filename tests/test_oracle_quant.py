@@ -1,0 +1,165 @@
+"""Pins for the oracle's quantizer (a1) against hand-worked fixtures, the
+error bound, exact rational re-encoding and per-group closed forms.
+Source: TailorKV article §2.2 (quant_1bit snippet); on-device article §3.1."""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import kvq_oracle as O
+
+pytestmark = pytest.mark.cpu
+
+
+def _load_quant_cases(golden_dir):
+    cases = []
+    with open(os.path.join(golden_dir, "quant_rounding.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            b, xs, codes, scale, zero = [c.strip() for c in line.split("|")]
+            cases.append((int(b), [float(v) for v in xs.split()],
+                          [int(v) for v in codes.split()], float(scale), float(zero)))
+    return cases
+
+
+def test_golden_rounding(golden_dir):
+    cases = _load_quant_cases(golden_dir)
+    assert len(cases) >= 6
+    for b, xs, codes, scale, zero in cases:
+        c, s16, z16, s32 = O.quantize_groups(np.array([xs], dtype=np.float16), b)
+        assert c[0].tolist() == codes, (b, xs)
+        assert float(s16[0]) == scale and float(z16[0]) == zero
+
+
+def test_golden_third_scale(golden_dir):
+    # 2-bit group [0, .25, .5, 1]: scale = fl32(1/3); quotients 0.75, 1.5, 3 after
+    # fp32 rounding -> codes 0,1,2,3 (1.5 rounds to even 2).
+    c, s16, z16, s32 = O.quantize_groups(np.array([[0.0, 0.25, 0.5, 1.0]], np.float16), 2)
+    assert c[0].tolist() == [0, 1, 2, 3]
+    assert s32[0] == np.float32(1.0) / np.float32(3.0)
+    assert s16[0] == np.float16(s32[0])
+
+
+@pytest.mark.parametrize("bits", [1, 2, 4, 8])
+def test_error_bound_and_range(bits):
+    rng = np.random.default_rng(100 + bits)
+    x = (rng.standard_normal((500, 64)) * rng.choice([1.0, 10.0], size=(500, 1))).astype(np.float16)
+    codes, s16, z16, s32 = O.quantize_groups(x, bits)
+    L = 2 ** bits - 1
+    assert codes.min() >= 0 and codes.max() <= L
+    xf = x.astype(np.float64)
+    mn = xf.min(axis=1)
+    mx = xf.max(axis=1)
+    # code(min) = 0 and code(max) = 2^b - 1
+    assert np.all(codes[np.arange(500), xf.argmin(axis=1)] == 0)
+    assert np.all(codes[np.arange(500), xf.argmax(axis=1)] == L)
+    # |x - (min + code*scale32)| <= scale32 * (1/2 + (2^b-1) 2^-23), in fp64: the
+    # fp32 quotient u <= 2^b-1 carries one rounding of at most u 2^-24.
+    slack = 0.5 + L * 2.0 ** -23
+    rec = mn[:, None] + codes * s32.astype(np.float64)[:, None]
+    err = np.abs(xf - rec)
+    assert np.all(err <= s32.astype(np.float64)[:, None] * slack)
+    assert np.max(err / s32.astype(np.float64)[:, None]) > 0.49   # the bound is tight
+    # with the stored fp16 scale: add (2^b-1) |scale32 - scale16|
+    rec16 = z16.astype(np.float64)[:, None] + codes * s16.astype(np.float64)[:, None]
+    bound = s32.astype(np.float64) * slack + L * np.abs(
+        s32.astype(np.float64) - s16.astype(np.float64))
+    assert np.all(np.abs(xf - rec16) <= bound[:, None] + 1e-12)
+    assert np.array_equal(z16.astype(np.float64), mn)
+
+
+@pytest.mark.parametrize("bits", [1, 2, 4, 8])
+def test_exact_rational_reencode(bits):
+    """Exact rational arithmetic (no fp rounding) gives the same codes except
+    where the exact quotient lies within 1e-6 of a half-integer."""
+    rng = np.random.default_rng(7 + bits)
+    x = rng.standard_normal((40, 64)).astype(np.float16)
+    codes, _, _, _ = O.quantize_groups(x, bits)
+    L = 2 ** bits - 1
+    mism = 0
+    for r in range(x.shape[0]):
+        vals = [Fraction(float(v)) for v in x[r]]
+        mn, mx = min(vals), max(vals)
+        for i, v in enumerate(vals):
+            u = (v - mn) * L / (mx - mn)
+            fl = u.numerator // u.denominator
+            frac = u - fl
+            if frac > Fraction(1, 2) or (frac == Fraction(1, 2) and fl % 2 == 1):
+                fl += 1
+            want = min(max(fl, 0), L)
+            if abs(frac - Fraction(1, 2)) < Fraction(1, 10 ** 6):
+                continue
+            mism += int(want != codes[r, i])
+    assert mism == 0
+
+
+def test_one_bit_is_midpoint_threshold():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((300, 64)).astype(np.float16)
+    codes, _, _, _ = O.quantize_groups(x, 1)
+    xf = x.astype(np.float64)
+    mn = xf.min(axis=1, keepdims=True)
+    mx = xf.max(axis=1, keepdims=True)
+    mid = (mx - mn) / 2
+    rel = (xf - mn) - mid
+    clear = np.abs(rel) > 1e-6 * (mx - mn)
+    assert np.array_equal(codes[clear], (rel > 0)[clear].astype(np.int64))
+
+
+@pytest.mark.parametrize("bits", [1, 2, 4, 8])
+def test_k_grouping_per_channel_64_tokens(bits):
+    """Group (g, c) of K holds tokens 64g..64g+63 of channel c: build K so every
+    group spans a known interval [lo, hi] and check the stored zero/scale."""
+    T, d = 64 * 3 + 10, 6
+    rng = np.random.default_rng(11)
+    lo = np.round(rng.uniform(-8, 0, size=(3, d)) * 4) / 4
+    hi = lo + np.round(rng.uniform(1, 8, size=(3, d)) * 4) / 4
+    K = np.zeros((T, d))
+    for g in range(3):
+        for c in range(d):
+            vals = rng.uniform(lo[g, c], hi[g, c], size=64)
+            vals[5] = lo[g, c]
+            vals[40] = hi[g, c]
+            K[64 * g:64 * g + 64, c] = vals
+    K[192:] = rng.standard_normal((10, d))
+    K16 = K.astype(np.float16)
+    pk = O.pack_k(K16, bits)
+    assert pk["n_packed"] == 192
+    L = 2 ** bits - 1
+    for g in range(3):
+        for c in range(d):
+            assert float(pk["zero16"][g, c]) == float(np.float16(lo[g, c]))
+            s = (np.float32(np.float16(hi[g, c])) - np.float32(np.float16(lo[g, c]))) / np.float32(L)
+            assert pk["scale32"][g, c] == s
+            assert pk["codes"][64 * g + 5, c] == 0 and pk["codes"][64 * g + 40, c] == L
+    assert np.array_equal(pk["tail"], K16[192:])
+    dq = O.dequant_k(pk)
+    assert np.array_equal(dq[192:], K16[192:].astype(np.float64))
+
+
+@pytest.mark.parametrize("gd", [32, 64])
+def test_v_grouping_per_token(gd):
+    T, d = 5, 128
+    rng = np.random.default_rng(5)
+    V = rng.standard_normal((T, d)).astype(np.float16)
+    pv = O.pack_v(V, 4, gd)
+    assert pv["zero16"].shape == (T, d // gd)
+    for t in range(T):
+        for j in range(d // gd):
+            seg = V[t, j * gd:(j + 1) * gd].astype(np.float32)
+            assert pv["zero16"][t, j] == np.float16(seg.min())
+            assert pv["scale32"][t, j] == (seg.max() - seg.min()) / np.float32(15)
+
+
+def test_sixteen_bit_is_nearly_lossless():
+    """At b=16 the only loss left is the fp16 rounding of the stored scale:
+    |x - x_hat| <= range * 2^-11 (+ the half-step range/65535/2)."""
+    rng = np.random.default_rng(9)
+    V = (rng.standard_normal((64, 128)) * 3).astype(np.float16)
+    pv = O.pack_v(V, 16, 64)
+    err = np.abs(O.dequant_v(pv) - V.astype(np.float64))
+    rng_g = np.ptp(V.astype(np.float64).reshape(64, 2, 64), axis=2).repeat(64, axis=1)
+    assert np.all(err <= rng_g * (2.0 ** -11 + 0.5 / 65535))
