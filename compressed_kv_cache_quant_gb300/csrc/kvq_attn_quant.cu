@@ -1,0 +1,339 @@
+// a3 kv_decode_attn_quant: fused dequant -> q.k/sqrt(d) -> online softmax ->
+// p.v over the quantized paged cache [OnDevice §3.2; TailorKV §2.2], with the
+// context split across CTAs and the partial softmax states merged by
+// log-sum-exp in the last CTA of every (sequence, kv head).
+//
+// One CTA = one (sequence b, kv head g, split): it walks 64-token chunks (one
+// K quantization group = four 16-token pages), stages the packed codes and
+// scales in shared memory and serves all GQ query heads of the group from
+// the same staged codes.  A chunk that holds the unfinished K group reads
+// its keys from the fp16 tail buffer.
+#include <algorithm>
+
+#include "kvq_internal.cuh"
+
+namespace {
+
+constexpr int D = KVQ_HEAD_DIM;
+constexpr int PG = KVQ_BLOCK_TOKENS;
+constexpr int KG = KVQ_K_GROUP_TOKENS;
+constexpr int NT = 128;
+constexpr int REC = 4 + D;  // partial record: m, l, pad, pad, o[128]
+
+struct QAttnArgs {
+    const uint8_t* k_codes;
+    const uint8_t* v_codes;
+    const uint32_t* k_sz;
+    const uint32_t* v_sz;
+    const uint16_t* k_tail;
+    int64_t num_blocks;
+    const int32_t* bt;
+    const int32_t* seq_lens;
+    int32_t max_blocks;
+    int32_t max_len;
+    int32_t H;     // kv heads
+    int32_t G;     // V group dims
+    const uint16_t* q;
+    float* out;
+    float* part;
+    int32_t* counters;
+    KvqWsHeader* hdr;
+    int32_t n_splits;
+    int32_t cps;   // chunks per split
+};
+
+__device__ __forceinline__ float2 unpack_sz(uint32_t w) {
+    return make_float2(kvq_h2f((uint16_t)(w & 0xffffu)), kvq_h2f((uint16_t)(w >> 16)));
+}
+
+template <int BITS, int GQ>
+__global__ void __launch_bounds__(NT) qattn_kernel(QAttnArgs a) {
+    constexpr int WPR = 4 * BITS;            // 32-bit words per token row
+    constexpr int U4_PAGE = PG * WPR / 4;    // uint4 per page of codes
+    __shared__ __align__(16) uint32_t kc[KG * WPR];
+    __shared__ __align__(16) uint32_t vc[KG * WPR];
+    __shared__ float2 vsz[KG * 4];           // (scale, zero) per token and V group
+    __shared__ float2 ksz[D];                // (scale, zero) per channel of the K group
+    __shared__ __align__(16) float qf[D * GQ];   // q[c][h]
+    __shared__ __align__(16) float ps[KG * GQ];  // p[t][h]
+    __shared__ float red[NT / 32][GQ];
+    __shared__ float m_run[GQ], l_run[GQ], alpha_s[GQ];
+    __shared__ int32_t pages[4];
+    __shared__ int is_last;
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = a.seq_lens[b];
+    const int n_full = T / KG;
+    const int n_chunks = (T + KG - 1) / KG;
+    const int nsplit_b = (n_chunks + a.cps - 1) / a.cps;
+    const int Hq = a.H * GQ;
+    if (T > a.max_len || T < 0) {
+        if (tid == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
+        return;
+    }
+    if (n_chunks == 0) {  // empty sequence: output 0
+        if (split == 0)
+            for (int i = tid; i < GQ * D; i += NT) a.out[((int64_t)b * Hq + g * GQ) * D + i] = 0.0f;
+        return;
+    }
+    if (split >= nsplit_b) return;
+    const int c_begin = split * a.cps;
+    const int c_end = min(n_chunks, c_begin + a.cps);
+    const int NGV = D / a.G;
+
+    // q of the group's heads as fp32, layout [c][h]
+    for (int i = tid; i < GQ * D; i += NT) {
+        const int h = i / D, c = i % D;
+        qf[c * GQ + h] = kvq_h2f(a.q[((int64_t)b * Hq + g * GQ + h) * D + c]);
+    }
+    if (tid < GQ) {
+        m_run[tid] = -INFINITY;
+        l_run[tid] = 0.0f;
+    }
+    float o[GQ];
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) o[h] = 0.0f;
+
+    const int t_loc = tid >> 1;   // token of this thread in the QK phase
+    const int half = tid & 1;     // channel half of this thread in the QK phase
+
+    for (int ch = c_begin; ch < c_end; ++ch) {
+        const int t0 = ch * KG;
+        const int n_tok = min(KG, T - t0);
+        const bool packed = ch < n_full;
+        const int n_pages = (n_tok + PG - 1) / PG;
+        __syncthreads();  // previous chunk fully consumed
+        if (tid < 4) {
+            int32_t p = 0;
+            if (tid < n_pages) {
+                p = a.bt[(int64_t)b * a.max_blocks + ch * 4 + tid];
+                if (p < 0 || p >= a.num_blocks) {
+                    kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
+                    p = 0;
+                }
+            }
+            pages[tid] = p;
+        }
+        __syncthreads();
+        // stage codes and scales of the chunk
+        for (int u = tid; u < n_pages * U4_PAGE; u += NT) {
+            const int j = u / U4_PAGE, r = u % U4_PAGE;
+            const int64_t base = ((int64_t)pages[j] * a.H + g) * PG * WPR;  // in words
+            reinterpret_cast<uint4*>(vc)[u] = reinterpret_cast<const uint4*>(a.v_codes)[base / 4 + r];
+            if (packed) reinterpret_cast<uint4*>(kc)[u] = reinterpret_cast<const uint4*>(a.k_codes)[base / 4 + r];
+        }
+        for (int u = tid; u < n_tok * NGV; u += NT) {
+            const int t = u / NGV, j = u % NGV;
+            const int64_t slot = ((int64_t)pages[t / PG] * a.H + g) * PG + (t % PG);
+            vsz[t * NGV + j] = unpack_sz(a.v_sz[slot * NGV + j]);
+        }
+        if (packed) ksz[tid] = unpack_sz(a.k_sz[((int64_t)pages[0] * a.H + g) * D + tid]);
+        __syncthreads();
+
+        // ---- scores: thread (t_loc, half) covers channels [64 half, 64 half + 64)
+        float acc[GQ];
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) acc[h] = 0.0f;
+        const bool valid = t_loc < n_tok;
+        if (valid) {
+            if (packed) {
+                const uint32_t* row = kc + t_loc * WPR;
+#pragma unroll 8
+                for (int c = 64 * half; c < 64 * half + 64; ++c) {
+                    const float2 sz = ksz[c];
+                    const float kh = fmaf(sz.x, (float)kvq_get_code<BITS>(row, c), sz.y);
+#pragma unroll
+                    for (int h = 0; h < GQ; ++h) acc[h] = fmaf(qf[c * GQ + h], kh, acc[h]);
+                }
+            } else {
+                const uint16_t* krow = a.k_tail + (((int64_t)b * a.H + g) * KG + t_loc) * D;
+#pragma unroll 8
+                for (int c = 64 * half; c < 64 * half + 64; ++c) {
+                    const float kh = kvq_h2f(krow[c]);
+#pragma unroll
+                    for (int h = 0; h < GQ; ++h) acc[h] = fmaf(qf[c * GQ + h], kh, acc[h]);
+                }
+            }
+        }
+        float s[GQ];
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 1);
+            s[h] = valid ? acc[h] * KVQ_SCORE_LOG2_SCALE : -INFINITY;
+            const float wm = kvq_warp_max(s[h]);
+            if (lane == 0) red[warp][h] = wm;
+        }
+        __syncthreads();
+        if (tid < GQ) {
+            float cm = red[0][tid];
+            for (int w = 1; w < NT / 32; ++w) cm = fmaxf(cm, red[w][tid]);
+            const float m_new = fmaxf(m_run[tid], cm);
+            alpha_s[tid] = exp2f(m_run[tid] - m_new);
+            m_run[tid] = m_new;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            const float p = valid ? exp2f(s[h] - m_run[h]) : 0.0f;
+            if (half == 0 && t_loc < KG) ps[t_loc * GQ + h] = p;
+            float ws = kvq_warp_sum(half == 0 ? p : 0.0f);
+            if (lane == 0) red[warp][h] = ws;
+        }
+        __syncthreads();
+        if (tid < GQ) {
+            float lsum = 0.0f;
+            for (int w = 0; w < NT / 32; ++w) lsum += red[w][tid];
+            l_run[tid] = l_run[tid] * alpha_s[tid] + lsum;
+        }
+        // ---- p.v: thread = channel d
+        {
+            const int d = tid;
+            const int jg = d / a.G;
+#pragma unroll
+            for (int h = 0; h < GQ; ++h) o[h] *= alpha_s[h];
+#pragma unroll 4
+            for (int t = 0; t < n_tok; ++t) {
+                const float2 sz = vsz[t * NGV + jg];
+                const float vh = fmaf(sz.x, (float)kvq_get_code<BITS>(vc + t * WPR, d), sz.y);
+#pragma unroll
+                for (int h = 0; h < GQ; ++h) o[h] = fmaf(ps[t * GQ + h], vh, o[h]);
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- partial state of this split
+    const int64_t rec0 = (((int64_t)b * a.H + g) * a.n_splits + split) * GQ;
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+        float* r = a.part + (rec0 + h) * REC;
+        if (tid == 0) {
+            r[0] = m_run[h];
+            r[1] = l_run[h];
+        }
+        r[4 + tid] = o[h];
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int prev = atomicAdd(&a.counters[b * a.H + g], 1);
+        is_last = (prev == nsplit_b - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // ---- last CTA of (b, g): merge the splits by log-sum-exp
+    for (int h = 0; h < GQ; ++h) {
+        float M = -INFINITY;
+        for (int sp = 0; sp < nsplit_b; ++sp) {
+            const float* r = a.part + ((((int64_t)b * a.H + g) * a.n_splits + sp) * GQ + h) * REC;
+            M = fmaxf(M, __ldcg(r));
+        }
+        float Lsum = 0.0f, acc = 0.0f;
+        for (int sp = 0; sp < nsplit_b; ++sp) {
+            const float* r = a.part + ((((int64_t)b * a.H + g) * a.n_splits + sp) * GQ + h) * REC;
+            const float w = exp2f(__ldcg(r) - M);
+            Lsum = fmaf(__ldcg(r + 1), w, Lsum);
+            acc = fmaf(__ldcg(r + 4 + tid), w, acc);
+        }
+        a.out[((int64_t)b * Hq + g * GQ + h) * D + tid] = acc / Lsum;
+    }
+    if (tid == 0) a.counters[b * a.H + g] = 0;
+}
+
+struct Plan {
+    int n_splits;
+    int cps;
+};
+
+Plan plan_splits(const kvq_layout* L, const kvq_seqs* S) {
+    const int n_chunks = (std::max(S->max_len, 1) + KG - 1) / KG;
+    const int64_t units = (int64_t)std::max(S->batch, 1) * L->n_kv_heads;
+    const int64_t target = 8LL * kvq_num_sms();  // resident CTAs to aim for
+    int splits = (int)std::max<int64_t>(1, (target + units - 1) / units);
+    int cps = std::max(4, (n_chunks + splits - 1) / splits);
+    cps = std::min(cps, n_chunks);
+    splits = (n_chunks + cps - 1) / cps;
+    return {splits, cps};
+}
+
+size_t ws_layout(const kvq_layout* L, const kvq_seqs* S, size_t* off_part, size_t* off_cnt) {
+    const Plan p = plan_splits(L, S);
+    const int GQ = L->n_q_heads / L->n_kv_heads;
+    const size_t recs = (size_t)std::max(S->batch, 1) * L->n_kv_heads * p.n_splits * GQ;
+    *off_part = sizeof(KvqWsHeader);
+    *off_cnt = kvq_round_up(*off_part + recs * REC * sizeof(float), 256);
+    return kvq_round_up(*off_cnt + (size_t)std::max(S->batch, 1) * L->n_kv_heads * sizeof(int32_t), 256);
+}
+
+template <int BITS>
+void launch_bits(int gq, dim3 grid, cudaStream_t s, const QAttnArgs& a) {
+    switch (gq) {
+        case 1: qattn_kernel<BITS, 1><<<grid, NT, 0, s>>>(a); break;
+        case 2: qattn_kernel<BITS, 2><<<grid, NT, 0, s>>>(a); break;
+        case 4: qattn_kernel<BITS, 4><<<grid, NT, 0, s>>>(a); break;
+        default: qattn_kernel<BITS, 8><<<grid, NT, 0, s>>>(a); break;
+    }
+}
+
+}  // namespace
+
+extern "C" size_t kv_decode_attn_quant_ws(const kvq_layout* L, const kvq_seqs* S) {
+    if (kvq_check_layout(L, "kv_decode_attn_quant_ws", true) || kvq_check_seqs_sizes(S, "kv_decode_attn_quant_ws"))
+        return 0;
+    size_t a, c;
+    return ws_layout(L, S, &a, &c);
+}
+
+extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
+                                    float* out, void* ws, size_t ws_bytes, void* stream) {
+    kvq_clear_error();
+    int st = kvq_check_layout(L, "kv_decode_attn_quant", true);
+    if (st) return st;
+    st = kvq_check_seqs(S, "kv_decode_attn_quant");
+    if (st) return st;
+    KVQ_REQUIRE(L->bits != 16, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: layer is not quantized (bits == 16)");
+    KVQ_REQUIRE(P != nullptr && P->k_codes && P->v_codes && P->k_sz && P->v_sz && P->k_tail, KVQ_ERR_INVALID_ARG,
+                "kv_decode_attn_quant: quantized pool arrays missing");
+    KVQ_REQUIRE(((uintptr_t)P->k_codes & 15u) == 0 && ((uintptr_t)P->v_codes & 15u) == 0, KVQ_ERR_INVALID_ARG,
+                "kv_decode_attn_quant: code arrays must be 16-byte aligned");
+    KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: batch exceeds max_seqs");
+    size_t off_part, off_cnt;
+    const size_t need = ws_layout(L, S, &off_part, &off_cnt);
+    st = kvq_check_ws(ws, ws_bytes, need, "kv_decode_attn_quant");
+    if (st) return st;
+    if (S->batch == 0) return KVQ_OK;
+    KVQ_REQUIRE(q && out && S->block_table, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: NULL q/out/block table");
+    const Plan p = plan_splits(L, S);
+    QAttnArgs a;
+    a.k_codes = P->k_codes;
+    a.v_codes = P->v_codes;
+    a.k_sz = reinterpret_cast<const uint32_t*>(P->k_sz);
+    a.v_sz = reinterpret_cast<const uint32_t*>(P->v_sz);
+    a.k_tail = P->k_tail;
+    a.num_blocks = P->num_blocks;
+    a.bt = S->block_table;
+    a.seq_lens = S->seq_lens;
+    a.max_blocks = S->max_blocks;
+    a.max_len = S->max_len;
+    a.H = L->n_kv_heads;
+    a.G = L->v_group_dims;
+    a.q = q;
+    a.out = out;
+    a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + off_part);
+    a.counters = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + off_cnt);
+    a.hdr = static_cast<KvqWsHeader*>(ws);
+    a.n_splits = p.n_splits;
+    a.cps = p.cps;
+    const int gq = L->n_q_heads / L->n_kv_heads;
+    dim3 grid(p.n_splits, L->n_kv_heads, S->batch);
+    cudaStream_t s = kvq_stream(stream);
+    switch (L->bits) {
+        case 1: launch_bits<1>(gq, grid, s, a); break;
+        case 2: launch_bits<2>(gq, grid, s, a); break;
+        case 4: launch_bits<4>(gq, grid, s, a); break;
+        default: launch_bits<8>(gq, grid, s, a); break;
+    }
+    return kvq_launch_status("kv_decode_attn_quant");
+}

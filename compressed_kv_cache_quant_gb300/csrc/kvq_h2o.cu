@@ -1,0 +1,508 @@
+// a7 kv_h2o_accumulate [KVSurvey §三.2, §三.1] and a8 kv_dense_pref_score
+// [TailorKV §2.1].
+#include <algorithm>
+
+#include "kvq_internal.cuh"
+
+namespace {
+
+constexpr int D = KVQ_HEAD_DIM;
+constexpr int PG = KVQ_BLOCK_TOKENS;
+
+// ================================================================ a7 H2O accumulate / evict / admit
+
+constexpr int HA_NT = 1024;
+
+struct H2OArgs {
+    const float* probs;
+    int32_t* retained;
+    int32_t* count;
+    float* cum;
+    int32_t cap;
+    int32_t budget, n_sink, window;
+    const int32_t* new_pos;
+    int32_t* n_evicted;
+    const int32_t* seq_lens;
+    int32_t H, GQ;
+    KvqWsHeader* hdr;
+};
+
+// Eviction order: lowest cumulative score first, then lowest position.
+__device__ __forceinline__ unsigned long long evict_key(float cum, int32_t pos) {
+    return ((unsigned long long)kvq_float_key(cum) << 32) | (uint32_t)pos;
+}
+
+__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, v, o);
+        v = y < v ? y : v;
+    }
+    return v;
+}
+
+__device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    uint32_t s = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
+    return s;
+}
+
+__global__ void __launch_bounds__(HA_NT) h2o_kernel(H2OArgs a) {
+    __shared__ uint32_t red[HA_NT / 32];
+    __shared__ unsigned long long redk[HA_NT / 32];
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t s_bin, s_below;
+    __shared__ uint32_t wsum[HA_NT / 32];
+    const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    const int Hq = a.H * a.GQ;
+    const int64_t base = ((int64_t)b * a.H + g) * a.cap;
+    int32_t* ret = a.retained + base;
+    float* cum = a.cum + base;
+    int n = a.count[(int64_t)b * a.H + g];
+    if (n < 0 || n > a.cap) {
+        if (tid == 0) kvq_dev_flag(a.hdr, KVQ_DEV_OVERFLOW, b);
+        n = max(0, min(n, a.cap));
+    }
+    const int T = a.seq_lens[b];
+    const int next_len = T + 1;
+    // 1. cum += p_0 + p_1 + ... (the group's heads in ascending order, fp32)
+    for (int i = tid; i < n; i += HA_NT) {
+        float inc = a.probs[((int64_t)b * Hq + g * a.GQ) * a.cap + i];
+        for (int hh = 1; hh < a.GQ; ++hh) inc += a.probs[((int64_t)b * Hq + g * a.GQ + hh) * a.cap + i];
+        cum[i] = cum[i] + inc;
+    }
+    __syncthreads();
+    // 2. evict unprotected tokens, lowest (cum, position) first
+    const int newp = a.new_pos ? a.new_pos[b] : -1;
+    const int target = newp >= 0 ? a.budget - 1 : a.budget;
+    const int excess = n - target;
+    int evicted = 0;
+    auto is_protected = [&](int32_t pos) { return pos < a.n_sink || pos >= next_len - a.window; };
+    if (excess == 1) {
+        unsigned long long best = ~0ull;
+        for (int i = tid; i < n; i += HA_NT) {
+            const int32_t pos = ret[i];
+            if (!is_protected(pos)) {
+                const unsigned long long k = evict_key(cum[i], pos);
+                best = k < best ? k : best;
+            }
+        }
+        best = warp_min_u64(best);
+        if ((tid & 31) == 0) redk[tid >> 5] = best;
+        __syncthreads();
+        if (tid < 32) {
+            unsigned long long v = redk[tid];
+            v = warp_min_u64(v);
+            if (tid == 0) redk[0] = v;
+        }
+        __syncthreads();
+        const unsigned long long kmin = redk[0];
+        __syncthreads();
+        if (kmin != ~0ull) {
+            // positions are unique: exactly one entry carries the minimum
+            __shared__ int s_idx;
+            if (tid == 0) s_idx = -1;
+            __syncthreads();
+            for (int i = tid; i < n; i += HA_NT)
+                if (!is_protected(ret[i]) && evict_key(cum[i], ret[i]) == kmin) s_idx = i;
+            __syncthreads();
+            if (tid == 0 && s_idx >= 0) {
+                ret[s_idx] = ret[n - 1];
+                cum[s_idx] = cum[n - 1];
+            }
+            __syncthreads();
+            n -= 1;
+            evicted = 1;
+        }
+    } else if (excess > 1) {
+        uint32_t n_un = 0;
+        for (int i = tid; i < n; i += HA_NT) n_un += !is_protected(ret[i]);
+        const uint32_t U = block_sum_u32(n_un, red);
+        unsigned long long thr;
+        if (U <= (uint32_t)excess) {
+            thr = ~0ull;  // every unprotected token goes
+        } else {
+            // radix select of the excess-th smallest 64-bit key among unprotected tokens
+            unsigned long long prefix = 0ull, mask = 0ull;
+            uint32_t remaining = (uint32_t)excess;
+            for (int pass = 0; pass < 8; ++pass) {
+                const int shift = 56 - 8 * pass;
+                for (int i = tid; i < 256; i += HA_NT) hist[i] = 0u;
+                __syncthreads();
+                for (int i = tid; i < n; i += HA_NT) {
+                    const int32_t pos = ret[i];
+                    if (is_protected(pos)) continue;
+                    const unsigned long long k = evict_key(cum[i], pos);
+                    if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255ull], 1u);
+                }
+                __syncthreads();
+                if (tid < 32) {
+                    // lane l owns bins [8l, 8l + 7]; lane 0 the smallest
+                    uint32_t ls = 0;
+                    for (int j = 0; j < 8; ++j) ls += hist[8 * tid + j];
+                    uint32_t incl = ls;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (tid >= o) incl += y;
+                    }
+                    const uint32_t ballot = __ballot_sync(0xffffffffu, incl >= remaining);
+                    const int l = __ffs(ballot) - 1;
+                    if (tid == l) {
+                        uint32_t run = incl - ls;
+                        for (int j = 0; j < 8; ++j) {
+                            const int bin = 8 * tid + j;
+                            if (run + hist[bin] >= remaining) {
+                                s_bin = (uint32_t)bin;
+                                s_below = run;
+                                break;
+                            }
+                            run += hist[bin];
+                        }
+                    }
+                }
+                __syncthreads();
+                remaining -= s_below;
+                prefix |= (unsigned long long)s_bin << shift;
+                mask |= 255ull << shift;
+                __syncthreads();
+            }
+            thr = prefix;
+        }
+        // order-preserving in-place compaction of the kept entries
+        uint32_t out_base = 0;
+        for (int t0 = 0; t0 < n; t0 += HA_NT) {
+            const int i = t0 + tid;
+            int32_t pos = 0;
+            float cv = 0.0f;
+            uint32_t keep = 0;
+            if (i < n) {
+                pos = ret[i];
+                cv = cum[i];
+                keep = is_protected(pos) || evict_key(cv, pos) > thr;
+            }
+            uint32_t tile_total;
+            // exclusive scan of `keep` over the CTA
+            const int lane = tid & 31, warp = tid >> 5;
+            uint32_t x = keep;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            __syncthreads();
+            if (lane == 31) wsum[warp] = x;
+            __syncthreads();
+            if (warp == 0) {
+                uint32_t w = wsum[lane];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+                    if (lane >= o) w += y;
+                }
+                wsum[lane] = w;
+            }
+            __syncthreads();
+            tile_total = wsum[HA_NT / 32 - 1];
+            const uint32_t before = x - keep + (warp > 0 ? wsum[warp - 1] : 0u);
+            if (keep) {
+                ret[out_base + before] = pos;
+                cum[out_base + before] = cv;
+            }
+            out_base += tile_total;
+            __syncthreads();
+        }
+        evicted = n - (int)out_base;
+        n = (int)out_base;
+    }
+    // 3. admit the next token with score 0
+    if (tid == 0) {
+        if (newp >= 0) {
+            if (n < a.cap) {
+                ret[n] = newp;
+                cum[n] = 0.0f;
+                ++n;
+            } else {
+                kvq_dev_flag(a.hdr, KVQ_DEV_OVERFLOW, b);
+            }
+        }
+        a.count[(int64_t)b * a.H + g] = n;
+        if (a.n_evicted) a.n_evicted[(int64_t)b * a.H + g] = evicted;
+    }
+}
+
+// ================================================================ a8 dense-preference score
+
+constexpr int DP_NT = 256;
+constexpr int DP_MAX_T = 49152;
+
+struct DPArgs {
+    const uint16_t* k16;
+    int64_t num_blocks;
+    const int32_t* bt;
+    const int32_t* seq_lens;
+    int32_t max_blocks, max_len;
+    int32_t H, GQ;
+    const uint16_t* q;
+    int32_t n_q, topk;
+    float* P;
+    float* rows;        // [B][H_q][n_q] per-query top-k mass
+    int32_t* counters;  // [B][H_q]
+    KvqWsHeader* hdr;
+};
+
+__device__ __forceinline__ float block_reduce_max(float v, float* red) {
+    v = kvq_warp_max(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = fmaxf(r, red[w]);
+    return r;
+}
+
+__device__ __forceinline__ float block_reduce_sum(float v, float* red) {
+    v = kvq_warp_sum(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r += red[w];
+    return r;
+}
+
+__global__ void __launch_bounds__(DP_NT) dense_pref_kernel(DPArgs a) {
+    extern __shared__ float sc[];  // scores of the row, log2 domain
+    __shared__ float qf[D];
+    __shared__ float redf[DP_NT / 32];
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t s_bin, s_above;
+    __shared__ int is_last;
+    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+    const int g = h / a.GQ;
+    const int Hq = a.H * a.GQ;
+    const int T = a.seq_lens[b];
+    const int L = T - a.n_q + i + 1;  // keys seen by query i
+    float r_i = 0.0f;
+    if (T > a.max_len || L <= 0) {
+        if (tid == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
+    } else {
+        if (tid < D) qf[tid] = kvq_h2f(a.q[(((int64_t)b * Hq + h) * a.n_q + i) * D + tid]) * KVQ_SCORE_LOG2_SCALE;
+        __syncthreads();
+        const int hw = tid >> 4, l16 = tid & 15;
+        for (int t0 = 0; t0 < L; t0 += DP_NT / 16) {
+            const int t = t0 + hw;
+            float acc = 0.0f;
+            if (t < L) {
+                int32_t page = a.bt[(int64_t)b * a.max_blocks + (t >> 4)];
+                if (page < 0 || page >= a.num_blocks) {
+                    if (l16 == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, t);
+                    page = 0;
+                }
+                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+                    a.k16 + (((int64_t)page * a.H + g) * PG + (t & 15)) * D + 8 * l16));
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc = fmaf(qf[8 * l16 + 2 * j], kvq_h2f((uint16_t)(w[j] & 0xffffu)), acc);
+                    acc = fmaf(qf[8 * l16 + 2 * j + 1], kvq_h2f((uint16_t)(w[j] >> 16)), acc);
+                }
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (t < L && l16 == 0) sc[t] = acc;
+        }
+        __syncthreads();
+        float mx = -INFINITY;
+        for (int t = tid; t < L; t += DP_NT) mx = fmaxf(mx, sc[t]);
+        mx = block_reduce_max(mx, redf);
+        float z = 0.0f;
+        for (int t = tid; t < L; t += DP_NT) z += exp2f(sc[t] - mx);
+        z = block_reduce_sum(z, redf);
+        const int kk = min(a.topk, L);
+        // radix select of the kk-th largest score
+        uint32_t prefix = 0u, mask = 0u, remaining = (uint32_t)kk;
+        for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            for (int j = tid; j < 256; j += DP_NT) hist[j] = 0u;
+            __syncthreads();
+            for (int t = tid; t < L; t += DP_NT) {
+                const uint32_t key = kvq_float_key(sc[t]);
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            }
+            __syncthreads();
+            if (tid < 32) {
+                uint32_t ls = 0;
+                for (int j = 0; j < 8; ++j) ls += hist[255 - 8 * tid - j];
+                uint32_t incl = ls;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o) incl += y;
+                }
+                const uint32_t ballot = __ballot_sync(0xffffffffu, incl >= remaining);
+                const int l = __ffs(ballot) - 1;
+                if (tid == l) {
+                    uint32_t run = incl - ls;
+                    for (int j = 0; j < 8; ++j) {
+                        const int bin = 255 - 8 * tid - j;
+                        if (run + hist[bin] >= remaining) {
+                            s_bin = (uint32_t)bin;
+                            s_above = run;
+                            break;
+                        }
+                        run += hist[bin];
+                    }
+                }
+            }
+            __syncthreads();
+            remaining -= s_above;
+            prefix |= s_bin << shift;
+            mask |= 255u << shift;
+            __syncthreads();
+        }
+        // top-k mass: every score above the k-th, plus the k-th value for the remaining slots
+        float top = 0.0f, kth_val = 0.0f;
+        uint32_t n_gt = 0;
+        for (int t = tid; t < L; t += DP_NT) {
+            const uint32_t key = kvq_float_key(sc[t]);
+            if (key > prefix) {
+                top += exp2f(sc[t] - mx);
+                ++n_gt;
+            } else if (key == prefix) {
+                kth_val = sc[t];
+            }
+        }
+        top = block_reduce_sum(top, redf);
+        n_gt = (uint32_t)block_reduce_sum((float)n_gt, redf);
+        // kth_val: any thread that saw the k-th key holds it
+        __shared__ float s_kth;
+        __syncthreads();
+        for (int t = tid; t < L; t += DP_NT)
+            if (kvq_float_key(sc[t]) == prefix) s_kth = sc[t];
+        __syncthreads();
+        kth_val = s_kth;
+        top += (float)(kk - (int)n_gt) * exp2f(kth_val - mx);
+        r_i = top / z;
+    }
+    // per-query mass -> workspace; the last CTA of (b, h) forms P = n_q - sum_i r_i
+    if (tid == 0) a.rows[((int64_t)b * Hq + h) * a.n_q + i] = r_i;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int prev = atomicAdd(&a.counters[(int64_t)b * Hq + h], 1);
+        is_last = (prev == a.n_q - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    if (tid == 0) {
+        double s = 0.0;
+        for (int j = 0; j < a.n_q; ++j) s += (double)__ldcg(a.rows + ((int64_t)b * Hq + h) * a.n_q + j);
+        a.P[(int64_t)b * Hq + h] = (float)((double)a.n_q - s);
+        a.counters[(int64_t)b * Hq + h] = 0;
+    }
+}
+
+size_t dp_ws_layout(const kvq_layout* L, const kvq_seqs* S, int32_t n_q, size_t* off_rows, size_t* off_cnt) {
+    const size_t rows = (size_t)std::max(S->batch, 1) * L->n_q_heads * (size_t)std::max(n_q, 1);
+    *off_rows = sizeof(KvqWsHeader);
+    *off_cnt = kvq_round_up(*off_rows + rows * sizeof(float), 256);
+    return kvq_round_up(*off_cnt + (size_t)std::max(S->batch, 1) * L->n_q_heads * sizeof(int32_t), 256);
+}
+
+}  // namespace
+
+// ================================================================ ABI
+
+extern "C" size_t kv_h2o_accumulate_ws(void) { return sizeof(KvqWsHeader); }
+
+extern "C" int kv_h2o_accumulate(const kvq_layout* L, const kvq_seqs* S, const float* probs, int32_t* retained,
+                                 int32_t* retained_count, float* cum, int32_t cap, int32_t budget, int32_t n_sink,
+                                 int32_t window, const int32_t* new_pos, int32_t* n_evicted, void* ws,
+                                 size_t ws_bytes, void* stream) {
+    kvq_clear_error();
+    int st = kvq_check_layout(L, "kv_h2o_accumulate", true);
+    if (st) return st;
+    st = kvq_check_seqs(S, "kv_h2o_accumulate");
+    if (st) return st;
+    st = kvq_check_ws(ws, ws_bytes, kv_h2o_accumulate_ws(), "kv_h2o_accumulate");
+    if (st) return st;
+    KVQ_REQUIRE(probs && retained && retained_count && cum, KVQ_ERR_INVALID_ARG, "kv_h2o_accumulate: NULL buffer");
+    KVQ_REQUIRE(cap > 0 && budget >= 1 && budget <= cap && n_sink >= 0 && window >= 0, KVQ_ERR_INVALID_ARG,
+                "kv_h2o_accumulate: need 1 <= budget <= cap, n_sink >= 0, window >= 0");
+    if (S->batch == 0) return KVQ_OK;
+    H2OArgs a;
+    a.probs = probs;
+    a.retained = retained;
+    a.count = retained_count;
+    a.cum = cum;
+    a.cap = cap;
+    a.budget = budget;
+    a.n_sink = n_sink;
+    a.window = window;
+    a.new_pos = new_pos;
+    a.n_evicted = n_evicted;
+    a.seq_lens = S->seq_lens;
+    a.H = L->n_kv_heads;
+    a.GQ = L->n_q_heads / L->n_kv_heads;
+    a.hdr = static_cast<KvqWsHeader*>(ws);
+    h2o_kernel<<<dim3(L->n_kv_heads, S->batch), HA_NT, 0, kvq_stream(stream)>>>(a);
+    return kvq_launch_status("kv_h2o_accumulate");
+}
+
+extern "C" size_t kv_dense_pref_score_ws(const kvq_layout* L, const kvq_seqs* S, int32_t n_q) {
+    if (kvq_check_layout(L, "kv_dense_pref_score_ws", true) || kvq_check_seqs_sizes(S, "kv_dense_pref_score_ws")) return 0;
+    size_t a, c;
+    return dp_ws_layout(L, S, n_q, &a, &c);
+}
+
+extern "C" int kv_dense_pref_score(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q_recent,
+                                   int32_t n_q, int32_t topk, float* Pout, void* ws, size_t ws_bytes, void* stream) {
+    kvq_clear_error();
+    int st = kvq_check_layout(L, "kv_dense_pref_score", true);
+    if (st) return st;
+    st = kvq_check_seqs(S, "kv_dense_pref_score");
+    if (st) return st;
+    KVQ_REQUIRE(P && P->k16, KVQ_ERR_INVALID_ARG, "kv_dense_pref_score: pool needs k16");
+    KVQ_REQUIRE(((uintptr_t)P->k16 & 15u) == 0, KVQ_ERR_INVALID_ARG, "kv_dense_pref_score: k16 must be 16-byte aligned");
+    KVQ_REQUIRE(n_q >= 1 && n_q <= S->max_len && topk >= 1, KVQ_ERR_INVALID_ARG,
+                "kv_dense_pref_score: need 1 <= n_q <= max_len and topk >= 1");
+    KVQ_REQUIRE(S->max_len <= DP_MAX_T, KVQ_ERR_UNSUPPORTED, "kv_dense_pref_score: max_len above %d", DP_MAX_T);
+    size_t off_rows, off_cnt;
+    const size_t need = dp_ws_layout(L, S, n_q, &off_rows, &off_cnt);
+    st = kvq_check_ws(ws, ws_bytes, need, "kv_dense_pref_score");
+    if (st) return st;
+    if (S->batch == 0) return KVQ_OK;
+    KVQ_REQUIRE(q_recent && Pout && S->block_table, KVQ_ERR_INVALID_ARG, "kv_dense_pref_score: NULL buffer");
+    DPArgs a;
+    a.k16 = P->k16;
+    a.num_blocks = P->num_blocks;
+    a.bt = S->block_table;
+    a.seq_lens = S->seq_lens;
+    a.max_blocks = S->max_blocks;
+    a.max_len = S->max_len;
+    a.H = L->n_kv_heads;
+    a.GQ = L->n_q_heads / L->n_kv_heads;
+    a.q = q_recent;
+    a.n_q = n_q;
+    a.topk = topk;
+    a.P = Pout;
+    a.rows = reinterpret_cast<float*>(static_cast<char*>(ws) + off_rows);
+    a.counters = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + off_cnt);
+    a.hdr = static_cast<KvqWsHeader*>(ws);
+    const size_t smem = (size_t)std::max(S->max_len, 1) * sizeof(float);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(dense_pref_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             DP_MAX_T * (int)sizeof(float));
+        if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_dense_pref_score: %s", cudaGetErrorString(e));
+    }
+    dense_pref_kernel<<<dim3(n_q, L->n_q_heads, S->batch), DP_NT, smem, kvq_stream(stream)>>>(a);
+    return kvq_launch_status("kv_dense_pref_score");
+}

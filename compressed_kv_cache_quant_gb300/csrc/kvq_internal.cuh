@@ -1,0 +1,108 @@
+// Internal helpers shared by the libkvq translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+#define KVQ_ABI_VERSION 1
+
+// ---------------------------------------------------------------- host side
+
+// Records a thread-local error message and returns `code`.
+int kvq_fail(int code, const char* fmt, ...);
+// Clears the thread-local error text.
+void kvq_clear_error();
+// Number of SMs of the current device (cached per device); 152 when no device.
+int kvq_num_sms();
+// Maps a launch / runtime error of the last launch to KVQ_ERR_CUDA.
+int kvq_launch_status(const char* what);
+
+#define KVQ_REQUIRE(cond, code, ...)            \
+    do {                                        \
+        if (!(cond)) return kvq_fail((code), __VA_ARGS__); \
+    } while (0)
+
+static inline cudaStream_t kvq_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Workspace header: the first 256 bytes of every workspace.
+struct KvqWsHeader {
+    int32_t status;      // 0 = clean; otherwise the first failing check
+    int32_t detail;      // an index describing the failure
+    int32_t pad[62];
+};
+static_assert(sizeof(KvqWsHeader) == 256, "workspace header is 256 bytes");
+
+// Device status codes written to KvqWsHeader::status.
+enum KvqDeviceCheck : int32_t {
+    KVQ_DEV_OK = 0,
+    KVQ_DEV_BAD_PAGE = 1,       // block table entry outside [0, num_blocks)
+    KVQ_DEV_BAD_INDEX = 2,      // selected / retained id outside [0, seq_len)
+    KVQ_DEV_BAD_LENGTH = 3,     // seq_len outside [0, max_len] or capacity
+    KVQ_DEV_OVERFLOW = 4,       // a list would exceed its capacity
+};
+
+static inline size_t kvq_round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- device side
+
+__device__ __forceinline__ void kvq_dev_flag(KvqWsHeader* h, int32_t code, int32_t detail) {
+    if (h != nullptr && atomicCAS(&h->status, 0, code) == 0) h->detail = detail;
+}
+
+__device__ __forceinline__ float kvq_h2f(uint16_t x) { return __half2float(__ushort_as_half(x)); }
+__device__ __forceinline__ uint16_t kvq_f2h(float x) { return __half_as_ushort(__float2half_rn(x)); }
+
+// Order-preserving map of an fp32 value to uint32 (larger float -> larger key);
+// -0 and +0 share one key.
+__device__ __forceinline__ uint32_t kvq_float_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u << 1) == 0u) u = 0u;  // -0 -> +0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Quantizer arithmetic, IEEE fp32 with explicit round-to-nearest operations:
+// scale = (max - min) / (2^b - 1); code = clamp(rint((x - min) / scale), 0, 2^b - 1).
+__device__ __forceinline__ float kvq_scale32(float mn, float mx, float levels) {
+    return __fdiv_rn(__fsub_rn(mx, mn), levels);
+}
+__device__ __forceinline__ uint32_t kvq_code(float x, float mn, float scale32, float levels) {
+    if (!(scale32 > 0.0f)) return 0u;
+    float u = __fdiv_rn(__fsub_rn(x, mn), scale32);
+    float r = rintf(u);
+    r = fminf(fmaxf(r, 0.0f), levels);
+    return (uint32_t)r;
+}
+
+// Reads the b-bit code of channel c from a token row held as 32-bit words.
+template <int BITS>
+__device__ __forceinline__ uint32_t kvq_get_code(const uint32_t* row, int c) {
+    const int bit = c * BITS;
+    return (row[bit >> 5] >> (bit & 31)) & ((1u << BITS) - 1u);
+}
+
+__device__ __forceinline__ float kvq_warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float kvq_warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// log2(e) / sqrt(128): scores are kept in the log2 domain, p = exp2(s - m).
+#define KVQ_SCORE_LOG2_SCALE 0.12751743074048468f
+
+// Validates the fields of a layout shared by all calls.  need_q: the call
+// reads query heads (H_q / H_kv must be 1, 2, 4 or 8).
+int kvq_check_layout(const kvq_layout* L, const char* fn, bool need_q);
+// Validates the batch descriptor (pointers, sizes).
+int kvq_check_seqs(const kvq_seqs* S, const char* fn);
+// Validates only the sizes of a batch descriptor (for workspace queries).
+int kvq_check_seqs_sizes(const kvq_seqs* S, const char* fn);
+// Validates a workspace pointer / size pair against the required size.
+int kvq_check_ws(void* ws, size_t ws_bytes, size_t need, const char* fn);

@@ -1,0 +1,356 @@
+/*
+ * kvq.h -- C ABI of libkvq: compressed-KV decode attention on one GB300 GPU.
+ *
+ * The library implements the decode-step hot path of a compressed KV cache:
+ * asymmetric b-bit packing, paged 16-token blocks, fused dequant attention,
+ * the sparse-layer path (critical-channel scores, top-K with sinks and a
+ * recent window, exact attention over the selection), the H2O cumulative
+ * score update and the dense-preference layer score.
+ *
+ * Sources cited below (page, then section):
+ *   [TailorKV]  "TailorKV" article, ijyty.com/news/1204784
+ *   [KVSurvey]  "大语言模型长上下文推理与KV Cache前沿压缩策略解析",
+ *               bbs.huaweicloud.com/blogs/490932
+ *   [OnDevice]  "端侧大模型KV缓存量化卸载协同：详解分层稀疏注意力与异构内存池动态迁移机制",
+ *               ufo.work/2026/495
+ *   [Meeting]   "长上下文会议大模型推理KV缓存稀疏化与量化联合压缩：剖析重要性评分指标与异构内存分层调度策略",
+ *               ufo.work/2026/545
+ *
+ * Conventions shared by every call
+ *   - Every function returns an int status: KVQ_OK (0) or a negative KVQ_ERR_*.
+ *     kvq_last_error() returns a message for the calling thread's last failure.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     rejected call launches nothing.
+ *   - The caller owns every buffer.  The library never allocates or frees
+ *     device memory.  Pointers documented "device" must be device-accessible
+ *     (cudaMalloc / torch CUDA tensors); "host" pointers are ordinary memory;
+ *     "mapped" pointers are pinned host memory the GPU can read.
+ *   - Device calls are asynchronous on the given stream (a cudaStream_t passed
+ *     as void*; NULL is the legacy default stream).
+ *   - fp16 data is IEEE binary16 passed as uint16_t.  head_dim d is 128.
+ *   - Workspaces ("ws") are device buffers of at least the size the matching
+ *     *_ws() function returns, 256-byte aligned, ZERO-FILLED BEFORE FIRST USE.
+ *     The library leaves them zeroed after every call that completes, so they
+ *     can be reused; after a call that failed on the device, zero them again.
+ *     Two calls that share a workspace must not run concurrently.
+ *   - Data-dependent device errors (a page id outside the pool, a selected id
+ *     outside the sequence) skip the faulty access and set a status word in
+ *     the workspace; kvq_check() reads and clears it.  Nothing traps.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_OK                 0
+#define KVQ_ERR_INVALID_ARG   -1
+#define KVQ_ERR_UNSUPPORTED   -2
+#define KVQ_ERR_CUDA          -3
+#define KVQ_ERR_NO_SPACE      -4
+#define KVQ_ERR_TIMEOUT       -5
+#define KVQ_ERR_DEVICE_CHECK  -6
+
+#define KVQ_HEAD_DIM          128
+#define KVQ_BLOCK_TOKENS      16
+#define KVQ_K_GROUP_TOKENS    64
+
+/* Thread-local text of the last error of the calling thread ("" if none). */
+const char* kvq_last_error(void);
+
+/* ABI version; bumped whenever a struct or signature below changes. */
+int kvq_version(void);
+
+/* ------------------------------------------------------------------------
+ * Descriptors (plain structs, passed by host pointer, read during the call).
+ * ---------------------------------------------------------------------- */
+
+/* Geometry of one layer's cache. */
+typedef struct kvq_layout {
+    int32_t head_dim;        /* d; must be 128 */
+    int32_t n_q_heads;       /* H_q; a multiple of n_kv_heads, H_q / H_kv <= 8 */
+    int32_t n_kv_heads;      /* H_kv; q head h reads kv head floor(h * H_kv / H_q) */
+    int32_t block_tokens;    /* tokens per page; must be 16 [KVSurvey §一.1] */
+    int32_t bits;            /* 1, 2, 4, 8: quantized layer; 16: fp16 layer */
+    int32_t k_group_tokens;  /* K quantization group along tokens; must be 64 [TailorKV §2.2] */
+    int32_t v_group_dims;    /* V quantization group along head_dim: 32, 64 or 128 [OnDevice §3.1] */
+} kvq_layout;
+
+/* Device storage of one layer.  Fields a layer kind does not use may be NULL.
+ * Pages are indexed by physical page id p in [0, num_blocks); per-sequence
+ * state is indexed by the sequence's batch index b in [0, max_seqs).
+ *
+ * Quantized layer (bits in {1,2,4,8}); R = d*bits/8 bytes per token row:
+ *   k_codes [num_blocks][H_kv][16][R]   uint8; K codes, token rows
+ *   v_codes [num_blocks][H_kv][16][R]   uint8; V codes, token rows
+ *     Within a row the code of channel c occupies bits [c*bits, (c+1)*bits)
+ *     of the row read as little-endian 32-bit words.
+ *   k_sz    [num_blocks][H_kv][d][2]    fp16 (scale, zero) of the 64-token K
+ *           group whose FIRST page is p (entries of other pages are unused)
+ *   v_sz    [num_blocks][H_kv][16][d/G][2]  fp16 (scale, zero) per token and
+ *           V group of G = v_group_dims channels
+ *   k_tail  [max_seqs][H_kv][64][d]     fp16 keys of the unfinished K group
+ *           (tokens 64*floor(T/64) .. T-1 at rows t mod 64)
+ * fp16 layer (bits == 16):
+ *   k16, v16 [num_blocks][H_kv][16][d]  fp16 token rows
+ *   kT       [max_seqs][H_kv][d][t_cap] fp16 channel-major copy of K, the
+ *            "critical key" buffer read by kv_critical_score (t_cap % 8 == 0)
+ *   k_absmax [max_seqs][H_kv][d]        fp32 running max_t |K[t][c]|
+ */
+typedef struct kvq_pool {
+    int64_t   num_blocks;
+    int32_t   max_seqs;
+    int32_t   t_cap;
+    uint8_t*  k_codes;
+    uint8_t*  v_codes;
+    uint16_t* k_sz;
+    uint16_t* v_sz;
+    uint16_t* k_tail;
+    uint16_t* k16;
+    uint16_t* v16;
+    uint16_t* kT;
+    float*    k_absmax;
+} kvq_pool;
+
+/* The batch of sequences a call works on.  Sequence b owns pool slot b. */
+typedef struct kvq_seqs {
+    const int32_t* block_table;  /* device [batch][max_blocks]: physical page of
+                                    logical page j (tokens 16j..16j+15) */
+    const int32_t* seq_lens;     /* device [batch]: tokens in the cache, counting
+                                    the newest one */
+    int32_t batch;               /* B <= max_seqs */
+    int32_t max_blocks;          /* row stride of block_table */
+    int32_t max_len;             /* host upper bound on every seq_lens[b]; sizes
+                                    grids and workspaces (<= 16 * max_blocks) */
+    int32_t reserved;
+} kvq_seqs;
+
+/* ------------------------------------------------------------------------
+ * a1: kv_quant_pack -- write a run of prompt tokens into a layer's cache.
+ * [TailorKV §2.2] scale = (max - min)/(2^b - 1), zero = min,
+ * code = clamp(round((x - zero)/scale), 0, 2^b - 1), scale/zero kept as fp16;
+ * K per channel over 64-token groups, V per token over G-channel groups
+ * [OnDevice §3.1].  Arithmetic: IEEE fp32 on fp16 inputs, codes computed
+ * with the fp32 scale, round half to even; a group with max == min gets
+ * scale 0 and codes 0.
+ *
+ * Writes tokens t_start .. t_start+n_tokens-1 of sequence `seq`.  k and v are
+ * device fp16 [n_tokens][H_kv][d] with `stride_t` elements between tokens
+ * (>= H_kv*d).  t_start must be a multiple of 64.  Complete 64-token K groups
+ * are quantized into k_codes/k_sz; the keys of a final partial group go to
+ * k_tail; every token's V is quantized.  For an fp16 layer (bits == 16) the
+ * rows go to k16/v16, kT and k_absmax (absmax is raised, never lowered).
+ * Pages block_table[seq][t/16] must be allocated.  No workspace.
+ * Errors: INVALID_ARG (NULL/shape/alignment), UNSUPPORTED (d, bits, G), CUDA.
+ * ---------------------------------------------------------------------- */
+int kv_quant_pack(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                  int32_t seq, int64_t t_start, int64_t n_tokens,
+                  const uint16_t* k, const uint16_t* v, int64_t stride_t,
+                  void* stream);
+
+/* ------------------------------------------------------------------------
+ * a2: kv_page_append -- append one decode token to every sequence.
+ * [KVSurvey §一.1] paged blocks of 16 tokens through a per-sequence block
+ * table; quantization as in kv_quant_pack.
+ *
+ * k_new, v_new: device fp16 [batch][H_kv][d].  The token is written at
+ * position seq_lens[b] - 1 (seq_lens already counts it; see kvq_seq_lens_add).
+ * Quantized layer: V is quantized at once; K goes to k_tail and, when it
+ * completes a 64-token group, the group is quantized into its four pages.
+ * fp16 layer: the rows go to k16/v16, kT and k_absmax.
+ * The page of the new token must be allocated and not shared (copy it first
+ * with kv_page_copy if its reference count is above one).
+ * ws: kv_page_append_ws() bytes (status word only).
+ * ---------------------------------------------------------------------- */
+int kv_page_append(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                   const uint16_t* k_new, const uint16_t* v_new,
+                   void* ws, size_t ws_bytes, void* stream);
+size_t kv_page_append_ws(void);
+
+/* ------------------------------------------------------------------------
+ * a3: kv_decode_attn_quant -- fused dequant -> q.k/sqrt(d) -> softmax -> p.v
+ * over the quantized cache [OnDevice §3.2; TailorKV §2.2].
+ *
+ * q: device fp16 [batch][H_q][d]; out: device fp32 [batch][H_q][d].
+ * Packed tokens use dequantized K (zero + code*scale with the stored fp16
+ * scale/zero); tail tokens use their fp16 keys exactly; V is dequantized.
+ * fp32 accumulation; the context is split across CTAs and the partial
+ * softmax states are merged by log-sum-exp.  An empty sequence gives 0.
+ * ws: kv_decode_attn_quant_ws(layout, seqs) bytes.
+ * ---------------------------------------------------------------------- */
+int kv_decode_attn_quant(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                         const uint16_t* q, float* out,
+                         void* ws, size_t ws_bytes, void* stream);
+size_t kv_decode_attn_quant_ws(const kvq_layout* layout, const kvq_seqs* seqs);
+
+/* ------------------------------------------------------------------------
+ * a4: kv_critical_score -- approximate token scores from critical channels
+ * [TailorKV §2.3]: s_c = |q_c| * max_t |K[t][c]| picks the n_crit channels
+ * with the largest s_c (ties -> lower channel); then for every cached token
+ * a_t = sum over those channels, in ascending channel order, of q_c*K[t][c],
+ * in fp32 starting from +0.
+ *
+ * Reads kT and k_absmax of an fp16 layer.  q: device fp16 [batch][H_q][d].
+ * crit (optional, may be NULL): device int32 [batch][H_q][n_crit], ascending.
+ * scores: device fp32 [batch][H_q][score_stride], entries t < seq_lens[b]
+ * written.  1 <= n_crit <= 128; score_stride >= max_len, multiple of 4.
+ * ---------------------------------------------------------------------- */
+int kv_critical_score(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                      const uint16_t* q, int32_t n_crit, int32_t* crit,
+                      float* scores, int64_t score_stride, void* stream);
+
+/* ------------------------------------------------------------------------
+ * a5: kv_topk_select -- token selection per query head [TailorKV §2.3, §5.1;
+ * KVSurvey §三.1]: tokens [0, n_sink) and [T-window, T) are always kept;
+ * among the others the k highest scores (ties -> lower position) are added;
+ * if n_sink + window + k >= T every token is kept.  Output ids ascending.
+ *
+ * scores: device fp32 [batch][n_heads][score_stride].  k = k_fixed when
+ * k_fixed >= 0, else floor(ratio * T) computed in double with T = seq_lens[b].
+ * sel: device int32 [batch][n_heads][sel_cap]; sel_count: device int32
+ * [batch][n_heads].  sel_cap must hold the largest selection.
+ * T <= 8 * 49152 per call (UNSUPPORTED above).
+ * ws: kv_topk_select_ws() bytes (status word only).
+ * ---------------------------------------------------------------------- */
+int kv_topk_select(const kvq_seqs* seqs, int32_t n_heads,
+                   const float* scores, int64_t score_stride,
+                   int32_t k_fixed, double ratio, int32_t n_sink, int32_t window,
+                   int32_t* sel, int32_t sel_cap, int32_t* sel_count,
+                   void* ws, size_t ws_bytes, void* stream);
+size_t kv_topk_select_ws(void);
+
+/* ------------------------------------------------------------------------
+ * a6: kv_sparse_attn -- exact softmax attention over selected tokens
+ * [Meeting §3.2: Softmax(Q K_ret^T / sqrt(d)) V_ret; Meeting §8.1].
+ *
+ * Reads fp16 rows k16/v16 through the block table.  q: device fp16
+ * [batch][H_q][d]; out: device fp32 [batch][H_q][d].
+ * sel_per_kv_head == 0: sel is [batch][H_q][sel_cap], one list per q head;
+ * sel_per_kv_head == 1: sel is [batch][H_kv][sel_cap], shared by the q heads
+ * of the group (each row is read once for the whole group).
+ * sel_count has the matching [batch][heads] shape; ids must be < seq_lens[b]
+ * (others are skipped and flagged).  probs (optional): device fp32
+ * [batch][H_q][sel_cap], the softmax probability of every listed token, in
+ * list order.  An empty list gives 0.
+ * ws: kv_sparse_attn_ws(layout, seqs, sel_cap) bytes.
+ * ---------------------------------------------------------------------- */
+int kv_sparse_attn(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                   const uint16_t* q, const int32_t* sel, int32_t sel_cap,
+                   const int32_t* sel_count, int32_t sel_per_kv_head,
+                   float* out, float* probs,
+                   void* ws, size_t ws_bytes, void* stream);
+size_t kv_sparse_attn_ws(const kvq_layout* layout, const kvq_seqs* seqs, int32_t sel_cap);
+
+/* ------------------------------------------------------------------------
+ * a7: kv_h2o_accumulate -- H2O heavy-hitter bookkeeping [KVSurvey §三.2, §三.1].
+ *
+ * Per (sequence b, kv head g) a retained list (unordered) of token positions
+ * retained[b][g][0..n) with cumulative scores cum[b][g][0..n), n =
+ * retained_count[b][g] <= cap.  probs: device fp32 [batch][H_q][cap] from
+ * kv_sparse_attn with sel_per_kv_head == 1 on that list.
+ *   1. cum[i] += p_0[i] + p_1[i] + ... (the group's heads summed in ascending
+ *      order in fp32, then added to cum).
+ *   2. With T = seq_lens[b], protected tokens are sinks (pos < n_sink) and
+ *      the next step's window (pos >= T + 1 - window).  Unprotected tokens
+ *      are evicted, lowest (cum, position) first, until n <= budget - 1 when
+ *      new_pos is given, else n <= budget.
+ *   3. If new_pos (device int32 [batch], may be NULL) has new_pos[b] >= 0,
+ *      that position is appended with cum 0.
+ * Eviction keeps the list order except that a single eviction moves the last
+ * entry into the freed slot.  n_evicted (optional): device int32
+ * [batch][H_kv], evictions of this call.
+ * ws: kv_h2o_accumulate_ws() bytes (status word only).
+ * ---------------------------------------------------------------------- */
+int kv_h2o_accumulate(const kvq_layout* layout, const kvq_seqs* seqs,
+                      const float* probs, int32_t* retained, int32_t* retained_count,
+                      float* cum, int32_t cap, int32_t budget, int32_t n_sink, int32_t window,
+                      const int32_t* new_pos, int32_t* n_evicted,
+                      void* ws, size_t ws_bytes, void* stream);
+size_t kv_h2o_accumulate_ws(void);
+
+/* ------------------------------------------------------------------------
+ * a8: kv_dense_pref_score -- [TailorKV §2.1] P = n_q - sum over the n_q most
+ * recent queries of the sum of the top-k entries of softmax(q K^T/sqrt(d)).
+ * Query i sits at position T - n_q + i and sees keys 0..T-n_q+i (causal);
+ * a row shorter than topk contributes all its entries.
+ *
+ * Reads fp16 keys k16 through the block table.  q_recent: device fp16
+ * [batch][H_q][n_q][d]; P: device fp32 [batch][H_q].  The layer is
+ * quantization-friendly when mean_h P/n_q > tau (decided by the caller).
+ * n_q <= T; T <= 49152.
+ * ws: kv_dense_pref_score_ws(layout, seqs, n_q) bytes.
+ * ---------------------------------------------------------------------- */
+int kv_dense_pref_score(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                        const uint16_t* q_recent, int32_t n_q, int32_t topk, float* P,
+                        void* ws, size_t ws_bytes, void* stream);
+size_t kv_dense_pref_score_ws(const kvq_layout* layout, const kvq_seqs* seqs, int32_t n_q);
+
+/* ------------------------------------------------------------------------
+ * a9: kv_offload_gather -- copy selected fp16 K and V rows of an offloaded
+ * layer from host memory into an HBM staging buffer laid out as pages, so
+ * that kv_sparse_attn can read it through an identity block table
+ * [Meeting §4.2 double buffer; TailorKV §2.3, §3.1].
+ *
+ * src_k, src_v: mapped (or device) fp16 [n_heads][src_stride_h / d rows][d];
+ * row t of head h is at src + h*src_stride_h + t*d.
+ * sel: device int32 [batch=1][n_heads][sel_cap] ids, sel_count [n_heads].
+ * dst_k, dst_v: device fp16 pages [ceil(sel_cap/16)][n_heads][16][d]; list
+ * entry i of head h lands in page i/16, slot i%16.
+ * ws: kv_offload_gather_ws() bytes (status word only).
+ * ---------------------------------------------------------------------- */
+int kv_offload_gather(const uint16_t* src_k, const uint16_t* src_v, int64_t src_stride_h,
+                      int64_t src_rows, int32_t n_heads,
+                      const int32_t* sel, int32_t sel_cap, const int32_t* sel_count,
+                      uint16_t* dst_k, uint16_t* dst_v,
+                      void* ws, size_t ws_bytes, void* stream);
+size_t kv_offload_gather_ws(void);
+
+/* ------------------------------------------------------------------------
+ * Device helpers.
+ * ---------------------------------------------------------------------- */
+
+/* seq_lens[b] += delta for b < batch (device int32), on the stream. */
+int kvq_seq_lens_add(int32_t* seq_lens, int32_t batch, int32_t delta, void* stream);
+
+/* Copy-on-write support [KVSurvey §一.2]: copy every array of page src to
+ * page dst (both in [0, num_blocks)) for the layer described by layout/pool. */
+int kv_page_copy(const kvq_layout* layout, const kvq_pool* pool, int32_t src, int32_t dst,
+                 void* stream);
+
+/* Synchronizes the stream, reads and clears the status word of a workspace.
+ * Returns KVQ_OK, KVQ_ERR_DEVICE_CHECK (with the failing check in
+ * kvq_last_error) or KVQ_ERR_CUDA. */
+int kvq_check(void* ws, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Host page allocator [KVSurvey §一.1-§一.2]: free list of physical pages,
+ * allocation on demand, reference counts for pages shared between sequences
+ * (prefix sharing).  Pure host code; thread-compatible (one thread at a time
+ * per allocator).
+ * ---------------------------------------------------------------------- */
+typedef struct kvq_allocator kvq_allocator;
+
+/* seed == 0: pages handed out in ascending id order; otherwise in an order
+ * shuffled by a splitmix64 sequence from `seed`. */
+kvq_allocator* kvq_alloc_create(int64_t num_blocks, uint64_t seed);
+void    kvq_alloc_destroy(kvq_allocator* a);
+/* n pages with reference count 1 into ids[0..n); KVQ_ERR_NO_SPACE (nothing
+ * taken) when fewer than n are free. */
+int     kvq_block_alloc(kvq_allocator* a, int32_t n, int32_t* ids);
+/* Add a reference (another sequence shares the page). */
+int     kvq_block_ref(kvq_allocator* a, int32_t id);
+/* Drop a reference; the page returns to the free list at zero. */
+int     kvq_block_free(kvq_allocator* a, int32_t id);
+/* Reference count of a page (0 = free), or a negative error. */
+int     kvq_block_refcount(const kvq_allocator* a, int32_t id);
+int64_t kvq_alloc_num_free(const kvq_allocator* a);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,105 @@
+"""Host-side checks of the C ABI (no GPU compute): the library loads, exports
+every function include/kvq.h declares, validates arguments before launching
+anything, and its host page allocator keeps free lists and reference counts."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from compressed_kv_cache_quant_gb300 import _abi, kvq
+from compressed_kv_cache_quant_gb300.build import build
+
+pytestmark = pytest.mark.cpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return kvq.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b((?:kv|kvq)_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_function(lib):
+    names = header_functions()
+    assert len(names) >= 28
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_abi.PROTOTYPES), set(names) ^ set(_abi.PROTOTYPES)
+    assert lib.kvq_version() == _abi.ABI_VERSION
+
+
+def test_validation_rejects_before_launch(lib):
+    L = kvq.make_layout(8, 2, 1, 64)
+    P = _abi.Pool()
+    S = _abi.Seqs(None, None, 0, 0, 0, 0)
+    by = ctypes.byref
+    # NULL layout / unsupported geometry / bad group size
+    assert lib.kv_decode_attn_quant(None, by(P), by(S), None, None, None, 0, None) == _abi.KVQ_ERR_INVALID_ARG
+    bad = kvq.make_layout(8, 2, 3, 64)
+    assert lib.kv_decode_attn_quant(by(bad), by(P), by(S), None, None, None, 0, None) == _abi.KVQ_ERR_UNSUPPORTED
+    assert "bits" in _abi.last_error()
+    bad = kvq.make_layout(8, 2, 4, 48)
+    assert lib.kv_quant_pack(by(bad), by(P), by(S), 0, 0, 0, None, None, 0, None) == _abi.KVQ_ERR_UNSUPPORTED
+    bad = kvq.make_layout(6, 4, 4, 64)
+    assert lib.kv_sparse_attn(by(bad), by(P), by(S), None, None, 1, None, 0, None, None, None, 0, None) \
+        == _abi.KVQ_ERR_INVALID_ARG
+    # missing pool arrays
+    assert lib.kv_decode_attn_quant(by(L), by(P), by(S), None, None, None, 0, None) == _abi.KVQ_ERR_INVALID_ARG
+    # workspace too small / misaligned
+    assert lib.kv_page_append(by(L), by(P), by(S), None, None, 256, 16, None) == _abi.KVQ_ERR_INVALID_ARG
+    assert lib.kv_topk_select(by(S), 1, None, 0, 1, 0.0, 0, 0, None, 1, None, 8, 256, None) \
+        == _abi.KVQ_ERR_INVALID_ARG
+    # too-long context for the cluster top-k
+    S2 = _abi.Seqs(None, None, 0, 100000, 8 * 49152 + 8, 0)
+    assert lib.kv_topk_select(by(S2), 1, 1024, 8 * 49152 + 8, 1, 0.0, 0, 0, 1024, 1, 1024, 256, 256, None) \
+        == _abi.KVQ_ERR_UNSUPPORTED
+    # max_len beyond the block table
+    S3 = _abi.Seqs(None, None, 0, 2, 33, 0)
+    assert lib.kv_page_append(by(L), by(P), by(S3), None, None, 256, 256, None) == _abi.KVQ_ERR_INVALID_ARG
+
+
+def test_workspace_sizes(lib):
+    L = kvq.make_layout(32, 8, 1, 64)
+    S = _abi.Seqs(None, None, 1, 8200, 131136, 0)
+    n = lib.kv_decode_attn_quant_ws(ctypes.byref(L), ctypes.byref(S))
+    assert n >= 256 and n % 256 == 0
+    m = lib.kv_sparse_attn_ws(ctypes.byref(L), ctypes.byref(S), 4064)
+    assert m >= 256 and m % 256 == 0
+    assert lib.kv_page_append_ws() == 256 and lib.kv_topk_select_ws() == 256
+
+
+def test_allocator_free_list_and_refcounts(lib):
+    a = kvq.Allocator(10, seed=0)
+    assert a.alloc(3) == [0, 1, 2]
+    assert a.num_free() == 7
+    a.ref(1)
+    assert a.refcount(1) == 2
+    a.free(1)
+    assert a.refcount(1) == 1 and a.num_free() == 7
+    a.free(1)
+    assert a.refcount(1) == 0 and a.num_free() == 8
+    assert a.alloc(1) == [1]          # most recently freed page is reused first
+    with pytest.raises(kvq.KvqError) as e:
+        a.alloc(8)
+    assert e.value.code == _abi.KVQ_ERR_NO_SPACE
+    assert a.num_free() == 7          # a failed allocation takes nothing
+    with pytest.raises(kvq.KvqError):
+        a.free(9)                     # never allocated
+    with pytest.raises(kvq.KvqError):
+        a.ref(9)
+
+
+def test_allocator_shuffled_is_a_permutation(lib):
+    a = kvq.Allocator(1000, seed=42)
+    ids = a.alloc(1000)
+    assert sorted(ids) == list(range(1000)) and ids != list(range(1000))
+    b = kvq.Allocator(1000, seed=42)
+    assert b.alloc(1000) == ids        # seeded: reproducible
