@@ -340,7 +340,10 @@ def main():
     stream = torch.cuda.Stream(device)
     torch.cuda.synchronize()
 
-    # ---- capture one full step
+    # ---- one eager step (first launches set kernel attributes), then capture one full step
+    with torch.cuda.stream(stream):
+        W.step(stream.cuda_stream)
+    stream.synchronize()
     g_step = W.capture(W.step, stream)
 
     def feed(i):

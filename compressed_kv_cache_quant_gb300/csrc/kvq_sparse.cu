@@ -62,6 +62,7 @@ struct CritArgs {
     const float* absmax;
     int32_t t_cap;
     const int32_t* seq_lens;
+    int32_t max_len;
     int32_t H, GQ;
     const uint16_t* q;
     int32_t n_crit;
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(CS_NT) crit_score_kernel(CritArgs a) {
     const int tid = threadIdx.x;
     const int g = h / a.GQ;
     const int Hq = a.H * a.GQ;
-    const int T = min(a.seq_lens[b], a.t_cap);
+    const int T = max(0, min(a.seq_lens[b], min(a.t_cap, a.max_len)));  // lengths past the buffers are cut
     if (tile > 0 && tile * CS_TILE >= T) return;
     if (tid < D) {
         const float qv = kvq_h2f(a.q[((int64_t)b * Hq + h) * D + tid]);
@@ -317,6 +318,7 @@ struct SAArgs {
     const int32_t* bt;
     const int32_t* seq_lens;
     int32_t max_blocks;
+    int32_t max_len;
     int32_t H, GQ;
     const uint16_t* q;
     const int32_t* sel;
@@ -342,7 +344,11 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
     const int Hq = a.H * a.GQ;
     const int g = a.per_kv ? list : list / a.GQ;
     const int h0 = a.per_kv ? list * a.GQ : list;
-    const int T = a.seq_lens[b];
+    int T = a.seq_lens[b];
+    if (T > a.max_len) {  // ids are checked against min(seq_len, max_len): the block table's reach
+        if (tid == 0 && split == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
+        T = a.max_len;
+    }
     int n = a.sel_count[(int64_t)b * n_lists + list];
     if (n > a.sel_cap || n < 0) {
         if (tid == 0 && split == 0) kvq_dev_flag(a.hdr, KVQ_DEV_OVERFLOW, b);
@@ -592,6 +598,7 @@ extern "C" int kv_critical_score(const kvq_layout* L, const kvq_pool* P, const k
     a.absmax = P->k_absmax;
     a.t_cap = P->t_cap;
     a.seq_lens = S->seq_lens;
+    a.max_len = S->max_len;
     a.H = L->n_kv_heads;
     a.GQ = L->n_q_heads / L->n_kv_heads;
     a.q = q;
@@ -686,6 +693,7 @@ extern "C" int kv_sparse_attn(const kvq_layout* L, const kvq_pool* P, const kvq_
     a.bt = S->block_table;
     a.seq_lens = S->seq_lens;
     a.max_blocks = S->max_blocks;
+    a.max_len = S->max_len;
     a.H = L->n_kv_heads;
     a.GQ = L->n_q_heads / L->n_kv_heads;
     a.q = q;
