@@ -144,16 +144,20 @@ class Workload:
         self.out = torch.zeros((n_layers, 1, HQ, D), device=device)
         self.ws_app = kvq.Workspace(kvq.kv_page_append_ws())
         self.ws_q = kvq.Workspace(kvq.kv_decode_attn_quant_ws(self.layers[0], self.batch))
-        self.ws_sel = kvq.Workspace(kvq.kv_topk_select_ws())
-        self.ws_sa = kvq.Workspace(kvq.kv_sparse_attn_ws(self.layers[-1], self.batch, self.sel_cap))
-        self.launches_per_step = 1 + n_layers + 1 + 3 * (n_layers - 1)
+        self.ws_sc = kvq.Workspace(kvq.kv_append_critical_score_ws())
+        self.ws_sx = kvq.Workspace(kvq.kv_select_sparse_attn_ws())
+        self.hist = torch.zeros((1, HQ, 4096), dtype=torch.int32, device=device)
+        self.launches_per_step = 1 + 2 + 2 * (n_layers - 1)
 
     def step(self, stream):
+        """One decode step: append + attention in every layer.  Layer 0: page
+        append and fused dequant attention; sparse layers: the fused append +
+        critical score (+ key histogram), then the fused top-K + attention."""
         kvq, b = self.kvq, self.batch
         kvq.kvq_seq_lens_add(b.seq_lens, 1, stream)
         for l, c in enumerate(self.layers):
-            kvq.kv_page_append(c, b, self.in_k[l], self.in_v[l], self.ws_app, stream)
             if l == 0:
+                kvq.kv_page_append(c, b, self.in_k[l], self.in_v[l], self.ws_app, stream)
                 kvq.kv_decode_attn_quant(c, b, self.in_q[l], self.out[l], self.ws_q, stream)
             else:
                 self.sparse_layer(l, stream)
@@ -161,12 +165,11 @@ class Workload:
     def sparse_layer(self, l, stream, part="all"):
         kvq, b, c = self.kvq, self.batch, self.layers[l]
         if part in ("all", "score"):
-            kvq.kv_critical_score(c, b, self.in_q[l], N_CRIT, None, self.scores, self.stride, stream)
-        if part in ("all", "select"):
-            kvq.kv_topk_select(b, HQ, self.scores, -1, RATIO, N_SINK, WINDOW, self.sel, self.cnt, self.ws_sel,
-                               self.stride, stream)
-        if part in ("all", "attn"):
-            kvq.kv_sparse_attn(c, b, self.in_q[l], self.sel, self.cnt, 0, self.out[l], None, self.ws_sa, stream)
+            kvq.kv_append_critical_score(c, b, self.in_k[l], self.in_v[l], self.in_q[l], N_CRIT, None, self.scores,
+                                         self.hist, N_SINK, WINDOW, self.ws_sc, self.stride, stream)
+        if part in ("all", "select_attn"):
+            kvq.kv_select_sparse_attn(c, b, self.in_q[l], self.scores, self.hist, -1, RATIO, N_SINK, WINDOW, None,
+                                      None, self.out[l], self.ws_sx, self.stride, stream)
 
     def capture(self, fn, stream):
         torch = self.torch
@@ -387,7 +390,7 @@ def main():
 
     # ---- per-kernel durations (CUDA events around graphs of one kernel kind, 31 launches each)
     kern = {}
-    for name, part in (("kv_sparse_attn", "attn"), ("kv_critical_score", "score"), ("kv_topk_select", "select")):
+    for name, part in (("kv_select_sparse_attn", "select_attn"), ("kv_append_critical_score", "score")):
         g = W.capture(lambda s, p=part: [W.sparse_layer(l, s, p) for l in range(1, args.layers)], stream)
         with torch.cuda.stream(stream):
             g.replay()
@@ -412,12 +415,12 @@ def main():
     kern["kv_decode_attn_quant"] = a.elapsed_time(b) / args.steps
     peak, peak_src = measured_peaks()
     Tk = args.prompt + step_i
-    kb = {"kv_sparse_attn": HQ * (N_SINK + WINDOW + math.floor(RATIO * Tk)) * 2 * D * 2,
-          "kv_critical_score": HQ * N_CRIT * Tk * 2 + HQ * Tk * 4,
+    kb = {"kv_select_sparse_attn": HQ * (N_SINK + WINDOW + math.floor(RATIO * Tk)) * 2 * D * 2,
+          "kv_append_critical_score": HQ * N_CRIT * Tk * 2 + HQ * Tk * 4,
           "kv_decode_attn_quant": HKV * Tk * 48}
     per_kernel = {k: {"ms": kern[k], "GBps": (kb[k] / (kern[k] * 1e-3) / 1e9) if k in kb else None}
                   for k in kern}
-    dom = max(("kv_sparse_attn", "kv_critical_score"), key=lambda k: kern[k])
+    dom = max(("kv_select_sparse_attn", "kv_append_critical_score"), key=lambda k: kern[k])
     achieved = kb[dom] / (kern[dom] * 1e-3) / 1e9
     tr = traffic_record(dom)
 

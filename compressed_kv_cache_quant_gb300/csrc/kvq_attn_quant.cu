@@ -267,13 +267,21 @@ size_t ws_layout(const kvq_layout* L, const kvq_seqs* S, size_t* off_part, size_
     return kvq_round_up(*off_cnt + (size_t)std::max(S->batch, 1) * L->n_kv_heads * sizeof(int32_t), 256);
 }
 
+template <int BITS, int GQ>
+int launch_one(dim3 grid, cudaStream_t s, const QAttnArgs& a) {
+    const int st = kvq_prepare_kernel((const void*)qattn_kernel<BITS, GQ>, 0);
+    if (st) return st;
+    qattn_kernel<BITS, GQ><<<grid, NT, 0, s>>>(a);
+    return KVQ_OK;
+}
+
 template <int BITS>
-void launch_bits(int gq, dim3 grid, cudaStream_t s, const QAttnArgs& a) {
+int launch_bits(int gq, dim3 grid, cudaStream_t s, const QAttnArgs& a) {
     switch (gq) {
-        case 1: qattn_kernel<BITS, 1><<<grid, NT, 0, s>>>(a); break;
-        case 2: qattn_kernel<BITS, 2><<<grid, NT, 0, s>>>(a); break;
-        case 4: qattn_kernel<BITS, 4><<<grid, NT, 0, s>>>(a); break;
-        default: qattn_kernel<BITS, 8><<<grid, NT, 0, s>>>(a); break;
+        case 1: return launch_one<BITS, 1>(grid, s, a);
+        case 2: return launch_one<BITS, 2>(grid, s, a);
+        case 4: return launch_one<BITS, 4>(grid, s, a);
+        default: return launch_one<BITS, 8>(grid, s, a);
     }
 }
 
@@ -330,10 +338,11 @@ extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, cons
     dim3 grid(p.n_splits, L->n_kv_heads, S->batch);
     cudaStream_t s = kvq_stream(stream);
     switch (L->bits) {
-        case 1: launch_bits<1>(gq, grid, s, a); break;
-        case 2: launch_bits<2>(gq, grid, s, a); break;
-        case 4: launch_bits<4>(gq, grid, s, a); break;
-        default: launch_bits<8>(gq, grid, s, a); break;
+        case 1: st = launch_bits<1>(gq, grid, s, a); break;
+        case 2: st = launch_bits<2>(gq, grid, s, a); break;
+        case 4: st = launch_bits<4>(gq, grid, s, a); break;
+        default: st = launch_bits<8>(gq, grid, s, a); break;
     }
+    if (st) return st;
     return kvq_launch_status("kv_decode_attn_quant");
 }

@@ -44,7 +44,7 @@ enum KvqDeviceCheck : int32_t {
     KVQ_DEV_OVERFLOW = 4,       // a list would exceed its capacity
 };
 
-static inline size_t kvq_round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ static inline size_t kvq_round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ---------------------------------------------------------------- device side
 
@@ -96,6 +96,12 @@ __device__ __forceinline__ float kvq_warp_sum(float v) {
 
 // log2(e) / sqrt(128): scores are kept in the log2 domain, p = exp2(s - m).
 #define KVQ_SCORE_LOG2_SCALE 0.12751743074048468f
+
+// Once per (kernel, device): prefer the largest shared-memory carveout, so that
+// the kernels of a decode step never make the SMs repartition L1 and shared
+// memory between launches, and allow `dyn_smem_max` bytes of dynamic shared
+// memory.  Returns KVQ_OK or KVQ_ERR_CUDA.
+int kvq_prepare_kernel(const void* func, int dyn_smem_max);
 
 // Validates the fields of a layout shared by all calls.  need_q: the call
 // reads query heads (H_q / H_kv must be 1, 2, 4 or 8).

@@ -421,11 +421,18 @@ extern "C" int kv_page_append(const kvq_layout* L, const kvq_pool* P, const kvq_
     if (L->bits == 16) {
         KVQ_REQUIRE(P->k16 && P->v16 && P->kT && P->k_absmax, KVQ_ERR_INVALID_ARG,
                     "kv_page_append: fp16 layer needs k16, v16, kT, k_absmax");
+        st = kvq_prepare_kernel((const void*)append_fp16_kernel, 0);
+        if (st) return st;
         append_fp16_kernel<<<grid, 128, 0, s>>>(a);
         return kvq_launch_status("kv_page_append");
     }
     KVQ_REQUIRE(P->k_codes && P->v_codes && P->k_sz && P->v_sz && P->k_tail, KVQ_ERR_INVALID_ARG,
                 "kv_page_append: quantized layer needs k_codes, v_codes, k_sz, v_sz, k_tail");
+    const void* fn = L->bits == 1 ? (const void*)append_quant_kernel<1>
+                   : L->bits == 2 ? (const void*)append_quant_kernel<2>
+                   : L->bits == 4 ? (const void*)append_quant_kernel<4> : (const void*)append_quant_kernel<8>;
+    st = kvq_prepare_kernel(fn, 0);
+    if (st) return st;
     switch (L->bits) {
         case 1: append_quant_kernel<1><<<grid, 128, 0, s>>>(a); break;
         case 2: append_quant_kernel<2><<<grid, 128, 0, s>>>(a); break;

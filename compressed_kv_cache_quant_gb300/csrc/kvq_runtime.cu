@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <map>
 #include <mutex>
 #include <vector>
 
@@ -47,6 +48,26 @@ int kvq_num_sms() {
     return cache[dev];
 }
 
+int kvq_prepare_kernel(const void* func, int dyn_smem_max) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> done;  // (kernel, device) -> dynamic limit set
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return kvq_fail(KVQ_ERR_CUDA, "no CUDA device");
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = done.find({func, dev});
+    if (it != done.end() && it->second >= dyn_smem_max) return KVQ_OK;
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess && dyn_smem_max > 48 * 1024)
+        e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem_max);
+    if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kernel attributes: %s", cudaGetErrorString(e));
+    done[{func, dev}] = dyn_smem_max;
+    return KVQ_OK;
+}
+
 int kvq_launch_status(const char* what) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -64,6 +85,8 @@ extern "C" int kvq_seq_lens_add(int32_t* seq_lens, int32_t batch, int32_t delta,
     kvq_clear_error();
     KVQ_REQUIRE(seq_lens != nullptr && batch >= 0, KVQ_ERR_INVALID_ARG, "kvq_seq_lens_add: bad arguments");
     if (batch == 0) return KVQ_OK;
+    int st = kvq_prepare_kernel((const void*)kvq_seq_lens_add_kernel, 0);
+    if (st) return st;
     kvq_seq_lens_add_kernel<<<(batch + 255) / 256, 256, 0, kvq_stream(stream)>>>(seq_lens, batch, delta);
     return kvq_launch_status("kvq_seq_lens_add");
 }

@@ -1,0 +1,775 @@
+// a5 kv_topk_select and the fused a5+a6 kv_select_sparse_attn.
+//
+// [TailorKV §2.3, §5.1] keep the k tokens with the highest approximate score,
+// [KVSurvey §三.1] always keep the attention sinks and the recent window;
+// [Meeting §3.2] exact softmax attention over the kept tokens.
+//
+// One cluster of 8 CTAs serves one (sequence, query head).  CTA r owns the
+// r-th eighth of the positions and holds their order-preserving 32-bit keys
+// in shared memory.  The k-th largest key is found by radix selection with a
+// 12-bit first digit (taken from the per-head histogram the score kernel
+// accumulated, or built here) and two 10-bit digits over the few candidates
+// that share the first digit; partial histograms are summed through
+// distributed shared memory.  Ties at the k-th key go to the lower positions
+// (a cluster-wide prefix count).  The kept positions are compacted in order;
+// each CTA then attends its own kept rows and the 8 partial softmax states are
+// merged by log-sum-exp in rank 0.
+#include <cooperative_groups.h>
+
+#include <algorithm>
+#include <cstddef>
+
+#include "kvq_internal.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace {
+
+constexpr int D = KVQ_HEAD_DIM;
+constexpr int PG = KVQ_BLOCK_TOKENS;
+constexpr int CL = 8;                 // CTAs per cluster
+constexpr int NT = 512;               // threads per CTA
+constexpr int NW = NT / 32;
+constexpr int MAX_CHUNK = 46080;      // positions per CTA (keys in shared memory)
+constexpr int MAXIT = (MAX_CHUNK + NT - 1) / NT;  // 32-position steps per warp in the compaction
+constexpr int CAND_MAX = 2048;        // first-digit candidates gathered in rank 0
+constexpr int H1 = 4096;              // first digit: key bits 31..20
+constexpr int H2 = 1024;              // second and third digits: bits 19..10, 9..0
+constexpr int NHW = NT / 16;          // half-warps (attention: one row per half-warp)
+constexpr int BATCH = 4;              // rows in flight per half-warp
+constexpr int REC = 4 + D;
+
+struct SXArgs {
+    const float* scores;
+    int64_t score_stride;
+    uint32_t* hist;          // [B][n_heads][4096] or NULL
+    const int32_t* seq_lens;
+    int32_t max_len;
+    int32_t n_heads;
+    int32_t k_fixed;
+    double ratio;
+    int32_t n_sink, window;
+    int32_t* sel;            // [B][n_heads][sel_cap] or NULL
+    int32_t sel_cap;
+    int32_t* sel_count;      // [B][n_heads] or NULL
+    KvqWsHeader* hdr;
+    // attention (q == NULL: selection only)
+    const uint16_t* q;
+    const uint16_t* k16;
+    const uint16_t* v16;
+    int64_t num_blocks;
+    const int32_t* bt;
+    int32_t max_blocks;
+    int32_t H, GQ;
+    float* out;
+};
+
+constexpr int CAP_S = 1024;           // kept positions collected per CTA in the one-pass path
+constexpr int CAP_C = 512;            // first-digit candidates collected per CTA
+
+// Shared state of one CTA; it follows the chunk's keys in dynamic shared memory.
+struct SXSmem {
+    union {
+        uint32_t hist[H1];                  // first-digit histogram
+        unsigned long long cand[CAND_MAX];  // rank 0: (key << 32 | position) of all first-digit candidates
+    } u;
+    union {
+        struct {
+            uint32_t h2[H2];                // second / third digit histogram
+            unsigned long long cl[CAP_C];   // this CTA's first-digit candidates
+            uint32_t wmask[NW][MAXIT];      // ballots of the ordered compaction
+        } w;
+        float scratch[NHW * REC];           // half-warp softmax states (attention)
+    } v;
+    uint32_t list[CAP_S];                   // kept positions, then their row offsets
+    uint32_t wsum[NW];
+    uint32_t wtot[NW], wtot2[NW];
+    int32_t n_cand;                         // rank 0: candidates gathered
+    int32_t n_s, n_c;                       // this CTA's kept positions / candidates
+    int32_t bc_cut;
+    uint32_t s_bin, s_above;
+    uint32_t eq_cnt, sel_cnt;               // this CTA's counts, read by the others
+    float st_m[CL], st_l[CL];               // rank 0: the CTAs' softmax states
+    float st_o[CL][D];
+};
+
+size_t smem_bytes(int chunk) { return kvq_round_up((size_t)std::max(chunk, 1) * sizeof(uint32_t), 16) + sizeof(SXSmem); }
+int chunk_of(int T) { return ((T + CL - 1) / CL + 31) / 32 * 32; }
+__device__ __forceinline__ int chunk_of_dev(int T) { return ((T + CL - 1) / CL + 31) / 32 * 32; }
+
+template <int N>
+__device__ __forceinline__ uint32_t excl_scan(uint32_t v, uint32_t* wsum, uint32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    __syncthreads();
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < N / 32 ? wsum[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < N / 32) wsum[lane] = w;
+    }
+    __syncthreads();
+    *total = wsum[N / 32 - 1];
+    return x - v + (warp > 0 ? wsum[warp - 1] : 0u);
+}
+
+// Over `nbins` bins in tot[], finds the bin (from the top) that holds the
+// `remaining`-th largest element: s.s_bin, and s.s_above = count in higher bins.
+// Called by a whole CTA; every thread owns nbins/NT consecutive bins.
+__device__ __forceinline__ void find_bin_from_top(const uint32_t* tot, int nbins, uint32_t remaining, SXSmem& s) {
+    const int per = nbins / NT;
+    const int top = nbins - per * (int)threadIdx.x;  // thread 0 owns the highest bins
+    uint32_t mine = 0;
+    for (int j = 1; j <= per; ++j) mine += tot[top - j];
+    uint32_t total;
+    const uint32_t before = excl_scan<NT>(mine, s.wsum, &total);
+    if (before < remaining && before + mine >= remaining) {
+        uint32_t run = before;
+        for (int j = 1; j <= per; ++j) {
+            const uint32_t c = tot[top - j];
+            if (run + c >= remaining) {
+                s.s_bin = (uint32_t)(top - j);
+                s.s_above = run;
+                break;
+            }
+            run += c;
+        }
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ void unpack8(const uint4& r, float* f) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
+    }
+}
+
+// Appends, in ballot order, the lanes with f set to list[*n] (capacity cap);
+// returns false if the list overflowed.
+template <typename V>
+__device__ __forceinline__ bool warp_append(bool f, V v, V* list, int32_t* n, int cap, int lane) {
+    const uint32_t m = __ballot_sync(0xffffffffu, f);
+    if (m == 0u) return true;
+    int base = 0;
+    if (lane == 0) base = atomicAdd(n, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int i = base + __popc(m & ((1u << lane) - 1u));
+    if (f && i < cap) list[i] = v;
+    return base + __popc(m) <= cap;
+}
+
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_kernel(SXArgs a, int chunk_cap) {
+    extern __shared__ __align__(16) uint32_t keys[];  // the chunk's keys; later its kept positions
+    SXSmem& s = *reinterpret_cast<SXSmem*>(reinterpret_cast<char*>(keys) +
+                                           kvq_round_up((size_t)max(chunk_cap, 1) * sizeof(uint32_t), 16));
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row = (int64_t)b * a.n_heads + h;
+    int T = a.seq_lens[b];
+    if (T < 0 || T > a.max_len) {
+        if (tid == 0 && rank == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
+        T = T < 0 ? 0 : a.max_len;
+    }
+    const int k = a.k_fixed >= 0 ? a.k_fixed : (int)floor(a.ratio * (double)T);
+    const int chunk = chunk_of_dev(T);  // a multiple of 32: the chunk starts 16-byte aligned
+    const int lo = min(T, rank * chunk), hi = min(T, lo + chunk);
+    const int n = hi - lo;
+    const bool keep_all = (int64_t)T <= (int64_t)a.n_sink + a.window + k;
+    const int cand_lo = a.n_sink, cand_hi = T - a.window;
+    const float* srow = a.scores + row * a.score_stride;
+    // warp w owns the contiguous run [w_lo, w_hi) of the chunk in the ordered passes
+    const int wlen = ((n + NW - 1) / NW + 31) / 32 * 32;
+    const int w_lo = min(hi, lo + warp * wlen), w_hi = min(hi, w_lo + wlen);
+    if (tid == 0) {
+        s.n_s = 0;
+        s.n_c = 0;
+    }
+
+    uint32_t kth = 0xffffffffu;  // kept: key > kth, or key == kth and position <= cut
+    int32_t cut = -1;
+    bool listed = false;         // s.list holds this CTA's kept positions (the one-pass path)
+    if (!keep_all) {
+        // ---- the chunk's keys (16-byte loads, eight in flight per thread)
+        for (int p0 = lo + 4 * tid; p0 < hi; p0 += 4 * NT * 8) {
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int p = p0 + j * 4 * NT;
+                if (p + 3 < hi) {
+                    v[j] = __ldcg(reinterpret_cast<const float4*>(srow + p));
+                } else {
+                    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (p < hi) v[j].x = srow[p];
+                    if (p + 1 < hi) v[j].y = srow[p + 1];
+                    if (p + 2 < hi) v[j].z = srow[p + 2];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int p = p0 + j * 4 * NT;
+                if (p + 3 < hi) {
+                    *reinterpret_cast<uint4*>(keys + (p - lo)) =
+                        make_uint4(kvq_float_key(v[j].x), kvq_float_key(v[j].y), kvq_float_key(v[j].z),
+                                   kvq_float_key(v[j].w));
+                } else {
+                    if (p < hi) keys[p - lo] = kvq_float_key(v[j].x);
+                    if (p + 1 < hi) keys[p + 1 - lo] = kvq_float_key(v[j].y);
+                    if (p + 2 < hi) keys[p + 2 - lo] = kvq_float_key(v[j].z);
+                }
+            }
+        }
+        if (k > 0) {
+            // ---- digit 1 (key bits 31..20): from the score kernel's histogram, or built here
+            if (a.hist != nullptr) {
+                const uint4* gh = reinterpret_cast<const uint4*>(a.hist + row * H1);
+                for (int i = tid; i < H1 / 4; i += NT) reinterpret_cast<uint4*>(s.u.hist)[i] = __ldcg(gh + i);
+                __syncthreads();
+            } else {
+                for (int i = tid; i < H1; i += NT) s.u.hist[i] = 0u;
+                __syncthreads();
+                for (int p = max(lo, cand_lo) + tid; p < min(hi, cand_hi); p += NT)
+                    atomicAdd(&s.u.hist[keys[p - lo] >> 20], 1u);
+                cluster.sync();
+                uint32_t sums[H1 / NT];
+#pragma unroll
+                for (int j = 0; j < H1 / NT; ++j) sums[j] = 0u;
+                for (int r = 0; r < CL; ++r) {
+                    const uint32_t* rh = cluster.map_shared_rank(s.u.hist, r);
+#pragma unroll
+                    for (int j = 0; j < H1 / NT; ++j) sums[j] += rh[tid + j * NT];
+                }
+                cluster.sync();
+#pragma unroll
+                for (int j = 0; j < H1 / NT; ++j) s.u.hist[tid + j * NT] = sums[j];
+                __syncthreads();
+            }
+            find_bin_from_top(s.u.hist, H1, (uint32_t)k, s);
+            const uint32_t b1 = s.s_bin;
+            uint32_t remaining = (uint32_t)k - s.s_above;
+            // ---- positions above digit 1 (and sinks, window) are kept; ties on digit 1 are
+            // candidates.  Count per warp, scan the warp totals, then write in order.
+            auto classify = [&](int p, bool& sure, bool& cnd, uint32_t& key) {
+                sure = cnd = false;
+                key = 0;
+                if (p < w_hi) {
+                    if (p < cand_lo || p >= cand_hi) {
+                        sure = true;
+                    } else {
+                        key = keys[p - lo];
+                        sure = (key >> 20) > b1;
+                        cnd = (key >> 20) == b1;
+                    }
+                }
+            };
+            {
+                uint32_t cs = 0, cc = 0;
+                for (int p0 = w_lo; p0 < w_hi; p0 += 32) {
+                    bool sure, cnd;
+                    uint32_t key;
+                    classify(p0 + lane, sure, cnd, key);
+                    cs += __popc(__ballot_sync(0xffffffffu, sure));
+                    cc += __popc(__ballot_sync(0xffffffffu, cnd));
+                }
+                if (lane == 0) {
+                    s.wtot[warp] = cs;
+                    s.wtot2[warp] = cc;
+                }
+                __syncthreads();
+                uint32_t bs = 0, bc = 0, ts = 0, tc = 0;
+                for (int w = 0; w < NW; ++w) {
+                    if (w < warp) {
+                        bs += s.wtot[w];
+                        bc += s.wtot2[w];
+                    }
+                    ts += s.wtot[w];
+                    tc += s.wtot2[w];
+                }
+                for (int p0 = w_lo; p0 < w_hi; p0 += 32) {
+                    bool sure, cnd;
+                    uint32_t key;
+                    const int p = p0 + lane;
+                    classify(p, sure, cnd, key);
+                    const uint32_t ms = __ballot_sync(0xffffffffu, sure);
+                    const uint32_t mc = __ballot_sync(0xffffffffu, cnd);
+                    const uint32_t lt = (1u << lane) - 1u;
+                    if (sure && bs + __popc(ms & lt) < (uint32_t)CAP_S) s.list[bs + __popc(ms & lt)] = (uint32_t)p;
+                    if (cnd && bc + __popc(mc & lt) < (uint32_t)CAP_C)
+                        s.v.w.cl[bc + __popc(mc & lt)] = ((unsigned long long)key << 32) | (uint32_t)p;
+                    bs += __popc(ms);
+                    bc += __popc(mc);
+                }
+                if (tid == 0) {
+                    s.n_s = (int32_t)ts;
+                    s.n_c = (int32_t)tc;
+                }
+            }
+            if (tid == 0) s.n_cand = 0;
+            cluster.sync();  // local lists complete; every CTA is done with its histogram
+            if (a.hist != nullptr && rank == 0)  // read by all: clear it for the next layer
+                for (int i = tid; i < H1; i += NT) a.hist[row * H1 + i] = 0u;
+            // ---- push the candidates to rank 0 (one reservation per CTA)
+            {
+                SXSmem* r0 = cluster.map_shared_rank(&s, 0);
+                __shared__ int s_base;
+                const int nc = min(s.n_c, CAP_C);
+                if (tid == 0) s_base = atomicAdd(&r0->n_cand, s.n_c > CAP_C ? CAND_MAX + 1 : nc);
+                __syncthreads();
+                const int base = s_base;
+                for (int i = tid; i < nc; i += NT)
+                    if (base + i < CAND_MAX) r0->u.cand[base + i] = s.v.w.cl[i];
+            }
+            cluster.sync();
+            const int n_c = cluster.map_shared_rank(&s, 0)->n_cand;
+            if (n_c <= CAND_MAX) {
+                // ---- fast path: every CTA finishes the selection over rank 0's candidate list
+                const SXSmem* r0 = cluster.map_shared_rank(&s, 0);
+                constexpr int PER = CAND_MAX / NT;
+                unsigned long long cr[PER];
+#pragma unroll
+                for (int j = 0; j < PER; ++j) {
+                    const int i = tid + j * NT;
+                    cr[j] = i < n_c ? r0->u.cand[i] : 0ull;
+                }
+                uint32_t prefix = b1;
+                for (int pass = 0; pass < 2; ++pass) {
+                    const int shift = pass == 0 ? 10 : 0;
+                    for (int i = tid; i < H2; i += NT) s.v.w.h2[i] = 0u;
+                    __syncthreads();
+#pragma unroll
+                    for (int j = 0; j < PER; ++j) {
+                        const uint32_t key = (uint32_t)(cr[j] >> 32);
+                        if (tid + j * NT < n_c && (key >> (shift + 10)) == prefix)
+                            atomicAdd(&s.v.w.h2[(key >> shift) & (H2 - 1)], 1u);
+                    }
+                    __syncthreads();
+                    find_bin_from_top(s.v.w.h2, H2, remaining, s);
+                    remaining -= s.s_above;
+                    prefix = (prefix << 10) | s.s_bin;
+                }
+                kth = prefix;
+                // ties at the k-th key: keep the `remaining` lowest positions among them
+                uint32_t c_eq = 0;
+#pragma unroll
+                for (int j = 0; j < PER; ++j) c_eq += tid + j * NT < n_c && (uint32_t)(cr[j] >> 32) == kth;
+                uint32_t eq_total;
+                excl_scan<NT>(c_eq, s.wsum, &eq_total);
+                if (remaining == 0) {
+                    cut = -1;
+                } else if (remaining >= eq_total) {
+                    cut = 0x7fffffff;
+                } else {
+                    if (tid == 0) s.bc_cut = 0x7fffffff;
+                    __syncthreads();
+#pragma unroll
+                    for (int j = 0; j < PER; ++j) {
+                        if (tid + j * NT >= n_c || (uint32_t)(cr[j] >> 32) != kth) continue;
+                        const uint32_t pi = (uint32_t)cr[j];
+                        uint32_t r = 0;
+                        for (int i = 0; i < n_c; ++i) {
+                            const unsigned long long ci = r0->u.cand[i];
+                            r += ((uint32_t)(ci >> 32) == kth) && ((uint32_t)ci < pi);
+                        }
+                        if (r == remaining - 1) s.bc_cut = (int32_t)pi;
+                    }
+                    __syncthreads();
+                    cut = s.bc_cut;
+                }
+                // the kept candidates of this CTA join its list
+                const int nc = min(s.n_c, CAP_C);
+                for (int i0 = 0; i0 < nc; i0 += NT) {  // uniform bound
+                    const int i = i0 + tid;
+                    bool f = false;
+                    uint32_t p = 0;
+                    if (i < nc) {
+                        const unsigned long long c = s.v.w.cl[i];
+                        const uint32_t key = (uint32_t)(c >> 32);
+                        p = (uint32_t)c;
+                        f = key > kth || (key == kth && (int32_t)p <= cut);
+                    }
+                    warp_append<uint32_t>(f, p, s.list, &s.n_s, CAP_S, lane);
+                }
+                __syncthreads();
+                listed = s.n_s <= CAP_S && a.sel == nullptr;
+            } else {
+                // ---- fallback (many candidates share digit 1, e.g. heavy ties): distributed passes
+                uint32_t prefix = b1;
+                for (int pass = 0; pass < 2; ++pass) {
+                    const int shift = pass == 0 ? 10 : 0;
+                    for (int i = tid; i < H2; i += NT) s.v.w.h2[i] = 0u;
+                    __syncthreads();
+                    for (int p = max(lo, cand_lo) + tid; p < min(hi, cand_hi); p += NT) {
+                        const uint32_t key = keys[p - lo];
+                        if ((key >> (shift + 10)) == prefix) atomicAdd(&s.v.w.h2[(key >> shift) & (H2 - 1)], 1u);
+                    }
+                    cluster.sync();
+                    uint32_t sums[H2 / NT];
+#pragma unroll
+                    for (int j = 0; j < H2 / NT; ++j) sums[j] = 0u;
+                    for (int r = 0; r < CL; ++r) {
+                        const uint32_t* rh = cluster.map_shared_rank(s.v.w.h2, r);
+#pragma unroll
+                        for (int j = 0; j < H2 / NT; ++j) sums[j] += rh[tid + j * NT];
+                    }
+                    cluster.sync();
+#pragma unroll
+                    for (int j = 0; j < H2 / NT; ++j) s.v.w.h2[tid + j * NT] = sums[j];
+                    __syncthreads();
+                    find_bin_from_top(s.v.w.h2, H2, remaining, s);
+                    remaining -= s.s_above;
+                    prefix = (prefix << 10) | s.s_bin;
+                }
+                kth = prefix;
+                // ties: the cut is the remaining-th lowest position with key == kth over the cluster
+                uint32_t my_eq = 0;
+                for (int p = max(lo, cand_lo) + tid; p < min(hi, cand_hi); p += NT) my_eq += keys[p - lo] == kth;
+                uint32_t eq_cta;
+                excl_scan<NT>(my_eq, s.wsum, &eq_cta);
+                if (tid == 0) {
+                    s.eq_cnt = eq_cta;
+                    s.bc_cut = 0x7fffffff;
+                }
+                cluster.sync();
+                uint32_t eq_before = 0, eq_total = 0;
+                for (int r = 0; r < CL; ++r) {
+                    const uint32_t c = cluster.map_shared_rank(&s, r)->eq_cnt;
+                    eq_total += c;
+                    if (r < rank) eq_before += c;
+                }
+                if (remaining == 0) {
+                    cut = -1;
+                } else if (remaining >= eq_total) {
+                    cut = 0x7fffffff;
+                } else {
+                    // the CTA holding the cut finds it with an ordered pass and tells everyone
+                    if (eq_before < remaining && remaining <= eq_before + eq_cta) {
+                        const uint32_t want = remaining - eq_before;  // 1-based rank inside this CTA
+                        uint32_t cnt = 0;
+                        for (int p0 = w_lo; p0 < w_hi; p0 += 32) {
+                            const int p = p0 + lane;
+                            const bool f = p < w_hi && p >= cand_lo && p < cand_hi && keys[p - lo] == kth;
+                            cnt += __popc(__ballot_sync(0xffffffffu, f));
+                        }
+                        if (lane == 0) s.wtot[warp] = cnt;
+                        __syncthreads();
+                        uint32_t before = 0;
+                        for (int w = 0; w < warp; ++w) before += s.wtot[w];
+                        if (before < want && want <= before + cnt) {
+                            uint32_t run = before;
+                            for (int p0 = w_lo; p0 < w_hi; p0 += 32) {
+                                const int p = p0 + lane;
+                                const bool f = p < w_hi && p >= cand_lo && p < cand_hi && keys[p - lo] == kth;
+                                const uint32_t m = __ballot_sync(0xffffffffu, f);
+                                if (run + __popc(m) >= want) {
+                                    if (f && run + __popc(m & ((1u << lane) - 1u)) + 1 == want)
+                                        for (int r = 0; r < CL; ++r) cluster.map_shared_rank(&s, r)->bc_cut = p;
+                                    break;
+                                }
+                                run += __popc(m);
+                            }
+                        }
+                    }
+                    cluster.sync();
+                    cut = s.bc_cut;
+                }
+            }
+        }
+    }
+    // the histogram was not needed (everything kept, or k == 0): clear it for the next layer
+    if (a.hist != nullptr && rank == 0 && (keep_all || k == 0))
+        for (int i = tid; i < H1; i += NT) a.hist[row * H1 + i] = 0u;
+
+    const uint32_t* plist;  // kept positions of this CTA
+    uint32_t nl;
+    if (listed) {
+        plist = s.list;
+        nl = (uint32_t)s.n_s;
+    } else {
+        // ---- ordered compaction over the chunk (positions ascending), in place into keys[]
+        uint32_t cnt = 0;
+        for (int it = 0, p0 = w_lo; p0 < w_hi; ++it, p0 += 32) {
+            const int p = p0 + lane;
+            bool f = p < w_hi;
+            if (f && !keep_all && p >= cand_lo && p < cand_hi) {
+                const uint32_t key = keys[p - lo];
+                f = key > kth || (key == kth && p <= cut);
+            }
+            const uint32_t m = __ballot_sync(0xffffffffu, f);
+            if (lane == 0) s.v.w.wmask[warp][it] = m;
+            cnt += __popc(m);
+        }
+        if (lane == 0) s.wtot[warp] = cnt;
+        __syncthreads();  // every key has been read
+        uint32_t base = 0;
+        nl = 0;
+        for (int w = 0; w < NW; ++w) {
+            const uint32_t c = s.wtot[w];
+            if (w < warp) base += c;
+            nl += c;
+        }
+        for (int it = 0, p0 = w_lo; p0 < w_hi; ++it, p0 += 32) {
+            const uint32_t m = s.v.w.wmask[warp][it];
+            if ((m >> lane) & 1u) keys[base + __popc(m & ((1u << lane) - 1u))] = (uint32_t)(p0 + lane);
+            base += __popc(m);
+        }
+        plist = keys;
+    }
+    if (tid == 0) s.sel_cnt = nl;
+    __syncthreads();
+
+    if (a.sel != nullptr) {
+        // the ordered selection: this CTA's positions follow those of the lower ranks
+        cluster.sync();
+        uint32_t off = 0;
+        for (int r = 0; r < rank; ++r) off += cluster.map_shared_rank(&s, r)->sel_cnt;
+        int32_t* out = a.sel + row * a.sel_cap;
+        bool ovf = false;
+        for (int i = tid; i < (int)nl; i += NT) {
+            if (off + i < (uint32_t)a.sel_cap) out[off + i] = (int32_t)plist[i];
+            else ovf = true;
+        }
+        if (ovf) kvq_dev_flag(a.hdr, KVQ_DEV_OVERFLOW, b);
+        if (rank == 0 && tid == 0 && a.sel_count != nullptr) {
+            const int total = keep_all ? T : a.n_sink + a.window + k;
+            a.sel_count[row] = min(total, a.sel_cap);
+        }
+        cluster.sync();  // remote counts read before any CTA moves on or leaves
+    }
+    if (a.q == nullptr) return;
+
+    // ---- attention over this CTA's kept rows
+    const int g = h / a.GQ;
+    uint32_t* rows = const_cast<uint32_t*>(plist);  // positions -> row offsets (in 128-element rows)
+    for (int i = tid; i < (int)nl; i += NT) {
+        const int t = (int)plist[i];
+        const int32_t page = a.bt[(int64_t)b * a.max_blocks + (t >> 4)];
+        uint32_t r = 0xffffffffu;
+        if (page >= 0 && page < a.num_blocks) r = (uint32_t)(((int64_t)page * a.H + g) * PG + (t & 15));
+        else kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, t);
+        rows[i] = r;
+    }
+    __syncthreads();
+    const int hw = tid >> 4, l16 = tid & 15;
+    float qv[8];
+    {
+        const uint4 raw = *reinterpret_cast<const uint4*>(a.q + row * D + 8 * l16);
+        unpack8(raw, qv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qv[i] *= KVQ_SCORE_LOG2_SCALE;
+    }
+    float m = -INFINITY, l = 0.0f, o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = 0.0f;
+    for (int it = 0; it < (int)nl; it += NHW * BATCH) {  // bound uniform over the CTA
+        uint4 kr[BATCH], vr[BATCH];
+        bool ok[BATCH];
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+            const int i = it + j * NHW + hw;
+            const uint32_t r = i < (int)nl ? rows[i] : 0xffffffffu;
+            ok[j] = r != 0xffffffffu;
+            kr[j] = make_uint4(0u, 0u, 0u, 0u);
+            vr[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (ok[j]) {
+                const int64_t off = (int64_t)r * D + 8 * l16;
+                kr[j] = __ldg(reinterpret_cast<const uint4*>(a.k16 + off));
+                vr[j] = __ldg(reinterpret_cast<const uint4*>(a.v16 + off));
+            }
+        }
+        float sc[BATCH];
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+            float kf[8];
+            unpack8(kr[j], kf);
+            float acc = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc = fmaf(qv[i], kf[i], acc);
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            sc[j] = ok[j] ? acc : -INFINITY;
+        }
+        float mn = m;
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) mn = fmaxf(mn, sc[j]);
+        if (mn != -INFINITY) {
+            const float alpha = exp2f(m - mn);
+            m = mn;
+            l *= alpha;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] *= alpha;
+#pragma unroll
+            for (int j = 0; j < BATCH; ++j) {
+                const float p = exp2f(sc[j] - mn);
+                l += p;
+                float vf[8];
+                unpack8(vr[j], vf);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = fmaf(p, vf[i], o[i]);
+            }
+        }
+    }
+    // the union buffer is free again: it holds the half-warp states
+    {
+        float* r = s.v.scratch + hw * REC;
+        if (l16 == 0) {
+            r[0] = m;
+            r[1] = l;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r[4 + 8 * l16 + i] = o[i];
+    }
+    __syncthreads();
+    SXSmem* r0 = cluster.map_shared_rank(&s, 0);
+    if (tid < D) {
+        float M = -INFINITY;
+        for (int w = 0; w < NHW; ++w) M = fmaxf(M, s.v.scratch[w * REC]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < NHW; ++w) {
+                const float wt = exp2f(s.v.scratch[w * REC] - M);
+                L = fmaf(s.v.scratch[w * REC + 1], wt, L);
+                O = fmaf(s.v.scratch[w * REC + 4 + tid], wt, O);
+            }
+        }
+        r0->st_o[rank][tid] = O;  // push this CTA's state to rank 0
+        if (tid == 0) {
+            r0->st_m[rank] = M;
+            r0->st_l[rank] = L;
+        }
+    }
+    cluster.sync();  // after it no CTA touches another's shared memory
+    if (rank == 0 && tid < D) {
+        float M = -INFINITY;
+        for (int r = 0; r < CL; ++r) M = fmaxf(M, s.st_m[r]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+            for (int r = 0; r < CL; ++r) {
+                const float wt = exp2f(s.st_m[r] - M);
+                L = fmaf(s.st_l[r], wt, L);
+                O = fmaf(s.st_o[r][tid], wt, O);
+            }
+        }
+        a.out[row * D + tid] = L > 0.0f ? O / L : 0.0f;
+    }
+}
+
+int launch(const SXArgs& a, int batch, cudaStream_t st) {
+    const int r = kvq_prepare_kernel((const void*)select_attn_kernel, (int)smem_bytes(MAX_CHUNK));
+    if (r) return r;
+    const int chunk_cap = chunk_of(a.max_len);
+    select_attn_kernel<<<dim3(CL, a.n_heads, batch), NT, smem_bytes(chunk_cap), st>>>(a, chunk_cap);
+    return KVQ_OK;
+}
+
+int check_common(const kvq_seqs* S, const char* fn, int32_t n_heads, int32_t k_fixed, double ratio, int32_t n_sink,
+                 int32_t window, const float* scores, int64_t score_stride) {
+    int st = kvq_check_seqs(S, fn);
+    if (st) return st;
+    KVQ_REQUIRE(n_heads > 0, KVQ_ERR_INVALID_ARG, "%s: n_heads", fn);
+    KVQ_REQUIRE(n_sink >= 0 && window >= 0, KVQ_ERR_INVALID_ARG, "%s: n_sink/window", fn);
+    KVQ_REQUIRE(k_fixed >= 0 || (ratio >= 0.0 && ratio <= 1.0), KVQ_ERR_INVALID_ARG, "%s: ratio", fn);
+    KVQ_REQUIRE(scores && score_stride >= S->max_len && score_stride % 4 == 0 && ((uintptr_t)scores & 15u) == 0,
+                KVQ_ERR_INVALID_ARG, "%s: scores 16-byte aligned, score_stride >= max_len and a multiple of 4", fn);
+    KVQ_REQUIRE(chunk_of(S->max_len) <= MAX_CHUNK, KVQ_ERR_UNSUPPORTED, "%s: max_len %d above %d", fn,
+                S->max_len, CL * MAX_CHUNK);
+    return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" size_t kv_topk_select_ws(void) { return sizeof(KvqWsHeader); }
+
+extern "C" int kv_topk_select(const kvq_seqs* S, int32_t n_heads, const float* scores, int64_t score_stride,
+                              int32_t k_fixed, double ratio, int32_t n_sink, int32_t window, int32_t* sel,
+                              int32_t sel_cap, int32_t* sel_count, void* ws, size_t ws_bytes, void* stream) {
+    kvq_clear_error();
+    int st = check_common(S, "kv_topk_select", n_heads, k_fixed, ratio, n_sink, window, scores, score_stride);
+    if (st) return st;
+    st = kvq_check_ws(ws, ws_bytes, kv_topk_select_ws(), "kv_topk_select");
+    if (st) return st;
+    KVQ_REQUIRE(sel && sel_count && sel_cap > 0, KVQ_ERR_INVALID_ARG, "kv_topk_select: sel / sel_count / sel_cap");
+    if (S->batch == 0) return KVQ_OK;
+    SXArgs a{};
+    a.scores = scores;
+    a.score_stride = score_stride;
+    a.hist = nullptr;
+    a.seq_lens = S->seq_lens;
+    a.max_len = S->max_len;
+    a.n_heads = n_heads;
+    a.k_fixed = k_fixed;
+    a.ratio = ratio;
+    a.n_sink = n_sink;
+    a.window = window;
+    a.sel = sel;
+    a.sel_cap = sel_cap;
+    a.sel_count = sel_count;
+    a.hdr = static_cast<KvqWsHeader*>(ws);
+    a.q = nullptr;
+    st = launch(a, S->batch, kvq_stream(stream));
+    if (st) return st;
+    return kvq_launch_status("kv_topk_select");
+}
+
+extern "C" size_t kv_select_sparse_attn_ws(void) { return sizeof(KvqWsHeader); }
+
+extern "C" int kv_select_sparse_attn(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
+                                     const float* scores, int64_t score_stride, uint32_t* hist, int32_t k_fixed,
+                                     double ratio, int32_t n_sink, int32_t window, int32_t* sel, int32_t sel_cap,
+                                     int32_t* sel_count, float* out, void* ws, size_t ws_bytes, void* stream) {
+    kvq_clear_error();
+    int st = kvq_check_layout(L, "kv_select_sparse_attn", true);
+    if (st) return st;
+    st = check_common(S, "kv_select_sparse_attn", L->n_q_heads, k_fixed, ratio, n_sink, window, scores,
+                      score_stride);
+    if (st) return st;
+    st = kvq_check_ws(ws, ws_bytes, kv_select_sparse_attn_ws(), "kv_select_sparse_attn");
+    if (st) return st;
+    KVQ_REQUIRE(P && P->k16 && P->v16 && (((uintptr_t)P->k16 | (uintptr_t)P->v16) & 15u) == 0, KVQ_ERR_INVALID_ARG,
+                "kv_select_sparse_attn: pool needs 16-byte aligned k16 and v16");
+    KVQ_REQUIRE(q && out && ((uintptr_t)q & 15u) == 0, KVQ_ERR_INVALID_ARG, "kv_select_sparse_attn: q / out");
+    KVQ_REQUIRE(sel == nullptr || sel_cap > 0, KVQ_ERR_INVALID_ARG, "kv_select_sparse_attn: sel_cap");
+    if (S->batch == 0) return KVQ_OK;
+    KVQ_REQUIRE(S->block_table != nullptr, KVQ_ERR_INVALID_ARG, "kv_select_sparse_attn: NULL block table");
+    SXArgs a{};
+    a.scores = scores;
+    a.score_stride = score_stride;
+    a.hist = hist;
+    a.seq_lens = S->seq_lens;
+    a.max_len = S->max_len;
+    a.n_heads = L->n_q_heads;
+    a.k_fixed = k_fixed;
+    a.ratio = ratio;
+    a.n_sink = n_sink;
+    a.window = window;
+    a.sel = sel;
+    a.sel_cap = sel_cap;
+    a.sel_count = sel_count;
+    a.hdr = static_cast<KvqWsHeader*>(ws);
+    a.q = q;
+    a.k16 = P->k16;
+    a.v16 = P->v16;
+    a.num_blocks = P->num_blocks;
+    a.bt = S->block_table;
+    a.max_blocks = S->max_blocks;
+    a.H = L->n_kv_heads;
+    a.GQ = L->n_q_heads / L->n_kv_heads;
+    a.out = out;
+    st = launch(a, S->batch, kvq_stream(stream));
+    if (st) return st;
+    return kvq_launch_status("kv_select_sparse_attn");
+}

@@ -51,15 +51,17 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, 
     return x - v + (warp > 0 ? wsum[warp - 1] : 0u);
 }
 
-// ================================================================ a4 critical score
+// ================================================================ a4 critical score (+ fused fp16 append)
 
 constexpr int CS_NT = 256;
-constexpr int CS_TOK = 8;                 // tokens per thread
-constexpr int CS_TILE = CS_NT * CS_TOK;   // tokens per CTA
+constexpr int CS_TOK = 8;                          // tokens per thread and pass
+constexpr int CS_IT = 2;                           // passes per CTA
+constexpr int CS_TILE = CS_NT * CS_TOK * CS_IT;    // tokens per CTA
+constexpr int CS_H1 = 4096;                        // histogram of key bits 31..20
 
 struct CritArgs {
-    const uint16_t* kT;
-    const float* absmax;
+    uint16_t* kT;
+    float* absmax;
     int32_t t_cap;
     const int32_t* seq_lens;
     int32_t max_len;
@@ -69,25 +71,66 @@ struct CritArgs {
     int32_t* crit;
     float* scores;
     int64_t score_stride;
+    // fused append of the newest token (k_new == NULL: no append)
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    uint16_t* k16;
+    uint16_t* v16;
+    int64_t num_blocks;
+    const int32_t* bt;
+    int32_t max_blocks;
+    // histogram of candidate keys for the selection (NULL: none)
+    uint32_t* hist;
+    int32_t n_sink, window;
+    KvqWsHeader* hdr;
 };
 
 __global__ void __launch_bounds__(CS_NT) crit_score_kernel(CritArgs a) {
     __shared__ float sc[D];
     __shared__ float qs[D];
+    __shared__ uint16_t knew[D];
     __shared__ int32_t clist[D];
     __shared__ uint32_t selmask[D / 32];
+    __shared__ uint32_t lhist[CS_H1];
     const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x;
     const int g = h / a.GQ;
     const int Hq = a.H * a.GQ;
-    const int T = max(0, min(a.seq_lens[b], min(a.t_cap, a.max_len)));  // lengths past the buffers are cut
+    const int64_t kvrow = (int64_t)b * a.H + g;
+    int T = a.seq_lens[b];
+    if (T < 0 || T > a.max_len || T > a.t_cap) {  // lengths past the buffers are cut and reported
+        if (tid == 0 && tile == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
+        T = max(0, min(T, min(a.t_cap, a.max_len)));
+    }
     if (tile > 0 && tile * CS_TILE >= T) return;
+    const int p_new = a.k_new != nullptr ? T - 1 : -1;
     if (tid < D) {
         const float qv = kvq_h2f(a.q[((int64_t)b * Hq + h) * D + tid]);
+        float am = a.absmax[kvrow * D + tid];
+        if (p_new >= 0) {
+            const uint16_t kn = a.k_new[kvrow * D + tid];
+            knew[tid] = kn;
+            am = fmaxf(am, fabsf(kvq_h2f(kn)));
+            if (tile == 0 && h % a.GQ == 0) {
+                // append the newest token of kv head g: fp16 rows, channel-major copy, running absmax
+                const int32_t page = a.bt[(int64_t)b * a.max_blocks + (p_new >> 4)];
+                if (page >= 0 && page < a.num_blocks) {
+                    const int64_t off = ((page * (int64_t)a.H + g) * PG + (p_new & 15)) * D + tid;
+                    a.k16[off] = kn;
+                    a.v16[off] = a.v_new[kvrow * D + tid];
+                } else {
+                    kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
+                }
+                a.kT[(kvrow * D + tid) * a.t_cap + p_new] = kn;
+                a.absmax[kvrow * D + tid] = am;
+            }
+        }
         qs[tid] = qv;
         // |q_c| * max|K_c|: both fp16 values, so the fp32 product is exact
-        sc[tid] = fabsf(qv) * a.absmax[((int64_t)b * a.H + g) * D + tid];
+        sc[tid] = fabsf(qv) * am;
     }
+    if (a.hist != nullptr)
+        for (int i = tid; i < CS_H1; i += CS_NT) lhist[i] = 0u;
     __syncthreads();
     bool sel = false;
     if (tid < D) {
@@ -109,199 +152,62 @@ __global__ void __launch_bounds__(CS_NT) crit_score_kernel(CritArgs a) {
     }
     __syncthreads();
     if (tile == 0 && a.crit != nullptr && tid < a.n_crit) a.crit[((int64_t)b * Hq + h) * a.n_crit + tid] = clist[tid];
-    const int t0 = (tile * CS_NT + tid) * CS_TOK;
-    if (t0 >= T) return;
-    float acc[CS_TOK];
+    const uint16_t* base = a.kT + kvrow * D * a.t_cap;
+    const int cand_lo = a.n_sink, cand_hi = T - a.window;
+    float acc[CS_IT][CS_TOK];
 #pragma unroll
-    for (int i = 0; i < CS_TOK; ++i) acc[i] = 0.0f;
-    const uint16_t* base = a.kT + ((int64_t)b * a.H + g) * D * a.t_cap + t0;
-#pragma unroll 8
+    for (int it = 0; it < CS_IT; ++it)
+#pragma unroll
+        for (int i = 0; i < CS_TOK; ++i) acc[it][i] = 0.0f;
+#pragma unroll 4
     for (int j = 0; j < a.n_crit; ++j) {
         const int c = clist[j];  // ascending channel order
         const float qc = qs[c];
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)c * a.t_cap));
-        float k[8];
-        unpack8(raw, k);
-        // fma == add of the exact fp16*fp16 product: the same fp32 result as (q*k) + acc
 #pragma unroll
-        for (int i = 0; i < CS_TOK; ++i) acc[i] = fmaf(qc, k[i], acc[i]);
-    }
-    float* out = a.scores + ((int64_t)b * Hq + h) * a.score_stride + t0;
-    if (t0 + CS_TOK <= T) {
-        reinterpret_cast<float4*>(out)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        reinterpret_cast<float4*>(out)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    } else {
-        for (int i = 0; i < T - t0; ++i) out[i] = acc[i];
-    }
-}
-
-// ================================================================ a5 top-k select
-
-constexpr int SEL_CL = 8;     // CTAs per cluster: one cluster per (sequence, head)
-constexpr int SEL_NT = 512;
-constexpr int SEL_MAX_CHUNK = 49152;  // keys per CTA held in shared memory
-
-struct SelArgs {
-    const float* scores;
-    int64_t score_stride;
-    const int32_t* seq_lens;
-    int32_t max_len;
-    int32_t n_heads;
-    int32_t k_fixed;
-    double ratio;
-    int32_t n_sink;
-    int32_t window;
-    int32_t* sel;
-    int32_t sel_cap;
-    int32_t* sel_count;
-    KvqWsHeader* hdr;
-};
-
-__global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_NT) topk_select_kernel(SelArgs a) {
-    extern __shared__ __align__(16) uint32_t keys[];
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t tot[256];
-    __shared__ uint32_t wsum[SEL_NT / 32];
-    __shared__ uint32_t xch[2];
-    __shared__ uint32_t s_bin, s_above;
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = (int)cluster.block_rank();
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x;
-    const int T = a.seq_lens[b];
-    int32_t* out = a.sel + ((int64_t)b * a.n_heads + h) * a.sel_cap;
-    if (T < 0 || T > a.max_len) {  // uniform over the cluster: every CTA leaves here
-        if (tid == 0 && rank == 0) {
-            kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
-            a.sel_count[(int64_t)b * a.n_heads + h] = 0;
-        }
-        return;
-    }
-    const int k = a.k_fixed >= 0 ? a.k_fixed : (int)floor(a.ratio * (double)T);
-    const int chunk = (T + SEL_CL - 1) / SEL_CL;
-    const int lo = min(T, rank * chunk), hi = min(T, lo + chunk);
-    if ((int64_t)T <= (int64_t)a.n_sink + a.window + k) {  // everything is kept
-        for (int p = lo + tid; p < hi; p += SEL_NT)
-            if (p < a.sel_cap) out[p] = p;
-        if (rank == 0 && tid == 0) {
-            if (T > a.sel_cap) kvq_dev_flag(a.hdr, KVQ_DEV_OVERFLOW, b);
-            a.sel_count[(int64_t)b * a.n_heads + h] = min(T, a.sel_cap);
-        }
-        return;
-    }
-    const int cand_lo = a.n_sink, cand_hi = T - a.window;
-    const float* row = a.scores + ((int64_t)b * a.n_heads + h) * a.score_stride;
-    for (int p = lo + tid; p < hi; p += SEL_NT) keys[p - lo] = kvq_float_key(row[p]);
-
-    // ---- radix select of the k-th largest candidate key, 8 bits per pass
-    uint32_t prefix = 0u, mask = 0u, remaining = (uint32_t)k;
-    if (k > 0) {
-        for (int pass = 0; pass < 4; ++pass) {
-            const int shift = 24 - 8 * pass;
-            for (int i = tid; i < 256; i += SEL_NT) hist[i] = 0u;
-            __syncthreads();
-            for (int p = max(lo, cand_lo) + tid; p < min(hi, cand_hi); p += SEL_NT) {
-                const uint32_t key = keys[p - lo];
-                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-            }
-            cluster.sync();
-            if (tid < 256) {
-                uint32_t s = 0;
-                for (int r = 0; r < SEL_CL; ++r) s += cluster.map_shared_rank(hist, r)[tid];
-                tot[tid] = s;
-            }
-            cluster.sync();
-            if (tid < 32) {
-                // lane l owns bins [248 - 8l, 255 - 8l]; lane 0 the largest
-                uint32_t ls = 0;
-                for (int j = 0; j < 8; ++j) ls += tot[255 - 8 * tid - j];
-                uint32_t incl = ls;
+        for (int it = 0; it < CS_IT; ++it) {
+            const int t0 = tile * CS_TILE + it * CS_NT * CS_TOK + tid * CS_TOK;
+            if (t0 < T) {
+                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)c * a.t_cap + t0));
+                float k[8];
+                unpack8(raw, k);
+                // the newest token is taken from k_new: its kT column may be written concurrently
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (tid >= o) incl += y;
-                }
-                const uint32_t ballot = __ballot_sync(0xffffffffu, incl >= remaining);
-                const int l = __ffs(ballot) - 1;  // first lane reaching `remaining`
-                if (tid == l) {
-                    uint32_t run = incl - ls;
-                    for (int j = 0; j < 8; ++j) {
-                        const int bin = 255 - 8 * tid - j;
-                        if (run + tot[bin] >= remaining) {
-                            s_bin = (uint32_t)bin;
-                            s_above = run;
-                            break;
-                        }
-                        run += tot[bin];
-                    }
-                }
+                for (int i = 0; i < CS_TOK; ++i)
+                    if (p_new == t0 + i) k[i] = kvq_h2f(knew[c]);
+                // fma == add of the exact fp16*fp16 product: the same fp32 result as (q*k) + acc
+#pragma unroll
+                for (int i = 0; i < CS_TOK; ++i) acc[it][i] = fmaf(qc, k[i], acc[it][i]);
             }
-            __syncthreads();
-            remaining -= s_above;
-            prefix |= s_bin << shift;
-            mask |= 255u << shift;
         }
-    } else {
-        prefix = 0xffffffffu;  // nothing above it, no equal candidate taken
     }
-    const uint32_t kth = prefix;
-    const uint32_t need_eq = k > 0 ? remaining : 0u;
-
-    // ---- ordered compaction: each thread owns a contiguous run of positions
-    const int n = hi - lo;
-    const int seg = (n + SEL_NT - 1) / SEL_NT;
-    const int s0 = lo + min(n, tid * seg), s1 = lo + min(n, (tid + 1) * seg);
-    uint32_t n_eq = 0;
-    for (int p = s0; p < s1; ++p)
-        if (p >= cand_lo && p < cand_hi && keys[p - lo] == kth) ++n_eq;
-    uint32_t eq_cta;
-    const uint32_t eq_before = block_excl_scan<SEL_NT>(n_eq, wsum, &eq_cta);
-    if (tid == 0) xch[0] = eq_cta;
-    cluster.sync();
-    uint32_t eq_base = 0;
-    for (int r = 0; r < rank; ++r) eq_base += cluster.map_shared_rank(xch, r)[0];
-    uint32_t run_eq = eq_base + eq_before, n_sel = 0;
-    for (int p = s0; p < s1; ++p) {
-        bool s;
-        if (p < cand_lo || p >= cand_hi) {
-            s = true;
+#pragma unroll
+    for (int it = 0; it < CS_IT; ++it) {
+        const int t0 = tile * CS_TILE + it * CS_NT * CS_TOK + tid * CS_TOK;
+        if (t0 >= T) continue;
+        float* out = a.scores + ((int64_t)b * Hq + h) * a.score_stride + t0;
+        if (t0 + CS_TOK <= T) {
+            reinterpret_cast<float4*>(out)[0] = make_float4(acc[it][0], acc[it][1], acc[it][2], acc[it][3]);
+            reinterpret_cast<float4*>(out)[1] = make_float4(acc[it][4], acc[it][5], acc[it][6], acc[it][7]);
         } else {
-            const uint32_t key = keys[p - lo];
-            s = key > kth;
-            if (key == kth) s = (run_eq++ < need_eq);
+#pragma unroll
+            for (int i = 0; i < CS_TOK; ++i)
+                if (i < T - t0) out[i] = acc[it][i];
         }
-        n_sel += s;
-    }
-    uint32_t sel_cta;
-    const uint32_t sel_before = block_excl_scan<SEL_NT>(n_sel, wsum, &sel_cta);
-    if (tid == 0) xch[1] = sel_cta;
-    cluster.sync();
-    uint32_t sel_base = 0;
-    for (int r = 0; r < rank; ++r) sel_base += cluster.map_shared_rank(xch, r)[1];
-    uint32_t o_idx = sel_base + sel_before;
-    run_eq = eq_base + eq_before;
-    bool overflow = false;
-    for (int p = s0; p < s1; ++p) {
-        bool s;
-        if (p < cand_lo || p >= cand_hi) {
-            s = true;
-        } else {
-            const uint32_t key = keys[p - lo];
-            s = key > kth;
-            if (key == kth) s = (run_eq++ < need_eq);
-        }
-        if (s) {
-            if (o_idx < (uint32_t)a.sel_cap) out[o_idx] = p;
-            else overflow = true;
-            ++o_idx;
+        if (a.hist != nullptr) {
+#pragma unroll
+            for (int i = 0; i < CS_TOK; ++i) {
+                const int t = t0 + i;
+                if (t >= cand_lo && t < cand_hi) atomicAdd(&lhist[kvq_float_key(acc[it][i]) >> 20], 1u);
+            }
         }
     }
-    if (overflow) kvq_dev_flag(a.hdr, KVQ_DEV_OVERFLOW, b);
-    if (rank == 0 && tid == 0) {
-        const int total = a.n_sink + a.window + k;
-        a.sel_count[(int64_t)b * a.n_heads + h] = min(total, a.sel_cap);
+    if (a.hist == nullptr) return;
+    __syncthreads();
+    uint32_t* gh = a.hist + ((int64_t)b * Hq + h) * CS_H1;
+    for (int i = tid; i < CS_H1; i += CS_NT) {
+        const uint32_t v = lhist[i];
+        if (v) atomicAdd(&gh[i], v);
     }
-    cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // ================================================================ a6 sparse attention
@@ -562,11 +468,8 @@ size_t sa_ws_layout(const kvq_layout* L, const kvq_seqs* S, int32_t sel_cap, siz
 template <int NH>
 int launch_sa(const SAArgs& a, dim3 grid, cudaStream_t s) {
     const size_t smem = (size_t)SA_HW * NH * SA_REC * sizeof(float);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_sparse_attn: %s", cudaGetErrorString(e));
-    }
+    const int st = kvq_prepare_kernel((const void*)sparse_attn_kernel<NH>, (int)smem);
+    if (st) return st;
     sparse_attn_kernel<NH><<<grid, SA_NT, smem, s>>>(a);
     return kvq_launch_status("kv_sparse_attn");
 }
@@ -575,25 +478,30 @@ int launch_sa(const SAArgs& a, dim3 grid, cudaStream_t s) {
 
 // ================================================================ ABI
 
-extern "C" int kv_critical_score(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
-                                 int32_t n_crit, int32_t* crit, float* scores, int64_t score_stride,
-                                 void* stream) {
-    kvq_clear_error();
-    int st = kvq_check_layout(L, "kv_critical_score", true);
+namespace {
+
+int crit_common(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q, int32_t n_crit,
+                float* scores, int64_t score_stride, const char* fn) {
+    int st = kvq_check_layout(L, fn, true);
     if (st) return st;
-    st = kvq_check_seqs(S, "kv_critical_score");
+    st = kvq_check_seqs(S, fn);
     if (st) return st;
-    KVQ_REQUIRE(P && P->kT && P->k_absmax, KVQ_ERR_INVALID_ARG, "kv_critical_score: pool needs kT and k_absmax");
-    KVQ_REQUIRE(n_crit >= 1 && n_crit <= D, KVQ_ERR_INVALID_ARG, "kv_critical_score: n_crit %d not in [1, 128]", n_crit);
+    KVQ_REQUIRE(L->bits == 16, KVQ_ERR_INVALID_ARG, "%s: not an fp16 layer", fn);
+    KVQ_REQUIRE(P && P->kT && P->k_absmax, KVQ_ERR_INVALID_ARG, "%s: pool needs kT and k_absmax", fn);
+    KVQ_REQUIRE(n_crit >= 1 && n_crit <= D, KVQ_ERR_INVALID_ARG, "%s: n_crit %d not in [1, 128]", fn, n_crit);
     KVQ_REQUIRE(P->t_cap % 8 == 0 && P->t_cap >= S->max_len, KVQ_ERR_INVALID_ARG,
-                "kv_critical_score: t_cap must be a multiple of 8 and >= max_len");
-    KVQ_REQUIRE(((uintptr_t)P->kT & 15u) == 0, KVQ_ERR_INVALID_ARG, "kv_critical_score: kT must be 16-byte aligned");
+                "%s: t_cap must be a multiple of 8 and >= max_len", fn);
+    KVQ_REQUIRE(((uintptr_t)P->kT & 15u) == 0, KVQ_ERR_INVALID_ARG, "%s: kT must be 16-byte aligned", fn);
     KVQ_REQUIRE(scores && ((uintptr_t)scores & 15u) == 0 && score_stride % 4 == 0 && score_stride >= S->max_len,
-                KVQ_ERR_INVALID_ARG, "kv_critical_score: scores must be 16-byte aligned, stride %% 4 == 0, >= max_len");
-    KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "kv_critical_score: batch exceeds max_seqs");
-    if (S->batch == 0) return KVQ_OK;
-    KVQ_REQUIRE(q != nullptr, KVQ_ERR_INVALID_ARG, "kv_critical_score: NULL q");
-    CritArgs a;
+                KVQ_ERR_INVALID_ARG, "%s: scores must be 16-byte aligned, stride %% 4 == 0, >= max_len", fn);
+    KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "%s: batch exceeds max_seqs", fn);
+    KVQ_REQUIRE(S->batch == 0 || q != nullptr, KVQ_ERR_INVALID_ARG, "%s: NULL q", fn);
+    return KVQ_OK;
+}
+
+CritArgs crit_args(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q, int32_t n_crit,
+                   int32_t* crit, float* scores, int64_t score_stride) {
+    CritArgs a{};
     a.kT = P->kT;
     a.absmax = P->k_absmax;
     a.t_cap = P->t_cap;
@@ -606,56 +514,60 @@ extern "C" int kv_critical_score(const kvq_layout* L, const kvq_pool* P, const k
     a.crit = crit;
     a.scores = scores;
     a.score_stride = score_stride;
+    return a;
+}
+
+}  // namespace
+
+extern "C" int kv_critical_score(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
+                                 int32_t n_crit, int32_t* crit, float* scores, int64_t score_stride,
+                                 void* stream) {
+    kvq_clear_error();
+    int st = crit_common(L, P, S, q, n_crit, scores, score_stride, "kv_critical_score");
+    if (st) return st;
+    if (S->batch == 0) return KVQ_OK;
+    CritArgs a = crit_args(L, P, S, q, n_crit, crit, scores, score_stride);
     const int tiles = std::max(1, (S->max_len + CS_TILE - 1) / CS_TILE);
+    st = kvq_prepare_kernel((const void*)crit_score_kernel, 0);
+    if (st) return st;
     crit_score_kernel<<<dim3(tiles, L->n_q_heads, S->batch), CS_NT, 0, kvq_stream(stream)>>>(a);
     return kvq_launch_status("kv_critical_score");
 }
 
-extern "C" size_t kv_topk_select_ws(void) { return sizeof(KvqWsHeader); }
+extern "C" size_t kv_append_critical_score_ws(void) { return sizeof(KvqWsHeader); }
 
-extern "C" int kv_topk_select(const kvq_seqs* S, int32_t n_heads, const float* scores, int64_t score_stride,
-                              int32_t k_fixed, double ratio, int32_t n_sink, int32_t window, int32_t* sel,
-                              int32_t sel_cap, int32_t* sel_count, void* ws, size_t ws_bytes, void* stream) {
+extern "C" int kv_append_critical_score(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S,
+                                        const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q,
+                                        int32_t n_crit, int32_t* crit, float* scores, int64_t score_stride,
+                                        uint32_t* hist, int32_t n_sink, int32_t window, void* ws, size_t ws_bytes,
+                                        void* stream) {
     kvq_clear_error();
-    int st = kvq_check_seqs(S, "kv_topk_select");
+    int st = crit_common(L, P, S, q, n_crit, scores, score_stride, "kv_append_critical_score");
     if (st) return st;
-    st = kvq_check_ws(ws, ws_bytes, kv_topk_select_ws(), "kv_topk_select");
+    st = kvq_check_ws(ws, ws_bytes, kv_append_critical_score_ws(), "kv_append_critical_score");
     if (st) return st;
-    KVQ_REQUIRE(n_heads > 0, KVQ_ERR_INVALID_ARG, "kv_topk_select: n_heads");
-    KVQ_REQUIRE(n_sink >= 0 && window >= 0 && sel_cap > 0, KVQ_ERR_INVALID_ARG, "kv_topk_select: sizes");
-    KVQ_REQUIRE(k_fixed >= 0 || (ratio >= 0.0 && ratio <= 1.0), KVQ_ERR_INVALID_ARG, "kv_topk_select: ratio");
-    KVQ_REQUIRE(scores && sel && sel_count && score_stride >= S->max_len, KVQ_ERR_INVALID_ARG,
-                "kv_topk_select: NULL buffer or score_stride < max_len");
-    const int chunk = (S->max_len + SEL_CL - 1) / SEL_CL;
-    KVQ_REQUIRE(chunk <= SEL_MAX_CHUNK, KVQ_ERR_UNSUPPORTED, "kv_topk_select: max_len %d above %d", S->max_len,
-                SEL_CL * SEL_MAX_CHUNK);
+    KVQ_REQUIRE(P->k16 && P->v16, KVQ_ERR_INVALID_ARG, "kv_append_critical_score: pool needs k16 and v16");
+    KVQ_REQUIRE(n_sink >= 0 && window >= 0, KVQ_ERR_INVALID_ARG, "kv_append_critical_score: n_sink / window");
     if (S->batch == 0) return KVQ_OK;
-    SelArgs a;
-    a.scores = scores;
-    a.score_stride = score_stride;
-    a.seq_lens = S->seq_lens;
-    a.max_len = S->max_len;
-    a.n_heads = n_heads;
-    a.k_fixed = k_fixed;
-    a.ratio = ratio;
+    KVQ_REQUIRE(k_new && v_new && S->block_table, KVQ_ERR_INVALID_ARG,
+                "kv_append_critical_score: NULL k_new / v_new / block table");
+    CritArgs a = crit_args(L, P, S, q, n_crit, crit, scores, score_stride);
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k16 = P->k16;
+    a.v16 = P->v16;
+    a.num_blocks = P->num_blocks;
+    a.bt = S->block_table;
+    a.max_blocks = S->max_blocks;
+    a.hist = hist;
     a.n_sink = n_sink;
     a.window = window;
-    a.sel = sel;
-    a.sel_cap = sel_cap;
-    a.sel_count = sel_count;
     a.hdr = static_cast<KvqWsHeader*>(ws);
-    const size_t smem = (size_t)std::max(chunk, 1) * sizeof(uint32_t);
-    static int configured = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured != dev) {
-        cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SEL_MAX_CHUNK * (int)sizeof(uint32_t));
-        if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_topk_select: %s", cudaGetErrorString(e));
-        configured = dev;
-    }
-    topk_select_kernel<<<dim3(SEL_CL, n_heads, S->batch), SEL_NT, smem, kvq_stream(stream)>>>(a);
-    return kvq_launch_status("kv_topk_select");
+    const int tiles = std::max(1, (S->max_len + CS_TILE - 1) / CS_TILE);
+    st = kvq_prepare_kernel((const void*)crit_score_kernel, 0);
+    if (st) return st;
+    crit_score_kernel<<<dim3(tiles, L->n_q_heads, S->batch), CS_NT, 0, kvq_stream(stream)>>>(a);
+    return kvq_launch_status("kv_append_critical_score");
 }
 
 extern "C" size_t kv_sparse_attn_ws(const kvq_layout* L, const kvq_seqs* S, int32_t sel_cap) {

@@ -173,6 +173,35 @@ def kv_critical_score(cache, seqs, q, n_crit, crit, scores, score_stride=None, s
                                          _p(scores), int(score_stride), _s(stream)), "kv_critical_score")
 
 
+def kv_append_critical_score_ws():
+    return lib().kv_append_critical_score_ws()
+
+
+def kv_append_critical_score(cache, seqs, k_new, v_new, q, n_crit, crit, scores, hist, n_sink, window, ws,
+                             score_stride=None, stream=None):
+    if score_stride is None:
+        score_stride = scores.shape[-1]
+    return check(lib().kv_append_critical_score(_ref(cache.layout), _ref(cache), _ref(seqs), _p(k_new), _p(v_new),
+                                                _p(q), int(n_crit), _p(crit), _p(scores), int(score_stride),
+                                                _p(hist), int(n_sink), int(window), ws.ptr, ws.nbytes, _s(stream)),
+                 "kv_append_critical_score")
+
+
+def kv_select_sparse_attn_ws():
+    return lib().kv_select_sparse_attn_ws()
+
+
+def kv_select_sparse_attn(cache, seqs, q, scores, hist, k_fixed, ratio, n_sink, window, sel, sel_count, out, ws,
+                          score_stride=None, stream=None):
+    if score_stride is None:
+        score_stride = scores.shape[-1]
+    sel_cap = int(sel.shape[-1]) if sel is not None else 0
+    return check(lib().kv_select_sparse_attn(_ref(cache.layout), _ref(cache), _ref(seqs), _p(q), _p(scores),
+                                             int(score_stride), _p(hist), int(k_fixed), float(ratio), int(n_sink),
+                                             int(window), _p(sel), sel_cap, _p(sel_count), _p(out), ws.ptr,
+                                             ws.nbytes, _s(stream)), "kv_select_sparse_attn")
+
+
 def kv_topk_select_ws():
     return lib().kv_topk_select_ws()
 

@@ -213,7 +213,7 @@ int kv_critical_score(const kvq_layout* layout, const kvq_pool* pool, const kvq_
  * k_fixed >= 0, else floor(ratio * T) computed in double with T = seq_lens[b].
  * sel: device int32 [batch][n_heads][sel_cap]; sel_count: device int32
  * [batch][n_heads].  sel_cap must hold the largest selection.
- * T <= 8 * 49152 per call (UNSUPPORTED above).
+ * T <= 8 * 46080 = 368640 per call (UNSUPPORTED above).
  * ws: kv_topk_select_ws() bytes (status word only).
  * ---------------------------------------------------------------------- */
 int kv_topk_select(const kvq_seqs* seqs, int32_t n_heads,
@@ -244,6 +244,41 @@ int kv_sparse_attn(const kvq_layout* layout, const kvq_pool* pool, const kvq_seq
                    float* out, float* probs,
                    void* ws, size_t ws_bytes, void* stream);
 size_t kv_sparse_attn_ws(const kvq_layout* layout, const kvq_seqs* seqs, int32_t sel_cap);
+
+/* ------------------------------------------------------------------------
+ * Fused decode step of a sparse (fp16) layer, two launches instead of four:
+ *
+ * kv_append_critical_score = kv_page_append (fp16 layer) + kv_critical_score.
+ * The newest token (position seq_lens[b] - 1, rows k_new/v_new as in
+ * kv_page_append) is written to k16/v16, kT and k_absmax, and the scores of
+ * every token -- the newest included -- are those kv_critical_score would
+ * give after the append.  If hist is not NULL (device uint32
+ * [batch][H_q][4096], zero-filled before first use), the call adds the
+ * histogram of bits 31..20 of the order-preserving keys of the candidate
+ * scores (positions n_sink <= t < T - window) for kv_select_sparse_attn,
+ * which clears it again.  ws: kv_append_critical_score_ws() bytes.
+ *
+ * kv_select_sparse_attn = kv_topk_select + kv_sparse_attn with one list per
+ * q head: the selection of kv_topk_select (same k_fixed / ratio / n_sink /
+ * window) and exact attention over it, in one launch; the output is that of
+ * kv_sparse_attn on the selected list.  hist: NULL or the histogram written
+ * by kv_append_critical_score for these scores with the same n_sink, window
+ * and seq_lens.  sel / sel_count: optional (NULL) copies of the selection in
+ * kv_topk_select's layout.  T <= 368640.  ws: kv_select_sparse_attn_ws().
+ * ---------------------------------------------------------------------- */
+int kv_append_critical_score(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                             const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q,
+                             int32_t n_crit, int32_t* crit, float* scores, int64_t score_stride,
+                             uint32_t* hist, int32_t n_sink, int32_t window,
+                             void* ws, size_t ws_bytes, void* stream);
+size_t kv_append_critical_score_ws(void);
+
+int kv_select_sparse_attn(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                          const uint16_t* q, const float* scores, int64_t score_stride, uint32_t* hist,
+                          int32_t k_fixed, double ratio, int32_t n_sink, int32_t window,
+                          int32_t* sel, int32_t sel_cap, int32_t* sel_count, float* out,
+                          void* ws, size_t ws_bytes, void* stream);
+size_t kv_select_sparse_attn_ws(void);
 
 /* ------------------------------------------------------------------------
  * a7: kv_h2o_accumulate -- H2O heavy-hitter bookkeeping [KVSurvey §三.2, §三.1].

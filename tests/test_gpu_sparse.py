@@ -207,3 +207,68 @@ def test_sparse_attn_flags_bad_index():
         kvq.kvq_check(w)
     # the valid row alone determines the output
     assert torch.allclose(out[0, 0].cpu().float(), KV[0][1][3, 0].float(), atol=1e-6)
+
+
+@pytest.mark.parametrize("use_hist,lengths,k,ratio,ns,w", [
+    (True, [4096 + 3, 1000], -1, 0.03, 4, 128),
+    (True, [4096], 128, 0.0, 4, 64),
+    (False, [3000, 300], 128, 0.0, 4, 64),
+    (True, [150], 128, 0.0, 4, 64),     # everything kept
+])
+def test_fused_append_score_select_attn(use_hist, lengths, k, ratio, ns, w):
+    """kv_append_critical_score + kv_select_sparse_attn (the fused two-launch
+    sparse-layer step) against the oracle: the newest token is appended, the
+    scores, the selection and the attention over it match."""
+    require_gpu()
+    Hq, Hkv = 8, 2
+    B = len(lengths)
+    seed = synth.mix(synth.BASE_SEED, 60, int(use_hist), k)
+    full = [T + 2 for T in lengths]
+    cache, batch, bt, KV = _fp16_layer(Hq, Hkv, full, seed)
+    # the cache holds T - 1 tokens before the step; rebuild it with the first T - 1 only
+    cache2 = kvq.LayerCache(Hq, Hkv, 16, cache.num_blocks, B, t_cap=cache.t_cap)
+    lens_before = [T - 1 for T in lengths]
+    batch2 = kvq.Batch(batch.block_table, torch.tensor(lens_before, dtype=torch.int32, device="cuda"), batch.max_len)
+    for b, T in enumerate(lengths):
+        kvq.kv_quant_pack(cache2, batch2, b, 0, T - 1, KV[b][0][:T - 1].cuda(), KV[b][1][:T - 1].cuda())
+    kvq.kvq_seq_lens_add(batch2.seq_lens, 1)
+    kn = torch.stack([KV[b][0][T - 1] for b, T in enumerate(lengths)]).cuda()
+    vn = torch.stack([KV[b][1][T - 1] for b, T in enumerate(lengths)]).cuda()
+    q = synth.queries((B, Hq, 128), synth.mix(seed, 1))
+    sc = _scores_buf(B, Hq, batch2.max_len)
+    hist = torch.zeros((B, Hq, 4096), dtype=torch.int32, device="cuda") if use_hist else None
+    wa = ws(kvq.kv_append_critical_score_ws())
+    kvq.kv_append_critical_score(cache2, batch2, kn, vn, q.cuda(), 8, None, sc, hist, ns, w, wa)
+    cap = max(O.topk_count(T, k if k >= 0 else O.ratio_k(T, ratio), ns, w) for T in lengths)
+    sel = torch.full((B, Hq, cap), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((B, Hq), dtype=torch.int32, device="cuda")
+    out = torch.full((B, Hq, 128), float("nan"), device="cuda")
+    wsx = ws(kvq.kv_select_sparse_attn_ws())
+    kvq.kv_select_sparse_attn(cache2, batch2, q.cuda(), sc, hist, k, ratio, ns, w, sel, cnt, out, wsx)
+    kvq.kvq_check(wa)
+    kvq.kvq_check(wsx)
+    if use_hist:
+        assert int(hist.abs().sum().item()) == 0     # cleared for the next layer
+    sc_np, sel_np, cnt_np, o = sc.cpu().numpy(), sel.cpu().numpy(), cnt.cpu().numpy(), out.cpu().numpy()
+    am = cache2.k_absmax.cpu().numpy()
+    for b, T in enumerate(lengths):
+        K, V = KV[b][0][:T].numpy(), KV[b][1][:T].numpy()
+        kk = k if k >= 0 else O.ratio_k(T, ratio)
+        for h in range(Hq):
+            g = O.kv_head_of(h, Hq, Hkv)
+            assert np.array_equal(am[b, g], O.key_absmax(K[:, g]).astype(np.float32))
+            C = O.critical_channels(q[b, h].numpy(), O.key_absmax(K[:, g]), 8)
+            a = O.critical_scores(q[b, h].numpy(), K[:, g], C)
+            assert np.array_equal(sc_np[b, h, :T].view(np.uint32), a.view(np.uint32)), (b, h)
+            ids = O.topk_select(a, kk, ns, w)
+            assert cnt_np[b, h] == len(ids)
+            assert sel_np[b, h, :len(ids)].tolist() == ids.tolist(), (b, h)
+            ref, _ = O.sparse_attn(q[b, h].numpy(), K[:, g], V[:, g], ids)
+            assert attn_err(o[b, h], ref) <= ATTN_TOL, (b, h)
+    # the appended rows are in the pages and the channel-major copy
+    for b, T in enumerate(lengths):
+        p = T - 1
+        for g in range(Hkv):
+            assert np.array_equal(cache2.k16[bt[b, p // 16], g, p % 16].cpu().numpy(), KV[b][0][p, g].numpy())
+            assert np.array_equal(cache2.v16[bt[b, p // 16], g, p % 16].cpu().numpy(), KV[b][1][p, g].numpy())
+            assert np.array_equal(cache2.kT[b, g, :, p].cpu().numpy(), KV[b][0][p, g].numpy())
