@@ -64,6 +64,8 @@ PROTOTYPES = {
     "kv_page_append_ws": (c_size_t, []),
     "kv_decode_attn_quant": (c_int, [PL, PP, PS, VP, VP, VP, c_size_t, VP]),
     "kv_decode_attn_quant_ws": (c_size_t, [PL, PS]),
+    "kv_decode_attn_quant_noalloc": (c_int, [PL, PP, PS, VP, VP, VP]),
+    "kv_decode_attn_quant_noalloc_max_scratch": (c_size_t, []),
     "kv_critical_score": (c_int, [PL, PP, PS, VP, c_int32, VP, VP, c_int64, VP]),
     "kv_topk_select": (c_int, [PS, c_int32, VP, c_int64, c_int32, c_double, c_int32, c_int32, VP, c_int32, VP,
                                VP, c_size_t, VP]),

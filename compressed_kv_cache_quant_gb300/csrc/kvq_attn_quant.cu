@@ -9,6 +9,8 @@
 // the same staged codes.  A chunk that holds the unfinished K group reads
 // its keys from the fp16 tail buffer.
 #include <algorithm>
+#include <map>
+#include <mutex>
 
 #include "kvq_internal.cuh"
 
@@ -345,4 +347,103 @@ extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, cons
     }
     if (st) return st;
     return kvq_launch_status("kv_decode_attn_quant");
+}
+
+// ---------------------------------------------------------------- allocation-free variant
+//
+// For callers that may not reserve device memory of their own: a plugin that
+// only receives input and output buffers from a host framework owning every
+// allocation, or a latency-critical decode loop that must not enter the CUDA
+// allocator (cudaMalloc can synchronize the device and stall other streams).
+// The split-K partial states and counters live in one fixed array in the
+// library's device image instead of a caller workspace.
+
+#define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+static __device__ __align__(256) unsigned char g_qattn_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_qattn_scratch for the current device, looked up once per
+// device (the host-side name of the array is not a device address).
+static int qattn_scratch(void** out) {
+    static std::mutex mu;
+    static std::map<int, void*> addr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant_noalloc: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = addr.find(dev);
+    if (it == addr.end()) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_qattn_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant_noalloc: scratch address: %s", cudaGetErrorString(e));
+        it = addr.emplace(dev, p).first;
+    }
+    *out = it->second;
+    return KVQ_OK;
+}
+
+extern "C" size_t kv_decode_attn_quant_noalloc_max_scratch(void) { return KVQ_NOALLOC_SCRATCH_BYTES; }
+
+extern "C" int kv_decode_attn_quant_noalloc(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S,
+                                            const uint16_t* q, float* out, void* stream) {
+    kvq_clear_error();
+    int st = kvq_check_layout(L, "kv_decode_attn_quant_noalloc", true);
+    if (st) return st;
+    st = kvq_check_seqs(S, "kv_decode_attn_quant_noalloc");
+    if (st) return st;
+    KVQ_REQUIRE(L->bits != 16, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: layer is not quantized");
+    KVQ_REQUIRE(P != nullptr && P->k_codes && P->v_codes && P->k_sz && P->v_sz && P->k_tail, KVQ_ERR_INVALID_ARG,
+                "kv_decode_attn_quant_noalloc: quantized pool arrays missing");
+    KVQ_REQUIRE(((uintptr_t)P->k_codes & 15u) == 0 && ((uintptr_t)P->v_codes & 15u) == 0, KVQ_ERR_INVALID_ARG,
+                "kv_decode_attn_quant_noalloc: code arrays must be 16-byte aligned");
+    KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: batch exceeds max_seqs");
+    size_t off_part, off_cnt;
+    const size_t need = ws_layout(L, S, &off_part, &off_cnt);
+    KVQ_REQUIRE(need <= KVQ_NOALLOC_SCRATCH_BYTES, KVQ_ERR_NO_SPACE,
+                "kv_decode_attn_quant_noalloc: this batch needs %zu bytes of scratch, the built-in array holds %u; "
+                "use kv_decode_attn_quant with a workspace", need, KVQ_NOALLOC_SCRATCH_BYTES);
+    if (S->batch == 0) return KVQ_OK;
+    KVQ_REQUIRE(q && out && S->block_table, KVQ_ERR_INVALID_ARG,
+                "kv_decode_attn_quant_noalloc: NULL q/out/block table");
+    void* ws = nullptr;
+    st = qattn_scratch(&ws);
+    if (st) return st;
+    cudaStream_t s = kvq_stream(stream);
+    // The array keeps whatever the previous call left: the status word and the
+    // split counters must start at zero.
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(KvqWsHeader), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(static_cast<char*>(ws) + off_cnt, 0, need - off_cnt, s);
+    if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant_noalloc: %s", cudaGetErrorString(e));
+    const Plan p = plan_splits(L, S);
+    QAttnArgs a;
+    a.k_codes = P->k_codes;
+    a.v_codes = P->v_codes;
+    a.k_sz = reinterpret_cast<const uint32_t*>(P->k_sz);
+    a.v_sz = reinterpret_cast<const uint32_t*>(P->v_sz);
+    a.k_tail = P->k_tail;
+    a.num_blocks = P->num_blocks;
+    a.bt = S->block_table;
+    a.seq_lens = S->seq_lens;
+    a.max_blocks = S->max_blocks;
+    a.max_len = S->max_len;
+    a.H = L->n_kv_heads;
+    a.G = L->v_group_dims;
+    a.q = q;
+    a.out = out;
+    a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + off_part);
+    a.counters = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + off_cnt);
+    a.hdr = static_cast<KvqWsHeader*>(ws);
+    a.n_splits = p.n_splits;
+    a.cps = p.cps;
+    const int gq = L->n_q_heads / L->n_kv_heads;
+    dim3 grid(p.n_splits, L->n_kv_heads, S->batch);
+    switch (L->bits) {
+        case 1: st = launch_bits<1>(gq, grid, s, a); break;
+        case 2: st = launch_bits<2>(gq, grid, s, a); break;
+        case 4: st = launch_bits<4>(gq, grid, s, a); break;
+        default: st = launch_bits<8>(gq, grid, s, a); break;
+    }
+    if (st) return st;
+    return kvq_launch_status("kv_decode_attn_quant_noalloc");
 }

@@ -166,6 +166,17 @@ def kv_decode_attn_quant(cache, seqs, q, out, ws, stream=None):
                                             ws.nbytes, _s(stream)), "kv_decode_attn_quant")
 
 
+def kv_decode_attn_quant_noalloc(cache, seqs, q, out, stream=None):
+    """kv_decode_attn_quant with the library's built-in scratch array instead of a
+    workspace, for callers that may not allocate device memory."""
+    return check(lib().kv_decode_attn_quant_noalloc(_ref(cache.layout), _ref(cache), _ref(seqs), _p(q), _p(out),
+                                                    _s(stream)), "kv_decode_attn_quant_noalloc")
+
+
+def kv_decode_attn_quant_noalloc_max_scratch():
+    return lib().kv_decode_attn_quant_noalloc_max_scratch()
+
+
 def kv_critical_score(cache, seqs, q, n_crit, crit, scores, score_stride=None, stream=None):
     if score_stride is None:
         score_stride = scores.shape[-1]

@@ -188,6 +188,32 @@ int kv_decode_attn_quant(const kvq_layout* layout, const kvq_pool* pool, const k
 size_t kv_decode_attn_quant_ws(const kvq_layout* layout, const kvq_seqs* seqs);
 
 /* ------------------------------------------------------------------------
+ * kv_decode_attn_quant_noalloc -- kv_decode_attn_quant without a workspace.
+ * (An addition of this library: the pages describe no such call.)
+ *
+ * For callers that cannot hand the library device memory: a plugin whose host
+ * framework owns every allocation and passes only input and output buffers,
+ * or a decode loop that must never enter the CUDA allocator (cudaMalloc can
+ * synchronize the device).  It computes exactly what kv_decode_attn_quant
+ * computes, with the same arguments minus the workspace; the split-K scratch
+ * is one fixed 8 MiB array inside the library (kv_decode_attn_quant_noalloc_
+ * max_scratch() bytes), which every GPU that loads the library keeps until
+ * the process exits.  No call allocates or frees memory.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - A batch whose scratch (kv_decode_attn_quant_ws) exceeds the array is
+ *     rejected with KVQ_ERR_NO_SPACE before anything is launched.
+ *   - All calls share the array and each clears the parts that must start at
+ *     zero; calls that overlap on the GPU (other streams, other threads) race
+ *     and give wrong results.  Device data checks still skip bad accesses, but
+ *     their status word is not reported (there is no workspace for kvq_check).
+ * ---------------------------------------------------------------------- */
+int kv_decode_attn_quant_noalloc(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                                 const uint16_t* q, float* out, void* stream);
+size_t kv_decode_attn_quant_noalloc_max_scratch(void);
+
+/* ------------------------------------------------------------------------
  * a4: kv_critical_score -- approximate token scores from critical channels
  * [TailorKV §2.3]: s_c = |q_c| * max_t |K[t][c]| picks the n_crit channels
  * with the largest s_c (ties -> lower channel); then for every cached token
