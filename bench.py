@@ -53,13 +53,16 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def algorithmic_bytes(T):
-    """Algorithmic HBM bytes of one decode step at context T (after append)."""
+def algorithmic_bytes(T, n_layers=32):
+    """Algorithmic HBM bytes of one decode step at context T (after append):
+    layer 0 reads its 1-bit K/V codes and (scale, zero) pairs, 48 B per token
+    and kv head; every sparse layer reads the critical-channel keys (8 fp16 per
+    token and q head) and the selected fp16 K and V rows (512 B per row)."""
     sel = N_SINK + WINDOW + math.floor(RATIO * T)
-    l0 = HKV * T * (16 + 16 + 8 + 8)            # 1-bit K/V codes + K and V (scale, zero)
-    crit = HQ * N_CRIT * T * 2 + HQ * T * 4      # critical-channel keys + score writes
-    rows = HQ * sel * 2 * D * 2                  # selected fp16 K and V rows
-    return l0 + 31 * (crit + rows), crit, rows, l0
+    l0 = HKV * T * (16 + 16 + 8 + 8)
+    crit = HQ * N_CRIT * T * 2
+    rows = HQ * sel * 2 * D * 2
+    return l0 + (n_layers - 1) * (crit + rows), crit, rows, l0
 
 
 class Clocks:
@@ -144,10 +147,8 @@ class Workload:
         self.out = torch.zeros((n_layers, 1, HQ, D), device=device)
         self.ws_app = kvq.Workspace(kvq.kv_page_append_ws())
         self.ws_q = kvq.Workspace(kvq.kv_decode_attn_quant_ws(self.layers[0], self.batch))
-        self.ws_sc = kvq.Workspace(kvq.kv_append_critical_score_ws())
-        self.ws_sx = kvq.Workspace(kvq.kv_select_sparse_attn_ws())
-        self.hist = torch.zeros((1, HQ, 4096), dtype=torch.int32, device=device)
-        self.launches_per_step = 1 + 2 + 2 * (n_layers - 1)
+        self.ws_sx = kvq.Workspace(kvq.kv_sparse_layer_decode_ws())
+        self.launches_per_step = 1 + 2 + (n_layers - 1)
 
     def step(self, stream):
         """One decode step: append + attention in every layer.  Layer 0: page
@@ -162,14 +163,10 @@ class Workload:
             else:
                 self.sparse_layer(l, stream)
 
-    def sparse_layer(self, l, stream, part="all"):
-        kvq, b, c = self.kvq, self.batch, self.layers[l]
-        if part in ("all", "score"):
-            kvq.kv_append_critical_score(c, b, self.in_k[l], self.in_v[l], self.in_q[l], N_CRIT, None, self.scores,
-                                         self.hist, N_SINK, WINDOW, self.ws_sc, self.stride, stream)
-        if part in ("all", "select_attn"):
-            kvq.kv_select_sparse_attn(c, b, self.in_q[l], self.scores, self.hist, -1, RATIO, N_SINK, WINDOW, None,
-                                      None, self.out[l], self.ws_sx, self.stride, stream)
+    def sparse_layer(self, l, stream):
+        """Sparse layer: append + critical scores + top-K + attention in one launch."""
+        self.kvq.kv_sparse_layer_decode(self.layers[l], self.batch, self.in_k[l], self.in_v[l], self.in_q[l], N_CRIT,
+                                        -1, RATIO, N_SINK, WINDOW, self.out[l], self.ws_sx, stream=stream)
 
     def capture(self, fn, stream):
         torch = self.torch
@@ -386,22 +383,22 @@ def main():
         dist.barrier()
     ms_per_step = ms / args.steps
     T_mid = args.prompt + step_i - args.steps // 2
-    step_bytes, crit_bytes, rows_bytes, l0_bytes = algorithmic_bytes(T_mid)
+    step_bytes, crit_bytes, rows_bytes, l0_bytes = algorithmic_bytes(T_mid, args.layers)
 
     # ---- per-kernel durations (CUDA events around graphs of one kernel kind, 31 launches each)
     kern = {}
-    for name, part in (("kv_select_sparse_attn", "select_attn"), ("kv_append_critical_score", "score")):
-        g = W.capture(lambda s, p=part: [W.sparse_layer(l, s, p) for l in range(1, args.layers)], stream)
-        with torch.cuda.stream(stream):
+    g = W.capture(lambda s: [W.sparse_layer(l, s) for l in range(1, args.layers)], stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
             g.replay()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(args.steps):
-                g.replay()
-            b.record(stream)
-        stream.synchronize()
-        kern[name] = a.elapsed_time(b) / (args.steps * (args.layers - 1))
-        del g
+        b.record(stream)
+    stream.synchronize()
+    kern["kv_sparse_layer_decode"] = a.elapsed_time(b) / (args.steps * (args.layers - 1))
+    step_i += args.steps + 1   # each replay appended one token to the sparse layers
+    del g
     g0 = W.capture(lambda s: W.kvq.kv_decode_attn_quant(W.layers[0], W.batch, W.in_q[0], W.out[0], W.ws_q, s),
                    stream)
     with torch.cuda.stream(stream):
@@ -415,12 +412,11 @@ def main():
     kern["kv_decode_attn_quant"] = a.elapsed_time(b) / args.steps
     peak, peak_src = measured_peaks()
     Tk = args.prompt + step_i
-    kb = {"kv_select_sparse_attn": HQ * (N_SINK + WINDOW + math.floor(RATIO * Tk)) * 2 * D * 2,
-          "kv_append_critical_score": HQ * N_CRIT * Tk * 2 + HQ * Tk * 4,
+    kb = {"kv_sparse_layer_decode": HQ * N_CRIT * Tk * 2 + HQ * (N_SINK + WINDOW + math.floor(RATIO * Tk)) * 2 * D * 2,
           "kv_decode_attn_quant": HKV * Tk * 48}
     per_kernel = {k: {"ms": kern[k], "GBps": (kb[k] / (kern[k] * 1e-3) / 1e9) if k in kb else None}
                   for k in kern}
-    dom = max(("kv_select_sparse_attn", "kv_append_critical_score"), key=lambda k: kern[k])
+    dom = "kv_sparse_layer_decode"
     achieved = kb[dom] / (kern[dom] * 1e-3) / 1e9
     tr = traffic_record(dom)
 

@@ -76,6 +76,9 @@ PROTOTYPES = {
     "kv_select_sparse_attn": (c_int, [PL, PP, PS, VP, VP, c_int64, VP, c_int32, c_double, c_int32, c_int32, VP,
                                       c_int32, VP, VP, VP, c_size_t, VP]),
     "kv_select_sparse_attn_ws": (c_size_t, []),
+    "kv_sparse_layer_decode": (c_int, [PL, PP, PS, VP, VP, VP, c_int32, c_int32, c_double, c_int32, c_int32, VP,
+                                       c_int64, VP, c_int32, VP, VP, VP, c_size_t, VP]),
+    "kv_sparse_layer_decode_ws": (c_size_t, []),
     "kv_sparse_attn": (c_int, [PL, PP, PS, VP, VP, c_int32, VP, c_int32, VP, VP, VP, c_size_t, VP]),
     "kv_sparse_attn_ws": (c_size_t, [PL, PS, c_int32]),
     "kv_h2o_accumulate": (c_int, [PL, PS, VP, VP, VP, VP, c_int32, c_int32, c_int32, c_int32, VP, VP, VP,

@@ -244,6 +244,337 @@ __global__ void __launch_bounds__(NT) qattn_kernel(QAttnArgs a) {
     if (tid == 0) a.counters[b * a.H + g] = 0;
 }
 
+// ---------------------------------------------------------------- register-centric kernel
+//
+// Every warp owns 32-token slices of the CTA's range and keeps its own online
+// softmax state.  Scores: one token per lane; the query scaled by the slice's K
+// group scale, q'[c][h] = q[h][c] * scale_c, sits in shared memory and reaches
+// the 32 lanes of a channel in one broadcast load, so
+//   s_t = sum_c q[h][c] zero_c + sum_c q'[c][h] code_t[c].
+// Values: a lane owns four channels; p'[t][h] = p_t,h * vscale_t is broadcast per
+// token and the zero term sum_t p_t,h vzero_t is accumulated per lane and
+// reduced once at the end.
+
+constexpr int NWARP = NT / 32;
+
+template <int BITS, int GQ>
+struct Q2Smem {
+    float qs[GQ][D];                        // query of the group's heads (fp32)
+    float qp[NWARP][D][GQ];                 // per warp: query scaled by the slice's K scales
+    uint32_t vrow[NWARP][32][4 * BITS];     // per warp: V codes of its 32 tokens
+    float pp[NWARP][32][4][GQ];             // per warp: p * V scale, per token, V group, head
+    float m[NWARP][GQ], l[NWARP][GQ];
+};
+
+__device__ __forceinline__ uint32_t bfe_u32(uint32_t w, uint32_t pos, uint32_t len) {
+    uint32_t r;
+    asm("bfe.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(w), "r"(pos), "r"(len));
+    return r;
+}
+
+// small unsigned integer -> float, exactly (2^23 + code, minus 2^23)
+__device__ __forceinline__ float code_f(uint32_t code) { return __uint_as_float(code | 0x4B000000u) - 8388608.0f; }
+
+// (d0, d1) += (a0, a1) * b as one packed fp32 FMA (two IEEE fma operations)
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b) {
+    asm("{.reg .b64 rd, ra, rb;\n\t"
+        "mov.b64 rd, {%0, %1};\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %4};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b));
+}
+
+template <int GQ>
+__device__ __forceinline__ void fma_heads(float* acc, const float* qv, float x) {
+    if constexpr (GQ == 1) {
+        acc[0] = fmaf(qv[0], x, acc[0]);
+    } else {
+#pragma unroll
+        for (int h = 0; h < GQ; h += 2) fma2(acc[h], acc[h + 1], qv[h], qv[h + 1], x);
+    }
+}
+
+template <int GQ>
+__device__ __forceinline__ void lds_heads(float* dst, const float* src) {
+    if constexpr (GQ % 4 == 0) {
+#pragma unroll
+        for (int h = 0; h < GQ; h += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src + h);
+            dst[h] = v.x;
+            dst[h + 1] = v.y;
+            dst[h + 2] = v.z;
+            dst[h + 3] = v.w;
+        }
+    } else if constexpr (GQ == 2) {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        dst[0] = v.x;
+        dst[1] = v.y;
+    } else {
+        dst[0] = src[0];
+    }
+}
+
+template <int BITS, int GQ>
+__global__ void __launch_bounds__(NT) qattn2_kernel(QAttnArgs a) {
+    constexpr int WPR = 4 * BITS;
+    extern __shared__ __align__(16) unsigned char smraw[];
+    Q2Smem<BITS, GQ>& S = *reinterpret_cast<Q2Smem<BITS, GQ>*>(smraw);
+    __shared__ int is_last;
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = a.seq_lens[b];
+    const int n_full = T / KG;
+    const int n_chunks = (T + KG - 1) / KG;
+    const int nsplit_b = (n_chunks + a.cps - 1) / a.cps;
+    const int Hq = a.H * GQ;
+    if (T > a.max_len || T < 0) {
+        if (tid == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
+        return;
+    }
+    if (n_chunks == 0) {  // empty sequence: output 0
+        if (split == 0)
+            for (int i = tid; i < GQ * D; i += NT) a.out[((int64_t)b * Hq + g * GQ) * D + i] = 0.0f;
+        return;
+    }
+    if (split >= nsplit_b) return;
+    const int t_begin = split * a.cps * KG;
+    const int t_end = min(T, t_begin + a.cps * KG);
+    const int NGV = D / a.G;
+    const int jd = (4 * lane) / a.G;  // V group of this lane's four channels
+    const int64_t kvrow = (int64_t)b * a.H + g;
+
+    for (int i = tid; i < GQ * D; i += NT) S.qs[i / D][i % D] = kvq_h2f(a.q[((int64_t)b * Hq + g * GQ) * D + i]);
+    __syncthreads();
+
+    float m[GQ], l[GQ], o[4][GQ], zt[4][GQ];
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            o[i][h] = 0.0f;
+            zt[i][h] = 0.0f;
+        }
+    }
+    float(*qp)[GQ] = S.qp[warp];
+    for (int s0 = t_begin + 32 * warp; s0 < t_end; s0 += 32 * NWARP) {  // uniform over the warp
+        const int t = s0 + lane;
+        const bool valid = t < t_end;
+        const int gi = s0 / KG;
+        const bool packed = gi < n_full;
+        int32_t page = 0;
+        if (valid) {
+            page = a.bt[(int64_t)b * a.max_blocks + (t >> 4)];
+            if (page < 0 || page >= a.num_blocks) {
+                kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
+                page = 0;
+            }
+        }
+        const int64_t slot = ((int64_t)page * a.H + g) * PG + (t & 15);
+        uint32_t kc[WPR];
+#pragma unroll
+        for (int w = 0; w < WPR; ++w) kc[w] = 0u;
+        uint4* vdst = reinterpret_cast<uint4*>(S.vrow[warp][lane]);
+#pragma unroll
+        for (int u = 0; u < WPR / 4; ++u) {
+            uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
+            if (valid) {
+                vv = __ldg(reinterpret_cast<const uint4*>(a.v_codes) + slot * (WPR / 4) + u);
+                if (packed) kv = __ldg(reinterpret_cast<const uint4*>(a.k_codes) + slot * (WPR / 4) + u);
+            }
+            kc[4 * u] = kv.x;
+            kc[4 * u + 1] = kv.y;
+            kc[4 * u + 2] = kv.z;
+            kc[4 * u + 3] = kv.w;
+            vdst[u] = vv;
+        }
+        float2 vsz[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            vsz[j] = make_float2(0.f, 0.f);
+            if (valid && j < NGV) vsz[j] = unpack_sz(a.v_sz[slot * NGV + j]);
+        }
+        // query scaled by the K scales of group gi (or plain, for the fp16 tail)
+        float c0[GQ];
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) c0[h] = 0.0f;
+        if (packed) {
+            int32_t pg = a.bt[(int64_t)b * a.max_blocks + gi * 4];
+            if (pg < 0 || pg >= a.num_blocks) {
+                kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
+                pg = 0;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = lane + 32 * i;
+                const float2 sz = unpack_sz(a.k_sz[((int64_t)pg * a.H + g) * D + c]);
+#pragma unroll
+                for (int h = 0; h < GQ; ++h) {
+                    qp[c][h] = S.qs[h][c] * sz.x;
+                    c0[h] = fmaf(S.qs[h][c], sz.y, c0[h]);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < GQ; ++h) c0[h] = kvq_warp_sum(c0[h]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = lane + 32 * i;
+#pragma unroll
+                for (int h = 0; h < GQ; ++h) qp[c][h] = S.qs[h][c];
+            }
+        }
+        __syncwarp();
+        float sc[GQ];
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) sc[h] = c0[h];
+        if (packed) {
+#pragma unroll
+            for (int w = 0; w < WPR; ++w) {
+                const uint32_t word = kc[w];
+#pragma unroll
+                for (int i = 0; i < 32 / BITS; ++i) {
+                    const int c = w * (32 / BITS) + i;
+                    float qv[GQ];
+                    lds_heads<GQ>(qv, qp[c]);
+                    fma_heads<GQ>(sc, qv, code_f(bfe_u32(word, i * BITS, BITS)));
+                }
+            }
+        } else if (valid) {
+            const uint16_t* kr = a.k_tail + (kvrow * KG + (t & (KG - 1))) * D;
+            for (int c8 = 0; c8 < D; c8 += 8) {
+                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(kr + c8));
+                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 kk = __half22float2(*reinterpret_cast<const __half2*>(&w4[i]));
+                    float qv[GQ];
+                    lds_heads<GQ>(qv, qp[c8 + 2 * i]);
+                    fma_heads<GQ>(sc, qv, kk.x);
+                    lds_heads<GQ>(qv, qp[c8 + 2 * i + 1]);
+                    fma_heads<GQ>(sc, qv, kk.y);
+                }
+            }
+        }
+        // online softmax per head over the warp's 32 tokens
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            const float sh = valid ? sc[h] * KVQ_SCORE_LOG2_SCALE : -INFINITY;
+            const float mn = fmaxf(m[h], kvq_warp_max(sh));
+            const float alpha = exp2f(m[h] - mn);
+            const float p = valid ? exp2f(sh - mn) : 0.0f;
+            l[h] = l[h] * alpha + kvq_warp_sum(p);
+            m[h] = mn;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                o[i][h] *= alpha;
+                zt[i][h] *= alpha;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (j < NGV) {
+                    S.pp[warp][lane][j][h] = p * vsz[j].x;
+                    zt[j][h] = fmaf(p, vsz[j].y, zt[j][h]);
+                }
+            }
+        }
+        __syncwarp();
+        // values: this lane's channels 4*lane .. 4*lane+3 over the 32 tokens
+        const int n_tok = min(32, t_end - s0);
+        for (int tt = 0; tt < n_tok; ++tt) {
+            float pv[GQ];
+            lds_heads<GQ>(pv, S.pp[warp][tt][jd]);
+            const uint32_t w = S.vrow[warp][tt][(4 * lane * BITS) >> 5];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x = code_f(bfe_u32(w, ((4 * lane + i) * BITS) & 31, BITS));
+                fma_heads<GQ>(o[i], pv, x);
+            }
+        }
+        __syncwarp();
+    }
+    // zero term: sum over the warp's lanes of sum_t p vzero, for this lane's V group
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) zt[j][h] = kvq_warp_sum(zt[j][h]);
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+        float z = zt[0][h];
+#pragma unroll
+        for (int j = 1; j < 4; ++j)
+            if (j == jd) z = zt[j][h];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i][h] += z;
+    }
+    // merge the warps of the CTA (the per-warp query buffers hold the values)
+    __syncthreads();
+    float* ro = &S.qp[0][0][0];  // [NWARP][GQ][D]
+    if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            S.m[warp][h] = m[h];
+            S.l[warp][h] = l[h];
+        }
+#pragma unroll
+    for (int h = 0; h < GQ; ++h)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ro[(warp * GQ + h) * D + 4 * lane + i] = o[i][h];
+    __syncthreads();
+    const int64_t rec0 = (((int64_t)b * a.H + g) * a.n_splits + split) * GQ;
+    for (int e = tid; e < GQ * D; e += NT) {
+        const int h = e / D, d = e % D;
+        float M = -INFINITY;
+        for (int w = 0; w < NWARP; ++w) M = fmaxf(M, S.m[w][h]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < NWARP; ++w) {
+                const float wt = exp2f(S.m[w][h] - M);
+                L = fmaf(S.l[w][h], wt, L);
+                O = fmaf(ro[(w * GQ + h) * D + d], wt, O);
+            }
+        }
+        float* r = a.part + (rec0 + h) * REC;
+        if (d == 0) {
+            r[0] = M;
+            r[1] = L;
+        }
+        r[4 + d] = O;
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int prev = atomicAdd(&a.counters[b * a.H + g], 1);
+        is_last = (prev == nsplit_b - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // ---- last CTA of (b, g): merge the splits by log-sum-exp
+    for (int e = tid; e < GQ * D; e += NT) {
+        const int h = e / D, d = e % D;
+        float M = -INFINITY;
+        for (int sp = 0; sp < nsplit_b; ++sp)
+            M = fmaxf(M, __ldcg(a.part + ((((int64_t)b * a.H + g) * a.n_splits + sp) * GQ + h) * REC));
+        float Lsum = 0.0f, acc = 0.0f;
+        if (M != -INFINITY) {
+            for (int sp = 0; sp < nsplit_b; ++sp) {
+                const float* r = a.part + ((((int64_t)b * a.H + g) * a.n_splits + sp) * GQ + h) * REC;
+                const float w = exp2f(__ldcg(r) - M);
+                Lsum = fmaf(__ldcg(r + 1), w, Lsum);
+                acc = fmaf(__ldcg(r + 4 + d), w, acc);
+            }
+        }
+        a.out[((int64_t)b * Hq + g * GQ + h) * D + d] = Lsum > 0.0f ? acc / Lsum : 0.0f;
+    }
+    if (tid == 0) a.counters[b * a.H + g] = 0;
+}
+
 struct Plan {
     int n_splits;
     int cps;
@@ -271,9 +602,10 @@ size_t ws_layout(const kvq_layout* L, const kvq_seqs* S, size_t* off_part, size_
 
 template <int BITS, int GQ>
 int launch_one(dim3 grid, cudaStream_t s, const QAttnArgs& a) {
-    const int st = kvq_prepare_kernel((const void*)qattn_kernel<BITS, GQ>, 0);
+    const int smem = (int)sizeof(Q2Smem<BITS, GQ>);
+    const int st = kvq_prepare_kernel((const void*)qattn2_kernel<BITS, GQ>, smem);
     if (st) return st;
-    qattn_kernel<BITS, GQ><<<grid, NT, 0, s>>>(a);
+    qattn2_kernel<BITS, GQ><<<grid, NT, smem, s>>>(a);
     return KVQ_OK;
 }
 

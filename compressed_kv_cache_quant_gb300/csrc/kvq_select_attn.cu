@@ -30,7 +30,7 @@ constexpr int PG = KVQ_BLOCK_TOKENS;
 constexpr int CL = 8;                 // CTAs per cluster
 constexpr int NT = 512;               // threads per CTA
 constexpr int NW = NT / 32;
-constexpr int MAX_CHUNK = 46080;      // positions per CTA (keys in shared memory)
+constexpr int MAX_CHUNK = 45056;      // positions per CTA (keys in shared memory)
 constexpr int MAXIT = (MAX_CHUNK + NT - 1) / NT;  // 32-position steps per warp in the compaction
 constexpr int CAND_MAX = 2048;        // first-digit candidates gathered in rank 0
 constexpr int H1 = 4096;              // first digit: key bits 31..20
@@ -62,6 +62,17 @@ struct SXArgs {
     int32_t max_blocks;
     int32_t H, GQ;
     float* out;
+    // fused critical scores (kT != NULL): the keys are computed here from the
+    // channel-major K copy after appending the newest token, instead of read
+    uint16_t* kT;
+    float* absmax;
+    int32_t t_cap;
+    int32_t n_crit;
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    uint16_t* k16w;
+    uint16_t* v16w;
+    float* scores_out;       // optional copy of the scores [B][H_q][score_stride]
 };
 
 constexpr int CAP_S = 1024;           // kept positions collected per CTA in the one-pass path
@@ -91,6 +102,11 @@ struct SXSmem {
     uint32_t eq_cnt, sel_cnt;               // this CTA's counts, read by the others
     float st_m[CL], st_l[CL];               // rank 0: the CTAs' softmax states
     float st_o[CL][D];
+    uint32_t slice[H1 / CL];                // digit-1 counts of this CTA's slice of bins, summed over the cluster
+    uint32_t slice_tot;
+    float qs[D], scs[D];                    // fused scores: query, channel importance
+    uint16_t knew[D];
+    int32_t clist[D];
 };
 
 size_t smem_bytes(int chunk) { return kvq_round_up((size_t)std::max(chunk, 1) * sizeof(uint32_t), 16) + sizeof(SXSmem); }
@@ -204,121 +220,257 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     uint32_t kth = 0xffffffffu;  // kept: key > kth, or key == kth and position <= cut
     int32_t cut = -1;
     bool listed = false;         // s.list holds this CTA's kept positions (the one-pass path)
-    if (!keep_all) {
-        // ---- the chunk's keys (16-byte loads, eight in flight per thread)
-        for (int p0 = lo + 4 * tid; p0 < hi; p0 += 4 * NT * 8) {
-            float4 v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int p = p0 + j * 4 * NT;
-                if (p + 3 < hi) {
-                    v[j] = __ldcg(reinterpret_cast<const float4*>(srow + p));
-                } else {
-                    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (p < hi) v[j].x = srow[p];
-                    if (p + 1 < hi) v[j].y = srow[p + 1];
-                    if (p + 2 < hi) v[j].z = srow[p + 2];
+    const bool fused = a.kT != nullptr;
+    if (fused) {
+        // ---- critical channels [TailorKV §2.3]: s_c = |q_c| max_t |K_c| with the newest token
+        // included; the n_crit largest (ties -> lower channel), kept in ascending order
+        const int g = h / a.GQ;
+        const int64_t kvrow = (int64_t)b * a.H + g;
+        const int p_new = T - 1;
+        if (tid < D) {
+            const float qv = kvq_h2f(a.q[row * D + tid]);
+            float am = a.absmax[kvrow * D + tid];
+            if (p_new >= 0) {
+                const uint16_t kn = a.k_new[kvrow * D + tid];
+                s.knew[tid] = kn;
+                am = fmaxf(am, fabsf(kvq_h2f(kn)));
+                if (rank == 0 && h % a.GQ == 0) {
+                    // append the newest token of kv head g (one CTA per kv head does it)
+                    const int32_t page = a.bt[(int64_t)b * a.max_blocks + (p_new >> 4)];
+                    if (page >= 0 && page < a.num_blocks) {
+                        const int64_t off = ((page * (int64_t)a.H + g) * PG + (p_new & 15)) * D + tid;
+                        a.k16w[off] = kn;
+                        a.v16w[off] = a.v_new[kvrow * D + tid];
+                    } else {
+                        kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
+                    }
+                    if (p_new < a.t_cap) a.kT[(kvrow * D + tid) * a.t_cap + p_new] = kn;
+                    a.absmax[kvrow * D + tid] = am;
                 }
             }
+            s.qs[tid] = qv;
+            s.scs[tid] = fabsf(qv) * am;  // product of two fp16 values: exact in fp32
+        }
+        for (int i = tid; i < H1; i += NT) s.u.hist[i] = 0u;
+        __syncthreads();
+        if (tid < 32) {
+            unsigned long long v[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int p = p0 + j * 4 * NT;
-                if (p + 3 < hi) {
-                    *reinterpret_cast<uint4*>(keys + (p - lo)) =
-                        make_uint4(kvq_float_key(v[j].x), kvq_float_key(v[j].y), kvq_float_key(v[j].z),
-                                   kvq_float_key(v[j].w));
-                } else {
-                    if (p < hi) keys[p - lo] = kvq_float_key(v[j].x);
-                    if (p + 1 < hi) keys[p + 1 - lo] = kvq_float_key(v[j].y);
-                    if (p + 2 < hi) keys[p + 2 - lo] = kvq_float_key(v[j].z);
+            for (int j = 0; j < 4; ++j) {
+                const int c = tid + 32 * j;
+                v[j] = ((unsigned long long)kvq_float_key(s.scs[c]) << 8) | (unsigned)(255 - c);
+            }
+            unsigned long long thr = 0ull;
+            for (int bit = 39; bit >= 0; --bit) {
+                const unsigned long long t = thr | (1ull << bit);
+                unsigned cnt = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cnt += v[j] >= t;
+                if ((int)__reduce_add_sync(0xffffffffu, cnt) >= a.n_crit) thr = t;
+            }
+            int before = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool sel = v[j] >= thr;
+                const uint32_t m = __ballot_sync(0xffffffffu, sel);
+                if (sel) s.clist[before + __popc(m & ((1u << tid) - 1u))] = tid + 32 * j;
+                before += __popc(m);
+            }
+        }
+        __syncthreads();
+        // ---- approximate scores a_t = sum over the channels, ascending, of q_c K[t][c] (fp32 from
+        // +0), their keys, and the local histogram of candidate keys
+        const uint16_t* kbase = a.kT + kvrow * D * a.t_cap;
+        for (int p0 = lo + 8 * tid; p0 < hi; p0 += 8 * NT) {
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            const bool has_new = p_new >= p0 && p_new < p0 + 8;
+            for (int j0 = 0; j0 < a.n_crit; j0 += 8) {
+                uint4 raw[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j0 + j < a.n_crit)
+                        raw[j] = __ldg(reinterpret_cast<const uint4*>(kbase + (int64_t)s.clist[j0 + j] * a.t_cap + p0));
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j0 + j >= a.n_crit) break;
+                    const int c = s.clist[j0 + j];
+                    const float qc = s.qs[c];
+                    float kf[8];
+                    unpack8(raw[j], kf);
+                    if (has_new) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (p_new == p0 + i) kf[i] = kvq_h2f(s.knew[c]);
+                    }
+                    // fma == add of the exact fp16*fp16 product: the same fp32 result as (q*k) + acc
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(qc, kf[i], acc[i]);
+                }
+            }
+            uint32_t kk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                kk[i] = kvq_float_key(acc[i]);
+                const int p = p0 + i;
+                if (p < hi && p >= cand_lo && p < cand_hi) atomicAdd(&s.u.hist[kk[i] >> 20], 1u);
+            }
+            if (p0 + 8 <= hi) {
+                *reinterpret_cast<uint4*>(keys + (p0 - lo)) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+                *reinterpret_cast<uint4*>(keys + (p0 - lo) + 4) = make_uint4(kk[4], kk[5], kk[6], kk[7]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (p0 + i < hi) keys[p0 + i - lo] = kk[i];
+            }
+            if (a.scores_out != nullptr) {
+                float* so = a.scores_out + row * a.score_stride + p0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (p0 + i < hi) so[i] = acc[i];
+            }
+        }
+        __syncthreads();
+    }
+    if (!keep_all) {
+        if (!fused) {
+            // ---- the chunk's keys (16-byte loads, eight in flight per thread)
+            for (int p0 = lo + 4 * tid; p0 < hi; p0 += 4 * NT * 8) {
+                float4 v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int p = p0 + j * 4 * NT;
+                    if (p + 3 < hi) {
+                        v[j] = __ldcg(reinterpret_cast<const float4*>(srow + p));
+                    } else {
+                        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (p < hi) v[j].x = srow[p];
+                        if (p + 1 < hi) v[j].y = srow[p + 1];
+                        if (p + 2 < hi) v[j].z = srow[p + 2];
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int p = p0 + j * 4 * NT;
+                    if (p + 3 < hi) {
+                        *reinterpret_cast<uint4*>(keys + (p - lo)) =
+                            make_uint4(kvq_float_key(v[j].x), kvq_float_key(v[j].y), kvq_float_key(v[j].z),
+                                       kvq_float_key(v[j].w));
+                    } else {
+                        if (p < hi) keys[p - lo] = kvq_float_key(v[j].x);
+                        if (p + 1 < hi) keys[p + 1 - lo] = kvq_float_key(v[j].y);
+                        if (p + 2 < hi) keys[p + 2 - lo] = kvq_float_key(v[j].z);
+                    }
                 }
             }
         }
         if (k > 0) {
-            // ---- digit 1 (key bits 31..20): from the score kernel's histogram, or built here
-            if (a.hist != nullptr) {
+            // ---- digit 1 (key bits 31..20): from the score kernel's histogram, or this cluster's
+            if (a.hist != nullptr && !fused) {
                 const uint4* gh = reinterpret_cast<const uint4*>(a.hist + row * H1);
                 for (int i = tid; i < H1 / 4; i += NT) reinterpret_cast<uint4*>(s.u.hist)[i] = __ldcg(gh + i);
                 __syncthreads();
+                find_bin_from_top(s.u.hist, H1, (uint32_t)k, s);
             } else {
-                for (int i = tid; i < H1; i += NT) s.u.hist[i] = 0u;
-                __syncthreads();
-                for (int p = max(lo, cand_lo) + tid; p < min(hi, cand_hi); p += NT)
-                    atomicAdd(&s.u.hist[keys[p - lo] >> 20], 1u);
-                cluster.sync();
-                uint32_t sums[H1 / NT];
-#pragma unroll
-                for (int j = 0; j < H1 / NT; ++j) sums[j] = 0u;
-                for (int r = 0; r < CL; ++r) {
-                    const uint32_t* rh = cluster.map_shared_rank(s.u.hist, r);
-#pragma unroll
-                    for (int j = 0; j < H1 / NT; ++j) sums[j] += rh[tid + j * NT];
+                if (!fused) {
+                    for (int i = tid; i < H1; i += NT) s.u.hist[i] = 0u;
+                    __syncthreads();
+                    for (int p = max(lo, cand_lo) + tid; p < min(hi, cand_hi); p += NT)
+                        atomicAdd(&s.u.hist[keys[p - lo] >> 20], 1u);
                 }
+                // every CTA sums one eighth of the bins over the cluster, then the slice holding
+                // the k-th largest key is found from the eight slice totals
+                constexpr int SL = H1 / CL;
+                static_assert(SL == NT, "one bin of the slice per thread");
                 cluster.sync();
-#pragma unroll
-                for (int j = 0; j < H1 / NT; ++j) s.u.hist[tid + j * NT] = sums[j];
+                uint32_t v = 0;
+                for (int r = 0; r < CL; ++r) v += cluster.map_shared_rank(s.u.hist, r)[SL * rank + tid];
+                s.slice[tid] = v;
+                uint32_t tot;
+                excl_scan<NT>(v, s.wsum, &tot);
+                if (tid == 0) s.slice_tot = tot;
+                cluster.sync();
+                uint32_t above = 0;
+                int rs = CL - 1;
+                for (; rs > 0; --rs) {
+                    const uint32_t t = cluster.map_shared_rank(&s, rs)->slice_tot;
+                    if (above + t >= (uint32_t)k) break;
+                    above += t;
+                }
+                // the bins of slice rs, highest first
+                uint32_t* sl = reinterpret_cast<uint32_t*>(s.v.w.h2);  // free until the later passes
+                sl[tid] = cluster.map_shared_rank(&s, rs)->slice[tid];
+                __syncthreads();
+                find_bin_from_top(sl, SL, (uint32_t)k - above, s);  // ends with a barrier
+                if (tid == 0) {
+                    s.s_bin += SL * rs;
+                    s.s_above += above;
+                }
                 __syncthreads();
             }
-            find_bin_from_top(s.u.hist, H1, (uint32_t)k, s);
             const uint32_t b1 = s.s_bin;
             uint32_t remaining = (uint32_t)k - s.s_above;
-            // ---- positions above digit 1 (and sinks, window) are kept; ties on digit 1 are
-            // candidates.  Count per warp, scan the warp totals, then write in order.
-            auto classify = [&](int p, bool& sure, bool& cnd, uint32_t& key) {
-                sure = cnd = false;
-                key = 0;
-                if (p < w_hi) {
-                    if (p < cand_lo || p >= cand_hi) {
-                        sure = true;
-                    } else {
-                        key = keys[p - lo];
-                        sure = (key >> 20) > b1;
-                        cnd = (key >> 20) == b1;
+            // ---- one pass, four positions per lane: positions above digit 1 (and sinks,
+            // window) are kept, ties on digit 1 are candidates; a warp reserves its slots with
+            // one atomic per list and places its lanes by an exclusive scan
+            if (tid == 0) {
+                s.n_s = 0;
+                s.n_c = 0;
+            }
+            __syncthreads();
+            for (int base = 0; base < n; base += 4 * NT) {  // bound uniform over the CTA
+                const int q0 = base + 4 * tid;
+                uint4 kv = make_uint4(0u, 0u, 0u, 0u);
+                if (q0 < n) kv = *reinterpret_cast<const uint4*>(keys + q0);
+                const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
+                uint32_t fs = 0u, fc = 0u;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int p = lo + q0 + i;
+                    if (p < hi) {
+                        if (p < cand_lo || p >= cand_hi) {
+                            fs |= 1u << i;
+                        } else {
+                            const uint32_t bin = kk[i] >> 20;
+                            if (bin > b1) fs |= 1u << i;
+                            else if (bin == b1) fc |= 1u << i;
+                        }
                     }
                 }
-            };
-            {
-                uint32_t cs = 0, cc = 0;
-                for (int p0 = w_lo; p0 < w_hi; p0 += 32) {
-                    bool sure, cnd;
-                    uint32_t key;
-                    classify(p0 + lane, sure, cnd, key);
-                    cs += __popc(__ballot_sync(0xffffffffu, sure));
-                    cc += __popc(__ballot_sync(0xffffffffu, cnd));
+                const uint32_t ns = __popc(fs), nc = __popc(fc);
+                uint32_t xs = ns, xc = nc;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t ys = __shfl_up_sync(0xffffffffu, xs, o);
+                    const uint32_t yc = __shfl_up_sync(0xffffffffu, xc, o);
+                    if (lane >= o) {
+                        xs += ys;
+                        xc += yc;
+                    }
                 }
+                const uint32_t ts = __shfl_sync(0xffffffffu, xs, 31), tc = __shfl_sync(0xffffffffu, xc, 31);
+                uint32_t bs = 0u, bc = 0u;
                 if (lane == 0) {
-                    s.wtot[warp] = cs;
-                    s.wtot2[warp] = cc;
+                    if (ts) bs = atomicAdd(reinterpret_cast<unsigned*>(&s.n_s), ts);
+                    if (tc) bc = atomicAdd(reinterpret_cast<unsigned*>(&s.n_c), tc);
                 }
-                __syncthreads();
-                uint32_t bs = 0, bc = 0, ts = 0, tc = 0;
-                for (int w = 0; w < NW; ++w) {
-                    if (w < warp) {
-                        bs += s.wtot[w];
-                        bc += s.wtot2[w];
+                bs = __shfl_sync(0xffffffffu, bs, 0) + xs - ns;
+                bc = __shfl_sync(0xffffffffu, bc, 0) + xc - nc;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t p = (uint32_t)(lo + q0 + i);
+                    if ((fs >> i) & 1u) {
+                        if (bs < (uint32_t)CAP_S) s.list[bs] = p;
+                        ++bs;
                     }
-                    ts += s.wtot[w];
-                    tc += s.wtot2[w];
-                }
-                for (int p0 = w_lo; p0 < w_hi; p0 += 32) {
-                    bool sure, cnd;
-                    uint32_t key;
-                    const int p = p0 + lane;
-                    classify(p, sure, cnd, key);
-                    const uint32_t ms = __ballot_sync(0xffffffffu, sure);
-                    const uint32_t mc = __ballot_sync(0xffffffffu, cnd);
-                    const uint32_t lt = (1u << lane) - 1u;
-                    if (sure && bs + __popc(ms & lt) < (uint32_t)CAP_S) s.list[bs + __popc(ms & lt)] = (uint32_t)p;
-                    if (cnd && bc + __popc(mc & lt) < (uint32_t)CAP_C)
-                        s.v.w.cl[bc + __popc(mc & lt)] = ((unsigned long long)key << 32) | (uint32_t)p;
-                    bs += __popc(ms);
-                    bc += __popc(mc);
-                }
-                if (tid == 0) {
-                    s.n_s = (int32_t)ts;
-                    s.n_c = (int32_t)tc;
+                    if ((fc >> i) & 1u) {
+                        if (bc < (uint32_t)CAP_C) s.v.w.cl[bc] = ((unsigned long long)kk[i] << 32) | p;
+                        ++bc;
+                    }
                 }
             }
+            __syncthreads();
             if (tid == 0) s.n_cand = 0;
             cluster.sync();  // local lists complete; every CTA is done with its histogram
             if (a.hist != nullptr && rank == 0)  // read by all: clear it for the next layer
@@ -772,4 +924,75 @@ extern "C" int kv_select_sparse_attn(const kvq_layout* L, const kvq_pool* P, con
     st = launch(a, S->batch, kvq_stream(stream));
     if (st) return st;
     return kvq_launch_status("kv_select_sparse_attn");
+}
+
+extern "C" size_t kv_sparse_layer_decode_ws(void) { return sizeof(KvqWsHeader); }
+
+extern "C" int kv_sparse_layer_decode(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S,
+                                      const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q, int32_t n_crit,
+                                      int32_t k_fixed, double ratio, int32_t n_sink, int32_t window, float* scores,
+                                      int64_t score_stride, int32_t* sel, int32_t sel_cap, int32_t* sel_count,
+                                      float* out, void* ws, size_t ws_bytes, void* stream) {
+    kvq_clear_error();
+    const char* fn = "kv_sparse_layer_decode";
+    int st = kvq_check_layout(L, fn, true);
+    if (st) return st;
+    st = kvq_check_seqs(S, fn);
+    if (st) return st;
+    st = kvq_check_ws(ws, ws_bytes, kv_sparse_layer_decode_ws(), fn);
+    if (st) return st;
+    KVQ_REQUIRE(L->bits == 16, KVQ_ERR_INVALID_ARG, "%s: not an fp16 layer", fn);
+    KVQ_REQUIRE(P && P->k16 && P->v16 && P->kT && P->k_absmax, KVQ_ERR_INVALID_ARG,
+                "%s: pool needs k16, v16, kT and k_absmax", fn);
+    KVQ_REQUIRE((((uintptr_t)P->k16 | (uintptr_t)P->v16 | (uintptr_t)P->kT) & 15u) == 0, KVQ_ERR_INVALID_ARG,
+                "%s: k16, v16 and kT must be 16-byte aligned", fn);
+    KVQ_REQUIRE(P->t_cap % 8 == 0 && P->t_cap >= S->max_len, KVQ_ERR_INVALID_ARG,
+                "%s: t_cap must be a multiple of 8 and >= max_len", fn);
+    KVQ_REQUIRE(n_crit >= 1 && n_crit <= D, KVQ_ERR_INVALID_ARG, "%s: n_crit %d not in [1, 128]", fn, n_crit);
+    KVQ_REQUIRE(n_sink >= 0 && window >= 0, KVQ_ERR_INVALID_ARG, "%s: n_sink / window", fn);
+    KVQ_REQUIRE(k_fixed >= 0 || (ratio >= 0.0 && ratio <= 1.0), KVQ_ERR_INVALID_ARG, "%s: ratio", fn);
+    KVQ_REQUIRE(chunk_of(S->max_len) <= MAX_CHUNK, KVQ_ERR_UNSUPPORTED, "%s: max_len %d above %d", fn, S->max_len,
+                CL * MAX_CHUNK);
+    KVQ_REQUIRE(scores == nullptr || score_stride >= S->max_len, KVQ_ERR_INVALID_ARG, "%s: score_stride", fn);
+    KVQ_REQUIRE(sel == nullptr || (sel_cap > 0 && sel_count != nullptr), KVQ_ERR_INVALID_ARG, "%s: sel", fn);
+    KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "%s: batch exceeds max_seqs", fn);
+    if (S->batch == 0) return KVQ_OK;
+    KVQ_REQUIRE(k_new && v_new && q && out && S->block_table && ((uintptr_t)q & 15u) == 0, KVQ_ERR_INVALID_ARG,
+                "%s: NULL k_new / v_new / q / out / block table, or q not 16-byte aligned", fn);
+    SXArgs a{};
+    a.scores = nullptr;
+    a.score_stride = scores ? score_stride : 0;
+    a.hist = nullptr;
+    a.seq_lens = S->seq_lens;
+    a.max_len = S->max_len;
+    a.n_heads = L->n_q_heads;
+    a.k_fixed = k_fixed;
+    a.ratio = ratio;
+    a.n_sink = n_sink;
+    a.window = window;
+    a.sel = sel;
+    a.sel_cap = sel_cap;
+    a.sel_count = sel_count;
+    a.hdr = static_cast<KvqWsHeader*>(ws);
+    a.q = q;
+    a.k16 = P->k16;
+    a.v16 = P->v16;
+    a.num_blocks = P->num_blocks;
+    a.bt = S->block_table;
+    a.max_blocks = S->max_blocks;
+    a.H = L->n_kv_heads;
+    a.GQ = L->n_q_heads / L->n_kv_heads;
+    a.out = out;
+    a.kT = P->kT;
+    a.absmax = P->k_absmax;
+    a.t_cap = P->t_cap;
+    a.n_crit = n_crit;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k16w = P->k16;
+    a.v16w = P->v16;
+    a.scores_out = scores;
+    st = launch(a, S->batch, kvq_stream(stream));
+    if (st) return st;
+    return kvq_launch_status(fn);
 }

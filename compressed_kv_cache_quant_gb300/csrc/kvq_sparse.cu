@@ -52,12 +52,17 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, 
 }
 
 // ================================================================ a4 critical score (+ fused fp16 append)
+//
+// A persistent grid: every CTA takes a contiguous run of work items
+// (sequence, q head, 2048-token tile), so each CTA meets few heads and
+// picks their critical channels once per head.
 
 constexpr int CS_NT = 256;
-constexpr int CS_TOK = 8;                          // tokens per thread and pass
-constexpr int CS_IT = 2;                           // passes per CTA
-constexpr int CS_TILE = CS_NT * CS_TOK * CS_IT;    // tokens per CTA
+constexpr int CS_TOK = 8;                          // tokens per thread and item
+constexpr int CS_TILE = CS_NT * CS_TOK;            // tokens per work item
 constexpr int CS_H1 = 4096;                        // histogram of key bits 31..20
+constexpr int CS_MINB = 4;                         // CTAs per SM the grid is sized for
+constexpr int CS_BATCH = 8;                        // channel rows loaded before any arithmetic
 
 struct CritArgs {
     uint16_t* kT;
@@ -71,6 +76,8 @@ struct CritArgs {
     int32_t* crit;
     float* scores;
     int64_t score_stride;
+    int32_t tiles;      // work items per (sequence, q head)
+    int32_t n_items;    // batch * H_q * tiles
     // fused append of the newest token (k_new == NULL: no append)
     const uint16_t* k_new;
     const uint16_t* v_new;
@@ -85,34 +92,103 @@ struct CritArgs {
     KvqWsHeader* hdr;
 };
 
-__global__ void __launch_bounds__(CS_NT) crit_score_kernel(CritArgs a) {
+__device__ __forceinline__ void unpack8h(const uint4& r, float* f) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
+    }
+}
+
+__global__ void __launch_bounds__(CS_NT, CS_MINB) crit_score_kernel(CritArgs a) {
     __shared__ float sc[D];
     __shared__ float qs[D];
     __shared__ uint16_t knew[D];
     __shared__ int32_t clist[D];
-    __shared__ uint32_t selmask[D / 32];
     __shared__ uint32_t lhist[CS_H1];
-    const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x;
-    const int g = h / a.GQ;
     const int Hq = a.H * a.GQ;
-    const int64_t kvrow = (int64_t)b * a.H + g;
-    int T = a.seq_lens[b];
-    if (T < 0 || T > a.max_len || T > a.t_cap) {  // lengths past the buffers are cut and reported
-        if (tid == 0 && tile == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
-        T = max(0, min(T, min(a.t_cap, a.max_len)));
-    }
-    if (tile > 0 && tile * CS_TILE >= T) return;
-    const int p_new = a.k_new != nullptr ? T - 1 : -1;
-    if (tid < D) {
-        const float qv = kvq_h2f(a.q[((int64_t)b * Hq + h) * D + tid]);
-        float am = a.absmax[kvrow * D + tid];
-        if (p_new >= 0) {
-            const uint16_t kn = a.k_new[kvrow * D + tid];
-            knew[tid] = kn;
-            am = fmaxf(am, fabsf(kvq_h2f(kn)));
-            if (tile == 0 && h % a.GQ == 0) {
+    const int i_begin = (int)(((int64_t)a.n_items * blockIdx.x) / gridDim.x);
+    const int i_end = (int)(((int64_t)a.n_items * (blockIdx.x + 1)) / gridDim.x);
+    int cur = -1;  // (sequence, q head) row whose channels and histogram are held
+    int T = 0, p_new = -1, cand_lo = 0, cand_hi = 0;
+    if (a.hist != nullptr)
+        for (int i = tid; i < CS_H1; i += CS_NT) lhist[i] = 0u;
+    for (int item = i_begin; item < i_end; ++item) {
+        const int rowi = item / a.tiles, tile = item % a.tiles;
+        const int b = rowi / Hq, h = rowi % Hq, g = h / a.GQ;
+        const int64_t kvrow = (int64_t)b * a.H + g;
+        if (rowi != cur) {
+            __syncthreads();  // the previous row's channels and histogram are no longer read
+            if (a.hist != nullptr && cur >= 0) {
+                uint32_t* gh = a.hist + (int64_t)cur * CS_H1;
+                for (int i = tid; i < CS_H1; i += CS_NT) {
+                    const uint32_t v = lhist[i];
+                    if (v) {
+                        atomicAdd(&gh[i], v);
+                        lhist[i] = 0u;
+                    }
+                }
+            }
+            cur = rowi;
+            T = a.seq_lens[b];
+            if (T < 0 || T > a.max_len || T > a.t_cap) {  // lengths past the buffers are cut and reported
+                if (tid == 0 && tile == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
+                T = max(0, min(T, min(a.t_cap, a.max_len)));
+            }
+            p_new = a.k_new != nullptr ? T - 1 : -1;
+            cand_lo = a.n_sink;
+            cand_hi = T - a.window;
+            if (tid < D) {
+                const float qv = kvq_h2f(a.q[(int64_t)rowi * D + tid]);
+                float am = a.absmax[kvrow * D + tid];
+                if (p_new >= 0) {
+                    const uint16_t kn = a.k_new[kvrow * D + tid];
+                    knew[tid] = kn;
+                    am = fmaxf(am, fabsf(kvq_h2f(kn)));
+                }
+                qs[tid] = qv;
+                // |q_c| * max|K_c|: both fp16 values, so the fp32 product is exact
+                sc[tid] = fabsf(qv) * am;
+            }
+            __syncthreads();
+            if (tid < 32) {
+                // The n_crit largest (s_c, -c): the largest threshold T with at least n_crit
+                // composites v_c = key(s_c) << 8 | (255 - c) >= T, found bit by bit.  The
+                // composites are distinct, so exactly n_crit channels reach T.
+                unsigned long long v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c = tid + 32 * j;
+                    v[j] = ((unsigned long long)kvq_float_key(sc[c]) << 8) | (unsigned)(255 - c);
+                }
+                unsigned long long thr = 0ull;
+                for (int bit = 39; bit >= 0; --bit) {
+                    const unsigned long long t = thr | (1ull << bit);
+                    unsigned cnt = 0;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) cnt += v[j] >= t;
+                    if ((int)__reduce_add_sync(0xffffffffu, cnt) >= a.n_crit) thr = t;
+                }
+                // list the chosen channels in ascending order
+                int before = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool sel = v[j] >= thr;
+                    const uint32_t m = __ballot_sync(0xffffffffu, sel);
+                    if (sel) clist[before + __popc(m & ((1u << tid) - 1u))] = tid + 32 * j;
+                    before += __popc(m);
+                }
+            }
+            __syncthreads();
+        }
+        if (tile == 0) {
+            if (a.crit != nullptr && tid < a.n_crit) a.crit[(int64_t)rowi * a.n_crit + tid] = clist[tid];
+            if (p_new >= 0 && h % a.GQ == 0 && tid < D) {
                 // append the newest token of kv head g: fp16 rows, channel-major copy, running absmax
+                const uint16_t kn = knew[tid];
                 const int32_t page = a.bt[(int64_t)b * a.max_blocks + (p_new >> 4)];
                 if (page >= 0 && page < a.num_blocks) {
                     const int64_t off = ((page * (int64_t)a.H + g) * PG + (p_new & 15)) * D + tid;
@@ -122,91 +198,65 @@ __global__ void __launch_bounds__(CS_NT) crit_score_kernel(CritArgs a) {
                     kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
                 }
                 a.kT[(kvrow * D + tid) * a.t_cap + p_new] = kn;
-                a.absmax[kvrow * D + tid] = am;
+                a.absmax[kvrow * D + tid] = fmaxf(a.absmax[kvrow * D + tid], fabsf(kvq_h2f(kn)));
             }
         }
-        qs[tid] = qv;
-        // |q_c| * max|K_c|: both fp16 values, so the fp32 product is exact
-        sc[tid] = fabsf(qv) * am;
-    }
-    if (a.hist != nullptr)
-        for (int i = tid; i < CS_H1; i += CS_NT) lhist[i] = 0u;
-    __syncthreads();
-    bool sel = false;
-    if (tid < D) {
-        const float my = sc[tid];
-        int rank = 0;
-        for (int c2 = 0; c2 < D; ++c2) {
-            const float v = sc[c2];
-            rank += (v > my) || (v == my && c2 < tid);
-        }
-        sel = rank < a.n_crit;
-        const uint32_t m = __ballot_sync(0xffffffffu, sel);
-        if ((tid & 31) == 0) selmask[tid >> 5] = m;
-    }
-    __syncthreads();
-    if (tid < D && sel) {
-        int idx = __popc(selmask[tid >> 5] & ((1u << (tid & 31)) - 1u));
-        for (int w = 0; w < (tid >> 5); ++w) idx += __popc(selmask[w]);
-        clist[idx] = tid;
-    }
-    __syncthreads();
-    if (tile == 0 && a.crit != nullptr && tid < a.n_crit) a.crit[((int64_t)b * Hq + h) * a.n_crit + tid] = clist[tid];
-    const uint16_t* base = a.kT + kvrow * D * a.t_cap;
-    const int cand_lo = a.n_sink, cand_hi = T - a.window;
-    float acc[CS_IT][CS_TOK];
+        const int t0 = tile * CS_TILE + tid * CS_TOK;
+        if (t0 >= T) continue;
+        const uint16_t* base = a.kT + kvrow * D * a.t_cap + t0;
+        float acc[CS_TOK];
 #pragma unroll
-    for (int it = 0; it < CS_IT; ++it)
+        for (int i = 0; i < CS_TOK; ++i) acc[i] = 0.0f;
+        for (int j0 = 0; j0 < a.n_crit; j0 += CS_BATCH) {
+            // all loads of the batch in flight before the arithmetic
+            uint4 raw[CS_BATCH];
 #pragma unroll
-        for (int i = 0; i < CS_TOK; ++i) acc[it][i] = 0.0f;
-#pragma unroll 4
-    for (int j = 0; j < a.n_crit; ++j) {
-        const int c = clist[j];  // ascending channel order
-        const float qc = qs[c];
+            for (int j = 0; j < CS_BATCH; ++j)
+                if (j0 + j < a.n_crit)
+                    raw[j] = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)clist[j0 + j] * a.t_cap));
+            const bool has_new = p_new >= t0 && p_new < t0 + CS_TOK;
 #pragma unroll
-        for (int it = 0; it < CS_IT; ++it) {
-            const int t0 = tile * CS_TILE + it * CS_NT * CS_TOK + tid * CS_TOK;
-            if (t0 < T) {
-                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)c * a.t_cap + t0));
+            for (int j = 0; j < CS_BATCH; ++j) {
+                if (j0 + j >= a.n_crit) break;
+                const int c = clist[j0 + j];  // ascending channel order
+                const float qc = qs[c];
                 float k[8];
-                unpack8(raw, k);
-                // the newest token is taken from k_new: its kT column may be written concurrently
+                unpack8h(raw[j], k);
+                if (has_new) {
+                    // the newest token is taken from k_new: its kT column may be written concurrently
 #pragma unroll
-                for (int i = 0; i < CS_TOK; ++i)
-                    if (p_new == t0 + i) k[i] = kvq_h2f(knew[c]);
+                    for (int i = 0; i < CS_TOK; ++i)
+                        if (p_new == t0 + i) k[i] = kvq_h2f(knew[c]);
+                }
                 // fma == add of the exact fp16*fp16 product: the same fp32 result as (q*k) + acc
 #pragma unroll
-                for (int i = 0; i < CS_TOK; ++i) acc[it][i] = fmaf(qc, k[i], acc[it][i]);
+                for (int i = 0; i < CS_TOK; ++i) acc[i] = fmaf(qc, k[i], acc[i]);
             }
         }
-    }
-#pragma unroll
-    for (int it = 0; it < CS_IT; ++it) {
-        const int t0 = tile * CS_TILE + it * CS_NT * CS_TOK + tid * CS_TOK;
-        if (t0 >= T) continue;
-        float* out = a.scores + ((int64_t)b * Hq + h) * a.score_stride + t0;
+        float* out = a.scores + (int64_t)rowi * a.score_stride + t0;
         if (t0 + CS_TOK <= T) {
-            reinterpret_cast<float4*>(out)[0] = make_float4(acc[it][0], acc[it][1], acc[it][2], acc[it][3]);
-            reinterpret_cast<float4*>(out)[1] = make_float4(acc[it][4], acc[it][5], acc[it][6], acc[it][7]);
+            reinterpret_cast<float4*>(out)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            reinterpret_cast<float4*>(out)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
         } else {
 #pragma unroll
             for (int i = 0; i < CS_TOK; ++i)
-                if (i < T - t0) out[i] = acc[it][i];
+                if (i < T - t0) out[i] = acc[i];
         }
         if (a.hist != nullptr) {
 #pragma unroll
             for (int i = 0; i < CS_TOK; ++i) {
                 const int t = t0 + i;
-                if (t >= cand_lo && t < cand_hi) atomicAdd(&lhist[kvq_float_key(acc[it][i]) >> 20], 1u);
+                if (t >= cand_lo && t < cand_hi) atomicAdd(&lhist[kvq_float_key(acc[i]) >> 20], 1u);
             }
         }
     }
-    if (a.hist == nullptr) return;
-    __syncthreads();
-    uint32_t* gh = a.hist + ((int64_t)b * Hq + h) * CS_H1;
-    for (int i = tid; i < CS_H1; i += CS_NT) {
-        const uint32_t v = lhist[i];
-        if (v) atomicAdd(&gh[i], v);
+    if (a.hist != nullptr && cur >= 0) {
+        __syncthreads();
+        uint32_t* gh = a.hist + (int64_t)cur * CS_H1;
+        for (int i = tid; i < CS_H1; i += CS_NT) {
+            const uint32_t v = lhist[i];
+            if (v) atomicAdd(&gh[i], v);
+        }
     }
 }
 
@@ -517,6 +567,16 @@ CritArgs crit_args(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, co
     return a;
 }
 
+int launch_crit(CritArgs& a, const kvq_layout* L, const kvq_seqs* S, cudaStream_t s) {
+    const int st = kvq_prepare_kernel((const void*)crit_score_kernel, 0);
+    if (st) return st;
+    a.tiles = std::max(1, (S->max_len + CS_TILE - 1) / CS_TILE);
+    a.n_items = S->batch * L->n_q_heads * a.tiles;
+    const int grid = std::min(a.n_items, kvq_num_sms() * CS_MINB);
+    crit_score_kernel<<<grid, CS_NT, 0, s>>>(a);
+    return KVQ_OK;
+}
+
 }  // namespace
 
 extern "C" int kv_critical_score(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
@@ -527,10 +587,8 @@ extern "C" int kv_critical_score(const kvq_layout* L, const kvq_pool* P, const k
     if (st) return st;
     if (S->batch == 0) return KVQ_OK;
     CritArgs a = crit_args(L, P, S, q, n_crit, crit, scores, score_stride);
-    const int tiles = std::max(1, (S->max_len + CS_TILE - 1) / CS_TILE);
-    st = kvq_prepare_kernel((const void*)crit_score_kernel, 0);
+    st = launch_crit(a, L, S, kvq_stream(stream));
     if (st) return st;
-    crit_score_kernel<<<dim3(tiles, L->n_q_heads, S->batch), CS_NT, 0, kvq_stream(stream)>>>(a);
     return kvq_launch_status("kv_critical_score");
 }
 
@@ -563,10 +621,8 @@ extern "C" int kv_append_critical_score(const kvq_layout* L, const kvq_pool* P, 
     a.n_sink = n_sink;
     a.window = window;
     a.hdr = static_cast<KvqWsHeader*>(ws);
-    const int tiles = std::max(1, (S->max_len + CS_TILE - 1) / CS_TILE);
-    st = kvq_prepare_kernel((const void*)crit_score_kernel, 0);
+    st = launch_crit(a, L, S, kvq_stream(stream));
     if (st) return st;
-    crit_score_kernel<<<dim3(tiles, L->n_q_heads, S->batch), CS_NT, 0, kvq_stream(stream)>>>(a);
     return kvq_launch_status("kv_append_critical_score");
 }
 

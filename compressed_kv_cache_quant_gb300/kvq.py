@@ -213,6 +213,20 @@ def kv_select_sparse_attn(cache, seqs, q, scores, hist, k_fixed, ratio, n_sink, 
                                              ws.nbytes, _s(stream)), "kv_select_sparse_attn")
 
 
+def kv_sparse_layer_decode_ws():
+    return lib().kv_sparse_layer_decode_ws()
+
+
+def kv_sparse_layer_decode(cache, seqs, k_new, v_new, q, n_crit, k_fixed, ratio, n_sink, window, out, ws,
+                           scores=None, sel=None, sel_count=None, stream=None):
+    stride = int(scores.shape[-1]) if scores is not None else 0
+    sel_cap = int(sel.shape[-1]) if sel is not None else 0
+    return check(lib().kv_sparse_layer_decode(_ref(cache.layout), _ref(cache), _ref(seqs), _p(k_new), _p(v_new),
+                                              _p(q), int(n_crit), int(k_fixed), float(ratio), int(n_sink),
+                                              int(window), _p(scores), stride, _p(sel), sel_cap, _p(sel_count),
+                                              _p(out), ws.ptr, ws.nbytes, _s(stream)), "kv_sparse_layer_decode")
+
+
 def kv_topk_select_ws():
     return lib().kv_topk_select_ws()
 

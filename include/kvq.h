@@ -239,7 +239,7 @@ int kv_critical_score(const kvq_layout* layout, const kvq_pool* pool, const kvq_
  * k_fixed >= 0, else floor(ratio * T) computed in double with T = seq_lens[b].
  * sel: device int32 [batch][n_heads][sel_cap]; sel_count: device int32
  * [batch][n_heads].  sel_cap must hold the largest selection.
- * T <= 8 * 46080 = 368640 per call (UNSUPPORTED above).
+ * T <= 8 * 45056 = 360448 per call (UNSUPPORTED above).
  * ws: kv_topk_select_ws() bytes (status word only).
  * ---------------------------------------------------------------------- */
 int kv_topk_select(const kvq_seqs* seqs, int32_t n_heads,
@@ -290,7 +290,7 @@ size_t kv_sparse_attn_ws(const kvq_layout* layout, const kvq_seqs* seqs, int32_t
  * kv_sparse_attn on the selected list.  hist: NULL or the histogram written
  * by kv_append_critical_score for these scores with the same n_sink, window
  * and seq_lens.  sel / sel_count: optional (NULL) copies of the selection in
- * kv_topk_select's layout.  T <= 368640.  ws: kv_select_sparse_attn_ws().
+ * kv_topk_select's layout.  T <= 360448.  ws: kv_select_sparse_attn_ws().
  * ---------------------------------------------------------------------- */
 int kv_append_critical_score(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
                              const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q,
@@ -305,6 +305,25 @@ int kv_select_sparse_attn(const kvq_layout* layout, const kvq_pool* pool, const 
                           int32_t* sel, int32_t sel_cap, int32_t* sel_count, float* out,
                           void* ws, size_t ws_bytes, void* stream);
 size_t kv_select_sparse_attn_ws(void);
+
+/* ------------------------------------------------------------------------
+ * kv_sparse_layer_decode -- the whole decode step of a sparse (fp16) layer in
+ * one launch: kv_page_append of the newest token, kv_critical_score,
+ * kv_topk_select and kv_sparse_attn (one list per q head).  Equal results:
+ * the same appended rows, the same fp32 scores and selection, the attention
+ * of kv_sparse_attn over that selection [TailorKV §2.3; KVSurvey §三.1;
+ * Meeting §3.2].  The scores never leave the GPU's shared memory unless
+ * `scores` (optional, device fp32 [batch][H_q][score_stride]) asks for a
+ * copy; `sel`/`sel_count` (optional) receive the selection as
+ * kv_topk_select writes it.  T <= 360448.  ws: kv_sparse_layer_decode_ws().
+ * ---------------------------------------------------------------------- */
+int kv_sparse_layer_decode(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                           const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q, int32_t n_crit,
+                           int32_t k_fixed, double ratio, int32_t n_sink, int32_t window,
+                           float* scores, int64_t score_stride,
+                           int32_t* sel, int32_t sel_cap, int32_t* sel_count, float* out,
+                           void* ws, size_t ws_bytes, void* stream);
+size_t kv_sparse_layer_decode_ws(void);
 
 /* ------------------------------------------------------------------------
  * a7: kv_h2o_accumulate -- H2O heavy-hitter bookkeeping [KVSurvey §三.2, §三.1].
