@@ -326,6 +326,7 @@ __global__ void __launch_bounds__(NT) qattn2_kernel(QAttnArgs a) {
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    kvq_pdl_begin();
     const int T = a.seq_lens[b];
     const int n_full = T / KG;
     const int n_chunks = (T + KG - 1) / KG;
@@ -605,7 +606,8 @@ int launch_one(dim3 grid, cudaStream_t s, const QAttnArgs& a) {
     const int smem = (int)sizeof(Q2Smem<BITS, GQ>);
     const int st = kvq_prepare_kernel((const void*)qattn2_kernel<BITS, GQ>, smem);
     if (st) return st;
-    qattn2_kernel<BITS, GQ><<<grid, NT, smem, s>>>(a);
+    const cudaError_t e = kvq_launch_pdl(qattn2_kernel<BITS, GQ>, grid, dim3(NT), (size_t)smem, s, a);
+    if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant launch: %s", cudaGetErrorString(e));
     return KVQ_OK;
 }
 

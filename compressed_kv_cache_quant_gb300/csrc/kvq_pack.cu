@@ -266,6 +266,7 @@ __global__ void __launch_bounds__(128) append_quant_kernel(AppendArgs a) {
     const int h = blockIdx.x;
     const int b = blockIdx.y;
     const int c = threadIdx.x;
+    kvq_pdl_begin();
     const int T = a.seq_lens[b];
     const int64_t p = (int64_t)T - 1;
     if (p < 0) return;
@@ -308,6 +309,7 @@ __global__ void __launch_bounds__(128) append_fp16_kernel(AppendArgs a) {
     const int h = blockIdx.x;
     const int b = blockIdx.y;
     const int c = threadIdx.x;
+    kvq_pdl_begin();
     const int T = a.seq_lens[b];
     const int64_t p = (int64_t)T - 1;
     if (p < 0) return;
@@ -423,8 +425,9 @@ extern "C" int kv_page_append(const kvq_layout* L, const kvq_pool* P, const kvq_
                     "kv_page_append: fp16 layer needs k16, v16, kT, k_absmax");
         st = kvq_prepare_kernel((const void*)append_fp16_kernel, 0);
         if (st) return st;
-        append_fp16_kernel<<<grid, 128, 0, s>>>(a);
-        return kvq_launch_status("kv_page_append");
+        const cudaError_t e = kvq_launch_pdl(append_fp16_kernel, grid, dim3(128), 0, s, a);
+        if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_page_append launch: %s", cudaGetErrorString(e));
+        return KVQ_OK;
     }
     KVQ_REQUIRE(P->k_codes && P->v_codes && P->k_sz && P->v_sz && P->k_tail, KVQ_ERR_INVALID_ARG,
                 "kv_page_append: quantized layer needs k_codes, v_codes, k_sz, v_sz, k_tail");
@@ -433,11 +436,13 @@ extern "C" int kv_page_append(const kvq_layout* L, const kvq_pool* P, const kvq_
                    : L->bits == 4 ? (const void*)append_quant_kernel<4> : (const void*)append_quant_kernel<8>;
     st = kvq_prepare_kernel(fn, 0);
     if (st) return st;
+    cudaError_t e;
     switch (L->bits) {
-        case 1: append_quant_kernel<1><<<grid, 128, 0, s>>>(a); break;
-        case 2: append_quant_kernel<2><<<grid, 128, 0, s>>>(a); break;
-        case 4: append_quant_kernel<4><<<grid, 128, 0, s>>>(a); break;
-        default: append_quant_kernel<8><<<grid, 128, 0, s>>>(a); break;
+        case 1: e = kvq_launch_pdl(append_quant_kernel<1>, grid, dim3(128), 0, s, a); break;
+        case 2: e = kvq_launch_pdl(append_quant_kernel<2>, grid, dim3(128), 0, s, a); break;
+        case 4: e = kvq_launch_pdl(append_quant_kernel<4>, grid, dim3(128), 0, s, a); break;
+        default: e = kvq_launch_pdl(append_quant_kernel<8>, grid, dim3(128), 0, s, a); break;
     }
+    if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_page_append launch: %s", cudaGetErrorString(e));
     return kvq_launch_status("kv_page_append");
 }

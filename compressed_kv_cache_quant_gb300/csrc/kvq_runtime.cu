@@ -77,6 +77,7 @@ int kvq_launch_status(const char* what) {
 // ---------------------------------------------------------------- device helpers
 
 __global__ void kvq_seq_lens_add_kernel(int32_t* lens, int32_t n, int32_t delta) {
+    kvq_pdl_begin();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) lens[i] += delta;
 }
@@ -87,8 +88,11 @@ extern "C" int kvq_seq_lens_add(int32_t* seq_lens, int32_t batch, int32_t delta,
     if (batch == 0) return KVQ_OK;
     int st = kvq_prepare_kernel((const void*)kvq_seq_lens_add_kernel, 0);
     if (st) return st;
-    kvq_seq_lens_add_kernel<<<(batch + 255) / 256, 256, 0, kvq_stream(stream)>>>(seq_lens, batch, delta);
-    return kvq_launch_status("kvq_seq_lens_add");
+    const cudaError_t e =
+        kvq_launch_pdl(kvq_seq_lens_add_kernel, dim3((batch + 255) / 256), dim3(256), 0, kvq_stream(stream), seq_lens,
+                       batch, delta);
+    if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kvq_seq_lens_add: %s", cudaGetErrorString(e));
+    return KVQ_OK;
 }
 
 extern "C" int kv_page_copy(const kvq_layout* L, const kvq_pool* P, int32_t src, int32_t dst, void* stream) {

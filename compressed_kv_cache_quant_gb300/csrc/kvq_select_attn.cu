@@ -197,6 +197,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     const int h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t row = (int64_t)b * a.n_heads + h;
+    kvq_pdl_begin();
     int T = a.seq_lens[b];
     if (T < 0 || T > a.max_len) {
         if (tid == 0 && rank == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
@@ -824,7 +825,9 @@ int launch(const SXArgs& a, int batch, cudaStream_t st) {
     const int r = kvq_prepare_kernel((const void*)select_attn_kernel, (int)smem_bytes(MAX_CHUNK));
     if (r) return r;
     const int chunk_cap = chunk_of(a.max_len);
-    select_attn_kernel<<<dim3(CL, a.n_heads, batch), NT, smem_bytes(chunk_cap), st>>>(a, chunk_cap);
+    const cudaError_t e =
+        kvq_launch_pdl(select_attn_kernel, dim3(CL, a.n_heads, batch), dim3(NT), smem_bytes(chunk_cap), st, a, chunk_cap);
+    if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "select kernel launch: %s", cudaGetErrorString(e));
     return KVQ_OK;
 }
 
