@@ -32,7 +32,7 @@ constexpr int NT = 512;               // threads per CTA
 constexpr int NW = NT / 32;
 constexpr int MAX_CHUNK = 45056;      // positions per CTA (keys in shared memory)
 constexpr int MAXIT = (MAX_CHUNK + NT - 1) / NT;  // 32-position steps per warp in the compaction
-constexpr int CAND_MAX = 2048;        // first-digit candidates gathered in rank 0
+constexpr int CAND_MAX = 4096;        // first-digit candidates gathered in rank 0
 constexpr int H1 = 4096;              // first digit: key bits 31..20
 constexpr int H2 = 1024;              // second and third digits: bits 19..10, 9..0
 constexpr int NHW = NT / 16;          // half-warps (attention: one row per half-warp)
@@ -82,7 +82,7 @@ constexpr int CAP_C = 512;            // first-digit candidates collected per CT
 struct SXSmem {
     union {
         uint32_t hist[H1];                  // first-digit histogram
-        unsigned long long cand[CAND_MAX];  // rank 0: (key << 32 | position) of all first-digit candidates
+        uint32_t cand[CAND_MAX];            // rank 0: (key bits 19..0) << 12 | owner rank, every candidate
     } u;
     union {
         struct {
@@ -104,7 +104,10 @@ struct SXSmem {
     float st_o[CL][D];
     uint32_t slice[H1 / CL];                // digit-1 counts of this CTA's slice of bins, summed over the cluster
     uint32_t slice_tot;
-    float qs[D], scs[D];                    // fused scores: query, channel importance
+    uint32_t eqr[CL];                       // candidates equal to the k-th key, per owner rank
+    float qs[D];                            // fused scores: the query
+    unsigned long long ck[D];               // channel importance key | (255 - channel)
+    uint32_t crank[D];                      // its rank among the channels
     uint16_t knew[D];
     int32_t clist[D];
 };
@@ -250,31 +253,31 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                 }
             }
             s.qs[tid] = qv;
-            s.scs[tid] = fabsf(qv) * am;  // product of two fp16 values: exact in fp32
+            // |q_c| max|K_c|: a product of two fp16 values, exact in fp32; ties -> lower channel
+            s.ck[tid] = ((unsigned long long)kvq_float_key(fabsf(qv) * am) << 8) | (unsigned)(255 - tid);
+            s.crank[tid] = 0u;
         }
         for (int i = tid; i < H1; i += NT) s.u.hist[i] = 0u;
         __syncthreads();
-        if (tid < 32) {
-            unsigned long long v[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int c = tid + 32 * j;
-                v[j] = ((unsigned long long)kvq_float_key(s.scs[c]) << 8) | (unsigned)(255 - c);
-            }
-            unsigned long long thr = 0ull;
-            for (int bit = 39; bit >= 0; --bit) {
-                const unsigned long long t = thr | (1ull << bit);
-                unsigned cnt = 0;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) cnt += v[j] >= t;
-                if ((int)__reduce_add_sync(0xffffffffu, cnt) >= a.n_crit) thr = t;
-            }
+        {
+            // rank of channel c = number of channels with a larger key; four threads per channel
+            static_assert(NT == 4 * D, "four threads per channel");
+            const int c = tid & (D - 1), part = tid >> 7;
+            const unsigned long long v = s.ck[c];
+            uint32_t r = 0;
+#pragma unroll 8
+            for (int j = 0; j < D / 4; ++j) r += s.ck[part * (D / 4) + j] > v;
+            atomicAdd(&s.crank[c], r);
+        }
+        __syncthreads();
+        if (warp == 0) {  // the n_crit channels of rank < n_crit, ascending
             int before = 0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const bool sel = v[j] >= thr;
+            for (int j = 0; j < D / 32; ++j) {
+                const int c = lane + 32 * j;
+                const bool sel = s.crank[c] < (uint32_t)a.n_crit;
                 const uint32_t m = __ballot_sync(0xffffffffu, sel);
-                if (sel) s.clist[before + __popc(m & ((1u << tid) - 1u))] = tid + 32 * j;
+                if (sel) s.clist[before + __popc(m & ((1u << lane) - 1u))] = c;
                 before += __popc(m);
             }
         }
@@ -412,63 +415,75 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
             }
             const uint32_t b1 = s.s_bin;
             uint32_t remaining = (uint32_t)k - s.s_above;
-            // ---- one pass, four positions per lane: positions above digit 1 (and sinks,
-            // window) are kept, ties on digit 1 are candidates; a warp reserves its slots with
-            // one atomic per list and places its lanes by an exclusive scan
+            // ---- one pass, eight positions per lane: positions above digit 1 (and the sinks and
+            // window) are kept, ties on digit 1 are candidates; a warp reserves its slots in both
+            // lists with one atomic each and places its lanes by a packed exclusive scan
             if (tid == 0) {
                 s.n_s = 0;
                 s.n_c = 0;
             }
             __syncthreads();
-            for (int base = 0; base < n; base += 4 * NT) {  // bound uniform over the CTA
-                const int q0 = base + 4 * tid;
-                uint4 kv = make_uint4(0u, 0u, 0u, 0u);
-                if (q0 < n) kv = *reinterpret_cast<const uint4*>(keys + q0);
-                const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
+            const bool inner = lo >= cand_lo && hi <= cand_hi;  // no sink or window position here
+            for (int base = 0; base < n; base += 8 * NT) {      // bound uniform over the CTA
+                const int q0 = base + 8 * tid;
+                uint4 ka = make_uint4(0u, 0u, 0u, 0u), kb = ka;
+                if (q0 < n) {  // q0 + 8 <= chunk_cap: both loads stay inside the key array
+                    ka = *reinterpret_cast<const uint4*>(keys + q0);
+                    kb = *reinterpret_cast<const uint4*>(keys + q0 + 4);
+                }
+                const uint32_t kk[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
                 uint32_t fs = 0u, fc = 0u;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int p = lo + q0 + i;
-                    if (p < hi) {
-                        if (p < cand_lo || p >= cand_hi) {
-                            fs |= 1u << i;
-                        } else {
-                            const uint32_t bin = kk[i] >> 20;
-                            if (bin > b1) fs |= 1u << i;
-                            else if (bin == b1) fc |= 1u << i;
-                        }
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t bin = kk[i] >> 20;
+                    fs |= (uint32_t)(bin > b1) << i;
+                    fc |= (uint32_t)(bin == b1) << i;
                 }
-                const uint32_t ns = __popc(fs), nc = __popc(fc);
-                uint32_t xs = ns, xc = nc;
+                const uint32_t valid = (1u << min(max(n - q0, 0), 8)) - 1u;
+                if (!inner) {
+                    uint32_t in = 0u;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int p = lo + q0 + i;
+                        in |= (uint32_t)(p >= cand_lo && p < cand_hi) << i;
+                    }
+                    fs = (fs & in) | ~in;
+                    fc &= in;
+                }
+                fs &= valid;
+                fc &= valid;
+                const uint32_t cnt = (uint32_t)__popc(fs) | ((uint32_t)__popc(fc) << 16);
+                uint32_t x = cnt;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t ys = __shfl_up_sync(0xffffffffu, xs, o);
-                    const uint32_t yc = __shfl_up_sync(0xffffffffu, xc, o);
-                    if (lane >= o) {
-                        xs += ys;
-                        xc += yc;
-                    }
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
                 }
-                const uint32_t ts = __shfl_sync(0xffffffffu, xs, 31), tc = __shfl_sync(0xffffffffu, xc, 31);
-                uint32_t bs = 0u, bc = 0u;
+                const uint32_t tot = __shfl_sync(0xffffffffu, x, 31);
+                uint32_t bases = 0u;
                 if (lane == 0) {
-                    if (ts) bs = atomicAdd(reinterpret_cast<unsigned*>(&s.n_s), ts);
-                    if (tc) bc = atomicAdd(reinterpret_cast<unsigned*>(&s.n_c), tc);
+                    uint32_t bs = 0u, bc = 0u;
+                    if (tot & 0xffffu) bs = atomicAdd(reinterpret_cast<unsigned*>(&s.n_s), tot & 0xffffu);
+                    if (tot >> 16) bc = atomicAdd(reinterpret_cast<unsigned*>(&s.n_c), tot >> 16);
+                    bases = bs | (bc << 16);  // both below the chunk size < 65536
                 }
-                bs = __shfl_sync(0xffffffffu, bs, 0) + xs - ns;
-                bc = __shfl_sync(0xffffffffu, bc, 0) + xc - nc;
+                bases = __shfl_sync(0xffffffffu, bases, 0) + x - cnt;
+                uint32_t bs = bases & 0xffffu, bc = bases >> 16;
+                const uint32_t p0 = (uint32_t)(lo + q0);
+                while (fs) {
+                    const int i = __ffs(fs) - 1;
+                    fs &= fs - 1u;
+                    if (bs < (uint32_t)CAP_S) s.list[bs] = p0 + i;
+                    ++bs;
+                }
+                while (fc) {
+                    const int i = __ffs(fc) - 1;
+                    fc &= fc - 1u;
+                    uint32_t key = kk[0];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t p = (uint32_t)(lo + q0 + i);
-                    if ((fs >> i) & 1u) {
-                        if (bs < (uint32_t)CAP_S) s.list[bs] = p;
-                        ++bs;
-                    }
-                    if ((fc >> i) & 1u) {
-                        if (bc < (uint32_t)CAP_C) s.v.w.cl[bc] = ((unsigned long long)kk[i] << 32) | p;
-                        ++bc;
-                    }
+                    for (int j = 1; j < 8; ++j) key = i == j ? kk[j] : key;
+                    if (bc < (uint32_t)CAP_C) s.v.w.cl[bc] = ((unsigned long long)key << 32) | (p0 + i);
+                    ++bc;
                 }
             }
             __syncthreads();
@@ -476,75 +491,85 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
             cluster.sync();  // local lists complete; every CTA is done with its histogram
             if (a.hist != nullptr && rank == 0)  // read by all: clear it for the next layer
                 for (int i = tid; i < H1; i += NT) a.hist[row * H1 + i] = 0u;
-            // ---- push the candidates to rank 0 (one reservation per CTA)
+            // ---- push the candidates to rank 0 (one reservation per CTA): the key's low 20 bits
+            // (digit 1 is common to all) and the owner rank
             {
-                SXSmem* r0 = cluster.map_shared_rank(&s, 0);
+                uint32_t* r0c = cluster.map_shared_rank(s.u.cand, 0);
                 __shared__ int s_base;
                 const int nc = min(s.n_c, CAP_C);
-                if (tid == 0) s_base = atomicAdd(&r0->n_cand, s.n_c > CAP_C ? CAND_MAX + 1 : nc);
+                if (tid == 0)
+                    s_base = atomicAdd(&cluster.map_shared_rank(&s, 0)->n_cand, s.n_c > CAP_C ? CAND_MAX + 1 : nc);
                 __syncthreads();
                 const int base = s_base;
                 for (int i = tid; i < nc; i += NT)
-                    if (base + i < CAND_MAX) r0->u.cand[base + i] = s.v.w.cl[i];
+                    if (base + i < CAND_MAX)
+                        r0c[base + i] = (((uint32_t)(s.v.w.cl[i] >> 32) & 0xfffffu) << 12) | (uint32_t)rank;
             }
             cluster.sync();
             const int n_c = cluster.map_shared_rank(&s, 0)->n_cand;
             if (n_c <= CAND_MAX) {
                 // ---- fast path: every CTA finishes the selection over rank 0's candidate list
-                const SXSmem* r0 = cluster.map_shared_rank(&s, 0);
+                const uint32_t* r0c = cluster.map_shared_rank(s.u.cand, 0);
                 constexpr int PER = CAND_MAX / NT;
-                unsigned long long cr[PER];
+                uint32_t cr[PER];
 #pragma unroll
                 for (int j = 0; j < PER; ++j) {
                     const int i = tid + j * NT;
-                    cr[j] = i < n_c ? r0->u.cand[i] : 0ull;
+                    cr[j] = i < n_c ? r0c[i] : 0u;
                 }
-                uint32_t prefix = b1;
+                uint32_t d2 = 0u, d3 = 0u;
                 for (int pass = 0; pass < 2; ++pass) {
-                    const int shift = pass == 0 ? 10 : 0;
                     for (int i = tid; i < H2; i += NT) s.v.w.h2[i] = 0u;
+                    if (pass == 1 && tid < CL) s.eqr[tid] = 0u;
                     __syncthreads();
 #pragma unroll
                     for (int j = 0; j < PER; ++j) {
-                        const uint32_t key = (uint32_t)(cr[j] >> 32);
-                        if (tid + j * NT < n_c && (key >> (shift + 10)) == prefix)
-                            atomicAdd(&s.v.w.h2[(key >> shift) & (H2 - 1)], 1u);
+                        if (tid + j * NT >= n_c) continue;
+                        if (pass == 0) atomicAdd(&s.v.w.h2[cr[j] >> 22], 1u);
+                        else if ((cr[j] >> 22) == d2) atomicAdd(&s.v.w.h2[(cr[j] >> 12) & (H2 - 1)], 1u);
                     }
                     __syncthreads();
                     find_bin_from_top(s.v.w.h2, H2, remaining, s);
                     remaining -= s.s_above;
-                    prefix = (prefix << 10) | s.s_bin;
+                    if (pass == 0) d2 = s.s_bin;
+                    else d3 = s.s_bin;
                 }
-                kth = prefix;
-                // ties at the k-th key: keep the `remaining` lowest positions among them
-                uint32_t c_eq = 0;
+                const uint32_t low = (d2 << 10) | d3;
+                kth = (b1 << 20) | low;
+                // ties at the k-th key: the `remaining` (>= 1) lowest positions among them are kept.
+                // Ranks own ascending position ranges, so this CTA keeps its own lowest
+                // remaining - (ties in lower ranks) of them, clamped to [0, its ties]
 #pragma unroll
-                for (int j = 0; j < PER; ++j) c_eq += tid + j * NT < n_c && (uint32_t)(cr[j] >> 32) == kth;
-                uint32_t eq_total;
-                excl_scan<NT>(c_eq, s.wsum, &eq_total);
-                if (remaining == 0) {
+                for (int j = 0; j < PER; ++j)
+                    if (tid + j * NT < n_c && (cr[j] >> 12) == low) atomicAdd(&s.eqr[cr[j] & (CL - 1)], 1u);
+                if (tid == 0) s.bc_cut = 0x7fffffff;
+                __syncthreads();
+                uint32_t eq_before = 0;
+                for (int r = 0; r < rank; ++r) eq_before += s.eqr[r];
+                const uint32_t eq_mine = s.eqr[rank];
+                const uint32_t keep_t = remaining > eq_before ? min(remaining - eq_before, eq_mine) : 0u;
+                const int nc = min(s.n_c, CAP_C);
+                if (keep_t == 0) {
                     cut = -1;
-                } else if (remaining >= eq_total) {
+                } else if (keep_t == eq_mine) {
                     cut = 0x7fffffff;
                 } else {
-                    if (tid == 0) s.bc_cut = 0x7fffffff;
-                    __syncthreads();
-#pragma unroll
-                    for (int j = 0; j < PER; ++j) {
-                        if (tid + j * NT >= n_c || (uint32_t)(cr[j] >> 32) != kth) continue;
-                        const uint32_t pi = (uint32_t)cr[j];
+                    // the keep_t-th lowest position among this CTA's ties
+                    for (int i = tid; i < nc; i += NT) {
+                        const unsigned long long c = s.v.w.cl[i];
+                        if ((uint32_t)(c >> 32) != kth) continue;
+                        const uint32_t p = (uint32_t)c;
                         uint32_t r = 0;
-                        for (int i = 0; i < n_c; ++i) {
-                            const unsigned long long ci = r0->u.cand[i];
-                            r += ((uint32_t)(ci >> 32) == kth) && ((uint32_t)ci < pi);
+                        for (int i2 = 0; i2 < nc; ++i2) {
+                            const unsigned long long c2 = s.v.w.cl[i2];
+                            r += (uint32_t)(c2 >> 32) == kth && (uint32_t)c2 < p;
                         }
-                        if (r == remaining - 1) s.bc_cut = (int32_t)pi;
+                        if (r == keep_t - 1) s.bc_cut = (int32_t)p;
                     }
                     __syncthreads();
                     cut = s.bc_cut;
                 }
                 // the kept candidates of this CTA join its list
-                const int nc = min(s.n_c, CAP_C);
                 for (int i0 = 0; i0 < nc; i0 += NT) {  // uniform bound
                     const int i = i0 + tid;
                     bool f = false;

@@ -76,10 +76,11 @@ def _select(scores_np, lengths, n_heads, k_fixed, ratio, ns, w):
     ([100, 196, 197], 128, 0.0, 4, 64),  # T <= n_s + W + k keeps everything
     ([131072 + 17], -1, 0.03, 4, 128),   # ratio mode at 128K
     ([20000, 5], 1000, 0.0, 0, 0),
+    ([60000, 131089], -1, 0.03, 4, 128),
 ])
 def test_topk_select_bitexact_with_ties(lengths, k, ratio, ns, w):
     require_gpu()
-    n_heads = 3
+    n_heads = 4
     stride = (max(lengths) + 7) // 8 * 8
     rng = np.random.default_rng(sum(lengths) + k)
     scores = np.full((len(lengths), n_heads, stride), np.nan, dtype=np.float32)
@@ -89,6 +90,8 @@ def test_topk_select_bitexact_with_ties(lengths, k, ratio, ns, w):
                 scores[b, h, :T] = np.round(rng.standard_normal(T) * 2).astype(np.float32)
             elif h == 1:  # all equal, including +0/-0
                 scores[b, h, :T] = np.where(rng.random(T) < 0.5, 0.0, -0.0).astype(np.float32)
+            elif h == 3:  # moderate ties: a tie group at the k-th value spread over the cluster
+                scores[b, h, :T] = (np.round(rng.standard_normal(T) * 64) / 64).astype(np.float32)
             else:
                 scores[b, h, :T] = rng.standard_normal(T).astype(np.float32)
     sel, cnt = _select(scores, lengths, n_heads, k, ratio, ns, w)
