@@ -32,7 +32,6 @@ constexpr int NT = 512;               // threads per CTA
 constexpr int NW = NT / 32;
 constexpr int MAX_CHUNK = 45056;      // positions per CTA (keys in shared memory)
 constexpr int MAXIT = (MAX_CHUNK + NT - 1) / NT;  // 32-position steps per warp in the compaction
-constexpr int CAND_MAX = 4096;        // first-digit candidates gathered in rank 0
 constexpr int H1 = 4096;              // first digit: key bits 31..20
 constexpr int H2 = 1024;              // second and third digits: bits 19..10, 9..0
 constexpr int NHW = NT / 16;          // half-warps (attention: one row per half-warp)
@@ -77,14 +76,16 @@ struct SXArgs {
 
 constexpr int CAP_S = 1024;           // kept positions collected per CTA in the one-pass path
 constexpr int CAP_C = 512;            // first-digit candidates collected per CTA
+static_assert(CL * CAP_C == H1 && CAP_C == NT, "candidate slots: one per thread and rank");
 
 // Shared state of one CTA; it follows the chunk's keys in dynamic shared memory.
 struct SXSmem {
     union {
-        uint32_t hist[H1];                  // first-digit histogram
-        uint32_t cand[CAND_MAX];            // rank 0: (key bits 19..0) << 12 | owner rank, every candidate
+        uint32_t hist[H1];                  // this CTA's first-digit histogram
+        uint32_t cand[CL * CAP_C];          // every rank's first-digit candidates (key bits 19..0), CAP_C slots each
     } u;
     union {
+        uint32_t gh[H1];                    // the cluster's first-digit histogram
         struct {
             uint32_t h2[H2];                // second / third digit histogram
             unsigned long long cl[CAP_C];   // this CTA's first-digit candidates
@@ -95,15 +96,13 @@ struct SXSmem {
     uint32_t list[CAP_S];                   // kept positions, then their row offsets
     uint32_t wsum[NW];
     uint32_t wtot[NW], wtot2[NW];
-    int32_t n_cand;                         // rank 0: candidates gathered
+    uint32_t ncand[CL];                     // first-digit candidates of each rank (above CAP_C: overflow)
     int32_t n_s, n_c;                       // this CTA's kept positions / candidates
     int32_t bc_cut;
     uint32_t s_bin, s_above;
     uint32_t eq_cnt, sel_cnt;               // this CTA's counts, read by the others
     float st_m[CL], st_l[CL];               // rank 0: the CTAs' softmax states
     float st_o[CL][D];
-    uint32_t slice[H1 / CL];                // digit-1 counts of this CTA's slice of bins, summed over the cluster
-    uint32_t slice_tot;
     uint32_t eqr[CL];                       // candidates equal to the k-th key, per owner rank
     float qs[D];                            // fused scores: the query
     unsigned long long ck[D];               // channel importance key | (255 - channel)
@@ -115,6 +114,11 @@ struct SXSmem {
 size_t smem_bytes(int chunk) { return kvq_round_up((size_t)std::max(chunk, 1) * sizeof(uint32_t), 16) + sizeof(SXSmem); }
 int chunk_of(int T) { return ((T + CL - 1) / CL + 31) / 32 * 32; }
 __device__ __forceinline__ int chunk_of_dev(int T) { return ((T + CL - 1) / CL + 31) / 32 * 32; }
+
+// A cluster barrier split in two: arrive (releasing this thread's earlier writes) early, wait
+// (acquiring the other CTAs' writes) where they are needed.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 template <int N>
 __device__ __forceinline__ uint32_t excl_scan(uint32_t v, uint32_t* wsum, uint32_t* total) {
@@ -177,6 +181,51 @@ __device__ __forceinline__ void unpack8(const uint4& r, float* f) {
     }
 }
 
+// acc[i] += q_c * K[p0 + i][c] for the 8 positions in `raw` (fp16); position p0 + inew is
+// the newest token, whose key `knew` is not in the channel-major copy's load yet.
+__device__ __forceinline__ void score_channel(const uint4& raw, float qc, bool has_new, int inew, uint16_t knew,
+                                              float* acc) {
+    float kf[8];
+    unpack8(raw, kf);
+    if (has_new) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (inew == i) kf[i] = kvq_h2f(knew);
+    }
+    // fma == add of the exact fp16*fp16 product: the same fp32 result as (q*k) + acc
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = fmaf(qc, kf[i], acc[i]);
+}
+
+// The 8 scores of positions p0.. (those below hi): their keys into the chunk's key array, the
+// candidates' first digits into the local histogram, the scores to srow_out if given.
+__device__ __forceinline__ void score_finish(const float* acc, int p0, int lo, int hi, int cand_lo, int cand_hi,
+                                             uint32_t* keys, uint32_t* hist, float* srow_out) {
+    if (srow_out != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (p0 + i < hi) srow_out[p0 + i] = acc[i];
+    }
+    const bool full = p0 + 8 <= hi;
+#pragma unroll
+    for (int h4 = 0; h4 < 8; h4 += 4) {  // four keys at a time: fewer live registers
+        uint32_t kk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            kk[i] = kvq_float_key(acc[h4 + i]);
+            const int p = p0 + h4 + i;
+            if (p < hi && p >= cand_lo && p < cand_hi) atomicAdd(&hist[kk[i] >> 20], 1u);
+        }
+        if (full) {
+            *reinterpret_cast<uint4*>(keys + (p0 - lo) + h4) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (p0 + h4 + i < hi) keys[p0 + h4 + i - lo] = kk[i];
+        }
+    }
+}
+
 // Appends, in ballot order, the lanes with f set to list[*n] (capacity cap);
 // returns false if the list overflowed.
 template <typename V>
@@ -220,11 +269,17 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         s.n_s = 0;
         s.n_c = 0;
     }
+    const bool fused = a.kT != nullptr;
+    // the first-digit histograms of the cluster's CTAs are summed into every CTA's copy
+    const bool exchange = !keep_all && k > 0 && (fused || a.hist == nullptr);
+    if (exchange) {
+        for (int i = tid; i < H1; i += NT) s.v.gh[i] = 0u;
+        cluster_arrive();  // the matching wait precedes the first remote add
+    }
 
     uint32_t kth = 0xffffffffu;  // kept: key > kth, or key == kth and position <= cut
     int32_t cut = -1;
     bool listed = false;         // s.list holds this CTA's kept positions (the one-pass path)
-    const bool fused = a.kT != nullptr;
     if (fused) {
         // ---- critical channels [TailorKV §2.3]: s_c = |q_c| max_t |K_c| with the newest token
         // included; the n_crit largest (ties -> lower channel), kept in ascending order
@@ -285,54 +340,55 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         // ---- approximate scores a_t = sum over the channels, ascending, of q_c K[t][c] (fp32 from
         // +0), their keys, and the local histogram of candidate keys
         const uint16_t* kbase = a.kT + kvrow * D * a.t_cap;
-        for (int p0 = lo + 8 * tid; p0 < hi; p0 += 8 * NT) {
-            float acc[8];
+        float* srow_out = a.scores_out != nullptr ? a.scores_out + row * a.score_stride : nullptr;
+        if (a.n_crit <= 8) {
+            // one 16-byte load per channel and 8 positions; a channel's registers are refilled
+            // with the next group's load as soon as they are consumed, so loads stay in flight
+            // channel row offsets: c * t_cap < 128 * 360448 fits in 32 bits
+            const uint32_t tcap = (uint32_t)a.t_cap;
+            uint4 raw[8];
+            int p0 = lo + 8 * tid;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-            const bool has_new = p_new >= p0 && p_new < p0 + 8;
-            for (int j0 = 0; j0 < a.n_crit; j0 += 8) {
-                uint4 raw[8];
+            for (int j = 0; j < 8; ++j) {
+                raw[j] = make_uint4(0u, 0u, 0u, 0u);
+                if (j < a.n_crit && p0 < hi)
+                    raw[j] = __ldg(reinterpret_cast<const uint4*>(kbase + (uint32_t)s.clist[j] * tcap + p0));
+            }
+            for (; p0 < hi; p0 += 8 * NT) {
+                const int pn = p0 + 8 * NT;
+                float acc[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (j0 + j < a.n_crit)
-                        raw[j] = __ldg(reinterpret_cast<const uint4*>(kbase + (int64_t)s.clist[j0 + j] * a.t_cap + p0));
+                for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+                const bool has_new = p_new >= p0 && p_new < p0 + 8;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    if (j0 + j >= a.n_crit) break;
-                    const int c = s.clist[j0 + j];
-                    const float qc = s.qs[c];
-                    float kf[8];
-                    unpack8(raw[j], kf);
-                    if (has_new) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            if (p_new == p0 + i) kf[i] = kvq_h2f(s.knew[c]);
-                    }
-                    // fma == add of the exact fp16*fp16 product: the same fp32 result as (q*k) + acc
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(qc, kf[i], acc[i]);
+                    if (j >= a.n_crit) break;
+                    const int c = s.clist[j];
+                    score_channel(raw[j], s.qs[c], has_new, p_new - p0, s.knew[c], acc);
+                    if (pn < hi) raw[j] = __ldg(reinterpret_cast<const uint4*>(kbase + (uint32_t)c * tcap + pn));
                 }
+                score_finish(acc, p0, lo, hi, cand_lo, cand_hi, keys, s.u.hist, srow_out);
             }
-            uint32_t kk[8];
+        } else {
+            for (int p0 = lo + 8 * tid; p0 < hi; p0 += 8 * NT) {
+                float acc[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                kk[i] = kvq_float_key(acc[i]);
-                const int p = p0 + i;
-                if (p < hi && p >= cand_lo && p < cand_hi) atomicAdd(&s.u.hist[kk[i] >> 20], 1u);
-            }
-            if (p0 + 8 <= hi) {
-                *reinterpret_cast<uint4*>(keys + (p0 - lo)) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
-                *reinterpret_cast<uint4*>(keys + (p0 - lo) + 4) = make_uint4(kk[4], kk[5], kk[6], kk[7]);
-            } else {
+                for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+                const bool has_new = p_new >= p0 && p_new < p0 + 8;
+                for (int j0 = 0; j0 < a.n_crit; j0 += 8) {
+                    uint4 raw[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (p0 + i < hi) keys[p0 + i - lo] = kk[i];
-            }
-            if (a.scores_out != nullptr) {
-                float* so = a.scores_out + row * a.score_stride + p0;
+                    for (int j = 0; j < 8; ++j)
+                        if (j0 + j < a.n_crit)
+                            raw[j] = __ldg(reinterpret_cast<const uint4*>(kbase + (int64_t)s.clist[j0 + j] * a.t_cap + p0));
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (p0 + i < hi) so[i] = acc[i];
+                    for (int j = 0; j < 8; ++j) {
+                        if (j0 + j >= a.n_crit) break;
+                        const int c = s.clist[j0 + j];
+                        score_channel(raw[j], s.qs[c], has_new, p_new - p0, s.knew[c], acc);
+                    }
+                }
+                score_finish(acc, p0, lo, hi, cand_lo, cand_hi, keys, s.u.hist, srow_out);
             }
         }
         __syncthreads();
@@ -371,11 +427,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         }
         if (k > 0) {
             // ---- digit 1 (key bits 31..20): from the score kernel's histogram, or this cluster's
-            if (a.hist != nullptr && !fused) {
+            if (!exchange) {
                 const uint4* gh = reinterpret_cast<const uint4*>(a.hist + row * H1);
-                for (int i = tid; i < H1 / 4; i += NT) reinterpret_cast<uint4*>(s.u.hist)[i] = __ldcg(gh + i);
+                for (int i = tid; i < H1 / 4; i += NT) reinterpret_cast<uint4*>(s.v.gh)[i] = __ldcg(gh + i);
                 __syncthreads();
-                find_bin_from_top(s.u.hist, H1, (uint32_t)k, s);
             } else {
                 if (!fused) {
                     for (int i = tid; i < H1; i += NT) s.u.hist[i] = 0u;
@@ -383,36 +438,17 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                     for (int p = max(lo, cand_lo) + tid; p < min(hi, cand_hi); p += NT)
                         atomicAdd(&s.u.hist[keys[p - lo] >> 20], 1u);
                 }
-                // every CTA sums one eighth of the bins over the cluster, then the slice holding
-                // the k-th largest key is found from the eight slice totals
-                constexpr int SL = H1 / CL;
-                static_assert(SL == NT, "one bin of the slice per thread");
-                cluster.sync();
-                uint32_t v = 0;
-                for (int r = 0; r < CL; ++r) v += cluster.map_shared_rank(s.u.hist, r)[SL * rank + tid];
-                s.slice[tid] = v;
-                uint32_t tot;
-                excl_scan<NT>(v, s.wsum, &tot);
-                if (tid == 0) s.slice_tot = tot;
-                cluster.sync();
-                uint32_t above = 0;
-                int rs = CL - 1;
-                for (; rs > 0; --rs) {
-                    const uint32_t t = cluster.map_shared_rank(&s, rs)->slice_tot;
-                    if (above + t >= (uint32_t)k) break;
-                    above += t;
+                __syncthreads();  // the local histogram is complete
+                cluster_wait();   // every CTA's copy is zeroed
+                // the non-zero bins go to every CTA's copy (a few hundred of the 4096)
+                for (int i = tid; i < H1; i += NT) {
+                    const uint32_t c = s.u.hist[i];
+                    if (c != 0u)
+                        for (int r = 0; r < CL; ++r) atomicAdd(cluster.map_shared_rank(&s.v.gh[i], (r + rank) & (CL - 1)), c);
                 }
-                // the bins of slice rs, highest first
-                uint32_t* sl = reinterpret_cast<uint32_t*>(s.v.w.h2);  // free until the later passes
-                sl[tid] = cluster.map_shared_rank(&s, rs)->slice[tid];
-                __syncthreads();
-                find_bin_from_top(sl, SL, (uint32_t)k - above, s);  // ends with a barrier
-                if (tid == 0) {
-                    s.s_bin += SL * rs;
-                    s.s_above += above;
-                }
-                __syncthreads();
+                cluster.sync();  // after it no CTA reads its local histogram again
             }
+            find_bin_from_top(s.v.gh, H1, (uint32_t)k, s);  // ends with a barrier
             const uint32_t b1 = s.s_bin;
             uint32_t remaining = (uint32_t)k - s.s_above;
             // ---- one pass, eight positions per lane: positions above digit 1 (and the sinks and
@@ -487,35 +523,31 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                 }
             }
             __syncthreads();
-            if (tid == 0) s.n_cand = 0;
-            cluster.sync();  // local lists complete; every CTA is done with its histogram
-            if (a.hist != nullptr && rank == 0)  // read by all: clear it for the next layer
-                for (int i = tid; i < H1; i += NT) a.hist[row * H1 + i] = 0u;
-            // ---- push the candidates to rank 0 (one reservation per CTA): the key's low 20 bits
-            // (digit 1 is common to all) and the owner rank
+            // ---- every CTA's candidates (key bits 19..0) go to its slots in every CTA; the
+            // target's local histogram is no longer read (see the cluster barrier above)
             {
-                uint32_t* r0c = cluster.map_shared_rank(s.u.cand, 0);
-                __shared__ int s_base;
                 const int nc = min(s.n_c, CAP_C);
-                if (tid == 0)
-                    s_base = atomicAdd(&cluster.map_shared_rank(&s, 0)->n_cand, s.n_c > CAP_C ? CAND_MAX + 1 : nc);
-                __syncthreads();
-                const int base = s_base;
-                for (int i = tid; i < nc; i += NT)
-                    if (base + i < CAND_MAX)
-                        r0c[base + i] = (((uint32_t)(s.v.w.cl[i] >> 32) & 0xfffffu) << 12) | (uint32_t)rank;
+                for (int r0 = 0; r0 < CL; ++r0) {
+                    SXSmem* d = cluster.map_shared_rank(&s, (r0 + rank) & (CL - 1));
+                    for (int i = tid; i < nc; i += NT)
+                        d->u.cand[rank * CAP_C + i] = (uint32_t)(s.v.w.cl[i] >> 32) & 0xfffffu;
+                    if (tid == 0) d->ncand[rank] = (uint32_t)s.n_c;
+                }
             }
             cluster.sync();
-            const int n_c = cluster.map_shared_rank(&s, 0)->n_cand;
-            if (n_c <= CAND_MAX) {
-                // ---- fast path: every CTA finishes the selection over rank 0's candidate list
-                const uint32_t* r0c = cluster.map_shared_rank(s.u.cand, 0);
-                constexpr int PER = CAND_MAX / NT;
-                uint32_t cr[PER];
+            if (a.hist != nullptr && rank == 0)  // read by all: clear it for the next layer
+                for (int i = tid; i < H1; i += NT) a.hist[row * H1 + i] = 0u;
+            bool ovf_c = false;
+            for (int r = 0; r < CL; ++r) ovf_c |= s.ncand[r] > (uint32_t)CAP_C;
+            if (!ovf_c) {
+                // ---- fast path: every CTA finishes the selection over all candidates; slot j
+                // of this thread holds rank j's candidate number tid
+                uint32_t cr[CL], vm = 0u;
 #pragma unroll
-                for (int j = 0; j < PER; ++j) {
-                    const int i = tid + j * NT;
-                    cr[j] = i < n_c ? r0c[i] : 0u;
+                for (int j = 0; j < CL; ++j) {
+                    const bool v = (uint32_t)tid < s.ncand[j];
+                    cr[j] = v ? s.u.cand[j * CAP_C + tid] : 0u;
+                    vm |= (uint32_t)v << j;
                 }
                 uint32_t d2 = 0u, d3 = 0u;
                 for (int pass = 0; pass < 2; ++pass) {
@@ -523,10 +555,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                     if (pass == 1 && tid < CL) s.eqr[tid] = 0u;
                     __syncthreads();
 #pragma unroll
-                    for (int j = 0; j < PER; ++j) {
-                        if (tid + j * NT >= n_c) continue;
-                        if (pass == 0) atomicAdd(&s.v.w.h2[cr[j] >> 22], 1u);
-                        else if ((cr[j] >> 22) == d2) atomicAdd(&s.v.w.h2[(cr[j] >> 12) & (H2 - 1)], 1u);
+                    for (int j = 0; j < CL; ++j) {
+                        if (!((vm >> j) & 1u)) continue;
+                        if (pass == 0) atomicAdd(&s.v.w.h2[cr[j] >> 10], 1u);
+                        else if ((cr[j] >> 10) == d2) atomicAdd(&s.v.w.h2[cr[j] & (H2 - 1)], 1u);
                     }
                     __syncthreads();
                     find_bin_from_top(s.v.w.h2, H2, remaining, s);
@@ -540,8 +572,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                 // Ranks own ascending position ranges, so this CTA keeps its own lowest
                 // remaining - (ties in lower ranks) of them, clamped to [0, its ties]
 #pragma unroll
-                for (int j = 0; j < PER; ++j)
-                    if (tid + j * NT < n_c && (cr[j] >> 12) == low) atomicAdd(&s.eqr[cr[j] & (CL - 1)], 1u);
+                for (int j = 0; j < CL; ++j)
+                    if (((vm >> j) & 1u) && cr[j] == low) atomicAdd(&s.eqr[j], 1u);
                 if (tid == 0) s.bc_cut = 0x7fffffff;
                 __syncthreads();
                 uint32_t eq_before = 0;
@@ -974,8 +1006,8 @@ extern "C" int kv_sparse_layer_decode(const kvq_layout* L, const kvq_pool* P, co
                 "%s: pool needs k16, v16, kT and k_absmax", fn);
     KVQ_REQUIRE((((uintptr_t)P->k16 | (uintptr_t)P->v16 | (uintptr_t)P->kT) & 15u) == 0, KVQ_ERR_INVALID_ARG,
                 "%s: k16, v16 and kT must be 16-byte aligned", fn);
-    KVQ_REQUIRE(P->t_cap % 8 == 0 && P->t_cap >= S->max_len, KVQ_ERR_INVALID_ARG,
-                "%s: t_cap must be a multiple of 8 and >= max_len", fn);
+    KVQ_REQUIRE(P->t_cap % 8 == 0 && P->t_cap >= S->max_len && P->t_cap <= (1 << 24), KVQ_ERR_INVALID_ARG,
+                "%s: t_cap must be a multiple of 8, >= max_len and <= 2^24", fn);
     KVQ_REQUIRE(n_crit >= 1 && n_crit <= D, KVQ_ERR_INVALID_ARG, "%s: n_crit %d not in [1, 128]", fn, n_crit);
     KVQ_REQUIRE(n_sink >= 0 && window >= 0, KVQ_ERR_INVALID_ARG, "%s: n_sink / window", fn);
     KVQ_REQUIRE(k_fixed >= 0 || (ratio >= 0.0 && ratio <= 1.0), KVQ_ERR_INVALID_ARG, "%s: ratio", fn);

@@ -98,7 +98,8 @@ typedef struct kvq_layout {
  * fp16 layer (bits == 16):
  *   k16, v16 [num_blocks][H_kv][16][d]  fp16 token rows
  *   kT       [max_seqs][H_kv][d][t_cap] fp16 channel-major copy of K, the
- *            "critical key" buffer read by kv_critical_score (t_cap % 8 == 0)
+ *            "critical key" buffer read by kv_critical_score (t_cap % 8 == 0;
+ *            kv_sparse_layer_decode also needs t_cap <= 2^24)
  *   k_absmax [max_seqs][H_kv][d]        fp32 running max_t |K[t][c]|
  */
 typedef struct kvq_pool {
