@@ -37,6 +37,8 @@ constexpr int H2 = 1024;              // second and third digits: bits 19..10, 9
 constexpr int NHW = NT / 16;          // half-warps (attention: one row per half-warp)
 constexpr int BATCH = 4;              // rows in flight per half-warp
 constexpr int REC = 4 + D;
+constexpr uint32_t ROW_NONE = 0xffffffffu;  // attention row ids: no row
+constexpr uint32_t ROW_NEW = 0xfffffffeu;   // the newest token, read from k_new / v_new
 
 struct SXArgs {
     const float* scores;
@@ -87,7 +89,8 @@ struct SXSmem {
     union {
         uint32_t gh[H1];                    // the cluster's first-digit histogram
         struct {
-            uint32_t h2[H2];                // second / third digit histogram
+            uint32_t h2[H2];                // second digit histogram
+            uint32_t h2b[H2];               // third digit histogram (fast path)
             unsigned long long cl[CAP_C];   // this CTA's first-digit candidates
             uint32_t wmask[NW][MAXIT];      // ballots of the ordered compaction
         } w;
@@ -98,6 +101,7 @@ struct SXSmem {
     uint32_t wtot[NW], wtot2[NW];
     uint32_t ncand[CL];                     // first-digit candidates of each rank (above CAP_C: overflow)
     int32_t n_s, n_c;                       // this CTA's kept positions / candidates
+    uint32_t nsc;                           // both, packed (low / high 16 bits) while classifying
     int32_t bc_cut;
     uint32_t s_bin, s_above;
     uint32_t eq_cnt, sel_cnt;               // this CTA's counts, read by the others
@@ -146,26 +150,50 @@ __device__ __forceinline__ uint32_t excl_scan(uint32_t v, uint32_t* wsum, uint32
     return x - v + (warp > 0 ? wsum[warp - 1] : 0u);
 }
 
-// Over `nbins` bins in tot[], finds the bin (from the top) that holds the
-// `remaining`-th largest element: s.s_bin, and s.s_above = count in higher bins.
-// Called by a whole CTA; every thread owns nbins/NT consecutive bins.
-__device__ __forceinline__ void find_bin_from_top(const uint32_t* tot, int nbins, uint32_t remaining, SXSmem& s) {
-    const int per = nbins / NT;
-    const int top = nbins - per * (int)threadIdx.x;  // thread 0 owns the highest bins
-    uint32_t mine = 0;
-    for (int j = 1; j <= per; ++j) mine += tot[top - j];
-    uint32_t total;
-    const uint32_t before = excl_scan<NT>(mine, s.wsum, &total);
-    if (before < remaining && before + mine >= remaining) {
-        uint32_t run = before;
-        for (int j = 1; j <= per; ++j) {
-            const uint32_t c = tot[top - j];
-            if (run + c >= remaining) {
-                s.s_bin = (uint32_t)(top - j);
-                s.s_above = run;
-                break;
+// Over the NT * PER bins in tot[], finds the bin (from the top) that holds the `remaining`-th
+// largest element: s.s_bin, and s.s_above = the count in higher bins.  Called by a whole CTA;
+// warp w owns 32 * PER consecutive bins (warp 0 the highest), lane l PER of them; two barriers.
+template <int PER>
+__device__ __forceinline__ void find_bin_from_top(const uint32_t* tot, uint32_t remaining, SXSmem& s) {
+    constexpr int NB = NT * PER;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int top = NB - 32 * PER * warp - PER * lane;  // this lane's bins: top - PER .. top - 1
+    uint32_t c[PER], mine = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        c[j] = tot[top - 1 - j];
+        mine += c[j];
+    }
+    uint32_t x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s.wsum[warp] = x;
+    __syncthreads();
+    uint32_t before = 0;
+    int ws = -1;
+    for (int w = 0; w < NW; ++w) {
+        const uint32_t t = s.wsum[w];
+        if (before + t >= remaining) {
+            ws = w;
+            break;
+        }
+        before += t;
+    }
+    if (warp == ws) {
+        uint32_t run = before + x - mine;  // the count above this lane's bins
+        if (run < remaining && run + mine >= remaining) {
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                if (run + c[j] >= remaining) {
+                    s.s_bin = (uint32_t)(top - 1 - j);
+                    s.s_above = run;
+                    break;
+                }
+                run += c[j];
             }
-            run += c;
         }
     }
     __syncthreads();
@@ -179,6 +207,13 @@ __device__ __forceinline__ void unpack8(const uint4& r, float* f) {
         f[2 * i] = v.x;
         f[2 * i + 1] = v.y;
     }
+}
+
+// Starts pulling the 256-byte row at p (256-byte aligned) into L2; no completion to wait for.
+__device__ __forceinline__ void prefetch_row_l2(const void* p) {
+    const char* c = static_cast<const char*>(p);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(c) : "memory");
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(c + 128) : "memory");
 }
 
 // acc[i] += q_c * K[p0 + i][c] for the 8 positions in `raw` (fp16); position p0 + inew is
@@ -250,6 +285,16 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t row = (int64_t)b * a.n_heads + h;
     kvq_pdl_begin();
+    const bool fused = a.kT != nullptr;
+    // the fused path's per-channel inputs are requested together with the length
+    uint16_t pre_q = 0, pre_kn = 0;
+    float pre_am = 0.0f;
+    if (fused && tid < D) {
+        const int64_t kvrow = (int64_t)b * a.H + h / a.GQ;
+        pre_q = a.q[row * D + tid];
+        pre_am = a.absmax[kvrow * D + tid];
+        pre_kn = a.k_new[kvrow * D + tid];
+    }
     int T = a.seq_lens[b];
     if (T < 0 || T > a.max_len) {
         if (tid == 0 && rank == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
@@ -269,7 +314,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         s.n_s = 0;
         s.n_c = 0;
     }
-    const bool fused = a.kT != nullptr;
     // the first-digit histograms of the cluster's CTAs are summed into every CTA's copy
     const bool exchange = !keep_all && k > 0 && (fused || a.hist == nullptr);
     if (exchange) {
@@ -287,10 +331,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         const int64_t kvrow = (int64_t)b * a.H + g;
         const int p_new = T - 1;
         if (tid < D) {
-            const float qv = kvq_h2f(a.q[row * D + tid]);
-            float am = a.absmax[kvrow * D + tid];
+            const float qv = kvq_h2f(pre_q);
+            float am = pre_am;
             if (p_new >= 0) {
-                const uint16_t kn = a.k_new[kvrow * D + tid];
+                const uint16_t kn = pre_kn;
                 s.knew[tid] = kn;
                 am = fmaxf(am, fabsf(kvq_h2f(kn)));
                 if (rank == 0 && h % a.GQ == 0) {
@@ -448,16 +492,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                 }
                 cluster.sync();  // after it no CTA reads its local histogram again
             }
-            find_bin_from_top(s.v.gh, H1, (uint32_t)k, s);  // ends with a barrier
+            find_bin_from_top<H1 / NT>(s.v.gh, (uint32_t)k, s);  // ends with a barrier
             const uint32_t b1 = s.s_bin;
             uint32_t remaining = (uint32_t)k - s.s_above;
             // ---- one pass, eight positions per lane: positions above digit 1 (and the sinks and
             // window) are kept, ties on digit 1 are candidates; a warp reserves its slots in both
             // lists with one atomic each and places its lanes by a packed exclusive scan
-            if (tid == 0) {
-                s.n_s = 0;
-                s.n_c = 0;
-            }
+            if (tid == 0) s.nsc = 0u;
             __syncthreads();
             const bool inner = lo >= cand_lo && hi <= cand_hi;  // no sink or window position here
             for (int base = 0; base < n; base += 8 * NT) {      // bound uniform over the CTA
@@ -496,13 +537,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                     if (lane >= o) x += y;
                 }
                 const uint32_t tot = __shfl_sync(0xffffffffu, x, 31);
-                uint32_t bases = 0u;
-                if (lane == 0) {
-                    uint32_t bs = 0u, bc = 0u;
-                    if (tot & 0xffffu) bs = atomicAdd(reinterpret_cast<unsigned*>(&s.n_s), tot & 0xffffu);
-                    if (tot >> 16) bc = atomicAdd(reinterpret_cast<unsigned*>(&s.n_c), tot >> 16);
-                    bases = bs | (bc << 16);  // both below the chunk size < 65536
-                }
+                uint32_t bases = 0u;  // both counts stay below the chunk size < 65536: no carry
+                if (lane == 0 && tot != 0u) bases = atomicAdd(&s.nsc, tot);
                 bases = __shfl_sync(0xffffffffu, bases, 0) + x - cnt;
                 uint32_t bs = bases & 0xffffu, bc = bases >> 16;
                 const uint32_t p0 = (uint32_t)(lo + q0);
@@ -523,15 +559,49 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                 }
             }
             __syncthreads();
+            const int n_s0 = (int)(s.nsc & 0xffffu), n_c0 = (int)(s.nsc >> 16);
+            // the rows of the positions kept so far (all but the candidates that will be kept)
+            // are pulled into L2 while the candidates are resolved; their pages are looked up first
+            const bool pf = a.q != nullptr;
+            const int n_pf = pf ? min(n_s0, CAP_S) : 0;
+            static_assert(CAP_S == 2 * NT, "two prefetched rows per thread");
+            uint32_t pf_t[2];
+            int32_t pf_pg[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = tid + j * NT;
+                pf_t[j] = i < n_pf ? s.list[i] : 0u;
+                pf_pg[j] = i < n_pf ? a.bt[(int64_t)b * a.max_blocks + (pf_t[j] >> 4)] : -1;
+            }
             // ---- every CTA's candidates (key bits 19..0) go to its slots in every CTA; the
             // target's local histogram is no longer read (see the cluster barrier above)
             {
-                const int nc = min(s.n_c, CAP_C);
+                const int nc = min(n_c0, CAP_C);
                 for (int r0 = 0; r0 < CL; ++r0) {
                     SXSmem* d = cluster.map_shared_rank(&s, (r0 + rank) & (CL - 1));
                     for (int i = tid; i < nc; i += NT)
                         d->u.cand[rank * CAP_C + i] = (uint32_t)(s.v.w.cl[i] >> 32) & 0xfffffu;
-                    if (tid == 0) d->ncand[rank] = (uint32_t)s.n_c;
+                    if (tid == 0) d->ncand[rank] = (uint32_t)n_c0;
+                }
+            }
+            // the fast path's digit histograms and tie counts start from zero
+            for (int i = tid; i < H2; i += NT) {
+                s.v.w.h2[i] = 0u;
+                s.v.w.h2b[i] = 0u;
+            }
+            if (tid < CL) s.eqr[tid] = 0u;
+            if (tid == 0) {
+                s.n_s = n_s0;
+                s.n_c = n_c0;
+            }
+            {
+                const int g = h / a.GQ;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (pf_pg[j] < 0 || pf_pg[j] >= a.num_blocks) continue;
+                    const int64_t off = (((int64_t)pf_pg[j] * a.H + g) * PG + (pf_t[j] & 15)) * D;
+                    prefetch_row_l2(a.k16 + off);
+                    prefetch_row_l2(a.v16 + off);
                 }
             }
             cluster.sync();
@@ -549,23 +619,20 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                     cr[j] = v ? s.u.cand[j * CAP_C + tid] : 0u;
                     vm |= (uint32_t)v << j;
                 }
-                uint32_t d2 = 0u, d3 = 0u;
-                for (int pass = 0; pass < 2; ++pass) {
-                    for (int i = tid; i < H2; i += NT) s.v.w.h2[i] = 0u;
-                    if (pass == 1 && tid < CL) s.eqr[tid] = 0u;
-                    __syncthreads();
 #pragma unroll
-                    for (int j = 0; j < CL; ++j) {
-                        if (!((vm >> j) & 1u)) continue;
-                        if (pass == 0) atomicAdd(&s.v.w.h2[cr[j] >> 10], 1u);
-                        else if ((cr[j] >> 10) == d2) atomicAdd(&s.v.w.h2[cr[j] & (H2 - 1)], 1u);
-                    }
-                    __syncthreads();
-                    find_bin_from_top(s.v.w.h2, H2, remaining, s);
-                    remaining -= s.s_above;
-                    if (pass == 0) d2 = s.s_bin;
-                    else d3 = s.s_bin;
-                }
+                for (int j = 0; j < CL; ++j)
+                    if ((vm >> j) & 1u) atomicAdd(&s.v.w.h2[cr[j] >> 10], 1u);
+                __syncthreads();
+                find_bin_from_top<H2 / NT>(s.v.w.h2, remaining, s);
+                remaining -= s.s_above;
+                const uint32_t d2 = s.s_bin;
+#pragma unroll
+                for (int j = 0; j < CL; ++j)
+                    if (((vm >> j) & 1u) && (cr[j] >> 10) == d2) atomicAdd(&s.v.w.h2b[cr[j] & (H2 - 1)], 1u);
+                __syncthreads();
+                find_bin_from_top<H2 / NT>(s.v.w.h2b, remaining, s);
+                remaining -= s.s_above;
+                const uint32_t d3 = s.s_bin;
                 const uint32_t low = (d2 << 10) | d3;
                 kth = (b1 << 20) | low;
                 // ties at the k-th key: the `remaining` (>= 1) lowest positions among them are kept.
@@ -640,7 +707,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
 #pragma unroll
                     for (int j = 0; j < H2 / NT; ++j) s.v.w.h2[tid + j * NT] = sums[j];
                     __syncthreads();
-                    find_bin_from_top(s.v.w.h2, H2, remaining, s);
+                    find_bin_from_top<H2 / NT>(s.v.w.h2, remaining, s);
                     remaining -= s.s_above;
                     prefix = (prefix << 10) | s.s_bin;
                 }
@@ -764,13 +831,21 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
 
     // ---- attention over this CTA's kept rows
     const int g = h / a.GQ;
+    // the newest token (appended by this launch, possibly by another cluster) is read from its source
+    const int t_new = a.k_new != nullptr ? T - 1 : -1;
+    const uint16_t* knew_row = a.k_new != nullptr ? a.k_new + ((int64_t)b * a.H + g) * D : nullptr;
+    const uint16_t* vnew_row = a.k_new != nullptr ? a.v_new + ((int64_t)b * a.H + g) * D : nullptr;
     uint32_t* rows = const_cast<uint32_t*>(plist);  // positions -> row offsets (in 128-element rows)
     for (int i = tid; i < (int)nl; i += NT) {
         const int t = (int)plist[i];
-        const int32_t page = a.bt[(int64_t)b * a.max_blocks + (t >> 4)];
-        uint32_t r = 0xffffffffu;
-        if (page >= 0 && page < a.num_blocks) r = (uint32_t)(((int64_t)page * a.H + g) * PG + (t & 15));
-        else kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, t);
+        uint32_t r = ROW_NONE;
+        if (t == t_new) {
+            r = ROW_NEW;
+        } else {
+            const int32_t page = a.bt[(int64_t)b * a.max_blocks + (t >> 4)];
+            if (page >= 0 && page < a.num_blocks) r = (uint32_t)(((int64_t)page * a.H + g) * PG + (t & 15));
+            else kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, t);
+        }
         rows[i] = r;
     }
     __syncthreads();
@@ -791,14 +866,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
 #pragma unroll
         for (int j = 0; j < BATCH; ++j) {
             const int i = it + j * NHW + hw;
-            const uint32_t r = i < (int)nl ? rows[i] : 0xffffffffu;
-            ok[j] = r != 0xffffffffu;
+            const uint32_t r = i < (int)nl ? rows[i] : ROW_NONE;
+            ok[j] = r != ROW_NONE;
             kr[j] = make_uint4(0u, 0u, 0u, 0u);
             vr[j] = make_uint4(0u, 0u, 0u, 0u);
             if (ok[j]) {
-                const int64_t off = (int64_t)r * D + 8 * l16;
-                kr[j] = __ldg(reinterpret_cast<const uint4*>(a.k16 + off));
-                vr[j] = __ldg(reinterpret_cast<const uint4*>(a.v16 + off));
+                const uint16_t* kp = r == ROW_NEW ? knew_row : a.k16 + (int64_t)r * D;
+                const uint16_t* vp = r == ROW_NEW ? vnew_row : a.v16 + (int64_t)r * D;
+                kr[j] = __ldg(reinterpret_cast<const uint4*>(kp + 8 * l16));
+                vr[j] = __ldg(reinterpret_cast<const uint4*>(vp + 8 * l16));
             }
         }
         float sc[BATCH];
@@ -1017,8 +1093,9 @@ extern "C" int kv_sparse_layer_decode(const kvq_layout* L, const kvq_pool* P, co
     KVQ_REQUIRE(sel == nullptr || (sel_cap > 0 && sel_count != nullptr), KVQ_ERR_INVALID_ARG, "%s: sel", fn);
     KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "%s: batch exceeds max_seqs", fn);
     if (S->batch == 0) return KVQ_OK;
-    KVQ_REQUIRE(k_new && v_new && q && out && S->block_table && ((uintptr_t)q & 15u) == 0, KVQ_ERR_INVALID_ARG,
-                "%s: NULL k_new / v_new / q / out / block table, or q not 16-byte aligned", fn);
+    KVQ_REQUIRE(k_new && v_new && q && out && S->block_table &&
+                    (((uintptr_t)q | (uintptr_t)k_new | (uintptr_t)v_new) & 15u) == 0,
+                KVQ_ERR_INVALID_ARG, "%s: NULL k_new / v_new / q / out / block table, or q / k_new / v_new not 16-byte aligned", fn);
     SXArgs a{};
     a.scores = nullptr;
     a.score_stride = scores ? score_stride : 0;

@@ -316,7 +316,9 @@ size_t kv_select_sparse_attn_ws(void);
  * Meeting §3.2].  The scores never leave the GPU's shared memory unless
  * `scores` (optional, device fp32 [batch][H_q][score_stride]) asks for a
  * copy; `sel`/`sel_count` (optional) receive the selection as
- * kv_topk_select writes it.  T <= 360448.  ws: kv_sparse_layer_decode_ws().
+ * kv_topk_select writes it.  T <= 360448.  q, k_new and v_new 16-byte
+ * aligned; the newest token's row is attended from k_new/v_new, so no CTA
+ * depends on another cluster's append.  ws: kv_sparse_layer_decode_ws().
  * ---------------------------------------------------------------------- */
 int kv_sparse_layer_decode(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
                            const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q, int32_t n_crit,
