@@ -3,11 +3,21 @@
 // context split across CTAs and the partial softmax states merged by
 // log-sum-exp in the last CTA of every (sequence, kv head).
 //
-// One CTA = one (sequence b, kv head g, split): it walks 64-token chunks (one
-// K quantization group = four 16-token pages), stages the packed codes and
-// scales in shared memory and serves all GQ query heads of the group from
-// the same staged codes.  A chunk that holds the unfinished K group reads
-// its keys from the fp16 tail buffer.
+// Both contractions run on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
+// accumulate), one warp per 64-token group (one K quantization group = four
+// 16-token pages).  With K = scale_c * code + zero_c per channel of the group,
+//   s_t = sum_c (q_c scale_c) code_t[c] + sum_c q_c zero_c,
+// the first term is a [slots x 128] x [128 x tokens] product whose A operand
+// holds q_c scale_c (exact in fp32) split into two fp16 halves (hi and lo
+// slots, summed afterwards), and whose B operand is the codes themselves,
+// turned into fp16 two at a time by one AND/OR and one exact fp16 FMA (the
+// codes are stored in pairs for that; see kvq_k_code_pos).  With V = vscale_t
+// code + vzero_t per token and V group,
+//   o[d] = sum_t (p_t vscale_t) code_t[d] + sum_t p_t vzero_t,
+// the first term is a [128 x tokens] x [tokens x heads] product: V codes
+// (stored channel-major per page, kvq_v_code_pos) against p_t vscale_t in
+// fp16.  The group's codes and scales are staged per warp with cp.async, one
+// group ahead.  An unfinished K group reads its keys from the fp16 tail buffer.
 #include <algorithm>
 #include <map>
 #include <mutex>
@@ -20,6 +30,7 @@ constexpr int D = KVQ_HEAD_DIM;
 constexpr int PG = KVQ_BLOCK_TOKENS;
 constexpr int KG = KVQ_K_GROUP_TOKENS;
 constexpr int NT = 128;
+constexpr int NWARP = NT / 32;
 constexpr int REC = 4 + D;  // partial record: m, l, pad, pad, o[128]
 
 struct QAttnArgs {
@@ -33,501 +44,397 @@ struct QAttnArgs {
     const int32_t* seq_lens;
     int32_t max_blocks;
     int32_t max_len;
-    int32_t H;     // kv heads
-    int32_t G;     // V group dims
+    int32_t H;       // kv heads of the cache
+    int32_t kv_div;  // grid kv groups per kv head (2 when 8 q heads share one: two halves of 4)
+    int32_t G;       // V group dims
     const uint16_t* q;
     float* out;
     float* part;
     int32_t* counters;
     KvqWsHeader* hdr;
     int32_t n_splits;
-    int32_t cps;   // chunks per split
+    int32_t cps;     // 64-token groups per split
 };
 
-__device__ __forceinline__ float2 unpack_sz(uint32_t w) {
-    return make_float2(kvq_h2f((uint16_t)(w & 0xffffu)), kvq_h2f((uint16_t)(w >> 16)));
+// ---------------------------------------------------------------- small helpers
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int BITS, int GQ>
-__global__ void __launch_bounds__(NT) qattn_kernel(QAttnArgs a) {
-    constexpr int WPR = 4 * BITS;            // 32-bit words per token row
-    constexpr int U4_PAGE = PG * WPR / 4;    // uint4 per page of codes
-    __shared__ __align__(16) uint32_t kc[KG * WPR];
-    __shared__ __align__(16) uint32_t vc[KG * WPR];
-    __shared__ float2 vsz[KG * 4];           // (scale, zero) per token and V group
-    __shared__ float2 ksz[D];                // (scale, zero) per channel of the K group
-    __shared__ __align__(16) float qf[D * GQ];   // q[c][h]
-    __shared__ __align__(16) float ps[KG * GQ];  // p[t][h]
-    __shared__ float red[NT / 32][GQ];
-    __shared__ float m_run[GQ], l_run[GQ], alpha_s[GQ];
-    __shared__ int32_t pages[4];
-    __shared__ int is_last;
-
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int T = a.seq_lens[b];
-    const int n_full = T / KG;
-    const int n_chunks = (T + KG - 1) / KG;
-    const int nsplit_b = (n_chunks + a.cps - 1) / a.cps;
-    const int Hq = a.H * GQ;
-    if (T > a.max_len || T < 0) {
-        if (tid == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
-        return;
-    }
-    if (n_chunks == 0) {  // empty sequence: output 0
-        if (split == 0)
-            for (int i = tid; i < GQ * D; i += NT) a.out[((int64_t)b * Hq + g * GQ) * D + i] = 0.0f;
-        return;
-    }
-    if (split >= nsplit_b) return;
-    const int c_begin = split * a.cps;
-    const int c_end = min(n_chunks, c_begin + a.cps);
-    const int NGV = D / a.G;
-
-    // q of the group's heads as fp32, layout [c][h]
-    for (int i = tid; i < GQ * D; i += NT) {
-        const int h = i / D, c = i % D;
-        qf[c * GQ + h] = kvq_h2f(a.q[((int64_t)b * Hq + g * GQ + h) * D + c]);
-    }
-    if (tid < GQ) {
-        m_run[tid] = -INFINITY;
-        l_run[tid] = 0.0f;
-    }
-    float o[GQ];
-#pragma unroll
-    for (int h = 0; h < GQ; ++h) o[h] = 0.0f;
-
-    const int t_loc = tid >> 1;   // token of this thread in the QK phase
-    const int half = tid & 1;     // channel half of this thread in the QK phase
-
-    for (int ch = c_begin; ch < c_end; ++ch) {
-        const int t0 = ch * KG;
-        const int n_tok = min(KG, T - t0);
-        const bool packed = ch < n_full;
-        const int n_pages = (n_tok + PG - 1) / PG;
-        __syncthreads();  // previous chunk fully consumed
-        if (tid < 4) {
-            int32_t p = 0;
-            if (tid < n_pages) {
-                p = a.bt[(int64_t)b * a.max_blocks + ch * 4 + tid];
-                if (p < 0 || p >= a.num_blocks) {
-                    kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
-                    p = 0;
-                }
-            }
-            pages[tid] = p;
-        }
-        __syncthreads();
-        // stage codes and scales of the chunk
-        for (int u = tid; u < n_pages * U4_PAGE; u += NT) {
-            const int j = u / U4_PAGE, r = u % U4_PAGE;
-            const int64_t base = ((int64_t)pages[j] * a.H + g) * PG * WPR;  // in words
-            reinterpret_cast<uint4*>(vc)[u] = reinterpret_cast<const uint4*>(a.v_codes)[base / 4 + r];
-            if (packed) reinterpret_cast<uint4*>(kc)[u] = reinterpret_cast<const uint4*>(a.k_codes)[base / 4 + r];
-        }
-        for (int u = tid; u < n_tok * NGV; u += NT) {
-            const int t = u / NGV, j = u % NGV;
-            const int64_t slot = ((int64_t)pages[t / PG] * a.H + g) * PG + (t % PG);
-            vsz[t * NGV + j] = unpack_sz(a.v_sz[slot * NGV + j]);
-        }
-        if (packed) ksz[tid] = unpack_sz(a.k_sz[((int64_t)pages[0] * a.H + g) * D + tid]);
-        __syncthreads();
-
-        // ---- scores: thread (t_loc, half) covers channels [64 half, 64 half + 64)
-        float acc[GQ];
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) acc[h] = 0.0f;
-        const bool valid = t_loc < n_tok;
-        if (valid) {
-            if (packed) {
-                const uint32_t* row = kc + t_loc * WPR;
-#pragma unroll 8
-                for (int c = 64 * half; c < 64 * half + 64; ++c) {
-                    const float2 sz = ksz[c];
-                    const float kh = fmaf(sz.x, (float)kvq_get_code<BITS>(row, c), sz.y);
-#pragma unroll
-                    for (int h = 0; h < GQ; ++h) acc[h] = fmaf(qf[c * GQ + h], kh, acc[h]);
-                }
-            } else {
-                const uint16_t* krow = a.k_tail + (((int64_t)b * a.H + g) * KG + t_loc) * D;
-#pragma unroll 8
-                for (int c = 64 * half; c < 64 * half + 64; ++c) {
-                    const float kh = kvq_h2f(krow[c]);
-#pragma unroll
-                    for (int h = 0; h < GQ; ++h) acc[h] = fmaf(qf[c * GQ + h], kh, acc[h]);
-                }
-            }
-        }
-        float s[GQ];
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) {
-            acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 1);
-            s[h] = valid ? acc[h] * KVQ_SCORE_LOG2_SCALE : -INFINITY;
-            const float wm = kvq_warp_max(s[h]);
-            if (lane == 0) red[warp][h] = wm;
-        }
-        __syncthreads();
-        if (tid < GQ) {
-            float cm = red[0][tid];
-            for (int w = 1; w < NT / 32; ++w) cm = fmaxf(cm, red[w][tid]);
-            const float m_new = fmaxf(m_run[tid], cm);
-            alpha_s[tid] = exp2f(m_run[tid] - m_new);
-            m_run[tid] = m_new;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) {
-            const float p = valid ? exp2f(s[h] - m_run[h]) : 0.0f;
-            if (half == 0 && t_loc < KG) ps[t_loc * GQ + h] = p;
-            float ws = kvq_warp_sum(half == 0 ? p : 0.0f);
-            if (lane == 0) red[warp][h] = ws;
-        }
-        __syncthreads();
-        if (tid < GQ) {
-            float lsum = 0.0f;
-            for (int w = 0; w < NT / 32; ++w) lsum += red[w][tid];
-            l_run[tid] = l_run[tid] * alpha_s[tid] + lsum;
-        }
-        // ---- p.v: thread = channel d
-        {
-            const int d = tid;
-            const int jg = d / a.G;
-#pragma unroll
-            for (int h = 0; h < GQ; ++h) o[h] *= alpha_s[h];
-#pragma unroll 4
-            for (int t = 0; t < n_tok; ++t) {
-                const float2 sz = vsz[t * NGV + jg];
-                const float vh = fmaf(sz.x, (float)kvq_get_code<BITS>(vc + t * WPR, d), sz.y);
-#pragma unroll
-                for (int h = 0; h < GQ; ++h) o[h] = fmaf(ps[t * GQ + h], vh, o[h]);
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---- partial state of this split
-    const int64_t rec0 = (((int64_t)b * a.H + g) * a.n_splits + split) * GQ;
-#pragma unroll
-    for (int h = 0; h < GQ; ++h) {
-        float* r = a.part + (rec0 + h) * REC;
-        if (tid == 0) {
-            r[0] = m_run[h];
-            r[1] = l_run[h];
-        }
-        r[4 + tid] = o[h];
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int prev = atomicAdd(&a.counters[b * a.H + g], 1);
-        is_last = (prev == nsplit_b - 1);
-    }
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    // ---- last CTA of (b, g): merge the splits by log-sum-exp
-    for (int h = 0; h < GQ; ++h) {
-        float M = -INFINITY;
-        for (int sp = 0; sp < nsplit_b; ++sp) {
-            const float* r = a.part + ((((int64_t)b * a.H + g) * a.n_splits + sp) * GQ + h) * REC;
-            M = fmaxf(M, __ldcg(r));
-        }
-        float Lsum = 0.0f, acc = 0.0f;
-        for (int sp = 0; sp < nsplit_b; ++sp) {
-            const float* r = a.part + ((((int64_t)b * a.H + g) * a.n_splits + sp) * GQ + h) * REC;
-            const float w = exp2f(__ldcg(r) - M);
-            Lsum = fmaf(__ldcg(r + 1), w, Lsum);
-            acc = fmaf(__ldcg(r + 4 + tid), w, acc);
-        }
-        a.out[((int64_t)b * Hq + g * GQ + h) * D + tid] = acc / Lsum;
-    }
-    if (tid == 0) a.counters[b * a.H + g] = 0;
+// d += A (16x16, row) * B (16x8, col), fp16 operands, fp32 accumulators
+__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// ---------------------------------------------------------------- register-centric kernel
-//
-// Every warp owns 32-token slices of the CTA's range and keeps its own online
-// softmax state.  Scores: one token per lane; the query scaled by the slice's K
-// group scale, q'[c][h] = q[h][c] * scale_c, sits in shared memory and reaches
-// the 32 lanes of a channel in one broadcast load, so
-//   s_t = sum_c q[h][c] zero_c + sum_c q'[c][h] code_t[c].
-// Values: a lane owns four channels; p'[t][h] = p_t,h * vscale_t is broadcast per
-// token and the zero term sum_t p_t,h vzero_t is accumulated per lane and
-// reduced once at the end.
-
-constexpr int NWARP = NT / 32;
-
-template <int BITS, int GQ>
-struct Q2Smem {
-    float qs[GQ][D];                        // query of the group's heads (fp32)
-    float qp[NWARP][D][GQ];                 // per warp: query scaled by the slice's K scales
-    uint32_t vrow[NWARP][32][4 * BITS];     // per warp: V codes of its 32 tokens
-    float pp[NWARP][32][4][GQ];             // per warp: p * V scale, per token, V group, head
-    float m[NWARP][GQ], l[NWARP][GQ];
-};
-
-__device__ __forceinline__ uint32_t bfe_u32(uint32_t w, uint32_t pos, uint32_t len) {
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     uint32_t r;
-    asm("bfe.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(w), "r"(pos), "r"(len));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ float2 unpack_h2(uint32_t x) {
+    return make_float2(kvq_h2f((uint16_t)(x & 0xffffu)), kvq_h2f((uint16_t)(x >> 16)));
+}
+
+// The code pair at bit offset POS (< 16) of both halves of w as two fp16 numbers.  The bits are
+// moved to offset E < 10 - BITS + 1 of the fp16 mantissa of 1024, giving 1024 + 2^E code
+// exactly; one fp16 FMA with 2^-E and -2^(10-E) then gives the code exactly.
+template <int BITS, int POS>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w) {
+    constexpr int X = BITS <= 2 ? 10 : 8;
+    constexpr int SH = POS - POS % X;
+    constexpr int E = POS - SH;
+    static_assert(E + BITS <= 10, "the code fits the fp16 mantissa");
+    constexpr uint32_t M = (1u << BITS) - 1u;
+    constexpr uint32_t MASK = (M << E) | (M << (16 + E));
+    const uint32_t x = ((w >> SH) & MASK) | 0x64006400u;
+    constexpr uint32_t SC = (uint32_t)(0x3C00 - (E << 10));                 // 2^-E
+    constexpr uint32_t OF = (uint32_t)(0x8000 | ((25 - E) << 10));          // -2^(10-E)
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(SC | (SC << 16)), "r"(OF | (OF << 16)));
     return r;
 }
 
-// small unsigned integer -> float, exactly (2^23 + code, minus 2^23)
-__device__ __forceinline__ float code_f(uint32_t code) { return __uint_as_float(code | 0x4B000000u) - 8388608.0f; }
-
-// (d0, d1) += (a0, a1) * b as one packed fp32 FMA (two IEEE fma operations)
-__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b) {
-    asm("{.reg .b64 rd, ra, rb;\n\t"
-        "mov.b64 rd, {%0, %1};\n\t"
-        "mov.b64 ra, {%2, %3};\n\t"
-        "mov.b64 rb, {%4, %4};\n\t"
-        "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
-        "mov.b64 {%0, %1}, rd;\n\t}"
-        : "+f"(d0), "+f"(d1)
-        : "f"(a0), "f"(a1), "f"(b));
+// K B-fragment register for pair m of this lane's column (see kvq_k_code_pos): kw = the
+// BITS words of the column in the token row.
+template <int BITS, int M>
+__device__ __forceinline__ uint32_t k_pair(const uint32_t* kw) {
+    constexpr int PER = 16 / BITS;
+    return code_pair<BITS, (M % PER) * BITS>(kw[M / PER]);
 }
 
-template <int GQ>
-__device__ __forceinline__ void fma_heads(float* acc, const float* qv, float x) {
-    if constexpr (GQ == 1) {
-        acc[0] = fmaf(qv[0], x, acc[0]);
+// The four V A-fragment registers of column r (pairs m = 4r .. 4r + 3, kvq_v_code_pos) from
+// the BITS words of row 8t + x of the page block.
+template <int BITS>
+__device__ __forceinline__ void v_pairs(const uint32_t* vw, int r, uint32_t* A) {
+    if constexpr (BITS == 1) {
+        const uint32_t x = vw[0] >> (4 * r);
+        A[0] = code_pair<1, 0>(x);
+        A[1] = code_pair<1, 1>(x);
+        A[2] = code_pair<1, 2>(x);
+        A[3] = code_pair<1, 3>(x);
+    } else if constexpr (BITS == 2) {
+        const uint32_t x = vw[r >> 1] >> (8 * (r & 1));
+        A[0] = code_pair<2, 0>(x);
+        A[1] = code_pair<2, 2>(x);
+        A[2] = code_pair<2, 4>(x);
+        A[3] = code_pair<2, 6>(x);
+    } else if constexpr (BITS == 4) {
+        const uint32_t x = vw[r];
+        A[0] = code_pair<4, 0>(x);
+        A[1] = code_pair<4, 4>(x);
+        A[2] = code_pair<4, 8>(x);
+        A[3] = code_pair<4, 12>(x);
     } else {
-#pragma unroll
-        for (int h = 0; h < GQ; h += 2) fma2(acc[h], acc[h + 1], qv[h], qv[h + 1], x);
+        const uint32_t x0 = vw[2 * r], x1 = vw[2 * r + 1];
+        A[0] = code_pair<8, 0>(x0);
+        A[1] = code_pair<8, 8>(x0);
+        A[2] = code_pair<8, 0>(x1);
+        A[3] = code_pair<8, 8>(x1);
     }
 }
 
-template <int GQ>
-__device__ __forceinline__ void lds_heads(float* dst, const float* src) {
-    if constexpr (GQ % 4 == 0) {
-#pragma unroll
-        for (int h = 0; h < GQ; h += 4) {
-            const float4 v = *reinterpret_cast<const float4*>(src + h);
-            dst[h] = v.x;
-            dst[h + 1] = v.y;
-            dst[h + 2] = v.z;
-            dst[h + 3] = v.w;
-        }
-    } else if constexpr (GQ == 2) {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        dst[0] = v.x;
-        dst[1] = v.y;
-    } else {
-        dst[0] = src[0];
-    }
-}
+// ---------------------------------------------------------------- the kernel
+
+// One warp's staged 64-token group.
+template <int BITS>
+struct GroupStage {
+    uint32_t k[KG * 4 * BITS];   // K token rows (complete groups only)
+    uint32_t v[4 * 64 * BITS];   // V page blocks
+    uint32_t ksz[D];             // K (scale, zero) per channel
+    uint32_t vsz[KG * 4];        // V (scale, zero) per token and V group (at most 4 groups)
+};
 
 template <int BITS, int GQ>
-__global__ void __launch_bounds__(NT) qattn2_kernel(QAttnArgs a) {
-    constexpr int WPR = 4 * BITS;
-    extern __shared__ __align__(16) unsigned char smraw[];
-    Q2Smem<BITS, GQ>& S = *reinterpret_cast<Q2Smem<BITS, GQ>*>(smraw);
-    __shared__ int is_last;
+struct QMSmem {
+    float qs[GQ][D];                  // the query heads of the kv group (fp32)
+    float m[NWARP][GQ], l[NWARP][GQ];
+    uint32_t afr[NWARP][16][32];      // per warp: the scores' A fragments, [register][lane]
+    union {
+        GroupStage<BITS> st[NWARP][2];
+        float ro[NWARP][GQ][D];       // per warp: unnormalised outputs, after the last group
+    } u;
+};
 
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    kvq_pdl_begin();
-    const int T = a.seq_lens[b];
-    const int n_full = T / KG;
-    const int n_chunks = (T + KG - 1) / KG;
-    const int nsplit_b = (n_chunks + a.cps - 1) / a.cps;
-    const int Hq = a.H * GQ;
-    if (T > a.max_len || T < 0) {
-        if (tid == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
-        return;
-    }
-    if (n_chunks == 0) {  // empty sequence: output 0
-        if (split == 0)
-            for (int i = tid; i < GQ * D; i += NT) a.out[((int64_t)b * Hq + g * GQ) * D + i] = 0.0f;
-        return;
-    }
-    if (split >= nsplit_b) return;
-    const int t_begin = split * a.cps * KG;
-    const int t_end = min(T, t_begin + a.cps * KG);
-    const int NGV = D / a.G;
-    const int jd = (4 * lane) / a.G;  // V group of this lane's four channels
-    const int64_t kvrow = (int64_t)b * a.H + g;
-
-    for (int i = tid; i < GQ * D; i += NT) S.qs[i / D][i % D] = kvq_h2f(a.q[((int64_t)b * Hq + g * GQ) * D + i]);
-    __syncthreads();
-
-    float m[GQ], l[GQ], o[4][GQ], zt[4][GQ];
-#pragma unroll
-    for (int h = 0; h < GQ; ++h) {
-        m[h] = -INFINITY;
-        l[h] = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            o[i][h] = 0.0f;
-            zt[i][h] = 0.0f;
-        }
-    }
-    float(*qp)[GQ] = S.qp[warp];
-    for (int s0 = t_begin + 32 * warp; s0 < t_end; s0 += 32 * NWARP) {  // uniform over the warp
-        const int t = s0 + lane;
-        const bool valid = t < t_end;
-        const int gi = s0 / KG;
-        const bool packed = gi < n_full;
-        int32_t page = 0;
-        if (valid) {
-            page = a.bt[(int64_t)b * a.max_blocks + (t >> 4)];
-            if (page < 0 || page >= a.num_blocks) {
-                kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
-                page = 0;
-            }
-        }
-        const int64_t slot = ((int64_t)page * a.H + g) * PG + (t & 15);
-        uint32_t kc[WPR];
-#pragma unroll
-        for (int w = 0; w < WPR; ++w) kc[w] = 0u;
-        uint4* vdst = reinterpret_cast<uint4*>(S.vrow[warp][lane]);
-#pragma unroll
-        for (int u = 0; u < WPR / 4; ++u) {
-            uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = make_uint4(0u, 0u, 0u, 0u);
-            if (valid) {
-                vv = __ldg(reinterpret_cast<const uint4*>(a.v_codes) + slot * (WPR / 4) + u);
-                if (packed) kv = __ldg(reinterpret_cast<const uint4*>(a.k_codes) + slot * (WPR / 4) + u);
-            }
-            kc[4 * u] = kv.x;
-            kc[4 * u + 1] = kv.y;
-            kc[4 * u + 2] = kv.z;
-            kc[4 * u + 3] = kv.w;
-            vdst[u] = vv;
-        }
-        float2 vsz[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            vsz[j] = make_float2(0.f, 0.f);
-            if (valid && j < NGV) vsz[j] = unpack_sz(a.v_sz[slot * NGV + j]);
-        }
-        // query scaled by the K scales of group gi (or plain, for the fp16 tail)
-        float c0[GQ];
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) c0[h] = 0.0f;
-        if (packed) {
-            int32_t pg = a.bt[(int64_t)b * a.max_blocks + gi * 4];
+// Issues the cp.async copies of group gi into st (one warp); pages past the sequence are
+// skipped (their tokens are masked), complete groups also bring their K rows and scales.
+template <int BITS>
+__device__ __forceinline__ void stage_group(const QAttnArgs& a, GroupStage<BITS>& st, int b, int gk, int gi,
+                                            int n_full, int n_pages, int NGV, int lane) {
+    int32_t pg = -1;
+    if (lane < 4) {
+        const int lp = 4 * gi + lane;
+        if (lp < n_pages) {
+            pg = a.bt[(int64_t)b * a.max_blocks + lp];
             if (pg < 0 || pg >= a.num_blocks) {
                 kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
                 pg = 0;
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c = lane + 32 * i;
-                const float2 sz = unpack_sz(a.k_sz[((int64_t)pg * a.H + g) * D + c]);
-#pragma unroll
-                for (int h = 0; h < GQ; ++h) {
-                    qp[c][h] = S.qs[h][c] * sz.x;
-                    c0[h] = fmaf(S.qs[h][c], sz.y, c0[h]);
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < GQ; ++h) c0[h] = kvq_warp_sum(c0[h]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c = lane + 32 * i;
-#pragma unroll
-                for (int h = 0; h < GQ; ++h) qp[c][h] = S.qs[h][c];
-            }
         }
+    }
+    int32_t P[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) P[i] = __shfl_sync(0xffffffffu, pg, i);
+    const bool packed = gi < n_full;
+    constexpr int CH = 16 * BITS;  // 16-byte chunks per page of K rows, and per V page block
+    for (int c = lane; c < 4 * CH; c += 32) {
+        const int i = c / CH, r = c % CH;
+        if (P[i] < 0) continue;
+        const int64_t off = (((int64_t)P[i] * a.H + gk) * PG) * (16 * BITS) + 16 * r;
+        if (packed) cp_async16(st.k + (i * CH + r) * 4, a.k_codes + off);
+        cp_async16(st.v + (i * CH + r) * 4, a.v_codes + off);
+    }
+    if (packed) cp_async16(st.ksz + 4 * lane, a.k_sz + ((int64_t)P[0] * a.H + gk) * D + 4 * lane);
+    const int vch = 4 * NGV;  // chunks of V scales per page
+    for (int c = lane; c < 4 * vch; c += 32) {
+        const int i = c / vch, r = c % vch;
+        if (P[i] < 0) continue;
+        cp_async16(st.vsz + i * 16 * NGV + 4 * r, a.v_sz + ((int64_t)P[i] * a.H + gk) * PG * NGV + 4 * r);
+    }
+}
+
+template <int BITS, int GQ>
+__global__ void __launch_bounds__(NT, 4) qmma_kernel(QAttnArgs a) {
+    static_assert(GQ <= 4, "at most four query heads per grid kv group");
+    extern __shared__ __align__(16) unsigned char smraw[];
+    QMSmem<BITS, GQ>& S = *reinterpret_cast<QMSmem<BITS, GQ>*>(smraw);
+    __shared__ int is_last;
+
+    const int split = blockIdx.x, gv = blockIdx.y, b = blockIdx.z;
+    const int Hv = gridDim.y, Hq = Hv * GQ;
+    const int gk = gv / a.kv_div;  // kv head of the codes
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g8 = lane >> 2, q4 = lane & 3;  // fragment row group / column pair
+    kvq_pdl_begin();
+    const int T = a.seq_lens[b];
+    if (T > a.max_len || T < 0) {
+        if (tid == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
+        return;
+    }
+    const int n_full = T / KG;
+    const int n_groups = (T + KG - 1) / KG;
+    const int n_pages = (T + PG - 1) / PG;
+    const int nsplit_b = (n_groups + a.cps - 1) / a.cps;
+    if (n_groups == 0) {  // empty sequence: output 0
+        if (split == 0)
+            for (int i = tid; i < GQ * D; i += NT) a.out[((int64_t)b * Hq + gv * GQ) * D + i] = 0.0f;
+        return;
+    }
+    if (split >= nsplit_b) return;
+    const int g_begin = split * a.cps, g_end = min(n_groups, g_begin + a.cps);
+    const int NGV = D / a.G;
+
+    for (int i = tid; i < GQ * D; i += NT) S.qs[i / D][i % D] = kvq_h2f(a.q[((int64_t)b * Hq + gv * GQ) * D + i]);
+    // A-fragment rows of absent heads (fewer than four) stay zero
+    for (int i = tid; i < NWARP * 16 * 32; i += NT) (&S.afr[0][0][0])[i] = 0u;
+    __syncthreads();
+
+    float acc[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mt][i] = 0.0f;
+    float zt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float mrun = -INFINITY, lrun = 0.0f;
+    const int hs = g8 >> 1;  // the head of this lane's score rows (slot g8 = 2 hs + hi/lo)
+
+    int gi = g_begin + warp, buf = 0;
+    if (gi < g_end) stage_group<BITS>(a, S.u.st[warp][0], b, gk, gi, n_full, n_pages, NGV, lane);
+    cp_commit();
+    for (; gi < g_end; gi += NWARP) {
+        if (gi + NWARP < g_end)
+            stage_group<BITS>(a, S.u.st[warp][buf ^ 1], b, gk, gi + NWARP, n_full, n_pages, NGV, lane);
+        cp_commit();
+        cp_wait<1>();
         __syncwarp();
-        float sc[GQ];
+        const GroupStage<BITS>& st = S.u.st[warp][buf];
+        const int t0 = gi * KG;
+        const bool packed = gi < n_full;
+
+        // ---- A fragments: slot 2h holds fp16(q_h,c scale_c), slot 2h + 1 the fp16 remainder;
+        // register 2s + i covers channels 16s + 8i + 2r + {0, 1} of fragment column r
+        float c0p[GQ];
 #pragma unroll
-        for (int h = 0; h < GQ; ++h) sc[h] = c0[h];
-        if (packed) {
+        for (int h = 0; h < GQ; ++h) c0p[h] = 0.0f;
 #pragma unroll
-            for (int w = 0; w < WPR; ++w) {
-                const uint32_t word = kc[w];
-#pragma unroll
-                for (int i = 0; i < 32 / BITS; ++i) {
-                    const int c = w * (32 / BITS) + i;
-                    float qv[GQ];
-                    lds_heads<GQ>(qv, qp[c]);
-                    fma_heads<GQ>(sc, qv, code_f(bfe_u32(word, i * BITS, BITS)));
-                }
+        for (int k = 0; k < 2 * GQ; ++k) {
+            const int u = lane + 32 * k;
+            const int h = k >> 1, s = (u >> 3) & 7, i = (u >> 2) & 1, r = u & 3;
+            const int c = 16 * s + 8 * i + 2 * r;
+            const float2 qv = *reinterpret_cast<const float2*>(&S.qs[h][c]);
+            float a0 = qv.x, a1 = qv.y;  // q_c scale_c: a product of two fp16 numbers, exact in fp32
+            if (packed) {
+                const float2 sz0 = unpack_h2(st.ksz[c]), sz1 = unpack_h2(st.ksz[c + 1]);
+                a0 *= sz0.x;
+                a1 *= sz1.x;
+                c0p[h] = fmaf(qv.x, sz0.y, c0p[h]);
+                c0p[h] = fmaf(qv.y, sz1.y, c0p[h]);
             }
-        } else if (valid) {
-            const uint16_t* kr = a.k_tail + (kvrow * KG + (t & (KG - 1))) * D;
-            for (int c8 = 0; c8 < D; c8 += 8) {
-                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(kr + c8));
-                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 kk = __half22float2(*reinterpret_cast<const __half2*>(&w4[i]));
-                    float qv[GQ];
-                    lds_heads<GQ>(qv, qp[c8 + 2 * i]);
-                    fma_heads<GQ>(sc, qv, kk.x);
-                    lds_heads<GQ>(qv, qp[c8 + 2 * i + 1]);
-                    fma_heads<GQ>(sc, qv, kk.y);
-                }
-            }
+            const uint32_t hi = pack_h2(a0, a1);
+            const float2 hf = unpack_h2(hi);
+            S.afr[warp][2 * s + i][4 * (2 * h) + r] = hi;
+            S.afr[warp][2 * s + i][4 * (2 * h + 1) + r] = pack_h2(a0 - hf.x, a1 - hf.y);
         }
-        // online softmax per head over the warp's 32 tokens
+        float c0 = 0.0f;
 #pragma unroll
         for (int h = 0; h < GQ; ++h) {
-            const float sh = valid ? sc[h] * KVQ_SCORE_LOG2_SCALE : -INFINITY;
-            const float mn = fmaxf(m[h], kvq_warp_max(sh));
-            const float alpha = exp2f(m[h] - mn);
-            const float p = valid ? exp2f(sh - mn) : 0.0f;
-            l[h] = l[h] * alpha + kvq_warp_sum(p);
-            m[h] = mn;
+            const float v = kvq_warp_sum(c0p[h]);
+            if (hs == h) c0 = v;
+        }
+        __syncwarp();
+        uint32_t af[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                o[i][h] *= alpha;
-                zt[i][h] *= alpha;
+        for (int r = 0; r < 16; ++r) af[r] = S.afr[warp][r][lane];
+
+        // ---- scores: 8 n-tiles of 8 tokens; this lane gets slot g8 of tokens 8nt + 2q4 + {0, 1}
+        float sc[8][2];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (packed) {
+                const uint32_t* kr = st.k + (8 * nt + g8) * (4 * BITS) + q4 * BITS;
+                uint32_t kw[BITS];
+#pragma unroll
+                for (int u = 0; u < BITS; ++u) kw[u] = kr[u];
+                mma16816(d, af[0], 0u, af[1], 0u, k_pair<BITS, 0>(kw), k_pair<BITS, 1>(kw));
+                mma16816(d, af[2], 0u, af[3], 0u, k_pair<BITS, 2>(kw), k_pair<BITS, 3>(kw));
+                mma16816(d, af[4], 0u, af[5], 0u, k_pair<BITS, 4>(kw), k_pair<BITS, 5>(kw));
+                mma16816(d, af[6], 0u, af[7], 0u, k_pair<BITS, 6>(kw), k_pair<BITS, 7>(kw));
+                mma16816(d, af[8], 0u, af[9], 0u, k_pair<BITS, 8>(kw), k_pair<BITS, 9>(kw));
+                mma16816(d, af[10], 0u, af[11], 0u, k_pair<BITS, 10>(kw), k_pair<BITS, 11>(kw));
+                mma16816(d, af[12], 0u, af[13], 0u, k_pair<BITS, 12>(kw), k_pair<BITS, 13>(kw));
+                mma16816(d, af[14], 0u, af[15], 0u, k_pair<BITS, 14>(kw), k_pair<BITS, 15>(kw));
+            } else {
+                // the unfinished group: fp16 keys (rows t mod 64 of the tail buffer), q unscaled
+                const uint32_t* kr = reinterpret_cast<const uint32_t*>(
+                    a.k_tail + (((int64_t)b * a.H + gk) * KG + 8 * nt + g8) * D + 2 * q4);
+#pragma unroll
+                for (int s = 0; s < 8; ++s) mma16816(d, af[2 * s], 0u, af[2 * s + 1], 0u, kr[8 * s], kr[8 * s + 4]);
             }
+            sc[nt][0] = d[0];
+            sc[nt][1] = d[1];
+        }
+
+        // ---- online softmax per head (log2 domain); the hi and lo slots are summed first
+        float gm = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float x = sc[nt][e] + __shfl_xor_sync(0xffffffffu, sc[nt][e], 4);
+                const int t = t0 + 8 * nt + 2 * q4 + e;
+                sc[nt][e] = t < T ? (x + c0) * KVQ_SCORE_LOG2_SCALE : -INFINITY;
+                gm = fmaxf(gm, sc[nt][e]);
+            }
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
+        const float mn = fmaxf(mrun, gm);
+        const float alpha = mn == -INFINITY ? 1.0f : exp2f(mrun - mn);
+        float ls = 0.0f;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float p = mn == -INFINITY ? 0.0f : exp2f(sc[nt][e] - mn);
+                sc[nt][e] = p;
+                ls += p;
+            }
+        mrun = mn;
+        lrun = fmaf(lrun, alpha, ls);
+        // the accumulator columns belong to head q4
+        const float aq = __shfl_sync(0xffffffffu, alpha, 8 * q4);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            acc[mt][0] *= aq;
+            acc[mt][2] *= aq;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) zt[j] *= alpha;
+
+        // ---- values, page by page: B column g8 = 2h carries fp16(p vscale) of head h, odd columns 0
+        const bool even = (g8 & 1) == 0;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const float pv[4] = {sc[2 * ks][0], sc[2 * ks][1], sc[2 * ks + 1][0], sc[2 * ks + 1][1]};
+            int tk[4];
+            tk[0] = 2 * q4;
+            tk[1] = 2 * q4 + 1;
+            tk[2] = 2 * q4 + 8;
+            tk[3] = 2 * q4 + 9;
+            uint32_t bv[4][2];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (j < NGV) {
-                    S.pp[warp][lane][j][h] = p * vsz[j].x;
-                    zt[j][h] = fmaf(p, vsz[j].y, zt[j][h]);
+                bv[j][0] = bv[j][1] = 0u;
+                if (j >= NGV) continue;
+                float pp[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool valid = t0 + 16 * ks + tk[e] < T;  // masked tokens may hold any scale
+                    const float2 sz = unpack_h2(st.vsz[(16 * ks + tk[e]) * NGV + j]);
+                    pp[e] = valid ? pv[e] * sz.x : 0.0f;
+                    zt[j] = valid ? fmaf(pv[e], sz.y, zt[j]) : zt[j];
+                }
+                if (even) {
+                    bv[j][0] = pack_h2(pp[0], pp[1]);
+                    bv[j][1] = pack_h2(pp[2], pp[3]);
                 }
             }
-        }
-        __syncwarp();
-        // values: this lane's channels 4*lane .. 4*lane+3 over the 32 tokens
-        const int n_tok = min(32, t_end - s0);
-        for (int tt = 0; tt < n_tok; ++tt) {
-            float pv[GQ];
-            lds_heads<GQ>(pv, S.pp[warp][tt][jd]);
-            const uint32_t w = S.vrow[warp][tt][(4 * lane * BITS) >> 5];
+            const uint32_t* vblk = st.v + ks * 64 * BITS;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float x = code_f(bfe_u32(w, ((4 * lane + i) * BITS) & 31, BITS));
-                fma_heads<GQ>(o[i], pv, x);
+            for (int mt = 0; mt < 8; ++mt) {
+                const int j = (mt * NGV) >> 3;  // V group of channels 16mt .. 16mt + 15
+                const uint32_t b0 = j == 0 ? bv[0][0] : j == 1 ? bv[1][0] : j == 2 ? bv[2][0] : bv[3][0];
+                const uint32_t b1 = j == 0 ? bv[0][1] : j == 1 ? bv[1][1] : j == 2 ? bv[2][1] : bv[3][1];
+                uint32_t A[4];
+                v_pairs<BITS>(vblk + (8 * mt + g8) * BITS, q4, A);
+                mma16816(acc[mt], A[0], A[1], A[2], A[3], b0, b1);
             }
         }
         __syncwarp();
+        buf ^= 1;
     }
-    // zero term: sum over the warp's lanes of sum_t p vzero, for this lane's V group
+    cp_wait<0>();
+
+    // ---- this warp's state per head: l and the zero terms summed over the head's four lanes
+    lrun += __shfl_xor_sync(0xffffffffu, lrun, 1);
+    lrun += __shfl_xor_sync(0xffffffffu, lrun, 2);
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) zt[j][h] = kvq_warp_sum(zt[j][h]);
-#pragma unroll
-    for (int h = 0; h < GQ; ++h) {
-        float z = zt[0][h];
-#pragma unroll
-        for (int j = 1; j < 4; ++j)
-            if (j == jd) z = zt[j][h];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[i][h] += z;
+    for (int j = 0; j < 4; ++j) {
+        zt[j] += __shfl_xor_sync(0xffffffffu, zt[j], 1);
+        zt[j] += __shfl_xor_sync(0xffffffffu, zt[j], 2);
     }
-    // merge the warps of the CTA (the per-warp query buffers hold the values)
-    __syncthreads();
-    float* ro = &S.qp[0][0][0];  // [NWARP][GQ][D]
-    if (lane == 0)
+    float zq[4];
 #pragma unroll
-        for (int h = 0; h < GQ; ++h) {
-            S.m[warp][h] = m[h];
-            S.l[warp][h] = l[h];
+    for (int j = 0; j < 4; ++j) zq[j] = __shfl_sync(0xffffffffu, zt[j], 8 * q4);
+    __syncthreads();  // every warp is done with its stages: the union now holds the outputs
+    if (q4 < GQ) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int j = (mt * NGV) >> 3;
+            const float z = j == 0 ? zq[0] : j == 1 ? zq[1] : j == 2 ? zq[2] : zq[3];
+            S.u.ro[warp][q4][16 * mt + g8] = acc[mt][0] + z;
+            S.u.ro[warp][q4][16 * mt + g8 + 8] = acc[mt][2] + z;
         }
-#pragma unroll
-    for (int h = 0; h < GQ; ++h)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ro[(warp * GQ + h) * D + 4 * lane + i] = o[i][h];
+    }
+    if (q4 == 0 && (g8 & 1) == 0 && hs < GQ) {
+        S.m[warp][hs] = mrun;
+        S.l[warp][hs] = lrun;
+    }
     __syncthreads();
-    const int64_t rec0 = (((int64_t)b * a.H + g) * a.n_splits + split) * GQ;
+
+    // ---- merge the warps, then the splits (the last CTA of the kv group)
+    const int64_t rec0 = (((int64_t)b * Hv + gv) * a.n_splits + split) * GQ;
     for (int e = tid; e < GQ * D; e += NT) {
         const int h = e / D, d = e % D;
         float M = -INFINITY;
@@ -537,7 +444,7 @@ __global__ void __launch_bounds__(NT) qattn2_kernel(QAttnArgs a) {
             for (int w = 0; w < NWARP; ++w) {
                 const float wt = exp2f(S.m[w][h] - M);
                 L = fmaf(S.l[w][h], wt, L);
-                O = fmaf(ro[(w * GQ + h) * D + d], wt, O);
+                O = fmaf(S.u.ro[w][h][d], wt, O);
             }
         }
         float* r = a.part + (rec0 + h) * REC;
@@ -550,31 +457,36 @@ __global__ void __launch_bounds__(NT) qattn2_kernel(QAttnArgs a) {
     __threadfence();
     __syncthreads();
     if (tid == 0) {
-        const int prev = atomicAdd(&a.counters[b * a.H + g], 1);
+        const int prev = atomicAdd(&a.counters[b * Hv + gv], 1);
         is_last = (prev == nsplit_b - 1);
     }
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    // ---- last CTA of (b, g): merge the splits by log-sum-exp
     for (int e = tid; e < GQ * D; e += NT) {
         const int h = e / D, d = e % D;
         float M = -INFINITY;
         for (int sp = 0; sp < nsplit_b; ++sp)
-            M = fmaxf(M, __ldcg(a.part + ((((int64_t)b * a.H + g) * a.n_splits + sp) * GQ + h) * REC));
-        float Lsum = 0.0f, acc = 0.0f;
+            M = fmaxf(M, __ldcg(a.part + ((((int64_t)b * Hv + gv) * a.n_splits + sp) * GQ + h) * REC));
+        float Lsum = 0.0f, acc2 = 0.0f;
         if (M != -INFINITY) {
             for (int sp = 0; sp < nsplit_b; ++sp) {
-                const float* r = a.part + ((((int64_t)b * a.H + g) * a.n_splits + sp) * GQ + h) * REC;
+                const float* r = a.part + ((((int64_t)b * Hv + gv) * a.n_splits + sp) * GQ + h) * REC;
                 const float w = exp2f(__ldcg(r) - M);
                 Lsum = fmaf(__ldcg(r + 1), w, Lsum);
-                acc = fmaf(__ldcg(r + 4 + d), w, acc);
+                acc2 = fmaf(__ldcg(r + 4 + d), w, acc2);
             }
         }
-        a.out[((int64_t)b * Hq + g * GQ + h) * D + d] = Lsum > 0.0f ? acc / Lsum : 0.0f;
+        a.out[((int64_t)b * Hq + gv * GQ + h) * D + d] = Lsum > 0.0f ? acc2 / Lsum : 0.0f;
     }
-    if (tid == 0) a.counters[b * a.H + g] = 0;
+    if (tid == 0) a.counters[b * Hv + gv] = 0;
 }
+
+// ---------------------------------------------------------------- planning and launch
+
+// q heads per grid kv group: 8 sharing one kv head are served as two groups of 4
+int grid_gq(int gq) { return gq > 4 ? 4 : gq; }
+int kv_div_of(int gq) { return gq > 4 ? gq / 4 : 1; }
 
 struct Plan {
     int n_splits;
@@ -582,42 +494,46 @@ struct Plan {
 };
 
 Plan plan_splits(const kvq_layout* L, const kvq_seqs* S) {
-    const int n_chunks = (std::max(S->max_len, 1) + KG - 1) / KG;
-    const int64_t units = (int64_t)std::max(S->batch, 1) * L->n_kv_heads;
-    const int64_t target = 8LL * kvq_num_sms();  // resident CTAs to aim for
+    const int n_groups = (std::max(S->max_len, 1) + KG - 1) / KG;
+    const int gq = L->n_q_heads / L->n_kv_heads;
+    const int64_t units = (int64_t)std::max(S->batch, 1) * L->n_kv_heads * kv_div_of(gq);
+    const int64_t target = 4LL * kvq_num_sms();  // resident CTAs to aim for (four per SM)
     int splits = (int)std::max<int64_t>(1, (target + units - 1) / units);
-    int cps = std::max(4, (n_chunks + splits - 1) / splits);
-    cps = std::min(cps, n_chunks);
-    splits = (n_chunks + cps - 1) / cps;
+    int cps = std::max(NWARP, (n_groups + splits - 1) / splits);
+    cps = std::min(cps, n_groups);
+    splits = (n_groups + cps - 1) / cps;
     return {splits, cps};
 }
 
 size_t ws_layout(const kvq_layout* L, const kvq_seqs* S, size_t* off_part, size_t* off_cnt) {
     const Plan p = plan_splits(L, S);
     const int GQ = L->n_q_heads / L->n_kv_heads;
-    const size_t recs = (size_t)std::max(S->batch, 1) * L->n_kv_heads * p.n_splits * GQ;
+    const size_t units = (size_t)std::max(S->batch, 1) * L->n_kv_heads * kv_div_of(GQ);
+    const size_t recs = units * p.n_splits * grid_gq(GQ);
     *off_part = sizeof(KvqWsHeader);
     *off_cnt = kvq_round_up(*off_part + recs * REC * sizeof(float), 256);
-    return kvq_round_up(*off_cnt + (size_t)std::max(S->batch, 1) * L->n_kv_heads * sizeof(int32_t), 256);
+    return kvq_round_up(*off_cnt + units * sizeof(int32_t), 256);
 }
 
 template <int BITS, int GQ>
 int launch_one(dim3 grid, cudaStream_t s, const QAttnArgs& a) {
-    const int smem = (int)sizeof(Q2Smem<BITS, GQ>);
-    const int st = kvq_prepare_kernel((const void*)qattn2_kernel<BITS, GQ>, smem);
+    const int smem = (int)sizeof(QMSmem<BITS, GQ>);
+    const int st = kvq_prepare_kernel((const void*)qmma_kernel<BITS, GQ>, smem);
     if (st) return st;
-    const cudaError_t e = kvq_launch_pdl(qattn2_kernel<BITS, GQ>, grid, dim3(NT), (size_t)smem, s, a);
+    const cudaError_t e = kvq_launch_pdl(qmma_kernel<BITS, GQ>, grid, dim3(NT), (size_t)smem, s, a);
     if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant launch: %s", cudaGetErrorString(e));
     return KVQ_OK;
 }
 
+// grid: (splits, kv heads, batch); widened here to the grid kv groups
 template <int BITS>
-int launch_bits(int gq, dim3 grid, cudaStream_t s, const QAttnArgs& a) {
-    switch (gq) {
+int launch_bits(int gq, dim3 grid, cudaStream_t s, QAttnArgs& a) {
+    a.kv_div = kv_div_of(gq);
+    grid.y *= a.kv_div;
+    switch (grid_gq(gq)) {
         case 1: return launch_one<BITS, 1>(grid, s, a);
         case 2: return launch_one<BITS, 2>(grid, s, a);
-        case 4: return launch_one<BITS, 4>(grid, s, a);
-        default: return launch_one<BITS, 8>(grid, s, a);
+        default: return launch_one<BITS, 4>(grid, s, a);
     }
 }
 
@@ -640,8 +556,8 @@ extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, cons
     KVQ_REQUIRE(L->bits != 16, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: layer is not quantized (bits == 16)");
     KVQ_REQUIRE(P != nullptr && P->k_codes && P->v_codes && P->k_sz && P->v_sz && P->k_tail, KVQ_ERR_INVALID_ARG,
                 "kv_decode_attn_quant: quantized pool arrays missing");
-    KVQ_REQUIRE(((uintptr_t)P->k_codes & 15u) == 0 && ((uintptr_t)P->v_codes & 15u) == 0, KVQ_ERR_INVALID_ARG,
-                "kv_decode_attn_quant: code arrays must be 16-byte aligned");
+    KVQ_REQUIRE((((uintptr_t)P->k_codes | (uintptr_t)P->v_codes | (uintptr_t)P->k_sz | (uintptr_t)P->v_sz) & 15u) == 0,
+                KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: code and scale arrays must be 16-byte aligned");
     KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: batch exceeds max_seqs");
     size_t off_part, off_cnt;
     const size_t need = ws_layout(L, S, &off_part, &off_cnt);
@@ -729,8 +645,8 @@ extern "C" int kv_decode_attn_quant_noalloc(const kvq_layout* L, const kvq_pool*
     KVQ_REQUIRE(L->bits != 16, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: layer is not quantized");
     KVQ_REQUIRE(P != nullptr && P->k_codes && P->v_codes && P->k_sz && P->v_sz && P->k_tail, KVQ_ERR_INVALID_ARG,
                 "kv_decode_attn_quant_noalloc: quantized pool arrays missing");
-    KVQ_REQUIRE(((uintptr_t)P->k_codes & 15u) == 0 && ((uintptr_t)P->v_codes & 15u) == 0, KVQ_ERR_INVALID_ARG,
-                "kv_decode_attn_quant_noalloc: code arrays must be 16-byte aligned");
+    KVQ_REQUIRE((((uintptr_t)P->k_codes | (uintptr_t)P->v_codes | (uintptr_t)P->k_sz | (uintptr_t)P->v_sz) & 15u) == 0,
+                KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: code and scale arrays must be 16-byte aligned");
     KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: batch exceeds max_seqs");
     size_t off_part, off_cnt;
     const size_t need = ws_layout(L, S, &off_part, &off_cnt);

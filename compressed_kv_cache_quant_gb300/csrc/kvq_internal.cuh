@@ -125,6 +125,33 @@ static inline cudaError_t kvq_launch_pdl(void (*kernel)(KArgs...), dim3 grid, di
 // log2(e) / sqrt(128): scores are kept in the log2 domain, p = exp2(s - m).
 #define KVQ_SCORE_LOG2_SCALE 0.12751743074048468f
 
+// ---- bit layout of the quantized codes (b = bits per code, 16 / b codes per 16-bit half word)
+//
+// Codes travel in pairs: the two codes of a pair sit at the same offset in the low and the
+// high half of a 32-bit word, so one AND/OR turns a pair into two fp16 numbers 1024 + code
+// (times a power of two) for the tensor-core fragments.
+//
+// K token row (4b words, one per token and kv head in its page): the pair of channels
+// (2p, 2p + 1) with p = 8s + r + 4e (s < 8, r < 4, e < 2) is the m-th (m = 2s + e) pair of
+// column r: word r*b + m / (16/b), offset (m % (16/b)) * b.
+__host__ __device__ static inline void kvq_k_code_pos(int c, int bits, int* word, int* bit) {
+    const int p = c >> 1, s = p >> 3, r = p & 3, e = (p >> 2) & 1;
+    const int m = 2 * s + e, per = 16 / bits;
+    *word = r * bits + m / per;
+    *bit = (m % per) * bits + 16 * (c & 1);
+}
+
+// V page block (64b words per page and kv head): channel d = 16t + 8u + x (x < 8, u < 2) and the
+// token pair (2y, 2y + 1) of the page with y = r + 4e form the m-th (m = 4r + 2e + u) pair of row
+// 8t + x: word (8t + x)*b + m / (16/b), offset (m % (16/b)) * b; the odd token in the high half.
+__host__ __device__ static inline void kvq_v_code_pos(int tok, int d, int bits, int* word, int* bit) {
+    const int t = d >> 4, x = d & 7, u = (d >> 3) & 1;
+    const int y = tok >> 1, r = y & 3, e = y >> 2;
+    const int m = 4 * r + 2 * e + u, per = 16 / bits;
+    *word = (8 * t + x) * bits + m / per;
+    *bit = (m % per) * bits + 16 * (tok & 1);
+}
+
 // Once per (kernel, device): prefer the largest shared-memory carveout, so that
 // the kernels of a decode step never make the SMs repartition L1 and shared
 // memory between launches, and allow `dyn_smem_max` bytes of dynamic shared

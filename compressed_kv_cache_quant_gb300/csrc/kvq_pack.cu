@@ -48,11 +48,11 @@ __device__ __forceinline__ uint32_t pack_sz(float scale32, float zero) {
     return (uint32_t)kvq_f2h(scale32) | ((uint32_t)kvq_f2h(zero) << 16);
 }
 
-// One warp quantizes one V token row of 128 channels in groups of G.
-// Lane l holds channels 4l..4l+3; its four codes occupy row bits [4*BITS*l, 4*BITS*(l+1)).
+// One warp quantizes one V token of 128 channels in groups of G.  Lane l holds channels
+// 4l..4l+3 and returns their codes; (scale, zero) of each group goes to dst_sz.
 template <int BITS>
-__device__ __forceinline__ void quant_v_row(const uint16_t* src, int G, uint32_t* dst_codes, uint32_t* dst_sz,
-                                            int lane) {
+__device__ __forceinline__ void quant_v_token(const uint16_t* src, int G, uint32_t* dst_sz, int lane,
+                                              uint32_t* codes) {
     const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
     float x[4];
     x[0] = kvq_h2f((uint16_t)(raw.x & 0xffffu));
@@ -68,15 +68,23 @@ __device__ __forceinline__ void quant_v_row(const uint16_t* src, int G, uint32_t
     }
     const float levels = (float)((1 << BITS) - 1);
     const float scale = kvq_scale32(mn, mx, levels);
-    uint32_t v = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v |= kvq_code(x[i], mn, scale, levels) << (i * BITS);
-    constexpr int LPW = 32 / (4 * BITS);  // lanes sharing one 32-bit word
-    uint32_t w = v << ((4 * BITS * lane) & 31);
-#pragma unroll
-    for (int o = 1; o < LPW; o <<= 1) w |= __shfl_xor_sync(0xffffffffu, w, o);
-    if ((lane % LPW) == 0) dst_codes[lane / LPW] = w;
+    for (int i = 0; i < 4; ++i) codes[i] = kvq_code(x[i], mn, scale, levels);
     if ((lane % lpg) == 0) dst_sz[lane / lpg] = pack_sz(scale, mn);
+}
+
+// Places the four codes of lane l (channels 4l..4l+3) of page token `tok` into a V page block,
+// replacing what was there (only this token's bits change).
+template <int BITS>
+__device__ __forceinline__ void put_v_codes(uint32_t* blk, int tok, int lane, const uint32_t* codes) {
+    constexpr uint32_t M = (1u << BITS) - 1u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int w, bit;
+        kvq_v_code_pos(tok, 4 * lane + i, BITS, &w, &bit);
+        atomicAnd(&blk[w], ~(M << bit));
+        if (codes[i]) atomicOr(&blk[w], codes[i] << bit);
+    }
 }
 
 // Thread c (of 128) quantizes channel c of a 64-token K group read from
@@ -95,11 +103,12 @@ __device__ __forceinline__ void quant_k_group(const uint16_t* src, int64_t row_s
     const float levels = (float)((1 << BITS) - 1);
     const float scale = kvq_scale32(mn, mx, levels);
     constexpr int WPR = 4 * BITS;  // 32-bit words per token row
-    const int bit = c * BITS;
+    int word, bit;
+    kvq_k_code_pos(c, BITS, &word, &bit);
     for (int i = 0; i < KG; ++i) {
         float x = kvq_h2f(src[(int64_t)i * row_stride + c]);
         uint32_t code = kvq_code(x, mn, scale, levels);
-        if (code) atomicOr(&rows[i * WPR + (bit >> 5)], code << (bit & 31));
+        if (code) atomicOr(&rows[i * WPR + word], code << bit);
     }
     *sz = pack_sz(scale, mn);
 }
@@ -135,22 +144,31 @@ struct PackArgs {
     int64_t stride_t;
 };
 
-// V rows: one warp per (token, head).
+// V: one CTA of 4 warps per (page, head) touched by the tokens; the page's block of codes is
+// assembled in shared memory (tokens outside the range keep their codes) and written back.
 template <int BITS>
-__global__ void __launch_bounds__(256) pack_v_kernel(PackArgs a) {
-    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= a.n_tokens * a.H) return;
-    const int64_t i = row / a.H;
-    const int h = (int)(row % a.H);
-    const int64_t t = a.t_start + i;
-    const int32_t page = a.bt_row[t / PG];
-    if (page < 0 || page >= a.pool.num_blocks) return;  // an invalid table entry skips the row
-    constexpr int R = 16 * BITS;
-    const int64_t slot = ((int64_t)page * a.H + h) * PG + (t % PG);
-    uint32_t* codes = reinterpret_cast<uint32_t*>(a.pool.v_codes + slot * R);
-    uint32_t* sz = a.pool.v_sz + slot * (D / a.G);
-    quant_v_row<BITS>(a.v + i * a.stride_t + (int64_t)h * D, a.G, codes, sz, lane);
+__global__ void __launch_bounds__(128) pack_v_kernel(PackArgs a) {
+    constexpr int BW = 64 * BITS;  // words per page block
+    __shared__ uint32_t blk[BW];
+    const int64_t lp = a.t_start / PG + blockIdx.x;  // logical page
+    const int h = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t page = a.bt_row[lp];
+    if (page < 0 || page >= a.pool.num_blocks) return;  // an invalid table entry skips the page
+    uint32_t* gblk = reinterpret_cast<uint32_t*>(a.pool.v_codes) + ((int64_t)page * a.H + h) * BW;
+    for (int w = threadIdx.x; w < BW; w += 128) blk[w] = gblk[w];
+    __syncthreads();
+    for (int tok = warp; tok < PG; tok += 4) {
+        const int64_t t = lp * PG + tok;
+        if (t < a.t_start || t >= a.t_start + a.n_tokens) continue;  // uniform over the warp
+        const int64_t i = t - a.t_start;
+        uint32_t codes[4];
+        quant_v_token<BITS>(a.v + i * a.stride_t + (int64_t)h * D, a.G,
+                            a.pool.v_sz + (((int64_t)page * a.H + h) * PG + tok) * (D / a.G), lane, codes);
+        put_v_codes<BITS>(blk, tok, lane, codes);
+    }
+    __syncthreads();
+    for (int w = threadIdx.x; w < BW; w += 128) gblk[w] = blk[w];
 }
 
 // K groups: one CTA of 128 threads per (complete 64-token group, head).
@@ -220,8 +238,8 @@ __global__ void __launch_bounds__(128) pack_fp16_kernel(PackArgs a) {
 
 template <int BITS>
 int launch_pack_quant(const PackArgs& a, cudaStream_t s) {
-    const int64_t rows = a.n_tokens * a.H;
-    if (rows > 0) pack_v_kernel<BITS><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a);
+    const int64_t n_pages = (a.t_start + a.n_tokens + PG - 1) / PG - a.t_start / PG;
+    if (n_pages > 0) pack_v_kernel<BITS><<<dim3((unsigned)n_pages, a.H), 128, 0, s>>>(a);
     const int64_t n_full = a.n_tokens / KG;
     if (n_full > 0) pack_k_kernel<BITS><<<dim3((unsigned)n_full, a.H), 128, 0, s>>>(a);
     const int64_t first_tail = a.t_start + n_full * KG;
@@ -278,11 +296,12 @@ __global__ void __launch_bounds__(128) append_quant_kernel(AppendArgs a) {
     if (page < 0) return;
     const uint16_t* kn = a.k_new + ((int64_t)b * a.H + h) * D;
     const uint16_t* vn = a.v_new + ((int64_t)b * a.H + h) * D;
-    constexpr int R = 16 * BITS;
     if (c < 32) {
         const int64_t slot = ((int64_t)page * a.H + h) * PG + (p % PG);
-        quant_v_row<BITS>(vn, a.G, reinterpret_cast<uint32_t*>(a.pool.v_codes + slot * R),
-                          a.pool.v_sz + slot * (D / a.G), c);
+        uint32_t codes[4];
+        quant_v_token<BITS>(vn, a.G, a.pool.v_sz + slot * (D / a.G), c, codes);
+        put_v_codes<BITS>(reinterpret_cast<uint32_t*>(a.pool.v_codes) + ((int64_t)page * a.H + h) * 64 * BITS,
+                          (int)(p % PG), c, codes);
     }
     uint16_t* tail = a.pool.k_tail + ((int64_t)b * a.H + h) * KG * D;
     tail[(p % KG) * D + c] = kn[c];

@@ -84,11 +84,21 @@ typedef struct kvq_layout {
  * Pages are indexed by physical page id p in [0, num_blocks); per-sequence
  * state is indexed by the sequence's batch index b in [0, max_seqs).
  *
- * Quantized layer (bits in {1,2,4,8}); R = d*bits/8 bytes per token row:
- *   k_codes [num_blocks][H_kv][16][R]   uint8; K codes, token rows
- *   v_codes [num_blocks][H_kv][16][R]   uint8; V codes, token rows
- *     Within a row the code of channel c occupies bits [c*bits, (c+1)*bits)
- *     of the row read as little-endian 32-bit words.
+ * Quantized layer (bits in {1,2,4,8}); R = d*bits/8 bytes per token row;
+ * blocks are read as little-endian 32-bit words, n = 16/bits codes per half
+ * word, and codes travel in pairs: the two codes of a pair sit at the same
+ * offset o in the low and the high half of one word (bits [o, o+bits) and
+ * [16+o, 16+o+bits)), the layout the tensor-core fragments read:
+ *   k_codes [num_blocks][H_kv][16][R]   uint8; K codes, one row per token.
+ *     Channels (2p, 2p+1), p = 8s + r + 4e (s < 8, r < 4, e < 2), form pair
+ *     m = 2s + e of column r: word r*bits + m/n of the row, o = (m%n)*bits,
+ *     the odd channel in the high half.
+ *   v_codes [num_blocks][H_kv][16][R]   uint8; V codes, one 16*R-byte block
+ *     per page and kv head, channel-major: channel d = 16t + 8u + x
+ *     (x < 8, u < 2) and the page's tokens (2y, 2y+1), y = r + 4e (r < 4,
+ *     e < 2), form pair m = 4r + 2e + u of row 8t + x: word
+ *     (8t + x)*bits + m/n of the block, o = (m%n)*bits, the odd token in the
+ *     high half.
  *   k_sz    [num_blocks][H_kv][d][2]    fp16 (scale, zero) of the 64-token K
  *           group whose FIRST page is p (entries of other pages are unused)
  *   v_sz    [num_blocks][H_kv][16][d/G][2]  fp16 (scale, zero) per token and

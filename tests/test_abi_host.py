@@ -103,3 +103,27 @@ def test_allocator_shuffled_is_a_permutation(lib):
     assert sorted(ids) == list(range(1000)) and ids != list(range(1000))
     b = kvq.Allocator(1000, seed=42)
     assert b.alloc(1000) == ids        # seeded: reproducible
+
+
+@pytest.mark.parametrize("bits", [1, 2, 4, 8])
+def test_code_layout_is_a_packing(bits):
+    """Every (token, channel) code of a K row and a V page block owns its own
+    bits, inside the block, with the two codes of a pair in the two half words."""
+    from kvq_format import k_code_pos, v_code_pos
+    seen = set()
+    for c in range(128):
+        w, b = k_code_pos(c, bits)
+        assert 0 <= w < 4 * bits and 0 <= b and b % 16 + bits <= 16
+        seen.update((w, b + i) for i in range(bits))
+        if c % 2 == 0:
+            assert k_code_pos(c + 1, bits) == (w, b + 16)
+    assert len(seen) == 128 * bits
+    seen = set()
+    for tok in range(16):
+        for d in range(128):
+            w, b = v_code_pos(tok, d, bits)
+            assert 0 <= w < 64 * bits and b % 16 + bits <= 16
+            seen.update((w, b + i) for i in range(bits))
+            if tok % 2 == 0:
+                assert v_code_pos(tok + 1, d, bits) == (w, b + 16)
+    assert len(seen) == 16 * 128 * bits

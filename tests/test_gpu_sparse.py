@@ -77,6 +77,9 @@ def _select(scores_np, lengths, n_heads, k_fixed, ratio, ns, w):
     ([131072 + 17], -1, 0.03, 4, 128),   # ratio mode at 128K
     ([20000, 5], 1000, 0.0, 0, 0),
     ([60000, 131089], -1, 0.03, 4, 128),
+    ([5000, 30000], 300, 0.0, 2, 5),      # a window narrower than the cluster
+    ([30000], 700, 0.0, 4, 130),          # a window that is not a multiple of 8
+    ([20000], 500, 0.0, 4, 600),          # a wide window spanning chunk boundaries
 ])
 def test_topk_select_bitexact_with_ties(lengths, k, ratio, ns, w):
     require_gpu()
