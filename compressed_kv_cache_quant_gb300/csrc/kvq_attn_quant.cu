@@ -8,15 +8,16 @@
 // 16-token pages).  With K = scale_c * code + zero_c per channel of the group,
 //   s_t = sum_c (q_c scale_c) code_t[c] + sum_c q_c zero_c,
 // the first term is a [slots x 128] x [128 x tokens] product whose A operand
-// holds q_c scale_c (exact in fp32) split into two fp16 halves (hi and lo
-// slots, summed afterwards), and whose B operand is the codes themselves,
-// turned into fp16 two at a time by one AND/OR and one exact fp16 FMA (the
-// codes are stored in pairs for that; see kvq_k_code_pos).  With V = vscale_t
+// holds q_c scale_c 2^b (exact in fp32) split into two fp16 halves (hi and lo
+// slots, summed afterwards), and whose B operand is 1 + code / 2^b, made two
+// codes at a time by one shift and one AND/OR into the mantissa of fp16 1.0
+// (the codes are stored in pairs for that, kvq_k_code_pos); the bias
+// sum_c q_c scale_c 2^b joins the zero-point term.  With V = vscale_t
 // code + vzero_t per token and V group,
-//   o[d] = sum_t (p_t vscale_t) code_t[d] + sum_t p_t vzero_t,
-// the first term is a [128 x tokens] x [tokens x heads] product: V codes
-// (stored channel-major per page, kvq_v_code_pos) against p_t vscale_t in
-// fp16.  The group's codes and scales are staged per warp with cp.async, one
+//   o[d] = sum_t p_t (vscale_t code_t[d] + vzero_t)
+// is a [128 x tokens] x [tokens x heads] product: the V codes (stored
+// channel-major per page, kvq_v_code_pos) dequantized into fp16 by one fp16
+// FMA per pair, against p_t in fp16.  The group's codes and scales are staged per warp with cp.async, one
 // group ahead.  An unfinished K group reads its keys from the fp16 tail buffer.
 #include <algorithm>
 #include <map>
@@ -29,8 +30,11 @@ namespace {
 constexpr int D = KVQ_HEAD_DIM;
 constexpr int PG = KVQ_BLOCK_TOKENS;
 constexpr int KG = KVQ_K_GROUP_TOKENS;
-constexpr int NT = 128;
-constexpr int NWARP = NT / 32;
+// warps per CTA (one CTA per SM): as many as the double-buffered group stages let fit
+template <int BITS>
+__host__ __device__ constexpr int nwarp_of() {
+    return BITS <= 2 ? 16 : (BITS == 4 ? 8 : 4);
+}
 constexpr int REC = 4 + D;  // partial record: m, l, pad, pad, o[128]
 
 struct QAttnArgs {
@@ -71,8 +75,7 @@ __device__ __forceinline__ void cp_wait() {
 // d += A (16x16, row) * B (16x8, col), fp16 operands, fp32 accumulators
 __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -83,6 +86,19 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// byte permute: the 4 bytes of the result chosen from {a, b} by the selector's nibbles
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+// fp16x2 a * b + c, one rounding per half
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
 __device__ __forceinline__ float2 unpack_h2(uint32_t x) {
     return make_float2(kvq_h2f((uint16_t)(x & 0xffffu)), kvq_h2f((uint16_t)(x >> 16)));
 }
@@ -107,11 +123,18 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w) {
 }
 
 // K B-fragment register for pair m of this lane's column (see kvq_k_code_pos): kw = the
-// BITS words of the column in the token row.
+// BITS words of the column in the token row.  The codes go to the top BITS mantissa bits of
+// fp16 1.0, giving 1 + code / 2^BITS exactly with one shift and one AND/OR; the 2^BITS factor
+// and the bias of 1 are taken up by the A operand and the per-head constant.
 template <int BITS, int M>
 __device__ __forceinline__ uint32_t k_pair(const uint32_t* kw) {
     constexpr int PER = 16 / BITS;
-    return code_pair<BITS, (M % PER) * BITS>(kw[M / PER]);
+    constexpr int POS = (M % PER) * BITS;
+    constexpr int SH = POS - (10 - BITS);  // right shift (left if negative)
+    constexpr uint32_t M1 = ((1u << BITS) - 1u) << (10 - BITS);
+    const uint32_t w = kw[M / PER];
+    const uint32_t x = SH >= 0 ? (w >> (SH >= 0 ? SH : 0)) : (w << (SH < 0 ? -SH : 0));
+    return (x & (M1 | (M1 << 16))) | 0x3C003C00u;
 }
 
 // The four V A-fragment registers of column r (pairs m = 4r .. 4r + 3, kvq_v_code_pos) from
@@ -156,11 +179,13 @@ struct GroupStage {
     uint32_t vsz[KG * 4];        // V (scale, zero) per token and V group (at most 4 groups)
 };
 
-template <int BITS, int GQ>
+constexpr int AFR_LD = 36;  // padded row: the lanes' stores of one register row hit distinct banks
+
+template <int BITS, int GQ, int NWARP = nwarp_of<BITS>()>
 struct QMSmem {
     float qs[GQ][D];                  // the query heads of the kv group (fp32)
     float m[NWARP][GQ], l[NWARP][GQ];
-    uint32_t afr[NWARP][16][32];      // per warp: the scores' A fragments, [register][lane]
+    uint32_t afr[NWARP][16][AFR_LD];  // per warp: the scores' A fragments, [register][lane]
     union {
         GroupStage<BITS> st[NWARP][2];
         float ro[NWARP][GQ][D];       // per warp: unnormalised outputs, after the last group
@@ -205,7 +230,8 @@ __device__ __forceinline__ void stage_group(const QAttnArgs& a, GroupStage<BITS>
 }
 
 template <int BITS, int GQ>
-__global__ void __launch_bounds__(NT, 4) qmma_kernel(QAttnArgs a) {
+__global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArgs a) {
+    constexpr int NWARP = nwarp_of<BITS>(), NT = 32 * NWARP;
     static_assert(GQ <= 4, "at most four query heads per grid kv group");
     extern __shared__ __align__(16) unsigned char smraw[];
     QMSmem<BITS, GQ>& S = *reinterpret_cast<QMSmem<BITS, GQ>*>(smraw);
@@ -237,7 +263,7 @@ __global__ void __launch_bounds__(NT, 4) qmma_kernel(QAttnArgs a) {
 
     for (int i = tid; i < GQ * D; i += NT) S.qs[i / D][i % D] = kvq_h2f(a.q[((int64_t)b * Hq + gv * GQ) * D + i]);
     // A-fragment rows of absent heads (fewer than four) stay zero
-    for (int i = tid; i < NWARP * 16 * 32; i += NT) (&S.afr[0][0][0])[i] = 0u;
+    for (int i = tid; i < NWARP * 16 * AFR_LD; i += NT) (&S.afr[0][0][0])[i] = 0u;
     __syncthreads();
 
     float acc[8][4];
@@ -245,7 +271,6 @@ __global__ void __launch_bounds__(NT, 4) qmma_kernel(QAttnArgs a) {
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[mt][i] = 0.0f;
-    float zt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     float mrun = -INFINITY, lrun = 0.0f;
     const int hs = g8 >> 1;  // the head of this lane's score rows (slot g8 = 2 hs + hi/lo)
 
@@ -273,18 +298,26 @@ __global__ void __launch_bounds__(NT, 4) qmma_kernel(QAttnArgs a) {
             const int h = k >> 1, s = (u >> 3) & 7, i = (u >> 2) & 1, r = u & 3;
             const int c = 16 * s + 8 * i + 2 * r;
             const float2 qv = *reinterpret_cast<const float2*>(&S.qs[h][c]);
-            float a0 = qv.x, a1 = qv.y;  // q_c scale_c: a product of two fp16 numbers, exact in fp32
+            // complete group: a_c = q_c scale_c 2^BITS (q, scale fp16: exact in fp32) against the
+            // codes' 1 + code / 2^BITS; the unfinished group: a_c = q_c against fp16 keys
+            float a0 = qv.x, a1 = qv.y;
             if (packed) {
                 const float2 sz0 = unpack_h2(st.ksz[c]), sz1 = unpack_h2(st.ksz[c + 1]);
-                a0 *= sz0.x;
-                a1 *= sz1.x;
+                a0 *= sz0.x * (float)(1 << BITS);
+                a1 *= sz1.x * (float)(1 << BITS);
                 c0p[h] = fmaf(qv.x, sz0.y, c0p[h]);
                 c0p[h] = fmaf(qv.y, sz1.y, c0p[h]);
             }
+            if (!(fabsf(a0) < 32768.0f && fabsf(a1) < 32768.0f)) kvq_dev_flag(a.hdr, KVQ_DEV_RANGE, b);
             const uint32_t hi = pack_h2(a0, a1);
             const float2 hf = unpack_h2(hi);
+            const uint32_t lo = pack_h2(a0 - hf.x, a1 - hf.y);
+            if (packed) {  // minus the bias: sum_c of the operand as the tensor cores see it
+                const float2 lf = unpack_h2(lo);
+                c0p[h] -= (hf.x + lf.x) + (hf.y + lf.y);
+            }
             S.afr[warp][2 * s + i][4 * (2 * h) + r] = hi;
-            S.afr[warp][2 * s + i][4 * (2 * h + 1) + r] = pack_h2(a0 - hf.x, a1 - hf.y);
+            S.afr[warp][2 * s + i][4 * (2 * h + 1) + r] = lo;
         }
         float c0 = 0.0f;
 #pragma unroll
@@ -359,46 +392,34 @@ __global__ void __launch_bounds__(NT, 4) qmma_kernel(QAttnArgs a) {
             acc[mt][0] *= aq;
             acc[mt][2] *= aq;
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) zt[j] *= alpha;
 
-        // ---- values, page by page: B column g8 = 2h carries fp16(p vscale) of head h, odd columns 0
+        // ---- values, page by page: the A operand is the dequantized V, fp16(vscale code + vzero)
+        // (the codes' pair at tokens 2q4, 2q4 + 1 and 2q4 + 8, 2q4 + 9 of the page, channels g8 and
+        // g8 + 8 of the m-tile); the B column g8 = 2h carries fp16(p) of head h, odd columns 0
         const bool even = (g8 & 1) == 0;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-            const float pv[4] = {sc[2 * ks][0], sc[2 * ks][1], sc[2 * ks + 1][0], sc[2 * ks + 1][1]};
-            int tk[4];
-            tk[0] = 2 * q4;
-            tk[1] = 2 * q4 + 1;
-            tk[2] = 2 * q4 + 8;
-            tk[3] = 2 * q4 + 9;
-            uint32_t bv[4][2];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                bv[j][0] = bv[j][1] = 0u;
-                if (j >= NGV) continue;
-                float pp[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const bool valid = t0 + 16 * ks + tk[e] < T;  // masked tokens may hold any scale
-                    const float2 sz = unpack_h2(st.vsz[(16 * ks + tk[e]) * NGV + j]);
-                    pp[e] = valid ? pv[e] * sz.x : 0.0f;
-                    zt[j] = valid ? fmaf(pv[e], sz.y, zt[j]) : zt[j];
-                }
-                if (even) {
-                    bv[j][0] = pack_h2(pp[0], pp[1]);
-                    bv[j][1] = pack_h2(pp[2], pp[3]);
-                }
-            }
+            const uint32_t b0 = even ? pack_h2(sc[2 * ks][0], sc[2 * ks][1]) : 0u;
+            const uint32_t b1 = even ? pack_h2(sc[2 * ks + 1][0], sc[2 * ks + 1][1]) : 0u;
+            const int tb = 16 * ks + 2 * q4;  // the lane's first token in the group
+            const int nv = T - t0 - tb;       // tokens tb, tb + 1 valid if > 0, > 1; tb + 8, + 9 if > 8, > 9
             const uint32_t* vblk = st.v + ks * 64 * BITS;
+            for (int j = 0; j < NGV; ++j) {  // V group j: m-tiles [8j / NGV, 8(j + 1) / NGV)
+                // (scale, zero) words of the lane's tokens; masked tokens may hold anything: zero them
+                const uint32_t w0 = nv > 0 ? st.vsz[tb * NGV + j] : 0u;
+                const uint32_t w1 = nv > 1 ? st.vsz[(tb + 1) * NGV + j] : 0u;
+                const uint32_t w2 = nv > 8 ? st.vsz[(tb + 8) * NGV + j] : 0u;
+                const uint32_t w3 = nv > 9 ? st.vsz[(tb + 9) * NGV + j] : 0u;
+                const uint32_t s01 = prmt(w0, w1, 0x5410u), z01 = prmt(w0, w1, 0x7632u);
+                const uint32_t s23 = prmt(w2, w3, 0x5410u), z23 = prmt(w2, w3, 0x7632u);
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                const int j = (mt * NGV) >> 3;  // V group of channels 16mt .. 16mt + 15
-                const uint32_t b0 = j == 0 ? bv[0][0] : j == 1 ? bv[1][0] : j == 2 ? bv[2][0] : bv[3][0];
-                const uint32_t b1 = j == 0 ? bv[0][1] : j == 1 ? bv[1][1] : j == 2 ? bv[2][1] : bv[3][1];
-                uint32_t A[4];
-                v_pairs<BITS>(vblk + (8 * mt + g8) * BITS, q4, A);
-                mma16816(acc[mt], A[0], A[1], A[2], A[3], b0, b1);
+                for (int mt = 0; mt < 8; ++mt) {
+                    if (((mt * NGV) >> 3) != j) continue;  // uniform over the warp
+                    uint32_t A[4];
+                    v_pairs<BITS>(vblk + (8 * mt + g8) * BITS, q4, A);
+                    mma16816(acc[mt], hfma2(A[0], s01, z01), hfma2(A[1], s01, z01), hfma2(A[2], s23, z23),
+                             hfma2(A[3], s23, z23), b0, b1);
+                }
             }
         }
         __syncwarp();
@@ -406,25 +427,15 @@ __global__ void __launch_bounds__(NT, 4) qmma_kernel(QAttnArgs a) {
     }
     cp_wait<0>();
 
-    // ---- this warp's state per head: l and the zero terms summed over the head's four lanes
+    // ---- this warp's state per head: l summed over the head's four lanes
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 1);
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 2);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        zt[j] += __shfl_xor_sync(0xffffffffu, zt[j], 1);
-        zt[j] += __shfl_xor_sync(0xffffffffu, zt[j], 2);
-    }
-    float zq[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) zq[j] = __shfl_sync(0xffffffffu, zt[j], 8 * q4);
     __syncthreads();  // every warp is done with its stages: the union now holds the outputs
     if (q4 < GQ) {
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-            const int j = (mt * NGV) >> 3;
-            const float z = j == 0 ? zq[0] : j == 1 ? zq[1] : j == 2 ? zq[2] : zq[3];
-            S.u.ro[warp][q4][16 * mt + g8] = acc[mt][0] + z;
-            S.u.ro[warp][q4][16 * mt + g8 + 8] = acc[mt][2] + z;
+            S.u.ro[warp][q4][16 * mt + g8] = acc[mt][0];
+            S.u.ro[warp][q4][16 * mt + g8 + 8] = acc[mt][2];
         }
     }
     if (q4 == 0 && (g8 & 1) == 0 && hs < GQ) {
@@ -497,9 +508,9 @@ Plan plan_splits(const kvq_layout* L, const kvq_seqs* S) {
     const int n_groups = (std::max(S->max_len, 1) + KG - 1) / KG;
     const int gq = L->n_q_heads / L->n_kv_heads;
     const int64_t units = (int64_t)std::max(S->batch, 1) * L->n_kv_heads * kv_div_of(gq);
-    const int64_t target = 4LL * kvq_num_sms();  // resident CTAs to aim for (four per SM)
+    const int64_t target = kvq_num_sms();  // resident CTAs to aim for (one per SM)
     int splits = (int)std::max<int64_t>(1, (target + units - 1) / units);
-    int cps = std::max(NWARP, (n_groups + splits - 1) / splits);
+    int cps = std::max(4, (n_groups + splits - 1) / splits);
     cps = std::min(cps, n_groups);
     splits = (n_groups + cps - 1) / cps;
     return {splits, cps};
@@ -518,9 +529,10 @@ size_t ws_layout(const kvq_layout* L, const kvq_seqs* S, size_t* off_part, size_
 template <int BITS, int GQ>
 int launch_one(dim3 grid, cudaStream_t s, const QAttnArgs& a) {
     const int smem = (int)sizeof(QMSmem<BITS, GQ>);
+    static_assert(sizeof(QMSmem<BITS, 4>) <= 227 * 1024, "one CTA's stages fit in shared memory");
     const int st = kvq_prepare_kernel((const void*)qmma_kernel<BITS, GQ>, smem);
     if (st) return st;
-    const cudaError_t e = kvq_launch_pdl(qmma_kernel<BITS, GQ>, grid, dim3(NT), (size_t)smem, s, a);
+    const cudaError_t e = kvq_launch_pdl(qmma_kernel<BITS, GQ>, grid, dim3(32 * nwarp_of<BITS>()), (size_t)smem, s, a);
     if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant launch: %s", cudaGetErrorString(e));
     return KVQ_OK;
 }

@@ -142,8 +142,9 @@ extern "C" int kvq_check(void* ws, void* stream) {
     if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kvq_check: %s", cudaGetErrorString(e));
     if (hdr[0] != 0) {
         static const char* names[] = {"ok", "page id outside the pool", "token id outside the sequence",
-                                      "sequence length outside its bounds", "list capacity exceeded"};
-        const char* nm = (hdr[0] > 0 && hdr[0] <= 4) ? names[hdr[0]] : "unknown";
+                                      "sequence length outside its bounds", "list capacity exceeded",
+                                      "query times K scale beyond the fp16 range"};
+        const char* nm = (hdr[0] > 0 && hdr[0] <= 5) ? names[hdr[0]] : "unknown";
         int32_t zero[2] = {0, 0};
         e = cudaMemcpyAsync(ws, zero, sizeof(zero), cudaMemcpyHostToDevice, s);
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);

@@ -189,8 +189,13 @@ size_t kv_page_append_ws(void);
  * q: device fp16 [batch][H_q][d]; out: device fp32 [batch][H_q][d].
  * Packed tokens use dequantized K (zero + code*scale with the stored fp16
  * scale/zero); tail tokens use their fp16 keys exactly; V is dequantized.
- * fp32 accumulation; the context is split across CTAs and the partial
- * softmax states are merged by log-sum-exp.  An empty sequence gives 0.
+ * Both products run on the tensor cores with fp32 accumulation: q*scale
+ * enters as two fp16 halves (about 22 bits), the dequantized V rows and the
+ * softmax weights as fp16 (relative rounding 2^-11 per element, averaging
+ * out over the tokens).  |q_c * scale_c| * 2^bits must stay below 32768 (the
+ * fp16 operand range); otherwise the status word reports a range error and
+ * the output is not valid.  The context is split across CTAs and the
+ * partial softmax states are merged by log-sum-exp.  An empty sequence gives 0.
  * ws: kv_decode_attn_quant_ws(layout, seqs) bytes.
  * ---------------------------------------------------------------------- */
 int kv_decode_attn_quant(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
