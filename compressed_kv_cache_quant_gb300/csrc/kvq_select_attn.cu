@@ -261,6 +261,56 @@ __device__ __forceinline__ void score_finish(const float* acc, int p0, int lo, i
     }
 }
 
+// Second phase of the classification, one queued group of eight keys per lane (has = false:
+// none): entry = chunk offset << 8 | mask of the keys at or above bin b1 or outside the
+// candidate range.  Those above the bin or outside the range are kept (s.list), those in the
+// bin are candidates (s.v.w.cl, with their keys); both counts are reserved with one packed
+// atomic per warp (each stays below the chunk size < 65536: no carry between the halves).
+__device__ __forceinline__ void classify_group(bool has, uint32_t e, const uint32_t* keys, int lo, int cand_lo,
+                                               int cand_hi, uint32_t hi_thr, SXSmem& s, int lane) {
+    const int q0 = has ? (int)(e >> 8) : 0;
+    const uint32_t m = has ? (e & 0xffu) : 0u;
+    const uint4 ka = *reinterpret_cast<const uint4*>(keys + q0);
+    const uint4 kb = *reinterpret_cast<const uint4*>(keys + q0 + 4);
+    const uint32_t kk[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+    uint32_t fs = 0u, fc = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (!((m >> i) & 1u)) continue;
+        const int p = lo + q0 + i;
+        if (p < cand_lo || p >= cand_hi || kk[i] > hi_thr) fs |= 1u << i;
+        else fc |= 1u << i;
+    }
+    const uint32_t cnt = (uint32_t)__popc(fs) | ((uint32_t)__popc(fc) << 16);
+    uint32_t x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    const uint32_t tot = __shfl_sync(0xffffffffu, x, 31);
+    uint32_t bases = 0u;
+    if (lane == 0 && tot != 0u) bases = atomicAdd(&s.nsc, tot);
+    bases = __shfl_sync(0xffffffffu, bases, 0) + x - cnt;
+    uint32_t bs = bases & 0xffffu, bc = bases >> 16;
+    const uint32_t p0 = (uint32_t)(lo + q0);
+    while (fs) {
+        const int i = __ffs(fs) - 1;
+        fs &= fs - 1u;
+        if (bs < (uint32_t)CAP_S) s.list[bs] = p0 + i;
+        ++bs;
+    }
+    while (fc) {
+        const int i = __ffs(fc) - 1;
+        fc &= fc - 1u;
+        uint32_t key = kk[0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j) key = i == j ? kk[j] : key;
+        if (bc < (uint32_t)CAP_C) s.v.w.cl[bc] = ((unsigned long long)key << 32) | (p0 + i);
+        ++bc;
+    }
+}
+
 // Appends, in ballot order, the lanes with f set to list[*n] (capacity cap);
 // returns false if the list overflowed.
 template <typename V>
@@ -495,69 +545,48 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
             find_bin_from_top<H1 / NT>(s.v.gh, (uint32_t)k, s);  // ends with a barrier
             const uint32_t b1 = s.s_bin;
             uint32_t remaining = (uint32_t)k - s.s_above;
-            // ---- one pass, eight positions per lane: positions above digit 1 (and the sinks and
-            // window) are kept, ties on digit 1 are candidates; a warp reserves its slots in both
-            // lists with one atomic each and places its lanes by a packed exclusive scan
+            // ---- classification in two phases.  (1) Each lane tests its eight keys against the
+            // start of bin b1 (and its positions against the candidate range); the warp queues the
+            // lanes with a hit, about a third of them.  (2) Every 32 queued groups, one per lane,
+            // are split into kept positions (above bin b1, sinks, window) and candidates (in bin
+            // b1), with one packed atomic per warp for the slots of both lists.
             if (tid == 0) s.nsc = 0u;
             __syncthreads();
             const bool inner = lo >= cand_lo && hi <= cand_hi;  // no sink or window position here
-            for (int base = 0; base < n; base += 8 * NT) {      // bound uniform over the CTA
+            const uint32_t lo_thr = b1 << 20, hi_thr = lo_thr | 0xfffffu;
+            static_assert(2 * H2 >= NW * 64, "the warps' queues fit the free digit histograms");
+            uint32_t* wq = s.v.w.h2 + warp * 64;  // free until the candidates are broadcast
+            int nq = 0;                            // queued groups (uniform over the warp)
+            for (int base = 0; base + 256 * warp < n; base += 8 * NT) {  // uniform over the warp
                 const int q0 = base + 8 * tid;
-                uint4 ka = make_uint4(0u, 0u, 0u, 0u), kb = ka;
+                uint32_t m = 0u;
                 if (q0 < n) {  // q0 + 8 <= chunk_cap: both loads stay inside the key array
-                    ka = *reinterpret_cast<const uint4*>(keys + q0);
-                    kb = *reinterpret_cast<const uint4*>(keys + q0 + 4);
-                }
-                const uint32_t kk[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-                uint32_t fs = 0u, fc = 0u;
+                    const uint4 ka = *reinterpret_cast<const uint4*>(keys + q0);
+                    const uint4 kb = *reinterpret_cast<const uint4*>(keys + q0 + 4);
+                    const uint32_t kk[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t bin = kk[i] >> 20;
-                    fs |= (uint32_t)(bin > b1) << i;
-                    fc |= (uint32_t)(bin == b1) << i;
-                }
-                const uint32_t valid = (1u << min(max(n - q0, 0), 8)) - 1u;
-                if (!inner) {
-                    uint32_t in = 0u;
+                    for (int i = 0; i < 8; ++i) m |= (uint32_t)(kk[i] >= lo_thr) << i;
+                    if (!inner) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int p = lo + q0 + i;
-                        in |= (uint32_t)(p >= cand_lo && p < cand_hi) << i;
+                        for (int i = 0; i < 8; ++i) {
+                            const int p = lo + q0 + i;
+                            m |= (uint32_t)(p < cand_lo || p >= cand_hi) << i;
+                        }
                     }
-                    fs = (fs & in) | ~in;
-                    fc &= in;
+                    m &= (1u << min(n - q0, 8)) - 1u;
                 }
-                fs &= valid;
-                fc &= valid;
-                const uint32_t cnt = (uint32_t)__popc(fs) | ((uint32_t)__popc(fc) << 16);
-                uint32_t x = cnt;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-                    if (lane >= o) x += y;
-                }
-                const uint32_t tot = __shfl_sync(0xffffffffu, x, 31);
-                uint32_t bases = 0u;  // both counts stay below the chunk size < 65536: no carry
-                if (lane == 0 && tot != 0u) bases = atomicAdd(&s.nsc, tot);
-                bases = __shfl_sync(0xffffffffu, bases, 0) + x - cnt;
-                uint32_t bs = bases & 0xffffu, bc = bases >> 16;
-                const uint32_t p0 = (uint32_t)(lo + q0);
-                while (fs) {
-                    const int i = __ffs(fs) - 1;
-                    fs &= fs - 1u;
-                    if (bs < (uint32_t)CAP_S) s.list[bs] = p0 + i;
-                    ++bs;
-                }
-                while (fc) {
-                    const int i = __ffs(fc) - 1;
-                    fc &= fc - 1u;
-                    uint32_t key = kk[0];
-#pragma unroll
-                    for (int j = 1; j < 8; ++j) key = i == j ? kk[j] : key;
-                    if (bc < (uint32_t)CAP_C) s.v.w.cl[bc] = ((unsigned long long)key << 32) | (p0 + i);
-                    ++bc;
+                const uint32_t bal = __ballot_sync(0xffffffffu, m != 0u);
+                if (m != 0u) wq[nq + __popc(bal & ((1u << lane) - 1u))] = ((uint32_t)q0 << 8) | m;
+                nq += __popc(bal);
+                if (nq >= 32) {
+                    __syncwarp();
+                    nq -= 32;
+                    classify_group(true, wq[nq + lane], keys, lo, cand_lo, cand_hi, hi_thr, s, lane);
+                    __syncwarp();  // the drained slots are refilled
                 }
             }
+            __syncwarp();
+            if (nq > 0) classify_group(lane < nq, lane < nq ? wq[lane] : 0u, keys, lo, cand_lo, cand_hi, hi_thr, s, lane);
             __syncthreads();
             const int n_s0 = (int)(s.nsc & 0xffffu), n_c0 = (int)(s.nsc >> 16);
             // the rows of the positions kept so far (all but the candidates that will be kept)
