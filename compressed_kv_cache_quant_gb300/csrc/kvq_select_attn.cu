@@ -589,19 +589,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
             if (nq > 0) classify_group(lane < nq, lane < nq ? wq[lane] : 0u, keys, lo, cand_lo, cand_hi, hi_thr, s, lane);
             __syncthreads();
             const int n_s0 = (int)(s.nsc & 0xffffu), n_c0 = (int)(s.nsc >> 16);
-            // the rows of the positions kept so far (all but the candidates that will be kept)
-            // are pulled into L2 while the candidates are resolved; their pages are looked up first
-            const bool pf = a.q != nullptr;
-            const int n_pf = pf ? min(n_s0, CAP_S) : 0;
-            static_assert(CAP_S == 2 * NT, "two prefetched rows per thread");
-            uint32_t pf_t[2];
-            int32_t pf_pg[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int i = tid + j * NT;
-                pf_t[j] = i < n_pf ? s.list[i] : 0u;
-                pf_pg[j] = i < n_pf ? a.bt[(int64_t)b * a.max_blocks + (pf_t[j] >> 4)] : -1;
-            }
             // ---- every CTA's candidates (key bits 19..0) go to its slots in every CTA; the
             // target's local histogram is no longer read (see the cluster barrier above)
             {
@@ -622,16 +609,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
             if (tid == 0) {
                 s.n_s = n_s0;
                 s.n_c = n_c0;
-            }
-            {
-                const int g = h / a.GQ;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    if (pf_pg[j] < 0 || pf_pg[j] >= a.num_blocks) continue;
-                    const int64_t off = (((int64_t)pf_pg[j] * a.H + g) * PG + (pf_t[j] & 15)) * D;
-                    prefetch_row_l2(a.k16 + off);
-                    prefetch_row_l2(a.v16 + off);
-                }
             }
             cluster.sync();
             if (a.hist != nullptr && rank == 0)  // read by all: clear it for the next layer
@@ -876,6 +853,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
             else kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, t);
         }
         rows[i] = r;
+        // every kept row goes to L2 now; the batches below then mostly hit L2
+        if (r < ROW_NEW) {
+            prefetch_row_l2(a.k16 + (int64_t)r * D);
+            prefetch_row_l2(a.v16 + (int64_t)r * D);
+        }
     }
     __syncthreads();
     const int hw = tid >> 4, l16 = tid & 15;
