@@ -79,7 +79,7 @@ class Clocks:
             self.path = os.path.join(out, f"clocks_bench_{os.getpid()}.csv")
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -295,7 +295,7 @@ def traffic_record(kernel):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)  # ~0.6 s timed: several clock samples
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--prompt", type=int, default=131072)
@@ -466,14 +466,7 @@ def main():
             "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp16 in / fp32 accumulate (1-bit codes in layer 0)", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "layers": args.layers, "q_heads": HQ, "kv_heads": HKV,
-                       "head_dim": D, "batch": 1, "prompt_tokens": args.prompt, "page_tokens": 16,
-                       "layer0": "1-bit K per-channel g64, V per-token g64",
-                       "sparse_layers": f"8 critical channels, top-K floor({RATIO} T), {N_SINK} sinks + "
-                                        f"{WINDOW} window",
-                       "l2": "inputs larger than L2: each step streams "
-                             f"{step_bytes / 1e9:.2f} GB", "parallelism": f"replicas x{world}",
-                       "cuda_graph": "one graph per step"},
+            "config": workload_config(args, world),
             "hbm_GBps_step": step_bytes * value / world / 1e9,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_src,
@@ -488,6 +481,17 @@ def main():
         dist.destroy_process_group()
 
 
+def workload_config(args, world):
+    """The workload description both arms print."""
+    step_bytes = algorithmic_bytes(args.prompt, args.layers)[0]
+    return {"workload": WORKLOAD, "layers": args.layers, "q_heads": HQ, "kv_heads": HKV,
+            "head_dim": D, "batch": 1, "prompt_tokens": args.prompt, "page_tokens": 16,
+            "layer0": "1-bit K per-channel g64, V per-token g64",
+            "sparse_layers": f"8 critical channels, top-K floor({RATIO} T), {N_SINK} sinks + {WINDOW} window",
+            "l2": f"inputs larger than L2: each step streams {step_bytes / 1e9:.2f} GB",
+            "parallelism": f"replicas x{world}", "cuda_graph": "one graph per step"}
+
+
 def run_reference(args, n_workers):
     """The reference arm: the CPU oracle on the same workload and metric."""
     pool = make_pool(n_workers)
@@ -495,27 +499,30 @@ def run_reference(args, n_workers):
     seed = synth.BASE_SEED + CONFIG_ID
     K0, V0 = synth.kv_rows(args.prompt, HKV, synth.mix(seed, 100), device="cpu")
     K1, V1 = synth.kv_rows(args.prompt, HKV, synth.mix(seed, 101), device="cpu")
-    qs = synth.normal((args.warmup + args.steps, 2, HQ, D), synth.mix(seed, 1), "cpu")
+    # every step is a bounded sample (~0.5 s of oracle work); at most 24 steps are timed so that
+    # any --steps finishes within minutes; the metric is 1 / (mean step time)
+    n_warm, n_time = min(args.warmup, 2), min(args.steps, 24)
+    qs = synth.normal((n_warm + n_time, 2, HQ, D), synth.mix(seed, 1), "cpu")
     sample = OracleSample(K0.numpy(), V0.numpy(), K1.numpy(), V1.numpy())
     del K0, V0, K1, V1
     times = []
-    for i in range(args.warmup + args.steps):
+    for i in range(n_warm + n_time):
         t_step, _, _ = sample.step_time(pool, qs[i, 0].numpy(), qs[i, 1].numpy(), args.layers)
-        if i >= args.warmup:
+        if i >= n_warm:
             times.append(t_step)
     sample.close()
     pool.close()
-    total = sum(times)
+    total = sum(times) * args.steps / n_time  # the K steps at the measured mean step time
     value = args.steps / total
     line = {"impl": "reference", "metric": "decode-attention steps/s (compressed KV, 128K context)",
             "value": value, "unit": "steps/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp64 attention / fp32 quantizer (oracle)", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "layers": args.layers, "q_heads": HQ, "kv_heads": HKV,
-                       "head_dim": D, "batch": 1, "prompt_tokens": args.prompt},
+            "config": workload_config(args, args.gpus),
             "cpu_baseline": {"value": value, "unit": "steps/s", "cores": n_workers, "kind": "oracle",
                              "sample": "per step: layer 0 and one sparse layer timed on the process pool, "
-                                       f"extrapolated to {args.layers} layers"},
+                                       f"extrapolated to {args.layers} layers; {n_time} steps timed "
+                                       f"after {n_warm} warm-up steps"},
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
