@@ -319,88 +319,106 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
             S.afr[warp][2 * s + i][4 * (2 * h) + r] = hi;
             S.afr[warp][2 * s + i][4 * (2 * h + 1) + r] = lo;
         }
-        float c0 = 0.0f;
+        float c0 = 0.0f;  // of head q4, the head of this lane's scores
 #pragma unroll
         for (int h = 0; h < GQ; ++h) {
             const float v = kvq_warp_sum(c0p[h]);
-            if (hs == h) c0 = v;
+            if (q4 == h) c0 = v;
         }
         __syncwarp();
         uint32_t af[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) af[r] = S.afr[warp][r][lane];
 
-        // ---- scores: 8 n-tiles of 8 tokens; this lane gets slot g8 of tokens 8nt + 2q4 + {0, 1}
-        float sc[8][2];
+        // ---- scores: the A operand is the codes (16 tokens x 16 channels per m-tile and k-step:
+        // tokens 16mt + g8 and + 8, channel pairs 2s and 2s + 1 of the lane's column), the B
+        // operand the fragments above (slot 2h: hi, 2h + 1: lo of head h); this lane gets
+        // head q4 of tokens 16mt + g8 (hi in d0, lo in d1) and 16mt + g8 + 8 (d2, d3)
+        float sc[4][2];
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
+        for (int mt = 0; mt < 4; ++mt) {
             float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             if (packed) {
-                const uint32_t* kr = st.k + (8 * nt + g8) * (4 * BITS) + q4 * BITS;
-                uint32_t kw[BITS];
+                const uint32_t* k0 = st.k + (16 * mt + g8) * (4 * BITS) + q4 * BITS;
+                const uint32_t* k1 = k0 + 8 * (4 * BITS);
+                uint32_t w0[BITS], w1[BITS];
 #pragma unroll
-                for (int u = 0; u < BITS; ++u) kw[u] = kr[u];
-                mma16816(d, af[0], 0u, af[1], 0u, k_pair<BITS, 0>(kw), k_pair<BITS, 1>(kw));
-                mma16816(d, af[2], 0u, af[3], 0u, k_pair<BITS, 2>(kw), k_pair<BITS, 3>(kw));
-                mma16816(d, af[4], 0u, af[5], 0u, k_pair<BITS, 4>(kw), k_pair<BITS, 5>(kw));
-                mma16816(d, af[6], 0u, af[7], 0u, k_pair<BITS, 6>(kw), k_pair<BITS, 7>(kw));
-                mma16816(d, af[8], 0u, af[9], 0u, k_pair<BITS, 8>(kw), k_pair<BITS, 9>(kw));
-                mma16816(d, af[10], 0u, af[11], 0u, k_pair<BITS, 10>(kw), k_pair<BITS, 11>(kw));
-                mma16816(d, af[12], 0u, af[13], 0u, k_pair<BITS, 12>(kw), k_pair<BITS, 13>(kw));
-                mma16816(d, af[14], 0u, af[15], 0u, k_pair<BITS, 14>(kw), k_pair<BITS, 15>(kw));
+                for (int u = 0; u < BITS; ++u) {
+                    w0[u] = k0[u];
+                    w1[u] = k1[u];
+                }
+#define KVQ_KSTEP(S)                                                                                       \
+    mma16816(d, k_pair<BITS, 2 * (S)>(w0), k_pair<BITS, 2 * (S)>(w1), k_pair<BITS, 2 * (S) + 1>(w0),       \
+             k_pair<BITS, 2 * (S) + 1>(w1), af[2 * (S)], af[2 * (S) + 1])
+                KVQ_KSTEP(0);
+                KVQ_KSTEP(1);
+                KVQ_KSTEP(2);
+                KVQ_KSTEP(3);
+                KVQ_KSTEP(4);
+                KVQ_KSTEP(5);
+                KVQ_KSTEP(6);
+                KVQ_KSTEP(7);
+#undef KVQ_KSTEP
             } else {
                 // the unfinished group: fp16 keys (rows t mod 64 of the tail buffer), q unscaled
-                const uint32_t* kr = reinterpret_cast<const uint32_t*>(
-                    a.k_tail + (((int64_t)b * a.H + gk) * KG + 8 * nt + g8) * D + 2 * q4);
+                const uint32_t* k0 = reinterpret_cast<const uint32_t*>(
+                    a.k_tail + (((int64_t)b * a.H + gk) * KG + 16 * mt + g8) * D + 2 * q4);
+                const uint32_t* k1 = k0 + 8 * D / 2;
 #pragma unroll
-                for (int s = 0; s < 8; ++s) mma16816(d, af[2 * s], 0u, af[2 * s + 1], 0u, kr[8 * s], kr[8 * s + 4]);
+                for (int s = 0; s < 8; ++s)
+                    mma16816(d, k0[8 * s], k1[8 * s], k0[8 * s + 4], k1[8 * s + 4], af[2 * s], af[2 * s + 1]);
             }
-            sc[nt][0] = d[0];
-            sc[nt][1] = d[1];
+            sc[mt][0] = d[0] + d[1];
+            sc[mt][1] = d[2] + d[3];
         }
 
-        // ---- online softmax per head (log2 domain); the hi and lo slots are summed first
+        // ---- online softmax of head q4 (log2 domain) over the group's 64 tokens: eight per lane
         float gm = -INFINITY;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const float x = sc[nt][e] + __shfl_xor_sync(0xffffffffu, sc[nt][e], 4);
-                const int t = t0 + 8 * nt + 2 * q4 + e;
-                sc[nt][e] = t < T ? (x + c0) * KVQ_SCORE_LOG2_SCALE : -INFINITY;
-                gm = fmaxf(gm, sc[nt][e]);
+                const int t = t0 + 16 * mt + g8 + 8 * e;
+                sc[mt][e] = t < T ? (sc[mt][e] + c0) * KVQ_SCORE_LOG2_SCALE : -INFINITY;
+                gm = fmaxf(gm, sc[mt][e]);
             }
-        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
-        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 16));
         const float mn = fmaxf(mrun, gm);
         const float alpha = mn == -INFINITY ? 1.0f : exp2f(mrun - mn);
         float ls = 0.0f;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const float p = mn == -INFINITY ? 0.0f : exp2f(sc[nt][e] - mn);
-                sc[nt][e] = p;
+                const float p = mn == -INFINITY ? 0.0f : exp2f(sc[mt][e] - mn);
+                sc[mt][e] = p;
                 ls += p;
             }
         mrun = mn;
         lrun = fmaf(lrun, alpha, ls);
-        // the accumulator columns belong to head q4
-        const float aq = __shfl_sync(0xffffffffu, alpha, 8 * q4);
+        // the accumulator columns belong to head q4 too
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-            acc[mt][0] *= aq;
-            acc[mt][2] *= aq;
+            acc[mt][0] *= alpha;
+            acc[mt][2] *= alpha;
         }
 
         // ---- values, page by page: the A operand is the dequantized V, fp16(vscale code + vzero)
         // (the codes' pair at tokens 2q4, 2q4 + 1 and 2q4 + 8, 2q4 + 9 of the page, channels g8 and
         // g8 + 8 of the m-tile); the B column g8 = 2h carries fp16(p) of head h, odd columns 0
-        const bool even = (g8 & 1) == 0;
+        const bool even = (g8 & 1) == 0 && hs < GQ;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t b0 = even ? pack_h2(sc[2 * ks][0], sc[2 * ks][1]) : 0u;
-            const uint32_t b1 = even ? pack_h2(sc[2 * ks + 1][0], sc[2 * ks + 1][1]) : 0u;
+            // p of head hs at the page's tokens 2q4, 2q4 + 1, 2q4 + 8, 2q4 + 9: token y sits in lane
+            // 4 (y mod 8) + hs, register e = y / 8 of m-tile ks
+            const float p0 = __shfl_sync(0xffffffffu, sc[ks][0], 8 * q4 + hs);
+            const float p1 = __shfl_sync(0xffffffffu, sc[ks][0], 8 * q4 + 4 + hs);
+            const float p2 = __shfl_sync(0xffffffffu, sc[ks][1], 8 * q4 + hs);
+            const float p3 = __shfl_sync(0xffffffffu, sc[ks][1], 8 * q4 + 4 + hs);
+            const uint32_t b0 = even ? pack_h2(p0, p1) : 0u;
+            const uint32_t b1 = even ? pack_h2(p2, p3) : 0u;
             const int tb = 16 * ks + 2 * q4;  // the lane's first token in the group
             const int nv = T - t0 - tb;       // tokens tb, tb + 1 valid if > 0, > 1; tb + 8, + 9 if > 8, > 9
             const uint32_t* vblk = st.v + ks * 64 * BITS;
@@ -427,9 +445,10 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
     }
     cp_wait<0>();
 
-    // ---- this warp's state per head: l summed over the head's four lanes
-    lrun += __shfl_xor_sync(0xffffffffu, lrun, 1);
-    lrun += __shfl_xor_sync(0xffffffffu, lrun, 2);
+    // ---- this warp's state per head: l summed over the head's eight lanes (g8)
+    lrun += __shfl_xor_sync(0xffffffffu, lrun, 4);
+    lrun += __shfl_xor_sync(0xffffffffu, lrun, 8);
+    lrun += __shfl_xor_sync(0xffffffffu, lrun, 16);
     __syncthreads();  // every warp is done with its stages: the union now holds the outputs
     if (q4 < GQ) {
 #pragma unroll
@@ -438,9 +457,9 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
             S.u.ro[warp][q4][16 * mt + g8 + 8] = acc[mt][2];
         }
     }
-    if (q4 == 0 && (g8 & 1) == 0 && hs < GQ) {
-        S.m[warp][hs] = mrun;
-        S.l[warp][hs] = lrun;
+    if (g8 == 0 && q4 < GQ) {
+        S.m[warp][q4] = mrun;
+        S.l[warp][q4] = lrun;
     }
     __syncthreads();
 

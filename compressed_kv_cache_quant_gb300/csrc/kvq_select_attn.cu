@@ -920,9 +920,19 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
             }
         }
     }
-    // the union buffer is free again: it holds the half-warp states
+    // the two half-warps of a warp merge in registers (lanes l and l ^ 16 hold the same channels)
     {
-        float* r = s.v.scratch + hw * REC;
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, 16), l2 = __shfl_xor_sync(0xffffffffu, l, 16);
+        const float mm = fmaxf(m, m2);
+        const float w1 = mm == -INFINITY ? 0.0f : exp2f(m - mm), w2 = mm == -INFINITY ? 0.0f : exp2f(m2 - mm);
+        l = l * w1 + l2 * w2;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = o[i] * w1 + __shfl_xor_sync(0xffffffffu, o[i], 16) * w2;
+        m = mm;
+    }
+    // the union buffer is free again: it holds the warp states
+    if (lane < 16) {
+        float* r = s.v.scratch + warp * REC;
         if (l16 == 0) {
             r[0] = m;
             r[1] = l;
@@ -934,10 +944,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     SXSmem* r0 = cluster.map_shared_rank(&s, 0);
     if (tid < D) {
         float M = -INFINITY;
-        for (int w = 0; w < NHW; ++w) M = fmaxf(M, s.v.scratch[w * REC]);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, s.v.scratch[w * REC]);
         float L = 0.0f, O = 0.0f;
         if (M != -INFINITY) {
-            for (int w = 0; w < NHW; ++w) {
+            for (int w = 0; w < NW; ++w) {
                 const float wt = exp2f(s.v.scratch[w * REC] - M);
                 L = fmaf(s.v.scratch[w * REC + 1], wt, L);
                 O = fmaf(s.v.scratch[w * REC + 4 + tid], wt, O);
