@@ -183,7 +183,7 @@ constexpr int AFR_LD = 36;  // padded row: the lanes' stores of one register row
 
 template <int BITS, int GQ, int NWARP = nwarp_of<BITS>()>
 struct QMSmem {
-    float qs[GQ][D];                  // the query heads of the kv group (fp32)
+    float qs[GQ][D];                  // the query heads of the kv group times 2^BITS (fp32)
     float m[NWARP][GQ], l[NWARP][GQ];
     uint32_t afr[NWARP][16][AFR_LD];  // per warp: the scores' A fragments, [register][lane]
     union {
@@ -194,42 +194,45 @@ struct QMSmem {
 
 // Issues the cp.async copies of group gi into st (one warp); pages past the sequence are
 // skipped (their tokens are masked), complete groups also bring their K rows and scales.
-template <int BITS>
+// Lane i < 4: the block-table entry of page i of group gi (-1 past the sequence), loaded an
+// iteration before stage_group needs it.
+__device__ __forceinline__ int32_t group_page(const QAttnArgs& a, int b, int gi, int n_pages, int lane) {
+    const int lp = 4 * gi + lane;
+    return lane < 4 && lp < n_pages ? a.bt[(int64_t)b * a.max_blocks + lp] : -1;
+}
+
+template <int BITS, int NGV>
 __device__ __forceinline__ void stage_group(const QAttnArgs& a, GroupStage<BITS>& st, int b, int gk, int gi,
-                                            int n_full, int n_pages, int NGV, int lane) {
-    int32_t pg = -1;
-    if (lane < 4) {
-        const int lp = 4 * gi + lane;
-        if (lp < n_pages) {
-            pg = a.bt[(int64_t)b * a.max_blocks + lp];
-            if (pg < 0 || pg >= a.num_blocks) {
-                kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
-                pg = 0;
-            }
-        }
+                                            int n_full, int32_t pg, int lane) {
+    if (lane < 4 && pg != -1 && (pg < 0 || pg >= a.num_blocks)) {
+        kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
+        pg = 0;
     }
-    int32_t P[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) P[i] = __shfl_sync(0xffffffffu, pg, i);
+    const int32_t P0 = __shfl_sync(0xffffffffu, pg, 0), P1 = __shfl_sync(0xffffffffu, pg, 1);
+    const int32_t P2 = __shfl_sync(0xffffffffu, pg, 2), P3 = __shfl_sync(0xffffffffu, pg, 3);
     const bool packed = gi < n_full;
     constexpr int CH = 16 * BITS;  // 16-byte chunks per page of K rows, and per V page block
-    for (int c = lane; c < 4 * CH; c += 32) {
-        const int i = c / CH, r = c % CH;
-        if (P[i] < 0) continue;
-        const int64_t off = (((int64_t)P[i] * a.H + gk) * PG) * (16 * BITS) + 16 * r;
+#pragma unroll
+    for (int c0 = 0; c0 < 4 * CH; c0 += 32) {
+        const int c = c0 + lane, i = c / CH, r = c % CH;
+        const int32_t P = i == 0 ? P0 : i == 1 ? P1 : i == 2 ? P2 : P3;
+        if (c >= 4 * CH || P < 0) continue;
+        const int64_t off = (((int64_t)P * a.H + gk) * PG) * (16 * BITS) + 16 * r;
         if (packed) cp_async16(st.k + (i * CH + r) * 4, a.k_codes + off);
         cp_async16(st.v + (i * CH + r) * 4, a.v_codes + off);
     }
-    if (packed) cp_async16(st.ksz + 4 * lane, a.k_sz + ((int64_t)P[0] * a.H + gk) * D + 4 * lane);
-    const int vch = 4 * NGV;  // chunks of V scales per page
-    for (int c = lane; c < 4 * vch; c += 32) {
-        const int i = c / vch, r = c % vch;
-        if (P[i] < 0) continue;
-        cp_async16(st.vsz + i * 16 * NGV + 4 * r, a.v_sz + ((int64_t)P[i] * a.H + gk) * PG * NGV + 4 * r);
+    if (packed) cp_async16(st.ksz + 4 * lane, a.k_sz + ((int64_t)P0 * a.H + gk) * D + 4 * lane);
+    constexpr int VCH = 4 * NGV;  // chunks of V scales per page
+#pragma unroll
+    for (int c0 = 0; c0 < 4 * VCH; c0 += 32) {
+        const int c = c0 + lane, i = c / VCH, r = c % VCH;
+        const int32_t P = i == 0 ? P0 : i == 1 ? P1 : i == 2 ? P2 : P3;
+        if (c >= 4 * VCH || P < 0) continue;
+        cp_async16(st.vsz + i * 16 * NGV + 4 * r, a.v_sz + ((int64_t)P * a.H + gk) * PG * NGV + 4 * r);
     }
 }
 
-template <int BITS, int GQ>
+template <int BITS, int GQ, int NGV>  // NGV = 128 / v_group_dims V groups per token
 __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArgs a) {
     constexpr int NWARP = nwarp_of<BITS>(), NT = 32 * NWARP;
     static_assert(GQ <= 4, "at most four query heads per grid kv group");
@@ -259,9 +262,9 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
     }
     if (split >= nsplit_b) return;
     const int g_begin = split * a.cps, g_end = min(n_groups, g_begin + a.cps);
-    const int NGV = D / a.G;
 
-    for (int i = tid; i < GQ * D; i += NT) S.qs[i / D][i % D] = kvq_h2f(a.q[((int64_t)b * Hq + gv * GQ) * D + i]);
+    for (int i = tid; i < GQ * D; i += NT)  // q 2^BITS (exact): the codes enter as 1 + code / 2^BITS
+        S.qs[i / D][i % D] = kvq_h2f(a.q[((int64_t)b * Hq + gv * GQ) * D + i]) * (float)(1 << BITS);
     // A-fragment rows of absent heads (fewer than four) stay zero
     for (int i = tid; i < NWARP * 16 * AFR_LD; i += NT) (&S.afr[0][0][0])[i] = 0u;
     __syncthreads();
@@ -275,12 +278,13 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
     const int hs = g8 >> 1;  // the head of this lane's score rows (slot g8 = 2 hs + hi/lo)
 
     int gi = g_begin + warp, buf = 0;
-    if (gi < g_end) stage_group<BITS>(a, S.u.st[warp][0], b, gk, gi, n_full, n_pages, NGV, lane);
+    if (gi < g_end) stage_group<BITS, NGV>(a, S.u.st[warp][0], b, gk, gi, n_full, group_page(a, b, gi, n_pages, lane), lane);
     cp_commit();
+    int32_t pg_next = group_page(a, b, gi + NWARP, n_pages, lane);
     for (; gi < g_end; gi += NWARP) {
-        if (gi + NWARP < g_end)
-            stage_group<BITS>(a, S.u.st[warp][buf ^ 1], b, gk, gi + NWARP, n_full, n_pages, NGV, lane);
+        if (gi + NWARP < g_end) stage_group<BITS, NGV>(a, S.u.st[warp][buf ^ 1], b, gk, gi + NWARP, n_full, pg_next, lane);
         cp_commit();
+        pg_next = group_page(a, b, gi + 2 * NWARP, n_pages, lane);
         cp_wait<1>();
         __syncwarp();
         const GroupStage<BITS>& st = S.u.st[warp][buf];
@@ -300,22 +304,22 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
             const float2 qv = *reinterpret_cast<const float2*>(&S.qs[h][c]);
             // complete group: a_c = q_c scale_c 2^BITS (q, scale fp16: exact in fp32) against the
             // codes' 1 + code / 2^BITS; the unfinished group: a_c = q_c against fp16 keys
-            float a0 = qv.x, a1 = qv.y;
+            // (the query in shared memory is q 2^BITS: a power of two, exact)
+            float a0, a1;
             if (packed) {
                 const float2 sz0 = unpack_h2(st.ksz[c]), sz1 = unpack_h2(st.ksz[c + 1]);
-                a0 *= sz0.x * (float)(1 << BITS);
-                a1 *= sz1.x * (float)(1 << BITS);
-                c0p[h] = fmaf(qv.x, sz0.y, c0p[h]);
-                c0p[h] = fmaf(qv.y, sz1.y, c0p[h]);
+                a0 = qv.x * sz0.x;
+                a1 = qv.y * sz1.x;
+                // zero-point term minus the bias sum_c a_c (hi + lo misses a_c by < 2^-22 |a_c|)
+                c0p[h] += fmaf(qv.x, sz0.y, qv.y * sz1.y) * (1.0f / (float)(1 << BITS)) - (a0 + a1);
+            } else {
+                a0 = qv.x * (1.0f / (float)(1 << BITS));
+                a1 = qv.y * (1.0f / (float)(1 << BITS));
             }
             if (!(fabsf(a0) < 32768.0f && fabsf(a1) < 32768.0f)) kvq_dev_flag(a.hdr, KVQ_DEV_RANGE, b);
             const uint32_t hi = pack_h2(a0, a1);
             const float2 hf = unpack_h2(hi);
             const uint32_t lo = pack_h2(a0 - hf.x, a1 - hf.y);
-            if (packed) {  // minus the bias: sum_c of the operand as the tensor cores see it
-                const float2 lf = unpack_h2(lo);
-                c0p[h] -= (hf.x + lf.x) + (hf.y + lf.y);
-            }
             S.afr[warp][2 * s + i][4 * (2 * h) + r] = hi;
             S.afr[warp][2 * s + i][4 * (2 * h + 1) + r] = lo;
         }
@@ -422,6 +426,7 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
             const int tb = 16 * ks + 2 * q4;  // the lane's first token in the group
             const int nv = T - t0 - tb;       // tokens tb, tb + 1 valid if > 0, > 1; tb + 8, + 9 if > 8, > 9
             const uint32_t* vblk = st.v + ks * 64 * BITS;
+#pragma unroll
             for (int j = 0; j < NGV; ++j) {  // V group j: m-tiles [8j / NGV, 8(j + 1) / NGV)
                 // (scale, zero) words of the lane's tokens; masked tokens may hold anything: zero them
                 const uint32_t w0 = nv > 0 ? st.vsz[tb * NGV + j] : 0u;
@@ -432,7 +437,7 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
                 const uint32_t s23 = prmt(w2, w3, 0x5410u), z23 = prmt(w2, w3, 0x7632u);
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
-                    if (((mt * NGV) >> 3) != j) continue;  // uniform over the warp
+                    if (((mt * NGV) >> 3) != j) continue;  // resolved at compile time
                     uint32_t A[4];
                     v_pairs<BITS>(vblk + (8 * mt + g8) * BITS, q4, A);
                     mma16816(acc[mt], hfma2(A[0], s01, z01), hfma2(A[1], s01, z01), hfma2(A[2], s23, z23),
@@ -545,15 +550,25 @@ size_t ws_layout(const kvq_layout* L, const kvq_seqs* S, size_t* off_part, size_
     return kvq_round_up(*off_cnt + units * sizeof(int32_t), 256);
 }
 
-template <int BITS, int GQ>
+template <int BITS, int GQ, int NGV>
 int launch_one(dim3 grid, cudaStream_t s, const QAttnArgs& a) {
     const int smem = (int)sizeof(QMSmem<BITS, GQ>);
     static_assert(sizeof(QMSmem<BITS, 4>) <= 227 * 1024, "one CTA's stages fit in shared memory");
-    const int st = kvq_prepare_kernel((const void*)qmma_kernel<BITS, GQ>, smem);
+    const int st = kvq_prepare_kernel((const void*)qmma_kernel<BITS, GQ, NGV>, smem);
     if (st) return st;
-    const cudaError_t e = kvq_launch_pdl(qmma_kernel<BITS, GQ>, grid, dim3(32 * nwarp_of<BITS>()), (size_t)smem, s, a);
+    const cudaError_t e =
+        kvq_launch_pdl(qmma_kernel<BITS, GQ, NGV>, grid, dim3(32 * nwarp_of<BITS>()), (size_t)smem, s, a);
     if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant launch: %s", cudaGetErrorString(e));
     return KVQ_OK;
+}
+
+template <int BITS, int GQ>
+int launch_ngv(dim3 grid, cudaStream_t s, const QAttnArgs& a) {
+    switch (a.G) {
+        case 128: return launch_one<BITS, GQ, 1>(grid, s, a);
+        case 64: return launch_one<BITS, GQ, 2>(grid, s, a);
+        default: return launch_one<BITS, GQ, 4>(grid, s, a);  // 32 (the only other size accepted)
+    }
 }
 
 // grid: (splits, kv heads, batch); widened here to the grid kv groups
@@ -562,9 +577,9 @@ int launch_bits(int gq, dim3 grid, cudaStream_t s, QAttnArgs& a) {
     a.kv_div = kv_div_of(gq);
     grid.y *= a.kv_div;
     switch (grid_gq(gq)) {
-        case 1: return launch_one<BITS, 1>(grid, s, a);
-        case 2: return launch_one<BITS, 2>(grid, s, a);
-        default: return launch_one<BITS, 4>(grid, s, a);
+        case 1: return launch_ngv<BITS, 1>(grid, s, a);
+        case 2: return launch_ngv<BITS, 2>(grid, s, a);
+        default: return launch_ngv<BITS, 4>(grid, s, a);
     }
 }
 
