@@ -108,6 +108,7 @@ struct SXSmem {
     float st_m[CL], st_l[CL];               // rank 0: the CTAs' softmax states
     float st_o[CL][D];
     uint32_t eqr[CL];                       // candidates equal to the k-th key, per owner rank
+    uint32_t sml[32], nsm;                  // candidates sharing the second digit (short list)
     float qs[D];                            // fused scores: the query
     unsigned long long ck[D];               // channel importance key | (255 - channel)
     uint32_t crank[D];                      // its rank among the channels
@@ -609,6 +610,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
             if (tid == 0) {
                 s.n_s = n_s0;
                 s.n_c = n_c0;
+                s.nsm = 0u;
             }
             cluster.sync();
             if (a.hist != nullptr && rank == 0)  // read by all: clear it for the next layer
@@ -632,23 +634,66 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                 find_bin_from_top<H2 / NT>(s.v.w.h2, remaining, s);
                 remaining -= s.s_above;
                 const uint32_t d2 = s.s_bin;
+                // the candidates sharing digit 2 (usually a few) go to a short list: digit 3 << 3 |
+                // owner rank; up to 32 of them one warp finds digit 3 and the per-rank ties at it
 #pragma unroll
-                for (int j = 0; j < CL; ++j)
-                    if (((vm >> j) & 1u) && (cr[j] >> 10) == d2) atomicAdd(&s.v.w.h2b[cr[j] & (H2 - 1)], 1u);
+                for (int j = 0; j < CL; ++j) {
+                    if (((vm >> j) & 1u) && (cr[j] >> 10) == d2) {
+                        const uint32_t i = atomicAdd(&s.nsm, 1u);
+                        if (i < 32u) s.sml[i] = ((cr[j] & (H2 - 1)) << 3) | (uint32_t)j;
+                    }
+                }
+                if (tid == 0) s.bc_cut = 0x7fffffff;
                 __syncthreads();
-                find_bin_from_top<H2 / NT>(s.v.w.h2b, remaining, s);
-                remaining -= s.s_above;
-                const uint32_t d3 = s.s_bin;
+                const uint32_t nsm = s.nsm;
+                uint32_t d3;
+                if (nsm <= 32u) {
+                    if (warp == 0) {
+                        const bool valid = (uint32_t)lane < nsm;
+                        const uint32_t e = valid ? s.sml[lane] : 0u;
+                        const uint32_t v = e >> 3, own = e & (CL - 1);
+                        uint32_t gt = 0, eq = 0;
+                        for (uint32_t i = 0; i < nsm; ++i) {
+                            const uint32_t vi = __shfl_sync(0xffffffffu, v, i);
+                            gt += vi > v;
+                            eq += vi == v;
+                        }
+                        // the digit whose run holds the remaining-th largest: above it gt, with it eq
+                        const uint32_t hit = __ballot_sync(0xffffffffu, valid && gt < remaining && remaining <= gt + eq);
+                        const int src = __ffs(hit) - 1;  // hit != 0: remaining <= nsm entries
+                        const uint32_t dv = __shfl_sync(0xffffffffu, v, src), above = __shfl_sync(0xffffffffu, gt, src);
+#pragma unroll
+                        for (int r = 0; r < CL; ++r) {
+                            const uint32_t c = __popc(__ballot_sync(0xffffffffu, valid && v == dv && own == (uint32_t)r));
+                            if (lane == 0) s.eqr[r] = c;
+                        }
+                        if (lane == 0) {
+                            s.s_bin = dv;
+                            s.s_above = above;
+                        }
+                    }
+                    __syncthreads();
+                    remaining -= s.s_above;
+                    d3 = s.s_bin;
+                } else {  // many share digit 2 (ties): a third histogram pass
+#pragma unroll
+                    for (int j = 0; j < CL; ++j)
+                        if (((vm >> j) & 1u) && (cr[j] >> 10) == d2) atomicAdd(&s.v.w.h2b[cr[j] & (H2 - 1)], 1u);
+                    __syncthreads();
+                    find_bin_from_top<H2 / NT>(s.v.w.h2b, remaining, s);
+                    remaining -= s.s_above;
+                    d3 = s.s_bin;
+                    const uint32_t low3 = (d2 << 10) | d3;
+#pragma unroll
+                    for (int j = 0; j < CL; ++j)
+                        if (((vm >> j) & 1u) && cr[j] == low3) atomicAdd(&s.eqr[j], 1u);
+                    __syncthreads();
+                }
                 const uint32_t low = (d2 << 10) | d3;
                 kth = (b1 << 20) | low;
                 // ties at the k-th key: the `remaining` (>= 1) lowest positions among them are kept.
                 // Ranks own ascending position ranges, so this CTA keeps its own lowest
                 // remaining - (ties in lower ranks) of them, clamped to [0, its ties]
-#pragma unroll
-                for (int j = 0; j < CL; ++j)
-                    if (((vm >> j) & 1u) && cr[j] == low) atomicAdd(&s.eqr[j], 1u);
-                if (tid == 0) s.bc_cut = 0x7fffffff;
-                __syncthreads();
                 uint32_t eq_before = 0;
                 for (int r = 0; r < rank; ++r) eq_before += s.eqr[r];
                 const uint32_t eq_mine = s.eqr[rank];
