@@ -16,6 +16,8 @@ score writes and selected fp16 rows of layers 1-31).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvq|reference]
                   [--prompt T0] [--layers L] [--no-e2e] [--no-cpu-baseline]
+  python bench.py --rows    # the other rows (pack, INT4 batch attention, H2O step, offload
+                            # gather, tiny-config kernels), one JSON line each
 
 For N > 1 (torchrun) every rank runs an independent replica on its own GPU
 (the path has no cross-GPU exchange); value = all ranks' steps / max time.
@@ -303,7 +305,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-workers", type=int, default=0)
+    ap.add_argument("--rows", action="store_true",
+                    help="instead of the step: time the other hot-path rows on their configurations, one JSON line each")
     args = ap.parse_args()
+    if args.rows:
+        run_rows(args)
+        return
     assert args.warmup >= 1 and args.steps >= 1 and args.layers >= 2
 
     rank = int(os.environ.get("RANK", "0"))
@@ -479,6 +486,272 @@ def main():
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------ per-row measurements (--rows)
+#
+# The hot-path rows outside the headline step, each timed on its configuration with CUDA
+# events on the launching stream (inputs larger than L2 where the row streams memory), next
+# to a bounded single-threaded sample of the oracle doing the same work.
+
+def _ev_ms(torch, fn, stream, reps, warm=2):
+    torch.cuda.synchronize()  # inputs made on other streams are complete
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+    stream.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def _wall(fn):
+    t = time.perf_counter()
+    fn()
+    return time.perf_counter() - t
+
+
+def _paged(torch, kvq, lengths, device, seed):
+    """Block table over a shuffled allocator, one row per sequence."""
+    pages = [-(-int(T) // 16) for T in lengths]
+    alloc = kvq.Allocator(sum(pages) + 4, seed=seed)
+    mb = max(pages)
+    bt = torch.full((len(lengths), mb), -1, dtype=torch.int32)
+    for b, n in enumerate(pages):
+        bt[b, :n] = torch.tensor(alloc.alloc(n), dtype=torch.int32)
+    seqs = kvq.Batch(bt.to(device), torch.tensor([int(T) for T in lengths], dtype=torch.int32, device=device),
+                     max(int(T) for T in lengths))
+    return seqs, sum(pages) + 4, alloc
+
+
+def _row_line(row, config, value, unit, roof, cpu, extra=None):
+    line = {"row": row, "config": config, "value": value, "unit": unit, "roofline": roof, "cpu_baseline": cpu}
+    if extra:
+        line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
+def run_rows(args):
+    import numpy as np
+    import torch
+
+    from compressed_kv_cache_quant_gb300 import kvq, synth
+    from compressed_kv_cache_quant_gb300.build import build
+    from oracle import kvq_oracle as O
+    build()
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device)
+    sh = stream.cuda_stream
+    peak, peak_src = measured_peaks()
+    seed = synth.BASE_SEED
+
+    def hbm(achieved):
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": peak_src}
+
+    # a1 kv_quant_pack: one Qwen-1.5-14B-shaped layer, 40 kv heads x 131072 tokens, 1-bit, G 64
+    try:
+        T, H = args.prompt, 40
+        seqs, npg, _ = _paged(torch, kvq, [T], device, 3)
+        cache = kvq.LayerCache(H, H, 1, npg, 1, v_group_dims=64)
+        K, V = synth.kv_rows(T, H, synth.mix(seed + 5, 1), device=device)
+        ms = _ev_ms(torch, lambda: kvq.kv_quant_pack(cache, seqs, 0, 0, T, K, V, stream=sh), stream, 5)
+        nbytes = 2 * T * H * D * 2 + T * H * 48
+        k1, v1 = K[:, 0].cpu().numpy(), V[:, 0].cpu().numpy()
+        del K, V, cache
+        t = _wall(lambda: (O.pack_k(k1, 1), O.pack_v(v1, 1, 64)))
+        cpu_gbs = (T * D * 2 * 2 + T * 48) / t / 1e9
+        _row_line("a1 kv_quant_pack", f"40 kv heads x {T} tokens, 1-bit, K g64 / V G64 (one layer)",
+                  nbytes / (ms * 1e-3) / 1e9, "GB/s", hbm(nbytes / (ms * 1e-3) / 1e9),
+                  {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "sample": f"one kv head of the layer ({T} tokens), numpy"}, {"ms": ms, "bytes": nbytes})
+    except Exception as e:  # report and go on with the other rows
+        print(json.dumps({"row": "a1 kv_quant_pack", "error": repr(e)}), flush=True)
+    torch.cuda.empty_cache()
+
+    # a3 kv_decode_attn_quant, INT4 serving batch: 16 sequences, lengths U[4096, 32768], 32 heads MHA,
+    # K 4-bit g64, V 4-bit G 32; one layer
+    try:
+        B, H = 16, 32
+        lens = [int(x) for x in synth.lengths_uniform(B, 4096, 32768, seed + 2)]
+        seqs, npg, _ = _paged(torch, kvq, lens, device, 7)
+        cache = kvq.LayerCache(H, H, 4, npg, B, v_group_dims=32)
+        for b, T in enumerate(lens):
+            K, V = synth.kv_rows(T, H, synth.mix(seed + 2, 10 + b), device=device)
+            kvq.kv_quant_pack(cache, seqs, b, 0, T, K, V)  # same stream as K, V
+            if b == 0:
+                k0, v0 = K[:, 0].cpu().numpy(), V[:, 0].cpu().numpy()
+            del K, V
+        stream.synchronize()
+        q = synth.normal((B, H, D), synth.mix(seed + 2, 99), device)
+        out = torch.empty((B, H, D), device=device)
+        wsq = kvq.Workspace(kvq.kv_decode_attn_quant_ws(cache, seqs))
+        ms = _ev_ms(torch, lambda: kvq.kv_decode_attn_quant(cache, seqs, q, out, wsq, stream=sh), stream, 20)
+        kvq.kvq_check(wsq, stream=sh)
+        nbytes = sum(lens) * H * 152
+        pk, pv = O.pack_k(k0, 4), O.pack_v(v0, 4, 32)
+        q0 = q[0, :1].cpu().numpy()
+        t = _wall(lambda: O.decode_attn_quant(q0, [pk], [pv]))
+        cpu_gbs = lens[0] * 152 / t / 1e9
+        _row_line("a3 kv_decode_attn_quant (INT4 batch)",
+                  f"16 sequences, T ~ U[4096, 32768] (sum {sum(lens)}), 32 heads MHA, K 4-bit g64, V 4-bit G32",
+                  nbytes / (ms * 1e-3) / 1e9, "GB/s", hbm(nbytes / (ms * 1e-3) / 1e9),
+                  {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "sample": f"one (sequence, head) of {lens[0]} tokens, numpy fp64"}, {"ms": ms, "bytes": nbytes})
+        del cache
+    except Exception as e:
+        print(json.dumps({"row": "a3 kv_decode_attn_quant (INT4 batch)", "error": repr(e)}), flush=True)
+    torch.cuda.empty_cache()
+
+    # a6 + a7: H2O layer step: attention over the retained set (shared per kv head, probabilities
+    # out), then accumulate and evict; 8 sequences x 8 kv heads, T = 32768, budget 6553
+    try:
+        B, Hq, Hkv, T, budget, ns, w = 8, 32, 8, 32768, 6553, 4, 2048
+        G = Hq // Hkv
+        seqs, npg, _ = _paged(torch, kvq, [T] * B, device, 11)
+        cache = kvq.LayerCache(Hq, Hkv, 16, npg, B, t_cap=T)
+        rng = np.random.default_rng(5)
+        cap = budget + 2
+        ret = np.zeros((B, Hkv, cap), np.int32)
+        for b in range(B):
+            K, V = synth.kv_rows(T, Hkv, synth.mix(seed + 4, b), device=device)
+            kvq.kv_quant_pack(cache, seqs, b, 0, T, K, V)  # same stream as K, V
+            if b == 0:
+                k0, v0 = K[:, 0].cpu().numpy(), V[:, 0].cpu().numpy()
+            del K, V
+            for g in range(Hkv):
+                mid = rng.choice(np.arange(ns, T - w), size=budget - ns - w, replace=False)
+                ret[b, g, :budget] = rng.permutation(np.concatenate([np.arange(ns), mid, np.arange(T - w, T)]))
+        stream.synchronize()
+        retained = torch.from_numpy(ret).to(device)
+        counts = torch.full((B, Hkv), budget, dtype=torch.int32, device=device)
+        cum = torch.from_numpy(rng.random((B, Hkv, cap)).astype(np.float32)).to(device)
+        probs = torch.zeros((B, Hq, cap), device=device)
+        q = synth.normal((B, Hq, D), synth.mix(seed + 4, 99), device)
+        out = torch.empty((B, Hq, D), device=device)
+        wsa = kvq.Workspace(kvq.kv_sparse_attn_ws(cache, seqs, cap))
+        wsh = kvq.Workspace(kvq.kv_h2o_accumulate_ws())
+
+        def h2o_step():
+            kvq.kv_sparse_attn(cache, seqs, q, retained, counts, 1, out, probs, wsa, stream=sh)
+            kvq.kv_h2o_accumulate(cache, seqs, probs, retained, counts, cum, budget, ns, w, None, None, wsh,
+                                  stream=sh)
+        ms = _ev_ms(torch, h2o_step, stream, 20)
+        ms_attn = _ev_ms(torch, lambda: kvq.kv_sparse_attn(cache, seqs, q, retained, counts, 1, out, probs, wsa,
+                                                           stream=sh), stream, 20)
+        kvq.kvq_check(wsa, stream=sh)
+        kvq.kvq_check(wsh, stream=sh)
+        nbytes = B * Hkv * budget * 2 * D * 2 + B * Hkv * cap * 8 + B * Hq * cap * 4
+        r0 = ret[0, 0, :budget].copy()
+        qg = q[0, :G].cpu().numpy()
+        t = _wall(lambda: O.h2o_step(qg, k0, v0, r0, np.zeros(budget), T - 1, budget, ns, w))
+        cpu_ms = t * 1e3 * B * Hkv
+        _row_line("a6+a7 kv_sparse_attn + kv_h2o_accumulate (H2O layer step)",
+                  f"8 sequences x 8 kv heads (GQA 4), T = {T}, budget {budget} = {ns} + {w} + {budget - ns - w}",
+                  nbytes / (ms * 1e-3) / 1e9, "GB/s", hbm(nbytes / (ms * 1e-3) / 1e9),
+                  {"value": cpu_ms, "unit": "ms per layer step", "cores": 1, "kind": "oracle",
+                   "sample": "one (sequence, kv head) of the step, numpy fp64, times 64"},
+                  {"ms": ms, "ms_sparse_attn_only": ms_attn, "bytes": nbytes})
+        del cache
+    except Exception as e:
+        print(json.dumps({"row": "a6+a7 H2O layer step", "error": repr(e)}), flush=True)
+    torch.cuda.empty_cache()
+
+    # a9 kv_offload_gather: 40 heads x 3932 selected rows of 131072 from pinned host memory
+    try:
+        T, H, sel_n = args.prompt, 40, math.floor(RATIO * args.prompt)
+        K, V = synth.kv_rows(T, H, synth.mix(seed + 5, 2), n_out=0)
+        src_k = K.permute(1, 0, 2).contiguous().pin_memory()
+        src_v = V.permute(1, 0, 2).contiguous().pin_memory()
+        del K, V
+        rng = np.random.default_rng(9)
+        sel = np.stack([np.sort(rng.choice(T, size=sel_n, replace=False)) for _ in range(H)]).astype(np.int32)
+        sel_t = torch.from_numpy(sel).to(device)
+        cnt = torch.full((H,), sel_n, dtype=torch.int32, device=device)
+        npg = -(-sel_n // 16)
+        dk = torch.empty((npg, H, 16, D), dtype=torch.float16, device=device)
+        dv = torch.empty_like(dk)
+        wg = kvq.Workspace(kvq.kv_offload_gather_ws())
+        ms = _ev_ms(torch, lambda: kvq.kv_offload_gather(src_k.data_ptr(), src_v.data_ptr(), T * D, T, H, sel_t, cnt,
+                                                        dk, dv, wg, stream=sh), stream, 10)
+        kvq.kvq_check(wg, stream=sh)
+        nbytes = H * sel_n * 2 * D * 2
+        # the link's roofline: one contiguous pinned -> device copy of the same size
+        hsrc = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        ddst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        ms_copy = _ev_ms(torch, lambda: ddst.copy_(hsrc, non_blocking=True), stream, 10)
+        link = nbytes / (ms_copy * 1e-3) / 1e9
+        k0 = src_k[0].numpy()
+        t = _wall(lambda: O.offload_gather(k0, sel[0]))
+        cpu_gbs = sel_n * D * 2 / t / 1e9
+        ach = nbytes / (ms * 1e-3) / 1e9
+        _row_line("a9 kv_offload_gather", f"40 heads x {sel_n} of {T} fp16 K and V rows from pinned host memory",
+                  ach, "GB/s", {"bound": "host link", "achieved": ach, "peak": link, "unit": "GB/s",
+                                "frac": ach / link, "peak_source": "measured pinned->device cudaMemcpyAsync, same bytes"},
+                  {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "sample": "one head's K rows, numpy fancy indexing (host to host)"}, {"ms": ms, "bytes": nbytes})
+        del src_k, src_v, hsrc, ddst
+    except Exception as e:
+        print(json.dumps({"row": "a9 kv_offload_gather", "error": repr(e)}), flush=True)
+    torch.cuda.empty_cache()
+
+    # a4, a5, a6, a8 at the tiny configuration: 8 q / 2 kv heads, T = 4096 (latency-bound; microseconds)
+    try:
+        Hq, Hkv, T, ncrit, kk, ns, w = 8, 2, 4096, 8, 128, 4, 64
+        seqs, npg, _ = _paged(torch, kvq, [T], device, 13)
+        cache = kvq.LayerCache(Hq, Hkv, 16, npg, 1, t_cap=T)
+        K, V = synth.kv_rows(T, Hkv, synth.mix(seed, 1), device=device)
+        kvq.kv_quant_pack(cache, seqs, 0, 0, T, K, V)
+        q = synth.queries((1, Hq, D), synth.mix(seed, 2)).to(device)
+        crit = torch.empty((1, Hq, ncrit), dtype=torch.int32, device=device)
+        scores = torch.empty((1, Hq, T), device=device)
+        sel = torch.empty((1, Hq, ns + w + kk), dtype=torch.int32, device=device)
+        cnt = torch.empty((1, Hq), dtype=torch.int32, device=device)
+        out = torch.empty((1, Hq, D), device=device)
+        probs = torch.empty((1, Hq, ns + w + kk), device=device)
+        wt = kvq.Workspace(kvq.kv_topk_select_ws())
+        wa = kvq.Workspace(kvq.kv_sparse_attn_ws(cache, seqs, ns + w + kk))
+        Q = synth.queries((1, Hq, 32, D), synth.mix(seed, 41)).to(device)
+        P = torch.empty((1, Hq), device=device)
+        wd = kvq.Workspace(kvq.kv_dense_pref_score_ws(cache, seqs, 32))
+        us = {
+            "a4 kv_critical_score": 1e3 * _ev_ms(torch, lambda: kvq.kv_critical_score(cache, seqs, q, ncrit, crit, scores,
+                                                                                     stream=sh), stream, 50),
+            "a5 kv_topk_select": 1e3 * _ev_ms(torch, lambda: kvq.kv_topk_select(seqs, Hq, scores, kk, 0.0, ns, w, sel,
+                                                                               cnt, wt, stream=sh), stream, 50),
+            "a6 kv_sparse_attn": 1e3 * _ev_ms(torch, lambda: kvq.kv_sparse_attn(cache, seqs, q, sel, cnt, 0, out, probs,
+                                                                               wa, stream=sh), stream, 50),
+            "a8 kv_dense_pref_score": 1e3 * _ev_ms(torch, lambda: kvq.kv_dense_pref_score(cache, seqs, Q, 32, 128, P, wd,
+                                                                                         stream=sh), stream, 20),
+        }
+        for wsx in (wt, wa, wd):
+            kvq.kvq_check(wsx, stream=sh)
+        Kc, Vc = K.cpu().numpy(), V.cpu().numpy()
+        qn, Qn = q.cpu().numpy()[0], Q.cpu().numpy()[0]
+        am = [O.key_absmax(Kc[:, g]) for g in range(Hkv)]
+        chans = [O.critical_channels(qn[h], am[O.kv_head_of(h, Hq, Hkv)], ncrit) for h in range(Hq)]
+        sc = []
+        cpu = {
+            "a4 kv_critical_score": _wall(lambda: sc.extend(O.critical_scores(qn[h], Kc[:, O.kv_head_of(h, Hq, Hkv)],
+                                                                              chans[h]) for h in range(Hq))),
+            "a5 kv_topk_select": _wall(lambda: [O.topk_select(sc[h], kk, ns, w) for h in range(Hq)]),
+            "a6 kv_sparse_attn": _wall(lambda: [O.sparse_attn(qn[h], Kc[:, O.kv_head_of(h, Hq, Hkv)],
+                                                              Vc[:, O.kv_head_of(h, Hq, Hkv)],
+                                                              O.topk_select(sc[h], kk, ns, w)) for h in range(Hq)]),
+            "a8 kv_dense_pref_score": _wall(lambda: [O.dense_pref_score(Qn[h], Kc[:, O.kv_head_of(h, Hq, Hkv)], 128)
+                                                     for h in range(Hq)]),
+        }
+        for name, v in us.items():
+            _row_line(name, "8 q / 2 kv heads, T = 4096 (8 critical channels, K = 128 + 4 sinks + 64 window; "
+                            "dense preference over 32 recent queries, top-128)", v, "us",
+                      {"bound": "latency", "note": "tiny parity configuration: microseconds, no roofline target"},
+                      {"value": cpu[name] * 1e6, "unit": "us", "cores": 1, "kind": "oracle",
+                       "sample": "the same call on the CPU oracle, numpy"})
+    except Exception as e:
+        print(json.dumps({"row": "a4/a5/a6/a8 tiny", "error": repr(e)}), flush=True)
 
 
 def workload_config(args, world):
