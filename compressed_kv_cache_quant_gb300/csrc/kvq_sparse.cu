@@ -266,6 +266,7 @@ constexpr int SA_NT = 256;
 constexpr int SA_HW = SA_NT / 16;  // half-warps per CTA
 constexpr int SA_BATCH = 4;        // rows in flight per half-warp
 constexpr int SA_REC = 4 + D;
+constexpr int SA_MAX_RPS = 2048;   // rows per split: their offsets are resolved into shared memory
 
 struct SAArgs {
     const uint16_t* k16;
@@ -320,6 +321,33 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
     const int r_begin = split * a.rps, r_end = min(n, r_begin + a.rps);
     const int32_t* ids = a.sel + ((int64_t)b * n_lists + list) * a.sel_cap;
 
+    // the split's rows: ids and pages resolved up front into row offsets (in 128-element rows;
+    // ~0u for a bad id or page), four per thread in flight
+    uint32_t* roff = reinterpret_cast<uint32_t*>(sm + SA_HW * NH * SA_REC);
+    for (int i0 = r_begin + tid; i0 < r_end; i0 += 4 * SA_NT) {
+        int t[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * SA_NT;
+            t[u] = i < r_end ? ids[i] : -1;
+        }
+        int32_t pg[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            pg[u] = t[u] >= 0 && t[u] < T ? a.bt[(int64_t)b * a.max_blocks + (t[u] >> 4)] : -1;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * SA_NT;
+            if (i >= r_end) continue;
+            uint32_t r = 0xffffffffu;
+            if (t[u] < 0 || t[u] >= T) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_INDEX, t[u]);
+            else if (pg[u] < 0 || pg[u] >= a.num_blocks) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, t[u]);
+            else r = (uint32_t)(((int64_t)pg[u] * a.H + g) * PG + (t[u] & 15));
+            roff[i - r_begin] = r;
+        }
+    }
+    __syncthreads();
+
     float qv[NH][8];
 #pragma unroll
     for (int hh = 0; hh < NH; ++hh) {
@@ -336,7 +364,6 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[hh][i] = 0.0f;
     }
-    const int64_t head_stride = (int64_t)PG * D;
     // The loop bound is uniform over the CTA so that every lane reaches the shuffles.
     for (int it = r_begin; it < r_end; it += SA_HW * SA_BATCH) {
         uint4 kr[SA_BATCH], vr[SA_BATCH];
@@ -347,21 +374,12 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
             ok[j] = false;
             kr[j] = make_uint4(0u, 0u, 0u, 0u);
             vr[j] = make_uint4(0u, 0u, 0u, 0u);
-            if (i < r_end) {
-                const int t = ids[i];
-                if (t >= 0 && t < T) {
-                    const int32_t page = a.bt[(int64_t)b * a.max_blocks + (t >> 4)];
-                    if (page >= 0 && page < a.num_blocks) {
-                        const int64_t off = ((int64_t)page * a.H + g) * head_stride + (int64_t)(t & 15) * D + 8 * l16;
-                        kr[j] = __ldg(reinterpret_cast<const uint4*>(a.k16 + off));
-                        vr[j] = __ldg(reinterpret_cast<const uint4*>(a.v16 + off));
-                        ok[j] = true;
-                    } else if (l16 == 0) {
-                        kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, t);
-                    }
-                } else if (l16 == 0) {
-                    kvq_dev_flag(a.hdr, KVQ_DEV_BAD_INDEX, t);
-                }
+            const uint32_t r = i < r_end ? roff[i - r_begin] : 0xffffffffu;
+            if (r != 0xffffffffu) {
+                const int64_t off = (int64_t)r * D + 8 * l16;
+                kr[j] = __ldg(reinterpret_cast<const uint4*>(a.k16 + off));
+                vr[j] = __ldg(reinterpret_cast<const uint4*>(a.v16 + off));
+                ok[j] = true;
             }
         }
         float s[SA_BATCH][NH];
@@ -478,13 +496,25 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
     if (tid == 0) a.counters[(int64_t)b * n_lists + list] = 0;
     if (a.probs == nullptr) return;
     __syncthreads();
-    for (int hh = 0; hh < NH; ++hh) {
-        float* pr = a.probs + ((int64_t)b * Hq + h0 + hh) * a.sel_cap;
-        const float M = fin_m[hh], L = fin_l[hh];
-        for (int i = tid; i < n; i += SA_NT) {
-            const float sv = __ldcg(pr + i);
-            pr[i] = (L > 0.0f && sv != -INFINITY) ? exp2f(sv - M) / L : 0.0f;
-        }
+    // the stored scores become probabilities; every thread keeps 2 x NH loads in flight
+    float* pr0 = a.probs + ((int64_t)b * Hq + h0) * a.sel_cap;
+    for (int i0 = tid; i0 < n; i0 += 2 * SA_NT) {
+        float sv[2][NH];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh) {
+                const int i = i0 + u * SA_NT;
+                sv[u][hh] = i < n ? __ldcg(pr0 + (int64_t)hh * a.sel_cap + i) : -INFINITY;
+            }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh) {
+                const int i = i0 + u * SA_NT;
+                const float M = fin_m[hh], L = fin_l[hh];
+                if (i < n) pr0[(int64_t)hh * a.sel_cap + i] = (L > 0.0f && sv[u][hh] != -INFINITY) ? exp2f(sv[u][hh] - M) / L : 0.0f;
+            }
     }
 }
 
@@ -498,7 +528,7 @@ SAPlan sa_plan(const kvq_layout* L, const kvq_seqs* S, int32_t sel_cap, int per_
     const int64_t target = 3LL * kvq_num_sms();
     int splits = (int)std::max<int64_t>(1, (target + units - 1) / units);
     int rps = (std::max(sel_cap, 1) + splits - 1) / splits;
-    rps = std::max(64, (rps + 63) / 64 * 64);
+    rps = std::min(SA_MAX_RPS, std::max(64, (rps + 63) / 64 * 64));
     splits = (std::max(sel_cap, 1) + rps - 1) / rps;
     return {splits, rps};
 }
@@ -517,8 +547,9 @@ size_t sa_ws_layout(const kvq_layout* L, const kvq_seqs* S, int32_t sel_cap, siz
 
 template <int NH>
 int launch_sa(const SAArgs& a, dim3 grid, cudaStream_t s) {
-    const size_t smem = (size_t)SA_HW * NH * SA_REC * sizeof(float);
-    const int st = kvq_prepare_kernel((const void*)sparse_attn_kernel<NH>, (int)smem);
+    const size_t smem = (size_t)SA_HW * NH * SA_REC * sizeof(float) + (size_t)a.rps * sizeof(uint32_t);
+    const int st = kvq_prepare_kernel((const void*)sparse_attn_kernel<NH>,
+                                      (int)((size_t)SA_HW * NH * SA_REC * sizeof(float) + SA_MAX_RPS * sizeof(uint32_t)));
     if (st) return st;
     sparse_attn_kernel<NH><<<grid, SA_NT, smem, s>>>(a);
     return kvq_launch_status("kv_sparse_attn");
