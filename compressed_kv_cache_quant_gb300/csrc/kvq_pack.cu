@@ -144,64 +144,342 @@ struct PackArgs {
     int64_t stride_t;
 };
 
-// V: one CTA of 4 warps per (page, head) touched by the tokens; the page's block of codes is
-// assembled in shared memory (tokens outside the range keep their codes) and written back.
+// Codes without a division.  For scale > 0 the code is rint(fl(d / scale)) with d = fl(x - zero)
+// (the quotient can't pass the level count, so the clamp never binds).  v = fma(d, 1/scale,
+// 1.5 * 2^23) rounds the product to the nearest integer (ties to even) and leaves it in v's low
+// mantissa bits; fr = fma(d, 1/scale, 1.5 * 2^23 - v) is the product's distance to that integer.
+// Below 256 the product is within 2^-16 of d / scale and the IEEE quotient within 2^-17, so the
+// rounding agrees unless |fr| > 1/2 - 2^-15: those codes are redone with the division.  A word is
+// the sum of the v bit patterns shifted to their code offsets; the magic constant's share of that
+// sum is a per-word constant, subtracted once.  The pairs (lo, hi) of a word go through packed
+// fp32x2 arithmetic, which rounds each lane as the scalar instruction does.
+constexpr float PK_MAGIC = 12582912.0f;  // 1.5 * 2^23
+constexpr uint32_t PK_MAGIC_BITS = 0x4B400000u;
+constexpr uint64_t PK_MAGIC2 = 0x4B4000004B400000ull;
+constexpr float PK_NEAR = 0.499969482421875f;  // 1/2 - 2^-15
+constexpr int PK_KRS = 68;                     // words per staged K row (rows 4 banks apart)
+
 template <int BITS>
-__global__ void __launch_bounds__(128) pack_v_kernel(PackArgs a) {
-    constexpr int BW = 64 * BITS;  // words per page block
-    __shared__ uint32_t blk[BW];
-    const int64_t lp = a.t_start / PG + blockIdx.x;  // logical page
-    const int h = blockIdx.y;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int32_t page = a.bt_row[lp];
-    if (page < 0 || page >= a.pool.num_blocks) return;  // an invalid table entry skips the page
-    uint32_t* gblk = reinterpret_cast<uint32_t*>(a.pool.v_codes) + ((int64_t)page * a.H + h) * BW;
-    for (int w = threadIdx.x; w < BW; w += 128) blk[w] = gblk[w];
-    __syncthreads();
-    for (int tok = warp; tok < PG; tok += 4) {
-        const int64_t t = lp * PG + tok;
-        if (t < a.t_start || t >= a.t_start + a.n_tokens) continue;  // uniform over the warp
-        const int64_t i = t - a.t_start;
-        uint32_t codes[4];
-        quant_v_token<BITS>(a.v + i * a.stride_t + (int64_t)h * D, a.G,
-                            a.pool.v_sz + (((int64_t)page * a.H + h) * PG + tok) * (D / a.G), lane, codes);
-        put_v_codes<BITS>(blk, tok, lane, codes);
+__host__ __device__ constexpr uint32_t pk_word_bias() {
+    uint32_t c = 0u;
+    for (int sl = 0; sl < 16 / BITS; ++sl) c += (PK_MAGIC_BITS << (sl * BITS)) + (PK_MAGIC_BITS << (sl * BITS + 16));
+    return c;
+}
+
+__device__ __forceinline__ uint64_t pk_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void pk_unpack(uint64_t v, uint32_t& lo, uint32_t& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t pk_sub2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t pk_fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// Adds the codes of the two fp16 values of `xw` (low half at bit `off`, high half at off + 16);
+// mn2 and rcp2 hold (zero, 1/scale) of the two values as fp32 pairs.
+__device__ __forceinline__ void pk_acc2(uint32_t xw, uint64_t mn2, uint64_t rcp2, int off, uint32_t& acc, float& far) {
+    const __half2 h = *reinterpret_cast<const __half2*>(&xw);
+    const uint64_t d2 = pk_sub2(pk_pack(__low2float(h), __high2float(h)), mn2);
+    const uint64_t v2 = pk_fma2(d2, rcp2, PK_MAGIC2);
+    uint32_t flo, fhi, vlo, vhi;
+    pk_unpack(pk_fma2(d2, rcp2, pk_sub2(PK_MAGIC2, v2)), flo, fhi);
+    pk_unpack(v2, vlo, vhi);
+    far = fmaxf(far, fmaxf(fabsf(__uint_as_float(flo)), fabsf(__uint_as_float(fhi))));
+    acc += (vlo << off) + (vhi << (off + 16));
+}
+
+// The same code, one value: when its quotient is close to a tie, replaces the fast code in `acc`
+// by the one the IEEE division gives.
+template <int BITS>
+__device__ __forceinline__ void pk_fix(float x, float mn, float rcp, float sc, int off, uint32_t& acc) {
+    const float d = __fsub_rn(x, mn);
+    const float v = __fmaf_rn(d, rcp, PK_MAGIC);
+    if (fabsf(__fmaf_rn(d, rcp, __fsub_rn(PK_MAGIC, v))) > PK_NEAR) {
+        const uint32_t fast = __float_as_uint(v) - PK_MAGIC_BITS;
+        acc += (kvq_code(x, mn, sc, (float)((1 << BITS) - 1)) - fast) << off;
+    }
+}
+
+__device__ __forceinline__ __half2 pk_h2(uint32_t u) {
+    __half2 h;
+    memcpy(&h, &u, 4);
+    return h;
+}
+__device__ __forceinline__ uint32_t pk_u32(__half2 h) {
+    uint32_t u;
+    memcpy(&u, &h, 4);
+    return u;
+}
+
+// Channel d of the staged V tile sits at column d ^ 8 * (bit 5 of d): the four 16-channel rows
+// a warp reads at once then fall in distinct banks.
+__device__ __forceinline__ int pk_vcol(int d) { return d ^ (((d >> 5) & 1) << 3); }
+
+// One thread's share of a (64-token group, kv head) unit: 4 chunks of K rows and 2 of V token
+// pairs (16 bytes each); rows past the range read as zeros.
+struct PkRegs {
+    uint4 k[4], va[2], vb[2];
+};
+
+__device__ __forceinline__ void pk_load(const PackArgs& a, int gi, int h, int nv, int tid, PkRegs& r) {
+    const int c8 = 8 * (tid & 15), i0 = tid >> 4;
+    const uint16_t* ksrc = a.k + ((int64_t)gi * KG + i0) * a.stride_t + (int64_t)h * D + c8;
+    const uint16_t* vsrc = a.v + ((int64_t)gi * KG + 2 * i0) * a.stride_t + (int64_t)h * D + c8;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        r.k[k] = i0 + 16 * k < nv ? __ldg(reinterpret_cast<const uint4*>(ksrc + (int64_t)(16 * k) * a.stride_t)) : z;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint16_t* r0 = vsrc + (int64_t)(32 * k) * a.stride_t;
+        r.va[k] = 2 * i0 + 32 * k < nv ? __ldg(reinterpret_cast<const uint4*>(r0)) : z;
+        r.vb[k] = 2 * i0 + 32 * k + 1 < nv ? __ldg(reinterpret_cast<const uint4*>(r0 + a.stride_t)) : z;
+    }
+}
+
+// K rows as they are (row stride 68 words); V as token pairs, word (y, d) = tokens 2y, 2y+1 at d.
+__device__ __forceinline__ void pk_store(const PkRegs& r, uint32_t* kt, uint32_t* vp, int tid) {
+    const int c8 = 8 * (tid & 15), i0 = tid >> 4;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(kt + (i0 + 16 * k) * PK_KRS + (c8 >> 1)) = r.k[k];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint4 A = r.va[k], B = r.vb[k];
+        uint4 lo, hi;
+        lo.x = __byte_perm(A.x, B.x, 0x5410); lo.y = __byte_perm(A.x, B.x, 0x7632);
+        lo.z = __byte_perm(A.y, B.y, 0x5410); lo.w = __byte_perm(A.y, B.y, 0x7632);
+        hi.x = __byte_perm(A.z, B.z, 0x5410); hi.y = __byte_perm(A.z, B.z, 0x7632);
+        hi.z = __byte_perm(A.w, B.w, 0x5410); hi.w = __byte_perm(A.w, B.w, 0x7632);
+        uint32_t* row = vp + (i0 + 16 * k) * D;
+        *reinterpret_cast<uint4*>(row + pk_vcol(c8)) = lo;
+        *reinterpret_cast<uint4*>(row + pk_vcol(c8 + 4)) = hi;
+    }
+}
+
+__device__ __forceinline__ int pk_valid(const PackArgs& a, int gi) {
+    return (int)min((int64_t)KG, a.n_tokens - (int64_t)gi * KG);
+}
+
+// One CTA of 8 warps per (64-token group, kv head) of the range.
+//   1. K rows staged as-is (word p of a row = channels 2p, 2p+1); V rows staged as token pairs
+//      (word (y, d) = tokens 2y, 2y+1 at channel d, the pair order of the page layout).
+//   2. Statistics: K per channel (complete groups only), V per token and V group.
+//   3. Code words, each built whole by one thread straight from the layout: K word (r, q) of
+//      token i holds pairs p = 4m + r, m = q*16/b + slot; V word (8t + x, q) of page j holds
+//      channels 16t + 8u + x of token pairs r + 4e, m = 4r + 2e + u.  No atomics.
+// A page only partly covered keeps its other tokens' V codes; the keys of an unfinished group go
+// to the tail buffer.  An invalid table entry skips its page (for K: the group).
+template <int BITS>
+__global__ void __launch_bounds__(256) pack_group_kernel(PackArgs a) {
+    constexpr int WPR = 4 * BITS;  // K code words per token row
+    constexpr int BW = 64 * BITS;  // V code words per page block
+    constexpr int PER = 16 / BITS; // codes per half word
+    constexpr uint32_t CM = (1u << BITS) - 1u;
+    constexpr float LEV = (float)((1 << BITS) - 1);
+    constexpr uint32_t BIAS = pk_word_bias<BITS>();
+    extern __shared__ __align__(16) unsigned char pk_smem[];
+    uint32_t* kt = reinterpret_cast<uint32_t*>(pk_smem);        // [64][68]
+    uint32_t* vp = kt + KG * PK_KRS;                             // [32][128] token pairs
+    float4* kst = reinterpret_cast<float4*>(vp + (KG / 2) * D);  // [64] per channel pair
+    float4* vst = kst + D / 2;                                   // [32][4] per pair and group
+    float* ksc = reinterpret_cast<float*>(vst + (KG / 2) * 4);   // [128]
+    float* vsc = ksc + D;                                        // [64][4]
+    uint32_t* part = reinterpret_cast<uint32_t*>(vsc + KG * 4);  // [2][4][64] half2 min, max of K
+    uint32_t* vmm = part + 2 * 256;                              // [32][4][2] half2 min, max of V
+    __shared__ int32_t pages[4];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = a.G, gsh = __ffs(G) - 1, NGV = D >> gsh;
+    const int gi = blockIdx.x, h = blockIdx.y;
+    const int64_t t0 = a.t_start + (int64_t)gi * KG;  // a multiple of 64: page aligned
+    const int nv = pk_valid(a, gi);
+    const int npage = (nv + PG - 1) / PG;
+    if (tid < 4) {
+        int32_t pg = tid < npage ? a.bt_row[t0 / PG + tid] : -1;
+        pages[tid] = pg >= 0 && pg < a.pool.num_blocks ? pg : -1;
+    }
+    {  // ---- 1. staging
+        PkRegs rg;
+        pk_load(a, gi, h, nv, tid, rg);
+        pk_store(rg, kt, vp, tid);
     }
     __syncthreads();
-    for (int w = threadIdx.x; w < BW; w += 128) gblk[w] = blk[w];
+    const bool full = nv == KG;
+    const bool k_ok = full && pages[0] >= 0 && pages[1] >= 0 && pages[2] >= 0 && pages[3] >= 0;
+    // ---- 2. statistics
+    if (k_ok) {  // K: thread (quarter, pair) over 16 tokens
+        const int cp = tid & 63, qq = tid >> 6;
+        __half2 mn2 = pk_h2(0x7c007c00u), mx2 = pk_h2(0xfc00fc00u);
+#pragma unroll 4
+        for (int i = 16 * qq; i < 16 * qq + 16; ++i) {
+            const __half2 x2 = pk_h2(kt[i * PK_KRS + cp]);
+            mn2 = __hmin2(mn2, x2);
+            mx2 = __hmax2(mx2, x2);
+        }
+        part[qq * 64 + cp] = pk_u32(mn2);
+        part[256 + qq * 64 + cp] = pk_u32(mx2);
+    }
+    {  // V: warp w takes token pairs w + 8k (k < 4), lane = 4 channels; pairs past the range are zeros
+        __half2 mn2[4], mx2[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint4 w4 = *reinterpret_cast<const uint4*>(vp + (warp + 8 * k) * D + pk_vcol(4 * lane));
+            mn2[k] = __hmin2(__hmin2(pk_h2(w4.x), pk_h2(w4.y)), __hmin2(pk_h2(w4.z), pk_h2(w4.w)));
+            mx2[k] = __hmax2(__hmax2(pk_h2(w4.x), pk_h2(w4.y)), __hmax2(pk_h2(w4.z), pk_h2(w4.w)));
+        }
+        for (int o = 1; o < (G >> 2); o <<= 1) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                mn2[k] = __hmin2(mn2[k], pk_h2(__shfl_xor_sync(0xffffffffu, pk_u32(mn2[k]), o)));
+                mx2[k] = __hmax2(mx2[k], pk_h2(__shfl_xor_sync(0xffffffffu, pk_u32(mx2[k]), o)));
+            }
+        }
+        if ((lane & ((G >> 2) - 1)) == 0) {  // one lane per group: min and max of the pair
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                vmm[((warp + 8 * k) * 4 + (lane >> (gsh - 2))) * 2] = pk_u32(mn2[k]);
+                vmm[((warp + 8 * k) * 4 + (lane >> (gsh - 2))) * 2 + 1] = pk_u32(mx2[k]);
+            }
+        }
+    }
+    __syncthreads();
+    // scale, zero and 1/scale: thread e < 128 finishes K channel e, the others a V (token, group)
+    for (int e = tid; e < D + KG * NGV; e += 256) {
+        float mn, mx;
+        if (e < D) {
+            if (!k_ok) continue;
+            const int cp = e >> 1;
+            __half2 m2 = pk_h2(part[cp]), x2 = pk_h2(part[256 + cp]);
+#pragma unroll
+            for (int qq = 1; qq < 4; ++qq) {
+                m2 = __hmin2(m2, pk_h2(part[qq * 64 + cp]));
+                x2 = __hmax2(x2, pk_h2(part[256 + qq * 64 + cp]));
+            }
+            mn = (e & 1) ? __high2float(m2) : __low2float(m2);
+            mx = (e & 1) ? __high2float(x2) : __low2float(x2);
+        } else {
+            const int tg = e - D, tok = tg >> (7 - gsh), g = tg & (NGV - 1);
+            const uint32_t* mm = vmm + ((tok >> 1) * 4 + g) * 2;
+            const __half2 m2 = pk_h2(mm[0]), x2 = pk_h2(mm[1]);
+            mn = (tok & 1) ? __high2float(m2) : __low2float(m2);
+            mx = (tok & 1) ? __high2float(x2) : __low2float(x2);
+        }
+        const float sc = kvq_scale32(mn, mx, LEV);
+        const float rcp = sc > 0.0f ? 1.0f / sc : 0.0f;
+        if (e < D) {
+            float* ks4 = reinterpret_cast<float*>(kst + (e >> 1));  // {zero lo, zero hi, 1/sc lo, 1/sc hi}
+            ks4[e & 1] = mn;
+            ks4[2 + (e & 1)] = rcp;
+            ksc[e] = sc;
+            a.pool.k_sz[((int64_t)pages[0] * a.H + h) * D + e] = pack_sz(sc, mn);
+        } else {
+            const int tg = e - D, tok = tg >> (7 - gsh), g = tg & (NGV - 1);
+            float* vs4 = reinterpret_cast<float*>(vst + (tok >> 1) * 4 + g);  // {zero even, zero odd, 1/sc ..}
+            vs4[tok & 1] = mn;
+            vs4[2 + (tok & 1)] = rcp;
+            vsc[tok * 4 + g] = sc;
+            const int32_t pj = pages[tok / PG];
+            if (tok < nv && pj >= 0)
+                a.pool.v_sz[(((int64_t)pj * a.H + h) * PG + tok % PG) * NGV + g] = pack_sz(sc, mn);
+        }
+    }
+    if (!full) {  // the unfinished group: its keys go to the tail buffer (rows t mod 64 = i)
+        uint4* tail = reinterpret_cast<uint4*>(a.pool.k_tail + (((int64_t)a.seq * a.H + h) * KG) * D);
+        for (int u = tid; u < nv * 16; u += 256)
+            tail[u] = reinterpret_cast<const uint4*>(kt)[(u >> 4) * (PK_KRS / 4) + (u & 15)];
+    }
+    __syncthreads();
+    // ---- 3. code words: K words (r, q) of token 8w + lane/4, V words (8t + x, q) of page w mod 4
+    if (k_ok) {
+        const int r = lane & 3, i = 8 * warp + (lane >> 2);
+        const uint32_t* row = kt + i * PK_KRS + r;
+        const ulonglong2* ks = reinterpret_cast<const ulonglong2*>(kst) + r;
+        uint32_t* dst = reinterpret_cast<uint32_t*>(a.pool.k_codes) +
+                        (((int64_t)pages[i / PG] * a.H + h) * PG + (i % PG)) * WPR + r * BITS;
+#pragma unroll
+        for (int q = 0; q < BITS; ++q) {
+            uint32_t acc = 0u;
+            float far = 0.0f;
+#pragma unroll
+            for (int sl = 0; sl < PER; ++sl) {
+                const int p4 = 4 * (q * PER + sl);
+                const ulonglong2 st = ks[p4];
+                pk_acc2(row[p4], st.x, st.y, sl * BITS, acc, far);
+            }
+            acc -= BIAS;
+            if (far > PK_NEAR) {
+#pragma unroll 1
+                for (int sl = 0; sl < PER; ++sl) {
+                    const int p4 = 4 * (q * PER + sl), c = 2 * (p4 + r);
+                    const __half2 x2 = pk_h2(row[p4]);
+                    const float4 st = kst[p4 + r];
+                    pk_fix<BITS>(__low2float(x2), st.x, st.z, ksc[c], sl * BITS, acc);
+                    pk_fix<BITS>(__high2float(x2), st.y, st.w, ksc[c + 1], sl * BITS + 16, acc);
+                }
+            }
+            dst[q] = acc;
+        }
+    }
+    {
+        const int x = lane & 7, j = warp & 3, t = 4 * (warp >> 2) + (lane >> 3);
+        const int32_t pg = j < npage ? pages[j] : -1;
+        if (pg >= 0) {
+            const uint32_t* v0 = vp + 8 * j * D + pk_vcol(16 * t + x);      // channel 16t + x
+            const uint32_t* v1 = vp + 8 * j * D + pk_vcol(16 * t + 8 + x);  // channel 16t + 8 + x
+            const int g = (16 * t) >> gsh;
+            const float4* vs = vst + 8 * j * 4 + g;
+            uint32_t* dst = reinterpret_cast<uint32_t*>(a.pool.v_codes) + ((int64_t)pg * a.H + h) * BW +
+                            (8 * t + x) * BITS;
+#pragma unroll
+            for (int q = 0; q < BITS; ++q) {
+                uint32_t acc = 0u;
+                float far = 0.0f;
+#pragma unroll
+                for (int sl = 0; sl < PER; ++sl) {
+                    const int m = q * PER + sl, yl = (m >> 2) + 4 * ((m >> 1) & 1);
+                    const ulonglong2 st = reinterpret_cast<const ulonglong2*>(vs)[yl * 4];
+                    pk_acc2(((m & 1) ? v1 : v0)[yl * D], st.x, st.y, sl * BITS, acc, far);
+                }
+                acc -= BIAS;
+                if (far > PK_NEAR) {
+#pragma unroll 1
+                    for (int sl = 0; sl < PER; ++sl) {
+                        const int m = q * PER + sl, yl = (m >> 2) + 4 * ((m >> 1) & 1), tok = 16 * j + 2 * yl;
+                        const __half2 x2 = pk_h2(((m & 1) ? v1 : v0)[yl * D]);
+                        const float4 st = vs[yl * 4];
+                        pk_fix<BITS>(__low2float(x2), st.x, st.z, vsc[tok * 4 + g], sl * BITS, acc);
+                        pk_fix<BITS>(__high2float(x2), st.y, st.w, vsc[(tok + 1) * 4 + g], sl * BITS + 16, acc);
+                    }
+                }
+                if (PG * (j + 1) > nv) {  // partly covered page: keep the codes of later tokens
+                    uint32_t keep = 0u;
+#pragma unroll
+                    for (int sl = 0; sl < PER; ++sl) {
+                        const int m = q * PER + sl, tok = PG * j + 2 * ((m >> 2) + 4 * ((m >> 1) & 1));
+                        if (tok >= nv) keep |= CM << (sl * BITS);
+                        if (tok + 1 >= nv) keep |= CM << (sl * BITS + 16);
+                    }
+                    dst[q] = (dst[q] & keep) | (acc & ~keep);
+                } else {
+                    dst[q] = acc;
+                }
+            }
+        }
+    }
 }
 
-// K groups: one CTA of 128 threads per (complete 64-token group, head).
-template <int BITS>
-__global__ void __launch_bounds__(128) pack_k_kernel(PackArgs a) {
-    __shared__ __align__(16) uint32_t rows[KG * 4 * BITS];
-    __shared__ int32_t pages[4];
-    const int gi = blockIdx.x;
-    const int h = blockIdx.y;
-    const int c = threadIdx.x;
-    for (int w = c; w < KG * 4 * BITS; w += 128) rows[w] = 0u;
-    const int64_t t0 = a.t_start + (int64_t)gi * KG;
-    if (c < 4) pages[c] = a.bt_row[t0 / PG + c];
-    __syncthreads();
-    for (int j = 0; j < 4; ++j)
-        if (pages[j] < 0 || pages[j] >= a.pool.num_blocks) return;  // invalid table entry: skip the group
-    uint32_t sz;
-    quant_k_group<BITS>(a.k + (int64_t)gi * KG * a.stride_t + (int64_t)h * D, a.stride_t, c, rows, &sz);
-    a.pool.k_sz[((int64_t)pages[0] * a.H + h) * D + c] = sz;
-    __syncthreads();
-    store_k_rows<BITS>(rows, pages, a.H, h, a.pool.k_codes, c, 128);
-}
-
-// Keys of the final partial group -> k_tail (rows t mod 64).
-__global__ void pack_tail_kernel(PackArgs a, int64_t first_tail, int64_t n_tail) {
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= n_tail * a.H * D) return;
-    const int c = (int)(idx % D);
-    const int h = (int)((idx / D) % a.H);
-    const int64_t j = idx / ((int64_t)D * a.H);
-    const int64_t t = first_tail + j;     // absolute position
-    const int64_t i = t - a.t_start;      // input row
-    a.pool.k_tail[(((int64_t)a.seq * a.H + h) * KG + (t % KG)) * D + c] = a.k[i * a.stride_t + (int64_t)h * D + c];
+constexpr size_t pack_group_smem() {
+    return (size_t)KG * PK_KRS * 4 + (size_t)(KG / 2) * D * 4 + (size_t)(D / 2) * 16 + (size_t)(KG / 2) * 4 * 16 +
+           (size_t)D * 4 + (size_t)KG * 4 * 4 + 2 * 256 * 4 + (size_t)(KG / 2) * 4 * 2 * 4;
 }
 
 // fp16 layer: one CTA of 128 threads per (64-token tile, head).
@@ -238,16 +516,12 @@ __global__ void __launch_bounds__(128) pack_fp16_kernel(PackArgs a) {
 
 template <int BITS>
 int launch_pack_quant(const PackArgs& a, cudaStream_t s) {
-    const int64_t n_pages = (a.t_start + a.n_tokens + PG - 1) / PG - a.t_start / PG;
-    if (n_pages > 0) pack_v_kernel<BITS><<<dim3((unsigned)n_pages, a.H), 128, 0, s>>>(a);
-    const int64_t n_full = a.n_tokens / KG;
-    if (n_full > 0) pack_k_kernel<BITS><<<dim3((unsigned)n_full, a.H), 128, 0, s>>>(a);
-    const int64_t first_tail = a.t_start + n_full * KG;
-    const int64_t n_tail = a.n_tokens - n_full * KG;
-    if (n_tail > 0) {
-        const int64_t n = n_tail * a.H * D;
-        pack_tail_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, first_tail, n_tail);
-    }
+    const int64_t n_groups = (a.n_tokens + KG - 1) / KG;
+    if (n_groups == 0) return KVQ_OK;
+    const int smem = (int)pack_group_smem();
+    const int st = kvq_prepare_kernel((const void*)pack_group_kernel<BITS>, smem);
+    if (st) return st;
+    pack_group_kernel<BITS><<<dim3((unsigned)n_groups, a.H), 256, smem, s>>>(a);
     return kvq_launch_status("kv_quant_pack");
 }
 

@@ -61,7 +61,7 @@ int kvq_prepare_kernel(const void* func, int dyn_smem_max) {
     if (it != done.end() && it->second >= dyn_smem_max) return KVQ_OK;
     cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          (int)cudaSharedmemCarveoutMaxShared);
-    if (e == cudaSuccess && dyn_smem_max > 48 * 1024)
+    if (e == cudaSuccess && dyn_smem_max > 0)  // (static shared memory counts against the default 48 KB too)
         e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem_max);
     if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kernel attributes: %s", cudaGetErrorString(e));
     done[{func, dev}] = dyn_smem_max;

@@ -36,7 +36,7 @@ def assert_codes(gpu, ref, x16, scale32, mn, axis_group):
         assert abs(u - math.floor(u) - 0.5) < 1e-6, f"code mismatch at {idx}: gpu {gpu[idx]} ref {ref[idx]} u={u}"
 
 
-def _check_quant(cache, bt_row, T, K, V, bits, G):
+def _check_quant(cache, bt_row, T, K, V, bits, G, strict=False):
     cnp = _cache_np(cache)
     H = K.shape[1]
     for h in range(H):
@@ -46,10 +46,14 @@ def _check_quant(cache, bt_row, T, K, V, bits, G):
         n_full = pk["n_packed"]
         kx = K[:n_full, h]
         k_mn = pk["zero16"].astype(np.float32)
+        if strict:
+            assert np.array_equal(lg["k_codes"], pk["codes"])
         assert_codes(lg["k_codes"], pk["codes"], kx, pk["scale32"], k_mn, lambda i: (i[0] // 64, i[1]))
         assert np.array_equal(lg["k_scale16"].view(np.uint16), pk["scale16"].view(np.uint16))
         assert np.array_equal(lg["k_zero16"].view(np.uint16), pk["zero16"].view(np.uint16))
         v_mn = pv["zero16"].astype(np.float32)
+        if strict:
+            assert np.array_equal(lg["v_codes"], pv["codes"])
         assert_codes(lg["v_codes"], pv["codes"], V[:, h], pv["scale32"], v_mn, lambda i: (i[0], i[1] // G))
         assert np.array_equal(lg["v_scale16"].view(np.uint16), pv["scale16"].view(np.uint16))
         assert np.array_equal(lg["v_zero16"].view(np.uint16), pv["zero16"].view(np.uint16))
@@ -70,6 +74,49 @@ def test_pack_quant_bitexact(bits, G, T):
     kvq.kv_quant_pack(cache, batch, 0, 0, T, K.cuda(), V.cuda())
     torch.cuda.synchronize()
     _check_quant(cache, bt[0], T, K.numpy(), V.numpy(), bits, G)
+
+
+def _grid_rows(T, H, bits, G, seed):
+    """K, V fp16 on half-steps of a quantization grid: x = offset + span * k / (2L),
+    k uniform in [0, 2L]; each K group of 64 tokens and each V group of G channels
+    holds k = 0 and k = 2L, so its zero and scale come from offset and span.  With
+    span = L, L/2 or L/4 the quotients of odd k are exact ties (x - zero = (k/2)
+    scale); the other spans put quotients a few ulps from a half-integer."""
+    L = 2 ** bits - 1
+    rng = np.random.default_rng(seed)
+    spans = np.array([L, L / 2, L / 4, 1.0, 0.7, 100.0])
+    offs = np.array([-1.5, 0.0, 0.25, -3.0])
+
+    kk = rng.integers(0, 2 * L + 1, size=(T, H, 128))
+    kk[0::64] = 0
+    kk[1::64] = 2 * L
+    ks = spans[rng.integers(0, len(spans), size=(1, H, 128))]
+    ko = offs[rng.integers(0, len(offs), size=(1, H, 128))]
+    K = (ko + ks * kk / (2 * L)).astype(np.float16)
+    vk = rng.integers(0, 2 * L + 1, size=(T, H, 128))
+    vk[:, :, 0::G] = 0
+    vk[:, :, 1::G] = 2 * L
+    vs = np.repeat(spans[rng.integers(0, len(spans), size=(T, H, 128 // G))], G, axis=2)
+    vo = np.repeat(offs[rng.integers(0, len(offs), size=(T, H, 128 // G))], G, axis=2)
+    V = (vo + vs * vk / (2 * L)).astype(np.float16)
+    return torch.from_numpy(K), torch.from_numpy(V)
+
+
+@pytest.mark.parametrize("bits,G", [(1, 64), (2, 32), (4, 128), (8, 64)])
+def test_pack_rounding_ties_bitexact(bits, G):
+    """Codes whose quotient is an exact tie or within a few ulps of one: the
+    quantizer takes the IEEE fp32 quotient and rounds half to even on both sides,
+    so every code matches bit for bit (no near-tie allowance here)."""
+    require_gpu()
+    H, T = 2, 640 + 23
+    K, V = _grid_rows(T, H, bits, G, synth.mix(synth.BASE_SEED, 91, bits, G))
+    n_pages = math.ceil(T / 16)
+    alloc = kvq.Allocator(n_pages + 3, seed=5)
+    batch, bt = paged_batch([T], alloc)
+    cache = kvq.LayerCache(8, H, bits, n_pages + 3, 1, v_group_dims=G)
+    kvq.kv_quant_pack(cache, batch, 0, 0, T, K.cuda(), V.cuda())
+    torch.cuda.synchronize()
+    _check_quant(cache, bt[0], T, K.numpy(), V.numpy(), bits, G, strict=True)
 
 
 @pytest.mark.parametrize("bits,G", [(1, 64), (4, 32), (2, 128)])
