@@ -79,13 +79,6 @@ __device__ __forceinline__ uint32_t kvq_code(float x, float mn, float scale32, f
     return (uint32_t)r;
 }
 
-// Reads the b-bit code of channel c from a token row held as 32-bit words.
-template <int BITS>
-__device__ __forceinline__ uint32_t kvq_get_code(const uint32_t* row, int c) {
-    const int bit = c * BITS;
-    return (row[bit >> 5] >> (bit & 31)) & ((1u << BITS) - 1u);
-}
-
 __device__ __forceinline__ float kvq_warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
