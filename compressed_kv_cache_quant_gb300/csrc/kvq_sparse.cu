@@ -15,15 +15,6 @@ namespace {
 constexpr int D = KVQ_HEAD_DIM;
 constexpr int PG = KVQ_BLOCK_TOKENS;
 
-__device__ __forceinline__ void unpack8(const uint4& r, float* f) {
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = kvq_h2f((uint16_t)(w[i] & 0xffffu));
-        f[2 * i + 1] = kvq_h2f((uint16_t)(w[i] >> 16));
-    }
-}
-
 // Exclusive scan over the CTA of one uint32 per thread; *total receives the sum.
 template <int NT>
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, uint32_t* total) {
@@ -262,11 +253,54 @@ __global__ void __launch_bounds__(CS_NT, CS_MINB) crit_score_kernel(CritArgs a) 
 
 // ================================================================ a6 sparse attention
 
-constexpr int SA_NT = 256;
-constexpr int SA_HW = SA_NT / 16;  // half-warps per CTA
-constexpr int SA_BATCH = 4;        // rows in flight per half-warp
+// Tensor-core form: a warp takes 16 listed rows at a time (its own tiles, staged SA_STAGES - 1
+// tiles ahead with cp.async).  Scores S^T (heads x 16 rows) = Q K^T with m16n8k16 products: A =
+// the q rows (heads; rows past the group's heads are zero), B = the K tile through ldmatrix.  The score
+// accumulators of a head are, element for element, the A fragment of P (heads x rows) for the
+// value product O += P V, B = the V tile through ldmatrix.trans.  Scores stay fp32 (fp16 q and
+// k, exact products); p enters the value product in fp16 (2^-11 relative per weight).
+constexpr int SA_NW = 4;                       // warps per CTA
+constexpr int SA_NT = 32 * SA_NW;
+constexpr int SA_TR = 16;                      // rows per warp tile
+constexpr int SA_TILE = SA_TR * D * 2;         // bytes of one K or V tile (8 KB for K and V)
+constexpr int SA_STAGES = 2;                   // tiles per warp in flight or in use
+constexpr int SA_TILES = SA_NW * SA_STAGES * 2 * SA_TILE;  // [warp][stage][K, V]
 constexpr int SA_REC = 4 + D;
 constexpr int SA_MAX_RPS = 2048;   // rows per split: their offsets are resolved into shared memory
+
+// 16-byte global -> shared copy; a row that is not there reads as zeros
+__device__ __forceinline__ void sa_cp16(uint32_t dst, const void* src, bool ok) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(ok ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void sa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void sa_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void sa_ldm4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void sa_ldm4t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+// (d0, d1) += A B for an A whose rows 8..15 are zero: a0, a2 are rows 0..7 (k 0..7, 8..15)
+__device__ __forceinline__ void sa_mma(float& d0, float& d1, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    [[maybe_unused]] float j2, j3;  // rows 8..15 of the product: not used
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %10, %10};"
+        : "+f"(d0), "+f"(d1), "=f"(j2), "=f"(j3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.0f));
+}
+__device__ __forceinline__ uint32_t sa_pack_h2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// byte offset of 16-byte chunk c of tile row r (chunks XOR-swizzled by r mod 8: conflict-free ldmatrix)
+__device__ __forceinline__ uint32_t sa_chunk(int r, int c) { return (uint32_t)((r * 16 + (c ^ (r & 7))) * 16); }
+
 
 struct SAArgs {
     const uint16_t* k16;
@@ -286,6 +320,7 @@ struct SAArgs {
     float* probs;
     float* part;
     int32_t* counters;
+    float2* fin;        // [batch][H_q] (max, sum) of the exp2 scores, for the probabilities
     KvqWsHeader* hdr;
     int32_t n_splits;
     int32_t rps;        // rows per split
@@ -293,10 +328,10 @@ struct SAArgs {
 
 template <int NH>
 __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
-    extern __shared__ __align__(16) float sm[];  // [SA_HW][NH][SA_REC] half-warp states
+    extern __shared__ __align__(16) float sm[];  // warp tiles (then [SA_NW][NH][SA_REC] warp states) | row offsets
     __shared__ int is_last;
     const int split = blockIdx.x, list = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, hw = tid >> 4, l16 = tid & 15;
+    const int tid = threadIdx.x;
     const int n_lists = a.per_kv ? a.H : a.H * a.GQ;
     const int Hq = a.H * a.GQ;
     const int g = a.per_kv ? list : list / a.GQ;
@@ -323,7 +358,7 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
 
     // the split's rows: ids and pages resolved up front into row offsets (in 128-element rows;
     // ~0u for a bad id or page), four per thread in flight
-    uint32_t* roff = reinterpret_cast<uint32_t*>(sm + SA_HW * NH * SA_REC);
+    uint32_t* roff = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(sm) + SA_TILES);
     for (int i0 = r_begin + tid; i0 < r_end; i0 += 4 * SA_NT) {
         int t[4];
 #pragma unroll
@@ -348,107 +383,120 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
     }
     __syncthreads();
 
-    float qv[NH][8];
+    const int warp = tid >> 5, lane = tid & 31, hq = lane >> 2, qd = lane & 3;
+    // A operand: q rows of the group's heads (fragment row hq), channel pairs 8ks + qd and 8ks + 4 + qd
+    uint32_t qa[8][2];
+    {
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)b * Hq + h0 + min(hq, NH - 1)) * D);
 #pragma unroll
-    for (int hh = 0; hh < NH; ++hh) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(a.q + ((int64_t)b * Hq + h0 + hh) * D + 8 * l16);
-        unpack8(raw, qv[hh]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) qv[hh][i] *= KVQ_SCORE_LOG2_SCALE;
-    }
-    float m[NH], l[NH], o[NH][8];
-#pragma unroll
-    for (int hh = 0; hh < NH; ++hh) {
-        m[hh] = -INFINITY;
-        l[hh] = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[hh][i] = 0.0f;
-    }
-    // The loop bound is uniform over the CTA so that every lane reaches the shuffles.
-    for (int it = r_begin; it < r_end; it += SA_HW * SA_BATCH) {
-        uint4 kr[SA_BATCH], vr[SA_BATCH];
-        bool ok[SA_BATCH];
-#pragma unroll
-        for (int j = 0; j < SA_BATCH; ++j) {
-            const int i = it + j * SA_HW + hw;
-            ok[j] = false;
-            kr[j] = make_uint4(0u, 0u, 0u, 0u);
-            vr[j] = make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t r = i < r_end ? roff[i - r_begin] : 0xffffffffu;
-            if (r != 0xffffffffu) {
-                const int64_t off = (int64_t)r * D + 8 * l16;
-                kr[j] = __ldg(reinterpret_cast<const uint4*>(a.k16 + off));
-                vr[j] = __ldg(reinterpret_cast<const uint4*>(a.v16 + off));
-                ok[j] = true;
-            }
-        }
-        float s[SA_BATCH][NH];
-#pragma unroll
-        for (int j = 0; j < SA_BATCH; ++j) {
-            float kf[8];
-            unpack8(kr[j], kf);
-#pragma unroll
-            for (int hh = 0; hh < NH; ++hh) {
-                float acc = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc = fmaf(qv[hh][i], kf[i], acc);
-#pragma unroll
-                for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-                s[j][hh] = ok[j] ? acc : -INFINITY;
-            }
-        }
-        if (a.probs != nullptr && l16 == 0) {
-#pragma unroll
-            for (int j = 0; j < SA_BATCH; ++j) {
-                const int i = it + j * SA_HW + hw;
-                if (i < r_end)
-#pragma unroll
-                    for (int hh = 0; hh < NH; ++hh)
-                        a.probs[((int64_t)b * Hq + h0 + hh) * a.sel_cap + i] = s[j][hh];
-            }
-        }
-#pragma unroll
-        for (int hh = 0; hh < NH; ++hh) {
-            float mn = m[hh];
-#pragma unroll
-            for (int j = 0; j < SA_BATCH; ++j) mn = fmaxf(mn, s[j][hh]);
-            if (mn == -INFINITY) continue;
-            const float alpha = exp2f(m[hh] - mn);
-            m[hh] = mn;
-            l[hh] *= alpha;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[hh][i] *= alpha;
-#pragma unroll
-            for (int j = 0; j < SA_BATCH; ++j) {
-                const float p = exp2f(s[j][hh] - mn);
-                l[hh] += p;
-                float vf[8];
-                unpack8(vr[j], vf);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) o[hh][i] = fmaf(p, vf[i], o[hh][i]);
-            }
+        for (int ks = 0; ks < 8; ++ks) {
+            qa[ks][0] = hq < NH ? qrow[8 * ks + qd] : 0u;
+            qa[ks][1] = hq < NH ? qrow[8 * ks + 4 + qd] : 0u;
         }
     }
-    // ---- merge the half-warp states of the CTA
+    const int n_tiles = (r_end - r_begin + SA_TR - 1) / SA_TR;
+    const uint32_t tiles = (uint32_t)__cvta_generic_to_shared(sm) + (uint32_t)(warp * SA_STAGES * 2 * SA_TILE);
+    // tile t of the split (list rows r_begin + 16 t ...) into stage buffer `buf`: K, then V
+    auto stage = [&](int t, uint32_t buf) {
+        if (t < n_tiles) {
 #pragma unroll
-    for (int hh = 0; hh < NH; ++hh) {
-        float* r = sm + (hw * NH + hh) * SA_REC;
-        if (l16 == 0) {
-            r[0] = m[hh];
-            r[1] = l[hh];
+            for (int k = 0; k < 8; ++k) {
+                const int row = (lane >> 4) + 2 * k, c = lane & 15;
+                const int i = r_begin + SA_TR * t + row;
+                const uint32_t r = i < r_end ? roff[i - r_begin] : 0xffffffffu;
+                const bool ok = r != 0xffffffffu;
+                const int64_t off = ok ? (int64_t)r * D + 8 * c : 0;
+                sa_cp16(buf + sa_chunk(row, c), a.k16 + off, ok);
+                sa_cp16(buf + SA_TILE + sa_chunk(row, c), a.v16 + off, ok);
+            }
+        }
+        sa_commit();
+    };
+    float m = -INFINITY, lsum = 0.0f, o[16][2];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = 0.0f;
+    int t = warp;
+#pragma unroll
+    for (int st = 0; st < SA_STAGES; ++st) stage(t + st * SA_NW, tiles + (uint32_t)(st * 2 * SA_TILE));
+    for (int it = 0; t < n_tiles; ++it, t += SA_NW) {  // uniform over the warp
+        const uint32_t buf = tiles + (uint32_t)((it % SA_STAGES) * 2 * SA_TILE);
+        sa_wait<SA_STAGES - 1>();
+        __syncwarp();
+        // scores of rows 2qd, 2qd + 1 (n-tile 0) and 8 + 2qd, 9 + 2qd (n-tile 1) for head hq
+        float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const int mi = lane >> 3, lr = lane & 7;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t b0, b1, b2, b3;
+            sa_ldm4(buf + sa_chunk(lr + 8 * (mi >> 1), 2 * ks + (mi & 1)), b0, b1, b2, b3);
+            sa_mma(x[0], x[1], qa[ks][0], qa[ks][1], b0, b1);
+            sa_mma(x[2], x[3], qa[ks][0], qa[ks][1], b2, b3);
+        }
+        const int i0 = r_begin + SA_TR * t;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + 8 * (j >> 1) + 2 * qd + (j & 1);
+            const bool ok = i < r_end && roff[i - r_begin] != 0xffffffffu;
+            x[j] = ok ? x[j] * KVQ_SCORE_LOG2_SCALE : -INFINITY;
+            mx = fmaxf(mx, x[j]);
+            if (a.probs != nullptr && hq < NH && i < r_end) a.probs[((int64_t)b * Hq + h0 + hq) * a.sel_cap + i] = x[j];
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m, mx);
+        float alpha = 1.0f, p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (mn != -INFINITY) {
+            alpha = exp2f(m - mn);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) p[j] = exp2f(x[j] - mn);
+            m = mn;
+        }
+        lsum = lsum * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                o[j][0] *= alpha;
+                o[j][1] *= alpha;
+            }
+        }
+        const uint32_t pa0 = sa_pack_h2(p[0], p[1]), pa2 = sa_pack_h2(p[2], p[3]);
+#pragma unroll
+        for (int nc = 0; nc < 8; ++nc) {
+            uint32_t b0, b1, b2, b3;
+            sa_ldm4t(buf + SA_TILE + sa_chunk(lr + 8 * (mi & 1), 2 * nc + (mi >> 1)), b0, b1, b2, b3);
+            sa_mma(o[2 * nc][0], o[2 * nc][1], pa0, pa2, b0, b1);
+            sa_mma(o[2 * nc + 1][0], o[2 * nc + 1][1], pa0, pa2, b2, b3);
+        }
+        __syncwarp();  // every lane is done with the buffer
+        stage(t + SA_STAGES * SA_NW, buf);
+    }
+    sa_wait<0>();
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+    // ---- merge the warp states of the CTA (the records reuse the tile buffers)
+    __syncthreads();
+    if (hq < NH) {
+        float* r = sm + (warp * NH + hq) * SA_REC;
+        if (qd == 0) {
+            r[0] = m;
+            r[1] = lsum;
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) r[4 + 8 * l16 + i] = o[hh][i];
+        for (int j = 0; j < 16; ++j) {
+            r[4 + 8 * j + 2 * qd] = o[j][0];
+            r[4 + 8 * j + 2 * qd + 1] = o[j][1];
+        }
     }
     __syncthreads();
     const int64_t rec0 = (((int64_t)b * n_lists + list) * a.n_splits + split) * NH;
     for (int e = tid; e < NH * D; e += SA_NT) {
         const int hh = e / D, d = e % D;
         float M = -INFINITY;
-        for (int w = 0; w < SA_HW; ++w) M = fmaxf(M, sm[(w * NH + hh) * SA_REC]);
+        for (int w = 0; w < SA_NW; ++w) M = fmaxf(M, sm[(w * NH + hh) * SA_REC]);
         float L = 0.0f, O = 0.0f;
         if (M != -INFINITY) {
-            for (int w = 0; w < SA_HW; ++w) {
+            for (int w = 0; w < SA_NW; ++w) {
                 const float* r = sm + (w * NH + hh) * SA_REC;
                 const float wt = exp2f(r[0] - M);
                 L = fmaf(r[1], wt, L);
@@ -496,26 +544,27 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
     if (tid == 0) a.counters[(int64_t)b * n_lists + list] = 0;
     if (a.probs == nullptr) return;
     __syncthreads();
-    // the stored scores become probabilities; every thread keeps 2 x NH loads in flight
-    float* pr0 = a.probs + ((int64_t)b * Hq + h0) * a.sel_cap;
-    for (int i0 = tid; i0 < n; i0 += 2 * SA_NT) {
-        float sv[2][NH];
+    if (tid < NH) a.fin[(int64_t)b * Hq + h0 + tid] = make_float2(fin_m[tid], fin_l[tid]);
+}
+
+// The stored exp2-domain scores become probabilities, p = 2^(s - max) / sum, one thread per
+// (row, q head) with four rows in flight; (max, sum) come from the attention kernel's last CTAs.
+__global__ void __launch_bounds__(256) sa_norm_kernel(SAArgs a) {
+    kvq_pdl_begin();
+    const int h = blockIdx.y, b = blockIdx.z, Hq = a.H * a.GQ;
+    const int n_lists = a.per_kv ? a.H : Hq;
+    const int list = a.per_kv ? h / a.GQ : h;
+    const int n = max(0, min(a.sel_count[(int64_t)b * n_lists + list], a.sel_cap));
+    const int i0 = blockIdx.x * 1024 + threadIdx.x;
+    if (i0 >= n) return;
+    const float2 f = a.fin[(int64_t)b * Hq + h];
+    float* pr = a.probs + ((int64_t)b * Hq + h) * a.sel_cap;
+    float sv[4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
+    for (int u = 0; u < 4; ++u) sv[u] = i0 + 256 * u < n ? __ldcg(pr + i0 + 256 * u) : -INFINITY;
 #pragma unroll
-            for (int hh = 0; hh < NH; ++hh) {
-                const int i = i0 + u * SA_NT;
-                sv[u][hh] = i < n ? __ldcg(pr0 + (int64_t)hh * a.sel_cap + i) : -INFINITY;
-            }
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-#pragma unroll
-            for (int hh = 0; hh < NH; ++hh) {
-                const int i = i0 + u * SA_NT;
-                const float M = fin_m[hh], L = fin_l[hh];
-                if (i < n) pr0[(int64_t)hh * a.sel_cap + i] = (L > 0.0f && sv[u][hh] != -INFINITY) ? exp2f(sv[u][hh] - M) / L : 0.0f;
-            }
-    }
+    for (int u = 0; u < 4; ++u)
+        if (i0 + 256 * u < n) pr[i0 + 256 * u] = (f.y > 0.0f && sv[u] != -INFINITY) ? exp2f(sv[u] - f.x) / f.y : 0.0f;
 }
 
 struct SAPlan {
@@ -525,15 +574,16 @@ struct SAPlan {
 SAPlan sa_plan(const kvq_layout* L, const kvq_seqs* S, int32_t sel_cap, int per_kv) {
     const int n_lists = per_kv ? L->n_kv_heads : L->n_q_heads;
     const int64_t units = (int64_t)std::max(S->batch, 1) * n_lists;
-    const int64_t target = 3LL * kvq_num_sms();
-    int splits = (int)std::max<int64_t>(1, (target + units - 1) / units);
+    const int64_t target = 3LL * kvq_num_sms();  // resident CTAs: one wave, no partial second one
+    int splits = (int)std::max<int64_t>(1, target / units);
     int rps = (std::max(sel_cap, 1) + splits - 1) / splits;
     rps = std::min(SA_MAX_RPS, std::max(64, (rps + 63) / 64 * 64));
     splits = (std::max(sel_cap, 1) + rps - 1) / rps;
     return {splits, rps};
 }
 
-size_t sa_ws_layout(const kvq_layout* L, const kvq_seqs* S, int32_t sel_cap, size_t* off_part, size_t* off_cnt) {
+size_t sa_ws_layout(const kvq_layout* L, const kvq_seqs* S, int32_t sel_cap, size_t* off_part, size_t* off_cnt,
+                    size_t* off_fin) {
     // sized for the larger of the two list modes so one workspace serves both
     const SAPlan p0 = sa_plan(L, S, sel_cap, 0), p1 = sa_plan(L, S, sel_cap, 1);
     const int GQ = L->n_q_heads / std::max(L->n_kv_heads, 1);
@@ -542,14 +592,16 @@ size_t sa_ws_layout(const kvq_layout* L, const kvq_seqs* S, int32_t sel_cap, siz
     const size_t recs = r0 > r1 ? r0 : r1;
     *off_part = sizeof(KvqWsHeader);
     *off_cnt = kvq_round_up(*off_part + recs * SA_REC * sizeof(float), 256);
-    return kvq_round_up(*off_cnt + (size_t)std::max(S->batch, 1) * L->n_q_heads * sizeof(int32_t), 256);
+    *off_fin = kvq_round_up(*off_cnt + (size_t)std::max(S->batch, 1) * L->n_q_heads * sizeof(int32_t), 256);
+    return kvq_round_up(*off_fin + (size_t)std::max(S->batch, 1) * L->n_q_heads * sizeof(float2), 256);
 }
 
 template <int NH>
 int launch_sa(const SAArgs& a, dim3 grid, cudaStream_t s) {
-    const size_t smem = (size_t)SA_HW * NH * SA_REC * sizeof(float) + (size_t)a.rps * sizeof(uint32_t);
+    static_assert((size_t)SA_NW * 8 * SA_REC * sizeof(float) <= (size_t)SA_TILES, "the warp states fit the tiles");
+    const size_t smem = (size_t)SA_TILES + (size_t)a.rps * sizeof(uint32_t);
     const int st = kvq_prepare_kernel((const void*)sparse_attn_kernel<NH>,
-                                      (int)((size_t)SA_HW * NH * SA_REC * sizeof(float) + SA_MAX_RPS * sizeof(uint32_t)));
+                                      (int)((size_t)SA_TILES + SA_MAX_RPS * sizeof(uint32_t)));
     if (st) return st;
     sparse_attn_kernel<NH><<<grid, SA_NT, smem, s>>>(a);
     return kvq_launch_status("kv_sparse_attn");
@@ -660,8 +712,8 @@ extern "C" int kv_append_critical_score(const kvq_layout* L, const kvq_pool* P, 
 extern "C" size_t kv_sparse_attn_ws(const kvq_layout* L, const kvq_seqs* S, int32_t sel_cap) {
     if (kvq_check_layout(L, "kv_sparse_attn_ws", true) || kvq_check_seqs_sizes(S, "kv_sparse_attn_ws") || sel_cap <= 0)
         return 0;
-    size_t a, c;
-    return sa_ws_layout(L, S, sel_cap, &a, &c);
+    size_t a, c, f;
+    return sa_ws_layout(L, S, sel_cap, &a, &c, &f);
 }
 
 extern "C" int kv_sparse_attn(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
@@ -677,8 +729,8 @@ extern "C" int kv_sparse_attn(const kvq_layout* L, const kvq_pool* P, const kvq_
                 "kv_sparse_attn: k16/v16 must be 16-byte aligned");
     KVQ_REQUIRE(sel_cap > 0 && sel && sel_count && out, KVQ_ERR_INVALID_ARG, "kv_sparse_attn: NULL buffer or sel_cap");
     KVQ_REQUIRE(sel_per_kv_head == 0 || sel_per_kv_head == 1, KVQ_ERR_INVALID_ARG, "kv_sparse_attn: sel_per_kv_head");
-    size_t off_part, off_cnt;
-    const size_t need = sa_ws_layout(L, S, sel_cap, &off_part, &off_cnt);
+    size_t off_part, off_cnt, off_fin;
+    const size_t need = sa_ws_layout(L, S, sel_cap, &off_part, &off_cnt, &off_fin);
     st = kvq_check_ws(ws, ws_bytes, need, "kv_sparse_attn");
     if (st) return st;
     if (S->batch == 0) return KVQ_OK;
@@ -704,17 +756,29 @@ extern "C" int kv_sparse_attn(const kvq_layout* L, const kvq_pool* P, const kvq_
     a.probs = probs;
     a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + off_part);
     a.counters = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + off_cnt);
+    a.fin = reinterpret_cast<float2*>(static_cast<char*>(ws) + off_fin);
     a.hdr = static_cast<KvqWsHeader*>(ws);
     a.n_splits = p.n_splits;
     a.rps = p.rps;
     const int n_lists = sel_per_kv_head ? L->n_kv_heads : L->n_q_heads;
     dim3 grid(p.n_splits, n_lists, S->batch);
     cudaStream_t s = kvq_stream(stream);
-    if (!sel_per_kv_head) return launch_sa<1>(a, grid, s);
-    switch (a.GQ) {
-        case 1: return launch_sa<1>(a, grid, s);
-        case 2: return launch_sa<2>(a, grid, s);
-        case 4: return launch_sa<4>(a, grid, s);
-        default: return launch_sa<8>(a, grid, s);
+    int e;
+    if (!sel_per_kv_head) {
+        e = launch_sa<1>(a, grid, s);
+    } else {
+        switch (a.GQ) {
+            case 1: e = launch_sa<1>(a, grid, s); break;
+            case 2: e = launch_sa<2>(a, grid, s); break;
+            case 4: e = launch_sa<4>(a, grid, s); break;
+            default: e = launch_sa<8>(a, grid, s); break;
+        }
     }
+    if (e || probs == nullptr) return e;
+    const dim3 ng((unsigned)((sel_cap + 1023) / 1024), (unsigned)L->n_q_heads, (unsigned)S->batch);
+    const int st2 = kvq_prepare_kernel((const void*)sa_norm_kernel, 0);
+    if (st2) return st2;
+    const cudaError_t le = kvq_launch_pdl(sa_norm_kernel, ng, dim3(256), 0, s, a);
+    if (le != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_sparse_attn launch: %s", cudaGetErrorString(le));
+    return kvq_launch_status("kv_sparse_attn");
 }

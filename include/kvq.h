@@ -277,7 +277,7 @@ size_t kv_topk_select_ws(void);
  * sel_count has the matching [batch][heads] shape; ids must be < seq_lens[b]
  * (others are skipped and flagged).  probs (optional): device fp32
  * [batch][H_q][sel_cap], the softmax probability of every listed token, in
- * list order.  An empty list gives 0.
+ * list order (a second, short launch normalizes them).  An empty list gives 0.
  * ws: kv_sparse_attn_ws(layout, seqs, sel_cap) bytes.
  * ---------------------------------------------------------------------- */
 int kv_sparse_attn(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
