@@ -33,7 +33,7 @@ constexpr int KG = KVQ_K_GROUP_TOKENS;
 // warps per CTA (one CTA per SM): as many as the double-buffered group stages let fit
 template <int BITS>
 __host__ __device__ constexpr int nwarp_of() {
-    return BITS <= 2 ? 16 : (BITS == 4 ? 8 : 4);
+    return BITS <= 2 ? 16 : (BITS == 4 ? 2 : 4);
 }
 constexpr int REC = 4 + D;  // partial record: m, l, pad, pad, o[128]
 
@@ -186,7 +186,7 @@ struct QMSmem {
     float qs[GQ][D];                  // the query heads of the kv group times 2^BITS (fp32)
     float m[NWARP][GQ], l[NWARP][GQ];
     uint32_t afr[NWARP][16][AFR_LD];  // per warp: the scores' A fragments, [register][lane]
-    union {
+    union alignas(16) {               // cp.async writes 16-byte chunks into the stages
         GroupStage<BITS> st[NWARP][2];
         float ro[NWARP][GQ][D];       // per warp: unnormalised outputs, after the last group
     } u;
@@ -528,20 +528,65 @@ struct Plan {
     int cps;
 };
 
-Plan plan_splits(const kvq_layout* L, const kvq_seqs* S) {
+template <int BITS, int GQ, int NGV>
+int resident_one() {
+    const int smem = (int)sizeof(QMSmem<BITS, GQ>);
+    constexpr int NT = 32 * nwarp_of<BITS>();
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        kvq_prepare_kernel((const void*)qmma_kernel<BITS, GQ, NGV>, smem) == KVQ_OK &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qmma_kernel<BITS, GQ, NGV>, NT, (size_t)smem) ==
+            cudaSuccess &&
+        n > 0)
+        return n;
+    cudaGetLastError();  // no device here: estimate from the thread and shared-memory budgets
+    return std::max(1, std::min(2048 / NT, 232448 / (smem + 1024)));
+}
+
+template <int BITS, int GQ>
+int resident_ngv(int G) {
+    return G == 128 ? resident_one<BITS, GQ, 1>() : G == 64 ? resident_one<BITS, GQ, 2>() : resident_one<BITS, GQ, 4>();
+}
+
+template <int BITS>
+int resident_bits(int gq, int G) {
+    const int g = grid_gq(gq);
+    return g == 1 ? resident_ngv<BITS, 1>(G) : g == 2 ? resident_ngv<BITS, 2>(G) : resident_ngv<BITS, 4>(G);
+}
+
+// CTAs of the layer's kernel that fit on one SM at once
+int resident_ctas(const kvq_layout* L) {
+    const int gq = L->n_q_heads / L->n_kv_heads, G = L->v_group_dims;
+    switch (L->bits) {
+        case 1: return resident_bits<1>(gq, G);
+        case 2: return resident_bits<2>(gq, G);
+        case 4: return resident_bits<4>(gq, G);
+        default: return resident_bits<8>(gq, G);
+    }
+}
+
+// Context splits.  With few (sequence, kv head) units the split count fills one wave of resident
+// CTAs.  With many units (a batch, lengths that may differ) every split takes a fixed 32 groups
+// (2048 tokens), so a sequence gets CTAs in proportion to its length and the waves stay even;
+// `compact` keeps the one-wave rule for callers with a small, fixed scratch.
+constexpr int QA_SPLIT_GROUPS = 32;
+
+Plan plan_splits(const kvq_layout* L, const kvq_seqs* S, bool compact) {
     const int n_groups = (std::max(S->max_len, 1) + KG - 1) / KG;
     const int gq = L->n_q_heads / L->n_kv_heads;
     const int64_t units = (int64_t)std::max(S->batch, 1) * L->n_kv_heads * kv_div_of(gq);
-    const int64_t target = kvq_num_sms();  // resident CTAs to aim for (one per SM)
-    int splits = (int)std::max<int64_t>(1, (target + units - 1) / units);
-    int cps = std::max(4, (n_groups + splits - 1) / splits);
-    cps = std::min(cps, n_groups);
-    splits = (n_groups + cps - 1) / cps;
-    return {splits, cps};
+    const int64_t target = (int64_t)kvq_num_sms() * resident_ctas(L);  // one wave
+    int cps;
+    if (!compact && 2 * units >= target) {
+        cps = std::min(n_groups, QA_SPLIT_GROUPS);
+    } else {
+        const int splits = (int)std::max<int64_t>(1, (target + units - 1) / units);
+        cps = std::min(n_groups, std::max(4, (n_groups + splits - 1) / splits));
+    }
+    return {(n_groups + cps - 1) / cps, cps};
 }
 
-size_t ws_layout(const kvq_layout* L, const kvq_seqs* S, size_t* off_part, size_t* off_cnt) {
-    const Plan p = plan_splits(L, S);
+size_t ws_layout(const kvq_layout* L, const kvq_seqs* S, const Plan& p, size_t* off_part, size_t* off_cnt) {
     const int GQ = L->n_q_heads / L->n_kv_heads;
     const size_t units = (size_t)std::max(S->batch, 1) * L->n_kv_heads * kv_div_of(GQ);
     const size_t recs = units * p.n_splits * grid_gq(GQ);
@@ -589,7 +634,7 @@ extern "C" size_t kv_decode_attn_quant_ws(const kvq_layout* L, const kvq_seqs* S
     if (kvq_check_layout(L, "kv_decode_attn_quant_ws", true) || kvq_check_seqs_sizes(S, "kv_decode_attn_quant_ws"))
         return 0;
     size_t a, c;
-    return ws_layout(L, S, &a, &c);
+    return ws_layout(L, S, plan_splits(L, S, false), &a, &c);
 }
 
 extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
@@ -606,12 +651,12 @@ extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, cons
                 KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: code and scale arrays must be 16-byte aligned");
     KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: batch exceeds max_seqs");
     size_t off_part, off_cnt;
-    const size_t need = ws_layout(L, S, &off_part, &off_cnt);
+    const Plan p = plan_splits(L, S, false);
+    const size_t need = ws_layout(L, S, p, &off_part, &off_cnt);
     st = kvq_check_ws(ws, ws_bytes, need, "kv_decode_attn_quant");
     if (st) return st;
     if (S->batch == 0) return KVQ_OK;
     KVQ_REQUIRE(q && out && S->block_table, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: NULL q/out/block table");
-    const Plan p = plan_splits(L, S);
     QAttnArgs a;
     a.k_codes = P->k_codes;
     a.v_codes = P->v_codes;
@@ -695,7 +740,12 @@ extern "C" int kv_decode_attn_quant_noalloc(const kvq_layout* L, const kvq_pool*
                 KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: code and scale arrays must be 16-byte aligned");
     KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: batch exceeds max_seqs");
     size_t off_part, off_cnt;
-    const size_t need = ws_layout(L, S, &off_part, &off_cnt);
+    Plan p = plan_splits(L, S, false);
+    size_t need = ws_layout(L, S, p, &off_part, &off_cnt);
+    if (need > KVQ_NOALLOC_SCRATCH_BYTES) {  // fewer splits, if that fits
+        p = plan_splits(L, S, true);
+        need = ws_layout(L, S, p, &off_part, &off_cnt);
+    }
     KVQ_REQUIRE(need <= KVQ_NOALLOC_SCRATCH_BYTES, KVQ_ERR_NO_SPACE,
                 "kv_decode_attn_quant_noalloc: this batch needs %zu bytes of scratch, the built-in array holds %u; "
                 "use kv_decode_attn_quant with a workspace", need, KVQ_NOALLOC_SCRATCH_BYTES);
@@ -711,7 +761,6 @@ extern "C" int kv_decode_attn_quant_noalloc(const kvq_layout* L, const kvq_pool*
     cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(KvqWsHeader), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(static_cast<char*>(ws) + off_cnt, 0, need - off_cnt, s);
     if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant_noalloc: %s", cudaGetErrorString(e));
-    const Plan p = plan_splits(L, S);
     QAttnArgs a;
     a.k_codes = P->k_codes;
     a.v_codes = P->v_codes;
