@@ -414,3 +414,53 @@ def offload_gather(rows16, ids):
     for i, t in enumerate(ids):
         out[i] = rows16[int(t)]
     return out
+
+
+# ---------------------------------------------------------------------------
+# f1: block-granular selection   [Meeting §8.1, item 1: block pruning]
+# ---------------------------------------------------------------------------
+
+def block_importance(scores, n_sink, window, block):
+    """[Meeting §8.1] importance of every ``block``-token block (block j holds
+    tokens [j*block, (j+1)*block) clipped to T): the mean of the approximate
+    scores of its candidate tokens (n_sink <= t < T - window).  READING: the
+    page asks for the block mean but fixes no arithmetic; the sum runs in fp64
+    in ascending t, is divided by the candidate count in fp64 and rounded to
+    fp32, because the importance decides an integer (the kept blocks).  A
+    block without candidates gets -inf.  Returns fp32 [ceil(T / block)]."""
+    scores = np.asarray(scores, dtype=np.float32)
+    T = scores.shape[0]
+    nb = -(-T // block)
+    imp = np.full(nb, -np.inf, dtype=np.float32)
+    for j in range(nb):
+        lo, hi = max(j * block, n_sink), min((j + 1) * block, T - window)
+        if lo < hi:
+            s = 0.0
+            for t in range(lo, hi):  # plain left-to-right fp64 sum
+                s += float(scores[t])
+            imp[j] = np.float32(s / (hi - lo))
+    return imp
+
+
+def block_select(scores, n_keep, n_sink, window, block):
+    """[Meeting §8.1] Selected token ids (ascending) with block pruning: the
+    sinks [0, n_sink) and the window [T - window, T) as in ``topk_select``, plus
+    every token of the ``n_keep`` blocks of highest importance (ties -> lower
+    block; blocks without candidates rank last, at -inf).  READING: the page
+    keeps the "top P%" of blocks; n_keep = floor(P * ceil(T / block)) is
+    ``block_count``."""
+    scores = np.asarray(scores, dtype=np.float32)
+    T = scores.shape[0]
+    imp = block_importance(scores, n_sink, window, block)
+    order = np.lexsort((np.arange(len(imp)), -imp.astype(np.float64)))
+    keep = np.zeros(T, dtype=bool)
+    keep[:min(n_sink, T)] = True
+    keep[max(T - window, 0):] = True
+    for j in order[:n_keep]:
+        keep[j * block:min((j + 1) * block, T)] = True
+    return np.nonzero(keep)[0].astype(np.int64)
+
+
+def block_count(T, ratio, block):
+    """Blocks kept at retention ratio P: floor(P * ceil(T / block))."""
+    return int(math.floor(ratio * float(-(-T // block))))

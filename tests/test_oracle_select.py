@@ -122,3 +122,79 @@ def test_offload_gather_bytes():
     ids = [49, 0, 7, 7, 13]
     got = O.offload_gather(rows, ids)
     assert got.tobytes() == b"".join(rows[i].tobytes() for i in ids)
+
+
+# ---- f1 block-granular selection   [Meeting §8.1, block pruning]
+
+@pytest.mark.parametrize("T,k", [(50, 10), (97, 33), (300, 40)])
+def test_block_select_of_single_tokens_is_topk(T, k):
+    """With one-token blocks the block mean is the token's own score, so block
+    pruning must pick exactly what the independent token top-K picks."""
+    s = np.random.default_rng(T).standard_normal(T).astype(np.float32)
+    assert T > 4 + 16 + k
+    got = O.block_select(s, k, 4, 16, 1)
+    assert got.tolist() == O.topk_select(s, k, 4, 16).tolist()
+
+
+def test_block_importance_closed_form():
+    """Scores t (exact in fp32): a block's importance is the midpoint of its
+    candidate range; blocks inside the sinks or the window are -inf."""
+    T, B, ns, W = 200, 16, 20, 40
+    imp = O.block_importance(np.arange(T, dtype=np.float32), ns, W, B)
+    assert len(imp) == 13
+    for j in range(13):
+        lo, hi = max(j * B, ns), min((j + 1) * B, T - W)
+        if lo < hi:
+            assert imp[j] == np.float32((lo + hi - 1) / 2)
+        else:
+            assert imp[j] == -np.inf
+    # block 0 lies in the sinks; T - W = 160 ends the candidates with block 9 = [144, 160)
+    assert imp[0] == -np.inf and imp[1] == np.float32(25.5) and imp[9] == np.float32(151.5)
+    assert np.all(imp[10:] == -np.inf)
+
+
+def test_block_select_constant_scores_keep_the_first_blocks():
+    T, B, ns, W, n = 1000, 64, 4, 128, 3
+    got = O.block_select(np.full(T, 0.25, np.float32), n, ns, W, B)
+    want = sorted(set(range(0, 3 * B)) | set(range(T - W, T)))
+    assert got.tolist() == want
+
+
+def test_block_select_planted_block_and_ties():
+    T, B = 640, 64
+    s = np.zeros(T, np.float32)
+    s[5 * B:6 * B] = 1.0          # the planted block wins
+    s[2 * B:3 * B:2] = 0.5        # blocks 2 and 7 tie at a mean of 0.25 ...
+    s[7 * B + 1:8 * B:2] = 0.5    # ... with different contents: the lower block goes first
+    got = O.block_select(s, 2, 0, 0, B)
+    assert got.tolist() == list(range(2 * B, 3 * B)) + list(range(5 * B, 6 * B))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_block_select_brute_force_invariant(seed):
+    """Small integer scores (exact means as fractions): the kept blocks are the
+    n best by (mean desc, block asc); every kept block beats every other block
+    that has candidates, and sinks/window are always kept."""
+    from fractions import Fraction
+    rng = np.random.default_rng(100 + seed)
+    T, B, ns, W = int(rng.integers(20, 60)), 8, int(rng.integers(0, 6)), int(rng.integers(0, 9))
+    s = rng.integers(-3, 4, size=T).astype(np.float32)
+    nb = -(-T // B)
+    n = int(rng.integers(0, nb + 1))
+    got = set(O.block_select(s, n, ns, W, B).tolist())
+    keyed = []
+    for j in range(nb):
+        lo, hi = max(j * B, ns), min((j + 1) * B, T - W)
+        m = Fraction(int(sum(int(x) for x in s[lo:hi])), hi - lo) if lo < hi else None
+        keyed.append((m, j))
+    ranked = sorted(keyed, key=lambda mj: (mj[0] is None, -(mj[0] or 0), mj[1]))
+    want = set(range(min(ns, T))) | set(range(max(T - W, 0), T))
+    for _, j in ranked[:n]:
+        want |= set(range(j * B, min((j + 1) * B, T)))
+    assert got == want
+
+
+def test_block_count():
+    assert O.block_count(131072, 0.03, 64) == 61
+    assert O.block_count(4096, 0.03, 64) == 1
+    assert O.block_count(100, 0.5, 64) == 1
