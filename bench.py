@@ -660,6 +660,57 @@ def run_rows(args):
         print(json.dumps({"row": "a6+a7 H2O layer step", "error": repr(e)}), flush=True)
     torch.cuda.empty_cache()
 
+    # f1 block-granular selection (block pruning in 64-token blocks) next to the token top-K on one
+    # Llama-3.1-8B-shaped sparse layer: selection over the critical-channel scores + exact attention
+    try:
+        Hq, Hkv, T, ns, w, blk = 32, 8, args.prompt, 4, 128, 64
+        seqs, npg, _ = _paged(torch, kvq, [T], device, 13)
+        cache = kvq.LayerCache(Hq, Hkv, 16, npg, 1, t_cap=(T + 7) // 8 * 8)
+        K, V = synth.kv_rows(T, Hkv, synth.mix(seed + 6, 0), device=device)
+        kvq.kv_quant_pack(cache, seqs, 0, 0, T, K, V)  # same stream as K, V
+        del K, V
+        q = synth.normal((1, Hq, D), synth.mix(seed + 6, 1), device)
+        sc = torch.empty((1, Hq, (T + 7) // 8 * 8), device=device)
+        crit = torch.empty((1, Hq, 8), dtype=torch.int32, device=device)
+        kvq.kv_critical_score(cache, seqs, q, 8, crit, sc)
+        kt, nb = O.ratio_k(T, RATIO), O.block_count(T, RATIO, blk)
+        cap = max(O.topk_count(T, kt, ns, w), ns + w + nb * blk)
+        sel_t = torch.empty((1, Hq, cap), dtype=torch.int32, device=device)
+        sel_b = torch.empty((1, Hq, cap), dtype=torch.int32, device=device)
+        cnt_t = torch.empty((1, Hq), dtype=torch.int32, device=device)
+        cnt_b = torch.empty((1, Hq), dtype=torch.int32, device=device)
+        out = torch.empty((1, Hq, D), device=device)
+        wt = kvq.Workspace(kvq.kv_topk_select_ws())
+        wb = kvq.Workspace(kvq.kv_block_select_ws(seqs, Hq, blk))
+        wa = kvq.Workspace(kvq.kv_sparse_attn_ws(cache, seqs, cap))
+        sel_tok = lambda: kvq.kv_topk_select(seqs, Hq, sc, -1, RATIO, ns, w, sel_t, cnt_t, wt, stream=sh)
+        sel_blk = lambda: kvq.kv_block_select(seqs, Hq, sc, -1, RATIO, ns, w, blk, sel_b, cnt_b, wb, stream=sh)
+        att_tok = lambda: kvq.kv_sparse_attn(cache, seqs, q, sel_t, cnt_t, 0, out, None, wa, stream=sh)
+        att_blk = lambda: kvq.kv_sparse_attn(cache, seqs, q, sel_b, cnt_b, 0, out, None, wa, stream=sh)
+        ms_tok = _ev_ms(torch, lambda: (sel_tok(), att_tok()), stream, 20)
+        ms_blk = _ev_ms(torch, lambda: (sel_blk(), att_blk()), stream, 20)
+        ms_att_tok = _ev_ms(torch, att_tok, stream, 20)
+        ms_att_blk = _ev_ms(torch, att_blk, stream, 20)
+        for wk in (wt, wb, wa):
+            kvq.kvq_check(wk, stream=sh)
+        rows_t, rows_b = int(cnt_t.sum().item()), int(cnt_b.sum().item())
+        by_t, by_b = Hq * T * 4 + rows_t * 2 * D * 2, Hq * T * 4 + rows_b * 2 * D * 2
+        s0 = sc[0, 0, :T].cpu().numpy()
+        t = _wall(lambda: O.block_select(s0, nb, ns, w, blk))
+        _row_line("f1 kv_block_select + kv_sparse_attn (block-sparse layer)",
+                  f"32 q / 8 kv heads, T = {T}, ratio {RATIO}: {nb} blocks of {blk} + {ns} sinks + {w} window "
+                  f"per q head (token top-K: {kt})",
+                  by_b / (ms_blk * 1e-3) / 1e9, "GB/s", hbm(by_b / (ms_blk * 1e-3) / 1e9),
+                  {"value": t * 1e3 * Hq, "unit": "ms per layer (selection only)", "cores": 1, "kind": "oracle",
+                   "sample": "block selection of one q head, numpy, times 32"},
+                  {"ms_block_path": ms_blk, "ms_token_path": ms_tok, "ms_attn_block_lists": ms_att_blk,
+                   "ms_attn_token_lists": ms_att_tok, "token_path_GBps": by_t / (ms_tok * 1e-3) / 1e9,
+                   "rows_block": rows_b, "rows_token": rows_t, "bytes": by_b})
+        del cache
+    except Exception as e:
+        print(json.dumps({"row": "f1 block-sparse layer", "error": repr(e)}), flush=True)
+    torch.cuda.empty_cache()
+
     # a9 kv_offload_gather: 40 heads x 3932 selected rows of 131072 from pinned host memory
     try:
         T, H, sel_n = args.prompt, 40, math.floor(RATIO * args.prompt)

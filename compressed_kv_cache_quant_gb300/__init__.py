@@ -6,7 +6,7 @@ only marshals arguments to the C ABI declared in include/kvq.h.
 """
 from . import _abi  # noqa: F401
 from .kvq import (Allocator, Batch, KvqError, LayerCache, Workspace, kv_append_critical_score,  # noqa: F401
-                  kv_append_critical_score_ws, kv_critical_score, kv_select_sparse_attn, kv_select_sparse_attn_ws,
+                  kv_append_critical_score_ws, kv_block_select, kv_block_select_ws, kv_critical_score, kv_select_sparse_attn, kv_select_sparse_attn_ws,
                   kv_decode_attn_quant, kv_decode_attn_quant_ws, kv_dense_pref_score, kv_dense_pref_score_ws,
                   kv_h2o_accumulate, kv_h2o_accumulate_ws, kv_offload_gather, kv_offload_gather_ws, kv_page_append,
                   kv_page_append_ws, kv_page_copy, kv_quant_pack, kv_sparse_attn, kv_sparse_attn_ws, kv_sparse_layer_decode,

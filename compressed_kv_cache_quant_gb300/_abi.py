@@ -70,6 +70,9 @@ PROTOTYPES = {
     "kv_topk_select": (c_int, [PS, c_int32, VP, c_int64, c_int32, c_double, c_int32, c_int32, VP, c_int32, VP,
                                VP, c_size_t, VP]),
     "kv_topk_select_ws": (c_size_t, []),
+    "kv_block_select": (c_int, [PS, c_int32, VP, c_int64, c_int32, c_double, c_int32, c_int32, c_int32, VP, c_int32,
+                                VP, VP, c_size_t, VP]),
+    "kv_block_select_ws": (c_size_t, [PS, c_int32, c_int32]),
     "kv_append_critical_score": (c_int, [PL, PP, PS, VP, VP, VP, c_int32, VP, VP, c_int64, VP, c_int32, c_int32, VP,
                                          c_size_t, VP]),
     "kv_append_critical_score_ws": (c_size_t, []),

@@ -240,6 +240,20 @@ def kv_topk_select(seqs, n_heads, scores, k_fixed, ratio, n_sink, window, sel, s
                                       _p(sel_count), ws.ptr, ws.nbytes, _s(stream)), "kv_topk_select")
 
 
+def kv_block_select_ws(seqs, n_heads, block_tokens):
+    return lib().kv_block_select_ws(_ref(seqs), int(n_heads), int(block_tokens))
+
+
+def kv_block_select(seqs, n_heads, scores, n_keep_fixed, ratio, n_sink, window, block_tokens, sel, sel_count, ws,
+                    score_stride=None, stream=None):
+    if score_stride is None:
+        score_stride = scores.shape[-1]
+    return check(lib().kv_block_select(_ref(seqs), int(n_heads), _p(scores), int(score_stride), int(n_keep_fixed),
+                                       float(ratio), int(n_sink), int(window), int(block_tokens), _p(sel),
+                                       int(sel.shape[-1]), _p(sel_count), ws.ptr, ws.nbytes, _s(stream)),
+                 "kv_block_select")
+
+
 def kv_sparse_attn_ws(cache, seqs, sel_cap):
     return lib().kv_sparse_attn_ws(_ref(cache.layout), _ref(seqs), int(sel_cap))
 

@@ -266,6 +266,32 @@ int kv_topk_select(const kvq_seqs* seqs, int32_t n_heads,
 size_t kv_topk_select_ws(void);
 
 /* ------------------------------------------------------------------------
+ * f1: kv_block_select -- block-granular selection, the block pruning of
+ * the meeting article [Meeting §8.1, item 1]: tokens are grouped into
+ * blocks of block_tokens (block j = tokens [j*block, (j+1)*block) of the
+ * sequence); a block's importance is the mean score of its candidate
+ * tokens (n_sink <= t < T - window): an fp32 sum in ascending t divided
+ * by the count in fp32 (-inf without candidates).  The n blocks of highest importance (ties -> lower block)
+ * are kept whole, with n = n_keep_fixed when >= 0, else
+ * floor(ratio * ceil(T / block)) in double.  Output: the sinks [0, n_sink),
+ * every token of the kept blocks and the window [T - window, T), as
+ * ascending ids; feeds kv_sparse_attn (contiguous runs of rows).
+ *
+ * scores: device fp32 [batch][n_heads][score_stride] (score_stride >=
+ * max_len).  sel: device int32 [batch][n_heads][sel_cap]; sel_count: device
+ * int32 [batch][n_heads]; a selection larger than sel_cap is cut and flags
+ * KVQ_DEV_OVERFLOW.  ceil(max_len / block) <= 24576 (UNSUPPORTED above).
+ * Two launches (the importances; the choice of blocks and the token ids).
+ * ws: kv_block_select_ws(seqs, n_heads, block_tokens) bytes.
+ * ---------------------------------------------------------------------- */
+int kv_block_select(const kvq_seqs* seqs, int32_t n_heads,
+                    const float* scores, int64_t score_stride,
+                    int32_t n_keep_fixed, double ratio, int32_t n_sink, int32_t window,
+                    int32_t block_tokens, int32_t* sel, int32_t sel_cap, int32_t* sel_count,
+                    void* ws, size_t ws_bytes, void* stream);
+size_t kv_block_select_ws(const kvq_seqs* seqs, int32_t n_heads, int32_t block_tokens);
+
+/* ------------------------------------------------------------------------
  * a6: kv_sparse_attn -- exact softmax attention over selected tokens
  * [Meeting §3.2: Softmax(Q K_ret^T / sqrt(d)) V_ret; Meeting §8.1].
  *

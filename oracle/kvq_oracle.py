@@ -424,10 +424,11 @@ def block_importance(scores, n_sink, window, block):
     """[Meeting §8.1] importance of every ``block``-token block (block j holds
     tokens [j*block, (j+1)*block) clipped to T): the mean of the approximate
     scores of its candidate tokens (n_sink <= t < T - window).  READING: the
-    page asks for the block mean but fixes no arithmetic; the sum runs in fp64
-    in ascending t, is divided by the candidate count in fp64 and rounded to
-    fp32, because the importance decides an integer (the kept blocks).  A
-    block without candidates gets -inf.  Returns fp32 [ceil(T / block)]."""
+    page asks for the block mean but fixes no arithmetic; it is taken in the
+    scores' own precision, an fp32 sum in ascending t divided by the
+    candidate count in fp32, in that fixed order because the importance
+    decides an integer (the kept blocks).  A block without candidates gets
+    -inf.  Returns fp32 [ceil(T / block)]."""
     scores = np.asarray(scores, dtype=np.float32)
     T = scores.shape[0]
     nb = -(-T // block)
@@ -435,10 +436,10 @@ def block_importance(scores, n_sink, window, block):
     for j in range(nb):
         lo, hi = max(j * block, n_sink), min((j + 1) * block, T - window)
         if lo < hi:
-            s = 0.0
-            for t in range(lo, hi):  # plain left-to-right fp64 sum
-                s += float(scores[t])
-            imp[j] = np.float32(s / (hi - lo))
+            s = np.float32(0.0)
+            for t in range(lo, hi):  # plain left-to-right fp32 sum
+                s = np.float32(s + scores[t])
+            imp[j] = np.float32(s / np.float32(hi - lo))
     return imp
 
 
