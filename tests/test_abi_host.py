@@ -66,6 +66,38 @@ def test_validation_rejects_before_launch(lib):
     assert lib.kv_page_append(by(L), by(P), by(S3), None, None, 256, 256, None) == _abi.KVQ_ERR_INVALID_ARG
 
 
+def test_block_select_validation(lib):
+    """kv_block_select rejects bad arguments on the host, before any launch."""
+    by = ctypes.byref
+    S = _abi.Seqs(None, None, 0, 8, 100, 0)
+    # block size, sink/window, ratio, capacity
+    assert lib.kv_block_select(by(S), 1, 8, 128, -1, 0.03, 4, 64, 0, 8, 16, 8, None, 0, None) \
+        == _abi.KVQ_ERR_INVALID_ARG
+    assert "block_tokens" in _abi.last_error()
+    assert lib.kv_block_select(by(S), 1, 8, 128, -1, 0.03, -1, 64, 64, 8, 16, 8, None, 0, None) \
+        == _abi.KVQ_ERR_INVALID_ARG
+    assert lib.kv_block_select(by(S), 1, 8, 128, -1, 1.5, 4, 64, 64, 8, 16, 8, None, 0, None) \
+        == _abi.KVQ_ERR_INVALID_ARG
+    assert lib.kv_block_select(by(S), 1, 8, 128, -1, 0.03, 4, 64, 64, 8, 0, 8, None, 0, None) \
+        == _abi.KVQ_ERR_INVALID_ARG
+    # score stride below max_len
+    assert lib.kv_block_select(by(S), 1, 8, 64, -1, 0.03, 4, 64, 64, 8, 16, 8, None, 0, None) \
+        == _abi.KVQ_ERR_INVALID_ARG
+    # more blocks per row than the selection CTA holds
+    S2 = _abi.Seqs(None, None, 0, 30000, 400000, 0)
+    need = lib.kv_block_select_ws(by(S2), 1, 16)
+    assert lib.kv_block_select(by(S2), 1, 8, 400000, -1, 0.03, 4, 64, 16, 8, 16, 8, None, need, None) \
+        == _abi.KVQ_ERR_UNSUPPORTED
+    # workspace too small
+    assert lib.kv_block_select(by(S), 1, 8, 128, -1, 0.03, 4, 64, 64, 8, 16, 8, None, 16, None) \
+        == _abi.KVQ_ERR_INVALID_ARG
+    # sizes: importances of every row, 256-byte aligned; 0 for invalid arguments
+    S3 = _abi.Seqs(None, None, 2, 8200, 131136, 0)
+    n = lib.kv_block_select_ws(by(S3), 32, 64)
+    assert n % 256 == 0 and n >= 256 + 2 * 32 * 2052 * 4
+    assert lib.kv_block_select_ws(by(S3), 0, 64) == 0 and lib.kv_block_select_ws(by(S3), 32, 0) == 0
+
+
 def test_workspace_sizes(lib):
     L = kvq.make_layout(32, 8, 1, 64)
     S = _abi.Seqs(None, None, 1, 8200, 131136, 0)
