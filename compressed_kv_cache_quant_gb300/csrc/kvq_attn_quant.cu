@@ -7,12 +7,12 @@
 // accumulate), one warp per 64-token group (one K quantization group = four
 // 16-token pages).  With K = scale_c * code + zero_c per channel of the group,
 //   s_t = sum_c (q_c scale_c) code_t[c] + sum_c q_c zero_c,
-// the first term is a [slots x 128] x [128 x tokens] product whose A operand
-// holds q_c scale_c 2^b (exact in fp32) split into two fp16 halves (hi and lo
-// slots, summed afterwards), and whose B operand is 1 + code / 2^b, made two
-// codes at a time by one shift and one AND/OR into the mantissa of fp16 1.0
-// (the codes are stored in pairs for that, kvq_k_code_pos); the bias
-// sum_c q_c scale_c 2^b joins the zero-point term.  With V = vscale_t
+// the first term is a [tokens x 128] x [128 x slots] product whose A operand
+// is 1 + code / 2^b, made two codes at a time by one shift and one AND/OR into
+// the mantissa of fp16 1.0 (the codes are stored in pairs for that,
+// kvq_k_code_pos), and whose B operand holds q_c scale_c 2^b (exact in fp32)
+// split into two fp16 halves (a hi and a lo column per head, summed
+// afterwards); the bias sum_c q_c scale_c 2^b joins the zero-point term.  With V = vscale_t
 // code + vzero_t per token and V group,
 //   o[d] = sum_t p_t (vscale_t code_t[d] + vzero_t)
 // is a [128 x tokens] x [tokens x heads] product: the V codes (stored
@@ -30,7 +30,9 @@ namespace {
 constexpr int D = KVQ_HEAD_DIM;
 constexpr int PG = KVQ_BLOCK_TOKENS;
 constexpr int KG = KVQ_K_GROUP_TOKENS;
-// warps per CTA (one CTA per SM): as many as the double-buffered group stages let fit
+// warps per CTA: 16 for 1- and 2-bit codes (one CTA per SM); 4-bit codes run in small CTAs
+// of 2 warps, several per SM (the measured best on a batch of MHA sequences of differing
+// lengths); 8-bit codes, whose staged groups are the largest, in CTAs of 4 warps
 template <int BITS>
 __host__ __device__ constexpr int nwarp_of() {
     return BITS <= 2 ? 16 : (BITS == 4 ? 2 : 4);
