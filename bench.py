@@ -33,6 +33,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -76,7 +77,7 @@ class Clocks:
     def __init__(self, gpu_index):
         self.proc, self.path = None, None
         try:
-            out = os.path.join(ROOT, "gpurun_out")
+            out = os.environ.get("KVQ_CLOCKS_DIR") or tempfile.gettempdir()  # the samples, summarised below
             os.makedirs(out, exist_ok=True)
             self.path = os.path.join(out, f"clocks_bench_{os.getpid()}.csv")
             self.f = open(self.path, "w")
