@@ -255,14 +255,14 @@ __global__ void __launch_bounds__(CS_NT, CS_MINB) crit_score_kernel(CritArgs a) 
 
 // Tensor-core form: a warp takes 16 listed rows at a time (its own tiles, staged SA_STAGES - 1
 // tiles ahead with cp.async).  Scores S^T (heads x 16 rows) = Q K^T with m16n8k16 products: A =
-// the q rows (heads; rows past the group's heads are zero), B = the K tile through ldmatrix.  The score
-// accumulators of a head are, element for element, the A fragment of P (heads x rows) for the
-// value product O += P V, B = the V tile through ldmatrix.trans.  Scores stay fp32 (fp16 q and
+// the q rows (heads; rows past the group's heads are zero), B = the K tile through ldmatrix.
+// The score accumulators of a head are, element for element, the A fragment of P (heads x rows)
+// for the value product O += P V, B = the V tile through ldmatrix.trans.  Scores stay fp32 (fp16 q and
 // k, exact products); p enters the value product in fp16 (2^-11 relative per weight).
 constexpr int SA_NW = 4;                       // warps per CTA
 constexpr int SA_NT = 32 * SA_NW;
 constexpr int SA_TR = 16;                      // rows per warp tile
-constexpr int SA_TILE = SA_TR * D * 2;         // bytes of one K or V tile (8 KB for K and V)
+constexpr int SA_TILE = SA_TR * D * 2;         // bytes of one K or V tile (4 KB; a stage holds both)
 constexpr int SA_STAGES = 2;                   // tiles per warp in flight or in use
 constexpr int SA_TILES = SA_NW * SA_STAGES * 2 * SA_TILE;  // [warp][stage][K, V]
 constexpr int SA_REC = 4 + D;
@@ -300,7 +300,6 @@ __device__ __forceinline__ uint32_t sa_pack_h2(float lo, float hi) {
 }
 // byte offset of 16-byte chunk c of tile row r (chunks XOR-swizzled by r mod 8: conflict-free ldmatrix)
 __device__ __forceinline__ uint32_t sa_chunk(int r, int c) { return (uint32_t)((r * 16 + (c ^ (r & 7))) * 16); }
-
 
 struct SAArgs {
     const uint16_t* k16;
