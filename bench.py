@@ -205,7 +205,8 @@ def _views(meta):
 
 
 def _oracle_task(args):
-    """One (layer, kv head) of a decode step on the CPU oracle; returns seconds."""
+    """One kv head of layer 0, or one q head of a sparse layer, of a decode step on the
+    CPU oracle; returns seconds."""
     from oracle import kvq_oracle as O
     kind, g, q, meta = args
     a = _views(meta)
@@ -217,14 +218,13 @@ def _oracle_task(args):
         pv = dict(codes=a["v_codes"][g], scale16=a["v_scale16"][g], zero16=a["v_zero16"][g], bits=1,
                   group_dims=64)
         O.decode_attn_quant(q, [pk], [pv])
-    else:
+    else:  # q is one q head of kv head g
         K, V = a["k1"][g], a["v1"][g]
         k = O.ratio_k(K.shape[0], RATIO)
-        for h in range(q.shape[0]):
-            C = O.critical_channels(q[h], O.key_absmax(K), N_CRIT)
-            s = O.critical_scores(q[h], K, C)
-            ids = O.topk_select(s, k, N_SINK, WINDOW)
-            O.sparse_attn(q[h], K, V, ids)
+        C = O.critical_channels(q, O.key_absmax(K), N_CRIT)
+        s = O.critical_scores(q, K, C)
+        ids = O.topk_select(s, k, N_SINK, WINDOW)
+        O.sparse_attn(q, K, V, ids)
     return time.perf_counter() - t
 
 
@@ -254,14 +254,14 @@ class OracleSample:
             self.meta[name] = (m.name, a.shape, a.dtype.str)
 
     def step_time(self, pool, q0, q1, n_layers):
-        """Oracle time of one decode step: layer 0 and one sparse layer on the
-        pool (8 kv-head tasks each), t_step = t0 + (n_layers - 1) * t1."""
+        """Oracle time of one decode step: layer 0 (8 kv-head tasks) and one sparse
+        layer (32 q-head tasks) on the pool, t_step = t0 + (n_layers - 1) * t1."""
         G = HQ // HKV
         t = time.perf_counter()
         pool.map(_oracle_task, [("quant", g, q0[g * G:(g + 1) * G], self.meta) for g in range(HKV)])
         t0 = time.perf_counter() - t
         t = time.perf_counter()
-        pool.map(_oracle_task, [("sparse", g, q1[g * G:(g + 1) * G], self.meta) for g in range(HKV)])
+        pool.map(_oracle_task, [("sparse", h // G, q1[h], self.meta) for h in range(HQ)], chunksize=1)
         t1 = time.perf_counter() - t
         return t0 + (n_layers - 1) * t1, t0, t1
 
@@ -317,7 +317,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    n_workers = args.cpu_workers or min(16, os.cpu_count() or 1)
+    n_workers = args.cpu_workers or (os.cpu_count() or 1)
 
     if args.impl == "reference":
         if rank != 0:
@@ -463,9 +463,10 @@ def main():
         sample.close()
         pool.close()
         cpu = {"value": 1.0 / t_step, "unit": "steps/s", "cores": n_workers, "kind": "oracle",
-               "sample": f"layer 0 (1-bit quantized) and one sparse layer, 8 kv-head tasks each, of a "
-                         f"{args.prompt}-token step on a {n_workers}-process pool; step time = t0 + "
-                         f"{args.layers - 1} x t_sparse = {t0c:.2f} s + {args.layers - 1} x {t1c:.2f} s"}
+               "sample": f"layer 0 (1-bit quantized, 8 kv-head tasks) and one sparse layer (32 q-head "
+                         f"tasks) of a {args.prompt}-token step on a {n_workers}-process pool (the host's "
+                         f"{os.cpu_count()} cores); step time = t0 + {args.layers - 1} x t_sparse = "
+                         f"{t0c:.2f} s + {args.layers - 1} x {t1c:.2f} s"}
 
     if rank == 0:
         value = world * args.steps / (ms * 1e-3)
@@ -845,9 +846,13 @@ def run_reference(args, n_workers):
             "vs_baseline": None, "dtype": "fp64 attention / fp32 quantizer (oracle)", "data": "synthetic",
             "config": workload_config(args, args.gpus),
             "cpu_baseline": {"value": value, "unit": "steps/s", "cores": n_workers, "kind": "oracle",
-                             "sample": "per step: layer 0 and one sparse layer timed on the process pool, "
+                             "sample": "per step: layer 0 and one sparse layer timed on the process pool "
+                                       f"({n_workers} processes, the host's {os.cpu_count()} cores), "
                                        f"extrapolated to {args.layers} layers; {n_time} steps timed "
                                        f"after {n_warm} warm-up steps"},
+            "extrapolated": f"ms_per_step is the mean of {n_time} sampled steps (each one layer 0 plus one "
+                            f"sparse layer scaled to {args.layers} layers); the wall time of this run is "
+                            f"shorter than steps x ms_per_step",
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 

@@ -8,7 +8,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, c_char_p, c_double, c_int, c_int32, c_int64, c_size_t, c_uint64, c_void_p
+from ctypes import POINTER, c_char_p, c_double, c_int, c_int32, c_int64, c_size_t, c_uint32, c_uint64, c_void_p
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libkvq.so")
@@ -25,6 +25,9 @@ ABI_VERSION = 1
 HEAD_DIM = 128
 BLOCK_TOKENS = 16
 K_GROUP_TOKENS = 64
+
+N_PATH_COUNTERS = 4
+PATH_LISTED, PATH_COMPACTED, PATH_RADIX_PASSES = 0, 1, 2
 
 
 class KvqError(RuntimeError):
@@ -66,6 +69,7 @@ PROTOTYPES = {
     "kv_decode_attn_quant_ws": (c_size_t, [PL, PS]),
     "kv_decode_attn_quant_noalloc": (c_int, [PL, PP, PS, VP, VP, VP]),
     "kv_decode_attn_quant_noalloc_max_scratch": (c_size_t, []),
+    "kv_decode_attn_quant_plan": (c_int, [PL, PS, c_int32, POINTER(c_int32), POINTER(c_int32)]),
     "kv_critical_score": (c_int, [PL, PP, PS, VP, c_int32, VP, VP, c_int64, VP]),
     "kv_topk_select": (c_int, [PS, c_int32, VP, c_int64, c_int32, c_double, c_int32, c_int32, VP, c_int32, VP,
                                VP, c_size_t, VP]),
@@ -94,6 +98,7 @@ PROTOTYPES = {
     "kvq_seq_lens_add": (c_int, [VP, c_int32, c_int32, VP]),
     "kv_page_copy": (c_int, [PL, PP, c_int32, c_int32, VP]),
     "kvq_check": (c_int, [VP, VP]),
+    "kvq_read_path_counters": (c_int, [VP, POINTER(c_uint32), VP]),
     "kvq_alloc_create": (VP, [c_int64, c_uint64]),
     "kvq_alloc_destroy": (None, [VP]),
     "kvq_block_alloc": (c_int, [VP, c_int32, POINTER(c_int32)]),

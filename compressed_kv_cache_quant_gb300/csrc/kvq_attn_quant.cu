@@ -639,6 +639,32 @@ extern "C" size_t kv_decode_attn_quant_ws(const kvq_layout* L, const kvq_seqs* S
     return ws_layout(L, S, plan_splits(L, S, false), &a, &c);
 }
 
+// The plan of the allocation-free variant: the default one if its scratch fits the built-in
+// array, else the one-wave plan; NO_SPACE if neither fits.
+static int noalloc_plan(const kvq_layout* L, const kvq_seqs* S, Plan* p, size_t* need, size_t* off_part,
+                        size_t* off_cnt);
+
+extern "C" int kv_decode_attn_quant_plan(const kvq_layout* L, const kvq_seqs* S, int32_t noalloc, int32_t* n_splits,
+                                         int32_t* groups_per_split) {
+    kvq_clear_error();
+    int st = kvq_check_layout(L, "kv_decode_attn_quant_plan", true);
+    if (st) return st;
+    st = kvq_check_seqs_sizes(S, "kv_decode_attn_quant_plan");
+    if (st) return st;
+    KVQ_REQUIRE(n_splits && groups_per_split, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_plan: NULL output");
+    Plan p;
+    if (noalloc) {
+        size_t need, a, c;
+        st = noalloc_plan(L, S, &p, &need, &a, &c);
+        if (st) return st;
+    } else {
+        p = plan_splits(L, S, false);
+    }
+    *n_splits = p.n_splits;
+    *groups_per_split = p.cps;
+    return KVQ_OK;
+}
+
 extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
                                     float* out, void* ws, size_t ws_bytes, void* stream) {
     kvq_clear_error();
@@ -728,6 +754,20 @@ static int qattn_scratch(void** out) {
 
 extern "C" size_t kv_decode_attn_quant_noalloc_max_scratch(void) { return KVQ_NOALLOC_SCRATCH_BYTES; }
 
+static int noalloc_plan(const kvq_layout* L, const kvq_seqs* S, Plan* p, size_t* need, size_t* off_part,
+                        size_t* off_cnt) {
+    *p = plan_splits(L, S, false);
+    *need = ws_layout(L, S, *p, off_part, off_cnt);
+    if (*need > KVQ_NOALLOC_SCRATCH_BYTES) {  // fewer splits, if that fits
+        *p = plan_splits(L, S, true);
+        *need = ws_layout(L, S, *p, off_part, off_cnt);
+    }
+    KVQ_REQUIRE(*need <= KVQ_NOALLOC_SCRATCH_BYTES, KVQ_ERR_NO_SPACE,
+                "kv_decode_attn_quant_noalloc: this batch needs %zu bytes of scratch, the built-in array holds %u; "
+                "use kv_decode_attn_quant with a workspace", *need, KVQ_NOALLOC_SCRATCH_BYTES);
+    return KVQ_OK;
+}
+
 extern "C" int kv_decode_attn_quant_noalloc(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S,
                                             const uint16_t* q, float* out, void* stream) {
     kvq_clear_error();
@@ -741,16 +781,10 @@ extern "C" int kv_decode_attn_quant_noalloc(const kvq_layout* L, const kvq_pool*
     KVQ_REQUIRE((((uintptr_t)P->k_codes | (uintptr_t)P->v_codes | (uintptr_t)P->k_sz | (uintptr_t)P->v_sz) & 15u) == 0,
                 KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: code and scale arrays must be 16-byte aligned");
     KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: batch exceeds max_seqs");
-    size_t off_part, off_cnt;
-    Plan p = plan_splits(L, S, false);
-    size_t need = ws_layout(L, S, p, &off_part, &off_cnt);
-    if (need > KVQ_NOALLOC_SCRATCH_BYTES) {  // fewer splits, if that fits
-        p = plan_splits(L, S, true);
-        need = ws_layout(L, S, p, &off_part, &off_cnt);
-    }
-    KVQ_REQUIRE(need <= KVQ_NOALLOC_SCRATCH_BYTES, KVQ_ERR_NO_SPACE,
-                "kv_decode_attn_quant_noalloc: this batch needs %zu bytes of scratch, the built-in array holds %u; "
-                "use kv_decode_attn_quant with a workspace", need, KVQ_NOALLOC_SCRATCH_BYTES);
+    size_t off_part, off_cnt, need;
+    Plan p;
+    st = noalloc_plan(L, S, &p, &need, &off_part, &off_cnt);
+    if (st) return st;
     if (S->batch == 0) return KVQ_OK;
     KVQ_REQUIRE(q && out && S->block_table, KVQ_ERR_INVALID_ARG,
                 "kv_decode_attn_quant_noalloc: NULL q/out/block table");

@@ -33,7 +33,8 @@ static inline cudaStream_t kvq_stream(void* s) { return reinterpret_cast<cudaStr
 struct KvqWsHeader {
     int32_t status;      // 0 = clean; otherwise the first failing check
     int32_t detail;      // an index describing the failure
-    int32_t pad[62];
+    uint32_t path[KVQ_N_PATH_COUNTERS];  // diagnostics: how many CTAs took which code path
+    int32_t pad[62 - KVQ_N_PATH_COUNTERS];
 };
 static_assert(sizeof(KvqWsHeader) == 256, "workspace header is 256 bytes");
 
@@ -53,6 +54,11 @@ __host__ __device__ static inline size_t kvq_round_up(size_t x, size_t a) { retu
 
 __device__ __forceinline__ void kvq_dev_flag(KvqWsHeader* h, int32_t code, int32_t detail) {
     if (h != nullptr && atomicCAS(&h->status, 0, code) == 0) h->detail = detail;
+}
+
+// Counts one use of code path `which` (KVQ_PATH_*) in the workspace header.
+__device__ __forceinline__ void kvq_dev_count(KvqWsHeader* h, int which) {
+    if (h != nullptr) atomicAdd(&h->path[which], 1u);
 }
 
 __device__ __forceinline__ float kvq_h2f(uint16_t x) { return __half2float(__ushort_as_half(x)); }

@@ -1,6 +1,7 @@
 // libkvq runtime: error reporting, device helpers, workspace status check and
 // the host page allocator (free list + reference counts for shared pages).
 #include <stdarg.h>
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -151,6 +152,19 @@ extern "C" int kvq_check(void* ws, void* stream) {
         if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kvq_check: %s", cudaGetErrorString(e));
         return kvq_fail(KVQ_ERR_DEVICE_CHECK, "device check failed: %s (detail %d)", nm, hdr[1]);
     }
+    return KVQ_OK;
+}
+
+extern "C" int kvq_read_path_counters(void* ws, uint32_t* out, void* stream) {
+    kvq_clear_error();
+    KVQ_REQUIRE(ws != nullptr && out != nullptr, KVQ_ERR_INVALID_ARG, "kvq_read_path_counters: NULL argument");
+    cudaStream_t s = kvq_stream(stream);
+    void* dev = static_cast<char*>(ws) + offsetof(KvqWsHeader, path);
+    const size_t n = sizeof(uint32_t) * KVQ_N_PATH_COUNTERS;
+    cudaError_t e = cudaMemcpyAsync(out, dev, n, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dev, 0, n, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kvq_read_path_counters: %s", cudaGetErrorString(e));
     return KVQ_OK;
 }
 

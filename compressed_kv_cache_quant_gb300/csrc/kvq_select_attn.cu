@@ -736,6 +736,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                 listed = s.n_s <= CAP_S && a.sel == nullptr;
             } else {
                 // ---- fallback (many candidates share digit 1, e.g. heavy ties): distributed passes
+                if (tid == 0 && rank == 0) kvq_dev_count(a.hdr, KVQ_PATH_RADIX_PASSES);
                 uint32_t prefix = b1;
                 for (int pass = 0; pass < 2; ++pass) {
                     const int shift = pass == 0 ? 10 : 0;
@@ -857,7 +858,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         }
         plist = keys;
     }
-    if (tid == 0) s.sel_cnt = nl;
+    if (tid == 0) {
+        s.sel_cnt = nl;
+        kvq_dev_count(a.hdr, listed ? KVQ_PATH_LISTED : KVQ_PATH_COMPACTED);
+    }
     __syncthreads();
 
     if (a.sel != nullptr) {

@@ -177,6 +177,14 @@ def kv_decode_attn_quant_noalloc_max_scratch():
     return lib().kv_decode_attn_quant_noalloc_max_scratch()
 
 
+def kv_decode_attn_quant_plan(cache, seqs, noalloc=False):
+    """(n_splits, groups_per_split) the quantized attention uses for this batch."""
+    n, g = ctypes.c_int32(0), ctypes.c_int32(0)
+    check(lib().kv_decode_attn_quant_plan(_ref(cache.layout), _ref(seqs), int(bool(noalloc)), ctypes.byref(n),
+                                          ctypes.byref(g)), "kv_decode_attn_quant_plan")
+    return n.value, g.value
+
+
 def kv_critical_score(cache, seqs, q, n_crit, crit, scores, score_stride=None, stream=None):
     if score_stride is None:
         score_stride = scores.shape[-1]
@@ -307,3 +315,10 @@ def kv_page_copy(cache, src, dst, stream=None):
 
 def kvq_check(ws, stream=None):
     return check(lib().kvq_check(ws.ptr, _s(stream)), "kvq_check")
+
+
+def kvq_read_path_counters(ws, stream=None):
+    """The workspace's diagnostic path counters (KVQ_PATH_*), read and cleared."""
+    out = (ctypes.c_uint32 * _abi.N_PATH_COUNTERS)()
+    check(lib().kvq_read_path_counters(ws.ptr, out, _s(stream)), "kvq_read_path_counters")
+    return [int(out[i]) for i in range(_abi.N_PATH_COUNTERS)]

@@ -32,7 +32,9 @@
  *     *_ws() function returns, 256-byte aligned, ZERO-FILLED BEFORE FIRST USE.
  *     The library leaves them zeroed after every call that completes, so they
  *     can be reused; after a call that failed on the device, zero them again.
- *     Two calls that share a workspace must not run concurrently.
+ *     The one exception is a handful of diagnostic path counters in the first
+ *     256 bytes (kvq_read_path_counters), which kernels only add to and never
+ *     read.  Two calls that share a workspace must not run concurrently.
  *   - Data-dependent device errors (a page id outside the pool, a selected id
  *     outside the sequence) skip the faulty access and set a status word in
  *     the workspace; kvq_check() reads and clears it.  Nothing traps.
@@ -54,6 +56,16 @@ extern "C" {
 #define KVQ_ERR_NO_SPACE      -4
 #define KVQ_ERR_TIMEOUT       -5
 #define KVQ_ERR_DEVICE_CHECK  -6
+
+/* Diagnostic path counters in a workspace header (kvq_read_path_counters). */
+#define KVQ_N_PATH_COUNTERS    4
+#define KVQ_PATH_LISTED        0  /* sparse-layer CTAs that attended their kept rows from the
+                                     one-pass list (no ordered compaction) */
+#define KVQ_PATH_COMPACTED     1  /* sparse-layer CTAs that compacted their kept positions in order
+                                     (a `sel` output, everything kept, or a list overflow) */
+#define KVQ_PATH_RADIX_PASSES  2  /* selections (clusters) whose first-digit candidates overflowed
+                                     their slots and took distributed radix passes */
+#define KVQ_PATH_RESERVED      3
 
 #define KVQ_HEAD_DIM          128
 #define KVQ_BLOCK_TOKENS      16
@@ -217,7 +229,10 @@ size_t kv_decode_attn_quant_ws(const kvq_layout* layout, const kvq_seqs* seqs);
  * the process exits.  No call allocates or frees memory.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture.  The address stays cached for the life of the process:
+ *     after cudaDeviceReset (or anything else that destroys the device's
+ *     primary context) the library must be unloaded and loaded again before
+ *     this entry point is called on that device.
  *   - A batch whose scratch (kv_decode_attn_quant_ws) exceeds the array is
  *     rejected with KVQ_ERR_NO_SPACE before anything is launched.
  *   - All calls share the array and each clears the parts that must start at
@@ -228,6 +243,15 @@ size_t kv_decode_attn_quant_ws(const kvq_layout* layout, const kvq_seqs* seqs);
 int kv_decode_attn_quant_noalloc(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
                                  const uint16_t* q, float* out, void* stream);
 size_t kv_decode_attn_quant_noalloc_max_scratch(void);
+
+/* The split of the context kv_decode_attn_quant (noalloc == 0) or
+ * kv_decode_attn_quant_noalloc (noalloc != 0) uses for this layout and batch:
+ * *n_splits CTAs per (sequence, group of up to 4 q heads), each taking
+ * *groups_per_split consecutive 64-token groups.  Host only; no launch.
+ * Errors: INVALID_ARG / UNSUPPORTED as the attention call would report;
+ * NO_SPACE for a noalloc batch beyond the built-in array. */
+int kv_decode_attn_quant_plan(const kvq_layout* layout, const kvq_seqs* seqs, int32_t noalloc,
+                              int32_t* n_splits, int32_t* groups_per_split);
 
 /* ------------------------------------------------------------------------
  * a4: kv_critical_score -- approximate token scores from critical channels
@@ -449,6 +473,12 @@ int kv_page_copy(const kvq_layout* layout, const kvq_pool* pool, int32_t src, in
  * Returns KVQ_OK, KVQ_ERR_DEVICE_CHECK (with the failing check in
  * kvq_last_error) or KVQ_ERR_CUDA. */
 int kvq_check(void* ws, void* stream);
+
+/* Synchronizes the stream, copies the KVQ_N_PATH_COUNTERS diagnostic counters
+ * of a workspace header to out[] (host) and clears them.  The counters tell
+ * which code paths the kernels that used this workspace took (KVQ_PATH_*);
+ * they never change a result. */
+int kvq_read_path_counters(void* ws, uint32_t* out, void* stream);
 
 /* ------------------------------------------------------------------------
  * Host page allocator [KVSurvey §一.1-§一.2]: free list of physical pages,

@@ -198,3 +198,48 @@ def test_block_count():
     assert O.block_count(131072, 0.03, 64) == 61
     assert O.block_count(4096, 0.03, 64) == 1
     assert O.block_count(100, 0.5, 64) == 1
+
+
+@pytest.mark.parametrize("case", ["normal", "critical_scores", "ties", "near_ties"])
+def test_block_mean_fp32_agrees_with_exact_mean_except_near_ties(case):
+    """The block importance is an fp32 mean (the scores' own precision, summed in a
+    fixed order).  Against the exact mean (a rational number, here in fp64 over
+    fp32 inputs, whose error is far below 1e-5 relative), the kept blocks are the
+    same except where the two blocks exchanged at the cut have exact means within
+    1e-5 relative of each other -- the near-tie allowance of the selection."""
+    rng = np.random.default_rng({"normal": 1, "critical_scores": 2, "ties": 3, "near_ties": 4}[case])
+    for rep in range(20):
+        T, B = int(rng.integers(2000, 9000)), int(rng.choice([16, 64, 128]))
+        ns, W = 4, 128
+        if case == "normal":
+            s = rng.standard_normal(T).astype(np.float32)
+        elif case == "critical_scores":  # sums of 8 products of fp16 values, like the critical scores
+            q = rng.standard_normal(8).astype(np.float16).astype(np.float32)
+            K = (rng.standard_normal((T, 8)) * np.where(rng.random(8) < 0.5, 10, 1)).astype(np.float16)
+            s = np.zeros(T, np.float32)
+            for c in range(8):
+                s = s + q[c] * K[:, c].astype(np.float32)
+        elif case == "ties":  # whole blocks repeat: many exactly equal means
+            base = rng.standard_normal(B).astype(np.float32)
+            s = np.tile(base, -(-T // B))[:T] * rng.choice([1.0, 1.0, 0.5], size=-(-T // B)).repeat(B)[:T]
+            s = s.astype(np.float32)
+        else:  # a block whose mean differs from another's by a rounding or two
+            s = rng.standard_normal(T).astype(np.float32)
+            j0, j1 = 3, 7
+            s[j1 * B:(j1 + 1) * B] = s[j0 * B:(j0 + 1) * B][::-1]
+        nb = -(-T // B)
+        n = int(rng.integers(1, max(2, nb // 3)))
+        imp32 = O.block_importance(s, ns, W, B)
+        exact = np.full(nb, -np.inf)
+        for j in range(nb):
+            lo, hi = max(j * B, ns), min((j + 1) * B, T - W)
+            if lo < hi:
+                exact[j] = float(np.sum(s[lo:hi].astype(np.float64))) / (hi - lo)
+        keep32 = set(np.lexsort((np.arange(nb), -imp32.astype(np.float64)))[:n].tolist())
+        keep64 = set(np.lexsort((np.arange(nb), -exact))[:n].tolist())
+        assert set(O.block_select(s, n, ns, W, B).tolist()) >= {t for j in keep32 for t in range(j * B, min((j + 1) * B, T))}
+        only32, only64 = keep32 - keep64, keep64 - keep32
+        assert len(only32) == len(only64)
+        for a in only32:
+            for b in only64:
+                assert abs(exact[a] - exact[b]) <= 1e-5 * max(abs(exact[a]), abs(exact[b])), (case, rep, a, b)

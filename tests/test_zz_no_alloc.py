@@ -64,3 +64,30 @@ def test_noalloc_rejects_batches_beyond_the_array():
                                                 None, None, None)
     assert st == _abi.KVQ_ERR_NO_SPACE
     assert "scratch" in _abi.last_error()
+
+
+def test_noalloc_compact_plan_when_the_default_does_not_fit():
+    """A batch whose default split needs more scratch than the built-in array (16
+    sequences of 32 MHA heads, one of them 65536 tokens long): the allocation-free
+    call plans fewer, longer splits, and twice in a row still gives the workspace
+    version's result."""
+    require_gpu()
+    lengths = [65536] + [100 + 7 * i for i in range(15)]
+    cache, batch = _layer(4, 32, 32, 32, lengths, synth.mix(synth.BASE_SEED, 902))
+    assert kvq.kv_decode_attn_quant_ws(cache, batch) > kvq.kv_decode_attn_quant_noalloc_max_scratch()
+    plan_ws = kvq.kv_decode_attn_quant_plan(cache, batch)
+    plan_na = kvq.kv_decode_attn_quant_plan(cache, batch, noalloc=True)
+    assert plan_na[0] < plan_ws[0], (plan_na, plan_ws)
+    B, Hq = len(lengths), 32
+    q = synth.queries((B, Hq, 128), synth.mix(synth.BASE_SEED, 903)).cuda()
+    ref = torch.empty((B, Hq, 128), device="cuda")
+    kvq.kv_decode_attn_quant(cache, batch, q, ref, ws(kvq.kv_decode_attn_quant_ws(cache, batch)))
+    r = ref.cpu().numpy()
+    for _ in range(2):
+        out = torch.full((B, Hq, 128), float("nan"), device="cuda")
+        kvq.kv_decode_attn_quant_noalloc(cache, batch, q, out)
+        torch.cuda.synchronize()
+        o = out.cpu().numpy()
+        for b in range(B):
+            for h in range(Hq):
+                assert attn_err(o[b, h], r[b, h]) <= ATTN_TOL, (b, h)
