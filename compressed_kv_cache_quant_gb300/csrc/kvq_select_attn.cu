@@ -217,6 +217,15 @@ __device__ __forceinline__ void prefetch_row_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(c + 128) : "memory");
 }
 
+// Row offset (in 128-element rows) of position t of kv head g of sequence b on page `page`; ROW_NEW
+// for the newest token (read from its source), ROW_NONE (flagged) for a page outside the pool.
+__device__ __forceinline__ uint32_t row_of(const SXArgs& a, int b, int g, int t, int t_new, int32_t page) {
+    if (t == t_new) return ROW_NEW;
+    if (page >= 0 && page < a.num_blocks) return (uint32_t)(((int64_t)page * a.H + g) * PG + (t & 15));
+    kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, t);
+    return ROW_NONE;
+}
+
 // acc[i] += q_c * K[p0 + i][c] for the 8 positions in `raw` (fp16); position p0 + inew is
 // the newest token, whose key `knew` is not in the channel-major copy's load yet.
 __device__ __forceinline__ void score_channel(const uint4& raw, float qc, bool has_new, int inew, uint16_t knew,
@@ -375,6 +384,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     uint32_t kth = 0xffffffffu;  // kept: key > kth, or key == kth and position <= cut
     int32_t cut = -1;
     bool listed = false;         // s.list holds this CTA's kept positions (the one-pass path)
+    int n_early = 0;             // s.list[0, n_early) already hold row offsets (rows in flight to L2)
+    const int gkv = a.q != nullptr ? h / a.GQ : 0;            // kv head of the attention
+    const int t_new = a.k_new != nullptr ? T - 1 : -1;        // the newest token: read from its source
     if (fused) {
         // ---- critical channels [TailorKV §2.3]: s_c = |q_c| max_t |K_c| with the newest token
         // included; the n_crit largest (ties -> lower channel), kept in ascending order
@@ -590,6 +602,22 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
             if (nq > 0) classify_group(lane < nq, lane < nq ? wq[lane] : 0u, keys, lo, cand_lo, cand_hi, hi_thr, s, lane);
             __syncthreads();
             const int n_s0 = (int)(s.nsc & 0xffffu), n_c0 = (int)(s.nsc >> 16);
+            // the positions kept so far (above bin b1, sinks and window: all but the few ties at the
+            // k-th key) are final.  Their pages are looked up now and their rows pulled into L2 while
+            // the candidates are exchanged and the last two digits found, so that the row traffic
+            // overlaps the rest of the selection (one-pass list path only)
+            static_assert(CAP_S == 2 * NT, "two early list entries per thread");
+            n_early = (a.q != nullptr && a.sel == nullptr) ? min(n_s0, CAP_S) : 0;
+            uint32_t e_pos[2];
+            int32_t e_pg[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = tid + j * NT;
+                e_pos[j] = i < n_early ? s.list[i] : 0u;
+                e_pg[j] = (i < n_early && (int)e_pos[j] != t_new)
+                              ? __ldg(a.bt + (int64_t)b * a.max_blocks + (e_pos[j] >> 4))
+                              : 0;
+            }
             // ---- every CTA's candidates (key bits 19..0) go to its slots in every CTA; the
             // target's local histogram is no longer read (see the cluster barrier above)
             {
@@ -612,7 +640,20 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                 s.n_c = n_c0;
                 s.nsm = 0u;
             }
-            cluster.sync();
+            cluster_arrive();  // the broadcast is released; the early rows go out meanwhile
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int i = tid + j * NT;
+                if (i < n_early) {
+                    const uint32_t r = row_of(a, b, gkv, (int)e_pos[j], t_new, e_pg[j]);
+                    s.list[i] = r;
+                    if (r < ROW_NEW) {
+                        prefetch_row_l2(a.k16 + (int64_t)r * D);
+                        prefetch_row_l2(a.v16 + (int64_t)r * D);
+                    }
+                }
+            }
+            cluster_wait();
             if (a.hist != nullptr && rank == 0)  // read by all: clear it for the next layer
                 for (int i = tid; i < H1; i += NT) a.hist[row * H1 + i] = 0u;
             bool ovf_c = false;
@@ -885,22 +926,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     if (a.q == nullptr) return;
 
     // ---- attention over this CTA's kept rows
-    const int g = h / a.GQ;
+    const int g = gkv;
     // the newest token (appended by this launch, possibly by another cluster) is read from its source
-    const int t_new = a.k_new != nullptr ? T - 1 : -1;
     const uint16_t* knew_row = a.k_new != nullptr ? a.k_new + ((int64_t)b * a.H + g) * D : nullptr;
     const uint16_t* vnew_row = a.k_new != nullptr ? a.v_new + ((int64_t)b * a.H + g) * D : nullptr;
     uint32_t* rows = const_cast<uint32_t*>(plist);  // positions -> row offsets (in 128-element rows)
-    for (int i = tid; i < (int)nl; i += NT) {
+    for (int i = (listed ? n_early : 0) + tid; i < (int)nl; i += NT) {
         const int t = (int)plist[i];
-        uint32_t r = ROW_NONE;
-        if (t == t_new) {
-            r = ROW_NEW;
-        } else {
-            const int32_t page = a.bt[(int64_t)b * a.max_blocks + (t >> 4)];
-            if (page >= 0 && page < a.num_blocks) r = (uint32_t)(((int64_t)page * a.H + g) * PG + (t & 15));
-            else kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, t);
-        }
+        const int32_t page = t == t_new ? 0 : a.bt[(int64_t)b * a.max_blocks + (t >> 4)];
+        const uint32_t r = row_of(a, b, g, t, t_new, page);
         rows[i] = r;
         // every kept row goes to L2 now; the batches below then mostly hit L2
         if (r < ROW_NEW) {
