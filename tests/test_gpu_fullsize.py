@@ -5,7 +5,8 @@ serving-batch row run, through the C ABI, against the oracle.
   benchmark calls it (no score copy, no selection output): every CTA attends
   its kept rows from the one-pass list; all 32 heads against the oracle's
   critical scores, top-K and exact attention.  A second case keeps about
-  1000 rows per CTA, next to the list capacity, so that some CTAs compact.
+  1000 rows per CTA, next to the list capacity, so that some CTAs compact; a
+  third runs 200000 tokens.
 * Layer 0 of the same step (1-bit K and V, groups of 64) at 131072 + 60
   prompt tokens plus 8 appended ones (a 64-token group completes during the
   appends): every warp of a CTA walks several groups through its double
@@ -45,13 +46,15 @@ def _sparse_layer(T, seed):
     return K, V, cache, batch, bt, alloc
 
 
-@pytest.mark.parametrize("k_fixed,ratio", [(-1, 0.03),      # the benchmark's selection: K = floor(0.03 T)
-                                           (7900, 0.0)])    # ~1000 kept rows per CTA (list capacity 1024)
-def test_sparse_layer_bench_path_128k(k_fixed, ratio):
+@pytest.mark.parametrize("T,k_fixed,ratio", [
+    (131072 + 5, -1, 0.03),     # the benchmark's selection: K = floor(0.03 T), four CTAs per head
+    (131072 + 5, 7900, 0.0),    # ~1000 kept rows per CTA, next to the list capacity (1024)
+    (200000, -1, 0.03),         # a longer context: ~750 kept rows per CTA
+])
+def test_sparse_layer_bench_path_long(T, k_fixed, ratio):
     require_gpu()
-    T = 131072 + 5
     n_crit, ns, w = 8, 4, 128
-    seed = synth.mix(synth.BASE_SEED + 1, 300, k_fixed)
+    seed = synth.mix(synth.BASE_SEED + 1, 300, k_fixed, T)
     K, V, cache, batch, bt, _ = _sparse_layer(T, seed)
     q = synth.queries((1, HQ, 128), synth.mix(seed, 1))
     out = torch.full((1, HQ, 128), float("nan"), device="cuda")
@@ -60,9 +63,9 @@ def test_sparse_layer_bench_path_128k(k_fixed, ratio):
                                k_fixed, ratio, ns, w, out, wk)
     kvq.kvq_check(wk)
     listed, compacted, radix, _ = kvq.kvq_read_path_counters(wk)
-    assert listed + compacted == HQ * 8 and radix == 0
+    assert listed + compacted == HQ * 8 and radix == 0   # one cluster of 8 CTAs per q head
     if k_fixed < 0:
-        assert listed == HQ * 8       # ~510 kept rows per CTA: every CTA attends from its one-pass list
+        assert compacted == 0         # every CTA attends its kept rows from the one-pass list
     else:
         assert listed > 0             # the CTAs whose kept rows fit the list; the others compact in order
     o = out.cpu().numpy()
