@@ -15,9 +15,14 @@ algorithmic bytes (packed K/V + scales of layer 0, critical-channel keys,
 score writes and selected fp16 rows of layers 1-31).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvq|reference]
-                  [--prompt T0] [--layers L] [--no-e2e] [--no-cpu-baseline]
-  python bench.py --rows    # the other rows (pack, INT4 batch attention, H2O step, offload
-                            # gather, tiny-config kernels), one JSON line each
+                  [--prompt T0] [--layers L] [--no-e2e] [--no-cpu-baseline] [--no-rows]
+  python bench.py --rows [--only NAME...]   # the other rows alone
+
+After the decode step, the same line carries under "rows" the other rows of
+the hot path, each timed on its own configuration with its own clock samples:
+the 40-layer 1-bit prefill pack (GB/s), the INT4 serving batch (steps/s), the
+H2O eviction run (steps/s), the offload gather pipeline (host-link GB/s and
+overlap fraction), block pruning, and the tiny-configuration kernels.
 
 For N > 1 (torchrun) every rank runs an independent replica on its own GPU
 (the path has no cross-GPU exchange); value = all ranks' steps / max time.
@@ -307,10 +312,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-workers", type=int, default=0)
     ap.add_argument("--rows", action="store_true",
-                    help="instead of the step: time the other hot-path rows on their configurations, one JSON line each")
+                    help="instead of the step: time the other hot-path rows on their configurations (one JSON line)")
+    ap.add_argument("--only", nargs="*", default=None, help="with --rows: the rows whose names start with these")
+    ap.add_argument("--no-rows", action="store_true", help="the decode step only, without the other rows")
     args = ap.parse_args()
     if args.rows:
-        run_rows(args)
+        import torch
+
+        from compressed_kv_cache_quant_gb300.build import build
+        build()
+        dev = torch.device("cuda", 0)
+        print(json.dumps({"rows": run_rows(dev, torch.cuda.Stream(dev), args.only)}))
         return
     assert args.warmup >= 1 and args.steps >= 1 and args.layers >= 2
 
@@ -468,6 +480,15 @@ def main():
                          f"{os.cpu_count()} cores); step time = t0 + {args.layers - 1} x t_sparse = "
                          f"{t0c:.2f} s + {args.layers - 1} x {t1c:.2f} s"}
 
+    # ---- the other rows of the hot path, each on its own configuration (rank 0, after the step)
+    rows = None
+    launches = W.launches_per_step * args.steps
+    if rank == 0 and not args.no_rows:
+        del W, g0, g_step, qs, ks, vs
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        rows = run_rows(device, stream)
+
     if rank == 0:
         value = world * args.steps / (ms * 1e-3)
         line = {
@@ -482,32 +503,45 @@ def main():
                          "traffic": tr["bytes_per_launch_scaled"] if tr else None,
                          "algorithmic_bytes_per_launch": kb[dom]},
             "kernels": per_kernel,
-            "e2e": e2e, "gpu_launches": W.launches_per_step * args.steps,
+            "e2e": e2e, "gpu_launches": launches,
             "clocks": clk, "cpu_baseline": cpu,
+            "rows": rows,
         }
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
 
 
-# ------------------------------------------------------------------------ per-row measurements (--rows)
+# ------------------------------------------------------------------------ the other rows
 #
-# The hot-path rows outside the headline step, each timed on its configuration with CUDA
-# events on the launching stream (inputs larger than L2 where the row streams memory), next
-# to a bounded single-threaded sample of the oracle doing the same work.
+# Every other row of the hot path on its configuration: CUDA events on the launching stream
+# around enough calls to fill a fraction of a second (inputs larger than L2 wherever a row
+# streams memory), nvidia-smi clocks sampled during that region, and a bounded single-threaded
+# sample of the oracle doing the same work.  Each row's inputs are built first and freed
+# after it, so that the rows run one after another in the same process as the decode step.
 
-def _ev_ms(torch, fn, stream, reps, warm=2):
-    torch.cuda.synchronize()  # inputs made on other streams are complete
+def _timed(torch, fn, stream, min_ms=250.0, warm=2):
+    """(ms per call, calls, clocks) of fn(), which launches on `stream`: CUDA events on that
+    stream around enough calls to fill about min_ms of device time."""
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         for _ in range(warm):
             fn()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+    stream.synchronize()
+    reps = max(3, min(2000, int(math.ceil(min_ms / max(a.elapsed_time(b), 1e-3)))))
+    clocks = Clocks(torch.cuda.current_device())
+    with torch.cuda.stream(stream):
         a.record(stream)
         for _ in range(reps):
             fn()
         b.record(stream)
     stream.synchronize()
-    return a.elapsed_time(b) / reps
+    clk = clocks.stop()
+    return a.elapsed_time(b) / reps, reps, clk
 
 
 def _wall(fn):
@@ -516,295 +550,432 @@ def _wall(fn):
     return time.perf_counter() - t
 
 
-def _paged(torch, kvq, lengths, device, seed):
-    """Block table over a shuffled allocator, one row per sequence."""
-    pages = [-(-int(T) // 16) for T in lengths]
-    alloc = kvq.Allocator(sum(pages) + 4, seed=seed)
-    mb = max(pages)
-    bt = torch.full((len(lengths), mb), -1, dtype=torch.int32)
-    for b, n in enumerate(pages):
-        bt[b, :n] = torch.tensor(alloc.alloc(n), dtype=torch.int32)
-    seqs = kvq.Batch(bt.to(device), torch.tensor([int(T) for T in lengths], dtype=torch.int32, device=device),
-                     max(int(T) for T in lengths))
-    return seqs, sum(pages) + 4, alloc
+def _hbm(peak, peak_src):
+    def f(achieved):
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": peak_src}
+    return f
 
 
-def _row_line(row, config, value, unit, roof, cpu, extra=None):
-    line = {"row": row, "config": config, "value": value, "unit": unit, "roofline": roof, "cpu_baseline": cpu}
-    if extra:
-        line.update(extra)
-    print(json.dumps(line), flush=True)
+def _capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    return g
 
 
-def run_rows(args):
+def row_pack(torch, np, kvq, synth, O, device, stream, hbm):
+    """a1 kv_quant_pack, the Qwen-1.5-14B-shaped prefill: 40 layers x 40 kv heads x 131072 tokens
+    to 1 bit (K per channel g64, V per token G64), one call per layer."""
+    T, H, L, n_in = 131072, 40, 40, 8
+    seed = synth.BASE_SEED + 4
+    n_pages = T // 16
+    seqs = kvq.Batch(torch.arange(n_pages, dtype=torch.int32, device=device)[None],
+                     torch.tensor([T], dtype=torch.int32, device=device), T)
+    ins = [synth.kv_rows(T, H, synth.mix(seed, 200 + j), device=device) for j in range(n_in)]
+    caches = [kvq.LayerCache(H, H, 1, n_pages, 1, v_group_dims=64, device=device) for _ in range(L)]
+    sh = stream.cuda_stream
+
+    def all_layers():
+        for l in range(L):
+            K, V = ins[l % n_in]
+            kvq.kv_quant_pack(caches[l], seqs, 0, 0, T, K, V, stream=sh)
+    ms, reps, clk = _timed(torch, all_layers, stream)
+    nbytes = L * (2 * T * H * D * 2 + T * H * 48)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    k1, v1 = ins[0][0][:, 0].cpu().numpy(), ins[0][1][:, 0].cpu().numpy()
+    del ins, caches
+    t = _wall(lambda: (O.pack_k(k1, 1), O.pack_v(v1, 1, 64)))
+    return {"config": "Qwen-1.5-14B-shaped prefill: 40 layers x 40 kv heads x 131072 tokens to 1 bit (K per channel "
+                      "g64, V per token G64), one call per layer; 8 distinct 2.68 GB fp16 inputs cycled over the layers",
+            "value": gbs, "unit": "GB/s (pack of all layers)", "ms_all_layers": ms, "bytes": nbytes, "calls": reps,
+            "roofline": hbm(gbs), "clocks": clk,
+            "cpu_baseline": {"value": (T * D * 2 * 2 + T * 48) / t / 1e9, "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": f"one kv head of one layer ({T} tokens), numpy"}}
+
+
+def row_int4(torch, np, kvq, synth, O, device, stream, hbm):
+    """a3 kv_decode_attn_quant, the Llama-2-7B-shaped INT4 serving batch: 16 sequences with
+    lengths U[4096, 32768], 32 heads MHA, K 4-bit g64, V 4-bit G32, sequences 0-7 sharing a
+    2048-token prefix (128 reference-counted pages), shuffled page ids; a step is 32 layers."""
+    B, H, L, n_c, pre = 16, 32, 32, 4, 2048
+    seed = synth.BASE_SEED + 2
+    lens = [int(x) for x in synth.lengths_uniform(B, 4096, 32768, seed)]
+    pages = [-(-T // 16) for T in lens]
+    alloc = kvq.Allocator(sum(pages) + 4, seed=7)
+    bt = np.full((B, max(pages)), -1, dtype=np.int32)
+    for b in range(B):
+        start = 0
+        if 0 < b < 8:
+            bt[b, :pre // 16] = bt[0, :pre // 16]
+            for pg in bt[0, :pre // 16]:
+                alloc.ref(int(pg))
+            start = pre // 16
+        bt[b, start:pages[b]] = alloc.alloc(pages[b] - start)
+    seqs = kvq.Batch(torch.from_numpy(bt).to(device), torch.tensor(lens, dtype=torch.int32, device=device), max(lens))
+    caches = []
+    for c in range(n_c):
+        cache = kvq.LayerCache(H, H, 4, sum(pages) + 4, B, v_group_dims=32, device=device)
+        prefix = None
+        for b, T in enumerate(lens):
+            K, V = synth.kv_rows(T, H, synth.mix(seed, 10 + b, c), device=device)
+            if b == 0:
+                prefix = (K[:pre].clone(), V[:pre].clone())
+            elif b < 8:
+                K[:pre], V[:pre] = prefix
+            t0 = pre if 0 < b < 8 else 0
+            kvq.kv_quant_pack(cache, seqs, b, t0, T - t0, K[t0:], V[t0:])
+            if c == 0 and b == 0:
+                k0, v0 = K[:, 0].cpu().numpy(), V[:, 0].cpu().numpy()
+            del K, V
+        caches.append(cache)
+        del prefix
+    torch.cuda.synchronize()
+    q = synth.normal((L, B, H, D), synth.mix(seed, 99), device)
+    out = torch.empty((L, B, H, D), device=device)
+    ws = kvq.Workspace(kvq.kv_decode_attn_quant_ws(caches[0], seqs))
+    plan = kvq.kv_decode_attn_quant_plan(caches[0], seqs)
+    g = _capture(torch, lambda: [kvq.kv_decode_attn_quant(caches[l % n_c], seqs, q[l], out[l], ws,
+                                                         stream=stream.cuda_stream) for l in range(L)], stream)
+    ms, reps, clk = _timed(torch, g.replay, stream)
+    kvq.kvq_check(ws, stream=stream.cuda_stream)
+    tails = sum(T % 64 for T in lens) * H * D * 2
+    unique = (sum(lens) - 7 * pre) * H * 152 + tails
+    per_request = sum(lens) * H * 152 + tails
+    gbs = L * unique / (ms * 1e-3) / 1e9
+    q0 = q[0, 0, :1].cpu().numpy()
+    del caches, g
+    pk, pv = O.pack_k(k0, 4), O.pack_v(v0, 4, 32)
+    t = _wall(lambda: O.decode_attn_quant(q0, [pk], [pv]))
+    return {"config": f"Llama-2-7B-shaped INT4 serving batch: 16 sequences, T ~ U[4096, 32768] (sum {sum(lens)}), "
+                      "32 heads MHA, K 4-bit g64, V 4-bit G32, sequences 0-7 sharing 128 prefix pages, shuffled "
+                      "page ids; one step = 32 layers (4 distinct 1.7 GB layer caches cycled, each larger than L2)",
+            "value": 1e3 / ms, "unit": "steps/s", "ms_per_step": ms, "GBps_unique": gbs,
+            "bytes_per_step_unique": L * unique, "bytes_per_step_per_request": L * per_request,
+            "split_plan": {"n_splits": plan[0], "groups_per_split": plan[1]}, "steps": reps,
+            "roofline": hbm(gbs), "clocks": clk,
+            "cpu_baseline": {"value": (lens[0] * 152) / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"one (sequence, head) of {lens[0]} tokens, numpy fp64"}}
+
+
+def row_h2o(torch, np, kvq, synth, O, device, stream, hbm, steps=256):
+    """a2 + a6 + a7, the Llama-3-8B-shaped H2O eviction run: 8 sequences, 32 layers of 32 q / 8 kv
+    heads, 32768-token prompts, budget 6553 = 4 sinks + 2048 window + 4501 heavy hitters; step 0
+    picks the initial heavy hitters from one full-context attention, then every decode step
+    appends a token, attends the retained set (one list per kv head, probabilities out), adds the
+    group's probabilities to the cumulative scores, evicts down to budget - 1 and admits the
+    next token.  Queries prefer 64 hot keys per (layer, sequence, kv head) with Zipf(1.2) weights."""
+    B, Hq, Hkv, L, T0, budget, ns, w = 8, 32, 8, 32, 32768, 6553, 4, 2048
+    G, n_hot = Hq // Hkv, 64
+    seed = synth.BASE_SEED + 3
+    cap_tok = T0 + steps + 16
+    per = -(-cap_tok // 16)
+    alloc = kvq.Allocator(B * per, seed=11)
+    bt = torch.tensor([alloc.alloc(per) for _ in range(B)], dtype=torch.int32, device=device)
+    seqs = kvq.Batch(bt, torch.full((B,), T0, dtype=torch.int32, device=device), cap_tok)
+    caches = []
+    kn = torch.empty((L, steps, B, Hkv, D), dtype=torch.float16, device=device)
+    vn = torch.empty_like(kn)
+    qb = torch.empty((L, steps, B, Hq, D), dtype=torch.float16, device=device)
+    for l in range(L):
+        cache = kvq.LayerCache(Hq, Hkv, 16, B * per, B, device=device)
+        hot = torch.empty((B, Hkv, n_hot, D), dtype=torch.float16, device=device)
+        for b in range(B):
+            K, V = synth.kv_rows(T0 + steps, Hkv, synth.mix(seed, l, b), device=device)
+            kvq.kv_quant_pack(cache, seqs, b, 0, T0, K[:T0], V[:T0])
+            kn[l, :, b], vn[l, :, b] = K[T0:], V[T0:]
+            pos, _ = synth.h2o_hot_positions(synth.mix(seed, l, b), T0, n_hot)
+            hot[b] = K[pos.to(device)].permute(1, 0, 2)
+            if l == 0 and b == 0:
+                k00, v00 = K[:T0, 0].cpu().numpy(), V[:T0, 0].cpu().numpy()
+            del K, V
+        bank = synth.h2o_query_bank(hot.reshape(B * Hkv, n_hot, D), steps * G, synth.mix(seed, 900, l))
+        qb[l] = bank.view(B, Hkv, steps, G, D).permute(2, 0, 1, 3, 4).reshape(steps, B, Hq, D)
+        caches.append(cache)
+    cap = T0 + 2
+    retained = torch.zeros((L, B, Hkv, cap), dtype=torch.int32, device=device)
+    retained[..., :T0] = torch.arange(T0, dtype=torch.int32, device=device)
+    counts = torch.full((L, B, Hkv), T0, dtype=torch.int32, device=device)
+    cum = torch.zeros((L, B, Hkv, cap), device=device)
+    probs = torch.zeros((B, Hq, cap), device=device)
+    out = torch.empty((L, B, Hq, D), device=device)
+    in_q = torch.empty((L, B, Hq, D), dtype=torch.float16, device=device)
+    in_k = torch.empty((L, B, Hkv, D), dtype=torch.float16, device=device)
+    in_v = torch.empty_like(in_k)
+    wsa = kvq.Workspace(kvq.kv_sparse_attn_ws(caches[0], seqs, cap))
+    wsh = kvq.Workspace(kvq.kv_h2o_accumulate_ws())
+    wsp = kvq.Workspace(kvq.kv_page_append_ws())
+    sh = stream.cuda_stream
+    torch.cuda.synchronize()
+    # step 0: the initial heavy hitters from one full-context attention per layer (not timed)
+    with torch.cuda.stream(stream):
+        for l in range(L):
+            kvq.kv_sparse_attn(caches[l], seqs, qb[l, 0], retained[l], counts[l], 1, out[l], probs, wsa, stream=sh)
+            kvq.kv_h2o_accumulate(caches[l], seqs, probs, retained[l], counts[l], cum[l], budget, ns, w,
+                                  seqs.seq_lens, None, wsh, stream=sh)
+    stream.synchronize()
+
+    def one_step():
+        kvq.kvq_seq_lens_add(seqs.seq_lens, 1, stream=sh)
+        for l in range(L):
+            kvq.kv_page_append(caches[l], seqs, in_k[l], in_v[l], wsp, stream=sh)
+            kvq.kv_sparse_attn(caches[l], seqs, in_q[l], retained[l], counts[l], 1, out[l], probs, wsa, stream=sh)
+            kvq.kv_h2o_accumulate(caches[l], seqs, probs, retained[l], counts[l], cum[l], budget, ns, w,
+                                  seqs.seq_lens, None, wsh, stream=sh)
+    g = _capture(torch, one_step, stream)
+
+    def feed(s):
+        in_q.copy_(qb[:, s], non_blocking=True)
+        in_k.copy_(kn[:, s - 1], non_blocking=True)
+        in_v.copy_(vn[:, s - 1], non_blocking=True)
+    torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device())
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for s in range(1, steps):
+            feed(s)
+            g.replay()
+        e.record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    for x in (wsa, wsh, wsp):
+        kvq.kvq_check(x, stream=sh)
+    ms = a.elapsed_time(e) / (steps - 1)
+    n_ret = int(counts.sum().item()) // (L * B * Hkv)
+    rows = B * Hkv * budget * 2 * D * 2
+    book = B * Hkv * budget * 12 + B * Hq * budget * 8   # ids + cum read/write, probabilities write + read
+    nbytes = L * (rows + book)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del caches, g, kn, vn, qb
+    r0 = np.concatenate([np.arange(ns), np.sort(np.random.default_rng(5).choice(np.arange(ns, T0 - w), budget - ns - w,
+                                                                                   replace=False)),
+                         np.arange(T0 - w, T0)])
+    qg = synth.normal((G, D), 17, "cpu").numpy()
+    t = _wall(lambda: O.h2o_step(qg, k00, v00, r0, np.zeros(budget), T0 - 1, budget, ns, w))
+    return {"config": "Llama-3-8B-shaped H2O eviction: 8 sequences, 32 layers of 32 q / 8 kv heads (GQA 4), 32768-token "
+                      "prompts, budget 6553 = 4 sinks + 2048 window + 4501 heavy hitters, power-law queries; one step = "
+                      "append + attention over the retained set + accumulate / evict / admit in every layer",
+            "value": 1e3 / ms, "unit": "steps/s", "ms_per_step": ms, "steps": steps - 1,
+            "retained_per_kv_head": n_ret, "GBps": gbs, "bytes_per_step": nbytes,
+            "roofline": hbm(gbs), "clocks": clk,
+            "cpu_baseline": {"value": 1.0 / (t * L * B * Hkv), "unit": "steps/s", "cores": 1, "kind": "oracle",
+                             "sample": "one (sequence, kv head, layer) step of the oracle, numpy fp64, times 2048"}}
+
+
+def row_offload(torch, np, kvq, synth, O, device, stream):
+    """a9, the Qwen-1.5-14B-shaped offload: 40 layers of 40 MHA heads at 131072 tokens, fp16 K/V in
+    pinned host memory; per layer the top-K (K = 3932) rows of every head are gathered over the
+    host link into an HBM double buffer while the previous layer attends."""
+    from compressed_kv_cache_quant_gb300.offload import OffloadLayers
+    H, T, L, n_res = 40, 131072, 40, 2
+    seed = synth.BASE_SEED + 4
+    KV = [synth.kv_rows(T, H, synth.mix(seed, 300 + j), device=device) for j in range(n_res)]
+    off = OffloadLayers(H, T, KV, [l % n_res for l in range(L)], device=device)
+    k0 = KV[0][0][:, 0].cpu().numpy()
+    del KV
+    torch.cuda.empty_cache()
+    qs = synth.normal((L, 1, H, D), synth.mix(seed, 301), device)
+    outs = torch.empty((L, 1, H, D), device=device)
+    copy_s = torch.cuda.Stream(device, priority=0)
+    attn_s = torch.cuda.Stream(device, priority=-1)   # the attention's CTAs go first when SMs free up
+
+    def pipelined():
+        off.step(qs, outs, copy_s, attn_s)
+
+    def gathers():            # the host-link side alone
+        for l in range(L):
+            off.gather(l, l % 2, attn_s)
+
+    def compute():            # the GPU side alone: selection and attention of every layer
+        for l in range(L):
+            off.select(l, qs[l], l % 2, attn_s)
+            off.attend(l, qs[l], outs[l], l % 2, attn_s)
+
+    def attention():
+        for l in range(L):
+            off.attend(l, qs[l], outs[l], l % 2, attn_s)
+    t_pipe, reps, clk = _timed(torch, pipelined, attn_s)
+    t_g = _timed(torch, gathers, attn_s, min_ms=150.0)[0]
+    t_c = _timed(torch, compute, attn_s, min_ms=150.0)[0]
+    t_attn = _timed(torch, attention, attn_s, min_ms=150.0)[0]
+    off.check()
+    link_bytes = L * off.gather_bytes_per_layer
+    hsrc = torch.empty(off.gather_bytes_per_layer, dtype=torch.uint8).pin_memory()
+    ddst = torch.empty(off.gather_bytes_per_layer, dtype=torch.uint8, device=device)
+    ms_copy = _timed(torch, lambda: ddst.copy_(hsrc, non_blocking=True), attn_s, min_ms=100.0)[0]
+    peak = off.gather_bytes_per_layer / (ms_copy * 1e-3) / 1e9
+    link = link_bytes / (t_g * 1e-3) / 1e9
+    overlap = (t_g + t_c - t_pipe) / min(t_g, t_c)
+    rng = np.random.default_rng(9)
+    ids = np.sort(rng.choice(T, size=off.K, replace=False))
+    t = _wall(lambda: O.offload_gather(k0, ids))
+    del off, hsrc, ddst
+    return {"config": "Qwen-1.5-14B-shaped offload: 40 layers of 40 MHA heads, T = 131072, fp16 K/V in pinned host memory "
+                      f"(2 distinct layers cycled), top-K = {math.floor(RATIO * T)} rows per head gathered into an HBM "
+                      "double buffer; critical keys, 4 sinks and the 128-token window in HBM",
+            "value": link, "unit": "GB/s over the host link (gathers alone)",
+            "overlap": overlap, "overlap_definition": "(t_gather + t_compute - t_pipelined) / min(t_gather, t_compute); "
+                                                      "gather = the host-link gathers alone, compute = selection + "
+                                                      "attention of every layer alone",
+            "ms_step_pipelined": t_pipe, "ms_gather": t_g, "ms_compute": t_c, "ms_attention": t_attn,
+            "bytes_per_step": link_bytes, "calls": reps,
+            "roofline": {"bound": "host link", "achieved": link, "peak": peak, "unit": "GB/s", "frac": link / peak,
+                         "peak_source": "measured pinned->device cudaMemcpyAsync of one layer's gather bytes"},
+            "clocks": clk,
+            "cpu_baseline": {"value": len(ids) * D * 2 / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "one head's K rows, numpy (host to host)"}}
+
+
+def row_block(torch, np, kvq, synth, O, device, stream, hbm, T=131072):
+    """f1 block pruning (64-token blocks) next to the token top-K on one Llama-3.1-8B-shaped
+    sparse layer: selection over the critical-channel scores + exact attention."""
+    Hq, Hkv, ns, w, blk = 32, 8, 4, 128, 64
+    seed = synth.BASE_SEED + 6
+    n_pages = -(-T // 16)
+    alloc = kvq.Allocator(n_pages, seed=13)
+    seqs = kvq.Batch(torch.tensor([alloc.alloc(n_pages)], dtype=torch.int32, device=device),
+                     torch.tensor([T], dtype=torch.int32, device=device), T)
+    cache = kvq.LayerCache(Hq, Hkv, 16, n_pages, 1, t_cap=(T + 7) // 8 * 8, device=device)
+    K, V = synth.kv_rows(T, Hkv, synth.mix(seed, 0), device=device)
+    kvq.kv_quant_pack(cache, seqs, 0, 0, T, K, V)
+    del K, V
+    sh = stream.cuda_stream
+    q = synth.normal((1, Hq, D), synth.mix(seed, 1), device)
+    sc = torch.empty((1, Hq, (T + 7) // 8 * 8), device=device)
+    kvq.kv_critical_score(cache, seqs, q, 8, None, sc)
+    kt, nb = O.ratio_k(T, RATIO), O.block_count(T, RATIO, blk)
+    cap = max(O.topk_count(T, kt, ns, w), ns + w + nb * blk)
+    sel_t = torch.empty((1, Hq, cap), dtype=torch.int32, device=device)
+    sel_b = torch.empty((1, Hq, cap), dtype=torch.int32, device=device)
+    cnt_t = torch.empty((1, Hq), dtype=torch.int32, device=device)
+    cnt_b = torch.empty((1, Hq), dtype=torch.int32, device=device)
+    out = torch.empty((1, Hq, D), device=device)
+    wt = kvq.Workspace(kvq.kv_topk_select_ws())
+    wb = kvq.Workspace(kvq.kv_block_select_ws(seqs, Hq, blk))
+    wa = kvq.Workspace(kvq.kv_sparse_attn_ws(cache, seqs, cap))
+
+    def tok():
+        kvq.kv_topk_select(seqs, Hq, sc, -1, RATIO, ns, w, sel_t, cnt_t, wt, stream=sh)
+        kvq.kv_sparse_attn(cache, seqs, q, sel_t, cnt_t, 0, out, None, wa, stream=sh)
+
+    def blkp():
+        kvq.kv_block_select(seqs, Hq, sc, -1, RATIO, ns, w, blk, sel_b, cnt_b, wb, stream=sh)
+        kvq.kv_sparse_attn(cache, seqs, q, sel_b, cnt_b, 0, out, None, wa, stream=sh)
+    ms_tok = _timed(torch, tok, stream, min_ms=100.0)[0]
+    ms_blk, reps, clk = _timed(torch, blkp, stream, min_ms=150.0)
+    for x in (wt, wb, wa):
+        kvq.kvq_check(x, stream=sh)
+    rows_t, rows_b = int(cnt_t.sum().item()), int(cnt_b.sum().item())
+    by_t, by_b = Hq * T * 4 + rows_t * 2 * D * 2, Hq * T * 4 + rows_b * 2 * D * 2
+    s0 = sc[0, 0, :T].cpu().numpy()
+    del cache
+    t = _wall(lambda: O.block_select(s0, nb, ns, w, blk))
+    gbs = by_b / (ms_blk * 1e-3) / 1e9
+    return {"config": f"32 q / 8 kv heads, T = {T}, ratio {RATIO}: {nb} blocks of {blk} + {ns} sinks + {w} window per "
+                      f"q head (token top-K: {kt}); selection over precomputed critical scores + exact attention",
+            "value": gbs, "unit": "GB/s", "ms_block_path": ms_blk, "ms_token_path": ms_tok,
+            "token_path_GBps": by_t / (ms_tok * 1e-3) / 1e9, "rows_block": rows_b, "rows_token": rows_t,
+            "bytes": by_b, "calls": reps, "roofline": hbm(gbs), "clocks": clk,
+            "cpu_baseline": {"value": t * 1e3 * Hq, "unit": "ms per layer (selection only)", "cores": 1,
+                             "kind": "oracle", "sample": "block selection of one q head, numpy, times 32"}}
+
+
+def row_tiny(torch, np, kvq, synth, O, device, stream):
+    """a4, a5, a6, a8 at the tiny single-layer configuration: 8 q / 2 kv heads, T = 4096
+    (latency-bound: microseconds, no roofline target)."""
+    Hq, Hkv, T, ncrit, kk, ns, w = 8, 2, 4096, 8, 128, 4, 64
+    seed = synth.BASE_SEED
+    alloc = kvq.Allocator(T // 16, seed=13)
+    seqs = kvq.Batch(torch.tensor([alloc.alloc(T // 16)], dtype=torch.int32, device=device),
+                     torch.tensor([T], dtype=torch.int32, device=device), T)
+    cache = kvq.LayerCache(Hq, Hkv, 16, T // 16, 1, t_cap=T, device=device)
+    K, V = synth.kv_rows(T, Hkv, synth.mix(seed, 1), device=device)
+    kvq.kv_quant_pack(cache, seqs, 0, 0, T, K, V)
+    sh = stream.cuda_stream
+    q = synth.queries((1, Hq, D), synth.mix(seed, 2)).to(device)
+    crit = torch.empty((1, Hq, ncrit), dtype=torch.int32, device=device)
+    scores = torch.empty((1, Hq, T), device=device)
+    sel = torch.empty((1, Hq, ns + w + kk), dtype=torch.int32, device=device)
+    cnt = torch.empty((1, Hq), dtype=torch.int32, device=device)
+    out = torch.empty((1, Hq, D), device=device)
+    probs = torch.empty((1, Hq, ns + w + kk), device=device)
+    wt = kvq.Workspace(kvq.kv_topk_select_ws())
+    wa = kvq.Workspace(kvq.kv_sparse_attn_ws(cache, seqs, ns + w + kk))
+    Q = synth.queries((1, Hq, 32, D), synth.mix(seed, 41)).to(device)
+    P = torch.empty((1, Hq), device=device)
+    wd = kvq.Workspace(kvq.kv_dense_pref_score_ws(cache, seqs, 32))
+    calls = {
+        "a4 kv_critical_score": lambda: kvq.kv_critical_score(cache, seqs, q, ncrit, crit, scores, stream=sh),
+        "a5 kv_topk_select": lambda: kvq.kv_topk_select(seqs, Hq, scores, kk, 0.0, ns, w, sel, cnt, wt, stream=sh),
+        "a6 kv_sparse_attn": lambda: kvq.kv_sparse_attn(cache, seqs, q, sel, cnt, 0, out, probs, wa, stream=sh),
+        "a8 kv_dense_pref_score": lambda: kvq.kv_dense_pref_score(cache, seqs, Q, 32, 128, P, wd, stream=sh),
+    }
+    us = {n: 1e3 * _timed(torch, f, stream, min_ms=30.0)[0] for n, f in calls.items()}
+    for x in (wt, wa, wd):
+        kvq.kvq_check(x, stream=sh)
+    Kc, Vc = K.cpu().numpy(), V.cpu().numpy()
+    qn, Qn = q.cpu().numpy()[0], Q.cpu().numpy()[0]
+    am = [O.key_absmax(Kc[:, g]) for g in range(Hkv)]
+    chans = [O.critical_channels(qn[h], am[O.kv_head_of(h, Hq, Hkv)], ncrit) for h in range(Hq)]
+    sc = []
+    cpu = {
+        "a4 kv_critical_score": _wall(lambda: sc.extend(O.critical_scores(qn[h], Kc[:, O.kv_head_of(h, Hq, Hkv)],
+                                                                          chans[h]) for h in range(Hq))),
+        "a5 kv_topk_select": _wall(lambda: [O.topk_select(sc[h], kk, ns, w) for h in range(Hq)]),
+        "a6 kv_sparse_attn": _wall(lambda: [O.sparse_attn(qn[h], Kc[:, O.kv_head_of(h, Hq, Hkv)],
+                                                          Vc[:, O.kv_head_of(h, Hq, Hkv)],
+                                                          O.topk_select(sc[h], kk, ns, w)) for h in range(Hq)]),
+        "a8 kv_dense_pref_score": _wall(lambda: [O.dense_pref_score(Qn[h], Kc[:, O.kv_head_of(h, Hq, Hkv)], 128)
+                                                 for h in range(Hq)]),
+    }
+    return {n: {"config": "8 q / 2 kv heads, T = 4096 (8 critical channels, K = 128 + 4 sinks + 64 window; dense "
+                          "preference over 32 recent queries, top-128)", "value": v, "unit": "us",
+                "roofline": {"bound": "latency", "note": "tiny parity configuration: microseconds, no roofline target"},
+                "cpu_baseline": {"value": cpu[n] * 1e6, "unit": "us", "cores": 1, "kind": "oracle",
+                                 "sample": "the same call on the CPU oracle, numpy"}}
+            for n, v in us.items()}
+
+
+ROWS = [
+    ("a1 kv_quant_pack (40-layer prefill)", row_pack),
+    ("a3 kv_decode_attn_quant (INT4 serving batch)", row_int4),
+    ("a2+a6+a7 H2O decode (append, attention, accumulate / evict / admit)", row_h2o),
+    ("a9 offload gather pipeline", row_offload),
+    ("f1 kv_block_select + kv_sparse_attn (block-sparse layer)", row_block),
+    ("tiny", row_tiny),
+]
+
+
+def run_rows(device, stream, only=None):
+    """Every row in turn (`only`: a list of name prefixes); returns {name: result}."""
     import numpy as np
     import torch
 
     from compressed_kv_cache_quant_gb300 import kvq, synth
-    from compressed_kv_cache_quant_gb300.build import build
     from oracle import kvq_oracle as O
-    build()
-    device = torch.device("cuda", 0)
-    stream = torch.cuda.Stream(device)
-    sh = stream.cuda_stream
-    peak, peak_src = measured_peaks()
-    seed = synth.BASE_SEED
-
-    def hbm(achieved):
-        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": peak_src}
-
-    # a1 kv_quant_pack: one Qwen-1.5-14B-shaped layer, 40 kv heads x 131072 tokens, 1-bit, G 64
-    try:
-        T, H = args.prompt, 40
-        seqs, npg, _ = _paged(torch, kvq, [T], device, 3)
-        cache = kvq.LayerCache(H, H, 1, npg, 1, v_group_dims=64)
-        K, V = synth.kv_rows(T, H, synth.mix(seed + 5, 1), device=device)
-        ms = _ev_ms(torch, lambda: kvq.kv_quant_pack(cache, seqs, 0, 0, T, K, V, stream=sh), stream, 5)
-        nbytes = 2 * T * H * D * 2 + T * H * 48
-        k1, v1 = K[:, 0].cpu().numpy(), V[:, 0].cpu().numpy()
-        del K, V, cache
-        t = _wall(lambda: (O.pack_k(k1, 1), O.pack_v(v1, 1, 64)))
-        cpu_gbs = (T * D * 2 * 2 + T * 48) / t / 1e9
-        _row_line("a1 kv_quant_pack", f"40 kv heads x {T} tokens, 1-bit, K g64 / V G64 (one layer)",
-                  nbytes / (ms * 1e-3) / 1e9, "GB/s", hbm(nbytes / (ms * 1e-3) / 1e9),
-                  {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                   "sample": f"one kv head of the layer ({T} tokens), numpy"}, {"ms": ms, "bytes": nbytes})
-    except Exception as e:  # report and go on with the other rows
-        print(json.dumps({"row": "a1 kv_quant_pack", "error": repr(e)}), flush=True)
-    torch.cuda.empty_cache()
-
-    # a3 kv_decode_attn_quant, INT4 serving batch: 16 sequences, lengths U[4096, 32768], 32 heads MHA,
-    # K 4-bit g64, V 4-bit G 32; one layer
-    try:
-        B, H = 16, 32
-        lens = [int(x) for x in synth.lengths_uniform(B, 4096, 32768, seed + 2)]
-        seqs, npg, _ = _paged(torch, kvq, lens, device, 7)
-        cache = kvq.LayerCache(H, H, 4, npg, B, v_group_dims=32)
-        for b, T in enumerate(lens):
-            K, V = synth.kv_rows(T, H, synth.mix(seed + 2, 10 + b), device=device)
-            kvq.kv_quant_pack(cache, seqs, b, 0, T, K, V)  # same stream as K, V
-            if b == 0:
-                k0, v0 = K[:, 0].cpu().numpy(), V[:, 0].cpu().numpy()
-            del K, V
-        stream.synchronize()
-        q = synth.normal((B, H, D), synth.mix(seed + 2, 99), device)
-        out = torch.empty((B, H, D), device=device)
-        wsq = kvq.Workspace(kvq.kv_decode_attn_quant_ws(cache, seqs))
-        ms = _ev_ms(torch, lambda: kvq.kv_decode_attn_quant(cache, seqs, q, out, wsq, stream=sh), stream, 20)
-        kvq.kvq_check(wsq, stream=sh)
-        nbytes = sum(lens) * H * 152
-        pk, pv = O.pack_k(k0, 4), O.pack_v(v0, 4, 32)
-        q0 = q[0, :1].cpu().numpy()
-        t = _wall(lambda: O.decode_attn_quant(q0, [pk], [pv]))
-        cpu_gbs = lens[0] * 152 / t / 1e9
-        _row_line("a3 kv_decode_attn_quant (INT4 batch)",
-                  f"16 sequences, T ~ U[4096, 32768] (sum {sum(lens)}), 32 heads MHA, K 4-bit g64, V 4-bit G32",
-                  nbytes / (ms * 1e-3) / 1e9, "GB/s", hbm(nbytes / (ms * 1e-3) / 1e9),
-                  {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                   "sample": f"one (sequence, head) of {lens[0]} tokens, numpy fp64"}, {"ms": ms, "bytes": nbytes})
-        del cache
-    except Exception as e:
-        print(json.dumps({"row": "a3 kv_decode_attn_quant (INT4 batch)", "error": repr(e)}), flush=True)
-    torch.cuda.empty_cache()
-
-    # a6 + a7: H2O layer step: attention over the retained set (shared per kv head, probabilities
-    # out), then accumulate and evict; 8 sequences x 8 kv heads, T = 32768, budget 6553
-    try:
-        B, Hq, Hkv, T, budget, ns, w = 8, 32, 8, 32768, 6553, 4, 2048
-        G = Hq // Hkv
-        seqs, npg, _ = _paged(torch, kvq, [T] * B, device, 11)
-        cache = kvq.LayerCache(Hq, Hkv, 16, npg, B, t_cap=T)
-        rng = np.random.default_rng(5)
-        cap = budget + 2
-        ret = np.zeros((B, Hkv, cap), np.int32)
-        for b in range(B):
-            K, V = synth.kv_rows(T, Hkv, synth.mix(seed + 4, b), device=device)
-            kvq.kv_quant_pack(cache, seqs, b, 0, T, K, V)  # same stream as K, V
-            if b == 0:
-                k0, v0 = K[:, 0].cpu().numpy(), V[:, 0].cpu().numpy()
-            del K, V
-            for g in range(Hkv):
-                mid = rng.choice(np.arange(ns, T - w), size=budget - ns - w, replace=False)
-                ret[b, g, :budget] = rng.permutation(np.concatenate([np.arange(ns), mid, np.arange(T - w, T)]))
-        stream.synchronize()
-        retained = torch.from_numpy(ret).to(device)
-        counts = torch.full((B, Hkv), budget, dtype=torch.int32, device=device)
-        cum = torch.from_numpy(rng.random((B, Hkv, cap)).astype(np.float32)).to(device)
-        probs = torch.zeros((B, Hq, cap), device=device)
-        q = synth.normal((B, Hq, D), synth.mix(seed + 4, 99), device)
-        out = torch.empty((B, Hq, D), device=device)
-        wsa = kvq.Workspace(kvq.kv_sparse_attn_ws(cache, seqs, cap))
-        wsh = kvq.Workspace(kvq.kv_h2o_accumulate_ws())
-
-        def h2o_step():
-            kvq.kv_sparse_attn(cache, seqs, q, retained, counts, 1, out, probs, wsa, stream=sh)
-            kvq.kv_h2o_accumulate(cache, seqs, probs, retained, counts, cum, budget, ns, w, None, None, wsh,
-                                  stream=sh)
-        ms = _ev_ms(torch, h2o_step, stream, 20)
-        ms_attn = _ev_ms(torch, lambda: kvq.kv_sparse_attn(cache, seqs, q, retained, counts, 1, out, probs, wsa,
-                                                           stream=sh), stream, 20)
-        kvq.kvq_check(wsa, stream=sh)
-        kvq.kvq_check(wsh, stream=sh)
-        nbytes = B * Hkv * budget * 2 * D * 2 + B * Hkv * cap * 8 + B * Hq * cap * 4
-        r0 = ret[0, 0, :budget].copy()
-        qg = q[0, :G].cpu().numpy()
-        t = _wall(lambda: O.h2o_step(qg, k0, v0, r0, np.zeros(budget), T - 1, budget, ns, w))
-        cpu_ms = t * 1e3 * B * Hkv
-        _row_line("a6+a7 kv_sparse_attn + kv_h2o_accumulate (H2O layer step)",
-                  f"8 sequences x 8 kv heads (GQA 4), T = {T}, budget {budget} = {ns} + {w} + {budget - ns - w}",
-                  nbytes / (ms * 1e-3) / 1e9, "GB/s", hbm(nbytes / (ms * 1e-3) / 1e9),
-                  {"value": cpu_ms, "unit": "ms per layer step", "cores": 1, "kind": "oracle",
-                   "sample": "one (sequence, kv head) of the step, numpy fp64, times 64"},
-                  {"ms": ms, "ms_sparse_attn_only": ms_attn, "bytes": nbytes})
-        del cache
-    except Exception as e:
-        print(json.dumps({"row": "a6+a7 H2O layer step", "error": repr(e)}), flush=True)
-    torch.cuda.empty_cache()
-
-    # f1 block-granular selection (block pruning in 64-token blocks) next to the token top-K on one
-    # Llama-3.1-8B-shaped sparse layer: selection over the critical-channel scores + exact attention
-    try:
-        Hq, Hkv, T, ns, w, blk = 32, 8, args.prompt, 4, 128, 64
-        seqs, npg, _ = _paged(torch, kvq, [T], device, 13)
-        cache = kvq.LayerCache(Hq, Hkv, 16, npg, 1, t_cap=(T + 7) // 8 * 8)
-        K, V = synth.kv_rows(T, Hkv, synth.mix(seed + 6, 0), device=device)
-        kvq.kv_quant_pack(cache, seqs, 0, 0, T, K, V)  # same stream as K, V
-        del K, V
-        q = synth.normal((1, Hq, D), synth.mix(seed + 6, 1), device)
-        sc = torch.empty((1, Hq, (T + 7) // 8 * 8), device=device)
-        crit = torch.empty((1, Hq, 8), dtype=torch.int32, device=device)
-        kvq.kv_critical_score(cache, seqs, q, 8, crit, sc)
-        kt, nb = O.ratio_k(T, RATIO), O.block_count(T, RATIO, blk)
-        cap = max(O.topk_count(T, kt, ns, w), ns + w + nb * blk)
-        sel_t = torch.empty((1, Hq, cap), dtype=torch.int32, device=device)
-        sel_b = torch.empty((1, Hq, cap), dtype=torch.int32, device=device)
-        cnt_t = torch.empty((1, Hq), dtype=torch.int32, device=device)
-        cnt_b = torch.empty((1, Hq), dtype=torch.int32, device=device)
-        out = torch.empty((1, Hq, D), device=device)
-        wt = kvq.Workspace(kvq.kv_topk_select_ws())
-        wb = kvq.Workspace(kvq.kv_block_select_ws(seqs, Hq, blk))
-        wa = kvq.Workspace(kvq.kv_sparse_attn_ws(cache, seqs, cap))
-        sel_tok = lambda: kvq.kv_topk_select(seqs, Hq, sc, -1, RATIO, ns, w, sel_t, cnt_t, wt, stream=sh)
-        sel_blk = lambda: kvq.kv_block_select(seqs, Hq, sc, -1, RATIO, ns, w, blk, sel_b, cnt_b, wb, stream=sh)
-        att_tok = lambda: kvq.kv_sparse_attn(cache, seqs, q, sel_t, cnt_t, 0, out, None, wa, stream=sh)
-        att_blk = lambda: kvq.kv_sparse_attn(cache, seqs, q, sel_b, cnt_b, 0, out, None, wa, stream=sh)
-        ms_tok = _ev_ms(torch, lambda: (sel_tok(), att_tok()), stream, 20)
-        ms_blk = _ev_ms(torch, lambda: (sel_blk(), att_blk()), stream, 20)
-        ms_att_tok = _ev_ms(torch, att_tok, stream, 20)
-        ms_att_blk = _ev_ms(torch, att_blk, stream, 20)
-        for wk in (wt, wb, wa):
-            kvq.kvq_check(wk, stream=sh)
-        rows_t, rows_b = int(cnt_t.sum().item()), int(cnt_b.sum().item())
-        by_t, by_b = Hq * T * 4 + rows_t * 2 * D * 2, Hq * T * 4 + rows_b * 2 * D * 2
-        s0 = sc[0, 0, :T].cpu().numpy()
-        t = _wall(lambda: O.block_select(s0, nb, ns, w, blk))
-        _row_line("f1 kv_block_select + kv_sparse_attn (block-sparse layer)",
-                  f"32 q / 8 kv heads, T = {T}, ratio {RATIO}: {nb} blocks of {blk} + {ns} sinks + {w} window "
-                  f"per q head (token top-K: {kt})",
-                  by_b / (ms_blk * 1e-3) / 1e9, "GB/s", hbm(by_b / (ms_blk * 1e-3) / 1e9),
-                  {"value": t * 1e3 * Hq, "unit": "ms per layer (selection only)", "cores": 1, "kind": "oracle",
-                   "sample": "block selection of one q head, numpy, times 32"},
-                  {"ms_block_path": ms_blk, "ms_token_path": ms_tok, "ms_attn_block_lists": ms_att_blk,
-                   "ms_attn_token_lists": ms_att_tok, "token_path_GBps": by_t / (ms_tok * 1e-3) / 1e9,
-                   "rows_block": rows_b, "rows_token": rows_t, "bytes": by_b})
-        del cache
-    except Exception as e:
-        print(json.dumps({"row": "f1 block-sparse layer", "error": repr(e)}), flush=True)
-    torch.cuda.empty_cache()
-
-    # a9 kv_offload_gather: 40 heads x 3932 selected rows of 131072 from pinned host memory
-    try:
-        T, H, sel_n = args.prompt, 40, math.floor(RATIO * args.prompt)
-        K, V = synth.kv_rows(T, H, synth.mix(seed + 5, 2), n_out=0)
-        src_k = K.permute(1, 0, 2).contiguous().pin_memory()
-        src_v = V.permute(1, 0, 2).contiguous().pin_memory()
-        del K, V
-        rng = np.random.default_rng(9)
-        sel = np.stack([np.sort(rng.choice(T, size=sel_n, replace=False)) for _ in range(H)]).astype(np.int32)
-        sel_t = torch.from_numpy(sel).to(device)
-        cnt = torch.full((H,), sel_n, dtype=torch.int32, device=device)
-        npg = -(-sel_n // 16)
-        dk = torch.empty((npg, H, 16, D), dtype=torch.float16, device=device)
-        dv = torch.empty_like(dk)
-        wg = kvq.Workspace(kvq.kv_offload_gather_ws())
-        ms = _ev_ms(torch, lambda: kvq.kv_offload_gather(src_k.data_ptr(), src_v.data_ptr(), T * D, T, H, sel_t, cnt,
-                                                        dk, dv, wg, stream=sh), stream, 10)
-        kvq.kvq_check(wg, stream=sh)
-        nbytes = H * sel_n * 2 * D * 2
-        # the link's roofline: one contiguous pinned -> device copy of the same size
-        hsrc = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
-        ddst = torch.empty(nbytes, dtype=torch.uint8, device=device)
-        ms_copy = _ev_ms(torch, lambda: ddst.copy_(hsrc, non_blocking=True), stream, 10)
-        link = nbytes / (ms_copy * 1e-3) / 1e9
-        k0 = src_k[0].numpy()
-        t = _wall(lambda: O.offload_gather(k0, sel[0]))
-        cpu_gbs = sel_n * D * 2 / t / 1e9
-        ach = nbytes / (ms * 1e-3) / 1e9
-        _row_line("a9 kv_offload_gather", f"40 heads x {sel_n} of {T} fp16 K and V rows from pinned host memory",
-                  ach, "GB/s", {"bound": "host link", "achieved": ach, "peak": link, "unit": "GB/s",
-                                "frac": ach / link, "peak_source": "measured pinned->device cudaMemcpyAsync, same bytes"},
-                  {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                   "sample": "one head's K rows, numpy fancy indexing (host to host)"}, {"ms": ms, "bytes": nbytes})
-        del src_k, src_v, hsrc, ddst
-    except Exception as e:
-        print(json.dumps({"row": "a9 kv_offload_gather", "error": repr(e)}), flush=True)
-    torch.cuda.empty_cache()
-
-    # a4, a5, a6, a8 at the tiny configuration: 8 q / 2 kv heads, T = 4096 (latency-bound; microseconds)
-    try:
-        Hq, Hkv, T, ncrit, kk, ns, w = 8, 2, 4096, 8, 128, 4, 64
-        seqs, npg, _ = _paged(torch, kvq, [T], device, 13)
-        cache = kvq.LayerCache(Hq, Hkv, 16, npg, 1, t_cap=T)
-        K, V = synth.kv_rows(T, Hkv, synth.mix(seed, 1), device=device)
-        kvq.kv_quant_pack(cache, seqs, 0, 0, T, K, V)
-        q = synth.queries((1, Hq, D), synth.mix(seed, 2)).to(device)
-        crit = torch.empty((1, Hq, ncrit), dtype=torch.int32, device=device)
-        scores = torch.empty((1, Hq, T), device=device)
-        sel = torch.empty((1, Hq, ns + w + kk), dtype=torch.int32, device=device)
-        cnt = torch.empty((1, Hq), dtype=torch.int32, device=device)
-        out = torch.empty((1, Hq, D), device=device)
-        probs = torch.empty((1, Hq, ns + w + kk), device=device)
-        wt = kvq.Workspace(kvq.kv_topk_select_ws())
-        wa = kvq.Workspace(kvq.kv_sparse_attn_ws(cache, seqs, ns + w + kk))
-        Q = synth.queries((1, Hq, 32, D), synth.mix(seed, 41)).to(device)
-        P = torch.empty((1, Hq), device=device)
-        wd = kvq.Workspace(kvq.kv_dense_pref_score_ws(cache, seqs, 32))
-        us = {
-            "a4 kv_critical_score": 1e3 * _ev_ms(torch, lambda: kvq.kv_critical_score(cache, seqs, q, ncrit, crit, scores,
-                                                                                     stream=sh), stream, 50),
-            "a5 kv_topk_select": 1e3 * _ev_ms(torch, lambda: kvq.kv_topk_select(seqs, Hq, scores, kk, 0.0, ns, w, sel,
-                                                                               cnt, wt, stream=sh), stream, 50),
-            "a6 kv_sparse_attn": 1e3 * _ev_ms(torch, lambda: kvq.kv_sparse_attn(cache, seqs, q, sel, cnt, 0, out, probs,
-                                                                               wa, stream=sh), stream, 50),
-            "a8 kv_dense_pref_score": 1e3 * _ev_ms(torch, lambda: kvq.kv_dense_pref_score(cache, seqs, Q, 32, 128, P, wd,
-                                                                                         stream=sh), stream, 20),
-        }
-        for wsx in (wt, wa, wd):
-            kvq.kvq_check(wsx, stream=sh)
-        Kc, Vc = K.cpu().numpy(), V.cpu().numpy()
-        qn, Qn = q.cpu().numpy()[0], Q.cpu().numpy()[0]
-        am = [O.key_absmax(Kc[:, g]) for g in range(Hkv)]
-        chans = [O.critical_channels(qn[h], am[O.kv_head_of(h, Hq, Hkv)], ncrit) for h in range(Hq)]
-        sc = []
-        cpu = {
-            "a4 kv_critical_score": _wall(lambda: sc.extend(O.critical_scores(qn[h], Kc[:, O.kv_head_of(h, Hq, Hkv)],
-                                                                              chans[h]) for h in range(Hq))),
-            "a5 kv_topk_select": _wall(lambda: [O.topk_select(sc[h], kk, ns, w) for h in range(Hq)]),
-            "a6 kv_sparse_attn": _wall(lambda: [O.sparse_attn(qn[h], Kc[:, O.kv_head_of(h, Hq, Hkv)],
-                                                              Vc[:, O.kv_head_of(h, Hq, Hkv)],
-                                                              O.topk_select(sc[h], kk, ns, w)) for h in range(Hq)]),
-            "a8 kv_dense_pref_score": _wall(lambda: [O.dense_pref_score(Qn[h], Kc[:, O.kv_head_of(h, Hq, Hkv)], 128)
-                                                     for h in range(Hq)]),
-        }
-        for name, v in us.items():
-            _row_line(name, "8 q / 2 kv heads, T = 4096 (8 critical channels, K = 128 + 4 sinks + 64 window; "
-                            "dense preference over 32 recent queries, top-128)", v, "us",
-                      {"bound": "latency", "note": "tiny parity configuration: microseconds, no roofline target"},
-                      {"value": cpu[name] * 1e6, "unit": "us", "cores": 1, "kind": "oracle",
-                       "sample": "the same call on the CPU oracle, numpy"})
-    except Exception as e:
-        print(json.dumps({"row": "a4/a5/a6/a8 tiny", "error": repr(e)}), flush=True)
+    peak, src = measured_peaks()
+    out = {}
+    for name, fn in ROWS:
+        if only and not any(name.startswith(o) for o in only):
+            continue
+        t0 = time.perf_counter()
+        try:
+            if fn in (row_offload, row_tiny):
+                r = fn(torch, np, kvq, synth, O, device, stream)
+            else:
+                r = fn(torch, np, kvq, synth, O, device, stream, _hbm(peak, src))
+            if fn is row_tiny:
+                out.update(r)
+            else:
+                r["wall_s"] = time.perf_counter() - t0
+                out[name] = r
+        except Exception as e:  # report the row's failure and go on with the others
+            out[name] = {"error": repr(e)}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 def workload_config(args, world):

@@ -490,7 +490,8 @@ __global__ void __launch_bounds__(128) pack_fp16_kernel(PackArgs a) {
     const int64_t i0 = (int64_t)tile * KG;
     const int n = (int)((a.n_tokens - i0) < KG ? (a.n_tokens - i0) : KG);
     float amax = 0.0f;
-    uint16_t* kT_row = a.pool.kT + (((int64_t)a.seq * a.H + h) * D + c) * a.pool.t_cap;
+    const bool has_kT = a.pool.kT != nullptr;  // a layer that is never scored has no channel-major copy
+    uint16_t* kT_row = has_kT ? a.pool.kT + (((int64_t)a.seq * a.H + h) * D + c) * a.pool.t_cap : nullptr;
     __align__(16) uint16_t buf[8];
     for (int i = 0; i < n; ++i) {
         const int64_t t = a.t_start + i0 + i;
@@ -504,11 +505,12 @@ __global__ void __launch_bounds__(128) pack_fp16_kernel(PackArgs a) {
         }
         amax = fmaxf(amax, fabsf(kvq_h2f(kx)));
         buf[i & 7] = kx;
-        if ((i & 7) == 7) {
+        if ((i & 7) == 7 && has_kT) {
             // t - 7 is a multiple of 8 because t_start and the tile start are multiples of 64
             *reinterpret_cast<uint4*>(kT_row + (t - 7)) = *reinterpret_cast<const uint4*>(buf);
         }
     }
+    if (!has_kT) return;
     const int rem = n & 7;
     for (int r = 0; r < rem; ++r) kT_row[a.t_start + i0 + (n - rem) + r] = buf[r];
     atomicMax(reinterpret_cast<int*>(a.pool.k_absmax + ((int64_t)a.seq * a.H + h) * D + c), __float_as_int(amax));
@@ -606,7 +608,7 @@ __global__ void __launch_bounds__(128) append_fp16_kernel(AppendArgs a) {
     const int T = a.seq_lens[b];
     const int64_t p = (int64_t)T - 1;
     if (p < 0) return;
-    if (T > a.max_len || p >= a.pool.t_cap) {
+    if (T > a.max_len || (a.pool.kT != nullptr && p >= a.pool.t_cap)) {
         if (c == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
         return;
     }
@@ -617,6 +619,7 @@ __global__ void __launch_bounds__(128) append_fp16_kernel(AppendArgs a) {
     const int64_t off = (((int64_t)page * a.H + h) * PG + (p % PG)) * D + c;
     a.pool.k16[off] = kx;
     a.pool.v16[off] = vx;
+    if (a.pool.kT == nullptr) return;  // a layer that is never scored
     a.pool.kT[(((int64_t)b * a.H + h) * D + c) * a.pool.t_cap + p] = kx;
     float* am = a.pool.k_absmax + ((int64_t)b * a.H + h) * D + c;
     *am = fmaxf(*am, fabsf(kvq_h2f(kx)));
@@ -663,9 +666,9 @@ extern "C" int kv_quant_pack(const kvq_layout* L, const kvq_pool* P, const kvq_s
     a.stride_t = stride_t;
     cudaStream_t s = kvq_stream(stream);
     if (L->bits == 16) {
-        KVQ_REQUIRE(P->k16 && P->v16 && P->kT && P->k_absmax, KVQ_ERR_INVALID_ARG,
-                    "kv_quant_pack: fp16 layer needs k16, v16, kT, k_absmax");
-        KVQ_REQUIRE(P->t_cap % 8 == 0 && t_start + n_tokens <= P->t_cap, KVQ_ERR_INVALID_ARG,
+        KVQ_REQUIRE(P->k16 && P->v16 && (P->kT == nullptr) == (P->k_absmax == nullptr), KVQ_ERR_INVALID_ARG,
+                    "kv_quant_pack: fp16 layer needs k16, v16, and kT with k_absmax or neither");
+        KVQ_REQUIRE(P->kT == nullptr || (P->t_cap % 8 == 0 && t_start + n_tokens <= P->t_cap), KVQ_ERR_INVALID_ARG,
                     "kv_quant_pack: t_cap must be a multiple of 8 covering the tokens");
         KVQ_REQUIRE(((uintptr_t)P->kT & 15u) == 0, KVQ_ERR_INVALID_ARG, "kv_quant_pack: kT must be 16-byte aligned");
         const int64_t tiles = (n_tokens + KG - 1) / KG;
@@ -714,8 +717,8 @@ extern "C" int kv_page_append(const kvq_layout* L, const kvq_pool* P, const kvq_
     cudaStream_t s = kvq_stream(stream);
     dim3 grid(a.H, S->batch);
     if (L->bits == 16) {
-        KVQ_REQUIRE(P->k16 && P->v16 && P->kT && P->k_absmax, KVQ_ERR_INVALID_ARG,
-                    "kv_page_append: fp16 layer needs k16, v16, kT, k_absmax");
+        KVQ_REQUIRE(P->k16 && P->v16 && (P->kT == nullptr) == (P->k_absmax == nullptr), KVQ_ERR_INVALID_ARG,
+                    "kv_page_append: fp16 layer needs k16, v16, and kT with k_absmax or neither");
         st = kvq_prepare_kernel((const void*)append_fp16_kernel, 0);
         if (st) return st;
         const cudaError_t e = kvq_launch_pdl(append_fp16_kernel, grid, dim3(128), 0, s, a);

@@ -121,6 +121,7 @@ class OffloadLayers:
         self.ws_sel = [kvq.Workspace(kvq.kv_topk_select_ws(), device) for _ in range(2)]
         self.ws_g = [kvq.Workspace(kvq.kv_offload_gather_ws(), device) for _ in range(2)]
         self.ws_a = kvq.Workspace(kvq.kv_sparse_attn_ws(self.att_view, self.att_seqs[0, 0], self.sel_cap), device)
+        self.ev_selected = [torch.cuda.Event() for _ in range(2)]
         self.ev_gathered = [torch.cuda.Event() for _ in range(2)]
         self.ev_attended = [torch.cuda.Event() for _ in range(2)]
 
@@ -152,24 +153,36 @@ class OffloadLayers:
     # ---- one decode step over all layers
 
     def step(self, qs, outs, copy_stream, attn_stream):
-        """Layers 0 .. L-1 with queries qs[l] into outs[l]: select + gather of layer l on
-        copy_stream into buffer l % 2, attention of layer l on attn_stream once its rows
-        are staged; buffer l % 2 is refilled (layer l + 2) only after that attention.
-        Waits are stream/event ordering only.  Both streams start after the work
-        already queued on attn_stream; attn_stream ends after the last attention."""
+        """Layers 0 .. L-1 with queries qs[l] into outs[l].  The host-link gathers run back to
+        back on copy_stream (layer l into buffer l % 2); the GPU work runs on attn_stream, the
+        selection of layer l + 1 ahead of the attention of layer l, so that neither waits on
+        the other's stream more than the data requires: gather l needs selection l, and
+        buffer l % 2 is refilled (gather l + 2) only after attention l has read it.  Waits
+        are stream/event ordering only.  Both streams start after the work already queued on
+        attn_stream; attn_stream ends after the last attention."""
         start = torch.cuda.Event()
         start.record(attn_stream)
         copy_stream.wait_event(start)
-        for l in range(self.L):
+
+        def select_and_gather(l):
             b = l % 2
+            # sel[b] was last read by gather l - 2, which attention l - 2 (earlier on attn_stream) waited for
+            self.select(l, qs[l], b, attn_stream)
+            self.ev_selected[b].record(attn_stream)
+            copy_stream.wait_event(self.ev_selected[b])
             if l >= 2:
                 copy_stream.wait_event(self.ev_attended[b])
-            self.select(l, qs[l], b, copy_stream)
             self.gather(l, b, copy_stream)
             self.ev_gathered[b].record(copy_stream)
+        select_and_gather(0)
+        for l in range(self.L):
+            b = l % 2
+            if l + 1 < self.L:
+                select_and_gather(l + 1)
             attn_stream.wait_event(self.ev_gathered[b])
             self.attend(l, qs[l], outs[l], b, attn_stream)
             self.ev_attended[b].record(attn_stream)
+        copy_stream.wait_stream(attn_stream)
 
     def check(self):
         for w in self.ws_sel + self.ws_g + [self.ws_a]:

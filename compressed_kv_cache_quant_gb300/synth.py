@@ -91,3 +91,23 @@ def lengths_uniform(B, lo, hi, seed):
     """B sequence lengths drawn uniformly from [lo, hi]."""
     g = generator(mix(seed, 7), "cpu")
     return torch.randint(lo, hi + 1, (B,), generator=g)
+
+
+def h2o_query_bank(K_hot, n_q, seed, n_pick=4, gain=2.0, noise=0.5, zipf=1.2):
+    """The power-law queries of ``h2o_queries`` for many key sets at once.
+
+    K_hot: fp16 [N][n_hot][d] rows of each set's hot positions (any device).
+    Returns fp16 [N][n_q][d] on that device: every query averages n_pick hot rows
+    drawn with Zipf(zipf) weights over the hot ranks, times gain, plus noise *
+    N(0, 1).  Draws come from one generator (seeded by `seed`) on K_hot's device."""
+    N, n_hot, d = K_hot.shape
+    dev = K_hot.device
+    g = generator(mix(seed, 8), dev)
+    w = torch.arange(1, n_hot + 1, dtype=torch.float64, device=dev) ** -zipf
+    cdf = torch.cumsum(w / w.sum(), 0)
+    u = torch.rand((N, n_q * n_pick), generator=g, device=dev, dtype=torch.float64)
+    picks = torch.searchsorted(cdf, u).clamp_(max=n_hot - 1)        # inverse-CDF draws of the hot ranks
+    rows = torch.gather(K_hot.float(), 1, picks[..., None].expand(N, n_q * n_pick, d))
+    q = gain * rows.view(N, n_q, n_pick, d).mean(2)
+    q += noise * torch.randn((N, n_q, d), generator=g, device=dev)
+    return q.to(torch.float16)

@@ -123,6 +123,8 @@ typedef struct kvq_layout {
  *            "critical key" buffer read by kv_critical_score (t_cap % 8 == 0;
  *            kv_sparse_layer_decode also needs t_cap <= 2^24)
  *   k_absmax [max_seqs][H_kv][d]        fp32 running max_t |K[t][c]|
+ *            (kT and k_absmax may both be NULL for a layer that is never
+ *            scored, e.g. an H2O layer; pack and append then skip them)
  */
 typedef struct kvq_pool {
     int64_t   num_blocks;

@@ -190,3 +190,33 @@ def test_int4_serving_batch_stated_shape():
             ref = O.decode_attn_quant(q[b, h:h + 1].numpy(), [pk], [pv])
             e = attn_err(o[b, h], ref[0])
             assert e <= ATTN_TOL, (b, h, T, e)
+
+
+def test_pack_qwen14b_layer_40_heads():
+    """One Qwen-1.5-14B-shaped layer packed to 1 bit in one call: 40 kv heads x
+    131072 tokens, K per channel g64, V per token G64; three heads bit for bit
+    against the oracle (codes, scales, zeros)."""
+    require_gpu()
+    bits, G, H, T = 1, 64, 40, 131072
+    K, V = synth.kv_rows(T, H, synth.mix(synth.BASE_SEED + 5, 302), device="cuda")
+    n_pages = T // 16
+    alloc = kvq.Allocator(n_pages, seed=17)
+    batch, bt = paged_batch([T], alloc)
+    cache = kvq.LayerCache(H, H, bits, n_pages, 1, v_group_dims=G)
+    kvq.kv_quant_pack(cache, batch, 0, 0, T, K, V)
+    torch.cuda.synchronize()
+    heads = (0, 17, 39)
+    Kh, Vh = K[:, heads].cpu().numpy(), V[:, heads].cpu().numpy()
+    del K, V
+    for j, h in enumerate(heads):
+        pk, pv = O.pack_k(Kh[:, j], bits), O.pack_v(Vh[:, j], bits, G)
+        kc = k_row_codes(cache.k_codes[:, h].cpu().numpy()[bt[0]].reshape(T, -1), bits)
+        assert np.array_equal(kc, pk["codes"]), h
+        ksz = cache.k_sz[:, h].cpu().numpy()[bt[0][0::4]]                 # [groups][d][2]
+        assert np.array_equal(ksz[..., 0].view(np.uint16), pk["scale16"].view(np.uint16)), h
+        assert np.array_equal(ksz[..., 1].view(np.uint16), pk["zero16"].view(np.uint16)), h
+        vc = v_page_codes(cache.v_codes[:, h].cpu().numpy()[bt[0]], bits).reshape(T, 128)
+        assert np.array_equal(vc, pv["codes"]), h
+        vsz = cache.v_sz[:, h].cpu().numpy()[bt[0]].reshape(T, -1, 2)
+        assert np.array_equal(vsz[..., 0].view(np.uint16), pv["scale16"].view(np.uint16)), h
+        assert np.array_equal(vsz[..., 1].view(np.uint16), pv["zero16"].view(np.uint16)), h

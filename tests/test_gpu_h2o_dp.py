@@ -79,15 +79,20 @@ def test_h2o_accumulate_bitexact(case):
                 assert r[b, g, :n - 1].tolist() == [t for t in retained[b, g, :n0].tolist() if t in set(kept.tolist())]
 
 
-def test_h2o_pipeline_matches_oracle():
+@pytest.mark.parametrize("T0,steps,budget,ns,w", [
+    (1024, 6, 200, 4, 32),
+    (32768, 16, 6553, 4, 2048),   # the H2O eviction configuration: budget 20% = 4 sinks + 2048 window + 4501
+])
+def test_h2o_pipeline_matches_oracle(T0, steps, budget, ns, w):
     """Init over T0 tokens, then decode steps: attention over the retained set
-    (shared per kv head), accumulate, evict, admit.  Sets are compared until a
-    divergence that fp32-vs-fp64 near-ties explain (then that head stops)."""
+    (shared per kv head), accumulate, evict, admit; queries with a power-law
+    affinity for 64 hot keys.  Sets are compared until a divergence that
+    fp32-vs-fp64 near-ties explain (then that head stops)."""
     require_gpu()
-    Hq, Hkv, T0, steps, budget, ns, w = 8, 2, 1024, 6, 200, 4, 32
+    Hq, Hkv = 8, 2
     G = Hq // Hkv
     T = T0 + steps
-    seed = synth.mix(synth.BASE_SEED + 3, 1)
+    seed = synth.mix(synth.BASE_SEED + 3, 1, T0)
     K, V = synth.kv_rows(T, Hkv, seed)
     n_pages = math.ceil(T / 16) + 2
     alloc = kvq.Allocator(n_pages, seed=4)
