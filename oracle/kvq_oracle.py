@@ -238,6 +238,41 @@ def critical_scores(q16, k16, channels):
 
 
 # ---------------------------------------------------------------------------
+# f1: selection shared by the query heads of one kv head (GQA)
+# [TailorKV §2.3 applied per kv head; meeting article §8.1 item 1]
+# ---------------------------------------------------------------------------
+
+def group_critical_channels(q16_group, absmax16, n_crit):
+    """Critical channels shared by the G query heads ``q16_group`` [G][d] of one
+    kv head.  READING (the pages say only "the query"): a channel's importance
+    for the kv head is the sum over the group's heads of |q_h,c| -- an fp32 sum
+    in ascending head order -- times max_t |K_t,c| (fp32); the n_crit most
+    important channels, ties -> lower channel, in ascending order.  fp32 in a
+    fixed order because it decides an integer (the channel set).  With G = 1
+    this is ``critical_channels``."""
+    q = np.abs(np.asarray(q16_group, dtype=np.float16).astype(np.float32))
+    s = q[0].copy()
+    for h in range(1, q.shape[0]):
+        s = (s + q[h]).astype(np.float32)
+    s = (s * np.asarray(absmax16, dtype=np.float16).astype(np.float32)).astype(np.float32)
+    idx = np.arange(s.shape[0])
+    order = np.lexsort((idx, -s.astype(np.float64)))
+    return np.sort(order[:n_crit])
+
+
+def group_critical_scores(q16_group, k16, channels):
+    """Approximate score of every cached token for the G query heads of one kv
+    head.  READING: each head's approximate score on the shared channels
+    (``critical_scores``: fp32, ascending channel) summed over the heads in
+    ascending order in fp32.  Returns float32 [T]."""
+    q16_group = np.asarray(q16_group, dtype=np.float16)
+    tot = critical_scores(q16_group[0], k16, channels)
+    for h in range(1, q16_group.shape[0]):
+        tot = (tot + critical_scores(q16_group[h], k16, channels)).astype(np.float32)
+    return tot
+
+
+# ---------------------------------------------------------------------------
 # a5: top-K selection with sinks and a recent window
 # [TailorKV §2.3 top-K, §5.1 sparse_ratio; KVSurvey §三.1 sinks + window]
 # ---------------------------------------------------------------------------

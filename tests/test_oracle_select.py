@@ -243,3 +243,68 @@ def test_block_mean_fp32_agrees_with_exact_mean_except_near_ties(case):
         for a in only32:
             for b in only64:
                 assert abs(exact[a] - exact[b]) <= 1e-5 * max(abs(exact[a]), abs(exact[b])), (case, rep, a, b)
+
+
+# ---- f1 selection shared by the query heads of a kv head (GQA)   [TailorKV §2.3 per kv head]
+
+def _golden_group(golden_dir):
+    rows = {}
+    with open(os.path.join(golden_dir, "group_select_small.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = [c.strip() for c in line.split("|")]
+                rows[k] = [float(x) for x in v.split()]
+    return rows
+
+
+def test_golden_group_selection(golden_dir):
+    g = _golden_group(golden_dir)
+    q = np.array([g["q0"], g["q1"]], dtype=np.float16)
+    K = np.array([g["K0"], g["K1"], g["K2"], g["K3"]], dtype=np.float16).T      # [T][d]
+    C = O.group_critical_channels(q, O.key_absmax(K), int(g["n_crit"][0]))
+    assert C.tolist() == [int(x) for x in g["channels"]]
+    s = O.group_critical_scores(q, K, C)
+    assert s.tolist() == g["scores"]
+    ns, w, k = [int(x) for x in g["n_sink window k"]]
+    assert O.topk_select(s, k, ns, w).tolist() == [int(x) for x in g["selected"]]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_group_of_one_is_the_per_head_definition(seed):
+    """A group of one query head reduces to the per-head channels and scores, bit for bit."""
+    rng = np.random.default_rng(30 + seed)
+    K = (rng.standard_normal((500, 128)) * np.where(rng.random(128) < 0.05, 10, 1)).astype(np.float16)
+    q = rng.standard_normal(128).astype(np.float16)
+    am = O.key_absmax(K)
+    C = O.critical_channels(q, am, 8)
+    assert O.group_critical_channels(q[None], am, 8).tolist() == C.tolist()
+    assert np.array_equal(O.group_critical_scores(q[None], K, C).view(np.uint32),
+                          O.critical_scores(q, K, C).view(np.uint32))
+
+
+def test_group_scores_on_all_channels_are_the_summed_dot_products():
+    """With every channel critical, the group score is sum_h q_h . K_t, up to fp32 rounding."""
+    rng = np.random.default_rng(41)
+    K = rng.standard_normal((300, 128)).astype(np.float16)
+    q = rng.standard_normal((4, 128)).astype(np.float16)
+    C = O.group_critical_channels(q, O.key_absmax(K), 128)
+    assert C.tolist() == list(range(128))
+    s = O.group_critical_scores(q, K, C).astype(np.float64)
+    exact = (K.astype(np.float64) @ q.astype(np.float64).T).sum(axis=1)
+    bound = (np.abs(K.astype(np.float64)) @ np.abs(q.astype(np.float64)).T).sum(axis=1) * 128 * 2.0 ** -24
+    assert np.all(np.abs(s - exact) <= bound)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_group_channels_brute_force(seed):
+    """Small integer queries (exact sums): the chosen channels are the n_crit best by
+    (sum_h |q_h,c| * max|K_c| desc, channel asc), computed with Python integers."""
+    rng = np.random.default_rng(50 + seed)
+    G, d, n = int(rng.integers(1, 5)), 16, int(rng.integers(1, 9))
+    q = rng.integers(-3, 4, size=(G, d)).astype(np.float16)
+    am = rng.integers(0, 5, size=d).astype(np.float16)
+    got = O.group_critical_channels(q, am, n).tolist()
+    imp = [(sum(abs(int(q[h, c])) for h in range(G)) * int(am[c]), c) for c in range(d)]
+    want = sorted(c for _, c in sorted(imp, key=lambda ic: (-ic[0], ic[1]))[:n])
+    assert got == want
