@@ -882,6 +882,71 @@ def row_block(torch, np, kvq, synth, O, device, stream, hbm, T=131072):
                              "kind": "oracle", "sample": "block selection of one q head, numpy, times 32"}}
 
 
+def row_group(torch, np, kvq, synth, O, device, stream, hbm, T=131072):
+    """f1 selection shared by the q heads of a kv head (GQA) on one Llama-3.1-8B-shaped sparse
+    layer: critical scores per kv head (the group's |q| summed), top-K per kv head, exact
+    attention of the 4 q heads over their kv head's list -- three launches -- next to the
+    per-q-head layer kernel of the decode step on the same cache."""
+    Hq, Hkv, ns, w = 32, 8, 4, 128
+    seed = synth.BASE_SEED + 7
+    n_pages = -(-(T + 64) // 16)
+    alloc = kvq.Allocator(n_pages, seed=19)
+    seqs = kvq.Batch(torch.tensor([alloc.alloc(n_pages)], dtype=torch.int32, device=device),
+                     torch.tensor([T], dtype=torch.int32, device=device), 16 * n_pages)
+    t_cap = 16 * n_pages
+    cache = kvq.LayerCache(Hq, Hkv, 16, n_pages, 1, t_cap=t_cap, device=device)
+    K, V = synth.kv_rows(T, Hkv, synth.mix(seed, 0), device=device)
+    kvq.kv_quant_pack(cache, seqs, 0, 0, T, K, V)
+    k_new, v_new = K[-1:].clone(), V[-1:].clone()
+    K0, V0 = K[:, 0].cpu().numpy(), V[:, 0].cpu().numpy()
+    del K, V
+    sh = stream.cuda_stream
+    q = synth.normal((1, Hq, D), synth.mix(seed, 1), device)
+    sc = torch.empty((1, Hkv, t_cap), device=device)
+    kt = O.ratio_k(T, RATIO)
+    cap = O.topk_count(T, kt, ns, w)
+    sel = torch.empty((1, Hkv, cap), dtype=torch.int32, device=device)
+    cnt = torch.empty((1, Hkv), dtype=torch.int32, device=device)
+    out = torch.empty((1, Hq, D), device=device)
+    wt = kvq.Workspace(kvq.kv_topk_select_ws())
+    wa = kvq.Workspace(kvq.kv_sparse_attn_ws(cache, seqs, cap))
+    wl = kvq.Workspace(kvq.kv_sparse_layer_decode_ws())
+
+    def grouped():
+        kvq.kv_group_critical_score(cache, seqs, q, N_CRIT, None, sc, stream=sh)
+        kvq.kv_topk_select(seqs, Hkv, sc, -1, RATIO, ns, w, sel, cnt, wt, stream=sh)
+        kvq.kv_sparse_attn(cache, seqs, q, sel, cnt, 1, out, None, wa, stream=sh)
+    g = _capture(torch, grouped, stream)
+    ms, reps, clk = _timed(torch, g.replay, stream, min_ms=150.0)
+    # the per-q-head layer kernel on the same cache (it also appends the newest token, rewriting
+    # the same position each call: the sequence length does not change)
+    g1 = _capture(torch, lambda: kvq.kv_sparse_layer_decode(cache, seqs, k_new, v_new, q, N_CRIT, -1, RATIO, ns, w,
+                                                            out, wl, stream=sh), stream)
+    ms_head = _timed(torch, g1.replay, stream, min_ms=100.0)[0]
+    for x in (wt, wa, wl):
+        kvq.kvq_check(x, stream=sh)
+    nbytes = Hkv * N_CRIT * T * 2 + 2 * Hkv * T * 4 + Hkv * cap * 2 * D * 2
+    head_bytes = Hq * N_CRIT * T * 2 + Hq * cap * 2 * D * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del cache, g, g1
+    qg = q[0, :Hq // Hkv].cpu().numpy()
+
+    def oracle_kv_head():
+        C = O.group_critical_channels(qg, O.key_absmax(K0), N_CRIT)
+        ids = O.topk_select(O.group_critical_scores(qg, K0, C), kt, ns, w)
+        for j in range(Hq // Hkv):
+            O.sparse_attn(qg[j], K0, V0, ids)
+    t = _wall(oracle_kv_head)
+    return {"config": f"32 q / 8 kv heads, T = {T}: per kv head 8 critical channels (|q| summed over its 4 q heads), "
+                      f"top-K = {kt} + 4 sinks + 128 window, the 4 q heads attend the shared list (3 launches); "
+                      "per-q-head layer kernel on the same cache for comparison",
+            "value": 1e3 / ms, "unit": "layers/s", "ms_per_layer": ms, "ms_per_layer_per_q_head_selection": ms_head,
+            "bytes_per_layer": nbytes, "bytes_per_layer_per_q_head_selection": head_bytes, "GBps": gbs,
+            "calls": reps, "roofline": hbm(gbs), "clocks": clk,
+            "cpu_baseline": {"value": 1.0 / (t * Hkv), "unit": "layers/s", "cores": 1, "kind": "oracle",
+                             "sample": "one kv head's selection and its 4 heads' attention, numpy, times 8"}}
+
+
 def row_tiny(torch, np, kvq, synth, O, device, stream):
     """a4, a5, a6, a8 at the tiny single-layer configuration: 8 q / 2 kv heads, T = 4096
     (latency-bound: microseconds, no roofline target)."""
@@ -944,6 +1009,7 @@ ROWS = [
     ("a2+a6+a7 H2O decode (append, attention, accumulate / evict / admit)", row_h2o),
     ("a9 offload gather pipeline", row_offload),
     ("f1 kv_block_select + kv_sparse_attn (block-sparse layer)", row_block),
+    ("f1 kv_group_critical_score + shared top-K + shared-list attention (GQA-shared selection)", row_group),
     ("tiny", row_tiny),
 ]
 

@@ -71,6 +71,7 @@ PROTOTYPES = {
     "kv_decode_attn_quant_noalloc_max_scratch": (c_size_t, []),
     "kv_decode_attn_quant_plan": (c_int, [PL, PS, c_int32, POINTER(c_int32), POINTER(c_int32)]),
     "kv_critical_score": (c_int, [PL, PP, PS, VP, c_int32, VP, VP, c_int64, VP]),
+    "kv_group_critical_score": (c_int, [PL, PP, PS, VP, c_int32, VP, VP, c_int64, VP]),
     "kv_topk_select": (c_int, [PS, c_int32, VP, c_int64, c_int32, c_double, c_int32, c_int32, VP, c_int32, VP,
                                VP, c_size_t, VP]),
     "kv_topk_select_ws": (c_size_t, []),

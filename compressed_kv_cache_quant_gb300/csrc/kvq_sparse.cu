@@ -93,23 +93,29 @@ __device__ __forceinline__ void unpack8h(const uint4& r, float* f) {
     }
 }
 
-__global__ void __launch_bounds__(CS_NT, CS_MINB) crit_score_kernel(CritArgs a) {
+// NHS query heads per score row: 1 = one row per q head (a4); NHS = GQ = one row per kv head,
+// its group's per-head scores summed (f1, the selection shared by a GQA group).
+template <int NHS>
+__global__ void __launch_bounds__(CS_NT, NHS <= 2 ? CS_MINB : 2) crit_score_kernel(CritArgs a) {
     __shared__ float sc[D];
-    __shared__ float qs[D];
+    __shared__ float qs[NHS][D];
     __shared__ uint16_t knew[D];
     __shared__ int32_t clist[D];
     __shared__ uint32_t lhist[CS_H1];
     const int tid = threadIdx.x;
     const int Hq = a.H * a.GQ;
+    const int R = NHS == 1 ? Hq : a.H;  // score rows per sequence
     const int i_begin = (int)(((int64_t)a.n_items * blockIdx.x) / gridDim.x);
     const int i_end = (int)(((int64_t)a.n_items * (blockIdx.x + 1)) / gridDim.x);
-    int cur = -1;  // (sequence, q head) row whose channels and histogram are held
+    int cur = -1;  // (sequence, row) whose channels and histogram are held
     int T = 0, p_new = -1, cand_lo = 0, cand_hi = 0;
     if (a.hist != nullptr)
         for (int i = tid; i < CS_H1; i += CS_NT) lhist[i] = 0u;
     for (int item = i_begin; item < i_end; ++item) {
         const int rowi = item / a.tiles, tile = item % a.tiles;
-        const int b = rowi / Hq, h = rowi % Hq, g = h / a.GQ;
+        const int b = rowi / R, r = rowi % R;
+        const int g = NHS == 1 ? r / a.GQ : r;
+        const int h = NHS == 1 ? r : g * a.GQ;  // the row's first q head
         const int64_t kvrow = (int64_t)b * a.H + g;
         if (rowi != cur) {
             __syncthreads();  // the previous row's channels and histogram are no longer read
@@ -133,16 +139,22 @@ __global__ void __launch_bounds__(CS_NT, CS_MINB) crit_score_kernel(CritArgs a) 
             cand_lo = a.n_sink;
             cand_hi = T - a.window;
             if (tid < D) {
-                const float qv = kvq_h2f(a.q[(int64_t)rowi * D + tid]);
                 float am = a.absmax[kvrow * D + tid];
                 if (p_new >= 0) {
                     const uint16_t kn = a.k_new[kvrow * D + tid];
                     knew[tid] = kn;
                     am = fmaxf(am, fabsf(kvq_h2f(kn)));
                 }
-                qs[tid] = qv;
-                // |q_c| * max|K_c|: both fp16 values, so the fp32 product is exact
-                sc[tid] = fabsf(qv) * am;
+                // sum over the row's heads of |q_c| (fp32, ascending head), times max|K_c|; for one
+                // head both factors are fp16 values, so the fp32 product is exact
+                float qa = 0.0f;
+#pragma unroll
+                for (int j = 0; j < NHS; ++j) {
+                    const float qv = kvq_h2f(a.q[((int64_t)b * Hq + h + j) * D + tid]);
+                    qs[j][tid] = qv;
+                    qa = j == 0 ? fabsf(qv) : __fadd_rn(qa, fabsf(qv));
+                }
+                sc[tid] = __fmul_rn(qa, am);
             }
             __syncthreads();
             if (tid < 32) {
@@ -195,9 +207,11 @@ __global__ void __launch_bounds__(CS_NT, CS_MINB) crit_score_kernel(CritArgs a) 
         const int t0 = tile * CS_TILE + tid * CS_TOK;
         if (t0 >= T) continue;
         const uint16_t* base = a.kT + kvrow * D * a.t_cap + t0;
-        float acc[CS_TOK];
+        float accs[NHS][CS_TOK];
 #pragma unroll
-        for (int i = 0; i < CS_TOK; ++i) acc[i] = 0.0f;
+        for (int j = 0; j < NHS; ++j)
+#pragma unroll
+            for (int i = 0; i < CS_TOK; ++i) accs[j][i] = 0.0f;
         for (int j0 = 0; j0 < a.n_crit; j0 += CS_BATCH) {
             // all loads of the batch in flight before the arithmetic
             uint4 raw[CS_BATCH];
@@ -210,7 +224,6 @@ __global__ void __launch_bounds__(CS_NT, CS_MINB) crit_score_kernel(CritArgs a) 
             for (int j = 0; j < CS_BATCH; ++j) {
                 if (j0 + j >= a.n_crit) break;
                 const int c = clist[j0 + j];  // ascending channel order
-                const float qc = qs[c];
                 float k[8];
                 unpack8h(raw[j], k);
                 if (has_new) {
@@ -221,8 +234,20 @@ __global__ void __launch_bounds__(CS_NT, CS_MINB) crit_score_kernel(CritArgs a) 
                 }
                 // fma == add of the exact fp16*fp16 product: the same fp32 result as (q*k) + acc
 #pragma unroll
-                for (int i = 0; i < CS_TOK; ++i) acc[i] = fmaf(qc, k[i], acc[i]);
+                for (int hh = 0; hh < NHS; ++hh) {
+                    const float qc = qs[hh][c];
+#pragma unroll
+                    for (int i = 0; i < CS_TOK; ++i) accs[hh][i] = fmaf(qc, k[i], accs[hh][i]);
+                }
             }
+        }
+        // the row's score: its heads' scores summed in ascending head order (fp32)
+        float acc[CS_TOK];
+#pragma unroll
+        for (int i = 0; i < CS_TOK; ++i) {
+            acc[i] = accs[0][i];
+#pragma unroll
+            for (int hh = 1; hh < NHS; ++hh) acc[i] = __fadd_rn(acc[i], accs[hh][i]);
         }
         float* out = a.scores + (int64_t)rowi * a.score_stride + t0;
         if (t0 + CS_TOK <= T) {
@@ -649,14 +674,25 @@ CritArgs crit_args(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, co
     return a;
 }
 
-int launch_crit(CritArgs& a, const kvq_layout* L, const kvq_seqs* S, cudaStream_t s) {
-    const int st = kvq_prepare_kernel((const void*)crit_score_kernel, 0);
+template <int NHS>
+int launch_crit_nhs(CritArgs& a, const kvq_layout* L, const kvq_seqs* S, cudaStream_t s) {
+    const int st = kvq_prepare_kernel((const void*)crit_score_kernel<NHS>, 0);
     if (st) return st;
     a.tiles = std::max(1, (S->max_len + CS_TILE - 1) / CS_TILE);
-    a.n_items = S->batch * L->n_q_heads * a.tiles;
-    const int grid = std::min(a.n_items, kvq_num_sms() * CS_MINB);
-    crit_score_kernel<<<grid, CS_NT, 0, s>>>(a);
+    a.n_items = S->batch * (NHS == 1 ? L->n_q_heads : L->n_kv_heads) * a.tiles;
+    const int grid = std::min(a.n_items, kvq_num_sms() * (NHS <= 2 ? CS_MINB : 2));
+    crit_score_kernel<NHS><<<grid, CS_NT, 0, s>>>(a);
     return KVQ_OK;
+}
+
+// group == false: one score row per q head; true: one row per kv head, its q heads summed.
+int launch_crit(CritArgs& a, const kvq_layout* L, const kvq_seqs* S, cudaStream_t s, bool group = false) {
+    switch (group ? a.GQ : 1) {
+        case 2: return launch_crit_nhs<2>(a, L, S, s);
+        case 4: return launch_crit_nhs<4>(a, L, S, s);
+        case 8: return launch_crit_nhs<8>(a, L, S, s);
+        default: return launch_crit_nhs<1>(a, L, S, s);
+    }
 }
 
 }  // namespace
@@ -672,6 +708,19 @@ extern "C" int kv_critical_score(const kvq_layout* L, const kvq_pool* P, const k
     st = launch_crit(a, L, S, kvq_stream(stream));
     if (st) return st;
     return kvq_launch_status("kv_critical_score");
+}
+
+extern "C" int kv_group_critical_score(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
+                                       int32_t n_crit, int32_t* crit, float* scores, int64_t score_stride,
+                                       void* stream) {
+    kvq_clear_error();
+    int st = crit_common(L, P, S, q, n_crit, scores, score_stride, "kv_group_critical_score");
+    if (st) return st;
+    if (S->batch == 0) return KVQ_OK;
+    CritArgs a = crit_args(L, P, S, q, n_crit, crit, scores, score_stride);
+    st = launch_crit(a, L, S, kvq_stream(stream), true);
+    if (st) return st;
+    return kvq_launch_status("kv_group_critical_score");
 }
 
 extern "C" size_t kv_append_critical_score_ws(void) { return sizeof(KvqWsHeader); }

@@ -192,6 +192,14 @@ def kv_critical_score(cache, seqs, q, n_crit, crit, scores, score_stride=None, s
                                          _p(scores), int(score_stride), _s(stream)), "kv_critical_score")
 
 
+def kv_group_critical_score(cache, seqs, q, n_crit, crit, scores, score_stride=None, stream=None):
+    if score_stride is None:
+        score_stride = scores.shape[-1]
+    return check(lib().kv_group_critical_score(_ref(cache.layout), _ref(cache), _ref(seqs), _p(q), int(n_crit),
+                                               _p(crit), _p(scores), int(score_stride), _s(stream)),
+                 "kv_group_critical_score")
+
+
 def kv_append_critical_score_ws():
     return lib().kv_append_critical_score_ws()
 

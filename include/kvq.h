@@ -272,6 +272,27 @@ int kv_critical_score(const kvq_layout* layout, const kvq_pool* pool, const kvq_
                       float* scores, int64_t score_stride, void* stream);
 
 /* ------------------------------------------------------------------------
+ * f1: kv_group_critical_score -- kv_critical_score shared by the query heads
+ * of one kv head (GQA) [TailorKV §2.3 applied per kv head; Meeting §8.1 item 1].
+ * Reading (the pages say only "the query"): a channel's importance for kv head
+ * g is (sum over g's q heads, ascending, of |q_h,c|, fp32) * max_t |K[t][c]|
+ * (fp32); the n_crit largest (ties -> lower channel) are the group's channels;
+ * a token's score is the fp32 sum, in ascending head order, of each head's
+ * approximate score on those channels (as kv_critical_score computes it).
+ * One selection per kv head then serves all its q heads: kv_topk_select with
+ * n_heads = H_kv, kv_sparse_attn with sel_per_kv_head = 1 -- the channel rows,
+ * the selection and the selected rows are read once per kv head instead of
+ * once per q head.
+ *
+ * q: device fp16 [batch][H_q][d]; crit (optional): device int32
+ * [batch][H_kv][n_crit], ascending; scores: device fp32
+ * [batch][H_kv][score_stride].  Otherwise as kv_critical_score.
+ * ---------------------------------------------------------------------- */
+int kv_group_critical_score(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                            const uint16_t* q, int32_t n_crit, int32_t* crit,
+                            float* scores, int64_t score_stride, void* stream);
+
+/* ------------------------------------------------------------------------
  * a5: kv_topk_select -- token selection per query head [TailorKV §2.3, §5.1;
  * KVSurvey §三.1]: tokens [0, n_sink) and [T-window, T) are always kept;
  * among the others the k highest scores (ties -> lower position) are added;
