@@ -157,6 +157,66 @@ def dequant_v(pv):
 
 
 # ---------------------------------------------------------------------------
+# f4: FP8 E4M3 KV cache   [meeting article §6 item 2: FP8 E4M3 preferred over INT4
+# where the hardware has it -- no dequantization arithmetic]
+# ---------------------------------------------------------------------------
+
+def fp8_e4m3_decode(codes):
+    """Values of E4M3 bytes: sign bit, 4 exponent bits (bias 7), 3 mantissa bits;
+    exponent 0 holds the subnormals m * 2^-9; S.1111.111 is NaN; no infinities.
+    Returns float64 (exact)."""
+    c = np.asarray(codes, dtype=np.int64) & 0xFF
+    sgn = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return sgn * val
+
+
+def fp8_e4m3_encode(x16):
+    """fp16 -> E4M3 byte, round to nearest with ties to even mantissa, finite
+    values beyond the largest (448) saturate to +-448.  READING: the pages name
+    the format (E4M3) but no scale; K and V are cast directly, one byte per value
+    (fp16 inputs here stay within the range).  Integer arithmetic on the fp16
+    value: for |x| in the normal range of E4M3 the significand keeps 3 fraction
+    bits, below 2^-6 the grid is 2^-9.  Returns uint8 codes."""
+    x = np.asarray(x16, dtype=np.float16).astype(np.float64)
+    sign = (np.signbit(x)).astype(np.int64) << 7
+    nan = np.isnan(x)
+    a = np.where(nan, 0.0, np.minimum(np.abs(x), 512.0))   # inf saturates like any |x| > 448
+    with np.errstate(divide="ignore", invalid="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0))).astype(np.int64)
+    e = np.clip(e, -6, 8)                      # the binade's exponent; below 2^-6 the subnormal grid 2^-9
+    ulp = np.exp2((e - 3).astype(np.float64))  # 3 fraction bits
+    q = a / ulp                                # exact: a is fp16, ulp a power of two
+    lo = np.floor(q)
+    frac = q - lo
+    up = (frac > 0.5) | ((frac == 0.5) & (lo.astype(np.int64) % 2 == 1))
+    n = (lo + up).astype(np.int64)             # multiple of ulp after rounding
+    mag = n * ulp                              # the rounded magnitude
+    # re-encode the magnitude (a carry may have moved it to the next binade)
+    sub = mag < 2.0 ** -6
+    code_sub = np.round(mag / 2.0 ** -9).astype(np.int64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        e2 = np.floor(np.log2(np.where(mag > 0, mag, 1.0))).astype(np.int64)
+    m2 = np.round((mag / np.exp2(e2.astype(np.float64)) - 1.0) * 8).astype(np.int64)
+    code_norm = ((e2 + 7) << 3) | m2
+    out = np.where(sub, code_sub, code_norm)
+    out = np.where(mag > 448.0, 0x7E, out)     # saturate (finite)
+    out = np.where(nan, 0x7F, out)
+    return (out | sign).astype(np.uint8)
+
+
+def fp8_attention(q16, k16, v16):
+    """Exact softmax attention (fp64) of one query over a cache stored as E4M3:
+    keys and values are the decoded E4M3 values of the fp16 rows."""
+    K = fp8_e4m3_decode(fp8_e4m3_encode(k16))
+    V = fp8_e4m3_decode(fp8_e4m3_encode(v16))
+    return softmax_attention(np.asarray(q16, dtype=np.float16), K, V)
+
+
+# ---------------------------------------------------------------------------
 # exact softmax attention (shared definition used by a3, a6, a7, a8)
 # [Meeting §3.2: Softmax(Q K_ret^T / sqrt(d)) V_ret; OnDevice §3.2]
 # ---------------------------------------------------------------------------
