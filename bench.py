@@ -947,6 +947,42 @@ def row_group(torch, np, kvq, synth, O, device, stream, hbm, T=131072):
                              "sample": "one kv head's selection and its 4 heads' attention, numpy, times 8"}}
 
 
+def row_fp8(torch, np, kvq, synth, O, device, stream, hbm, T=131072):
+    """f4 an FP8 E4M3 layer of the Llama-3.1-8B shape (32 q / 8 kv heads, 131072 tokens): decode
+    attention over the E4M3 cache (pages staged by bulk asynchronous copies, tensor cores)."""
+    Hq, Hkv = 32, 8
+    seed = synth.BASE_SEED + 8
+    n_pages = T // 16
+    alloc = kvq.Allocator(n_pages, seed=23)
+    seqs = kvq.Batch(torch.tensor([alloc.alloc(n_pages)], dtype=torch.int32, device=device),
+                     torch.tensor([T], dtype=torch.int32, device=device), T)
+    cache = kvq.LayerCache(Hq, Hkv, kvq.BITS_E4M3, n_pages, 1, device=device)
+    K, V = synth.kv_rows(T, Hkv, synth.mix(seed, 0), device=device)
+    kvq.kv_quant_pack(cache, seqs, 0, 0, T, K, V)
+    K0, V0 = K[:, 0].cpu().numpy(), V[:, 0].cpu().numpy()
+    del K, V
+    q = synth.normal((1, Hq, D), synth.mix(seed, 1), device)
+    out = torch.empty((1, Hq, D), device=device)
+    ws = kvq.Workspace(kvq.kv_decode_attn_quant_ws(cache, seqs))
+    sh = stream.cuda_stream
+    g = _capture(torch, lambda: kvq.kv_decode_attn_quant(cache, seqs, q, out, ws, stream=sh), stream)
+    ms, reps, clk = _timed(torch, g.replay, stream, min_ms=150.0)
+    kvq.kvq_check(ws, stream=sh)
+    plan = kvq.kv_decode_attn_quant_plan(cache, seqs)
+    nbytes = Hkv * T * 2 * D
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    q0 = q[0, 0].cpu().numpy()
+    del cache, g
+    t = _wall(lambda: O.fp8_attention(q0, K0, V0))
+    return {"config": f"FP8 E4M3 layer, 32 q / 8 kv heads (GQA 4), T = {T}: K and V rows as E4M3 bytes (256 B per token "
+                      "and kv head), decode attention of all 32 heads",
+            "value": gbs, "unit": "GB/s", "us_per_launch": ms * 1e3, "bytes_per_launch": nbytes,
+            "split_plan": {"n_splits": plan[0], "groups_per_split": plan[1]}, "calls": reps,
+            "roofline": hbm(gbs), "clocks": clk,
+            "cpu_baseline": {"value": T * 2 * D / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "one q head over one kv head's E4M3 cache, numpy fp64"}}
+
+
 def row_tiny(torch, np, kvq, synth, O, device, stream):
     """a4, a5, a6, a8 at the tiny single-layer configuration: 8 q / 2 kv heads, T = 4096
     (latency-bound: microseconds, no roofline target)."""
@@ -1010,6 +1046,7 @@ ROWS = [
     ("a9 offload gather pipeline", row_offload),
     ("f1 kv_block_select + kv_sparse_attn (block-sparse layer)", row_block),
     ("f1 kv_group_critical_score + shared top-K + shared-list attention (GQA-shared selection)", row_group),
+    ("f4 kv_decode_attn_quant on an FP8 E4M3 layer", row_fp8),
     ("tiny", row_tiny),
 ]
 

@@ -519,6 +519,326 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
     if (tid == 0) a.counters[b * Hv + gv] = 0;
 }
 
+// ---------------------------------------------------------------- FP8 E4M3 layer
+//
+// K and V rows are E4M3 bytes (128 per token and kv head).  A warp takes 32 tokens (two pages) at
+// a time; lane 0 stages the two pages of K and of V (four 2 KB blocks, contiguous per page and
+// kv head) into the warp's shared-memory stage with bulk asynchronous copies that complete on the
+// stage's mbarrier, one step ahead (two stages per warp).  E4M3 widens to fp16 exactly, so the
+// scores are m16n8k16 products of exact fp16 keys with the fp16 query (exact products, fp32
+// sums) and the values products of exact fp16 values with fp16 weights.  Channels are permuted
+// inside each product (a dot product does not depend on the order), so that every lane reads
+// whole 16-byte runs: in the score product lane q4 takes channels 32 q4 .. 32 q4 + 31 of a key
+// row (k-step s: channels 32 q4 + 4 s + 0..3), in the value product output row (m-tile mt, g8)
+// is channel 16 g8 + 2 mt and (mt, g8 + 8) channel 16 g8 + 2 mt + 1.  Head h of the kv group is
+// column 2h of both products (odd columns zero), as in the code kernel above.
+
+constexpr int F8_NW = 12;                 // warps per CTA (one CTA per SM)
+constexpr int F8_PAGE = PG * D;           // bytes of one page of one kv head (2 KB)
+constexpr int F8_STAGE = 4 * F8_PAGE;     // K page 0, K page 1, V page 0, V page 1
+constexpr uint32_t F8_SPIN = 1u << 16;    // bound on the polls of one mbarrier wait
+
+template <int GQ>
+struct F8Smem {
+    union alignas(16) {
+        uint8_t st[F8_NW][2][F8_STAGE];   // per warp: two stages
+        float ro[F8_NW][GQ][D];           // per warp: unnormalised outputs, after the last step
+    } u;
+    unsigned long long bar[F8_NW][2];     // one mbarrier per stage (one arrival + the copied bytes)
+    float m[F8_NW][GQ], l[F8_NW][GQ];
+};
+
+__device__ __forceinline__ uint32_t f8_saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void f8_expect(unsigned long long* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(f8_saddr(bar)), "r"(bytes)
+                 : "memory");
+}
+// global -> shared bulk copy (16-byte aligned, a multiple of 16 bytes), completing on bar
+__device__ __forceinline__ void f8_bulk(void* dst, const void* src, uint32_t bytes, unsigned long long* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     f8_saddr(dst)),
+                 "l"(src), "r"(bytes), "r"(f8_saddr(bar))
+                 : "memory");
+}
+// waits for the phase of bar with the given parity; false after F8_SPIN polls
+__device__ __forceinline__ bool f8_wait(unsigned long long* bar, uint32_t parity) {
+    for (uint32_t it = 0; it < F8_SPIN; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(f8_saddr(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+// E4M3 x2 (low / high 16 bits of w) -> f16x2, exact
+__device__ __forceinline__ uint32_t f8_lo(uint32_t w) {
+    uint32_t r;
+    asm("{\n.reg .b16 a, b;\nmov.b32 {a, b}, %1;\ncvt.rn.f16x2.e4m3x2 %0, a;\n}" : "=r"(r) : "r"(w));
+    return r;
+}
+__device__ __forceinline__ uint32_t f8_hi(uint32_t w) {
+    uint32_t r;
+    asm("{\n.reg .b16 a, b;\nmov.b32 {a, b}, %1;\ncvt.rn.f16x2.e4m3x2 %0, b;\n}" : "=r"(r) : "r"(w));
+    return r;
+}
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+
+template <int GQ>
+__global__ void __launch_bounds__(32 * F8_NW, 1) f8_attn_kernel(QAttnArgs a) {
+    constexpr int NT = 32 * F8_NW;
+    static_assert(GQ <= 4, "at most four query heads per grid kv group");
+    extern __shared__ __align__(16) unsigned char f8raw[];  // 16-byte aligned: every bulk copy's target is
+    F8Smem<GQ>& S = *reinterpret_cast<F8Smem<GQ>*>(f8raw);   // at a multiple of 2 KB from it
+    __shared__ int is_last;
+
+    const int split = blockIdx.x, gv = blockIdx.y, b = blockIdx.z;
+    const int Hv = gridDim.y, Hq = Hv * GQ;
+    const int gk = gv / a.kv_div;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g8 = lane >> 2, q4 = lane & 3;
+    if (tid < 2 * F8_NW) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(f8_saddr(&S.bar[tid >> 1][tid & 1])) : "memory");
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();
+    kvq_pdl_begin();
+    const int T = a.seq_lens[b];
+    if (T > a.max_len || T < 0) {
+        if (tid == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
+        return;
+    }
+    const int n_groups = (T + KG - 1) / KG;
+    const int n_pages = (T + PG - 1) / PG;
+    const int nsplit_b = (n_groups + a.cps - 1) / a.cps;
+    if (n_groups == 0) {
+        if (split == 0)
+            for (int i = tid; i < GQ * D; i += NT) a.out[((int64_t)b * Hq + gv * GQ) * D + i] = 0.0f;
+        return;
+    }
+    if (split >= nsplit_b) return;
+    const int hb = 2 * split * a.cps;                                   // this split's 32-token steps
+    const int he = min(2 * min(n_groups, (split + 1) * a.cps), (n_pages + 1) / 2);
+
+    // the query as the B operand of the score product: column 2h = head h (fp16, unscaled)
+    const int hs = g8 >> 1;
+    const bool qcol = (g8 & 1) == 0 && hs < GQ;
+    uint32_t qb[8][2];
+    {
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(a.q + ((int64_t)b * Hq + gv * GQ + (qcol ? hs : 0)) * D);
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+            qb[st][0] = qcol ? qw[16 * q4 + 2 * st] : 0u;
+            qb[st][1] = qcol ? qw[16 * q4 + 2 * st + 1] : 0u;
+        }
+    }
+    float acc[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mt][i] = 0.0f;
+    float mrun = -INFINITY, lrun = 0.0f;
+    bool ok_run = true;
+
+    // lane 0: stage step j (tokens 32 j .. 32 j + 31) into stage stg of this warp
+    auto issue = [&](int j, int stg) {
+        uint8_t* dst = S.u.st[warp][stg];
+        uint32_t bytes = 0;
+        int32_t pg[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int lp = 2 * j + u;
+            pg[u] = lp < n_pages ? a.bt[(int64_t)b * a.max_blocks + lp] : -1;
+            if (lp < n_pages && (pg[u] < 0 || pg[u] >= a.num_blocks)) {
+                kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
+                pg[u] = -1;
+            }
+            if (pg[u] >= 0) bytes += 2 * F8_PAGE;
+        }
+        f8_expect(&S.bar[warp][stg], bytes);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (pg[u] < 0) continue;
+            const int64_t off = ((int64_t)pg[u] * a.H + gk) * F8_PAGE;
+            f8_bulk(dst + u * F8_PAGE, a.k_codes + off, F8_PAGE, &S.bar[warp][stg]);
+            f8_bulk(dst + (2 + u) * F8_PAGE, a.v_codes + off, F8_PAGE, &S.bar[warp][stg]);
+        }
+    };
+
+    int it = 0;
+    if (lane == 0 && hb + warp < he) issue(hb + warp, 0);
+    for (int j = hb + warp; j < he; j += F8_NW, ++it) {
+        const int stg = it & 1;
+        if (lane == 0 && j + F8_NW < he) {
+            // the other stage was read in the previous step (ordered by the __syncwarp that ended it)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(j + F8_NW, stg ^ 1);
+        }
+        if (!__all_sync(0xffffffffu, f8_wait(&S.bar[warp][stg], (uint32_t)(it >> 1) & 1u))) {  // warp-uniform
+            if (lane == 0) kvq_dev_flag(a.hdr, KVQ_DEV_TIMEOUT, b);
+            ok_run = false;
+            break;
+        }
+        // pages of this step present in the stage (a page outside the pool was flagged, not copied)
+        bool pv[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int lp = 2 * j + u;
+            const int32_t pg = lp < n_pages ? a.bt[(int64_t)b * a.max_blocks + lp] : -1;
+            pv[u] = pg >= 0 && pg < a.num_blocks;
+        }
+        const uint8_t* sb = S.u.st[warp][stg];
+        const int t0 = 32 * j;
+
+        // ---- scores: per page, rows g8 and g8 + 8 (head q4 in column 2 q4)
+        float sc[2][2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const uint8_t* kp = sb + u * F8_PAGE + 32 * q4;
+            const uint4 a0 = *reinterpret_cast<const uint4*>(kp + g8 * D);
+            const uint4 a1 = *reinterpret_cast<const uint4*>(kp + g8 * D + 16);
+            const uint4 b0 = *reinterpret_cast<const uint4*>(kp + (g8 + 8) * D);
+            const uint4 b1 = *reinterpret_cast<const uint4*>(kp + (g8 + 8) * D + 16);
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int st = 0; st < 8; ++st) {
+                const uint32_t wa = word_of(st < 4 ? a0 : a1, st & 3), wb = word_of(st < 4 ? b0 : b1, st & 3);
+                mma16816(d, f8_lo(wa), f8_lo(wb), f8_hi(wa), f8_hi(wb), qb[st][0], qb[st][1]);
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = t0 + 16 * u + g8 + 8 * e;
+                sc[u][e] = (pv[u] && t < T) ? d[2 * e] * KVQ_SCORE_LOG2_SCALE : -INFINITY;
+            }
+        }
+        // ---- online softmax of head q4 over the step's 32 tokens
+        float gm = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
+        gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 16));
+        const float mn = fmaxf(mrun, gm);
+        const float alpha = mn == -INFINITY ? 1.0f : exp2f(mrun - mn);
+        float ls = 0.0f;
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float p = mn == -INFINITY ? 0.0f : exp2f(sc[u][e] - mn);
+                sc[u][e] = p;
+                ls += p;
+            }
+        mrun = mn;
+        lrun = fmaf(lrun, alpha, ls);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            acc[mt][0] *= alpha;
+            acc[mt][2] *= alpha;
+        }
+        // ---- values, page by page: A = V^T (channels x tokens), B = p (column 2h = head h)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float p0 = __shfl_sync(0xffffffffu, sc[u][0], 8 * q4 + hs);
+            const float p1 = __shfl_sync(0xffffffffu, sc[u][0], 8 * q4 + 4 + hs);
+            const float p2 = __shfl_sync(0xffffffffu, sc[u][1], 8 * q4 + hs);
+            const float p3 = __shfl_sync(0xffffffffu, sc[u][1], 8 * q4 + 4 + hs);
+            const uint32_t bb0 = qcol ? pack_h2(p0, p1) : 0u;
+            const uint32_t bb1 = qcol ? pack_h2(p2, p3) : 0u;
+            const uint8_t* vp = sb + (2 + u) * F8_PAGE + 16 * g8;
+            const int tb = t0 + 16 * u + 2 * q4;  // the lane's first token
+            // tokens past the sequence (or on a page that was not copied) hold anything: zero them
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 vA = (pv[u] && tb < T) ? *reinterpret_cast<const uint4*>(vp + (2 * q4) * D) : z;
+            const uint4 vB = (pv[u] && tb + 1 < T) ? *reinterpret_cast<const uint4*>(vp + (2 * q4 + 1) * D) : z;
+            const uint4 vC = (pv[u] && tb + 8 < T) ? *reinterpret_cast<const uint4*>(vp + (2 * q4 + 8) * D) : z;
+            const uint4 vE = (pv[u] && tb + 9 < T) ? *reinterpret_cast<const uint4*>(vp + (2 * q4 + 9) * D) : z;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;  // bytes 2k, 2k + 1 of two tokens, interleaved
+                const uint32_t x01 = prmt(word_of(vA, mt >> 1), word_of(vB, mt >> 1), sel);
+                const uint32_t x23 = prmt(word_of(vC, mt >> 1), word_of(vE, mt >> 1), sel);
+                mma16816(acc[mt], f8_lo(x01), f8_hi(x01), f8_lo(x23), f8_hi(x23), bb0, bb1);
+            }
+        }
+        __syncwarp();  // the stage is read: lane 0 may refill it
+    }
+    if (!ok_run && lane == 0) {
+        // a wait that gave up: wait (bounded) for this warp's copies still in flight before the stage
+        // memory goes away (the step it waited for, and the next one if it was issued)
+        const int stg = it & 1;
+        f8_wait(&S.bar[warp][stg], (uint32_t)(it >> 1) & 1u);
+        if (hb + warp + (it + 1) * F8_NW < he) f8_wait(&S.bar[warp][stg ^ 1], (uint32_t)((it + 1) >> 1) & 1u);
+    }
+
+    // ---- this warp's state per head
+    lrun += __shfl_xor_sync(0xffffffffu, lrun, 4);
+    lrun += __shfl_xor_sync(0xffffffffu, lrun, 8);
+    lrun += __shfl_xor_sync(0xffffffffu, lrun, 16);
+    __syncthreads();  // every warp is done with its stages: the union now holds the outputs
+    if (q4 < GQ) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            S.u.ro[warp][q4][16 * g8 + 2 * mt] = acc[mt][0];
+            S.u.ro[warp][q4][16 * g8 + 2 * mt + 1] = acc[mt][2];
+        }
+    }
+    if (g8 == 0 && q4 < GQ) {
+        S.m[warp][q4] = mrun;
+        S.l[warp][q4] = lrun;
+    }
+    __syncthreads();
+
+    // ---- merge the warps, then the splits (the last CTA of the kv group)
+    const int64_t rec0 = (((int64_t)b * Hv + gv) * a.n_splits + split) * GQ;
+    for (int e = tid; e < GQ * D; e += NT) {
+        const int h = e / D, d = e % D;
+        float M = -INFINITY;
+        for (int w = 0; w < F8_NW; ++w) M = fmaxf(M, S.m[w][h]);
+        float L = 0.0f, O = 0.0f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < F8_NW; ++w) {
+                const float wt = exp2f(S.m[w][h] - M);
+                L = fmaf(S.l[w][h], wt, L);
+                O = fmaf(S.u.ro[w][h][d], wt, O);
+            }
+        }
+        float* r = a.part + (rec0 + h) * REC;
+        if (d == 0) {
+            r[0] = M;
+            r[1] = L;
+        }
+        r[4 + d] = O;
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int prev = atomicAdd(&a.counters[b * Hv + gv], 1);
+        is_last = (prev == nsplit_b - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    for (int e = tid; e < GQ * D; e += NT) {
+        const int h = e / D, d = e % D;
+        float M = -INFINITY;
+        for (int sp = 0; sp < nsplit_b; ++sp)
+            M = fmaxf(M, __ldcg(a.part + ((((int64_t)b * Hv + gv) * a.n_splits + sp) * GQ + h) * REC));
+        float Lsum = 0.0f, acc2 = 0.0f;
+        if (M != -INFINITY) {
+            for (int sp = 0; sp < nsplit_b; ++sp) {
+                const float* r = a.part + ((((int64_t)b * Hv + gv) * a.n_splits + sp) * GQ + h) * REC;
+                const float w = exp2f(__ldcg(r) - M);
+                Lsum = fmaf(__ldcg(r + 1), w, Lsum);
+                acc2 = fmaf(__ldcg(r + 4 + d), w, acc2);
+            }
+        }
+        a.out[((int64_t)b * Hq + gv * GQ + h) * D + d] = Lsum > 0.0f ? acc2 / Lsum : 0.0f;
+    }
+    if (tid == 0) a.counters[b * Hv + gv] = 0;
+}
+
 // ---------------------------------------------------------------- planning and launch
 
 // q heads per grid kv group: 8 sharing one kv head are served as two groups of 4
@@ -559,6 +879,7 @@ int resident_bits(int gq, int G) {
 // CTAs of the layer's kernel that fit on one SM at once
 int resident_ctas(const kvq_layout* L) {
     const int gq = L->n_q_heads / L->n_kv_heads, G = L->v_group_dims;
+    if (L->bits == KVQ_BITS_E4M3) return 1;  // the E4M3 kernel's stages fill an SM's shared memory
     switch (L->bits) {
         case 1: return resident_bits<1>(gq, G);
         case 2: return resident_bits<2>(gq, G);
@@ -618,6 +939,27 @@ int launch_ngv(dim3 grid, cudaStream_t s, const QAttnArgs& a) {
     }
 }
 
+template <int GQ>
+int launch_f8_gq(dim3 grid, cudaStream_t s, const QAttnArgs& a) {
+    const int smem = (int)sizeof(F8Smem<GQ>);
+    static_assert(sizeof(F8Smem<4>) <= 227 * 1024, "the E4M3 kernel's stages fit in shared memory");
+    const int st = kvq_prepare_kernel((const void*)f8_attn_kernel<GQ>, smem);
+    if (st) return st;
+    const cudaError_t e = kvq_launch_pdl(f8_attn_kernel<GQ>, grid, dim3(32 * F8_NW), (size_t)smem, s, a);
+    if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant (E4M3) launch: %s", cudaGetErrorString(e));
+    return KVQ_OK;
+}
+
+int launch_f8(int gq, dim3 grid, cudaStream_t s, QAttnArgs& a) {
+    a.kv_div = kv_div_of(gq);
+    grid.y *= a.kv_div;
+    switch (grid_gq(gq)) {
+        case 1: return launch_f8_gq<1>(grid, s, a);
+        case 2: return launch_f8_gq<2>(grid, s, a);
+        default: return launch_f8_gq<4>(grid, s, a);
+    }
+}
+
 // grid: (splits, kv heads, batch); widened here to the grid kv groups
 template <int BITS>
 int launch_bits(int gq, dim3 grid, cudaStream_t s, QAttnArgs& a) {
@@ -673,8 +1015,9 @@ extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, cons
     st = kvq_check_seqs(S, "kv_decode_attn_quant");
     if (st) return st;
     KVQ_REQUIRE(L->bits != 16, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: layer is not quantized (bits == 16)");
-    KVQ_REQUIRE(P != nullptr && P->k_codes && P->v_codes && P->k_sz && P->v_sz && P->k_tail, KVQ_ERR_INVALID_ARG,
-                "kv_decode_attn_quant: quantized pool arrays missing");
+    KVQ_REQUIRE(P != nullptr && P->k_codes && P->v_codes &&
+                    (L->bits == KVQ_BITS_E4M3 || (P->k_sz && P->v_sz && P->k_tail)),
+                KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: quantized pool arrays missing");
     KVQ_REQUIRE((((uintptr_t)P->k_codes | (uintptr_t)P->v_codes | (uintptr_t)P->k_sz | (uintptr_t)P->v_sz) & 15u) == 0,
                 KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: code and scale arrays must be 16-byte aligned");
     KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: batch exceeds max_seqs");
@@ -709,6 +1052,7 @@ extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, cons
     dim3 grid(p.n_splits, L->n_kv_heads, S->batch);
     cudaStream_t s = kvq_stream(stream);
     switch (L->bits) {
+        case KVQ_BITS_E4M3: st = launch_f8(gq, grid, s, a); break;
         case 1: st = launch_bits<1>(gq, grid, s, a); break;
         case 2: st = launch_bits<2>(gq, grid, s, a); break;
         case 4: st = launch_bits<4>(gq, grid, s, a); break;
@@ -776,8 +1120,9 @@ extern "C" int kv_decode_attn_quant_noalloc(const kvq_layout* L, const kvq_pool*
     st = kvq_check_seqs(S, "kv_decode_attn_quant_noalloc");
     if (st) return st;
     KVQ_REQUIRE(L->bits != 16, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: layer is not quantized");
-    KVQ_REQUIRE(P != nullptr && P->k_codes && P->v_codes && P->k_sz && P->v_sz && P->k_tail, KVQ_ERR_INVALID_ARG,
-                "kv_decode_attn_quant_noalloc: quantized pool arrays missing");
+    KVQ_REQUIRE(P != nullptr && P->k_codes && P->v_codes &&
+                    (L->bits == KVQ_BITS_E4M3 || (P->k_sz && P->v_sz && P->k_tail)),
+                KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: quantized pool arrays missing");
     KVQ_REQUIRE((((uintptr_t)P->k_codes | (uintptr_t)P->v_codes | (uintptr_t)P->k_sz | (uintptr_t)P->v_sz) & 15u) == 0,
                 KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: code and scale arrays must be 16-byte aligned");
     KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: batch exceeds max_seqs");
@@ -820,6 +1165,7 @@ extern "C" int kv_decode_attn_quant_noalloc(const kvq_layout* L, const kvq_pool*
     const int gq = L->n_q_heads / L->n_kv_heads;
     dim3 grid(p.n_splits, L->n_kv_heads, S->batch);
     switch (L->bits) {
+        case KVQ_BITS_E4M3: st = launch_f8(gq, grid, s, a); break;
         case 1: st = launch_bits<1>(gq, grid, s, a); break;
         case 2: st = launch_bits<2>(gq, grid, s, a); break;
         case 4: st = launch_bits<4>(gq, grid, s, a); break;

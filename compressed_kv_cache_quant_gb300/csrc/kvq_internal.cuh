@@ -46,6 +46,7 @@ enum KvqDeviceCheck : int32_t {
     KVQ_DEV_BAD_LENGTH = 3,     // seq_len outside [0, max_len] or capacity
     KVQ_DEV_OVERFLOW = 4,       // a list would exceed its capacity
     KVQ_DEV_RANGE = 5,          // a value beyond the fp16 range of a tensor-core operand
+    KVQ_DEV_TIMEOUT = 6,        // a bounded wait for an asynchronous copy gave up
 };
 
 __host__ __device__ static inline size_t kvq_round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -516,6 +516,33 @@ __global__ void __launch_bounds__(128) pack_fp16_kernel(PackArgs a) {
     atomicMax(reinterpret_cast<int*>(a.pool.k_absmax + ((int64_t)a.seq * a.H + h) * D + c), __float_as_int(amax));
 }
 
+// fp16 x4 (two f16x2 words) -> E4M3 x4, round to nearest even, finite values saturate at +-448
+__device__ __forceinline__ uint32_t e4m3x4(uint32_t lo, uint32_t hi) {
+    uint32_t r;
+    asm("{\n.reg .b16 a, b;\ncvt.rn.satfinite.e4m3x2.f16x2 a, %1;\ncvt.rn.satfinite.e4m3x2.f16x2 b, %2;\n"
+        "mov.b32 %0, {a, b};\n}"
+        : "=r"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+
+// FP8 E4M3 layer: 16 threads per token row (8 values each), 16 rows per CTA; K and V rows cast
+// to E4M3 bytes at the row's page slot.
+__global__ void __launch_bounds__(256) pack_e4m3_kernel(PackArgs a) {
+    const int h = blockIdx.y;
+    const int l16 = threadIdx.x & 15;
+    const int64_t i = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4);
+    if (i >= a.n_tokens) return;
+    const int64_t t = a.t_start + i;
+    const int32_t page = a.bt_row[t / PG];
+    if (page < 0 || page >= a.pool.num_blocks) return;  // an invalid table entry skips the row
+    const int64_t src = i * a.stride_t + (int64_t)h * D + 8 * l16;
+    const uint4 kx = *reinterpret_cast<const uint4*>(a.k + src);
+    const uint4 vx = *reinterpret_cast<const uint4*>(a.v + src);
+    const int64_t dst = (((int64_t)page * a.H + h) * PG + (t % PG)) * D + 8 * l16;
+    *reinterpret_cast<uint2*>(a.pool.k_codes + dst) = make_uint2(e4m3x4(kx.x, kx.y), e4m3x4(kx.z, kx.w));
+    *reinterpret_cast<uint2*>(a.pool.v_codes + dst) = make_uint2(e4m3x4(vx.x, vx.y), e4m3x4(vx.z, vx.w));
+}
+
 template <int BITS>
 int launch_pack_quant(const PackArgs& a, cudaStream_t s) {
     const int64_t n_groups = (a.n_tokens + KG - 1) / KG;
@@ -600,6 +627,27 @@ __global__ void __launch_bounds__(128) append_quant_kernel(AppendArgs a) {
     store_k_rows<BITS>(rows, pages, a.H, h, a.pool.k_codes, c, 128);
 }
 
+// FP8 E4M3 layer: the newest token of every (sequence, kv head), 16 threads per row (K and V)
+__global__ void __launch_bounds__(32) append_e4m3_kernel(AppendArgs a) {
+    const int h = blockIdx.x;
+    const int b = blockIdx.y;
+    const int l16 = threadIdx.x & 15;
+    kvq_pdl_begin();
+    const int T = a.seq_lens[b];
+    const int64_t p = (int64_t)T - 1;
+    if (p < 0) return;
+    if (T > a.max_len) {
+        if (threadIdx.x == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
+        return;
+    }
+    const int32_t page = page_of(a, b, p / PG);
+    if (page < 0) return;
+    const bool is_v = threadIdx.x >= 16;
+    const uint4 x = *reinterpret_cast<const uint4*>((is_v ? a.v_new : a.k_new) + ((int64_t)b * a.H + h) * D + 8 * l16);
+    uint8_t* dst = (is_v ? a.pool.v_codes : a.pool.k_codes) + (((int64_t)page * a.H + h) * PG + (p % PG)) * D + 8 * l16;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(e4m3x4(x.x, x.y), e4m3x4(x.z, x.w));
+}
+
 __global__ void __launch_bounds__(128) append_fp16_kernel(AppendArgs a) {
     const int h = blockIdx.x;
     const int b = blockIdx.y;
@@ -675,6 +723,15 @@ extern "C" int kv_quant_pack(const kvq_layout* L, const kvq_pool* P, const kvq_s
         pack_fp16_kernel<<<dim3((unsigned)tiles, H), 128, 0, s>>>(a);
         return kvq_launch_status("kv_quant_pack");
     }
+    if (L->bits == KVQ_BITS_E4M3) {
+        KVQ_REQUIRE(P->k_codes && P->v_codes && (((uintptr_t)P->k_codes | (uintptr_t)P->v_codes) & 7u) == 0,
+                    KVQ_ERR_INVALID_ARG, "kv_quant_pack: E4M3 layer needs 8-byte aligned k_codes and v_codes");
+        KVQ_REQUIRE(((uintptr_t)k & 15u) == 0 && ((uintptr_t)v & 15u) == 0 && stride_t % 8 == 0, KVQ_ERR_INVALID_ARG,
+                    "kv_quant_pack: E4M3 layer needs 16-byte aligned k, v rows (stride_t % 8 == 0)");
+        if (n_tokens == 0) return KVQ_OK;
+        pack_e4m3_kernel<<<dim3((unsigned)((n_tokens + 15) / 16), H), 256, 0, s>>>(a);
+        return kvq_launch_status("kv_quant_pack");
+    }
     KVQ_REQUIRE(P->k_codes && P->v_codes && P->k_sz && P->v_sz && P->k_tail, KVQ_ERR_INVALID_ARG,
                 "kv_quant_pack: quantized layer needs k_codes, v_codes, k_sz, v_sz, k_tail");
     KVQ_REQUIRE(((uintptr_t)P->k_codes & 15u) == 0 && ((uintptr_t)P->v_codes & 15u) == 0, KVQ_ERR_INVALID_ARG,
@@ -722,6 +779,17 @@ extern "C" int kv_page_append(const kvq_layout* L, const kvq_pool* P, const kvq_
         st = kvq_prepare_kernel((const void*)append_fp16_kernel, 0);
         if (st) return st;
         const cudaError_t e = kvq_launch_pdl(append_fp16_kernel, grid, dim3(128), 0, s, a);
+        if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_page_append launch: %s", cudaGetErrorString(e));
+        return KVQ_OK;
+    }
+    if (L->bits == KVQ_BITS_E4M3) {
+        KVQ_REQUIRE(P->k_codes && P->v_codes && (((uintptr_t)P->k_codes | (uintptr_t)P->v_codes) & 7u) == 0,
+                    KVQ_ERR_INVALID_ARG, "kv_page_append: E4M3 layer needs 8-byte aligned k_codes and v_codes");
+        KVQ_REQUIRE((((uintptr_t)k_new | (uintptr_t)v_new) & 15u) == 0, KVQ_ERR_INVALID_ARG,
+                    "kv_page_append: E4M3 layer needs 16-byte aligned k_new and v_new");
+        st = kvq_prepare_kernel((const void*)append_e4m3_kernel, 0);
+        if (st) return st;
+        const cudaError_t e = kvq_launch_pdl(append_e4m3_kernel, grid, dim3(32), 0, s, a);
         if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_page_append launch: %s", cudaGetErrorString(e));
         return KVQ_OK;
     }

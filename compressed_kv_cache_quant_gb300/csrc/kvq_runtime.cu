@@ -113,6 +113,10 @@ extern "C" int kv_page_copy(const kvq_layout* L, const kvq_pool* P, int32_t src,
         KVQ_REQUIRE(P->k16 && P->v16, KVQ_ERR_INVALID_ARG, "kv_page_copy: k16/v16 NULL");
         arrs[n++] = {P->k16, H * B * d * 2};
         arrs[n++] = {P->v16, H * B * d * 2};
+    } else if (L->bits == KVQ_BITS_E4M3) {
+        KVQ_REQUIRE(P->k_codes && P->v_codes, KVQ_ERR_INVALID_ARG, "kv_page_copy: k_codes/v_codes NULL");
+        arrs[n++] = {P->k_codes, H * B * d};
+        arrs[n++] = {P->v_codes, H * B * d};
     } else {
         KVQ_REQUIRE(P->k_codes && P->v_codes && P->k_sz && P->v_sz, KVQ_ERR_INVALID_ARG,
                     "kv_page_copy: quantized arrays NULL");
@@ -144,8 +148,9 @@ extern "C" int kvq_check(void* ws, void* stream) {
     if (hdr[0] != 0) {
         static const char* names[] = {"ok", "page id outside the pool", "token id outside the sequence",
                                       "sequence length outside its bounds", "list capacity exceeded",
-                                      "query times K scale beyond the fp16 range"};
-        const char* nm = (hdr[0] > 0 && hdr[0] <= 5) ? names[hdr[0]] : "unknown";
+                                      "query times K scale beyond the fp16 range",
+                                      "a bounded wait for an asynchronous copy gave up"};
+        const char* nm = (hdr[0] > 0 && hdr[0] <= 6) ? names[hdr[0]] : "unknown";
         int32_t zero[2] = {0, 0};
         e = cudaMemcpyAsync(ws, zero, sizeof(zero), cudaMemcpyHostToDevice, s);
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -254,9 +259,10 @@ int kvq_check_layout(const kvq_layout* L, const char* fn, bool need_q) {
     KVQ_REQUIRE(L->block_tokens == KVQ_BLOCK_TOKENS, KVQ_ERR_UNSUPPORTED, "%s: block_tokens %d (only 16)", fn,
                 L->block_tokens);
     KVQ_REQUIRE(L->n_kv_heads > 0 && L->n_q_heads > 0, KVQ_ERR_INVALID_ARG, "%s: head counts", fn);
-    KVQ_REQUIRE(L->bits == 1 || L->bits == 2 || L->bits == 4 || L->bits == 8 || L->bits == 16, KVQ_ERR_UNSUPPORTED,
-                "%s: bits %d (1, 2, 4, 8 or 16)", fn, L->bits);
-    if (L->bits != 16) {
+    KVQ_REQUIRE(L->bits == 1 || L->bits == 2 || L->bits == 4 || L->bits == 8 || L->bits == 16 ||
+                    L->bits == KVQ_BITS_E4M3,
+                KVQ_ERR_UNSUPPORTED, "%s: bits %d (1, 2, 4, 8, 16 or KVQ_BITS_E4M3)", fn, L->bits);
+    if (L->bits != 16 && L->bits != KVQ_BITS_E4M3) {
         KVQ_REQUIRE(L->k_group_tokens == KVQ_K_GROUP_TOKENS, KVQ_ERR_UNSUPPORTED, "%s: k_group_tokens %d (only 64)",
                     fn, L->k_group_tokens);
         KVQ_REQUIRE(L->v_group_dims == 32 || L->v_group_dims == 64 || L->v_group_dims == 128, KVQ_ERR_UNSUPPORTED,

@@ -18,7 +18,7 @@ import ctypes
 import torch
 
 from . import _abi
-from ._abi import BLOCK_TOKENS, HEAD_DIM, K_GROUP_TOKENS, KvqError, Layout, Pool, Seqs, check, lib  # noqa: F401
+from ._abi import BITS_E4M3, BLOCK_TOKENS, HEAD_DIM, K_GROUP_TOKENS, KvqError, Layout, Pool, Seqs, check, lib  # noqa: F401
 
 
 def _p(x):
@@ -59,7 +59,10 @@ class LayerCache:
         z = lambda shape, dt: torch.zeros(shape, dtype=dt, device=device)  # noqa: E731
         self.k_codes = self.v_codes = self.k_sz = self.v_sz = self.k_tail = None
         self.k16 = self.v16 = self.kT = self.k_absmax = None
-        if bits == 16:
+        if bits == _abi.BITS_E4M3:
+            self.k_codes = z((num_blocks, H, P, d), torch.uint8)
+            self.v_codes = z((num_blocks, H, P, d), torch.uint8)
+        elif bits == 16:
             self.k16 = z((num_blocks, H, P, d), torch.float16)
             self.v16 = z((num_blocks, H, P, d), torch.float16)
             if t_cap:

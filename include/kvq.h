@@ -67,6 +67,12 @@ extern "C" {
                                      their slots and took distributed radix passes */
 #define KVQ_PATH_RESERVED      3
 
+/* kvq_layout.bits of an FP8 E4M3 layer: K and V rows cast to E4M3 bytes (round
+ * to nearest even, finite values saturate at +-448), 128 bytes per token and kv
+ * head, no scales [Meeting §6 item 2: FP8 E4M3 preferred where the hardware
+ * has it, no dequantization arithmetic]. */
+#define KVQ_BITS_E4M3         0xE4
+
 #define KVQ_HEAD_DIM          128
 #define KVQ_BLOCK_TOKENS      16
 #define KVQ_K_GROUP_TOKENS    64
@@ -87,7 +93,8 @@ typedef struct kvq_layout {
     int32_t n_q_heads;       /* H_q; a multiple of n_kv_heads, H_q / H_kv <= 8 */
     int32_t n_kv_heads;      /* H_kv; q head h reads kv head floor(h * H_kv / H_q) */
     int32_t block_tokens;    /* tokens per page; must be 16 [KVSurvey §一.1] */
-    int32_t bits;            /* 1, 2, 4, 8: quantized layer; 16: fp16 layer */
+    int32_t bits;            /* 1, 2, 4, 8: quantized layer; 16: fp16 layer;
+                                KVQ_BITS_E4M3: FP8 E4M3 layer */
     int32_t k_group_tokens;  /* K quantization group along tokens; must be 64 [TailorKV §2.2] */
     int32_t v_group_dims;    /* V quantization group along head_dim: 32, 64 or 128 [OnDevice §3.1] */
 } kvq_layout;
@@ -117,6 +124,9 @@ typedef struct kvq_layout {
  *           V group of G = v_group_dims channels
  *   k_tail  [max_seqs][H_kv][64][d]     fp16 keys of the unfinished K group
  *           (tokens 64*floor(T/64) .. T-1 at rows t mod 64)
+ * FP8 E4M3 layer (bits == KVQ_BITS_E4M3):
+ *   k_codes, v_codes [num_blocks][H_kv][16][d] E4M3 bytes of the K and V rows
+ *   (k_sz, v_sz, k_tail unused)
  * fp16 layer (bits == 16):
  *   k16, v16 [num_blocks][H_kv][16][d]  fp16 token rows
  *   kT       [max_seqs][H_kv][d][t_cap] fp16 channel-major copy of K, the
@@ -162,6 +172,9 @@ typedef struct kvq_seqs {
  * [OnDevice §3.1].  Arithmetic: IEEE fp32 on fp16 inputs, codes computed
  * with the fp32 scale, round half to even; a group with max == min gets
  * scale 0 and codes 0.
+ *
+ * An FP8 E4M3 layer (bits == KVQ_BITS_E4M3) stores every K and V value as an
+ * E4M3 byte (cvt with round-to-nearest-even, saturating), no scales.
  *
  * Writes tokens t_start .. t_start+n_tokens-1 of sequence `seq`.  k and v are
  * device fp16 [n_tokens][H_kv][d] with `stride_t` elements between tokens
@@ -210,6 +223,10 @@ size_t kv_page_append_ws(void);
  * fp16 operand range); otherwise the status word reports a range error and
  * the output is not valid.  The context is split across CTAs and the
  * partial softmax states are merged by log-sum-exp.  An empty sequence gives 0.
+ * An FP8 E4M3 layer (bits == KVQ_BITS_E4M3) is attended the same way: its
+ * pages are staged into shared memory by bulk asynchronous copies, keys and
+ * values widened to fp16 (exactly) for the tensor cores; products with q are
+ * exact, sums fp32, p enters the value product in fp16.
  * ws: kv_decode_attn_quant_ws(layout, seqs) bytes.
  * ---------------------------------------------------------------------- */
 int kv_decode_attn_quant(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
