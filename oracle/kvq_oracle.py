@@ -132,6 +132,44 @@ def pack_v(v16, bits, group_dims):
                 bits=bits, group_dims=group_dims)
 
 
+def quantize_groups_sym(x16, bits):
+    """Symmetric quantization of every group (the LAST axis of ``x16``).
+
+    [On-device article §3.1: V quantized INT4 symmetric, in groups of 32/64
+    channels] per group: scale = max |x| / L, code = clamp(round(x / scale), -L, L)
+    with L = 2^(b-1) - 1; the scale is stored as fp16.
+
+    READING: the restricted symmetric range -L..L (no -2^(b-1)), round half to
+    even, IEEE fp32 arithmetic on the fp16 inputs and codes computed with the
+    fp32 scale as in ``quantize_groups``; an all-zero group gets scale 0 and codes
+    0; b >= 2 (for b = 1 the range is empty).
+    Returns (codes int64 in [-L, L], scale16 float16, scale32 float32)."""
+    assert bits >= 2
+    x = np.asarray(x16, dtype=np.float16).astype(np.float32)
+    L = np.float32(2 ** (bits - 1) - 1)
+    amax = np.abs(x).max(axis=-1, keepdims=True)
+    scale32 = (amax / L).astype(np.float32)           # fp32, one rounding
+    ok = scale32 > 0
+    safe = np.where(ok, scale32, np.float32(1.0))
+    with np.errstate(over="ignore", invalid="ignore"):
+        u = (x / safe).astype(np.float32)             # fp32, one rounding
+    codes = np.clip(np.rint(u), -L, L)
+    codes = np.where(ok, codes, np.float32(0)).astype(np.int64)
+    return codes, scale32[..., 0].astype(np.float16), scale32[..., 0]
+
+
+def pack_v_sym(v16, bits, group_dims):
+    """Symmetric quantization of the values of one (sequence, kv head), per token
+    in groups of ``group_dims`` channels [on-device article §3.1].
+    Returns dict(codes [T][d] int64 in [-L, L], scale16/scale32 [T][d/group_dims])."""
+    v16 = np.asarray(v16, dtype=np.float16)
+    T, d = v16.shape
+    g = v16.reshape(T, d // group_dims, group_dims)
+    codes, s16, s32 = quantize_groups_sym(g, bits)
+    return dict(codes=codes.reshape(T, d), scale16=s16, scale32=s32, bits=bits, group_dims=group_dims,
+                symmetric=True)
+
+
 def dequant_k(pk):
     """fp64 keys as the quantized cache represents them: zero + code * scale
     for packed tokens (stored fp16 scale/zero), fp16 values for the tail."""
@@ -148,12 +186,15 @@ def dequant_k(pk):
 
 
 def dequant_v(pv):
-    """fp64 values as the quantized cache represents them."""
+    """fp64 values as the quantized cache represents them: zero + code * scale,
+    or code * scale for a symmetric cache (``pack_v_sym``)."""
     T, d = pv["codes"].shape
     gd = pv["group_dims"]
     j = np.arange(d) // gd
-    return (pv["zero16"].astype(np.float64)[:, j]
-            + pv["codes"].astype(np.float64) * pv["scale16"].astype(np.float64)[:, j])
+    vals = pv["codes"].astype(np.float64) * pv["scale16"].astype(np.float64)[:, j]
+    if pv.get("symmetric"):
+        return vals
+    return pv["zero16"].astype(np.float64)[:, j] + vals
 
 
 # ---------------------------------------------------------------------------

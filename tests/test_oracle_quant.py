@@ -163,3 +163,77 @@ def test_sixteen_bit_is_nearly_lossless():
     err = np.abs(O.dequant_v(pv) - V.astype(np.float64))
     rng_g = np.ptp(V.astype(np.float64).reshape(64, 2, 64), axis=2).repeat(64, axis=1)
     assert np.all(err <= rng_g * (2.0 ** -11 + 0.5 / 65535))
+
+
+# ---- symmetric V quantization   [on-device article §3.1: V INT4 symmetric, group quantization]
+
+def test_golden_symmetric_groups(golden_dir):
+    import os
+    n = 0
+    with open(os.path.join(golden_dir, "sym_v_small.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            bits, xs, cs, sc = [c.strip() for c in line.split("|")]
+            x = np.array([float(v) for v in xs.split()], np.float16)
+            codes, s16, s32 = O.quantize_groups_sym(x, int(bits))
+            assert codes.tolist() == [int(v) for v in cs.split()]
+            assert float(s32) == float(sc) and float(s16) == float(sc)
+            n += 1
+    assert n == 4
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_symmetric_bound_range_and_extremes(bits):
+    """|x - code * scale32| <= scale32 / 2 (fp64, plus the one-rounding slack L * 2^-23 of the
+    fp32 quotient), codes in [-L, L], max |x| -> +-L."""
+    rng = np.random.default_rng(60 + bits)
+    x = (rng.standard_normal((500, 64)) * rng.choice([0.01, 1, 30], size=(500, 1))).astype(np.float16)
+    codes, s16, s32 = O.quantize_groups_sym(x, bits)
+    L = 2 ** (bits - 1) - 1
+    assert codes.min() >= -L and codes.max() <= L
+    err = np.abs(x.astype(np.float64) - codes * s32.astype(np.float64)[:, None])
+    assert np.all(err <= s32.astype(np.float64)[:, None] * (0.5 + L * 2.0 ** -23))
+    i = np.argmax(np.abs(x.astype(np.float32)), axis=1)
+    assert np.all(np.abs(codes[np.arange(500), i]) == L)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_symmetric_mirror(bits):
+    """A group and its negation get the same scale and negated codes (ties go to even either way)."""
+    rng = np.random.default_rng(70 + bits)
+    x = rng.standard_normal((300, 32)).astype(np.float16)
+    c1, s1, _ = O.quantize_groups_sym(x, bits)
+    c2, s2, _ = O.quantize_groups_sym(-x, bits)
+    assert np.array_equal(c1, -c2) and np.array_equal(s1.view(np.uint16), s2.view(np.uint16))
+
+
+def test_symmetric_exact_rounding_away_from_ties():
+    """Codes equal the exact rational round-to-nearest of x / scale32 where the quotient is not
+    within 1e-6 of a half-integer (computed with Python fractions)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(80)
+    x = rng.standard_normal((200, 16)).astype(np.float16)
+    codes, _, s32 = O.quantize_groups_sym(x, 4)
+    for g in range(200):
+        sc = Fraction(float(s32[g]))
+        for k in range(16):
+            q = Fraction(float(x[g, k])) / sc
+            frac = q - (q.numerator // q.denominator)
+            if abs(frac - Fraction(1, 2)) < Fraction(1, 10 ** 6):
+                continue
+            want = max(-7, min(7, round(q)))
+            assert codes[g, k] == want
+
+
+def test_symmetric_dequant_and_attention():
+    """The symmetric cache dequantizes to code * scale16; attention over it stays close to
+    attention over the fp16 values (4-bit, G 32)."""
+    rng = np.random.default_rng(81)
+    V = rng.standard_normal((400, 128)).astype(np.float16)
+    pv = O.pack_v_sym(V, 4, 32)
+    vh = O.dequant_v(pv)
+    j = np.arange(128) // 32
+    assert np.array_equal(vh, pv["codes"] * pv["scale16"].astype(np.float64)[:, j])
+    assert np.max(np.abs(vh - V.astype(np.float64))) <= np.max(pv["scale32"]) * 0.51 + 1e-3
