@@ -25,6 +25,7 @@ ABI_VERSION = 1
 HEAD_DIM = 128
 BLOCK_TOKENS = 16
 BITS_E4M3 = 0xE4          # kvq_layout.bits of an FP8 E4M3 layer
+V_SYMMETRIC = 0x100       # or-ed into kvq_layout.bits: V quantized symmetrically
 K_GROUP_TOKENS = 64
 
 N_PATH_COUNTERS = 4

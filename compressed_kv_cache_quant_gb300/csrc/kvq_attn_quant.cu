@@ -879,8 +879,8 @@ int resident_bits(int gq, int G) {
 // CTAs of the layer's kernel that fit on one SM at once
 int resident_ctas(const kvq_layout* L) {
     const int gq = L->n_q_heads / L->n_kv_heads, G = L->v_group_dims;
-    if (L->bits == KVQ_BITS_E4M3) return 1;  // the E4M3 kernel's stages fill an SM's shared memory
-    switch (L->bits) {
+    if (kvq_code_bits(L) == KVQ_BITS_E4M3) return 1;  // the E4M3 kernel's stages fill an SM's shared memory
+    switch (kvq_code_bits(L)) {
         case 1: return resident_bits<1>(gq, G);
         case 2: return resident_bits<2>(gq, G);
         case 4: return resident_bits<4>(gq, G);
@@ -1014,9 +1014,9 @@ extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, cons
     if (st) return st;
     st = kvq_check_seqs(S, "kv_decode_attn_quant");
     if (st) return st;
-    KVQ_REQUIRE(L->bits != 16, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: layer is not quantized (bits == 16)");
+    KVQ_REQUIRE(kvq_code_bits(L) != 16, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: layer is not quantized (bits == 16)");
     KVQ_REQUIRE(P != nullptr && P->k_codes && P->v_codes &&
-                    (L->bits == KVQ_BITS_E4M3 || (P->k_sz && P->v_sz && P->k_tail)),
+                    (kvq_code_bits(L) == KVQ_BITS_E4M3 || (P->k_sz && P->v_sz && P->k_tail)),
                 KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: quantized pool arrays missing");
     KVQ_REQUIRE((((uintptr_t)P->k_codes | (uintptr_t)P->v_codes | (uintptr_t)P->k_sz | (uintptr_t)P->v_sz) & 15u) == 0,
                 KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: code and scale arrays must be 16-byte aligned");
@@ -1051,7 +1051,7 @@ extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, cons
     const int gq = L->n_q_heads / L->n_kv_heads;
     dim3 grid(p.n_splits, L->n_kv_heads, S->batch);
     cudaStream_t s = kvq_stream(stream);
-    switch (L->bits) {
+    switch (kvq_code_bits(L)) {
         case KVQ_BITS_E4M3: st = launch_f8(gq, grid, s, a); break;
         case 1: st = launch_bits<1>(gq, grid, s, a); break;
         case 2: st = launch_bits<2>(gq, grid, s, a); break;
@@ -1119,9 +1119,9 @@ extern "C" int kv_decode_attn_quant_noalloc(const kvq_layout* L, const kvq_pool*
     if (st) return st;
     st = kvq_check_seqs(S, "kv_decode_attn_quant_noalloc");
     if (st) return st;
-    KVQ_REQUIRE(L->bits != 16, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: layer is not quantized");
+    KVQ_REQUIRE(kvq_code_bits(L) != 16, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: layer is not quantized");
     KVQ_REQUIRE(P != nullptr && P->k_codes && P->v_codes &&
-                    (L->bits == KVQ_BITS_E4M3 || (P->k_sz && P->v_sz && P->k_tail)),
+                    (kvq_code_bits(L) == KVQ_BITS_E4M3 || (P->k_sz && P->v_sz && P->k_tail)),
                 KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: quantized pool arrays missing");
     KVQ_REQUIRE((((uintptr_t)P->k_codes | (uintptr_t)P->v_codes | (uintptr_t)P->k_sz | (uintptr_t)P->v_sz) & 15u) == 0,
                 KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_noalloc: code and scale arrays must be 16-byte aligned");
@@ -1164,7 +1164,7 @@ extern "C" int kv_decode_attn_quant_noalloc(const kvq_layout* L, const kvq_pool*
     a.cps = p.cps;
     const int gq = L->n_q_heads / L->n_kv_heads;
     dim3 grid(p.n_splits, L->n_kv_heads, S->batch);
-    switch (L->bits) {
+    switch (kvq_code_bits(L)) {
         case KVQ_BITS_E4M3: st = launch_f8(gq, grid, s, a); break;
         case 1: st = launch_bits<1>(gq, grid, s, a); break;
         case 2: st = launch_bits<2>(gq, grid, s, a); break;

@@ -86,6 +86,17 @@ __device__ __forceinline__ uint32_t kvq_code(float x, float mn, float scale32, f
     return (uint32_t)r;
 }
 
+// Symmetric code of x, stored offset by L: clamp(rint(fl(x / scale)), -L, L) + L; L for scale 0.
+__device__ __forceinline__ uint32_t kvq_code_sym(float x, float scale32, int L) {
+    if (!(scale32 > 0.0f)) return (uint32_t)L;
+    const float r = fminf(fmaxf(rintf(__fdiv_rn(x, scale32)), (float)-L), (float)L);
+    return (uint32_t)((int)r + L);
+}
+// The stored zero of a symmetric group: -L * fp16(scale), exact in fp32 (rounded to fp16 on store).
+__device__ __forceinline__ float kvq_sym_zero(float scale32, int L) {
+    return -(float)L * __half2float(__float2half_rn(scale32));
+}
+
 __device__ __forceinline__ float kvq_warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -158,6 +169,10 @@ __host__ __device__ static inline void kvq_v_code_pos(int tok, int d, int bits, 
 // memory between launches, and allow `dyn_smem_max` bytes of dynamic shared
 // memory.  Returns KVQ_OK or KVQ_ERR_CUDA.
 int kvq_prepare_kernel(const void* func, int dyn_smem_max);
+
+// The code width of a layout (its bits without the KVQ_V_SYMMETRIC flag) and the flag.
+static inline int kvq_code_bits(const kvq_layout* L) { return L->bits & 0xFF; }
+static inline bool kvq_v_sym(const kvq_layout* L) { return (L->bits & KVQ_V_SYMMETRIC) != 0; }
 
 // Validates the fields of a layout shared by all calls.  need_q: the call
 // reads query heads (H_q / H_kv must be 1, 2, 4 or 8).

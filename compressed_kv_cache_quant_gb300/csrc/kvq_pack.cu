@@ -50,7 +50,7 @@ __device__ __forceinline__ uint32_t pack_sz(float scale32, float zero) {
 
 // One warp quantizes one V token of 128 channels in groups of G.  Lane l holds channels
 // 4l..4l+3 and returns their codes; (scale, zero) of each group goes to dst_sz.
-template <int BITS>
+template <int BITS, bool SYM>
 __device__ __forceinline__ void quant_v_token(const uint16_t* src, int G, uint32_t* dst_sz, int lane,
                                               uint32_t* codes) {
     const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
@@ -66,11 +66,19 @@ __device__ __forceinline__ void quant_v_token(const uint16_t* src, int G, uint32
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
-    const float levels = (float)((1 << BITS) - 1);
-    const float scale = kvq_scale32(mn, mx, levels);
+    if constexpr (SYM) {  // scale = max|x| / L, codes offset by L, zero = -L * scale16
+        constexpr int L = (1 << (BITS - 1)) - 1;
+        const float scale = __fdiv_rn(fmaxf(fabsf(mn), fabsf(mx)), (float)L);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) codes[i] = kvq_code(x[i], mn, scale, levels);
-    if ((lane % lpg) == 0) dst_sz[lane / lpg] = pack_sz(scale, mn);
+        for (int i = 0; i < 4; ++i) codes[i] = kvq_code_sym(x[i], scale, L);
+        if ((lane % lpg) == 0) dst_sz[lane / lpg] = pack_sz(scale, kvq_sym_zero(scale, L));
+    } else {
+        const float levels = (float)((1 << BITS) - 1);
+        const float scale = kvq_scale32(mn, mx, levels);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) codes[i] = kvq_code(x[i], mn, scale, levels);
+        if ((lane % lpg) == 0) dst_sz[lane / lpg] = pack_sz(scale, mn);
+    }
 }
 
 // Places the four codes of lane l (channels 4l..4l+3) of page token `tok` into a V page block,
@@ -166,6 +174,15 @@ __host__ __device__ constexpr uint32_t pk_word_bias() {
     return c;
 }
 
+// The symmetric V words: the same sums of v patterns, each code then offset by L.
+template <int BITS>
+__host__ __device__ constexpr uint32_t pk_word_bias_sym() {
+    uint32_t c = pk_word_bias<BITS>();
+    constexpr uint32_t L = BITS >= 2 ? (1u << (BITS - 1)) - 1u : 0u;
+    for (int sl = 0; sl < 16 / BITS; ++sl) c -= (L << (sl * BITS)) + (L << (sl * BITS + 16));
+    return c;
+}
+
 __device__ __forceinline__ uint64_t pk_pack(float lo, float hi) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -200,13 +217,20 @@ __device__ __forceinline__ void pk_acc2(uint32_t xw, uint64_t mn2, uint64_t rcp2
 
 // The same code, one value: when its quotient is close to a tie, replaces the fast code in `acc`
 // by the one the IEEE division gives.
-template <int BITS>
+template <int BITS, bool SYM = false>
 __device__ __forceinline__ void pk_fix(float x, float mn, float rcp, float sc, int off, uint32_t& acc) {
     const float d = __fsub_rn(x, mn);
     const float v = __fmaf_rn(d, rcp, PK_MAGIC);
     if (fabsf(__fmaf_rn(d, rcp, __fsub_rn(PK_MAGIC, v))) > PK_NEAR) {
-        const uint32_t fast = __float_as_uint(v) - PK_MAGIC_BITS;
-        acc += (kvq_code(x, mn, sc, (float)((1 << BITS) - 1)) - fast) << off;
+        const uint32_t fast = __float_as_uint(v) - PK_MAGIC_BITS;  // signed code (symmetric: before the offset)
+        uint32_t exact;
+        if constexpr (SYM) {
+            constexpr int L = (1 << (BITS - 1)) - 1;
+            exact = kvq_code_sym(x, sc, L) - (uint32_t)L;
+        } else {
+            exact = kvq_code(x, mn, sc, (float)((1 << BITS) - 1));
+        }
+        acc += (exact - fast) << off;
     }
 }
 
@@ -279,7 +303,7 @@ __device__ __forceinline__ int pk_valid(const PackArgs& a, int gi) {
 //      channels 16t + 8u + x of token pairs r + 4e, m = 4r + 2e + u.  No atomics.
 // A page only partly covered keeps its other tokens' V codes; the keys of an unfinished group go
 // to the tail buffer.  An invalid table entry skips its page (for K: the group).
-template <int BITS>
+template <int BITS, bool SYMV>
 __global__ void __launch_bounds__(256) pack_group_kernel(PackArgs a) {
     constexpr int WPR = 4 * BITS;  // K code words per token row
     constexpr int BW = 64 * BITS;  // V code words per page block
@@ -373,7 +397,12 @@ __global__ void __launch_bounds__(256) pack_group_kernel(PackArgs a) {
             mn = (tok & 1) ? __high2float(m2) : __low2float(m2);
             mx = (tok & 1) ? __high2float(x2) : __low2float(x2);
         }
-        const float sc = kvq_scale32(mn, mx, LEV);
+        float sc = kvq_scale32(mn, mx, LEV);
+        float zs = mn;  // the zero the code words subtract (symmetric V: none)
+        if (SYMV && e >= D) {
+            sc = __fdiv_rn(fmaxf(fabsf(mn), fabsf(mx)), (float)((1 << (BITS - 1)) - 1));
+            zs = 0.0f;
+        }
         const float rcp = sc > 0.0f ? 1.0f / sc : 0.0f;
         if (e < D) {
             float* ks4 = reinterpret_cast<float*>(kst + (e >> 1));  // {zero lo, zero hi, 1/sc lo, 1/sc hi}
@@ -384,12 +413,13 @@ __global__ void __launch_bounds__(256) pack_group_kernel(PackArgs a) {
         } else {
             const int tg = e - D, tok = tg >> (7 - gsh), g = tg & (NGV - 1);
             float* vs4 = reinterpret_cast<float*>(vst + (tok >> 1) * 4 + g);  // {zero even, zero odd, 1/sc ..}
-            vs4[tok & 1] = mn;
+            vs4[tok & 1] = zs;
             vs4[2 + (tok & 1)] = rcp;
             vsc[tok * 4 + g] = sc;
             const int32_t pj = pages[tok / PG];
+            const float zst = SYMV ? kvq_sym_zero(sc, (1 << (BITS - 1)) - 1) : mn;
             if (tok < nv && pj >= 0)
-                a.pool.v_sz[(((int64_t)pj * a.H + h) * PG + tok % PG) * NGV + g] = pack_sz(sc, mn);
+                a.pool.v_sz[(((int64_t)pj * a.H + h) * PG + tok % PG) * NGV + g] = pack_sz(sc, zst);
         }
     }
     if (!full) {  // the unfinished group: its keys go to the tail buffer (rows t mod 64 = i)
@@ -449,15 +479,16 @@ __global__ void __launch_bounds__(256) pack_group_kernel(PackArgs a) {
                     const ulonglong2 st = reinterpret_cast<const ulonglong2*>(vs)[yl * 4];
                     pk_acc2(((m & 1) ? v1 : v0)[yl * D], st.x, st.y, sl * BITS, acc, far);
                 }
-                acc -= BIAS;
+                acc -= SYMV ? pk_word_bias_sym<BITS>() : BIAS;
                 if (far > PK_NEAR) {
 #pragma unroll 1
                     for (int sl = 0; sl < PER; ++sl) {
                         const int m = q * PER + sl, yl = (m >> 2) + 4 * ((m >> 1) & 1), tok = 16 * j + 2 * yl;
                         const __half2 x2 = pk_h2(((m & 1) ? v1 : v0)[yl * D]);
                         const float4 st = vs[yl * 4];
-                        pk_fix<BITS>(__low2float(x2), st.x, st.z, vsc[tok * 4 + g], sl * BITS, acc);
-                        pk_fix<BITS>(__high2float(x2), st.y, st.w, vsc[(tok + 1) * 4 + g], sl * BITS + 16, acc);
+                        pk_fix<BITS, SYMV>(__low2float(x2), st.x, st.z, vsc[tok * 4 + g], sl * BITS, acc);
+                        pk_fix<BITS, SYMV>(__high2float(x2), st.y, st.w, vsc[(tok + 1) * 4 + g], sl * BITS + 16,
+                                           acc);
                     }
                 }
                 if (PG * (j + 1) > nv) {  // partly covered page: keep the codes of later tokens
@@ -543,14 +574,14 @@ __global__ void __launch_bounds__(256) pack_e4m3_kernel(PackArgs a) {
     *reinterpret_cast<uint2*>(a.pool.v_codes + dst) = make_uint2(e4m3x4(vx.x, vx.y), e4m3x4(vx.z, vx.w));
 }
 
-template <int BITS>
+template <int BITS, bool SYMV>
 int launch_pack_quant(const PackArgs& a, cudaStream_t s) {
     const int64_t n_groups = (a.n_tokens + KG - 1) / KG;
     if (n_groups == 0) return KVQ_OK;
     const int smem = (int)pack_group_smem();
-    const int st = kvq_prepare_kernel((const void*)pack_group_kernel<BITS>, smem);
+    const int st = kvq_prepare_kernel((const void*)pack_group_kernel<BITS, SYMV>, smem);
     if (st) return st;
-    pack_group_kernel<BITS><<<dim3((unsigned)n_groups, a.H), 256, smem, s>>>(a);
+    pack_group_kernel<BITS, SYMV><<<dim3((unsigned)n_groups, a.H), 256, smem, s>>>(a);
     return kvq_launch_status("kv_quant_pack");
 }
 
@@ -579,7 +610,7 @@ __device__ __forceinline__ int32_t page_of(const AppendArgs& a, int b, int64_t l
     return p;
 }
 
-template <int BITS>
+template <int BITS, bool SYMV>
 __global__ void __launch_bounds__(128) append_quant_kernel(AppendArgs a) {
     __shared__ __align__(16) uint32_t rows[KG * 4 * BITS];
     __shared__ int32_t pages[4];
@@ -602,7 +633,7 @@ __global__ void __launch_bounds__(128) append_quant_kernel(AppendArgs a) {
     if (c < 32) {
         const int64_t slot = ((int64_t)page * a.H + h) * PG + (p % PG);
         uint32_t codes[4];
-        quant_v_token<BITS>(vn, a.G, a.pool.v_sz + slot * (D / a.G), c, codes);
+        quant_v_token<BITS, SYMV>(vn, a.G, a.pool.v_sz + slot * (D / a.G), c, codes);
         put_v_codes<BITS>(reinterpret_cast<uint32_t*>(a.pool.v_codes) + ((int64_t)page * a.H + h) * 64 * BITS,
                           (int)(p % PG), c, codes);
     }
@@ -713,7 +744,7 @@ extern "C" int kv_quant_pack(const kvq_layout* L, const kvq_pool* P, const kvq_s
     a.v = v;
     a.stride_t = stride_t;
     cudaStream_t s = kvq_stream(stream);
-    if (L->bits == 16) {
+    if (kvq_code_bits(L) == 16) {
         KVQ_REQUIRE(P->k16 && P->v16 && (P->kT == nullptr) == (P->k_absmax == nullptr), KVQ_ERR_INVALID_ARG,
                     "kv_quant_pack: fp16 layer needs k16, v16, and kT with k_absmax or neither");
         KVQ_REQUIRE(P->kT == nullptr || (P->t_cap % 8 == 0 && t_start + n_tokens <= P->t_cap), KVQ_ERR_INVALID_ARG,
@@ -723,7 +754,7 @@ extern "C" int kv_quant_pack(const kvq_layout* L, const kvq_pool* P, const kvq_s
         pack_fp16_kernel<<<dim3((unsigned)tiles, H), 128, 0, s>>>(a);
         return kvq_launch_status("kv_quant_pack");
     }
-    if (L->bits == KVQ_BITS_E4M3) {
+    if (kvq_code_bits(L) == KVQ_BITS_E4M3) {
         KVQ_REQUIRE(P->k_codes && P->v_codes && (((uintptr_t)P->k_codes | (uintptr_t)P->v_codes) & 7u) == 0,
                     KVQ_ERR_INVALID_ARG, "kv_quant_pack: E4M3 layer needs 8-byte aligned k_codes and v_codes");
         KVQ_REQUIRE(((uintptr_t)k & 15u) == 0 && ((uintptr_t)v & 15u) == 0 && stride_t % 8 == 0, KVQ_ERR_INVALID_ARG,
@@ -736,11 +767,12 @@ extern "C" int kv_quant_pack(const kvq_layout* L, const kvq_pool* P, const kvq_s
                 "kv_quant_pack: quantized layer needs k_codes, v_codes, k_sz, v_sz, k_tail");
     KVQ_REQUIRE(((uintptr_t)P->k_codes & 15u) == 0 && ((uintptr_t)P->v_codes & 15u) == 0, KVQ_ERR_INVALID_ARG,
                 "kv_quant_pack: code arrays must be 16-byte aligned");
-    switch (L->bits) {
-        case 1: return launch_pack_quant<1>(a, s);
-        case 2: return launch_pack_quant<2>(a, s);
-        case 4: return launch_pack_quant<4>(a, s);
-        default: return launch_pack_quant<8>(a, s);
+    const bool sym = kvq_v_sym(L);
+    switch (kvq_code_bits(L)) {
+        case 1: return launch_pack_quant<1, false>(a, s);
+        case 2: return sym ? launch_pack_quant<2, true>(a, s) : launch_pack_quant<2, false>(a, s);
+        case 4: return sym ? launch_pack_quant<4, true>(a, s) : launch_pack_quant<4, false>(a, s);
+        default: return sym ? launch_pack_quant<8, true>(a, s) : launch_pack_quant<8, false>(a, s);
     }
 }
 
@@ -773,7 +805,7 @@ extern "C" int kv_page_append(const kvq_layout* L, const kvq_pool* P, const kvq_
     a.hdr = static_cast<KvqWsHeader*>(ws);
     cudaStream_t s = kvq_stream(stream);
     dim3 grid(a.H, S->batch);
-    if (L->bits == 16) {
+    if (kvq_code_bits(L) == 16) {
         KVQ_REQUIRE(P->k16 && P->v16 && (P->kT == nullptr) == (P->k_absmax == nullptr), KVQ_ERR_INVALID_ARG,
                     "kv_page_append: fp16 layer needs k16, v16, and kT with k_absmax or neither");
         st = kvq_prepare_kernel((const void*)append_fp16_kernel, 0);
@@ -782,7 +814,7 @@ extern "C" int kv_page_append(const kvq_layout* L, const kvq_pool* P, const kvq_
         if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_page_append launch: %s", cudaGetErrorString(e));
         return KVQ_OK;
     }
-    if (L->bits == KVQ_BITS_E4M3) {
+    if (kvq_code_bits(L) == KVQ_BITS_E4M3) {
         KVQ_REQUIRE(P->k_codes && P->v_codes && (((uintptr_t)P->k_codes | (uintptr_t)P->v_codes) & 7u) == 0,
                     KVQ_ERR_INVALID_ARG, "kv_page_append: E4M3 layer needs 8-byte aligned k_codes and v_codes");
         KVQ_REQUIRE((((uintptr_t)k_new | (uintptr_t)v_new) & 15u) == 0, KVQ_ERR_INVALID_ARG,
@@ -795,18 +827,15 @@ extern "C" int kv_page_append(const kvq_layout* L, const kvq_pool* P, const kvq_
     }
     KVQ_REQUIRE(P->k_codes && P->v_codes && P->k_sz && P->v_sz && P->k_tail, KVQ_ERR_INVALID_ARG,
                 "kv_page_append: quantized layer needs k_codes, v_codes, k_sz, v_sz, k_tail");
-    const void* fn = L->bits == 1 ? (const void*)append_quant_kernel<1>
-                   : L->bits == 2 ? (const void*)append_quant_kernel<2>
-                   : L->bits == 4 ? (const void*)append_quant_kernel<4> : (const void*)append_quant_kernel<8>;
-    st = kvq_prepare_kernel(fn, 0);
+    const int cb = kvq_code_bits(L);
+    const bool sym = kvq_v_sym(L);
+    void (*fn)(AppendArgs) = cb == 1 ? append_quant_kernel<1, false>
+                           : cb == 2 ? (sym ? append_quant_kernel<2, true> : append_quant_kernel<2, false>)
+                           : cb == 4 ? (sym ? append_quant_kernel<4, true> : append_quant_kernel<4, false>)
+                                     : (sym ? append_quant_kernel<8, true> : append_quant_kernel<8, false>);
+    st = kvq_prepare_kernel((const void*)fn, 0);
     if (st) return st;
-    cudaError_t e;
-    switch (L->bits) {
-        case 1: e = kvq_launch_pdl(append_quant_kernel<1>, grid, dim3(128), 0, s, a); break;
-        case 2: e = kvq_launch_pdl(append_quant_kernel<2>, grid, dim3(128), 0, s, a); break;
-        case 4: e = kvq_launch_pdl(append_quant_kernel<4>, grid, dim3(128), 0, s, a); break;
-        default: e = kvq_launch_pdl(append_quant_kernel<8>, grid, dim3(128), 0, s, a); break;
-    }
+    const cudaError_t e = kvq_launch_pdl(fn, grid, dim3(128), 0, s, a);
     if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_page_append launch: %s", cudaGetErrorString(e));
     return kvq_launch_status("kv_page_append");
 }

@@ -109,11 +109,13 @@ extern "C" int kv_page_copy(const kvq_layout* L, const kvq_pool* P, int32_t src,
     struct Arr { void* base; size_t bytes_per_page; };
     Arr arrs[6];
     int n = 0;
-    if (L->bits == 16) {
+    KVQ_REQUIRE((L->bits & ~(0xFF | KVQ_V_SYMMETRIC)) == 0, KVQ_ERR_UNSUPPORTED, "kv_page_copy: bits");
+    const int cb = kvq_code_bits(L);
+    if (cb == 16) {
         KVQ_REQUIRE(P->k16 && P->v16, KVQ_ERR_INVALID_ARG, "kv_page_copy: k16/v16 NULL");
         arrs[n++] = {P->k16, H * B * d * 2};
         arrs[n++] = {P->v16, H * B * d * 2};
-    } else if (L->bits == KVQ_BITS_E4M3) {
+    } else if (cb == KVQ_BITS_E4M3) {
         KVQ_REQUIRE(P->k_codes && P->v_codes, KVQ_ERR_INVALID_ARG, "kv_page_copy: k_codes/v_codes NULL");
         arrs[n++] = {P->k_codes, H * B * d};
         arrs[n++] = {P->v_codes, H * B * d};
@@ -122,7 +124,7 @@ extern "C" int kv_page_copy(const kvq_layout* L, const kvq_pool* P, int32_t src,
                     "kv_page_copy: quantized arrays NULL");
         KVQ_REQUIRE(L->v_group_dims == 32 || L->v_group_dims == 64 || L->v_group_dims == 128,
                     KVQ_ERR_UNSUPPORTED, "kv_page_copy: v_group_dims");
-        const size_t R = d * (size_t)L->bits / 8;
+        const size_t R = d * (size_t)cb / 8;
         arrs[n++] = {P->k_codes, H * B * R};
         arrs[n++] = {P->v_codes, H * B * R};
         arrs[n++] = {P->k_sz, H * d * 4};
@@ -259,10 +261,13 @@ int kvq_check_layout(const kvq_layout* L, const char* fn, bool need_q) {
     KVQ_REQUIRE(L->block_tokens == KVQ_BLOCK_TOKENS, KVQ_ERR_UNSUPPORTED, "%s: block_tokens %d (only 16)", fn,
                 L->block_tokens);
     KVQ_REQUIRE(L->n_kv_heads > 0 && L->n_q_heads > 0, KVQ_ERR_INVALID_ARG, "%s: head counts", fn);
-    KVQ_REQUIRE(L->bits == 1 || L->bits == 2 || L->bits == 4 || L->bits == 8 || L->bits == 16 ||
-                    L->bits == KVQ_BITS_E4M3,
+    const int cb = kvq_code_bits(L);
+    KVQ_REQUIRE((L->bits & ~(0xFF | KVQ_V_SYMMETRIC)) == 0 &&
+                    (cb == 1 || cb == 2 || cb == 4 || cb == 8 || cb == 16 || cb == KVQ_BITS_E4M3),
                 KVQ_ERR_UNSUPPORTED, "%s: bits %d (1, 2, 4, 8, 16 or KVQ_BITS_E4M3)", fn, L->bits);
-    if (L->bits != 16 && L->bits != KVQ_BITS_E4M3) {
+    KVQ_REQUIRE(!kvq_v_sym(L) || cb == 2 || cb == 4 || cb == 8, KVQ_ERR_UNSUPPORTED,
+                "%s: symmetric V needs 2, 4 or 8 bits", fn);
+    if (cb != 16 && cb != KVQ_BITS_E4M3) {
         KVQ_REQUIRE(L->k_group_tokens == KVQ_K_GROUP_TOKENS, KVQ_ERR_UNSUPPORTED, "%s: k_group_tokens %d (only 64)",
                     fn, L->k_group_tokens);
         KVQ_REQUIRE(L->v_group_dims == 32 || L->v_group_dims == 64 || L->v_group_dims == 128, KVQ_ERR_UNSUPPORTED,

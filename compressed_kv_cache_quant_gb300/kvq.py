@@ -18,7 +18,8 @@ import ctypes
 import torch
 
 from . import _abi
-from ._abi import BITS_E4M3, BLOCK_TOKENS, HEAD_DIM, K_GROUP_TOKENS, KvqError, Layout, Pool, Seqs, check, lib  # noqa: F401
+from ._abi import (BITS_E4M3, BLOCK_TOKENS, HEAD_DIM, K_GROUP_TOKENS, V_SYMMETRIC, KvqError, Layout, Pool,  # noqa: F401
+                   Seqs, check, lib)
 
 
 def _p(x):
@@ -69,7 +70,7 @@ class LayerCache:
                 self.kT = z((max_seqs, H, d, t_cap), torch.float16)
                 self.k_absmax = z((max_seqs, H, d), torch.float32)
         else:
-            R = d * bits // 8
+            R = d * (bits & 0xFF) // 8
             self.k_codes = z((num_blocks, H, P, R), torch.uint8)
             self.v_codes = z((num_blocks, H, P, R), torch.uint8)
             self.k_sz = z((num_blocks, H, d, 2), torch.float16)

@@ -73,6 +73,14 @@ extern "C" {
  * has it, no dequantization arithmetic]. */
 #define KVQ_BITS_E4M3         0xE4
 
+/* Or-ed into kvq_layout.bits of a 2-, 4- or 8-bit layer: V is quantized
+ * symmetrically [OnDevice §3.1: V INT4 symmetric, group quantization]: per token
+ * and V group, scale = max|x| / L with L = 2^(b-1) - 1, code = clamp(round(x /
+ * scale), -L, L) (fp32, round half to even), scale stored fp16.  The page layout
+ * is the asymmetric one with the code stored as code + L and the (scale, zero)
+ * pair as (scale16, fp16(-L * scale16)), so attention reads it unchanged. */
+#define KVQ_V_SYMMETRIC       0x100
+
 #define KVQ_HEAD_DIM          128
 #define KVQ_BLOCK_TOKENS      16
 #define KVQ_K_GROUP_TOKENS    64
@@ -93,7 +101,8 @@ typedef struct kvq_layout {
     int32_t n_q_heads;       /* H_q; a multiple of n_kv_heads, H_q / H_kv <= 8 */
     int32_t n_kv_heads;      /* H_kv; q head h reads kv head floor(h * H_kv / H_q) */
     int32_t block_tokens;    /* tokens per page; must be 16 [KVSurvey §一.1] */
-    int32_t bits;            /* 1, 2, 4, 8: quantized layer; 16: fp16 layer;
+    int32_t bits;            /* 1, 2, 4, 8: quantized layer (2, 4, 8 may carry
+                                KVQ_V_SYMMETRIC); 16: fp16 layer;
                                 KVQ_BITS_E4M3: FP8 E4M3 layer */
     int32_t k_group_tokens;  /* K quantization group along tokens; must be 64 [TailorKV §2.2] */
     int32_t v_group_dims;    /* V quantization group along head_dim: 32, 64 or 128 [OnDevice §3.1] */
