@@ -538,6 +538,18 @@ def classify_layer(P_heads, n_q, tau):
     return float(np.mean(P_heads)) / n_q > tau
 
 
+def classify_heads(P_heads, n_q, tau, n_kv_heads):
+    """[TailorKV §6: the layer-level strategy carried down to attention heads]
+    READING: the unit that is quantized or made sparse is a kv head's cache, so a
+    kv head is quantization-friendly when the dense-preference score averaged over
+    the q heads sharing it (ascending head order, fp64) and normalised by n_q
+    exceeds tau -- ``classify_layer`` applied to each group of q heads.  With one
+    kv head this is the layer rule.  Returns a list of bools, one per kv head."""
+    P = np.asarray(P_heads, dtype=np.float64)
+    G = P.shape[0] // n_kv_heads
+    return [classify_layer(P[g * G:(g + 1) * G], n_q, tau) for g in range(n_kv_heads)]
+
+
 # ---------------------------------------------------------------------------
 # a9: offload gather   [Meeting §4.2 double buffer; TailorKV §2.3, §3.1]
 # ---------------------------------------------------------------------------

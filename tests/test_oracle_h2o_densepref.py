@@ -177,3 +177,19 @@ def test_classify_layer_threshold():
     assert O.classify_layer([10.0, 8.0], 32, 0.2) is True      # mean 9 / 32 = 0.28
     assert O.classify_layer([5.0, 6.0], 32, 0.2) is False      # 0.17
     assert O.classify_layer([6.4, 6.4], 32, 0.2) is False      # equal: not above
+
+
+def test_classify_heads_per_kv_group():
+    """[TailorKV §6] per kv head: the group's mean P / n_q against tau (hand-worked):
+    groups (10, 8) -> 0.28 > 0.2 quantize; (5, 6) -> 0.17 sparse; (6.4, 6.4) -> 0.2, not above."""
+    P = [10.0, 8.0, 5.0, 6.0, 6.4, 6.4]
+    assert O.classify_heads(P, 32, 0.2, 3) == [True, False, False]
+
+
+def test_classify_heads_reduces_to_the_layer_rule():
+    rng = np.random.default_rng(9)
+    for _ in range(50):
+        P = rng.random(8) * 32
+        assert O.classify_heads(P, 32, 0.2, 1) == [O.classify_layer(P, 32, 0.2)]
+        # one q head per kv head: each head on its own
+        assert O.classify_heads(P, 32, 0.2, 8) == [p / 32 > 0.2 for p in P]
