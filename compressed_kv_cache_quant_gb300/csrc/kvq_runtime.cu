@@ -175,6 +175,25 @@ extern "C" int kvq_read_path_counters(void* ws, uint32_t* out, void* stream) {
     return KVQ_OK;
 }
 
+// ---------------------------------------------------------------- head-level classification
+
+extern "C" int kvq_classify_heads(const float* P, int32_t n_q_heads, int32_t n_kv_heads, int32_t n_q, double tau,
+                                  int32_t* dense) {
+    kvq_clear_error();
+    KVQ_REQUIRE(P && dense, KVQ_ERR_INVALID_ARG, "kvq_classify_heads: NULL P / dense");
+    KVQ_REQUIRE(n_kv_heads > 0 && n_q_heads > 0 && n_q_heads % n_kv_heads == 0 && n_q > 0, KVQ_ERR_INVALID_ARG,
+                "kvq_classify_heads: head counts / n_q");
+    const int G = n_q_heads / n_kv_heads;
+    int n_dense = 0;
+    for (int g = 0; g < n_kv_heads; ++g) {
+        double sum = 0.0;
+        for (int j = 0; j < G; ++j) sum += (double)P[g * G + j];  // ascending head order
+        dense[g] = (sum / G) / n_q > tau ? 1 : 0;
+        n_dense += dense[g];
+    }
+    return n_dense;
+}
+
 // ---------------------------------------------------------------- host page allocator
 
 struct kvq_allocator {

@@ -74,6 +74,7 @@ struct SXArgs {
     uint16_t* k16w;
     uint16_t* v16w;
     float* scores_out;       // optional copy of the scores [B][H_q][score_stride]
+    const int32_t* dense;    // [B][H_kv] (or NULL): non-zero = the kv head's q heads attend every token
 };
 
 constexpr int CAP_S = 1024;           // kept positions collected per CTA in the one-pass path
@@ -364,7 +365,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     const int chunk = chunk_of_dev(T);  // a multiple of 32: the chunk starts 16-byte aligned
     const int lo = min(T, rank * chunk), hi = min(T, lo + chunk);
     const int n = hi - lo;
-    const bool keep_all = (int64_t)T <= (int64_t)a.n_sink + a.window + k;
+    // a dense head (head-level classification: quantization-friendly) attends every token: no
+    // critical scores, no selection -- the same launch, dispatched by the head's class
+    const bool dense = a.dense != nullptr && a.dense[(int64_t)b * a.H + h / a.GQ] != 0;
+    const bool keep_all = dense || (int64_t)T <= (int64_t)a.n_sink + a.window + k;
     const int cand_lo = a.n_sink, cand_hi = T - a.window;
     const float* srow = a.scores + row * a.score_stride;
     // warp w owns the contiguous run [w_lo, w_hi) of the chunk in the ordered passes
@@ -445,10 +449,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         }
         __syncthreads();
         // ---- approximate scores a_t = sum over the channels, ascending, of q_c K[t][c] (fp32 from
-        // +0), their keys, and the local histogram of candidate keys
+        // +0), their keys, and the local histogram of candidate keys (a dense head has none)
         const uint16_t* kbase = a.kT + kvrow * D * a.t_cap;
         float* srow_out = a.scores_out != nullptr ? a.scores_out + row * a.score_stride : nullptr;
-        if (a.n_crit <= 8) {
+        if (dense) {
+        } else if (a.n_crit <= 8) {
             // one 16-byte load per channel and 8 positions; a channel's registers are refilled
             // with the next group's load as soon as they are consumed, so loads stay in flight
             // channel row offsets: c * t_cap < 128 * 360448 fits in 32 bits
@@ -1168,13 +1173,12 @@ extern "C" int kv_select_sparse_attn(const kvq_layout* L, const kvq_pool* P, con
 
 extern "C" size_t kv_sparse_layer_decode_ws(void) { return sizeof(KvqWsHeader); }
 
-extern "C" int kv_sparse_layer_decode(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S,
-                                      const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q, int32_t n_crit,
-                                      int32_t k_fixed, double ratio, int32_t n_sink, int32_t window, float* scores,
-                                      int64_t score_stride, int32_t* sel, int32_t sel_cap, int32_t* sel_count,
-                                      float* out, void* ws, size_t ws_bytes, void* stream) {
+static int layer_decode(const char* fn, const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S,
+                        const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q, int32_t n_crit,
+                        int32_t k_fixed, double ratio, int32_t n_sink, int32_t window, float* scores,
+                        int64_t score_stride, int32_t* sel, int32_t sel_cap, int32_t* sel_count, const int32_t* dense,
+                        float* out, void* ws, size_t ws_bytes, void* stream) {
     kvq_clear_error();
-    const char* fn = "kv_sparse_layer_decode";
     int st = kvq_check_layout(L, fn, true);
     if (st) return st;
     st = kvq_check_seqs(S, fn);
@@ -1233,7 +1237,32 @@ extern "C" int kv_sparse_layer_decode(const kvq_layout* L, const kvq_pool* P, co
     a.k16w = P->k16;
     a.v16w = P->v16;
     a.scores_out = scores;
+    a.dense = dense;
     st = launch(a, S->batch, kvq_stream(stream));
     if (st) return st;
     return kvq_launch_status(fn);
+}
+
+extern "C" int kv_sparse_layer_decode(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S,
+                                      const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q, int32_t n_crit,
+                                      int32_t k_fixed, double ratio, int32_t n_sink, int32_t window, float* scores,
+                                      int64_t score_stride, int32_t* sel, int32_t sel_cap, int32_t* sel_count,
+                                      float* out, void* ws, size_t ws_bytes, void* stream) {
+    return layer_decode("kv_sparse_layer_decode", L, P, S, k_new, v_new, q, n_crit, k_fixed, ratio, n_sink, window,
+                        scores, score_stride, sel, sel_cap, sel_count, nullptr, out, ws, ws_bytes, stream);
+}
+
+extern "C" size_t kv_mixed_layer_decode_ws(void) { return sizeof(KvqWsHeader); }
+
+extern "C" int kv_mixed_layer_decode(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S,
+                                     const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q, int32_t n_crit,
+                                     int32_t k_fixed, double ratio, int32_t n_sink, int32_t window,
+                                     const int32_t* dense, int32_t* sel, int32_t sel_cap, int32_t* sel_count,
+                                     float* out, void* ws, size_t ws_bytes, void* stream) {
+    if (dense == nullptr) {
+        kvq_clear_error();
+        return kvq_fail(KVQ_ERR_INVALID_ARG, "kv_mixed_layer_decode: NULL dense");
+    }
+    return layer_decode("kv_mixed_layer_decode", L, P, S, k_new, v_new, q, n_crit, k_fixed, ratio, n_sink, window,
+                        nullptr, 0, sel, sel_cap, sel_count, dense, out, ws, ws_bytes, stream);
 }

@@ -247,6 +247,29 @@ def kv_sparse_layer_decode(cache, seqs, k_new, v_new, q, n_crit, k_fixed, ratio,
                                               _p(out), ws.ptr, ws.nbytes, _s(stream)), "kv_sparse_layer_decode")
 
 
+def kv_mixed_layer_decode_ws():
+    return lib().kv_mixed_layer_decode_ws()
+
+
+def kv_mixed_layer_decode(cache, seqs, k_new, v_new, q, n_crit, k_fixed, ratio, n_sink, window, dense, out, ws,
+                          sel=None, sel_count=None, stream=None):
+    sel_cap = int(sel.shape[-1]) if sel is not None else 0
+    return check(lib().kv_mixed_layer_decode(_ref(cache.layout), _ref(cache), _ref(seqs), _p(k_new), _p(v_new),
+                                             _p(q), int(n_crit), int(k_fixed), float(ratio), int(n_sink), int(window),
+                                             _p(dense), _p(sel), sel_cap, _p(sel_count), _p(out), ws.ptr, ws.nbytes,
+                                             _s(stream)), "kv_mixed_layer_decode")
+
+
+def kvq_classify_heads(P, n_q_heads, n_kv_heads, n_q, tau):
+    """Per kv head: 1 if its q heads' mean dense-preference score over n_q exceeds tau."""
+    Pa = (ctypes.c_float * n_q_heads)(*[float(x) for x in P])
+    out = (ctypes.c_int32 * n_kv_heads)()
+    r = lib().kvq_classify_heads(Pa, int(n_q_heads), int(n_kv_heads), int(n_q), float(tau), out)
+    if r < 0:
+        raise KvqError(r, "kvq_classify_heads", _abi.last_error())
+    return [int(out[i]) for i in range(n_kv_heads)]
+
+
 def kv_topk_select_ws():
     return lib().kv_topk_select_ws()
 

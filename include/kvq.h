@@ -443,6 +443,36 @@ int kv_sparse_layer_decode(const kvq_layout* layout, const kvq_pool* pool, const
 size_t kv_sparse_layer_decode_ws(void);
 
 /* ------------------------------------------------------------------------
+ * kv_mixed_layer_decode -- kv_sparse_layer_decode for a layer whose heads were
+ * classified one by one [TailorKV §6: the layer-level strategy carried down to
+ * attention heads; §2.1 dense-preference score]: in the same launch every
+ * (sequence, q head) is dispatched by its kv head's class, dense[b][g] (device
+ * int32 [batch][H_kv], e.g. from kvq_classify_heads): non-zero -> the head
+ * attends every cached token exactly (no critical scores, no selection; a
+ * `sel` copy lists every token); zero -> the sparse path of
+ * kv_sparse_layer_decode (critical scores, top-K with sinks and window,
+ * attention over the selection).  The newest token is appended for every kv
+ * head.  Other arguments as kv_sparse_layer_decode (no score copy).
+ * ws: kv_mixed_layer_decode_ws() bytes.
+ * ---------------------------------------------------------------------- */
+int kv_mixed_layer_decode(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                          const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q, int32_t n_crit,
+                          int32_t k_fixed, double ratio, int32_t n_sink, int32_t window,
+                          const int32_t* dense, int32_t* sel, int32_t sel_cap, int32_t* sel_count,
+                          float* out, void* ws, size_t ws_bytes, void* stream);
+size_t kv_mixed_layer_decode_ws(void);
+
+/* Head-level classification [TailorKV §6, §2.1], host code: kv head g (of
+ * n_kv_heads; its q heads g*G .. g*G+G-1, G = n_q_heads / n_kv_heads) is dense
+ * (quantization-friendly) when (sum over its q heads, ascending, of P[h]) / G /
+ * n_q > tau, in double.  P: host fp32 [n_q_heads] dense-preference scores
+ * (kv_dense_pref_score of one sequence); dense: host int32 [n_kv_heads] out
+ * (1 dense, 0 sparse).  Returns the number of dense kv heads, or a negative
+ * error.  With one kv head this is the layer rule (mean_h P_h / n_q > tau). */
+int kvq_classify_heads(const float* P, int32_t n_q_heads, int32_t n_kv_heads, int32_t n_q, double tau,
+                       int32_t* dense);
+
+/* ------------------------------------------------------------------------
  * a7: kv_h2o_accumulate -- H2O heavy-hitter bookkeeping [KVSurvey §三.2, §三.1].
  *
  * Per (sequence b, kv head g) a retained list (unordered) of token positions

@@ -159,3 +159,18 @@ def test_code_layout_is_a_packing(bits):
             if tok % 2 == 0:
                 assert v_code_pos(tok + 1, d, bits) == (w, b + 16)
     assert len(seen) == 16 * 128 * bits
+
+
+def test_classify_heads_matches_the_oracle(lib):
+    """Head-level classification (TailorKV section 6) is host code: it equals the oracle's rule."""
+    import numpy as np
+
+    from oracle import kvq_oracle as O
+    rng = np.random.default_rng(4)
+    for Hq, Hkv in ((8, 2), (32, 8), (4, 4), (8, 1)):
+        for _ in range(20):
+            P = (rng.random(Hq) * 32).astype(np.float32)
+            got = kvq.kvq_classify_heads(P.tolist(), Hq, Hkv, 32, 0.2)
+            assert got == [int(x) for x in O.classify_heads(P.astype(np.float64), 32, 0.2, Hkv)]
+    assert kvq.kvq_classify_heads([8.0, 8.0], 2, 1, 32, 0.25) == [0]      # equal: not above
+    assert lib.kvq_classify_heads(None, 2, 1, 32, 0.2, None) == _abi.KVQ_ERR_INVALID_ARG
