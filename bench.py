@@ -983,6 +983,53 @@ def row_fp8(torch, np, kvq, synth, O, device, stream, hbm, T=131072):
                              "sample": "one q head over one kv head's E4M3 cache, numpy fp64"}}
 
 
+def row_mixed(torch, np, kvq, synth, O, device, stream, hbm, T=131072):
+    """f2 + f4 head-level: one Llama-3.1-8B-shaped layer (32 q / 8 kv heads, T = 131072) whose kv
+    heads were classified one by one; 2 of the 8 dense (their q heads attend every token), 6 sparse
+    (critical scores + top-K + attention), all in one launch."""
+    Hq, Hkv, ns, w = 32, 8, 4, 128
+    dense = [1, 0, 0, 0, 0, 1, 0, 0]
+    seed = synth.BASE_SEED + 9
+    n_pages = -(-(T + 64) // 16)
+    alloc = kvq.Allocator(n_pages, seed=29)
+    seqs = kvq.Batch(torch.tensor([alloc.alloc(n_pages)], dtype=torch.int32, device=device),
+                     torch.tensor([T], dtype=torch.int32, device=device), 16 * n_pages)
+    cache = kvq.LayerCache(Hq, Hkv, 16, n_pages, 1, t_cap=16 * n_pages, device=device)
+    K, V = synth.kv_rows(T, Hkv, synth.mix(seed, 0), device=device)
+    kvq.kv_quant_pack(cache, seqs, 0, 0, T, K, V)
+    k_new, v_new = K[-1:].clone(), V[-1:].clone()
+    K0, V0 = K[:, 0].cpu().numpy(), V[:, 0].cpu().numpy()
+    del K, V
+    q = synth.normal((1, Hq, D), synth.mix(seed, 1), device)
+    out = torch.empty((1, Hq, D), device=device)
+    dn = torch.tensor([dense], dtype=torch.int32, device=device)
+    wk = kvq.Workspace(kvq.kv_mixed_layer_decode_ws())
+    sh = stream.cuda_stream
+    g = _capture(torch, lambda: kvq.kv_mixed_layer_decode(cache, seqs, k_new, v_new, q, N_CRIT, -1, RATIO, ns, w, dn,
+                                                          out, wk, stream=sh), stream)
+    ms, reps, clk = _timed(torch, g.replay, stream, min_ms=150.0)
+    kvq.kvq_check(wk, stream=sh)
+    n_d = sum(dense) * (Hq // Hkv)
+    sel = ns + w + math.floor(RATIO * T)
+    nbytes = n_d * T * 2 * D * 2 + (Hq - n_d) * (N_CRIT * T * 2 + sel * 2 * D * 2)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del cache, g
+    q0 = q[0, 0].cpu().numpy()
+    t_d = _wall(lambda: O.sparse_attn(q0, K0, V0, np.arange(T)))
+
+    def one_sparse():
+        C = O.critical_channels(q0, O.key_absmax(K0), N_CRIT)
+        O.sparse_attn(q0, K0, V0, O.topk_select(O.critical_scores(q0, K0, C), O.ratio_k(T, RATIO), ns, w))
+    t_s = _wall(one_sparse)
+    return {"config": f"32 q / 8 kv heads, T = {T}: kv heads {[i for i, x in enumerate(dense) if x]} classified dense "
+                      "(their 8 q heads attend all tokens), the other 24 q heads sparse (8 critical channels, top-K = "
+                      "floor(0.03 T) + 4 sinks + 128 window); one launch",
+            "value": gbs, "unit": "GB/s", "us_per_launch": ms * 1e3, "bytes_per_launch": nbytes, "calls": reps,
+            "roofline": hbm(gbs), "clocks": clk,
+            "cpu_baseline": {"value": 1.0 / (n_d * t_d + (Hq - n_d) * t_s), "unit": "layers/s", "cores": 1,
+                             "kind": "oracle", "sample": "one dense and one sparse q head, numpy, scaled to 8 + 24"}}
+
+
 def row_tiny(torch, np, kvq, synth, O, device, stream):
     """a4, a5, a6, a8 at the tiny single-layer configuration: 8 q / 2 kv heads, T = 4096
     (latency-bound: microseconds, no roofline target)."""
@@ -1047,6 +1094,7 @@ ROWS = [
     ("f1 kv_block_select + kv_sparse_attn (block-sparse layer)", row_block),
     ("f1 kv_group_critical_score + shared top-K + shared-list attention (GQA-shared selection)", row_group),
     ("f4 kv_decode_attn_quant on an FP8 E4M3 layer", row_fp8),
+    ("f2 kv_mixed_layer_decode (head-level classes, one launch)", row_mixed),
     ("tiny", row_tiny),
 ]
 
