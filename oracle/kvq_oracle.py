@@ -170,9 +170,48 @@ def pack_v_sym(v16, bits, group_dims):
                 symmetric=True)
 
 
+def outlier_channels(k16, n_out):
+    """[Meeting §8.2] outlier channels of one (sequence, kv head): the channels of
+    largest variance.  READING (the page calibrates offline on 1000 samples; here
+    the prompt itself is the calibration set, as the on-device article's online
+    calibration from prefill statistics, §3.2): Var_c = (S2 - S1^2 / T) / T in fp64
+    from the exact sums S1 = sum_t K_t,c and S2 = sum_t K_t,c^2 of the fp16 values
+    (exact in fp64 for T <= 2^24); the n_out largest, ties -> lower channel,
+    returned ascending.  The page's "top 0.5 %" of a 128-channel head is
+    n_out = ceil(0.005 * 128) = 1."""
+    K = np.asarray(k16, dtype=np.float16).astype(np.float64)
+    T = K.shape[0]
+    s1 = K.sum(axis=0)
+    s2 = (K * K).sum(axis=0)
+    var = (s2 - s1 * s1 / T) / T
+    order = np.lexsort((np.arange(K.shape[1]), -var))
+    return np.sort(order[:n_out])
+
+
+def pack_k_outlier(k16, bits, out_ch, group_tokens=K_GROUP_TOKENS):
+    """[Meeting §8.2] keys with outlier channels isolated: the main cache is
+    ``pack_k`` with the outlier channels' codes, scale and zero set to 0 (they
+    contribute nothing there); the outlier channels of the packed tokens are kept
+    as fp16 in a side cache (``outlier_values`` [n_packed][n_out]).  READING: the
+    page's main cache is "INT4 ... symmetric ... scale, zero_point" (a
+    contradiction); the main cache here is the K quantizer of this library
+    (asymmetric, per channel), unchanged for the normal channels."""
+    pk = pack_k(k16, bits, group_tokens)
+    out_ch = np.asarray(out_ch, dtype=np.int64)
+    n = pk["n_packed"]
+    pk["codes"][:, out_ch] = 0
+    pk["scale16"][:, out_ch] = 0
+    pk["zero16"][:, out_ch] = 0
+    pk["scale32"][:, out_ch] = 0
+    pk["outliers"] = out_ch
+    pk["outlier_values"] = np.asarray(k16, dtype=np.float16)[:n][:, out_ch].copy()
+    return pk
+
+
 def dequant_k(pk):
     """fp64 keys as the quantized cache represents them: zero + code * scale
-    for packed tokens (stored fp16 scale/zero), fp16 values for the tail."""
+    for packed tokens (stored fp16 scale/zero), fp16 values for the tail and,
+    with isolated outlier channels (``pack_k_outlier``), for those channels."""
     n_packed = pk["n_packed"]
     gt = pk["group_tokens"]
     d = pk["tail"].shape[1]
@@ -181,6 +220,8 @@ def dequant_k(pk):
         grp = np.arange(n_packed) // gt
         out[:n_packed] = (pk["zero16"].astype(np.float64)[grp]
                           + pk["codes"].astype(np.float64) * pk["scale16"].astype(np.float64)[grp])
+        if "outliers" in pk:
+            out[:n_packed, pk["outliers"]] = pk["outlier_values"].astype(np.float64)
     out[n_packed:] = pk["tail"].astype(np.float64)
     return out
 

@@ -237,3 +237,69 @@ def test_symmetric_dequant_and_attention():
     j = np.arange(128) // 32
     assert np.array_equal(vh, pv["codes"] * pv["scale16"].astype(np.float64)[:, j])
     assert np.max(np.abs(vh - V.astype(np.float64))) <= np.max(pv["scale32"]) * 0.51 + 1e-3
+
+
+# ---- outlier-channel isolation   [meeting article §8.2]
+
+def test_outlier_channels_find_planted_channels_and_break_ties_low():
+    rng = np.random.default_rng(90)
+    K = rng.standard_normal((1000, 128)).astype(np.float32)
+    K[:, [7, 70, 99]] *= [10, 20, 5]
+    K = K.astype(np.float16)
+    assert O.outlier_channels(K, 1).tolist() == [70]
+    assert O.outlier_channels(K, 3).tolist() == [7, 70, 99]
+    # identical channels: the lower one first
+    K2 = np.zeros((64, 128), np.float16)
+    K2[::2, 3] = 1
+    K2[::2, 9] = 1
+    assert O.outlier_channels(K2, 1).tolist() == [3]
+
+
+def test_outlier_variance_brute_force():
+    """Small integer keys: the chosen channels are the n largest exact variances (fractions), ties
+    low -- except where two exact variances at the boundary lie within fp64 rounding of each
+    other (1e-12 relative), where the fp64 definition may order them either way."""
+    from fractions import Fraction
+    rng = np.random.default_rng(91)
+    for _ in range(10):
+        T, d, n = int(rng.integers(2, 40)), 16, int(rng.integers(1, 5))
+        K = rng.integers(-4, 5, size=(T, d)).astype(np.float16)
+        var = []
+        for c in range(d):
+            xs = [Fraction(int(x)) for x in K[:, c]]
+            m = sum(xs) / T
+            var.append(sum((x - m) ** 2 for x in xs) / T)
+        want = sorted(sorted(range(d), key=lambda c: (-var[c], c))[:n])
+        got = O.outlier_channels(K, n).tolist()
+        for a in set(got) ^ set(want):          # exchanged at the boundary: near-equal variances only
+            b = sorted(range(d), key=lambda c: (-var[c], c))[n - 1 if a not in want else n]
+            assert abs(float(var[a]) - float(var[b])) <= 1e-12 * max(1.0, abs(float(var[b]))), (got, want)
+
+
+def test_pack_k_outlier_keeps_outliers_exact_and_the_rest_unchanged():
+    rng = np.random.default_rng(92)
+    K = (rng.standard_normal((64 * 5 + 9, 128)) * np.where(rng.random(128) < 0.05, 10, 1)).astype(np.float16)
+    ch = O.outlier_channels(K, 4)
+    po, pk = O.pack_k_outlier(K, 4, ch), O.pack_k(K, 4)
+    normal = np.setdiff1d(np.arange(128), ch)
+    assert np.array_equal(po["codes"][:, normal], pk["codes"][:, normal])
+    assert np.array_equal(po["scale16"][:, normal].view(np.uint16), pk["scale16"][:, normal].view(np.uint16))
+    dq, dk = O.dequant_k(po), O.dequant_k(pk)
+    assert np.array_equal(dq[:, ch], K[:, ch].astype(np.float64))          # outliers exact (packed and tail)
+    assert np.array_equal(dq[:, normal], dk[:, normal])
+    assert np.all(po["codes"][:, ch] == 0) and np.all(po["scale16"][:, ch] == 0)
+    # no outliers: the plain pack
+    pe = O.pack_k_outlier(K, 4, [])
+    assert np.array_equal(O.dequant_k(pe), dk)
+
+
+def test_all_channels_outliers_is_attention_over_fp16_keys():
+    rng = np.random.default_rng(93)
+    K = rng.standard_normal((200, 128)).astype(np.float16)
+    V = rng.standard_normal((200, 128)).astype(np.float16)
+    q = rng.standard_normal(128).astype(np.float16)
+    po = O.pack_k_outlier(K, 1, np.arange(128))
+    pv = O.pack_v(V, 1, 64)
+    o = O.decode_attn_quant(q[None], [po], [pv])[0]
+    ref, _ = O.softmax_attention(q, K, O.dequant_v(pv))
+    assert np.allclose(o, ref, rtol=0, atol=1e-12)
