@@ -170,21 +170,39 @@ def pack_v_sym(v16, bits, group_dims):
                 symmetric=True)
 
 
+def channel_variance(k16):
+    """[Meeting §8.2] per-channel variance of fp16 keys [T][d], order-independent:
+    every fp16 value is an integer multiple of 2^-24, so the sums S1 = sum_t K_t,c
+    (in units of 2^-24) and S2 = sum_t K_t,c^2 (in units of 2^-48) are formed
+    exactly as integers, each rounded once to fp64 (round to nearest even), and
+    Var_c = (S2 - S1^2 / T) / T follows in fp64 with one rounding per operation.
+    S2 is summed in three int64 parts of the 40-bit magnitude u = a 2^20 + b
+    (u^2 = a^2 2^40 + 2ab 2^20 + b^2), exact for T <= 2^22."""
+    K = np.asarray(k16, dtype=np.float16)
+    T = K.shape[0]
+    assert T <= 1 << 22
+    x = (K.astype(np.float64) * 2.0 ** 24).astype(np.int64)       # exact: |x| < 2^40
+    s1 = x.sum(axis=0)
+    u = np.abs(x)
+    a, b = u >> 20, u & ((1 << 20) - 1)
+    p2, p1, p0 = (a * a).sum(axis=0), (2 * a * b).sum(axis=0), (b * b).sum(axis=0)
+    var = np.empty(K.shape[1], dtype=np.float64)
+    for c in range(K.shape[1]):
+        S1 = float(int(s1[c])) * 2.0 ** -24                          # Python int -> float rounds to nearest even
+        S2 = float((int(p2[c]) << 40) + (int(p1[c]) << 20) + int(p0[c])) * 2.0 ** -48
+        var[c] = (S2 - S1 * S1 / T) / T if T else 0.0
+    return var
+
+
 def outlier_channels(k16, n_out):
     """[Meeting §8.2] outlier channels of one (sequence, kv head): the channels of
     largest variance.  READING (the page calibrates offline on 1000 samples; here
     the prompt itself is the calibration set, as the on-device article's online
-    calibration from prefill statistics, §3.2): Var_c = (S2 - S1^2 / T) / T in fp64
-    from the exact sums S1 = sum_t K_t,c and S2 = sum_t K_t,c^2 of the fp16 values
-    (exact in fp64 for T <= 2^24); the n_out largest, ties -> lower channel,
-    returned ascending.  The page's "top 0.5 %" of a 128-channel head is
-    n_out = ceil(0.005 * 128) = 1."""
-    K = np.asarray(k16, dtype=np.float16).astype(np.float64)
-    T = K.shape[0]
-    s1 = K.sum(axis=0)
-    s2 = (K * K).sum(axis=0)
-    var = (s2 - s1 * s1 / T) / T
-    order = np.lexsort((np.arange(K.shape[1]), -var))
+    calibration from prefill statistics, §3.2): Var_c from ``channel_variance``;
+    the n_out largest, ties -> lower channel, returned ascending.  The page's
+    "top 0.5 %" of a 128-channel head is n_out = ceil(0.005 * 128) = 1."""
+    var = channel_variance(k16)
+    order = np.lexsort((np.arange(var.shape[0]), -var))
     return np.sort(order[:n_out])
 
 

@@ -276,6 +276,31 @@ def test_outlier_variance_brute_force():
             assert abs(float(var[a]) - float(var[b])) <= 1e-12 * max(1.0, abs(float(var[b]))), (got, want)
 
 
+def test_channel_variance_exact_sums_order_independent_and_near_exact():
+    """The sums are exact, so any token order gives the same bits (a plain fp64 running sum of
+    these squares does not: values near 2^-14 and near 2^8 need more than 53 bits together); and
+    the result lies within a few roundings of the exact (fraction) variance, mean of the order of
+    the spread here so the subtraction does not cancel."""
+    from fractions import Fraction
+    rng = np.random.default_rng(94)
+    T = 3000
+    K = (rng.standard_normal((T, 8)) * np.array([1e-4, 1e-3, 1, 30, 200, 1, 5e-4, 2])).astype(np.float16)
+    K[::7, 0] = np.float16(300.0)                  # tiny and large values in one channel
+    v = O.channel_variance(K)
+    perm = rng.permutation(T)
+    assert np.array_equal(O.channel_variance(K[perm]).view(np.uint64), v.view(np.uint64))
+    assert np.array_equal(O.channel_variance(K[::-1]).view(np.uint64), v.view(np.uint64))
+    for c in range(8):
+        xs = [Fraction(float(x)) for x in K[:, c]]
+        m = sum(xs) / T
+        exact = sum((x - m) ** 2 for x in xs) / T
+        assert abs(v[c] - float(exact)) <= 1e-13 * float(exact), c
+    # constant channel: zero variance; a single token: zero
+    Kc = np.full((100, 4), np.float16(3.5))
+    assert np.all(O.channel_variance(Kc) == 0.0)
+    assert np.all(O.channel_variance(K[:1]) == 0.0)
+
+
 def test_pack_k_outlier_keeps_outliers_exact_and_the_rest_unchanged():
     rng = np.random.default_rng(92)
     K = (rng.standard_normal((64 * 5 + 9, 128)) * np.where(rng.random(128) < 0.05, 10, 1)).astype(np.float16)
