@@ -659,6 +659,77 @@ def row_int4(torch, np, kvq, synth, O, device, stream, hbm):
                              "sample": f"one (sequence, head) of {lens[0]} tokens, numpy fp64"}}
 
 
+def row_outlier(torch, np, kvq, synth, O, device, stream, hbm):
+    """f3 kv_decode_attn_quant_outlier: the INT4 serving batch shape (16 sequences, lengths
+    U[4096, 32768], 32 heads MHA, K 4-bit g64, V 4-bit G32; no shared prefix, since the outlier
+    channels are chosen per sequence) with the top-0.5 % key channel of every (sequence, head)
+    isolated in fp16 (n_out = ceil(0.005 * 128) = 1), chosen from the prompt; a step is 32
+    layers.  The plain attention over the same main caches is timed beside it (the fp16 outlier
+    term is then missing: the cost of the isolation, not a second answer)."""
+    B, H, L, n_c, n_out = 16, 32, 32, 4, 1
+    seed = synth.BASE_SEED + 2
+    lens = [int(x) for x in synth.lengths_uniform(B, 4096, 32768, seed)]
+    pages = [-(-T // 16) for T in lens]
+    alloc = kvq.Allocator(sum(pages) + 4, seed=7)
+    bt = np.full((B, max(pages)), -1, dtype=np.int32)
+    for b in range(B):
+        bt[b, :pages[b]] = alloc.alloc(pages[b])
+    seqs = kvq.Batch(torch.from_numpy(bt).to(device), torch.tensor(lens, dtype=torch.int32, device=device), max(lens))
+    caches, chs, kos = [], [], []
+    wc = kvq.Workspace(kvq.kv_outlier_channels_ws(kvq.make_layout(H, H, 4, 32)))
+    t_iso = 0.0
+    for c in range(n_c):
+        cache = kvq.LayerCache(H, H, 4, sum(pages) + 4, B, v_group_dims=32, device=device)
+        och = torch.zeros((B, H, n_out), dtype=torch.int32, device=device)
+        k_out = torch.zeros((sum(pages) + 4, H, 16, n_out), dtype=torch.float16, device=device)
+        for b, T in enumerate(lens):
+            K, V = synth.kv_rows(T, H, synth.mix(seed, 10 + b, c), device=device)
+            kvq.kv_quant_pack(cache, seqs, b, 0, T, K, V)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            kvq.kv_outlier_channels(cache, K, T, n_out, och[b], wc)
+            kvq.kv_outlier_isolate(cache, seqs, b, 0, T, K, n_out, och, k_out)
+            e1.record()
+            e1.synchronize()
+            t_iso += e0.elapsed_time(e1)
+            if c == 0 and b == 0:
+                k0, v0 = K[:, 0].cpu().numpy(), V[:, 0].cpu().numpy()
+            del K, V
+        caches.append(cache)
+        chs.append(och)
+        kos.append(k_out)
+    torch.cuda.synchronize()
+    q = synth.normal((L, B, H, D), synth.mix(seed, 99), device)
+    out = torch.empty((L, B, H, D), device=device)
+    ws = kvq.Workspace(kvq.kv_decode_attn_quant_ws(caches[0], seqs))
+    g = _capture(torch, lambda: [kvq.kv_decode_attn_quant_outlier(caches[l % n_c], seqs, q[l], n_out, chs[l % n_c],
+                                                                  kos[l % n_c], out[l], ws, stream=stream.cuda_stream)
+                                 for l in range(L)], stream)
+    ms, reps, clk = _timed(torch, g.replay, stream)
+    kvq.kvq_check(ws, stream=stream.cuda_stream)
+    gp = _capture(torch, lambda: [kvq.kv_decode_attn_quant(caches[l % n_c], seqs, q[l], out[l], ws,
+                                                          stream=stream.cuda_stream) for l in range(L)], stream)
+    ms_plain, _, _ = _timed(torch, gp.replay, stream)
+    tails = sum(T % 64 for T in lens) * H * D * 2
+    per_tok = 152 + 2 * n_out
+    unique = sum(lens) * H * per_tok + tails
+    gbs = L * unique / (ms * 1e-3) / 1e9
+    q0 = q[0, 0, :1].cpu().numpy()
+    del caches, kos, g, gp
+    ch0 = O.outlier_channels(k0, n_out)
+    t = _wall(lambda: O.decode_attn_quant(q0, [O.pack_k_outlier(k0, 4, ch0)], [O.pack_v(v0, 4, 32)]))
+    return {"config": f"INT4 serving batch with isolated outlier channels: 16 sequences, T ~ U[4096, 32768] "
+                      f"(sum {sum(lens)}), 32 heads MHA, K 4-bit g64 + {n_out} fp16 outlier channel per (sequence, "
+                      "head), V 4-bit G32, shuffled page ids; one step = 32 layers (4 distinct layer caches cycled)",
+            "value": 1e3 / ms, "unit": "steps/s", "ms_per_step": ms, "GBps": gbs,
+            "bytes_per_step": L * unique, "plain_attention_ms_per_step": ms_plain,
+            "isolation_overhead": ms / ms_plain - 1.0,
+            "prefill_channels_and_isolate_ms_per_layer": t_iso / n_c, "steps": reps,
+            "roofline": hbm(gbs), "clocks": clk,
+            "cpu_baseline": {"value": (lens[0] * per_tok) / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"one (sequence, head) of {lens[0]} tokens, numpy fp64"}}
+
+
 def row_h2o(torch, np, kvq, synth, O, device, stream, hbm, steps=256):
     """a2 + a6 + a7, the Llama-3-8B-shaped H2O eviction run: 8 sequences, 32 layers of 32 q / 8 kv
     heads, 32768-token prompts, budget 6553 = 4 sinks + 2048 window + 4501 heavy hitters; step 0
@@ -1094,6 +1165,7 @@ ROWS = [
     ("f1 kv_block_select + kv_sparse_attn (block-sparse layer)", row_block),
     ("f1 kv_group_critical_score + shared top-K + shared-list attention (GQA-shared selection)", row_group),
     ("f4 kv_decode_attn_quant on an FP8 E4M3 layer", row_fp8),
+    ("f3 kv_decode_attn_quant_outlier (isolated outlier key channels, INT4 batch)", row_outlier),
     ("f2 kv_mixed_layer_decode (head-level classes, one launch)", row_mixed),
     ("tiny", row_tiny),
 ]

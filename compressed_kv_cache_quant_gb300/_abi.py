@@ -72,6 +72,12 @@ PROTOTYPES = {
     "kv_decode_attn_quant_noalloc": (c_int, [PL, PP, PS, VP, VP, VP]),
     "kv_decode_attn_quant_noalloc_max_scratch": (c_size_t, []),
     "kv_decode_attn_quant_plan": (c_int, [PL, PS, c_int32, POINTER(c_int32), POINTER(c_int32)]),
+    "kv_outlier_channels": (c_int, [PL, VP, c_int64, c_int64, c_int32, VP, VP, VP, c_size_t, VP]),
+    "kv_outlier_channels_ws": (c_size_t, [PL]),
+    "kv_outlier_isolate": (c_int, [PL, PP, PS, c_int32, c_int64, c_int64, VP, c_int64, c_int32, VP, VP, VP]),
+    "kv_outlier_append": (c_int, [PL, PP, PS, c_int32, VP, VP, VP, c_size_t, VP]),
+    "kv_outlier_append_ws": (c_size_t, []),
+    "kv_decode_attn_quant_outlier": (c_int, [PL, PP, PS, VP, c_int32, VP, VP, VP, VP, c_size_t, VP]),
     "kv_critical_score": (c_int, [PL, PP, PS, VP, c_int32, VP, VP, c_int64, VP]),
     "kv_group_critical_score": (c_int, [PL, PP, PS, VP, c_int32, VP, VP, c_int64, VP]),
     "kv_topk_select": (c_int, [PS, c_int32, VP, c_int64, c_int32, c_double, c_int32, c_int32, VP, c_int32, VP,

@@ -22,6 +22,7 @@
 #include <algorithm>
 #include <map>
 #include <mutex>
+#include <type_traits>
 
 #include "kvq_internal.cuh"
 
@@ -60,6 +61,11 @@ struct QAttnArgs {
     KvqWsHeader* hdr;
     int32_t n_splits;
     int32_t cps;     // 64-token groups per split
+    // isolated outlier channels (the outlier form of the kernel only): fp16 keys of the packed
+    // tokens [num_blocks][H][16][n_out], the channels [batch][H][n_out]
+    const uint16_t* k_out = nullptr;
+    const int32_t* out_ch = nullptr;
+    int32_t n_out = 0;
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -194,6 +200,16 @@ struct QMSmem {
     } u;
 };
 
+// The outlier form adds, per warp and stage, the fp16 outlier keys of the group's 64 tokens
+// (token-major, n_out <= 8 per token)
+constexpr int MAX_OUT = 8;
+template <int BITS, int GQ, int NWARP = nwarp_of<BITS>()>
+struct QMSmemOut : QMSmem<BITS, GQ, NWARP> {
+    alignas(16) uint16_t ko[NWARP][2][KG * MAX_OUT];
+};
+template <int BITS, int GQ, bool OUT>
+using QMSmemOf = std::conditional_t<OUT, QMSmemOut<BITS, GQ>, QMSmem<BITS, GQ>>;
+
 // Issues the cp.async copies of group gi into st (one warp); pages past the sequence are
 // skipped (their tokens are masked), complete groups also bring their K rows and scales.
 // Lane i < 4: the block-table entry of page i of group gi (-1 past the sequence), loaded an
@@ -203,9 +219,9 @@ __device__ __forceinline__ int32_t group_page(const QAttnArgs& a, int b, int gi,
     return lane < 4 && lp < n_pages ? a.bt[(int64_t)b * a.max_blocks + lp] : -1;
 }
 
-template <int BITS, int NGV>
+template <int BITS, int NGV, bool OUT = false>
 __device__ __forceinline__ void stage_group(const QAttnArgs& a, GroupStage<BITS>& st, int b, int gk, int gi,
-                                            int n_full, int32_t pg, int lane) {
+                                            int n_full, int32_t pg, int lane, uint16_t* ko = nullptr) {
     if (lane < 4 && pg != -1 && (pg < 0 || pg >= a.num_blocks)) {
         kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, b);
         pg = 0;
@@ -232,14 +248,27 @@ __device__ __forceinline__ void stage_group(const QAttnArgs& a, GroupStage<BITS>
         if (c >= 4 * VCH || P < 0) continue;
         cp_async16(st.vsz + i * 16 * NGV + 4 * r, a.v_sz + ((int64_t)P * a.H + gk) * PG * NGV + 4 * r);
     }
+    if constexpr (OUT) {  // the packed tokens' outlier keys: 32 n_out bytes per page
+        const int nc = 2 * a.n_out;
+        if (packed)
+            for (int c = lane; c < 4 * nc; c += 32) {
+                const int i = c / nc, r = c % nc;
+                const int32_t P = i == 0 ? P0 : i == 1 ? P1 : i == 2 ? P2 : P3;
+                if (P < 0) continue;
+                cp_async16(ko + i * PG * a.n_out + 8 * r, a.k_out + ((int64_t)P * a.H + gk) * PG * a.n_out + 8 * r);
+            }
+    }
 }
 
-template <int BITS, int GQ, int NGV>  // NGV = 128 / v_group_dims V groups per token
+// OUT: the outlier form (isolated outlier channels of the keys, meeting article §8.2): their codes,
+// scales and zeros are 0 in the main cache, and their fp16 keys, staged beside the group's codes,
+// add sum_j q_(c_j) K_(t, c_j) to the packed tokens' scores.
+template <int BITS, int GQ, int NGV, bool OUT = false>  // NGV = 128 / v_group_dims V groups per token
 __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArgs a) {
     constexpr int NWARP = nwarp_of<BITS>(), NT = 32 * NWARP;
     static_assert(GQ <= 4, "at most four query heads per grid kv group");
     extern __shared__ __align__(16) unsigned char smraw[];
-    QMSmem<BITS, GQ>& S = *reinterpret_cast<QMSmem<BITS, GQ>*>(smraw);
+    QMSmemOf<BITS, GQ, OUT>& S = *reinterpret_cast<QMSmemOf<BITS, GQ, OUT>*>(smraw);
     __shared__ int is_last;
 
     const int split = blockIdx.x, gv = blockIdx.y, b = blockIdx.z;
@@ -278,13 +307,36 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
         for (int i = 0; i < 4; ++i) acc[mt][i] = 0.0f;
     float mrun = -INFINITY, lrun = 0.0f;
     const int hs = g8 >> 1;  // the head of this lane's score rows (slot g8 = 2 hs + hi/lo)
+    // outlier form: q of head q4 at the outlier channels (0 for absent heads and bad channels)
+    float oq[MAX_OUT];
+    if constexpr (OUT) {
+#pragma unroll
+        for (int j = 0; j < MAX_OUT; ++j) {
+            oq[j] = 0.0f;
+            if (j < a.n_out) {
+                const int c = a.out_ch[((int64_t)b * a.H + gk) * a.n_out + j];
+                if (c < 0 || c >= D)
+                    kvq_dev_flag(a.hdr, KVQ_DEV_BAD_INDEX, b);
+                else if (q4 < GQ)
+                    oq[j] = S.qs[q4][c] * (1.0f / (float)(1 << BITS));
+            }
+        }
+    }
+    auto ko_of = [&](int bf) -> uint16_t* {
+        if constexpr (OUT) return S.ko[warp][bf];
+        else return nullptr;
+    };
 
     int gi = g_begin + warp, buf = 0;
-    if (gi < g_end) stage_group<BITS, NGV>(a, S.u.st[warp][0], b, gk, gi, n_full, group_page(a, b, gi, n_pages, lane), lane);
+    if (gi < g_end)
+        stage_group<BITS, NGV, OUT>(a, S.u.st[warp][0], b, gk, gi, n_full, group_page(a, b, gi, n_pages, lane), lane,
+                                    ko_of(0));
     cp_commit();
     int32_t pg_next = group_page(a, b, gi + NWARP, n_pages, lane);
     for (; gi < g_end; gi += NWARP) {
-        if (gi + NWARP < g_end) stage_group<BITS, NGV>(a, S.u.st[warp][buf ^ 1], b, gk, gi + NWARP, n_full, pg_next, lane);
+        if (gi + NWARP < g_end)
+            stage_group<BITS, NGV, OUT>(a, S.u.st[warp][buf ^ 1], b, gk, gi + NWARP, n_full, pg_next, lane,
+                                        ko_of(buf ^ 1));
         cp_commit();
         pg_next = group_page(a, b, gi + 2 * NWARP, n_pages, lane);
         cp_wait<1>();
@@ -376,6 +428,22 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
             }
             sc[mt][0] = d[0] + d[1];
             sc[mt][1] = d[2] + d[3];
+        }
+        if constexpr (OUT) {  // the outlier channels of the packed tokens 16mt + g8 + 8e, exact fp16 keys
+            if (packed) {
+                const uint16_t* ko = S.ko[warp][buf];
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const uint16_t* kr = ko + (16 * mt + g8 + 8 * e) * a.n_out;
+                        float cr = 0.0f;
+#pragma unroll
+                        for (int j = 0; j < MAX_OUT; ++j)
+                            if (j < a.n_out) cr = fmaf(oq[j], kvq_h2f(kr[j]), cr);
+                        sc[mt][e] += cr;
+                    }
+            }
         }
 
         // ---- online softmax of head q4 (log2 domain) over the group's 64 tokens: eight per lane
@@ -918,24 +986,24 @@ size_t ws_layout(const kvq_layout* L, const kvq_seqs* S, const Plan& p, size_t* 
     return kvq_round_up(*off_cnt + units * sizeof(int32_t), 256);
 }
 
-template <int BITS, int GQ, int NGV>
+template <int BITS, int GQ, int NGV, bool OUT = false>
 int launch_one(dim3 grid, cudaStream_t s, const QAttnArgs& a) {
-    const int smem = (int)sizeof(QMSmem<BITS, GQ>);
-    static_assert(sizeof(QMSmem<BITS, 4>) <= 227 * 1024, "one CTA's stages fit in shared memory");
-    const int st = kvq_prepare_kernel((const void*)qmma_kernel<BITS, GQ, NGV>, smem);
+    const int smem = (int)sizeof(QMSmemOf<BITS, GQ, OUT>);
+    static_assert(sizeof(QMSmemOf<BITS, 4, OUT>) <= 227 * 1024, "one CTA's stages fit in shared memory");
+    const int st = kvq_prepare_kernel((const void*)qmma_kernel<BITS, GQ, NGV, OUT>, smem);
     if (st) return st;
     const cudaError_t e =
-        kvq_launch_pdl(qmma_kernel<BITS, GQ, NGV>, grid, dim3(32 * nwarp_of<BITS>()), (size_t)smem, s, a);
+        kvq_launch_pdl(qmma_kernel<BITS, GQ, NGV, OUT>, grid, dim3(32 * nwarp_of<BITS>()), (size_t)smem, s, a);
     if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant launch: %s", cudaGetErrorString(e));
     return KVQ_OK;
 }
 
-template <int BITS, int GQ>
+template <int BITS, int GQ, bool OUT = false>
 int launch_ngv(dim3 grid, cudaStream_t s, const QAttnArgs& a) {
     switch (a.G) {
-        case 128: return launch_one<BITS, GQ, 1>(grid, s, a);
-        case 64: return launch_one<BITS, GQ, 2>(grid, s, a);
-        default: return launch_one<BITS, GQ, 4>(grid, s, a);  // 32 (the only other size accepted)
+        case 128: return launch_one<BITS, GQ, 1, OUT>(grid, s, a);
+        case 64: return launch_one<BITS, GQ, 2, OUT>(grid, s, a);
+        default: return launch_one<BITS, GQ, 4, OUT>(grid, s, a);  // 32 (the only other size accepted)
     }
 }
 
@@ -961,14 +1029,14 @@ int launch_f8(int gq, dim3 grid, cudaStream_t s, QAttnArgs& a) {
 }
 
 // grid: (splits, kv heads, batch); widened here to the grid kv groups
-template <int BITS>
+template <int BITS, bool OUT = false>
 int launch_bits(int gq, dim3 grid, cudaStream_t s, QAttnArgs& a) {
     a.kv_div = kv_div_of(gq);
     grid.y *= a.kv_div;
     switch (grid_gq(gq)) {
-        case 1: return launch_ngv<BITS, 1>(grid, s, a);
-        case 2: return launch_ngv<BITS, 2>(grid, s, a);
-        default: return launch_ngv<BITS, 4>(grid, s, a);
+        case 1: return launch_ngv<BITS, 1, OUT>(grid, s, a);
+        case 2: return launch_ngv<BITS, 2, OUT>(grid, s, a);
+        default: return launch_ngv<BITS, 4, OUT>(grid, s, a);
     }
 }
 
@@ -1007,27 +1075,37 @@ extern "C" int kv_decode_attn_quant_plan(const kvq_layout* L, const kvq_seqs* S,
     return KVQ_OK;
 }
 
-extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
-                                    float* out, void* ws, size_t ws_bytes, void* stream) {
-    kvq_clear_error();
-    int st = kvq_check_layout(L, "kv_decode_attn_quant", true);
+// kv_decode_attn_quant and its outlier form; fn names the entry in messages.  k_out == NULL: the
+// plain form.
+static int decode_attn(const char* fn, const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
+                       int32_t n_out, const int32_t* out_ch, const uint16_t* k_out, float* out, void* ws,
+                       size_t ws_bytes, void* stream) {
+    int st = kvq_check_layout(L, fn, true);
     if (st) return st;
-    st = kvq_check_seqs(S, "kv_decode_attn_quant");
+    st = kvq_check_seqs(S, fn);
     if (st) return st;
-    KVQ_REQUIRE(kvq_code_bits(L) != 16, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: layer is not quantized (bits == 16)");
+    KVQ_REQUIRE(kvq_code_bits(L) != 16, KVQ_ERR_INVALID_ARG, "%s: layer is not quantized (bits == 16)", fn);
     KVQ_REQUIRE(P != nullptr && P->k_codes && P->v_codes &&
                     (kvq_code_bits(L) == KVQ_BITS_E4M3 || (P->k_sz && P->v_sz && P->k_tail)),
-                KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: quantized pool arrays missing");
+                KVQ_ERR_INVALID_ARG, "%s: quantized pool arrays missing", fn);
     KVQ_REQUIRE((((uintptr_t)P->k_codes | (uintptr_t)P->v_codes | (uintptr_t)P->k_sz | (uintptr_t)P->v_sz) & 15u) == 0,
-                KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: code and scale arrays must be 16-byte aligned");
-    KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: batch exceeds max_seqs");
+                KVQ_ERR_INVALID_ARG, "%s: code and scale arrays must be 16-byte aligned", fn);
+    KVQ_REQUIRE(S->batch <= P->max_seqs, KVQ_ERR_INVALID_ARG, "%s: batch exceeds max_seqs", fn);
+    if (k_out) {
+        const int cb = kvq_code_bits(L);
+        KVQ_REQUIRE(cb == 4 || cb == 8, KVQ_ERR_UNSUPPORTED, "%s: isolated outlier channels need 4- or 8-bit codes",
+                    fn);
+        KVQ_REQUIRE(n_out >= 1 && n_out <= MAX_OUT && out_ch, KVQ_ERR_INVALID_ARG,
+                    "%s: n_out %d not in [1, 8], or NULL out_ch", fn, n_out);
+        KVQ_REQUIRE(((uintptr_t)k_out & 15u) == 0, KVQ_ERR_INVALID_ARG, "%s: k_out must be 16-byte aligned", fn);
+    }
     size_t off_part, off_cnt;
     const Plan p = plan_splits(L, S, false);
     const size_t need = ws_layout(L, S, p, &off_part, &off_cnt);
-    st = kvq_check_ws(ws, ws_bytes, need, "kv_decode_attn_quant");
+    st = kvq_check_ws(ws, ws_bytes, need, fn);
     if (st) return st;
     if (S->batch == 0) return KVQ_OK;
-    KVQ_REQUIRE(q && out && S->block_table, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant: NULL q/out/block table");
+    KVQ_REQUIRE(q && out && S->block_table, KVQ_ERR_INVALID_ARG, "%s: NULL q/out/block table", fn);
     QAttnArgs a;
     a.k_codes = P->k_codes;
     a.v_codes = P->v_codes;
@@ -1048,18 +1126,40 @@ extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, cons
     a.hdr = static_cast<KvqWsHeader*>(ws);
     a.n_splits = p.n_splits;
     a.cps = p.cps;
+    a.k_out = k_out;
+    a.out_ch = out_ch;
+    a.n_out = k_out ? n_out : 0;
     const int gq = L->n_q_heads / L->n_kv_heads;
     dim3 grid(p.n_splits, L->n_kv_heads, S->batch);
     cudaStream_t s = kvq_stream(stream);
-    switch (kvq_code_bits(L)) {
-        case KVQ_BITS_E4M3: st = launch_f8(gq, grid, s, a); break;
-        case 1: st = launch_bits<1>(gq, grid, s, a); break;
-        case 2: st = launch_bits<2>(gq, grid, s, a); break;
-        case 4: st = launch_bits<4>(gq, grid, s, a); break;
-        default: st = launch_bits<8>(gq, grid, s, a); break;
+    if (k_out) {
+        st = kvq_code_bits(L) == 4 ? launch_bits<4, true>(gq, grid, s, a) : launch_bits<8, true>(gq, grid, s, a);
+    } else {
+        switch (kvq_code_bits(L)) {
+            case KVQ_BITS_E4M3: st = launch_f8(gq, grid, s, a); break;
+            case 1: st = launch_bits<1>(gq, grid, s, a); break;
+            case 2: st = launch_bits<2>(gq, grid, s, a); break;
+            case 4: st = launch_bits<4>(gq, grid, s, a); break;
+            default: st = launch_bits<8>(gq, grid, s, a); break;
+        }
     }
     if (st) return st;
-    return kvq_launch_status("kv_decode_attn_quant");
+    return kvq_launch_status(fn);
+}
+
+extern "C" int kv_decode_attn_quant(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
+                                    float* out, void* ws, size_t ws_bytes, void* stream) {
+    kvq_clear_error();
+    return decode_attn("kv_decode_attn_quant", L, P, S, q, 0, nullptr, nullptr, out, ws, ws_bytes, stream);
+}
+
+extern "C" int kv_decode_attn_quant_outlier(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S,
+                                            const uint16_t* q, int32_t n_out, const int32_t* out_ch,
+                                            const uint16_t* k_out, float* out, void* ws, size_t ws_bytes,
+                                            void* stream) {
+    kvq_clear_error();
+    KVQ_REQUIRE(k_out, KVQ_ERR_INVALID_ARG, "kv_decode_attn_quant_outlier: NULL k_out");
+    return decode_attn("kv_decode_attn_quant_outlier", L, P, S, q, n_out, out_ch, k_out, out, ws, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------- allocation-free variant

@@ -189,6 +189,44 @@ def kv_decode_attn_quant_plan(cache, seqs, noalloc=False):
     return n.value, g.value
 
 
+def _layout_of(x):
+    return x.layout if hasattr(x, "layout") else x
+
+
+def kv_outlier_channels_ws(layout):
+    """Workspace bytes of kv_outlier_channels (`layout`: a Layout or a cache)."""
+    return lib().kv_outlier_channels_ws(ctypes.byref(_layout_of(layout)))
+
+
+def kv_outlier_channels(layout, k, n_tokens, n_out, out_ch, ws, var=None, stride_t=None, stream=None):
+    """The n_out largest-variance key channels per kv head of k [n_tokens][H_kv][d] (fp16)
+    into out_ch [H_kv][n_out] (int32), optionally the variances into var [H_kv][d] (fp64)."""
+    st = stride_t if stride_t is not None else k.stride(0)
+    return check(lib().kv_outlier_channels(ctypes.byref(_layout_of(layout)), _p(k), n_tokens, st, n_out, _p(out_ch),
+                                           _p(var), ws.ptr, ws.nbytes, _s(stream)), "kv_outlier_channels")
+
+
+def kv_outlier_isolate(cache, seqs, seq, t_start, n_tokens, k, n_out, out_ch, k_out, stride_t=None, stream=None):
+    st = stride_t if stride_t is not None else k.stride(0)
+    return check(lib().kv_outlier_isolate(_ref(cache.layout), _ref(cache), _ref(seqs), seq, t_start, n_tokens, _p(k),
+                                          st, n_out, _p(out_ch), _p(k_out), _s(stream)), "kv_outlier_isolate")
+
+
+def kv_outlier_append_ws():
+    return lib().kv_outlier_append_ws()
+
+
+def kv_outlier_append(cache, seqs, n_out, out_ch, k_out, ws, stream=None):
+    return check(lib().kv_outlier_append(_ref(cache.layout), _ref(cache), _ref(seqs), n_out, _p(out_ch), _p(k_out),
+                                         ws.ptr, ws.nbytes, _s(stream)), "kv_outlier_append")
+
+
+def kv_decode_attn_quant_outlier(cache, seqs, q, n_out, out_ch, k_out, out, ws, stream=None):
+    return check(lib().kv_decode_attn_quant_outlier(_ref(cache.layout), _ref(cache), _ref(seqs), _p(q), n_out,
+                                                    _p(out_ch), _p(k_out), _p(out), ws.ptr, ws.nbytes, _s(stream)),
+                 "kv_decode_attn_quant_outlier")
+
+
 def kv_critical_score(cache, seqs, q, n_crit, crit, scores, score_stride=None, stream=None):
     if score_stride is None:
         score_stride = scores.shape[-1]

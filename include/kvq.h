@@ -282,6 +282,74 @@ int kv_decode_attn_quant_plan(const kvq_layout* layout, const kvq_seqs* seqs, in
                               int32_t* n_splits, int32_t* groups_per_split);
 
 /* ------------------------------------------------------------------------
+ * f3: outlier-channel isolation of the keys [Meeting §8.2: the channels of
+ * largest variance per layer and head kept in fp16 beside a quantized main
+ * cache, and a single fused attention kernel over both].
+ *
+ * Outlier channels are chosen per (sequence, kv head) from that sequence's
+ * prompt keys; the main cache is the layer's ordinary cache (kv_quant_pack /
+ * kv_page_append) in which those channels' codes, K scale and K zero are then
+ * set to 0, and their fp16 keys are kept in a side cache
+ *   k_out   [num_blocks][H_kv][16][n_out]  fp16, rows of packed tokens only
+ *           (tail tokens keep every channel in k_tail)
+ *   out_ch  [batch][H_kv][n_out]           int32, ascending channels of the
+ *           sequence in batch slot b
+ * 1 <= n_out <= 8; only 4- and 8-bit layers (the page's INT4 main cache, and
+ * 8 bits).  k_out rows and page rows follow the same block table.  V is not
+ * split.  An isolated cache must be attended with kv_decode_attn_quant_outlier
+ * (kv_decode_attn_quant would omit the outlier channels).
+ * ---------------------------------------------------------------------- */
+
+/* kv_outlier_channels: the n_out channels of largest variance per kv head of
+ * n_tokens fp16 keys k [n_tokens][H_kv][d] (device, `stride_t` elements
+ * between tokens, finite values).  Var_c = (S2 - S1^2/T)/T in fp64 from the
+ * exact sums S1 = sum K[t][c], S2 = sum K[t][c]^2 (integer arithmetic: fp16
+ * values are multiples of 2^-24), each rounded once to fp64; one rounding per
+ * operation after that.  Ties -> lower channel.  out_ch: device int32
+ * [H_kv][n_out], ascending.  var (optional, may be NULL): device fp64
+ * [H_kv][d].  n_tokens <= 2^22; n_tokens == 0 gives variance 0 and channels
+ * 0 .. n_out-1.  ws: kv_outlier_channels_ws(layout) bytes, zeroed before the
+ * first call; the call leaves it zeroed.  Errors: INVALID_ARG, CUDA. */
+int kv_outlier_channels(const kvq_layout* layout, const uint16_t* k, int64_t n_tokens, int64_t stride_t,
+                        int32_t n_out, int32_t* out_ch, double* var, void* ws, size_t ws_bytes,
+                        void* stream);
+size_t kv_outlier_channels_ws(const kvq_layout* layout);
+
+/* kv_outlier_isolate: after kv_quant_pack of tokens t_start .. t_start +
+ * n_tokens - 1 of sequence `seq` (the same k, stride_t), isolates the outlier
+ * channels out_ch[seq] of every complete 64-token group of that run: their
+ * fp16 keys into k_out, their codes in k_codes and their (scale, zero) in
+ * k_sz set to 0.  A final partial group stays in k_tail (all channels fp16)
+ * and is isolated by kv_outlier_append when it completes.  t_start must be a
+ * multiple of 64.  No workspace; device checks skip bad pages or channels
+ * without a status word.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+int kv_outlier_isolate(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                       int32_t seq, int64_t t_start, int64_t n_tokens, const uint16_t* k, int64_t stride_t,
+                       int32_t n_out, const int32_t* out_ch, uint16_t* k_out, void* stream);
+
+/* kv_outlier_append: after kv_page_append, for every sequence whose new token
+ * completed a 64-token K group (seq_lens[b] % 64 == 0), isolates the outlier
+ * channels of that group (keys read from k_tail).  Run it after every append
+ * of an isolated layer, before the next append.  ws: kv_outlier_append_ws()
+ * bytes (status word: bad page or channel). */
+int kv_outlier_append(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                      int32_t n_out, const int32_t* out_ch, uint16_t* k_out,
+                      void* ws, size_t ws_bytes, void* stream);
+size_t kv_outlier_append_ws(void);
+
+/* kv_decode_attn_quant_outlier: kv_decode_attn_quant over an isolated cache.
+ * Packed tokens' scores add sum_j q[c_j] * k_out[t][j] (fp16 products, exact
+ * in fp32, summed in fp32) to the main cache's score, inside the same kernel:
+ * the outlier keys of a 64-token group are staged into shared memory beside
+ * its codes.  k_out 16-byte aligned.  ws: kv_decode_attn_quant_ws(layout,
+ * seqs) bytes.  Errors as kv_decode_attn_quant; UNSUPPORTED for bits other
+ * than 4 and 8. */
+int kv_decode_attn_quant_outlier(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
+                                 const uint16_t* q, int32_t n_out, const int32_t* out_ch,
+                                 const uint16_t* k_out, float* out,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * a4: kv_critical_score -- approximate token scores from critical channels
  * [TailorKV §2.3]: s_c = |q_c| * max_t |K[t][c]| picks the n_crit channels
  * with the largest s_c (ties -> lower channel); then for every cached token
