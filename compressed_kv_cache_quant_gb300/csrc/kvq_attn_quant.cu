@@ -22,7 +22,6 @@
 #include <algorithm>
 #include <map>
 #include <mutex>
-#include <type_traits>
 
 #include "kvq_internal.cuh"
 
@@ -200,15 +199,13 @@ struct QMSmem {
     } u;
 };
 
-// The outlier form adds, per warp and stage, the fp16 outlier keys of the group's 64 tokens
-// (token-major, n_out <= 8 per token)
+// The outlier form adds, after QMSmem in dynamic shared memory, per warp and stage the fp16
+// outlier keys of the group's 64 tokens (token-major, n_out <= 8 per token): 128 n_out bytes each
 constexpr int MAX_OUT = 8;
-template <int BITS, int GQ, int NWARP = nwarp_of<BITS>()>
-struct QMSmemOut : QMSmem<BITS, GQ, NWARP> {
-    alignas(16) uint16_t ko[NWARP][2][KG * MAX_OUT];
-};
-template <int BITS, int GQ, bool OUT>
-using QMSmemOf = std::conditional_t<OUT, QMSmemOut<BITS, GQ>, QMSmem<BITS, GQ>>;
+template <int BITS>
+__host__ __device__ constexpr size_t ko_bytes(int n_out) {
+    return (size_t)nwarp_of<BITS>() * 2 * KG * n_out * sizeof(uint16_t);
+}
 
 // Issues the cp.async copies of group gi into st (one warp); pages past the sequence are
 // skipped (their tokens are masked), complete groups also bring their K rows and scales.
@@ -252,7 +249,7 @@ __device__ __forceinline__ void stage_group(const QAttnArgs& a, GroupStage<BITS>
         const int nc = 2 * a.n_out;
         if (packed)
             for (int c = lane; c < 4 * nc; c += 32) {
-                const int i = c / nc, r = c % nc;
+                const int i = (c >= nc) + (c >= 2 * nc) + (c >= 3 * nc), r = c - i * nc;
                 const int32_t P = i == 0 ? P0 : i == 1 ? P1 : i == 2 ? P2 : P3;
                 if (P < 0) continue;
                 cp_async16(ko + i * PG * a.n_out + 8 * r, a.k_out + ((int64_t)P * a.H + gk) * PG * a.n_out + 8 * r);
@@ -263,12 +260,15 @@ __device__ __forceinline__ void stage_group(const QAttnArgs& a, GroupStage<BITS>
 // OUT: the outlier form (isolated outlier channels of the keys, meeting article §8.2): their codes,
 // scales and zeros are 0 in the main cache, and their fp16 keys, staged beside the group's codes,
 // add sum_j q_(c_j) K_(t, c_j) to the packed tokens' scores.
+// (the 4-bit outlier form is held to 168 registers: three 2-warp CTAs' warps per SM sub-partition, so
+// that shared memory, not registers, limits it to five CTAs per SM as the plain form)
 template <int BITS, int GQ, int NGV, bool OUT = false>  // NGV = 128 / v_group_dims V groups per token
-__global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArgs a) {
+__global__ void __launch_bounds__(32 * nwarp_of<BITS>(), OUT && BITS == 4 ? 6 : 1) qmma_kernel(QAttnArgs a) {
     constexpr int NWARP = nwarp_of<BITS>(), NT = 32 * NWARP;
     static_assert(GQ <= 4, "at most four query heads per grid kv group");
     extern __shared__ __align__(16) unsigned char smraw[];
-    QMSmemOf<BITS, GQ, OUT>& S = *reinterpret_cast<QMSmemOf<BITS, GQ, OUT>*>(smraw);
+    QMSmem<BITS, GQ>& S = *reinterpret_cast<QMSmem<BITS, GQ>*>(smraw);
+    uint16_t* const ko_base = reinterpret_cast<uint16_t*>(smraw + sizeof(QMSmem<BITS, GQ>));  // OUT only
     __shared__ int is_last;
 
     const int split = blockIdx.x, gv = blockIdx.y, b = blockIdx.z;
@@ -307,25 +307,26 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
         for (int i = 0; i < 4; ++i) acc[mt][i] = 0.0f;
     float mrun = -INFINITY, lrun = 0.0f;
     const int hs = g8 >> 1;  // the head of this lane's score rows (slot g8 = 2 hs + hi/lo)
-    // outlier form: q of head q4 at the outlier channels (0 for absent heads and bad channels)
-    float oq[MAX_OUT];
+    // outlier form: the score product gets one more k-step per m-tile whose k slots are the
+    // outlier channels j < n_out (k = 2 q4, 2 q4 + 1 in this lane's registers): B column 2h holds
+    // q of head h at channel c_j (fp16, exact), A the staged fp16 outlier keys of the tokens
+    uint32_t ob0 = 0u;
+    bool has0 = false, has1 = false;
     if constexpr (OUT) {
-#pragma unroll
-        for (int j = 0; j < MAX_OUT; ++j) {
-            oq[j] = 0.0f;
-            if (j < a.n_out) {
-                const int c = a.out_ch[((int64_t)b * a.H + gk) * a.n_out + j];
-                if (c < 0 || c >= D)
-                    kvq_dev_flag(a.hdr, KVQ_DEV_BAD_INDEX, b);
-                else if (q4 < GQ)
-                    oq[j] = S.qs[q4][c] * (1.0f / (float)(1 << BITS));
-            }
+        has0 = 2 * q4 < a.n_out;
+        has1 = 2 * q4 + 1 < a.n_out;
+        float qlo = 0.0f, qhi = 0.0f;
+        const int32_t* chs = a.out_ch + ((int64_t)b * a.H + gk) * a.n_out;
+        const int c0 = has0 ? chs[2 * q4] : 0, c1 = has1 ? chs[2 * q4 + 1] : 0;
+        if (c0 < 0 || c0 >= D || c1 < 0 || c1 >= D) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_INDEX, b);
+        const int h = g8 >> 1;
+        if ((g8 & 1) == 0 && h < GQ) {  // q 2^BITS back to q: exact
+            if (has0 && c0 >= 0 && c0 < D) qlo = S.qs[h][c0] * (1.0f / (float)(1 << BITS));
+            if (has1 && c1 >= 0 && c1 < D) qhi = S.qs[h][c1] * (1.0f / (float)(1 << BITS));
         }
+        ob0 = pack_h2(qlo, qhi);
     }
-    auto ko_of = [&](int bf) -> uint16_t* {
-        if constexpr (OUT) return S.ko[warp][bf];
-        else return nullptr;
-    };
+    auto ko_of = [&](int bf) -> uint16_t* { return OUT ? ko_base + (warp * 2 + bf) * KG * a.n_out : nullptr; };
 
     int gi = g_begin + warp, buf = 0;
     if (gi < g_end)
@@ -417,6 +418,16 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
                 KVQ_KSTEP(6);
                 KVQ_KSTEP(7);
 #undef KVQ_KSTEP
+                if constexpr (OUT) {  // the outlier channels of tokens 16mt + g8 (+ 8): exact fp16 keys
+                    uint32_t oa0 = 0u, oa1 = 0u;
+                    if (has0) {
+                        const uint16_t* kr = ko_of(buf) + (16 * mt + g8) * a.n_out + 2 * q4;
+                        const uint16_t* kr8 = kr + 8 * a.n_out;
+                        oa0 = (uint32_t)kr[0] | (has1 ? (uint32_t)kr[1] << 16 : 0u);
+                        oa1 = (uint32_t)kr8[0] | (has1 ? (uint32_t)kr8[1] << 16 : 0u);
+                    }
+                    mma16816(d, oa0, oa1, 0u, 0u, ob0, 0u);
+                }
             } else {
                 // the unfinished group: fp16 keys (rows t mod 64 of the tail buffer), q unscaled
                 const uint32_t* k0 = reinterpret_cast<const uint32_t*>(
@@ -429,23 +440,6 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), 1) qmma_kernel(QAttnArg
             sc[mt][0] = d[0] + d[1];
             sc[mt][1] = d[2] + d[3];
         }
-        if constexpr (OUT) {  // the outlier channels of the packed tokens 16mt + g8 + 8e, exact fp16 keys
-            if (packed) {
-                const uint16_t* ko = S.ko[warp][buf];
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const uint16_t* kr = ko + (16 * mt + g8 + 8 * e) * a.n_out;
-                        float cr = 0.0f;
-#pragma unroll
-                        for (int j = 0; j < MAX_OUT; ++j)
-                            if (j < a.n_out) cr = fmaf(oq[j], kvq_h2f(kr[j]), cr);
-                        sc[mt][e] += cr;
-                    }
-            }
-        }
-
         // ---- online softmax of head q4 (log2 domain) over the group's 64 tokens: eight per lane
         float gm = -INFINITY;
 #pragma unroll
@@ -988,8 +982,9 @@ size_t ws_layout(const kvq_layout* L, const kvq_seqs* S, const Plan& p, size_t* 
 
 template <int BITS, int GQ, int NGV, bool OUT = false>
 int launch_one(dim3 grid, cudaStream_t s, const QAttnArgs& a) {
-    const int smem = (int)sizeof(QMSmemOf<BITS, GQ, OUT>);
-    static_assert(sizeof(QMSmemOf<BITS, 4, OUT>) <= 227 * 1024, "one CTA's stages fit in shared memory");
+    const int smem = (int)(sizeof(QMSmem<BITS, GQ>) + (OUT ? ko_bytes<BITS>(a.n_out) : 0));
+    static_assert(sizeof(QMSmem<BITS, 4>) + (OUT ? ko_bytes<BITS>(MAX_OUT) : 0) <= 227 * 1024,
+                  "one CTA's stages fit in shared memory");
     const int st = kvq_prepare_kernel((const void*)qmma_kernel<BITS, GQ, NGV, OUT>, smem);
     if (st) return st;
     const cudaError_t e =

@@ -238,9 +238,24 @@ __global__ void __launch_bounds__(HA_NT) h2o_kernel(H2OArgs a) {
 }
 
 // ================================================================ a8 dense-preference score
+//
+// Two launches.  dp_scores_kernel, per (128-token tile, kv head, sequence): the scores of all the
+// kv head's R = GQ n_q query rows against the tile's keys as m16n8k16 tensor-core products (fp16
+// inputs, exact products, fp32 sums; channels permuted inside each k-step identically in both
+// operands so that every lane reads whole 8-byte runs), scaled to the log2 domain and written to
+// the workspace score matrix [B][H_q][n_q][ld]: K is read once per kv head, not once per query.
+// dp_row_kernel, per row (query i of q head h of sequence b) over its causal prefix L = T - n_q +
+// i + 1: max and sum of exp2 (one online pass), the k-th largest score by a four-pass 8-bit radix
+// select on order-preserving keys, the top-k mass; the last row of (b, h) forms P.  A row of up to
+// DP_SMEM_T scores is copied to shared memory first; a longer row is read from the workspace in
+// every pass (no length limit).
 
 constexpr int DP_NT = 256;
-constexpr int DP_MAX_T = 49152;
+constexpr int DP_SMEM_T = 49152;         // rows up to this length are reduced in shared memory
+constexpr int DPS_NW = 8;                // warps of the scores kernel: one 16-token page each
+constexpr int DPS_TILE = DPS_NW * PG;    // tokens per scores CTA
+constexpr int DPS_QLD = D + 16;          // padded query row in shared memory (halves, 288 bytes)
+constexpr int DP_MAX_ROWS = 512;         // GQ n_q query rows of one kv head
 
 struct DPArgs {
     const uint16_t* k16;
@@ -252,10 +267,94 @@ struct DPArgs {
     const uint16_t* q;
     int32_t n_q, topk;
     float* P;
+    float* S;           // [B][H_q][n_q][ld] log2-domain scores
+    int64_t ld;
     float* rows;        // [B][H_q][n_q] per-query top-k mass
     int32_t* counters;  // [B][H_q]
     KvqWsHeader* hdr;
 };
+
+__device__ __forceinline__ void dp_mma(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                       uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(32 * DPS_NW) dp_scores_kernel(DPArgs a) {
+    extern __shared__ __align__(16) uint16_t qsm[];  // [R16][DPS_QLD]
+    const int tile = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, q4 = lane & 3;
+    const int R = a.GQ * a.n_q, R16 = (R + 15) & ~15;
+    const int Hq = a.H * a.GQ;
+    const int T = a.seq_lens[b];
+    if (T > a.max_len || T < 0) {
+        if (tid == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
+        return;
+    }
+    const int t_base = tile * DPS_TILE;
+    if (t_base >= T) return;
+    // the kv head's query rows (row j n_q + i: query i of q head g GQ + j), zero rows up to R16
+    const uint16_t* qsrc = a.q + ((int64_t)b * Hq + g * a.GQ) * a.n_q * D;
+    for (int e = tid; e < R16 * (D / 8); e += 32 * DPS_NW) {
+        const int r = e / (D / 8), c8 = e % (D / 8);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < R) v = __ldg(reinterpret_cast<const uint4*>(qsrc + (int64_t)r * D + 8 * c8));
+        *reinterpret_cast<uint4*>(qsm + r * DPS_QLD + 8 * c8) = v;
+    }
+    __syncthreads();
+    const int t0 = t_base + warp * PG;  // this warp's page
+    if (t0 >= T) return;                // (no block barrier below)
+    int32_t page = a.bt[(int64_t)b * a.max_blocks + t0 / PG];
+    if (page < 0 || page >= a.num_blocks) {
+        if (lane == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, t0);
+        return;
+    }
+    // B fragments of the page's tokens g8 (n-tile 0) and g8 + 8 (n-tile 1): k slot 2 q4 + e of k-step
+    // s is channel 16 s + 4 q4 + e, slot 8 + 2 q4 + e is channel 16 s + 4 q4 + 2 + e (the A operand
+    // below uses the same map, so the sums are the dot products over all 128 channels)
+    uint32_t kb[2][8][2];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        const int tok = g8 + 8 * n;
+        const bool valid = t0 + tok < T;
+        const uint16_t* kr = a.k16 + (((int64_t)page * a.H + g) * PG + tok) * D + 4 * q4;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint2 w = valid ? __ldg(reinterpret_cast<const uint2*>(kr + 16 * s)) : make_uint2(0u, 0u);
+            kb[n][s][0] = w.x;
+            kb[n][s][1] = w.y;
+        }
+    }
+    float* srow = a.S + ((int64_t)b * Hq + g * a.GQ) * a.n_q * a.ld;  // row r at srow + r ld
+    for (int mt = 0; mt < R16 / 16; ++mt) {
+        float d[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) d[n][0] = d[n][1] = d[n][2] = d[n][3] = 0.0f;
+        const uint16_t* q0 = qsm + (16 * mt + g8) * DPS_QLD + 4 * q4;
+        const uint16_t* q1 = q0 + 8 * DPS_QLD;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint2 x0 = *reinterpret_cast<const uint2*>(q0 + 16 * s);
+            const uint2 x1 = *reinterpret_cast<const uint2*>(q1 + 16 * s);
+#pragma unroll
+            for (int n = 0; n < 2; ++n) dp_mma(d[n], x0.x, x1.x, x0.y, x1.y, kb[n][s][0], kb[n][s][1]);
+        }
+        // d[n][0..1]: row 16 mt + g8, tokens t0 + 8 n + 2 q4 + {0, 1}; d[n][2..3]: row 16 mt + g8 + 8
+        const int r0 = 16 * mt + g8, r1 = r0 + 8;
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const int tt = t0 + 8 * n + 2 * q4;
+            if (r0 < R)
+                *reinterpret_cast<float2*>(srow + (int64_t)r0 * a.ld + tt) =
+                    make_float2(d[n][0] * KVQ_SCORE_LOG2_SCALE, d[n][1] * KVQ_SCORE_LOG2_SCALE);
+            if (r1 < R)
+                *reinterpret_cast<float2*>(srow + (int64_t)r1 * a.ld + tt) =
+                    make_float2(d[n][2] * KVQ_SCORE_LOG2_SCALE, d[n][3] * KVQ_SCORE_LOG2_SCALE);
+        }
+    }
+}
 
 __device__ __forceinline__ float block_reduce_max(float v, float* red) {
     v = kvq_warp_max(v);
@@ -277,15 +376,14 @@ __device__ __forceinline__ float block_reduce_sum(float v, float* red) {
     return r;
 }
 
-__global__ void __launch_bounds__(DP_NT) dense_pref_kernel(DPArgs a) {
-    extern __shared__ float sc[];  // scores of the row, log2 domain
-    __shared__ float qf[D];
+__global__ void __launch_bounds__(DP_NT) dp_row_kernel(DPArgs a) {
+    extern __shared__ float sc[];  // the row, when it has at most DP_SMEM_T scores
     __shared__ float redf[DP_NT / 32];
     __shared__ uint32_t hist[256];
     __shared__ uint32_t s_bin, s_above;
+    __shared__ float s_kth;
     __shared__ int is_last;
     const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
-    const int g = h / a.GQ;
     const int Hq = a.H * a.GQ;
     const int T = a.seq_lens[b];
     const int L = T - a.n_q + i + 1;  // keys seen by query i
@@ -293,38 +391,26 @@ __global__ void __launch_bounds__(DP_NT) dense_pref_kernel(DPArgs a) {
     if (T > a.max_len || L <= 0) {
         if (tid == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
     } else {
-        if (tid < D) qf[tid] = kvq_h2f(a.q[(((int64_t)b * Hq + h) * a.n_q + i) * D + tid]) * KVQ_SCORE_LOG2_SCALE;
-        __syncthreads();
-        const int hw = tid >> 4, l16 = tid & 15;
-        for (int t0 = 0; t0 < L; t0 += DP_NT / 16) {
-            const int t = t0 + hw;
-            float acc = 0.0f;
-            if (t < L) {
-                int32_t page = a.bt[(int64_t)b * a.max_blocks + (t >> 4)];
-                if (page < 0 || page >= a.num_blocks) {
-                    if (l16 == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_PAGE, t);
-                    page = 0;
-                }
-                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-                    a.k16 + (((int64_t)page * a.H + g) * PG + (t & 15)) * D + 8 * l16));
-                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    acc = fmaf(qf[8 * l16 + 2 * j], kvq_h2f((uint16_t)(w[j] & 0xffffu)), acc);
-                    acc = fmaf(qf[8 * l16 + 2 * j + 1], kvq_h2f((uint16_t)(w[j] >> 16)), acc);
-                }
-            }
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (t < L && l16 == 0) sc[t] = acc;
+        const float* row = a.S + (((int64_t)b * Hq + h) * a.n_q + i) * a.ld;
+        const bool in_smem = L <= DP_SMEM_T;
+        if (in_smem) {
+            for (int t = tid; t < L; t += DP_NT) sc[t] = __ldcg(row + t);
+            __syncthreads();
         }
-        __syncthreads();
-        float mx = -INFINITY;
-        for (int t = tid; t < L; t += DP_NT) mx = fmaxf(mx, sc[t]);
-        mx = block_reduce_max(mx, redf);
-        float z = 0.0f;
-        for (int t = tid; t < L; t += DP_NT) z += exp2f(sc[t] - mx);
-        z = block_reduce_sum(z, redf);
+        const float* src = in_smem ? sc : row;
+        // max and sum of exp2 in one pass (a running sum rescaled when the running max grows)
+        float mx = -INFINITY, z = 0.0f;
+        for (int t = tid; t < L; t += DP_NT) {
+            const float v = src[t];
+            if (v > mx) {
+                z = fmaf(z, exp2f(mx - v), 1.0f);
+                mx = v;
+            } else {
+                z += exp2f(v - mx);
+            }
+        }
+        const float M = block_reduce_max(mx, redf);
+        z = block_reduce_sum(mx == -INFINITY ? 0.0f : z * exp2f(mx - M), redf);
         const int kk = min(a.topk, L);
         // radix select of the kk-th largest score
         uint32_t prefix = 0u, mask = 0u, remaining = (uint32_t)kk;
@@ -333,7 +419,7 @@ __global__ void __launch_bounds__(DP_NT) dense_pref_kernel(DPArgs a) {
             for (int j = tid; j < 256; j += DP_NT) hist[j] = 0u;
             __syncthreads();
             for (int t = tid; t < L; t += DP_NT) {
-                const uint32_t key = kvq_float_key(sc[t]);
+                const uint32_t key = kvq_float_key(src[t]);
                 if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
             }
             __syncthreads();
@@ -367,28 +453,23 @@ __global__ void __launch_bounds__(DP_NT) dense_pref_kernel(DPArgs a) {
             mask |= 255u << shift;
             __syncthreads();
         }
-        // top-k mass: every score above the k-th, plus the k-th value for the remaining slots
-        float top = 0.0f, kth_val = 0.0f;
+        // top-k mass: every score above the k-th, plus the k-th value for the remaining slots (every
+        // thread that meets the k-th key writes the same value)
+        float top = 0.0f;
         uint32_t n_gt = 0;
         for (int t = tid; t < L; t += DP_NT) {
-            const uint32_t key = kvq_float_key(sc[t]);
+            const float v = src[t];
+            const uint32_t key = kvq_float_key(v);
             if (key > prefix) {
-                top += exp2f(sc[t] - mx);
+                top += exp2f(v - M);
                 ++n_gt;
             } else if (key == prefix) {
-                kth_val = sc[t];
+                s_kth = v;
             }
         }
         top = block_reduce_sum(top, redf);
-        n_gt = (uint32_t)block_reduce_sum((float)n_gt, redf);
-        // kth_val: any thread that saw the k-th key holds it
-        __shared__ float s_kth;
-        __syncthreads();
-        for (int t = tid; t < L; t += DP_NT)
-            if (kvq_float_key(sc[t]) == prefix) s_kth = sc[t];
-        __syncthreads();
-        kth_val = s_kth;
-        top += (float)(kk - (int)n_gt) * exp2f(kth_val - mx);
+        n_gt = (uint32_t)block_reduce_sum((float)n_gt, redf);  // (block_reduce_sum synchronizes)
+        top += (float)(kk - (int)n_gt) * exp2f(s_kth - M);
         r_i = top / z;
     }
     // per-query mass -> workspace; the last CTA of (b, h) forms P = n_q - sum_i r_i
@@ -410,11 +491,17 @@ __global__ void __launch_bounds__(DP_NT) dense_pref_kernel(DPArgs a) {
     }
 }
 
-size_t dp_ws_layout(const kvq_layout* L, const kvq_seqs* S, int32_t n_q, size_t* off_rows, size_t* off_cnt) {
+int64_t dp_ld(const kvq_seqs* S) {
+    return ((int64_t)std::max(S->max_len, 1) + DPS_TILE - 1) / DPS_TILE * DPS_TILE;
+}
+
+size_t dp_ws_layout(const kvq_layout* L, const kvq_seqs* S, int32_t n_q, size_t* off_rows, size_t* off_cnt,
+                    size_t* off_s) {
     const size_t rows = (size_t)std::max(S->batch, 1) * L->n_q_heads * (size_t)std::max(n_q, 1);
     *off_rows = sizeof(KvqWsHeader);
     *off_cnt = kvq_round_up(*off_rows + rows * sizeof(float), 256);
-    return kvq_round_up(*off_cnt + (size_t)std::max(S->batch, 1) * L->n_q_heads * sizeof(int32_t), 256);
+    *off_s = kvq_round_up(*off_cnt + (size_t)std::max(S->batch, 1) * L->n_q_heads * sizeof(int32_t), 256);
+    return kvq_round_up(*off_s + rows * (size_t)dp_ld(S) * sizeof(float), 256);
 }
 
 }  // namespace
@@ -459,28 +546,32 @@ extern "C" int kv_h2o_accumulate(const kvq_layout* L, const kvq_seqs* S, const f
 
 extern "C" size_t kv_dense_pref_score_ws(const kvq_layout* L, const kvq_seqs* S, int32_t n_q) {
     if (kvq_check_layout(L, "kv_dense_pref_score_ws", true) || kvq_check_seqs_sizes(S, "kv_dense_pref_score_ws")) return 0;
-    size_t a, c;
-    return dp_ws_layout(L, S, n_q, &a, &c);
+    size_t a, c, s;
+    return dp_ws_layout(L, S, n_q, &a, &c, &s);
 }
 
 extern "C" int kv_dense_pref_score(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q_recent,
                                    int32_t n_q, int32_t topk, float* Pout, void* ws, size_t ws_bytes, void* stream) {
     kvq_clear_error();
-    int st = kvq_check_layout(L, "kv_dense_pref_score", true);
+    const char* fn = "kv_dense_pref_score";
+    int st = kvq_check_layout(L, fn, true);
     if (st) return st;
-    st = kvq_check_seqs(S, "kv_dense_pref_score");
+    st = kvq_check_seqs(S, fn);
     if (st) return st;
-    KVQ_REQUIRE(P && P->k16, KVQ_ERR_INVALID_ARG, "kv_dense_pref_score: pool needs k16");
-    KVQ_REQUIRE(((uintptr_t)P->k16 & 15u) == 0, KVQ_ERR_INVALID_ARG, "kv_dense_pref_score: k16 must be 16-byte aligned");
+    KVQ_REQUIRE(P && P->k16, KVQ_ERR_INVALID_ARG, "%s: pool needs k16", fn);
+    KVQ_REQUIRE(((uintptr_t)P->k16 & 15u) == 0 && ((uintptr_t)q_recent & 15u) == 0, KVQ_ERR_INVALID_ARG,
+                "%s: k16 and q_recent must be 16-byte aligned", fn);
     KVQ_REQUIRE(n_q >= 1 && n_q <= S->max_len && topk >= 1, KVQ_ERR_INVALID_ARG,
-                "kv_dense_pref_score: need 1 <= n_q <= max_len and topk >= 1");
-    KVQ_REQUIRE(S->max_len <= DP_MAX_T, KVQ_ERR_UNSUPPORTED, "kv_dense_pref_score: max_len above %d", DP_MAX_T);
-    size_t off_rows, off_cnt;
-    const size_t need = dp_ws_layout(L, S, n_q, &off_rows, &off_cnt);
-    st = kvq_check_ws(ws, ws_bytes, need, "kv_dense_pref_score");
+                "%s: need 1 <= n_q <= max_len and topk >= 1", fn);
+    const int gq = L->n_q_heads / L->n_kv_heads;
+    KVQ_REQUIRE((int64_t)gq * n_q <= DP_MAX_ROWS, KVQ_ERR_UNSUPPORTED,
+                "%s: (q heads per kv head) x n_q = %d above %d", fn, gq * n_q, DP_MAX_ROWS);
+    size_t off_rows, off_cnt, off_s;
+    const size_t need = dp_ws_layout(L, S, n_q, &off_rows, &off_cnt, &off_s);
+    st = kvq_check_ws(ws, ws_bytes, need, fn);
     if (st) return st;
     if (S->batch == 0) return KVQ_OK;
-    KVQ_REQUIRE(q_recent && Pout && S->block_table, KVQ_ERR_INVALID_ARG, "kv_dense_pref_score: NULL buffer");
+    KVQ_REQUIRE(q_recent && Pout && S->block_table, KVQ_ERR_INVALID_ARG, "%s: NULL buffer", fn);
     DPArgs a;
     a.k16 = P->k16;
     a.num_blocks = P->num_blocks;
@@ -489,20 +580,28 @@ extern "C" int kv_dense_pref_score(const kvq_layout* L, const kvq_pool* P, const
     a.max_blocks = S->max_blocks;
     a.max_len = S->max_len;
     a.H = L->n_kv_heads;
-    a.GQ = L->n_q_heads / L->n_kv_heads;
+    a.GQ = gq;
     a.q = q_recent;
     a.n_q = n_q;
     a.topk = topk;
     a.P = Pout;
+    a.S = reinterpret_cast<float*>(static_cast<char*>(ws) + off_s);
+    a.ld = dp_ld(S);
     a.rows = reinterpret_cast<float*>(static_cast<char*>(ws) + off_rows);
     a.counters = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + off_cnt);
     a.hdr = static_cast<KvqWsHeader*>(ws);
-    const size_t smem = (size_t)std::max(S->max_len, 1) * sizeof(float);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(dense_pref_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             DP_MAX_T * (int)sizeof(float));
-        if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_dense_pref_score: %s", cudaGetErrorString(e));
-    }
-    dense_pref_kernel<<<dim3(n_q, L->n_q_heads, S->batch), DP_NT, smem, kvq_stream(stream)>>>(a);
-    return kvq_launch_status("kv_dense_pref_score");
+    cudaStream_t s = kvq_stream(stream);
+    const int r16 = (gq * n_q + 15) & ~15;
+    const int smem_q = r16 * DPS_QLD * (int)sizeof(uint16_t);
+    st = kvq_prepare_kernel((const void*)dp_scores_kernel, smem_q);
+    if (st) return st;
+    const unsigned tiles = (unsigned)((std::max(S->max_len, 1) + DPS_TILE - 1) / DPS_TILE);
+    dp_scores_kernel<<<dim3(tiles, L->n_kv_heads, S->batch), 32 * DPS_NW, smem_q, s>>>(a);
+    st = kvq_launch_status(fn);
+    if (st) return st;
+    const int smem_row = std::min(std::max(S->max_len, 1), DP_SMEM_T) * (int)sizeof(float);
+    st = kvq_prepare_kernel((const void*)dp_row_kernel, smem_row);
+    if (st) return st;
+    dp_row_kernel<<<dim3(n_q, L->n_q_heads, S->batch), DP_NT, smem_row, s>>>(a);
+    return kvq_launch_status(fn);
 }

@@ -10,6 +10,7 @@ constexpr int D = KVQ_HEAD_DIM;
 constexpr int PG = KVQ_BLOCK_TOKENS;
 constexpr int KG = KVQ_K_GROUP_TOKENS;
 constexpr int MAX_OUT = 8;
+static_assert(KG == 64, "the group index below divides by shifting");
 
 // ---- outlier channels: per-channel variance from exact integer sums
 //
@@ -22,49 +23,68 @@ constexpr int MAX_OUT = 8;
 // Var = (S2 - S1^2 / T) / T with one rounding per operation, picks the n_out largest (ties -> lower
 // channel) and zeroes the workspace again.
 
-constexpr int OC_LANES = 4;      // token lanes per CTA (x 128 channels = 512 threads)
-constexpr int OC_CHUNK = 1024;   // tokens per CTA
+constexpr int OC_NT = 256;       // threads per CTA: 16 channel groups of 8 x 16 token lanes
+constexpr int OC_CHUNK = 2048;   // tokens per CTA
 constexpr int OC_MAX_T = 1 << 22;
 
 // fp16 bits -> the value in units of 2^-24 (exact); finite inputs only
-__device__ __forceinline__ int64_t h_units(uint16_t h) {
+__device__ __forceinline__ int64_t h_units(uint32_t h) {
     const uint32_t e = (h >> 10) & 31u, m = h & 1023u;
     const int64_t mag = e == 0 ? (int64_t)m : (int64_t)(m | 1024u) << (e - 1);
     return (h & 0x8000u) ? -mag : mag;
 }
 
-__global__ void __launch_bounds__(OC_LANES * D) outlier_sums_kernel(const uint16_t* k, int64_t n_tokens,
-                                                                    int64_t stride_t, unsigned long long* sums) {
-    __shared__ unsigned long long part[OC_LANES][4][D];
-    const int h = blockIdx.y, c = threadIdx.x % D, lane = threadIdx.x / D;
+// grid (chunks of 2048 tokens, kv heads); thread: channels 8 cg .. 8 cg + 7 (one 16-byte load per
+// token) of tokens t0 + lt + 16 j
+__global__ void __launch_bounds__(OC_NT) outlier_sums_kernel(const uint16_t* k, int64_t n_tokens, int64_t stride_t,
+                                                             unsigned long long* sums) {
+    __shared__ unsigned long long part[OC_NT / 32][4][D];
+    const int h = blockIdx.y, tid = threadIdx.x, cg = tid & 15, lt = tid >> 4;
     const int64_t t0 = (int64_t)blockIdx.x * OC_CHUNK;
     const int64_t t1 = min(n_tokens, t0 + OC_CHUNK);
-    int64_t s1 = 0;
-    unsigned long long p2 = 0, p1 = 0, p0 = 0;
-    const uint16_t* src = k + (int64_t)h * D + c;
-    for (int64_t t = t0 + lane; t < t1; t += OC_LANES) {
-        const int64_t x = h_units(src[t * stride_t]);
-        s1 += x;
-        const uint64_t u = (uint64_t)(x < 0 ? -x : x);
-        const uint32_t ua = (uint32_t)(u >> 20), ub = (uint32_t)(u & 0xFFFFFu);
-        p2 += (unsigned long long)ua * ua;
-        p1 += 2ull * ((unsigned long long)ua * ub);
-        p0 += (unsigned long long)ub * ub;
-    }
-    part[lane][0][c] = (unsigned long long)s1;  // two's complement: wrapping sums stay exact
-    part[lane][1][c] = p2;
-    part[lane][2][c] = p1;
-    part[lane][3][c] = p0;
-    __syncthreads();
-    if (lane == 0) {
-        unsigned long long* dst = sums + (int64_t)h * 4 * D;
+    int64_t s1[8];
+    unsigned long long p2[8], p1[8], p0[8];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            unsigned long long v = 0;
+    for (int i = 0; i < 8; ++i) s1[i] = 0, p2[i] = p1[i] = p0[i] = 0ull;
+    const uint16_t* src = k + (int64_t)h * D + 8 * cg;
+    for (int64_t t = t0 + lt; t < t1; t += 16) {
+        const uint4 w = *reinterpret_cast<const uint4*>(src + t * stride_t);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int l = 0; l < OC_LANES; ++l) v += part[l][w][c];
-            atomicAdd(dst + w * D + c, v);
+        for (int i = 0; i < 8; ++i) {
+            const int64_t x = h_units((ws[i >> 1] >> (16 * (i & 1))) & 0xFFFFu);
+            s1[i] += x;
+            const uint64_t u = (uint64_t)(x < 0 ? -x : x);
+            const uint32_t ua = (uint32_t)(u >> 20), ub = (uint32_t)(u & 0xFFFFFu);
+            p2[i] += (unsigned long long)ua * ua;
+            p1[i] += 2ull * ((unsigned long long)ua * ub);
+            p0[i] += (unsigned long long)ub * ub;
         }
+    }
+    // the warp's two token lanes (lanes l and l + 16 share cg), then the eight warps
+    const int warp = tid >> 5;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        unsigned long long v0 = (unsigned long long)s1[i], v1 = p2[i], v2 = p1[i], v3 = p0[i];
+        v0 += __shfl_xor_sync(0xffffffffu, v0, 16);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 16);
+        v2 += __shfl_xor_sync(0xffffffffu, v2, 16);
+        v3 += __shfl_xor_sync(0xffffffffu, v3, 16);
+        if ((tid & 31) < 16) {
+            part[warp][0][8 * cg + i] = v0;  // two's complement: wrapping sums stay exact
+            part[warp][1][8 * cg + i] = v1;
+            part[warp][2][8 * cg + i] = v2;
+            part[warp][3][8 * cg + i] = v3;
+        }
+    }
+    __syncthreads();
+    unsigned long long* dst = sums + (int64_t)h * 4 * D;
+    for (int e = tid; e < 4 * D; e += OC_NT) {
+        const int w = e / D, c = e % D;
+        unsigned long long v = 0;
+#pragma unroll
+        for (int l = 0; l < OC_NT / 32; ++l) v += part[l][w][c];
+        atomicAdd(dst + w * D + c, v);
     }
 }
 
@@ -142,9 +162,9 @@ struct IsoArgs {
 };
 
 // Isolates the outlier channels of one complete 64-token group (group index gi of sequence b, kv
-// head h): thread i < 64 = token 64 gi + i.  src(i, c): the fp16 key of token i of the group at c.
-template <typename Src>
-__device__ __forceinline__ void isolate_group(const IsoArgs& a, int b, int h, int gi, Src src) {
+// head h): thread i < 64 = token 64 gi + i, whose fp16 key at channel c is src[i * ld + c].
+__device__ __forceinline__ void isolate_group(const IsoArgs& a, int b, int h, int gi, const uint16_t* src,
+                                              int64_t ld) {
     const int i = threadIdx.x;
     const int32_t* ch = a.out_ch + ((int64_t)b * a.H + h) * a.n_out;
     const int32_t page = a.bt[(int64_t)b * a.max_blocks + 4 * gi + i / PG];
@@ -162,7 +182,7 @@ __device__ __forceinline__ void isolate_group(const IsoArgs& a, int b, int h, in
             a.k_out[row * a.n_out + j] = 0;
             continue;
         }
-        a.k_out[row * a.n_out + j] = src(i, c);
+        a.k_out[row * a.n_out + j] = src[(int64_t)i * ld + c];
         int w, bit;
         kvq_k_code_pos(c, a.bits, &w, &bit);
         codes[w] &= ~(M << bit);  // this thread owns the token's row
@@ -177,9 +197,9 @@ __device__ __forceinline__ void isolate_group(const IsoArgs& a, int b, int h, in
 __global__ void __launch_bounds__(KG) isolate_prefill_kernel(IsoArgs a, int64_t n_full) {
     const int gl = blockIdx.x, h = blockIdx.y;
     if (gl >= n_full) return;
-    const int gi = (int)(a.t_start / KG) + gl;
+    const int gi = (int)(a.t_start >> 6) + gl;  // t_start / 64 (a multiple of 64, checked on the host)
     const uint16_t* base = a.k + (int64_t)gl * KG * a.stride_t + (int64_t)h * D;
-    isolate_group(a, a.seq, h, gi, [&](int i, int c) { return base[(int64_t)i * a.stride_t + c]; });
+    isolate_group(a, a.seq, h, gi, base, a.stride_t);
 }
 
 // decode form: grid (H, batch); a sequence whose newest token completed a group (T % 64 == 0)
@@ -190,7 +210,7 @@ __global__ void __launch_bounds__(KG) isolate_append_kernel(IsoArgs a) {
     const int T = a.seq_lens[b];
     if (T <= 0 || T % KG != 0) return;
     const uint16_t* tail = a.k_tail + ((int64_t)b * a.H + h) * KG * D;
-    isolate_group(a, b, h, T / KG - 1, [&](int i, int c) { return tail[(int64_t)i * D + c]; });
+    isolate_group(a, b, h, T / KG - 1, tail, D);
 }
 
 int check_iso(const kvq_layout* L, const kvq_pool* P, int32_t n_out, const int32_t* out_ch, uint16_t* k_out,
@@ -238,7 +258,8 @@ extern "C" int kv_outlier_channels(const kvq_layout* L, const uint16_t* k, int64
     if (st) return st;
     KVQ_REQUIRE(out_ch && n_tokens >= 0 && n_tokens <= OC_MAX_T && (k || n_tokens == 0), KVQ_ERR_INVALID_ARG,
                 "%s: NULL k / out_ch, or n_tokens outside [0, 2^22]", fn);
-    KVQ_REQUIRE(stride_t >= (int64_t)L->n_kv_heads * D, KVQ_ERR_INVALID_ARG, "%s: stride_t", fn);
+    KVQ_REQUIRE(stride_t >= (int64_t)L->n_kv_heads * D && stride_t % 8 == 0 && ((uintptr_t)k & 15u) == 0,
+                KVQ_ERR_INVALID_ARG, "%s: stride_t (>= H_kv * d, a multiple of 8) / k (16-byte aligned)", fn);
     KVQ_REQUIRE(n_out >= 1 && n_out <= MAX_OUT, KVQ_ERR_INVALID_ARG, "%s: n_out %d not in [1, 8]", fn, n_out);
     st = kvq_check_ws(ws, ws_bytes, kv_outlier_channels_ws(L), fn);
     if (st) return st;
@@ -247,7 +268,7 @@ extern "C" int kv_outlier_channels(const kvq_layout* L, const uint16_t* k, int64
     cudaStream_t s = kvq_stream(stream);
     if (n_tokens > 0) {
         const dim3 grid((unsigned)((n_tokens + OC_CHUNK - 1) / OC_CHUNK), L->n_kv_heads);
-        outlier_sums_kernel<<<grid, OC_LANES * D, 0, s>>>(k, n_tokens, stride_t, sums);
+        outlier_sums_kernel<<<grid, OC_NT, 0, s>>>(k, n_tokens, stride_t, sums);
     }
     outlier_rank_kernel<<<L->n_kv_heads, D, 0, s>>>(sums, n_tokens, n_out, out_ch, var);
     return kvq_launch_status(fn);

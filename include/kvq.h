@@ -574,10 +574,17 @@ size_t kv_h2o_accumulate_ws(void);
  * a row shorter than topk contributes all its entries.
  *
  * Reads fp16 keys k16 through the block table.  q_recent: device fp16
- * [batch][H_q][n_q][d]; P: device fp32 [batch][H_q].  The layer is
- * quantization-friendly when mean_h P/n_q > tau (decided by the caller).
- * n_q <= T; T <= 49152.
- * ws: kv_dense_pref_score_ws(layout, seqs, n_q) bytes.
+ * [batch][H_q][n_q][d], 16-byte aligned; P: device fp32 [batch][H_q].  The
+ * layer is quantization-friendly when mean_h P/n_q > tau (decided by the
+ * caller; kvq_classify_heads per kv head).  Two launches: the scores of the
+ * GQ*n_q query rows of a kv head against its keys as tensor-core products
+ * (fp16 inputs, exact products, fp32 sums; K read once per kv head) into the
+ * workspace, then one CTA per query row for max, sum, the k-th largest score
+ * (radix select) and the top-k mass; no length limit.  1 <= n_q <= T;
+ * (n_q_heads / n_kv_heads) * n_q <= 512.
+ * ws: kv_dense_pref_score_ws(layout, seqs, n_q) bytes, which includes the
+ * score matrix: batch * H_q * n_q * ceil(max_len / 128) * 128 fp32
+ * (512 MiB for one sequence of 32 q heads, n_q = 32, at 128K).
  * ---------------------------------------------------------------------- */
 int kv_dense_pref_score(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
                         const uint16_t* q_recent, int32_t n_q, int32_t topk, float* P,

@@ -217,3 +217,29 @@ def test_offload_gather_bytes():
         got_k = np.stack([dk[i // 16, h, i % 16] for i in range(cnt[h])]) if cnt[h] else ref_k
         got_v = np.stack([dv[i // 16, h, i % 16] for i in range(cnt[h])]) if cnt[h] else ref_v
         assert got_k.tobytes() == ref_k.tobytes() and got_v.tobytes() == ref_v.tobytes()
+
+
+@pytest.mark.parametrize("T,topk", [(131072, 4096), (70000 + 3, 1)])
+def test_dense_pref_score_long_context(T, topk):
+    """Rows longer than the shared-memory path (49152 scores): the per-row passes read the
+    workspace score matrix.  32 q / 8 kv heads, n_q = 32 recent queries; four q heads (one per
+    kv head pair) compared with the oracle within 1e-4 n_q."""
+    require_gpu()
+    Hq, Hkv, n_q = 32, 8, 32
+    seed = synth.mix(synth.BASE_SEED + 1, 42, T)
+    K, V = synth.kv_rows(T, Hkv, seed)
+    n_pages = math.ceil(T / 16)
+    alloc = kvq.Allocator(n_pages, seed=8)
+    batch, bt = paged_batch([T], alloc)
+    cache = kvq.LayerCache(Hq, Hkv, 16, n_pages, 1, t_cap=(T + 7) // 8 * 8)
+    kvq.kv_quant_pack(cache, batch, 0, 0, T, K.cuda(), V.cuda())
+    Q = synth.queries((1, Hq, n_q, 128), synth.mix(seed, 41))
+    P = torch.empty((1, Hq), device="cuda")
+    w = ws(kvq.kv_dense_pref_score_ws(cache, batch, n_q))
+    kvq.kv_dense_pref_score(cache, batch, Q.cuda(), n_q, topk, P, w)
+    kvq.kvq_check(w)
+    Pg = P.cpu().numpy()[0]
+    assert np.all((Pg >= 0) & (Pg <= n_q))
+    for h in (0, 9, 18, 31):
+        ref = O.dense_pref_score(Q[0, h].numpy(), K[:, O.kv_head_of(h, Hq, Hkv)].numpy(), topk)
+        assert abs(Pg[h] - ref) <= 1e-4 * n_q, (h, Pg[h], ref)
