@@ -61,6 +61,15 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s (burst) of this GPU: the measured figure, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1900.0
+
+
 def algorithmic_bytes(T, n_layers=32):
     """Algorithmic HBM bytes of one decode step at context T (after append):
     layer 0 reads its 1-bit K/V codes and (scale, zero) pairs, 48 B per token
@@ -1057,7 +1066,10 @@ def row_fp8(torch, np, kvq, synth, O, device, stream, hbm, T=131072):
 def row_mixed(torch, np, kvq, synth, O, device, stream, hbm, T=131072):
     """f2 + f4 head-level: one Llama-3.1-8B-shaped layer (32 q / 8 kv heads, T = 131072) whose kv
     heads were classified one by one; 2 of the 8 dense (their q heads attend every token), 6 sparse
-    (critical scores + top-K + attention), all in one launch."""
+    (critical scores + top-K + attention); classes dispatched on the device (the cluster launch for
+    the sparse heads and every append, then the dense kv heads' GQA-shared attention).  Algorithmic
+    bytes: a dense kv head's K and V once (its q heads share them), a sparse q head's critical
+    channels and selected rows."""
     Hq, Hkv, ns, w = 32, 8, 4, 128
     dense = [1, 0, 0, 0, 0, 1, 0, 0]
     seed = synth.BASE_SEED + 9
@@ -1074,7 +1086,7 @@ def row_mixed(torch, np, kvq, synth, O, device, stream, hbm, T=131072):
     q = synth.normal((1, Hq, D), synth.mix(seed, 1), device)
     out = torch.empty((1, Hq, D), device=device)
     dn = torch.tensor([dense], dtype=torch.int32, device=device)
-    wk = kvq.Workspace(kvq.kv_mixed_layer_decode_ws())
+    wk = kvq.Workspace(kvq.kv_mixed_layer_decode_ws(cache, seqs))
     sh = stream.cuda_stream
     g = _capture(torch, lambda: kvq.kv_mixed_layer_decode(cache, seqs, k_new, v_new, q, N_CRIT, -1, RATIO, ns, w, dn,
                                                           out, wk, stream=sh), stream)
@@ -1082,7 +1094,7 @@ def row_mixed(torch, np, kvq, synth, O, device, stream, hbm, T=131072):
     kvq.kvq_check(wk, stream=sh)
     n_d = sum(dense) * (Hq // Hkv)
     sel = ns + w + math.floor(RATIO * T)
-    nbytes = n_d * T * 2 * D * 2 + (Hq - n_d) * (N_CRIT * T * 2 + sel * 2 * D * 2)
+    nbytes = sum(dense) * T * 2 * D * 2 + (Hq - n_d) * (N_CRIT * T * 2 + sel * 2 * D * 2)
     gbs = nbytes / (ms * 1e-3) / 1e9
     del cache, g
     q0 = q[0, 0].cpu().numpy()
@@ -1094,11 +1106,48 @@ def row_mixed(torch, np, kvq, synth, O, device, stream, hbm, T=131072):
     t_s = _wall(one_sparse)
     return {"config": f"32 q / 8 kv heads, T = {T}: kv heads {[i for i, x in enumerate(dense) if x]} classified dense "
                       "(their 8 q heads attend all tokens), the other 24 q heads sparse (8 critical channels, top-K = "
-                      "floor(0.03 T) + 4 sinks + 128 window); one launch",
-            "value": gbs, "unit": "GB/s", "us_per_launch": ms * 1e3, "bytes_per_launch": nbytes, "calls": reps,
+                      "floor(0.03 T) + 4 sinks + 128 window); classes dispatched on the device (cluster launch + the dense kv heads' GQA-shared attention)",
+            "value": gbs, "unit": "GB/s", "us_per_layer": ms * 1e3, "bytes_per_layer": nbytes, "calls": reps,
             "roofline": hbm(gbs), "clocks": clk,
             "cpu_baseline": {"value": 1.0 / (n_d * t_d + (Hq - n_d) * t_s), "unit": "layers/s", "cores": 1,
                              "kind": "oracle", "sample": "one dense and one sparse q head, numpy, scaled to 8 + 24"}}
+
+
+def row_densepref(torch, np, kvq, synth, O, device, stream, tensor_peak):
+    """a8 kv_dense_pref_score at the 128K layer shape: 32 q / 8 kv heads, T = 131072, the
+    n_q = 32 most recent queries, top-k = floor(0.03 T) = 3932 (the sparse layers' K).  One call
+    = the tensor-core scores of 8 kv heads x 128 query rows x 131072 keys (34.4 GFLOP, K read
+    once per kv head) + per-row reductions of 1024 rows of up to 131072 scores."""
+    Hq, Hkv, T, n_q = 32, 8, 131072, 32
+    topk = int(0.03 * T)
+    seed = synth.BASE_SEED + 1
+    alloc = kvq.Allocator(T // 16, seed=21)
+    seqs = kvq.Batch(torch.tensor([alloc.alloc(T // 16)], dtype=torch.int32, device=device),
+                     torch.tensor([T], dtype=torch.int32, device=device), T)
+    cache = kvq.LayerCache(Hq, Hkv, 16, T // 16, 1, t_cap=T, device=device)
+    K, V = synth.kv_rows(T, Hkv, synth.mix(seed, 60), device=device)
+    kvq.kv_quant_pack(cache, seqs, 0, 0, T, K, V)
+    Q = synth.queries((1, Hq, n_q, D), synth.mix(seed, 61)).to(device)
+    P = torch.empty((1, Hq), device=device)
+    wd = kvq.Workspace(kvq.kv_dense_pref_score_ws(cache, seqs, n_q))
+    sh = stream.cuda_stream
+    ms, reps, clk = _timed(torch, lambda: kvq.kv_dense_pref_score(cache, seqs, Q, n_q, topk, P, wd, stream=sh),
+                           stream, min_ms=100.0)
+    kvq.kvq_check(wd, stream=sh)
+    flops = 2.0 * Hkv * (Hq // Hkv) * n_q * T * D
+    kh, qh = K[:, 0].cpu().numpy(), Q[0, 0].cpu().numpy()
+    del cache, wd, K, V
+    t = _wall(lambda: O.dense_pref_score(qh, kh, topk))
+    return {"config": f"32 q / 8 kv heads, T = {T}, n_q = {n_q} recent queries, top-k = {topk}; one call over "
+                      "all heads", "value": ms, "unit": "ms per call", "steps": reps,
+            "scores_tflops_if_alone": flops / (ms * 1e-3) / 1e12,
+            "roofline": {"bound": "latency", "note": "one call per layer at prefill (classification); the score "
+                         f"product is {flops / 1e9:.1f} GFLOP, the per-row reductions read 1024 rows of "
+                         f"{T} fp32 scores; reported as time, with the contraction rate it implies as a lower "
+                         f"bound against the measured bf16 peak {tensor_peak} TFLOP/s"},
+            "clocks": clk,
+            "cpu_baseline": {"value": t * 1e3 * Hq, "unit": "ms per call", "cores": 1, "kind": "oracle",
+                             "sample": "one q head with numpy fp64, scaled to 32 heads"}}
 
 
 def row_tiny(torch, np, kvq, synth, O, device, stream):
@@ -1166,7 +1215,8 @@ ROWS = [
     ("f1 kv_group_critical_score + shared top-K + shared-list attention (GQA-shared selection)", row_group),
     ("f4 kv_decode_attn_quant on an FP8 E4M3 layer", row_fp8),
     ("f3 kv_decode_attn_quant_outlier (isolated outlier key channels, INT4 batch)", row_outlier),
-    ("f2 kv_mixed_layer_decode (head-level classes, one launch)", row_mixed),
+    ("f2 kv_mixed_layer_decode (head-level classes dispatched on the device)", row_mixed),
+    ("a8 kv_dense_pref_score (128K layer classification)", row_densepref),
     ("tiny", row_tiny),
 ]
 
@@ -1187,6 +1237,8 @@ def run_rows(device, stream, only=None):
         try:
             if fn in (row_offload, row_tiny):
                 r = fn(torch, np, kvq, synth, O, device, stream)
+            elif fn is row_densepref:
+                r = fn(torch, np, kvq, synth, O, device, stream, measured_tensor_peak())
             else:
                 r = fn(torch, np, kvq, synth, O, device, stream, _hbm(peak, src))
             if fn is row_tiny:

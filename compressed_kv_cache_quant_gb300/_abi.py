@@ -97,7 +97,7 @@ PROTOTYPES = {
     "kv_sparse_layer_decode_ws": (c_size_t, []),
     "kv_mixed_layer_decode": (c_int, [PL, PP, PS, VP, VP, VP, c_int32, c_int32, c_double, c_int32, c_int32, VP, VP,
                                       c_int32, VP, VP, VP, c_size_t, VP]),
-    "kv_mixed_layer_decode_ws": (c_size_t, []),
+    "kv_mixed_layer_decode_ws": (c_size_t, [PL, PS]),
     "kvq_classify_heads": (c_int, [POINTER(ctypes.c_float), c_int32, c_int32, c_int32, c_double, POINTER(c_int32)]),
     "kv_sparse_attn": (c_int, [PL, PP, PS, VP, VP, c_int32, VP, c_int32, VP, VP, VP, c_size_t, VP]),
     "kv_sparse_attn_ws": (c_size_t, [PL, PS, c_int32]),

@@ -269,6 +269,7 @@ struct DPArgs {
     float* P;
     float* S;           // [B][H_q][n_q][ld] log2-domain scores
     int64_t ld;
+    int32_t smem_cap;   // scores the row kernel's shared memory holds (0: every row read from S)
     float* rows;        // [B][H_q][n_q] per-query top-k mass
     int32_t* counters;  // [B][H_q]
     KvqWsHeader* hdr;
@@ -376,14 +377,22 @@ __device__ __forceinline__ float block_reduce_sum(float v, float* red) {
     return r;
 }
 
+// Adds 1 to bin `bin` (< 256; 256 = nothing) of this warp's histogram, equal bins of the warp's
+// lanes combined into one shared-memory atomic.  Called by all 32 lanes.
+__device__ __forceinline__ void dp_hist_add(uint32_t* wh, uint32_t bin) {
+    const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+    if (bin < 256u && (threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1)) atomicAdd(&wh[bin], (uint32_t)__popc(peers));
+}
+
 __global__ void __launch_bounds__(DP_NT) dp_row_kernel(DPArgs a) {
-    extern __shared__ float sc[];  // the row, when it has at most DP_SMEM_T scores
-    __shared__ float redf[DP_NT / 32];
-    __shared__ uint32_t hist[256];
+    extern __shared__ __align__(16) float sc[];  // the row, when it has at most a.smem_cap scores
+    constexpr int NWR = DP_NT / 32;
+    __shared__ float redf[NWR];
+    __shared__ uint32_t hist[NWR][256];  // per-warp digit histograms; hist[0] then holds their sum
     __shared__ uint32_t s_bin, s_above;
     __shared__ float s_kth;
     __shared__ int is_last;
-    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+    const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hq = a.H * a.GQ;
     const int T = a.seq_lens[b];
     const int L = T - a.n_q + i + 1;  // keys seen by query i
@@ -391,41 +400,78 @@ __global__ void __launch_bounds__(DP_NT) dp_row_kernel(DPArgs a) {
     if (T > a.max_len || L <= 0) {
         if (tid == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
     } else {
+        // the row: ld >= L rounded up to 128 floats, 512-byte aligned, so whole float4 groups may be
+        // read past L (their extra lanes are masked)
         const float* row = a.S + (((int64_t)b * Hq + h) * a.n_q + i) * a.ld;
-        const bool in_smem = L <= DP_SMEM_T;
-        if (in_smem) {
-            for (int t = tid; t < L; t += DP_NT) sc[t] = __ldcg(row + t);
-            __syncthreads();
-        }
-        const float* src = in_smem ? sc : row;
-        // max and sum of exp2 in one pass (a running sum rescaled when the running max grows)
+        const int L4 = (L + 3) >> 2;
+        const bool in_smem = L <= a.smem_cap;
+        if (in_smem)
+            for (int t = tid; t < L4; t += DP_NT)
+                reinterpret_cast<float4*>(sc)[t] = __ldcg(reinterpret_cast<const float4*>(row) + t);
+        for (int j = tid; j < NWR * 256; j += DP_NT) (&hist[0][0])[j] = 0u;
+        __syncthreads();
+        const float4* src = reinterpret_cast<const float4*>(in_smem ? sc : row);
+        const int kk = min(a.topk, L);
+        // pass 0: max and sum of exp2 (a running sum rescaled when the running max grows) and the
+        // histogram of the keys' top byte; the loops below walk warp-uniform blocks of 32 float4s
         float mx = -INFINITY, z = 0.0f;
-        for (int t = tid; t < L; t += DP_NT) {
-            const float v = src[t];
-            if (v > mx) {
-                z = fmaf(z, exp2f(mx - v), 1.0f);
-                mx = v;
-            } else {
-                z += exp2f(v - mx);
+        for (int t0 = 32 * warp; t0 < L4; t0 += DP_NT) {
+            const int t4 = t0 + lane;
+            float v[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (t4 < L4) {
+                const float4 x = src[t4];
+                v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool ok = 4 * t4 + e < L;
+                uint32_t bin = 256u;
+                if (ok) {
+                    if (v[e] > mx) {
+                        z = fmaf(z, exp2f(mx - v[e]), 1.0f);
+                        mx = v[e];
+                    } else {
+                        z += exp2f(v[e] - mx);
+                    }
+                    bin = kvq_float_key(v[e]) >> 24;
+                }
+                dp_hist_add(hist[warp], bin);
             }
         }
         const float M = block_reduce_max(mx, redf);
         z = block_reduce_sum(mx == -INFINITY ? 0.0f : z * exp2f(mx - M), redf);
-        const int kk = min(a.topk, L);
-        // radix select of the kk-th largest score
+        // radix select of the kk-th largest key, 8 bits per pass
         uint32_t prefix = 0u, mask = 0u, remaining = (uint32_t)kk;
         for (int pass = 0; pass < 4; ++pass) {
             const int shift = 24 - 8 * pass;
-            for (int j = tid; j < 256; j += DP_NT) hist[j] = 0u;
+            if (pass > 0) {
+                for (int t0 = 32 * warp; t0 < L4; t0 += DP_NT) {
+                    const int t4 = t0 + lane;
+                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (t4 < L4) x = src[t4];
+                    const float v[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t bin = 256u;
+                        if (4 * t4 + e < L) {
+                            const uint32_t key = kvq_float_key(v[e]);
+                            if ((key & mask) == prefix) bin = (key >> shift) & 255u;
+                        }
+                        dp_hist_add(hist[warp], bin);
+                    }
+                }
+            }
             __syncthreads();
-            for (int t = tid; t < L; t += DP_NT) {
-                const uint32_t key = kvq_float_key(src[t]);
-                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            for (int j = tid; j < 256; j += DP_NT) {  // the warps' histograms summed into hist[0]
+                uint32_t tot = 0;
+#pragma unroll
+                for (int w = 0; w < NWR; ++w) tot += hist[w][j];
+                hist[0][j] = tot;
             }
             __syncthreads();
             if (tid < 32) {
                 uint32_t ls = 0;
-                for (int j = 0; j < 8; ++j) ls += hist[255 - 8 * tid - j];
+                for (int j = 0; j < 8; ++j) ls += hist[0][255 - 8 * tid - j];
                 uint32_t incl = ls;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -438,12 +484,12 @@ __global__ void __launch_bounds__(DP_NT) dp_row_kernel(DPArgs a) {
                     uint32_t run = incl - ls;
                     for (int j = 0; j < 8; ++j) {
                         const int bin = 255 - 8 * tid - j;
-                        if (run + hist[bin] >= remaining) {
+                        if (run + hist[0][bin] >= remaining) {
                             s_bin = (uint32_t)bin;
                             s_above = run;
                             break;
                         }
-                        run += hist[bin];
+                        run += hist[0][bin];
                     }
                 }
             }
@@ -451,20 +497,26 @@ __global__ void __launch_bounds__(DP_NT) dp_row_kernel(DPArgs a) {
             remaining -= s_above;
             prefix |= s_bin << shift;
             mask |= 255u << shift;
+            for (int j = tid; j < NWR * 256; j += DP_NT) (&hist[0][0])[j] = 0u;
             __syncthreads();
         }
         // top-k mass: every score above the k-th, plus the k-th value for the remaining slots (every
         // thread that meets the k-th key writes the same value)
         float top = 0.0f;
         uint32_t n_gt = 0;
-        for (int t = tid; t < L; t += DP_NT) {
-            const float v = src[t];
-            const uint32_t key = kvq_float_key(v);
-            if (key > prefix) {
-                top += exp2f(v - M);
-                ++n_gt;
-            } else if (key == prefix) {
-                s_kth = v;
+        for (int t4 = tid; t4 < L4; t4 += DP_NT) {
+            const float4 x = src[t4];
+            const float v[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (4 * t4 + e >= L) break;
+                const uint32_t key = kvq_float_key(v[e]);
+                if (key > prefix) {
+                    top += exp2f(v[e] - M);
+                    ++n_gt;
+                } else if (key == prefix) {
+                    s_kth = v[e];
+                }
             }
         }
         top = block_reduce_sum(top, redf);
@@ -599,7 +651,10 @@ extern "C" int kv_dense_pref_score(const kvq_layout* L, const kvq_pool* P, const
     dp_scores_kernel<<<dim3(tiles, L->n_kv_heads, S->batch), 32 * DPS_NW, smem_q, s>>>(a);
     st = kvq_launch_status(fn);
     if (st) return st;
-    const int smem_row = std::min(std::max(S->max_len, 1), DP_SMEM_T) * (int)sizeof(float);
+    // rows up to DP_SMEM_T scores are reduced in shared memory; when the longest row is longer, no
+    // shared memory is reserved (every row is read from the workspace) so that many rows share an SM
+    a.smem_cap = S->max_len <= DP_SMEM_T ? (std::max(S->max_len, 1) + 3) / 4 * 4 : 0;
+    const int smem_row = a.smem_cap * (int)sizeof(float);
     st = kvq_prepare_kernel((const void*)dp_row_kernel, smem_row);
     if (st) return st;
     dp_row_kernel<<<dim3(n_q, L->n_q_heads, S->batch), DP_NT, smem_row, s>>>(a);

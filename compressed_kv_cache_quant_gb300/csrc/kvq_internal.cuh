@@ -169,6 +169,10 @@ __host__ __device__ static inline void kvq_v_code_pos(int tok, int d, int bits, 
 // memory between launches, and allow `dyn_smem_max` bytes of dynamic shared
 // memory.  Returns KVQ_OK or KVQ_ERR_CUDA.
 int kvq_prepare_kernel(const void* func, int dyn_smem_max);
+// kv_mixed_layer_decode's second launch (kvq_sparse.cu): the dense kv heads' attention over every token
+size_t kvq_dense_heads_attn_ws(const kvq_layout* L, const kvq_seqs* S);
+int kvq_dense_heads_attn(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
+                         const int32_t* dense, float* out, void* ws, cudaStream_t s);
 
 // The code width of a layout (its bits without the KVQ_V_SYMMETRIC flag) and the flag.
 static inline int kvq_code_bits(const kvq_layout* L) { return L->bits & 0xFF; }

@@ -36,6 +36,8 @@ constexpr int H1 = 4096;              // first digit: key bits 31..20
 constexpr int H2 = 1024;              // second and third digits: bits 19..10, 9..0
 constexpr int NHW = NT / 16;          // half-warps (attention: one row per half-warp)
 constexpr int BATCH = 4;              // rows in flight per half-warp
+constexpr int PF_ALL_MAX = 1024;      // kept rows per CTA prefetched to L2 before the attention
+constexpr int PF_AHEAD = 2;           // longer lists: rows prefetched this many batches ahead
 constexpr int REC = 4 + D;
 constexpr uint32_t ROW_NONE = 0xffffffffu;  // attention row ids: no row
 constexpr uint32_t ROW_NEW = 0xfffffffeu;   // the newest token, read from k_new / v_new
@@ -75,6 +77,7 @@ struct SXArgs {
     uint16_t* v16w;
     float* scores_out;       // optional copy of the scores [B][H_q][score_stride]
     const int32_t* dense;    // [B][H_kv] (or NULL): non-zero = the kv head's q heads attend every token
+    int32_t dense_elsewhere; // dense heads: append and list only (their attention is a second launch)
 };
 
 constexpr int CAP_S = 1024;           // kept positions collected per CTA in the one-pass path
@@ -422,6 +425,19 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
             // |q_c| max|K_c|: a product of two fp16 values, exact in fp32; ties -> lower channel
             s.ck[tid] = ((unsigned long long)kvq_float_key(fabsf(qv) * am) << 8) | (unsigned)(255 - tid);
             s.crank[tid] = 0u;
+        }
+        if (dense && a.dense_elsewhere) {
+            // a dense kv head of a mixed layer: appended above; its attention is the second launch.
+            // The ordered selection lists every token: position p at entry p (this CTA's chunk)
+            if (a.sel != nullptr) {
+                int32_t* outl = a.sel + row * a.sel_cap;
+                for (int p = lo + tid; p < hi; p += NT) {
+                    if (p < a.sel_cap) outl[p] = p;
+                    else kvq_dev_flag(a.hdr, KVQ_DEV_OVERFLOW, b);
+                }
+                if (rank == 0 && tid == 0 && a.sel_count != nullptr) a.sel_count[row] = min(T, a.sel_cap);
+            }
+            return;  // uniform over the cluster: no cluster barrier is pending
         }
         for (int i = tid; i < H1; i += NT) s.u.hist[i] = 0u;
         __syncthreads();
@@ -936,13 +952,16 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     const uint16_t* knew_row = a.k_new != nullptr ? a.k_new + ((int64_t)b * a.H + g) * D : nullptr;
     const uint16_t* vnew_row = a.k_new != nullptr ? a.v_new + ((int64_t)b * a.H + g) * D : nullptr;
     uint32_t* rows = const_cast<uint32_t*>(plist);  // positions -> row offsets (in 128-element rows)
+    // a short list (the sparse heads') goes to L2 at once; a long one (a dense head keeps a whole
+    // chunk, megabytes per CTA) a few batches ahead of its use, so that it does not evict itself
+    const bool pf_all = nl <= (uint32_t)PF_ALL_MAX;
     for (int i = (listed ? n_early : 0) + tid; i < (int)nl; i += NT) {
         const int t = (int)plist[i];
         const int32_t page = t == t_new ? 0 : a.bt[(int64_t)b * a.max_blocks + (t >> 4)];
         const uint32_t r = row_of(a, b, g, t, t_new, page);
         rows[i] = r;
         // every kept row goes to L2 now; the batches below then mostly hit L2
-        if (r < ROW_NEW) {
+        if (pf_all && r < ROW_NEW) {
             prefetch_row_l2(a.k16 + (int64_t)r * D);
             prefetch_row_l2(a.v16 + (int64_t)r * D);
         }
@@ -960,6 +979,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = 0.0f;
     for (int it = 0; it < (int)nl; it += NHW * BATCH) {  // bound uniform over the CTA
+        if (!pf_all && l16 < 2 * BATCH) {  // lane: row j = l16 / 2 of this half-warp, K or V
+            const int i = it + PF_AHEAD * NHW * BATCH + (l16 >> 1) * NHW + hw;
+            const uint32_t r = i < (int)nl ? rows[i] : ROW_NONE;
+            if (r < ROW_NEW) prefetch_row_l2(((l16 & 1) ? a.v16 : a.k16) + (int64_t)r * D);
+        }
         uint4 kr[BATCH], vr[BATCH];
         bool ok[BATCH];
 #pragma unroll
@@ -1183,7 +1207,7 @@ static int layer_decode(const char* fn, const kvq_layout* L, const kvq_pool* P, 
     if (st) return st;
     st = kvq_check_seqs(S, fn);
     if (st) return st;
-    st = kvq_check_ws(ws, ws_bytes, kv_sparse_layer_decode_ws(), fn);
+    st = kvq_check_ws(ws, ws_bytes, dense ? kvq_dense_heads_attn_ws(L, S) : kv_sparse_layer_decode_ws(), fn);
     if (st) return st;
     KVQ_REQUIRE(L->bits == 16, KVQ_ERR_INVALID_ARG, "%s: not an fp16 layer", fn);
     KVQ_REQUIRE(P && P->k16 && P->v16 && P->kT && P->k_absmax, KVQ_ERR_INVALID_ARG,
@@ -1238,7 +1262,15 @@ static int layer_decode(const char* fn, const kvq_layout* L, const kvq_pool* P, 
     a.v16w = P->v16;
     a.scores_out = scores;
     a.dense = dense;
-    st = launch(a, S->batch, kvq_stream(stream));
+    a.dense_elsewhere = dense != nullptr;
+    cudaStream_t cs = kvq_stream(stream);
+    st = launch(a, S->batch, cs);
+    if (st) return st;
+    st = kvq_launch_status(fn);
+    if (st || dense == nullptr) return st;
+    // the dense kv heads: every token, the group's q heads sharing each staged tile (stream-ordered
+    // after the first launch, which appended the newest token)
+    st = kvq_dense_heads_attn(L, P, S, q, dense, out, ws, cs);
     if (st) return st;
     return kvq_launch_status(fn);
 }
@@ -1252,7 +1284,11 @@ extern "C" int kv_sparse_layer_decode(const kvq_layout* L, const kvq_pool* P, co
                         scores, score_stride, sel, sel_cap, sel_count, nullptr, out, ws, ws_bytes, stream);
 }
 
-extern "C" size_t kv_mixed_layer_decode_ws(void) { return sizeof(KvqWsHeader); }
+extern "C" size_t kv_mixed_layer_decode_ws(const kvq_layout* L, const kvq_seqs* S) {
+    if (kvq_check_layout(L, "kv_mixed_layer_decode_ws", true) || kvq_check_seqs_sizes(S, "kv_mixed_layer_decode_ws"))
+        return 0;
+    return kvq_dense_heads_attn_ws(L, S);
+}
 
 extern "C" int kv_mixed_layer_decode(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S,
                                      const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q, int32_t n_crit,

@@ -348,6 +348,10 @@ struct SAArgs {
     KvqWsHeader* hdr;
     int32_t n_splits;
     int32_t rps;        // rows per split
+    // dense kv heads of a mixed layer: every token is listed (no sel), and only the kv heads g with
+    // dense[b][g] != 0 are attended (lists per kv head)
+    const int32_t* dense = nullptr;
+    int32_t all_tokens = 0;
 };
 
 template <int NH>
@@ -365,7 +369,8 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
         if (tid == 0 && split == 0) kvq_dev_flag(a.hdr, KVQ_DEV_BAD_LENGTH, b);
         T = a.max_len;
     }
-    int n = a.sel_count[(int64_t)b * n_lists + list];
+    if (a.dense != nullptr && a.dense[(int64_t)b * a.H + g] == 0) return;  // a sparse kv head: not here
+    int n = a.all_tokens ? T : a.sel_count[(int64_t)b * n_lists + list];
     if (n > a.sel_cap || n < 0) {
         if (tid == 0 && split == 0) kvq_dev_flag(a.hdr, KVQ_DEV_OVERFLOW, b);
         n = max(0, min(n, a.sel_cap));
@@ -378,7 +383,7 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
     const int nsplit_b = (n + a.rps - 1) / a.rps;
     if (split >= nsplit_b) return;
     const int r_begin = split * a.rps, r_end = min(n, r_begin + a.rps);
-    const int32_t* ids = a.sel + ((int64_t)b * n_lists + list) * a.sel_cap;
+    const int32_t* ids = a.all_tokens ? nullptr : a.sel + ((int64_t)b * n_lists + list) * a.sel_cap;
 
     // the split's rows: ids and pages resolved up front into row offsets (in 128-element rows;
     // ~0u for a bad id or page), four per thread in flight
@@ -388,7 +393,7 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int i = i0 + u * SA_NT;
-            t[u] = i < r_end ? ids[i] : -1;
+            t[u] = i < r_end ? (ids != nullptr ? ids[i] : i) : -1;
         }
         int32_t pg[4];
 #pragma unroll
@@ -543,31 +548,88 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    // ---- last CTA: merge the splits, write the output and normalize the probabilities
-    __shared__ float fin_m[8], fin_l[8];
-    for (int e = tid; e < NH * D; e += SA_NT) {
-        const int hh = e / D, d = e % D;
-        float M = -INFINITY;
-        for (int sp = 0; sp < nsplit_b; ++sp)
-            M = fmaxf(M, __ldcg(a.part + ((((int64_t)b * n_lists + list) * a.n_splits + sp) * NH + hh) * SA_REC));
-        float L = 0.0f, O = 0.0f;
-        if (M != -INFINITY) {
-            for (int sp = 0; sp < nsplit_b; ++sp) {
-                const float* r = a.part + ((((int64_t)b * n_lists + list) * a.n_splits + sp) * NH + hh) * SA_REC;
-                const float wt = exp2f(__ldcg(r) - M);
-                L = fmaf(__ldcg(r + 1), wt, L);
-                O = fmaf(__ldcg(r + 4 + d), wt, O);
+    // ---- last CTA: merge the splits (in parallel over the splits: the heads' max and sum by block
+    // reductions, each split's weight kept in shared memory, every warp accumulating all outputs
+    // over its share of the splits, the warps' sums added in a fixed order), write the output
+    __shared__ float red_m[SA_NW][NH], red_l[SA_NW][NH];
+    __shared__ float fin_m[NH], fin_l[NH];
+    const float* rec = a.part + ((int64_t)b * n_lists + list) * a.n_splits * NH * SA_REC;  // [split][head]
+    float* wsp = sm;                               // [split][head] weights
+    float* po = sm + ((nsplit_b * NH + 3) & ~3);   // [warp][head * D + d] partial outputs
+    static_assert(NH * D % 32 == 0, "whole warps of outputs");
+    float mh[NH];
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) mh[hh] = -INFINITY;
+    for (int sp = tid; sp < nsplit_b; sp += SA_NT)
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) mh[hh] = fmaxf(mh[hh], __ldcg(rec + (sp * NH + hh) * SA_REC));
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) {
+        float v = mh[hh];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) red_m[warp][hh] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) {
+        float v = red_m[0][hh];
+        for (int w = 1; w < SA_NW; ++w) v = fmaxf(v, red_m[w][hh]);
+        mh[hh] = v;
+    }
+    float lh[NH];
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) lh[hh] = 0.0f;
+    for (int sp = tid; sp < nsplit_b; sp += SA_NT)
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) {
+            const float* r = rec + (sp * NH + hh) * SA_REC;
+            const float w = mh[hh] == -INFINITY ? 0.0f : exp2f(__ldcg(r) - mh[hh]);
+            lh[hh] = fmaf(__ldcg(r + 1), w, lh[hh]);
+            wsp[sp * NH + hh] = w;
+        }
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) {
+        float v = lh[hh];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red_l[warp][hh] = v;
+    }
+    __syncthreads();  // weights and per-warp sums visible
+    {
+        constexpr int NJ = NH * D / 32;  // outputs per lane: e = lane + 32 j
+        float acc[NJ];
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) acc[j] = 0.0f;
+        for (int sp = warp; sp < nsplit_b; sp += SA_NW) {
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const int e = lane + 32 * j, hh = e / D, d = e % D;
+                acc[j] = fmaf(wsp[sp * NH + hh], __ldcg(rec + (sp * NH + hh) * SA_REC + 4 + d), acc[j]);
             }
         }
-        a.out[((int64_t)b * Hq + h0 + hh) * D + d] = L > 0.0f ? O / L : 0.0f;
-        if (d == 0) {
-            fin_m[hh] = M;
-            fin_l[hh] = L;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) po[warp * NH * D + lane + 32 * j] = acc[j];
+    }
+    if (tid < NH) {  // (the max again from the warps' maxima: no register array indexed by tid)
+        float v = 0.0f, m = red_m[0][tid];
+        for (int w = 0; w < SA_NW; ++w) {
+            v += red_l[w][tid];
+            m = fmaxf(m, red_m[w][tid]);
         }
+        fin_m[tid] = m;
+        fin_l[tid] = v;
+    }
+    __syncthreads();
+    for (int e = tid; e < NH * D; e += SA_NT) {
+        const int hh = e / D, d = e % D;
+        float O = 0.0f;
+        for (int w = 0; w < SA_NW; ++w) O += po[w * NH * D + e];
+        const float L = fin_l[hh];
+        a.out[((int64_t)b * Hq + h0 + hh) * D + d] = L > 0.0f ? O / L : 0.0f;
     }
     if (tid == 0) a.counters[(int64_t)b * n_lists + list] = 0;
     if (a.probs == nullptr) return;
-    __syncthreads();
     if (tid < NH) a.fin[(int64_t)b * Hq + h0 + tid] = make_float2(fin_m[tid], fin_l[tid]);
 }
 
@@ -755,6 +817,73 @@ extern "C" int kv_append_critical_score(const kvq_layout* L, const kvq_pool* P, 
     st = launch_crit(a, L, S, kvq_stream(stream));
     if (st) return st;
     return kvq_launch_status("kv_append_critical_score");
+}
+
+// The dense kv heads of a mixed layer (kv_mixed_layer_decode's second launch): exact attention of each
+// dense kv head's q heads over every cached token, lists per kv head with the group's heads sharing
+// each staged K/V tile; sparse kv heads' CTAs return at once.  The workspace is kv_sparse_attn's
+// for sel_cap = max_len.
+// Splits of the all-tokens mode: at most 1024 rows each (a warp then walks at most 16 staged
+// tiles), at least 64 rows
+static SAPlan sa_plan_all(const kvq_seqs* S) {
+    const int cap = std::max(S->max_len, 1);
+    const int rps = std::min(1024, std::max(64, ((cap + 127) / 128 + 63) / 64 * 64));
+    return {(cap + rps - 1) / rps, rps};
+}
+
+static size_t dense_ws_layout(const kvq_layout* L, const kvq_seqs* S, size_t* off_part, size_t* off_cnt, size_t* off_fin) {
+    const SAPlan p = sa_plan_all(S);
+    const int GQ = L->n_q_heads / std::max(L->n_kv_heads, 1);
+    const size_t recs = (size_t)std::max(S->batch, 1) * L->n_kv_heads * p.n_splits * GQ;
+    *off_part = sizeof(KvqWsHeader);
+    *off_cnt = kvq_round_up(*off_part + recs * SA_REC * sizeof(float), 256);
+    *off_fin = kvq_round_up(*off_cnt + (size_t)std::max(S->batch, 1) * L->n_q_heads * sizeof(int32_t), 256);
+    return kvq_round_up(*off_fin + (size_t)std::max(S->batch, 1) * L->n_q_heads * sizeof(float2), 256);
+}
+
+size_t kvq_dense_heads_attn_ws(const kvq_layout* L, const kvq_seqs* S) {
+    size_t a, c, f;
+    return dense_ws_layout(L, S, &a, &c, &f);
+}
+
+int kvq_dense_heads_attn(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
+                         const int32_t* dense, float* out, void* ws, cudaStream_t s) {
+    size_t off_part, off_cnt, off_fin;
+    const int32_t cap = std::max(S->max_len, 1);
+    dense_ws_layout(L, S, &off_part, &off_cnt, &off_fin);
+    const SAPlan p = sa_plan_all(S);
+    SAArgs a;
+    a.k16 = P->k16;
+    a.v16 = P->v16;
+    a.num_blocks = P->num_blocks;
+    a.bt = S->block_table;
+    a.seq_lens = S->seq_lens;
+    a.max_blocks = S->max_blocks;
+    a.max_len = S->max_len;
+    a.H = L->n_kv_heads;
+    a.GQ = L->n_q_heads / L->n_kv_heads;
+    a.q = q;
+    a.sel = nullptr;
+    a.sel_cap = cap;
+    a.sel_count = nullptr;
+    a.per_kv = 1;
+    a.out = out;
+    a.probs = nullptr;
+    a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + off_part);
+    a.counters = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + off_cnt);
+    a.fin = reinterpret_cast<float2*>(static_cast<char*>(ws) + off_fin);
+    a.hdr = static_cast<KvqWsHeader*>(ws);
+    a.n_splits = p.n_splits;
+    a.rps = p.rps;
+    a.dense = dense;
+    a.all_tokens = 1;
+    const dim3 grid(p.n_splits, L->n_kv_heads, S->batch);
+    switch (a.GQ) {
+        case 1: return launch_sa<1>(a, grid, s);
+        case 2: return launch_sa<2>(a, grid, s);
+        case 4: return launch_sa<4>(a, grid, s);
+        default: return launch_sa<8>(a, grid, s);
+    }
 }
 
 extern "C" size_t kv_sparse_attn_ws(const kvq_layout* L, const kvq_seqs* S, int32_t sel_cap) {

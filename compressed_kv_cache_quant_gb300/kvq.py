@@ -285,8 +285,8 @@ def kv_sparse_layer_decode(cache, seqs, k_new, v_new, q, n_crit, k_fixed, ratio,
                                               _p(out), ws.ptr, ws.nbytes, _s(stream)), "kv_sparse_layer_decode")
 
 
-def kv_mixed_layer_decode_ws():
-    return lib().kv_mixed_layer_decode_ws()
+def kv_mixed_layer_decode_ws(cache, seqs):
+    return lib().kv_mixed_layer_decode_ws(_ref(cache.layout), _ref(seqs))
 
 
 def kv_mixed_layer_decode(cache, seqs, k_new, v_new, q, n_crit, k_fixed, ratio, n_sink, window, dense, out, ws,

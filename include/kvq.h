@@ -513,22 +513,26 @@ size_t kv_sparse_layer_decode_ws(void);
 /* ------------------------------------------------------------------------
  * kv_mixed_layer_decode -- kv_sparse_layer_decode for a layer whose heads were
  * classified one by one [TailorKV §6: the layer-level strategy carried down to
- * attention heads; §2.1 dense-preference score]: in the same launch every
- * (sequence, q head) is dispatched by its kv head's class, dense[b][g] (device
- * int32 [batch][H_kv], e.g. from kvq_classify_heads): non-zero -> the head
- * attends every cached token exactly (no critical scores, no selection; a
- * `sel` copy lists every token); zero -> the sparse path of
- * kv_sparse_layer_decode (critical scores, top-K with sinks and window,
- * attention over the selection).  The newest token is appended for every kv
- * head.  Other arguments as kv_sparse_layer_decode (no score copy).
- * ws: kv_mixed_layer_decode_ws() bytes.
+ * attention heads; §2.1 dense-preference score]: every (sequence, q head) is
+ * dispatched on the device by its kv head's class, dense[b][g] (device int32
+ * [batch][H_kv], e.g. from kvq_classify_heads): non-zero -> the head attends
+ * every cached token exactly (no critical scores, no selection; a `sel` copy
+ * lists every token); zero -> the sparse path of kv_sparse_layer_decode
+ * (critical scores, top-K with sinks and window, attention over the
+ * selection).  The newest token is appended for every kv head.  Two launches,
+ * stream-ordered: the cluster launch of kv_sparse_layer_decode, in which a
+ * dense head's clusters only append and list; then the dense kv heads'
+ * attention, the GQ q heads of a kv head sharing every staged K/V tile on the
+ * tensor cores (the CTAs of sparse kv heads return at once).  Other arguments
+ * as kv_sparse_layer_decode (no score copy).
+ * ws: kv_mixed_layer_decode_ws(layout, seqs) bytes.
  * ---------------------------------------------------------------------- */
 int kv_mixed_layer_decode(const kvq_layout* layout, const kvq_pool* pool, const kvq_seqs* seqs,
                           const uint16_t* k_new, const uint16_t* v_new, const uint16_t* q, int32_t n_crit,
                           int32_t k_fixed, double ratio, int32_t n_sink, int32_t window,
                           const int32_t* dense, int32_t* sel, int32_t sel_cap, int32_t* sel_count,
                           float* out, void* ws, size_t ws_bytes, void* stream);
-size_t kv_mixed_layer_decode_ws(void);
+size_t kv_mixed_layer_decode_ws(const kvq_layout* layout, const kvq_seqs* seqs);
 
 /* Head-level classification [TailorKV §6, §2.1], host code: kv head g (of
  * n_kv_heads; its q heads g*G .. g*G+G-1, G = n_q_heads / n_kv_heads) is dense
