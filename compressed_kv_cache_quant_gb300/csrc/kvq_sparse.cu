@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(CS_NT, NHS <= 2 ? CS_MINB : 2) crit_score_kern
 
 // ================================================================ a6 sparse attention
 
-// Tensor-core form: a warp takes 16 listed rows at a time (its own tiles, staged SA_STAGES - 1
+// Tensor-core form: a warp takes 16 listed rows at a time (its own tiles, staged sa_stages(NH) - 1
 // tiles ahead with cp.async).  Scores S^T (heads x 16 rows) = Q K^T with m16n8k16 products: A =
 // the q rows (heads; rows past the group's heads are zero), B = the K tile through ldmatrix.
 // The score accumulators of a head are, element for element, the A fragment of P (heads x rows)
@@ -288,8 +288,11 @@ constexpr int SA_NW = 4;                       // warps per CTA
 constexpr int SA_NT = 32 * SA_NW;
 constexpr int SA_TR = 16;                      // rows per warp tile
 constexpr int SA_TILE = SA_TR * D * 2;         // bytes of one K or V tile (4 KB; a stage holds both)
-constexpr int SA_STAGES = 2;                   // tiles per warp in flight or in use
-constexpr int SA_TILES = SA_NW * SA_STAGES * 2 * SA_TILE;  // [warp][stage][K, V]
+// tiles per warp in flight or in use: three where several q heads share each tile (lists per kv
+// head: fewer CTAs, each tile worth more work), two for one head per list (more CTAs per SM)
+__host__ __device__ constexpr int sa_stages(int nh) { return nh > 1 ? 3 : 2; }
+__host__ __device__ constexpr int sa_tiles(int nh) { return SA_NW * sa_stages(nh) * 2 * SA_TILE; }  // [warp][stage][K, V]
+constexpr int SA_TILES = sa_tiles(1);  // the smaller stage area (the warp states of the merge fit it)
 constexpr int SA_REC = 4 + D;
 constexpr int SA_MAX_RPS = 2048;   // rows per split: their offsets are resolved into shared memory
 
@@ -387,7 +390,8 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
 
     // the split's rows: ids and pages resolved up front into row offsets (in 128-element rows;
     // ~0u for a bad id or page), four per thread in flight
-    uint32_t* roff = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(sm) + SA_TILES);
+    constexpr int SA_STAGES = sa_stages(NH);
+    uint32_t* roff = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(sm) + sa_tiles(NH));
     for (int i0 = r_begin + tid; i0 < r_end; i0 += 4 * SA_NT) {
         int t[4];
 #pragma unroll
@@ -685,9 +689,9 @@ size_t sa_ws_layout(const kvq_layout* L, const kvq_seqs* S, int32_t sel_cap, siz
 template <int NH>
 int launch_sa(const SAArgs& a, dim3 grid, cudaStream_t s) {
     static_assert((size_t)SA_NW * 8 * SA_REC * sizeof(float) <= (size_t)SA_TILES, "the warp states fit the tiles");
-    const size_t smem = (size_t)SA_TILES + (size_t)a.rps * sizeof(uint32_t);
+    const size_t smem = (size_t)sa_tiles(NH) + (size_t)a.rps * sizeof(uint32_t);
     const int st = kvq_prepare_kernel((const void*)sparse_attn_kernel<NH>,
-                                      (int)((size_t)SA_TILES + SA_MAX_RPS * sizeof(uint32_t)));
+                                      (int)((size_t)sa_tiles(NH) + SA_MAX_RPS * sizeof(uint32_t)));
     if (st) return st;
     sparse_attn_kernel<NH><<<grid, SA_NT, smem, s>>>(a);
     return kvq_launch_status("kv_sparse_attn");
