@@ -174,3 +174,58 @@ def test_classify_heads_matches_the_oracle(lib):
             assert got == [int(x) for x in O.classify_heads(P.astype(np.float64), 32, 0.2, Hkv)]
     assert kvq.kvq_classify_heads([8.0, 8.0], 2, 1, 32, 0.25) == [0]      # equal: not above
     assert lib.kvq_classify_heads(None, 2, 1, 32, 0.2, None) == _abi.KVQ_ERR_INVALID_ARG
+
+
+def test_outlier_and_dense_pref_validation(lib):
+    """The outlier-isolation entries, the mixed layer's and the dense-preference workspace sizes:
+    bad arguments rejected on the host before any launch."""
+    by = ctypes.byref
+    L4 = kvq.make_layout(8, 2, 4, 32)
+    L2 = kvq.make_layout(8, 2, 2, 64)
+    S = _abi.Seqs(None, None, 0, 8, 100, 0)
+    fake = 1 << 20            # a 16-byte aligned non-NULL address: never dereferenced by these checks
+    ws = lib.kv_outlier_channels_ws(by(L4))
+    assert ws == 256 + 2 * 4 * 128 * 8
+    H, d = 2, 128
+    for n_out in (0, 9):
+        assert lib.kv_outlier_channels(by(L4), fake, 10, H * d, n_out, fake, None, fake, ws, None) \
+            == _abi.KVQ_ERR_INVALID_ARG
+    assert lib.kv_outlier_channels(by(L4), fake, (1 << 22) + 1, H * d, 1, fake, None, fake, ws, None) \
+        == _abi.KVQ_ERR_INVALID_ARG
+    assert lib.kv_outlier_channels(by(L4), fake, 10, H * d - 8, 1, fake, None, fake, ws, None) \
+        == _abi.KVQ_ERR_INVALID_ARG
+    assert lib.kv_outlier_channels(by(L4), fake + 8, 10, H * d, 1, fake, None, fake, ws, None) \
+        == _abi.KVQ_ERR_INVALID_ARG                                   # k not 16-byte aligned
+    assert lib.kv_outlier_channels(by(L4), fake, 10, H * d, 1, fake, None, fake, ws - 8, None) \
+        == _abi.KVQ_ERR_INVALID_ARG                                   # workspace too small
+    P = _abi.Pool(8, 1, 0, fake, fake, fake, fake, fake, None, None, None, None)
+    # isolation and the outlier attention: 4- and 8-bit layers only, 1 <= n_out <= 8
+    assert lib.kv_outlier_isolate(by(L2), by(P), by(S), 0, 0, 64, fake, H * d, 1, fake, fake, None) \
+        == _abi.KVQ_ERR_UNSUPPORTED
+    assert lib.kv_outlier_isolate(by(L4), by(P), by(S), 0, 0, 64, fake, H * d, 9, fake, fake, None) \
+        == _abi.KVQ_ERR_INVALID_ARG
+    S0 = _abi.Seqs(None, None, 0, 0, 0, 0)
+    wa = lib.kv_decode_attn_quant_ws(by(L4), by(S0))
+    assert lib.kv_decode_attn_quant_outlier(by(L2), by(P), by(S0), fake, 1, fake, fake, fake, fake, wa, None) \
+        == _abi.KVQ_ERR_UNSUPPORTED
+    assert lib.kv_decode_attn_quant_outlier(by(L4), by(P), by(S0), fake, 9, fake, fake, fake, fake, wa, None) \
+        == _abi.KVQ_ERR_INVALID_ARG
+    assert lib.kv_decode_attn_quant_outlier(by(L4), by(P), by(S0), fake, 1, fake, None, fake, fake, wa, None) \
+        == _abi.KVQ_ERR_INVALID_ARG                                   # NULL k_out
+    assert lib.kv_decode_attn_quant_outlier(by(L4), by(P), by(S0), fake, 1, fake, fake + 8, fake, fake, wa, None) \
+        == _abi.KVQ_ERR_INVALID_ARG                                   # k_out not 16-byte aligned
+    # the mixed layer's workspace holds the dense kv heads' split records; the dense-preference
+    # workspace holds the score matrix (batch x H_q x n_q x max_len rounded up to 128, fp32)
+    L16 = kvq.make_layout(32, 8, 16)
+    S1 = _abi.Seqs(None, None, 1, 8200, 131136, 0)
+    m = lib.kv_mixed_layer_decode_ws(by(L16), by(S1))
+    assert m % 256 == 0 and m > 8 * 128 * 4 * (4 + 128) * 4
+    n = lib.kv_dense_pref_score_ws(by(L16), by(S1), 32)
+    assert n % 256 == 0 and n >= 32 * 32 * 131200 * 4
+    # (q heads per kv head) x n_q above 512 rows: not supported
+    Lw = kvq.make_layout(32, 2, 16)
+    S2 = _abi.Seqs(None, None, 1, 64, 1024, 0)
+    Pk = _abi.Pool(64, 1, 1024, None, None, None, None, None, fake, fake, None, None)
+    nw = lib.kv_dense_pref_score_ws(by(Lw), by(S2), 64)
+    assert lib.kv_dense_pref_score(by(Lw), by(Pk), by(S2), fake, 64, 8, fake, fake, nw, None) \
+        == _abi.KVQ_ERR_UNSUPPORTED
