@@ -293,6 +293,23 @@ def make_pool(n):
 
 # ------------------------------------------------------------------------ main
 
+def rank_max_ms(ms, world, device):
+    """The job's time for one timed region: the slowest rank's (an all-reduce MAX over the ranks of
+    the process group); with one rank, its own."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_steps_per_s(world, steps, ms):
+    """Whole-job throughput of replicas: the steps every rank ran, over the slowest rank's time."""
+    return world * steps / (ms * 1e-3)
+
+
 def traffic_record(kernel):
     """ncu DRAM bytes per launch for `kernel`, if taken on the current source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -405,10 +422,8 @@ def main():
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     clk = clocks.stop()
+    ms = rank_max_ms(ms, world, device)
     if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     ms_per_step = ms / args.steps
     T_mid = args.prompt + step_i - args.steps // 2
@@ -467,10 +482,10 @@ def main():
                 g_step.replay()
                 hout.copy_(W.out, non_blocking=True)
         stream.synchronize()
-        t_e2e = time.perf_counter() - t0
+        t_e2e = rank_max_ms(1e3 * (time.perf_counter() - t0), world, device) * 1e-3
         step_i += args.steps
         bi = (W.in_q.numel() + W.in_k.numel() + W.in_v.numel()) * 2
-        e2e = {"value": world * args.steps / t_e2e, "unit": "steps/s", "h2d_bytes_per_step": bi,
+        e2e = {"value": job_steps_per_s(world, args.steps, t_e2e * 1e3), "unit": "steps/s", "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": W.out.numel() * 4}
 
     # ---- CPU oracle baseline (rank 0, bounded sample of the same workload)
@@ -499,7 +514,7 @@ def main():
         rows = run_rows(device, stream)
 
     if rank == 0:
-        value = world * args.steps / (ms * 1e-3)
+        value = job_steps_per_s(world, args.steps, ms)
         line = {
             "metric": "decode-attention steps/s (compressed KV, 128K context)",
             "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
