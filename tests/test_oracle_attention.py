@@ -85,7 +85,7 @@ def test_quant_attention_within_perturbation_bound(T, bits):
 
 @pytest.mark.parametrize("T", [64, 100, 257, 1000])
 def test_sixteen_bit_quant_attention_reduces_to_dense(T):
-    """The benchmark spec / TailorKV §2.2: at b=16 the quantized decode attention
+    """TailorKV §2.2 (quantization at b bits): at b=16 the quantized decode attention
     reduces to dense fp16 attention: the residual error, left by the fp16
     rounding of the stored scale, is below 2e-3 of the value range max|v|
     and at least 5x below the b=8 error.  (The output of random-data
