@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(HA_NT) h2o_kernel(H2OArgs a) {
 // every pass (no length limit).
 
 constexpr int DP_NT = 256;
-constexpr int DP_SMEM_T = 49152;         // rows up to this length are reduced in shared memory
+constexpr int DP_SMEM_T = 40960;         // rows up to this length are reduced in shared memory
 constexpr int DPS_NW = 8;                // warps of the scores kernel: one 16-token page each
 constexpr int DPS_TILE = DPS_NW * PG;    // tokens per scores CTA
 constexpr int DPS_QLD = D + 16;          // padded query row in shared memory (halves, 288 bytes)
@@ -377,20 +377,64 @@ __device__ __forceinline__ float block_reduce_sum(float v, float* red) {
     return r;
 }
 
-// Adds 1 to bin `bin` (< 256; 256 = nothing) of this warp's histogram, equal bins of the warp's
-// lanes combined into one shared-memory atomic.  Called by all 32 lanes.
-__device__ __forceinline__ void dp_hist_add(uint32_t* wh, uint32_t bin) {
+// Adds 1 to bin `bin` of the histogram h (bin >= nb: nothing), equal bins of the warp's lanes
+// combined into one shared-memory atomic.  Called by all 32 lanes.
+__device__ __forceinline__ void dp_hist_add(uint32_t* h, uint32_t bin, uint32_t nb) {
     const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-    if (bin < 256u && (threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1)) atomicAdd(&wh[bin], (uint32_t)__popc(peers));
+    if (bin < nb && (threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1)) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+}
+
+// The float whose order-preserving key is k (kvq_float_key; -0 reads as +0)
+__device__ __forceinline__ float dp_key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+constexpr int DP_H1 = 2048;       // first digit: the keys' top 11 bits
+constexpr int DP_CAND = 6144;     // scores of the k-th key's first-digit bin kept in shared memory
+
+// Over nb bins (a multiple of DP_NT: nb / DP_NT consecutive bins per thread, thread 0 the highest),
+// finds from the top the bin holding the `remaining`-th largest element: *bin, and *above = the
+// count in the higher bins.  Called by the whole CTA; ends with a barrier.
+__device__ __forceinline__ void dp_find_bin(const uint32_t* h, int nb, uint32_t remaining, uint32_t* bin,
+                                            uint32_t* above, uint32_t* wsum) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = nb / DP_NT;                 // bins per thread, thread 0 the highest
+    const int top = nb - per * tid;             // this thread's bins: top - per .. top - 1
+    uint32_t mine = 0;
+    for (int j = 0; j < per; ++j) mine += h[top - 1 - j];
+    uint32_t x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += wsum[w];
+    uint32_t run = before + x - mine;           // the count above this thread's bins
+    if (run < remaining && run + mine >= remaining) {
+        for (int j = 0; j < per; ++j) {
+            const uint32_t c = h[top - 1 - j];
+            if (run + c >= remaining) {
+                *bin = (uint32_t)(top - 1 - j);
+                *above = run;
+                break;
+            }
+            run += c;
+        }
+    }
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(DP_NT) dp_row_kernel(DPArgs a) {
     extern __shared__ __align__(16) float sc[];  // the row, when it has at most a.smem_cap scores
     constexpr int NWR = DP_NT / 32;
     __shared__ float redf[NWR];
-    __shared__ uint32_t hist[NWR][256];  // per-warp digit histograms; hist[0] then holds their sum
-    __shared__ uint32_t s_bin, s_above;
-    __shared__ float s_kth;
+    __shared__ uint32_t wsum[NWR];
+    __shared__ uint32_t hist[DP_H1];             // digit histograms (2048 bins, then 256)
+    __shared__ float cand[DP_CAND];              // the first-digit bin's scores
+    __shared__ uint32_t s_bin, s_above, n_cand;
     __shared__ int is_last;
     const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hq = a.H * a.GQ;
@@ -408,12 +452,13 @@ __global__ void __launch_bounds__(DP_NT) dp_row_kernel(DPArgs a) {
         if (in_smem)
             for (int t = tid; t < L4; t += DP_NT)
                 reinterpret_cast<float4*>(sc)[t] = __ldcg(reinterpret_cast<const float4*>(row) + t);
-        for (int j = tid; j < NWR * 256; j += DP_NT) (&hist[0][0])[j] = 0u;
+        for (int j = tid; j < DP_H1; j += DP_NT) hist[j] = 0u;
+        if (tid == 0) n_cand = 0u;
         __syncthreads();
         const float4* src = reinterpret_cast<const float4*>(in_smem ? sc : row);
         const int kk = min(a.topk, L);
-        // pass 0: max and sum of exp2 (a running sum rescaled when the running max grows) and the
-        // histogram of the keys' top byte; the loops below walk warp-uniform blocks of 32 float4s
+        // pass 1: max and sum of exp2 (a running sum rescaled when the running max grows) and the
+        // histogram of the keys' top 11 bits; the loops walk warp-uniform blocks of 32 float4s
         float mx = -INFINITY, z = 0.0f;
         for (int t0 = 32 * warp; t0 < L4; t0 += DP_NT) {
             const int t4 = t0 + lane;
@@ -424,27 +469,65 @@ __global__ void __launch_bounds__(DP_NT) dp_row_kernel(DPArgs a) {
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const bool ok = 4 * t4 + e < L;
-                uint32_t bin = 256u;
-                if (ok) {
+                uint32_t bin = DP_H1;
+                if (4 * t4 + e < L) {
                     if (v[e] > mx) {
                         z = fmaf(z, exp2f(mx - v[e]), 1.0f);
                         mx = v[e];
                     } else {
                         z += exp2f(v[e] - mx);
                     }
-                    bin = kvq_float_key(v[e]) >> 24;
+                    bin = kvq_float_key(v[e]) >> 21;
                 }
-                dp_hist_add(hist[warp], bin);
+                dp_hist_add(hist, bin, DP_H1);
             }
         }
         const float M = block_reduce_max(mx, redf);
-        z = block_reduce_sum(mx == -INFINITY ? 0.0f : z * exp2f(mx - M), redf);
-        // radix select of the kk-th largest key, 8 bits per pass
-        uint32_t prefix = 0u, mask = 0u, remaining = (uint32_t)kk;
-        for (int pass = 0; pass < 4; ++pass) {
-            const int shift = 24 - 8 * pass;
-            if (pass > 0) {
+        z = block_reduce_sum(mx == -INFINITY ? 0.0f : z * exp2f(mx - M), redf);  // (synchronizes)
+        dp_find_bin(hist, DP_H1, (uint32_t)kk, &s_bin, &s_above, wsum);
+        const uint32_t b1 = s_bin;
+        const uint32_t rem1 = (uint32_t)kk - s_above;  // still to take from bin b1
+        // pass 2: the mass of the bins above b1; bin b1's scores into the candidate buffer
+        float top = 0.0f;
+        for (int t0 = 32 * warp; t0 < L4; t0 += DP_NT) {
+            const int t4 = t0 + lane;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t4 < L4) x = src[t4];
+            const float v[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool ok = 4 * t4 + e < L;
+                const uint32_t bin = ok ? kvq_float_key(v[e]) >> 21 : 0u;
+                if (ok && bin > b1) top += exp2f(v[e] - M);
+                const bool c = ok && bin == b1;
+                const uint32_t bal = __ballot_sync(0xffffffffu, c);
+                uint32_t base = 0;
+                if (lane == 0 && bal != 0u) base = atomicAdd(&n_cand, (uint32_t)__popc(bal));
+                base = __shfl_sync(0xffffffffu, base, 0) + (uint32_t)__popc(bal & ((1u << lane) - 1u));
+                if (c && base < (uint32_t)DP_CAND) cand[base] = v[e];
+            }
+        }
+        for (int j = tid; j < DP_H1; j += DP_NT) hist[j] = 0u;
+        __syncthreads();
+        // the low 21 bits of the k-th key among bin b1's scores: digits of 8, 8 and 5 bits over the
+        // candidate buffer, or, if it overflowed (more than DP_CAND equal top bits), over the row
+        const uint32_t nc = n_cand;
+        const bool in_buf = nc <= (uint32_t)DP_CAND;
+        uint32_t prefix = b1 << 21, mask = 0xffe00000u, remaining = rem1;
+        for (int pass = 0; pass < 3; ++pass) {
+            const int shift = pass == 0 ? 13 : pass == 1 ? 5 : 0;
+            const uint32_t dm = pass == 2 ? 31u : 255u;
+            if (in_buf) {
+                for (int j0 = 32 * warp; j0 < (int)nc; j0 += DP_NT) {
+                    const int j = j0 + lane;
+                    uint32_t bin = 256u;
+                    if (j < (int)nc) {
+                        const uint32_t key = kvq_float_key(cand[j]);
+                        if ((key & mask) == prefix) bin = (key >> shift) & dm;
+                    }
+                    dp_hist_add(hist, bin, 256u);
+                }
+            } else {
                 for (int t0 = 32 * warp; t0 < L4; t0 += DP_NT) {
                     const int t4 = t0 + lane;
                     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -455,73 +538,50 @@ __global__ void __launch_bounds__(DP_NT) dp_row_kernel(DPArgs a) {
                         uint32_t bin = 256u;
                         if (4 * t4 + e < L) {
                             const uint32_t key = kvq_float_key(v[e]);
-                            if ((key & mask) == prefix) bin = (key >> shift) & 255u;
+                            if ((key & mask) == prefix) bin = (key >> shift) & dm;
                         }
-                        dp_hist_add(hist[warp], bin);
+                        dp_hist_add(hist, bin, 256u);
                     }
                 }
             }
             __syncthreads();
-            for (int j = tid; j < 256; j += DP_NT) {  // the warps' histograms summed into hist[0]
-                uint32_t tot = 0;
-#pragma unroll
-                for (int w = 0; w < NWR; ++w) tot += hist[w][j];
-                hist[0][j] = tot;
-            }
-            __syncthreads();
-            if (tid < 32) {
-                uint32_t ls = 0;
-                for (int j = 0; j < 8; ++j) ls += hist[0][255 - 8 * tid - j];
-                uint32_t incl = ls;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (tid >= o) incl += y;
-                }
-                const uint32_t ballot = __ballot_sync(0xffffffffu, incl >= remaining);
-                const int l = __ffs(ballot) - 1;
-                if (tid == l) {
-                    uint32_t run = incl - ls;
-                    for (int j = 0; j < 8; ++j) {
-                        const int bin = 255 - 8 * tid - j;
-                        if (run + hist[0][bin] >= remaining) {
-                            s_bin = (uint32_t)bin;
-                            s_above = run;
-                            break;
-                        }
-                        run += hist[0][bin];
-                    }
-                }
-            }
-            __syncthreads();
+            dp_find_bin(hist, 256, remaining, &s_bin, &s_above, wsum);
             remaining -= s_above;
             prefix |= s_bin << shift;
-            mask |= 255u << shift;
-            for (int j = tid; j < NWR * 256; j += DP_NT) (&hist[0][0])[j] = 0u;
+            mask |= dm << shift;
+            for (int j = tid; j < 256; j += DP_NT) hist[j] = 0u;
             __syncthreads();
         }
-        // top-k mass: every score above the k-th, plus the k-th value for the remaining slots (every
-        // thread that meets the k-th key writes the same value)
-        float top = 0.0f;
-        uint32_t n_gt = 0;
-        for (int t4 = tid; t4 < L4; t4 += DP_NT) {
-            const float4 x = src[t4];
-            const float v[4] = {x.x, x.y, x.z, x.w};
+        // prefix is the k-th key: bin b1's scores above it join the mass, and the k-th value fills
+        // the slots left (ties at the k-th key)
+        float top2 = 0.0f;
+        uint32_t n_gt2 = 0;
+        if (in_buf) {
+            for (int j = tid; j < (int)nc; j += DP_NT) {
+                const float v = cand[j];
+                if (kvq_float_key(v) > prefix) {
+                    top2 += exp2f(v - M);
+                    ++n_gt2;
+                }
+            }
+        } else {
+            for (int t4 = tid; t4 < L4; t4 += DP_NT) {
+                const float4 x = src[t4];
+                const float v[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (4 * t4 + e >= L) break;
-                const uint32_t key = kvq_float_key(v[e]);
-                if (key > prefix) {
-                    top += exp2f(v[e] - M);
-                    ++n_gt;
-                } else if (key == prefix) {
-                    s_kth = v[e];
+                for (int e = 0; e < 4; ++e) {
+                    if (4 * t4 + e >= L) break;
+                    const uint32_t key = kvq_float_key(v[e]);
+                    if ((key >> 21) == b1 && key > prefix) {
+                        top2 += exp2f(v[e] - M);
+                        ++n_gt2;
+                    }
                 }
             }
         }
-        top = block_reduce_sum(top, redf);
-        n_gt = (uint32_t)block_reduce_sum((float)n_gt, redf);  // (block_reduce_sum synchronizes)
-        top += (float)(kk - (int)n_gt) * exp2f(s_kth - M);
+        top = block_reduce_sum(top + top2, redf);
+        n_gt2 = (uint32_t)block_reduce_sum((float)n_gt2, redf);
+        top += (float)(rem1 - n_gt2) * exp2f(dp_key_float(prefix) - M);
         r_i = top / z;
     }
     // per-query mass -> workspace; the last CTA of (b, h) forms P = n_q - sum_i r_i
