@@ -312,9 +312,14 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), OUT && BITS == 4 ? 6 : 
     // q of head h at channel c_j (fp16, exact), A the staged fp16 outlier keys of the tokens
     uint32_t ob0 = 0u;
     bool has0 = false, has1 = false;
+    int oj0 = 0, oj1 = 0;       // the lane's two k slots, clamped into the row (branch-free loads)
+    uint32_t omask = 0u;        // the halves of the A register that are real slots
     if constexpr (OUT) {
         has0 = 2 * q4 < a.n_out;
         has1 = 2 * q4 + 1 < a.n_out;
+        oj0 = min(2 * q4, a.n_out - 1);
+        oj1 = min(2 * q4 + 1, a.n_out - 1);
+        omask = (has0 ? 0x0000ffffu : 0u) | (has1 ? 0xffff0000u : 0u);
         float qlo = 0.0f, qhi = 0.0f;
         const int32_t* chs = a.out_ch + ((int64_t)b * a.H + gk) * a.n_out;
         const int c0 = has0 ? chs[2 * q4] : 0, c1 = has1 ? chs[2 * q4 + 1] : 0;
@@ -345,6 +350,7 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), OUT && BITS == 4 ? 6 : 
         const GroupStage<BITS>& st = S.u.st[warp][buf];
         const int t0 = gi * KG;
         const bool packed = gi < n_full;
+        [[maybe_unused]] const uint16_t* kob = OUT ? ko_of(buf) + g8 * a.n_out : nullptr;  // outlier keys, row g8
 
         // ---- A fragments: slot 2h holds fp16(q_h,c scale_c), slot 2h + 1 the fp16 remainder;
         // register 2s + i covers channels 16s + 8i + 2r + {0, 1} of fragment column r
@@ -419,13 +425,10 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), OUT && BITS == 4 ? 6 : 
                 KVQ_KSTEP(7);
 #undef KVQ_KSTEP
                 if constexpr (OUT) {  // the outlier channels of tokens 16mt + g8 (+ 8): exact fp16 keys
-                    uint32_t oa0 = 0u, oa1 = 0u;
-                    if (has0) {
-                        const uint16_t* kr = ko_of(buf) + (16 * mt + g8) * a.n_out + 2 * q4;
-                        const uint16_t* kr8 = kr + 8 * a.n_out;
-                        oa0 = (uint32_t)kr[0] | (has1 ? (uint32_t)kr[1] << 16 : 0u);
-                        oa1 = (uint32_t)kr8[0] | (has1 ? (uint32_t)kr8[1] << 16 : 0u);
-                    }
+                    const uint16_t* kr = kob + 16 * mt * a.n_out;  // row 16mt + g8 of the stage
+                    const uint16_t* kr8 = kr + 8 * a.n_out;
+                    const uint32_t oa0 = prmt(kr[oj0], kr[oj1], 0x5410u) & omask;
+                    const uint32_t oa1 = prmt(kr8[oj0], kr8[oj1], 0x5410u) & omask;
                     mma16816(d, oa0, oa1, 0u, 0u, ob0, 0u);
                 }
             } else {
