@@ -5,7 +5,11 @@
  * asymmetric b-bit packing, paged 16-token blocks, fused dequant attention,
  * the sparse-layer path (critical-channel scores, top-K with sinks and a
  * recent window, exact attention over the selection), the H2O cumulative
- * score update and the dense-preference layer score.
+ * score update and the dense-preference layer score; and around it the
+ * host-link gather of offloaded rows, block-granular and GQA-shared
+ * selection, a layer whose kv heads are classified one by one (dense or
+ * sparse), isolated fp16 outlier key channels beside a quantized cache, an
+ * FP8 E4M3 cache and symmetric V quantization.
  *
  * Sources cited below (page, then section):
  *   [TailorKV]  "TailorKV" article, ijyty.com/news/1204784
@@ -37,7 +41,10 @@
  *     read.  Two calls that share a workspace must not run concurrently.
  *   - Data-dependent device errors (a page id outside the pool, a selected id
  *     outside the sequence) skip the faulty access and set a status word in
- *     the workspace; kvq_check() reads and clears it.  Nothing traps.
+ *     the workspace; kvq_check() reads and clears it.  Nothing traps, and no
+ *     kernel waits on another CTA's flag: the only waits are bounded waits for
+ *     a kernel's own asynchronous copies, which on expiry set the status word
+ *     (KVQ_ERR_DEVICE_CHECK from kvq_check, "a bounded wait ... gave up").
  */
 #ifndef KVQ_H
 #define KVQ_H
