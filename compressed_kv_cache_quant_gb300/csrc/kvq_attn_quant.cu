@@ -599,6 +599,7 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), OUT && BITS == 4 ? 6 : 
 // column 2h of both products (odd columns zero), as in the code kernel above.
 
 constexpr int F8_NW = 12;                 // warps per CTA (one CTA per SM)
+constexpr int F8_NS = 2;                  // stages per warp (F8_NS - 1 steps in flight ahead of the one in use)
 constexpr int F8_PAGE = PG * D;           // bytes of one page of one kv head (2 KB)
 constexpr int F8_STAGE = 4 * F8_PAGE;     // K page 0, K page 1, V page 0, V page 1
 constexpr uint32_t F8_SPIN = 1u << 16;    // bound on the polls of one mbarrier wait
@@ -606,10 +607,10 @@ constexpr uint32_t F8_SPIN = 1u << 16;    // bound on the polls of one mbarrier 
 template <int GQ>
 struct F8Smem {
     union alignas(16) {
-        uint8_t st[F8_NW][2][F8_STAGE];   // per warp: two stages
+        uint8_t st[F8_NW][F8_NS][F8_STAGE];  // per warp: F8_NS stages
         float ro[F8_NW][GQ][D];           // per warp: unnormalised outputs, after the last step
     } u;
-    unsigned long long bar[F8_NW][2];     // one mbarrier per stage (one arrival + the copied bytes)
+    unsigned long long bar[F8_NW][F8_NS];  // one mbarrier per stage (one arrival + the copied bytes)
     float m[F8_NW][GQ], l[F8_NW][GQ];
 };
 
@@ -665,8 +666,9 @@ __global__ void __launch_bounds__(32 * F8_NW, 1) f8_attn_kernel(QAttnArgs a) {
     const int gk = gv / a.kv_div;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, q4 = lane & 3;
-    if (tid < 2 * F8_NW) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(f8_saddr(&S.bar[tid >> 1][tid & 1])) : "memory");
+    if (tid < F8_NS * F8_NW) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(f8_saddr(&S.bar[tid / F8_NS][tid % F8_NS]))
+                     : "memory");
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
@@ -734,15 +736,18 @@ __global__ void __launch_bounds__(32 * F8_NW, 1) f8_attn_kernel(QAttnArgs a) {
     };
 
     int it = 0;
-    if (lane == 0 && hb + warp < he) issue(hb + warp, 0);
+    if (lane == 0)
+        for (int k = 0; k < F8_NS - 1; ++k)
+            if (hb + warp + k * F8_NW < he) issue(hb + warp + k * F8_NW, k);
     for (int j = hb + warp; j < he; j += F8_NW, ++it) {
-        const int stg = it & 1;
-        if (lane == 0 && j + F8_NW < he) {
-            // the other stage was read in the previous step (ordered by the __syncwarp that ended it)
+        const int stg = it % F8_NS;
+        const int ahead = j + (F8_NS - 1) * F8_NW;
+        if (lane == 0 && ahead < he) {
+            // that stage was read in the previous step (ordered by the __syncwarp that ended it)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(j + F8_NW, stg ^ 1);
+            issue(ahead, (it + F8_NS - 1) % F8_NS);
         }
-        if (!__all_sync(0xffffffffu, f8_wait(&S.bar[warp][stg], (uint32_t)(it >> 1) & 1u))) {  // warp-uniform
+        if (!__all_sync(0xffffffffu, f8_wait(&S.bar[warp][stg], (uint32_t)(it / F8_NS) & 1u))) {  // warp-uniform
             if (lane == 0) kvq_dev_flag(a.hdr, KVQ_DEV_TIMEOUT, b);
             ok_run = false;
             break;
@@ -831,10 +836,9 @@ __global__ void __launch_bounds__(32 * F8_NW, 1) f8_attn_kernel(QAttnArgs a) {
     }
     if (!ok_run && lane == 0) {
         // a wait that gave up: wait (bounded) for this warp's copies still in flight before the stage
-        // memory goes away (the step it waited for, and the next one if it was issued)
-        const int stg = it & 1;
-        f8_wait(&S.bar[warp][stg], (uint32_t)(it >> 1) & 1u);
-        if (hb + warp + (it + 1) * F8_NW < he) f8_wait(&S.bar[warp][stg ^ 1], (uint32_t)((it + 1) >> 1) & 1u);
+        // memory goes away (the step it waited for, and the ones issued after it)
+        for (int k = it; k < it + F8_NS; ++k)
+            if (hb + warp + k * F8_NW < he) f8_wait(&S.bar[warp][k % F8_NS], (uint32_t)(k / F8_NS) & 1u);
     }
 
     // ---- this warp's state per head
