@@ -112,6 +112,7 @@ PROTOTYPES = {
     "kv_page_copy": (c_int, [PL, PP, c_int32, c_int32, VP]),
     "kvq_check": (c_int, [VP, VP]),
     "kvq_read_path_counters": (c_int, [VP, POINTER(c_uint32), VP]),
+    "kvq_selftest_bounded_wait": (c_int, [VP, c_size_t, VP]),
     "kvq_alloc_create": (VP, [c_int64, c_uint64]),
     "kvq_alloc_destroy": (None, [VP]),
     "kvq_block_alloc": (c_int, [VP, c_int32, POINTER(c_int32)]),

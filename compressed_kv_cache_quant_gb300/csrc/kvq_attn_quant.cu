@@ -1042,6 +1042,17 @@ int launch_bits(int gq, dim3 grid, cudaStream_t s, QAttnArgs& a) {
     }
 }
 
+// The bounded wait of the E4M3 kernel (f8_wait) on an mbarrier that nothing completes: one arrival
+// is expected and none is made, so the phase never ends and the wait must give up.  Records
+// KVQ_DEV_TIMEOUT, then returns: the diagnostic of kvq_selftest_bounded_wait.
+__global__ void __launch_bounds__(32) f8_wait_selftest_kernel(KvqWsHeader* hdr) {
+    __shared__ __align__(8) unsigned long long bar;
+    if (threadIdx.x == 0) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(f8_saddr(&bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, f8_wait(&bar, 0u)) && threadIdx.x == 0) kvq_dev_flag(hdr, KVQ_DEV_TIMEOUT, 0);
+}
+
 }  // namespace
 
 extern "C" size_t kv_decode_attn_quant_ws(const kvq_layout* L, const kvq_seqs* S) {
@@ -1199,6 +1210,14 @@ static int qattn_scratch(void** out) {
 }
 
 extern "C" size_t kv_decode_attn_quant_noalloc_max_scratch(void) { return KVQ_NOALLOC_SCRATCH_BYTES; }
+
+extern "C" int kvq_selftest_bounded_wait(void* ws, size_t ws_bytes, void* stream) {
+    kvq_clear_error();
+    int st = kvq_check_ws(ws, ws_bytes, sizeof(KvqWsHeader), "kvq_selftest_bounded_wait");
+    if (st) return st;
+    f8_wait_selftest_kernel<<<1, 32, 0, kvq_stream(stream)>>>(static_cast<KvqWsHeader*>(ws));
+    return kvq_launch_status("kvq_selftest_bounded_wait");
+}
 
 static int noalloc_plan(const kvq_layout* L, const kvq_seqs* S, Plan* p, size_t* need, size_t* off_part,
                         size_t* off_cnt) {

@@ -390,6 +390,11 @@ def kvq_check(ws, stream=None):
     return check(lib().kvq_check(ws.ptr, _s(stream)), "kvq_check")
 
 
+def kvq_selftest_bounded_wait(ws, stream=None):
+    """Runs the library's bounded mbarrier wait on a barrier nothing completes (see kvq.h)."""
+    return check(lib().kvq_selftest_bounded_wait(ws.ptr, ws.nbytes, _s(stream)), "kvq_selftest_bounded_wait")
+
+
 def kvq_read_path_counters(ws, stream=None):
     """The workspace's diagnostic path counters (KVQ_PATH_*), read and cleared."""
     out = (ctypes.c_uint32 * _abi.N_PATH_COUNTERS)()

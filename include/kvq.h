@@ -645,6 +645,16 @@ int kvq_check(void* ws, void* stream);
  * they never change a result. */
 int kvq_read_path_counters(void* ws, uint32_t* out, void* stream);
 
+/* Diagnostic (an addition of this library): launches one warp that runs the
+ * bounded mbarrier wait the E4M3 attention uses for its bulk copies, on a
+ * barrier that nothing completes.  The wait gives up after its poll limit
+ * (a fraction of a second) and records a timeout in the workspace status
+ * word, so the next kvq_check returns KVQ_ERR_DEVICE_CHECK ("a bounded wait
+ * for an asynchronous copy gave up") and the context stays usable.  It shows
+ * that a copy that never lands ends in a status, not a hang.
+ * ws: at least 256 bytes, zeroed. */
+int kvq_selftest_bounded_wait(void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------
  * Host page allocator [KVSurvey §一.1-§一.2]: free list of physical pages,
  * allocation on demand, reference counts for pages shared between sequences

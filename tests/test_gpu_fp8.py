@@ -106,3 +106,20 @@ def test_decode_attention_128k():
         g = O.kv_head_of(h, 32, 8)
         ref, _ = O.fp8_attention(q[0, h].numpy(), KV[0][0][:, g].numpy(), KV[0][1][:, g].numpy())
         assert attn_err(o[0, h], ref) <= ATTN_TOL, h
+
+
+def test_bounded_wait_gives_up_with_a_status():
+    """The E4M3 kernel's wait for its bulk copies is bounded: run on a barrier that nothing
+    completes, it gives up, the workspace status word says so, and the context stays usable."""
+    import time
+    require_gpu()
+    w = ws(256)
+    t0 = time.time()
+    kvq.kvq_selftest_bounded_wait(w)
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_check(w)
+    assert e.value.code == -6 and "bounded wait" in str(e.value)
+    assert time.time() - t0 < 60
+    kvq.kvq_check(w)                       # the status word was cleared
+    x = torch.arange(8, device="cuda", dtype=torch.float32)
+    assert float(x.sum()) == 28.0          # later work runs normally
