@@ -1173,7 +1173,8 @@ def row_densepref(torch, np, kvq, synth, O, device, stream, tensor_peak):
 
 
 def row_tiny(torch, np, kvq, synth, O, device, stream):
-    """a4, a5, a6, a8 at the tiny single-layer configuration: 8 q / 2 kv heads, T = 4096
+    """a1, a3, a4, a5, a6, a8 at the tiny single-layer configuration: 8 q / 2 kv heads, T = 4096;
+    a1/a3 on a 1-bit cache (K per channel g64, V per token G64) of the same keys and values
     (latency-bound: microseconds, no roofline target)."""
     Hq, Hkv, T, ncrit, kk, ns, w = 8, 2, 4096, 8, 128, 4, 64
     seed = synth.BASE_SEED
@@ -1196,21 +1197,31 @@ def row_tiny(torch, np, kvq, synth, O, device, stream):
     Q = synth.queries((1, Hq, 32, D), synth.mix(seed, 41)).to(device)
     P = torch.empty((1, Hq), device=device)
     wd = kvq.Workspace(kvq.kv_dense_pref_score_ws(cache, seqs, 32))
+    qc = kvq.LayerCache(Hq, Hkv, 1, T // 16, 1, v_group_dims=64, device=device)
+    kvq.kv_quant_pack(qc, seqs, 0, 0, T, K, V)
+    oq = torch.empty((1, Hq, D), device=device)
+    wq = kvq.Workspace(kvq.kv_decode_attn_quant_ws(qc, seqs))
     calls = {
+        "a1 kv_quant_pack": lambda: kvq.kv_quant_pack(qc, seqs, 0, 0, T, K, V, stream=sh),
+        "a3 kv_decode_attn_quant": lambda: kvq.kv_decode_attn_quant(qc, seqs, q, oq, wq, stream=sh),
         "a4 kv_critical_score": lambda: kvq.kv_critical_score(cache, seqs, q, ncrit, crit, scores, stream=sh),
         "a5 kv_topk_select": lambda: kvq.kv_topk_select(seqs, Hq, scores, kk, 0.0, ns, w, sel, cnt, wt, stream=sh),
         "a6 kv_sparse_attn": lambda: kvq.kv_sparse_attn(cache, seqs, q, sel, cnt, 0, out, probs, wa, stream=sh),
         "a8 kv_dense_pref_score": lambda: kvq.kv_dense_pref_score(cache, seqs, Q, 32, 128, P, wd, stream=sh),
     }
     us = {n: 1e3 * _timed(torch, f, stream, min_ms=30.0)[0] for n, f in calls.items()}
-    for x in (wt, wa, wd):
+    for x in (wt, wa, wd, wq):
         kvq.kvq_check(x, stream=sh)
     Kc, Vc = K.cpu().numpy(), V.cpu().numpy()
     qn, Qn = q.cpu().numpy()[0], Q.cpu().numpy()[0]
     am = [O.key_absmax(Kc[:, g]) for g in range(Hkv)]
     chans = [O.critical_channels(qn[h], am[O.kv_head_of(h, Hq, Hkv)], ncrit) for h in range(Hq)]
     sc = []
+    pk, pv = [], []
     cpu = {
+        "a1 kv_quant_pack": _wall(lambda: (pk.extend(O.pack_k(Kc[:, g], 1) for g in range(Hkv)),
+                                           pv.extend(O.pack_v(Vc[:, g], 1, 64) for g in range(Hkv)))),
+        "a3 kv_decode_attn_quant": _wall(lambda: O.decode_attn_quant(qn, pk, pv)),
         "a4 kv_critical_score": _wall(lambda: sc.extend(O.critical_scores(qn[h], Kc[:, O.kv_head_of(h, Hq, Hkv)],
                                                                           chans[h]) for h in range(Hq))),
         "a5 kv_topk_select": _wall(lambda: [O.topk_select(sc[h], kk, ns, w) for h in range(Hq)]),
@@ -1220,8 +1231,9 @@ def row_tiny(torch, np, kvq, synth, O, device, stream):
         "a8 kv_dense_pref_score": _wall(lambda: [O.dense_pref_score(Qn[h], Kc[:, O.kv_head_of(h, Hq, Hkv)], 128)
                                                  for h in range(Hq)]),
     }
-    return {n: {"config": "8 q / 2 kv heads, T = 4096 (8 critical channels, K = 128 + 4 sinks + 64 window; dense "
-                          "preference over 32 recent queries, top-128)", "value": v, "unit": "us",
+    return {n: {"config": "8 q / 2 kv heads, T = 4096 (1-bit cache: K per channel g64, V per token G64; 8 critical "
+                          "channels, K = 128 + 4 sinks + 64 window; dense preference over 32 recent queries, "
+                          "top-128)", "value": v, "unit": "us",
                 "roofline": {"bound": "latency", "note": "tiny parity configuration: microseconds, no roofline target"},
                 "cpu_baseline": {"value": cpu[n] * 1e6, "unit": "us", "cores": 1, "kind": "oracle",
                                  "sample": "the same call on the CPU oracle, numpy"}}
