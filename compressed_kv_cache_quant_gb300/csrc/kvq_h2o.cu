@@ -13,8 +13,10 @@ constexpr int PG = KVQ_BLOCK_TOKENS;
 
 constexpr int HA_NT = 1024;
 
+constexpr int HA_U = 4;        // list entries per thread and pass step (their loads in flight together)
+
 struct H2OArgs {
-    const float* probs;
+    const float* probs;      // [B][H_q][cap]
     int32_t* retained;
     int32_t* count;
     float* cum;
@@ -71,54 +73,84 @@ __global__ void __launch_bounds__(HA_NT) h2o_kernel(H2OArgs a) {
     }
     const int T = a.seq_lens[b];
     const int next_len = T + 1;
-    // 1. cum += p_0 + p_1 + ... (the group's heads in ascending order, fp32)
-    for (int i = tid; i < n; i += HA_NT) {
-        float inc = a.probs[((int64_t)b * Hq + g * a.GQ) * a.cap + i];
-        for (int hh = 1; hh < a.GQ; ++hh) inc += a.probs[((int64_t)b * Hq + g * a.GQ + hh) * a.cap + i];
-        cum[i] = cum[i] + inc;
-    }
-    __syncthreads();
-    // 2. evict unprotected tokens, lowest (cum, position) first
     const int newp = a.new_pos ? a.new_pos[b] : -1;
     const int target = newp >= 0 ? a.budget - 1 : a.budget;
     const int excess = n - target;
     int evicted = 0;
     auto is_protected = [&](int32_t pos) { return pos < a.n_sink || pos >= next_len - a.window; };
+    // 1. cum += p_0 + p_1 + ... (the group's heads in ascending order, fp32).  When exactly one
+    //    token goes, the same pass finds it: the lowest (cum, position) key among the unprotected
+    //    entries, with its index.
+    const float* const pr = a.probs + ((int64_t)b * Hq + g * a.GQ) * a.cap;
+    unsigned long long best = ~0ull;
+    int best_i = -1;
+    for (int i0 = tid; i0 < n; i0 += HA_U * HA_NT) {
+        float cv[HA_U], inc[HA_U];
+        int32_t pv[HA_U];
+#pragma unroll
+        for (int u = 0; u < HA_U; ++u) {
+            const int i = i0 + u * HA_NT;
+            cv[u] = i < n ? cum[i] : 0.0f;
+            pv[u] = i < n ? ret[i] : 0;
+            inc[u] = 0.0f;
+        }
+        for (int hh = 0; hh < a.GQ; ++hh) {
+            const float* const ph = pr + (int64_t)hh * a.cap;
+            float sv[HA_U];
+#pragma unroll
+            for (int u = 0; u < HA_U; ++u) sv[u] = i0 + u * HA_NT < n ? ph[i0 + u * HA_NT] : 0.0f;
+#pragma unroll
+            for (int u = 0; u < HA_U; ++u) inc[u] = hh == 0 ? sv[u] : inc[u] + sv[u];
+        }
+#pragma unroll
+        for (int u = 0; u < HA_U; ++u) {
+            const int i = i0 + u * HA_NT;
+            if (i < n) {
+                const float c = cv[u] + inc[u];
+                cum[i] = c;
+                if (excess == 1 && !is_protected(pv[u])) {
+                    const unsigned long long k = evict_key(c, pv[u]);
+                    if (k < best) {
+                        best = k;
+                        best_i = i;
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // 2. evict unprotected tokens, lowest (cum, position) first
     if (excess == 1) {
-        unsigned long long best = ~0ull;
-        for (int i = tid; i < n; i += HA_NT) {
-            const int32_t pos = ret[i];
-            if (!is_protected(pos)) {
-                const unsigned long long k = evict_key(cum[i], pos);
-                best = k < best ? k : best;
+        // the block's minimum key and its index (positions are unique: one entry carries it)
+        __shared__ int redi[HA_NT / 32];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long k2 = __shfl_xor_sync(0xffffffffu, best, o);
+            const int i2 = __shfl_xor_sync(0xffffffffu, best_i, o);
+            if (k2 < best) {
+                best = k2;
+                best_i = i2;
             }
         }
-        best = warp_min_u64(best);
-        if ((tid & 31) == 0) redk[tid >> 5] = best;
-        __syncthreads();
-        if (tid < 32) {
-            unsigned long long v = redk[tid];
-            v = warp_min_u64(v);
-            if (tid == 0) redk[0] = v;
+        if ((tid & 31) == 0) {
+            redk[tid >> 5] = best;
+            redi[tid >> 5] = best_i;
         }
         __syncthreads();
-        const unsigned long long kmin = redk[0];
-        __syncthreads();
-        if (kmin != ~0ull) {
-            // positions are unique: exactly one entry carries the minimum
-            __shared__ int s_idx;
-            if (tid == 0) s_idx = -1;
-            __syncthreads();
-            for (int i = tid; i < n; i += HA_NT)
-                if (!is_protected(ret[i]) && evict_key(cum[i], ret[i]) == kmin) s_idx = i;
-            __syncthreads();
-            if (tid == 0 && s_idx >= 0) {
-                ret[s_idx] = ret[n - 1];
-                cum[s_idx] = cum[n - 1];
+        if (tid == 0) {
+            unsigned long long kmin = redk[0];
+            int imin = redi[0];
+            for (int w = 1; w < HA_NT / 32; ++w)
+                if (redk[w] < kmin) {
+                    kmin = redk[w];
+                    imin = redi[w];
+                }
+            if (kmin != ~0ull) {
+                ret[imin] = ret[n - 1];
+                cum[imin] = cum[n - 1];
+                n -= 1;
+                evicted = 1;
             }
-            __syncthreads();
-            n -= 1;
-            evicted = 1;
         }
     } else if (excess > 1) {
         uint32_t n_un = 0;

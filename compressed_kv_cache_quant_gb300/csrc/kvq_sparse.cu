@@ -294,6 +294,7 @@ __host__ __device__ constexpr int sa_stages(int nh) { return nh > 1 ? 3 : 2; }
 __host__ __device__ constexpr int sa_tiles(int nh) { return SA_NW * sa_stages(nh) * 2 * SA_TILE; }  // [warp][stage][K, V]
 constexpr int SA_TILES = sa_tiles(1);  // the smaller stage area (the warp states of the merge fit it)
 constexpr int SA_REC = 4 + D;
+constexpr int SA_NORM_CHUNKS = 4;  // CTAs per (sequence, q head) row of the normalization launch
 constexpr int SA_MAX_RPS = 2048;   // rows per split: their offsets are resolved into shared memory
 
 // 16-byte global -> shared copy; a row that is not there reads as zeros
@@ -361,7 +362,9 @@ template <int NH>
 __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
     extern __shared__ __align__(16) float sm[];  // warp tiles (then [SA_NW][NH][SA_REC] warp states) | row offsets
     __shared__ int is_last;
-    const int split = blockIdx.x, list = blockIdx.y, b = blockIdx.z;
+    // splits vary slowest over the grid: the first splits of every list, the ones that have rows
+    // whatever the lists' lengths, are scheduled first
+    const int list = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x;
     const int n_lists = a.per_kv ? a.H : a.H * a.GQ;
     const int Hq = a.H * a.GQ;
@@ -383,9 +386,13 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
             for (int i = tid; i < NH * D; i += SA_NT) a.out[((int64_t)b * Hq + h0) * D + i] = 0.0f;
         return;
     }
-    const int nsplit_b = (n + a.rps - 1) / a.rps;
+    // the list's rows over as few splits of at most a.rps rows as hold them, in equal shares (whole
+    // 16-row tiles): the list is done when its longest share is
+    const int k_min = (n + a.rps - 1) / a.rps;
+    const int rps_b = ((n + k_min - 1) / k_min + SA_TR - 1) / SA_TR * SA_TR;
+    const int nsplit_b = (n + rps_b - 1) / rps_b;
     if (split >= nsplit_b) return;
-    const int r_begin = split * a.rps, r_end = min(n, r_begin + a.rps);
+    const int r_begin = split * rps_b, r_end = min(n, r_begin + rps_b);
     const int32_t* ids = a.all_tokens ? nullptr : a.sel + ((int64_t)b * n_lists + list) * a.sel_cap;
 
     // the split's rows: ids and pages resolved up front into row offsets (in 128-element rows;
@@ -645,16 +652,20 @@ __global__ void __launch_bounds__(256) sa_norm_kernel(SAArgs a) {
     const int n_lists = a.per_kv ? a.H : Hq;
     const int list = a.per_kv ? h / a.GQ : h;
     const int n = max(0, min(a.sel_count[(int64_t)b * n_lists + list], a.sel_cap));
-    const int i0 = blockIdx.x * 1024 + threadIdx.x;
-    if (i0 >= n) return;
+    if ((int)blockIdx.x * 1024 >= n) return;
     const float2 f = a.fin[(int64_t)b * Hq + h];
     float* pr = a.probs + ((int64_t)b * Hq + h) * a.sel_cap;
-    float sv[4];
+    // 1024-entry chunks, strided over the few CTAs of the row: the grid is sized by the capacity,
+    // not by the lists' lengths (on the device), so it stays small
+    for (int i0 = blockIdx.x * 1024 + threadIdx.x; i0 < n; i0 += gridDim.x * 1024) {
+        float sv[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) sv[u] = i0 + 256 * u < n ? __ldcg(pr + i0 + 256 * u) : -INFINITY;
+        for (int u = 0; u < 4; ++u) sv[u] = i0 + 256 * u < n ? __ldcg(pr + i0 + 256 * u) : -INFINITY;
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-        if (i0 + 256 * u < n) pr[i0 + 256 * u] = (f.y > 0.0f && sv[u] != -INFINITY) ? exp2f(sv[u] - f.x) / f.y : 0.0f;
+        for (int u = 0; u < 4; ++u)
+            if (i0 + 256 * u < n)
+                pr[i0 + 256 * u] = (f.y > 0.0f && sv[u] != -INFINITY) ? exp2f(sv[u] - f.x) / f.y : 0.0f;
+    }
 }
 
 struct SAPlan {
@@ -881,7 +892,7 @@ int kvq_dense_heads_attn(const kvq_layout* L, const kvq_pool* P, const kvq_seqs*
     a.rps = p.rps;
     a.dense = dense;
     a.all_tokens = 1;
-    const dim3 grid(p.n_splits, L->n_kv_heads, S->batch);
+    const dim3 grid(L->n_kv_heads, p.n_splits, S->batch);
     switch (a.GQ) {
         case 1: return launch_sa<1>(a, grid, s);
         case 2: return launch_sa<2>(a, grid, s);
@@ -897,10 +908,11 @@ extern "C" size_t kv_sparse_attn_ws(const kvq_layout* L, const kvq_seqs* S, int3
     return sa_ws_layout(L, S, sel_cap, &a, &c, &f);
 }
 
-extern "C" int kv_sparse_attn(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
+// kv_sparse_attn without its normalization launch: probs (when given) keeps the log2-domain scores
+// and the workspace the (max, sum) per (sequence, q head) that make them probabilities.
+static int sparse_attn_scores(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
                               const int32_t* sel, int32_t sel_cap, const int32_t* sel_count, int32_t sel_per_kv_head,
                               float* out, float* probs, void* ws, size_t ws_bytes, void* stream) {
-    kvq_clear_error();
     int st = kvq_check_layout(L, "kv_sparse_attn", true);
     if (st) return st;
     st = kvq_check_seqs(S, "kv_sparse_attn");
@@ -942,7 +954,7 @@ extern "C" int kv_sparse_attn(const kvq_layout* L, const kvq_pool* P, const kvq_
     a.n_splits = p.n_splits;
     a.rps = p.rps;
     const int n_lists = sel_per_kv_head ? L->n_kv_heads : L->n_q_heads;
-    dim3 grid(p.n_splits, n_lists, S->batch);
+    dim3 grid(n_lists, p.n_splits, S->batch);
     cudaStream_t s = kvq_stream(stream);
     int e;
     if (!sel_per_kv_head) {
@@ -955,11 +967,31 @@ extern "C" int kv_sparse_attn(const kvq_layout* L, const kvq_pool* P, const kvq_
             default: e = launch_sa<8>(a, grid, s); break;
         }
     }
-    if (e || probs == nullptr) return e;
-    const dim3 ng((unsigned)((sel_cap + 1023) / 1024), (unsigned)L->n_q_heads, (unsigned)S->batch);
+    return e;
+}
+
+extern "C" int kv_sparse_attn(const kvq_layout* L, const kvq_pool* P, const kvq_seqs* S, const uint16_t* q,
+                              const int32_t* sel, int32_t sel_cap, const int32_t* sel_count, int32_t sel_per_kv_head,
+                              float* out, float* probs, void* ws, size_t ws_bytes, void* stream) {
+    kvq_clear_error();
+    const int e = sparse_attn_scores(L, P, S, q, sel, sel_cap, sel_count, sel_per_kv_head, out, probs, ws, ws_bytes,
+                                     stream);
+    if (e || probs == nullptr || S->batch == 0) return e;
+    // the stored scores become probabilities (a second, short launch)
+    size_t off_part, off_cnt, off_fin;
+    sa_ws_layout(L, S, sel_cap, &off_part, &off_cnt, &off_fin);
+    SAArgs a{};
+    a.H = L->n_kv_heads;
+    a.GQ = L->n_q_heads / L->n_kv_heads;
+    a.sel_cap = sel_cap;
+    a.sel_count = sel_count;
+    a.per_kv = sel_per_kv_head;
+    a.probs = probs;
+    a.fin = reinterpret_cast<float2*>(static_cast<char*>(ws) + off_fin);
+    const dim3 ng((unsigned)std::min((sel_cap + 1023) / 1024, SA_NORM_CHUNKS), (unsigned)L->n_q_heads, (unsigned)S->batch);
     const int st2 = kvq_prepare_kernel((const void*)sa_norm_kernel, 0);
     if (st2) return st2;
-    const cudaError_t le = kvq_launch_pdl(sa_norm_kernel, ng, dim3(256), 0, s, a);
+    const cudaError_t le = kvq_launch_pdl(sa_norm_kernel, ng, dim3(256), 0, kvq_stream(stream), a);
     if (le != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_sparse_attn launch: %s", cudaGetErrorString(le));
     return kvq_launch_status("kv_sparse_attn");
 }

@@ -99,3 +99,42 @@ def test_sparse_layer_decode_without_optional_outputs_is_the_same():
     del alloc
     for h in range(Hq):
         assert attn_err(outs[1][0, h], outs[0][0, h]) <= 1e-5
+
+
+@pytest.mark.parametrize("n_crit,T,k,expect_radix", [
+    (8, 40000, 600, False),   # many tie at the k-th key: third digit pass, the cut inside one CTA
+    (2, 40000, 6000, True),   # thousands tie: distributed radix passes after the early attention
+])
+def test_sparse_layer_bench_path_ties(n_crit, T, k, expect_radix):
+    """Integer keys in {-1, 0, 1} and a unit query: the approximate scores tie in bulk, the
+    kept set follows the lower-position rule at the k-th key, and the one-pass path's early
+    attention over the rows kept for certain plus the attention over the rest equals the
+    oracle (TailorKV §2.3; KV-cache survey §三.1)."""
+    require_gpu()
+    Hq, Hkv, ns, w = 8, 2, 4, 64
+    seed = synth.mix(synth.BASE_SEED + 1, 302, n_crit, k)
+    g = torch.Generator().manual_seed(seed)
+    K = torch.randint(-1, 2, (T, Hkv, 128), generator=g).to(torch.float16)
+    V = synth.normal((T, Hkv, 128), synth.mix(seed, 2))
+    n_pages = math.ceil(T / 16) + 2
+    alloc = kvq.Allocator(n_pages, seed=7)
+    batch, bt = paged_batch([T], alloc, lengths=[T - 1])
+    cache = kvq.LayerCache(Hq, Hkv, 16, n_pages, 1, t_cap=(T + 7) // 8 * 8)
+    kvq.kv_quant_pack(cache, batch, 0, 0, T - 1, K[:T - 1].cuda(), V[:T - 1].cuda())
+    kvq.kvq_seq_lens_add(batch.seq_lens, 1)
+    q = torch.ones((1, Hq, 128), dtype=torch.float16)
+    out = torch.full((1, Hq, 128), float("nan"), device="cuda")
+    wk = ws(kvq.kv_sparse_layer_decode_ws())
+    kvq.kv_sparse_layer_decode(cache, batch, K[T - 1][None].cuda(), V[T - 1][None].cuda(), q.cuda(), n_crit, k, 0.0,
+                               ns, w, out, wk)
+    kvq.kvq_check(wk)
+    listed, compacted, radix, _ = kvq.kvq_read_path_counters(wk)
+    assert (radix > 0) == expect_radix
+    o = out.cpu().numpy()
+    Kn, Vn = K.numpy(), V.numpy()
+    for h in range(Hq):
+        gk = O.kv_head_of(h, Hq, Hkv)
+        C = O.critical_channels(q[0, h].numpy(), O.key_absmax(Kn[:, gk]), n_crit)
+        ids = O.topk_select(O.critical_scores(q[0, h].numpy(), Kn[:, gk], C), k, ns, w)
+        ref, _ = O.sparse_attn(q[0, h].numpy(), Kn[:, gk], Vn[:, gk], ids)
+        assert attn_err(o[0, h], ref) <= ATTN_TOL, h
