@@ -288,9 +288,9 @@ constexpr int SA_NW = 4;                       // warps per CTA
 constexpr int SA_NT = 32 * SA_NW;
 constexpr int SA_TR = 16;                      // rows per warp tile
 constexpr int SA_TILE = SA_TR * D * 2;         // bytes of one K or V tile (4 KB; a stage holds both)
-// tiles per warp in flight or in use: three where several q heads share each tile (lists per kv
-// head: fewer CTAs, each tile worth more work), two for one head per list (more CTAs per SM)
-__host__ __device__ constexpr int sa_stages(int nh) { return nh > 1 ? 3 : 2; }
+// tiles per warp in flight or in use: two, so that three CTAs fit an SM (the splits of a launch
+// are sized to fill those slots; three stages at two CTAs per SM were 5% slower on lists per kv head)
+__host__ __device__ constexpr int sa_stages(int) { return 2; }
 __host__ __device__ constexpr int sa_tiles(int nh) { return SA_NW * sa_stages(nh) * 2 * SA_TILE; }  // [warp][stage][K, V]
 constexpr int SA_TILES = sa_tiles(1);  // the smaller stage area (the warp states of the merge fit it)
 constexpr int SA_REC = 4 + D;
@@ -351,7 +351,8 @@ struct SAArgs {
     float2* fin;        // [batch][H_q] (max, sum) of the exp2 scores, for the probabilities
     KvqWsHeader* hdr;
     int32_t n_splits;
-    int32_t rps;        // rows per split
+    int32_t rps;        // rows per split (at most)
+    int32_t k_target;   // splits per list that fill the resident CTA slots of the launch
     // dense kv heads of a mixed layer: every token is listed (no sel), and only the kv heads g with
     // dense[b][g] != 0 are attended (lists per kv head)
     const int32_t* dense = nullptr;
@@ -386,10 +387,12 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
             for (int i = tid; i < NH * D; i += SA_NT) a.out[((int64_t)b * Hq + h0) * D + i] = 0.0f;
         return;
     }
-    // the list's rows over as few splits of at most a.rps rows as hold them, in equal shares (whole
-    // 16-row tiles): the list is done when its longest share is
+    // the list's rows in equal shares (whole 16-row tiles) over enough splits to fill the launch's
+    // resident CTA slots (k_target per list), at most a.rps rows and at least 64 rows a split: the
+    // list is done when its longest share is
     const int k_min = (n + a.rps - 1) / a.rps;
-    const int rps_b = ((n + k_min - 1) / k_min + SA_TR - 1) / SA_TR * SA_TR;
+    const int k = min(a.n_splits, max(k_min, min(max(a.k_target, 1), (n + 63) / 64)));
+    const int rps_b = ((n + k - 1) / k + SA_TR - 1) / SA_TR * SA_TR;
     const int nsplit_b = (n + rps_b - 1) / rps_b;
     if (split >= nsplit_b) return;
     const int r_begin = split * rps_b, r_end = min(n, r_begin + rps_b);
@@ -704,7 +707,13 @@ int launch_sa(const SAArgs& a, dim3 grid, cudaStream_t s) {
     const int st = kvq_prepare_kernel((const void*)sparse_attn_kernel<NH>,
                                       (int)((size_t)sa_tiles(NH) + SA_MAX_RPS * sizeof(uint32_t)));
     if (st) return st;
-    sparse_attn_kernel<NH><<<grid, SA_NT, smem, s>>>(a);
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_attn_kernel<NH>, SA_NT, smem) != cudaSuccess)
+        occ = 1;
+    SAArgs b = a;
+    const int64_t units = (int64_t)grid.x * grid.z;
+    b.k_target = (int)std::max<int64_t>(1, (int64_t)std::max(occ, 1) * kvq_num_sms() / std::max<int64_t>(units, 1));
+    sparse_attn_kernel<NH><<<grid, SA_NT, smem, s>>>(b);
     return kvq_launch_status("kv_sparse_attn");
 }
 
