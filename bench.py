@@ -341,6 +341,8 @@ def main():
                     help="instead of the step: time the other hot-path rows on their configurations (one JSON line)")
     ap.add_argument("--only", nargs="*", default=None, help="with --rows: the rows whose names start with these")
     ap.add_argument("--no-rows", action="store_true", help="the decode step only, without the other rows")
+    ap.add_argument("--row-layers", type=int, default=0,
+                    help="with --rows: layers of the H2O run (default: its 32; fewer for a profiler capture)")
     args = ap.parse_args()
     if args.rows:
         import torch
@@ -348,6 +350,8 @@ def main():
         from compressed_kv_cache_quant_gb300.build import build
         build()
         dev = torch.device("cuda", 0)
+        global ROW_LAYERS
+        ROW_LAYERS = args.row_layers
         print(json.dumps({"rows": run_rows(dev, torch.cuda.Stream(dev), args.only)}))
         return
     assert args.warmup >= 1 and args.steps >= 1 and args.layers >= 2
@@ -768,7 +772,7 @@ def row_h2o(torch, np, kvq, synth, O, device, stream, hbm, steps=256):
     appends a token, attends the retained set (one list per kv head, probabilities out), adds the
     group's probabilities to the cumulative scores, evicts down to budget - 1 and admits the
     next token.  Queries prefer 64 hot keys per (layer, sequence, kv head) with Zipf(1.2) weights."""
-    B, Hq, Hkv, L, T0, budget, ns, w = 8, 32, 8, 32, 32768, 6553, 4, 2048
+    B, Hq, Hkv, L, T0, budget, ns, w = 8, 32, 8, ROW_LAYERS or 32, 32768, 6553, 4, 2048
     G, n_hot = Hq // Hkv, 64
     seed = synth.BASE_SEED + 3
     cap_tok = T0 + steps + 16
@@ -1239,6 +1243,8 @@ def row_tiny(torch, np, kvq, synth, O, device, stream):
                                  "sample": "the same call on the CPU oracle, numpy"}}
             for n, v in us.items()}
 
+
+ROW_LAYERS = 0  # layers of the H2O run when set (a smaller case for a profiler capture)
 
 ROWS = [
     ("a1 kv_quant_pack (40-layer prefill)", row_pack),
