@@ -342,7 +342,8 @@ def main():
     ap.add_argument("--only", nargs="*", default=None, help="with --rows: the rows whose names start with these")
     ap.add_argument("--no-rows", action="store_true", help="the decode step only, without the other rows")
     ap.add_argument("--row-layers", type=int, default=0,
-                    help="with --rows: layers of the H2O run (default: its 32; fewer for a profiler capture)")
+                    help="with --rows: layers of the H2O run and of the pack (default: 32 and 40; fewer for a "
+                         "profiler capture)")
     args = ap.parse_args()
     if args.rows:
         import torch
@@ -596,7 +597,8 @@ def _capture(torch, fn, stream):
 def row_pack(torch, np, kvq, synth, O, device, stream, hbm):
     """a1 kv_quant_pack, the Qwen-1.5-14B-shaped prefill: 40 layers x 40 kv heads x 131072 tokens
     to 1 bit (K per channel g64, V per token G64), one call per layer."""
-    T, H, L, n_in = 131072, 40, 40, 8
+    T, H, L = 131072, 40, ROW_LAYERS or 40
+    n_in = min(8, L)
     seed = synth.BASE_SEED + 4
     n_pages = T // 16
     seqs = kvq.Batch(torch.arange(n_pages, dtype=torch.int32, device=device)[None],
@@ -1244,7 +1246,7 @@ def row_tiny(torch, np, kvq, synth, O, device, stream):
             for n, v in us.items()}
 
 
-ROW_LAYERS = 0  # layers of the H2O run when set (a smaller case for a profiler capture)
+ROW_LAYERS = 0  # layers of the H2O run and of the pack when set (a smaller case for a profiler capture)
 
 ROWS = [
     ("a1 kv_quant_pack (40-layer prefill)", row_pack),
