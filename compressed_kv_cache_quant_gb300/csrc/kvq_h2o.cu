@@ -34,15 +34,6 @@ __device__ __forceinline__ unsigned long long evict_key(float cum, int32_t pos) 
     return ((unsigned long long)kvq_float_key(cum) << 32) | (uint32_t)pos;
 }
 
-__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long y = __shfl_xor_sync(0xffffffffu, v, o);
-        v = y < v ? y : v;
-    }
-    return v;
-}
-
 __device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -55,12 +46,119 @@ __device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, uint32_t* red) {
     return s;
 }
 
-__global__ void __launch_bounds__(HA_NT) h2o_kernel(H2OArgs a) {
-    __shared__ uint32_t red[HA_NT / 32];
-    __shared__ unsigned long long redk[HA_NT / 32];
+// Evicts the `excess` (> 1) unprotected entries of lowest (cum, position) key from ret/cum[0, n)
+// (all of them when there are no more), keeping the order of the others; returns the new length.
+// Called by all NTH threads of a CTA.
+template <int NTH>
+__device__ int h2o_evict_many(int32_t* ret, float* cum, int n, int excess, int n_sink, int window, int next_len) {
+    __shared__ uint32_t red[NTH / 32];
     __shared__ uint32_t hist[256];
     __shared__ uint32_t s_bin, s_below;
-    __shared__ uint32_t wsum[HA_NT / 32];
+    __shared__ uint32_t wsum[NTH / 32];
+    const int tid = threadIdx.x;
+    auto is_protected = [&](int32_t pos) { return pos < n_sink || pos >= next_len - window; };
+    uint32_t n_un = 0;
+    for (int i = tid; i < n; i += NTH) n_un += !is_protected(ret[i]);
+    const uint32_t U = block_sum_u32(n_un, red);
+    unsigned long long thr;
+    if (U <= (uint32_t)excess) {
+        thr = ~0ull;  // every unprotected token goes
+    } else {
+        // radix select of the excess-th smallest 64-bit key among unprotected tokens
+        unsigned long long prefix = 0ull, mask = 0ull;
+        uint32_t remaining = (uint32_t)excess;
+        for (int pass = 0; pass < 8; ++pass) {
+            const int shift = 56 - 8 * pass;
+            for (int i = tid; i < 256; i += NTH) hist[i] = 0u;
+            __syncthreads();
+            for (int i = tid; i < n; i += NTH) {
+                const int32_t pos = ret[i];
+                if (is_protected(pos)) continue;
+                const unsigned long long k = evict_key(cum[i], pos);
+                if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255ull], 1u);
+            }
+            __syncthreads();
+            if (tid < 32) {
+                // lane l owns bins [8l, 8l + 7]; lane 0 the smallest
+                uint32_t ls = 0;
+                for (int j = 0; j < 8; ++j) ls += hist[8 * tid + j];
+                uint32_t incl = ls;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o) incl += y;
+                }
+                const uint32_t ballot = __ballot_sync(0xffffffffu, incl >= remaining);
+                const int l = __ffs(ballot) - 1;
+                if (tid == l) {
+                    uint32_t run = incl - ls;
+                    for (int j = 0; j < 8; ++j) {
+                        const int bin = 8 * tid + j;
+                        if (run + hist[bin] >= remaining) {
+                            s_bin = (uint32_t)bin;
+                            s_below = run;
+                            break;
+                        }
+                        run += hist[bin];
+                    }
+                }
+            }
+            __syncthreads();
+            remaining -= s_below;
+            prefix |= (unsigned long long)s_bin << shift;
+            mask |= 255ull << shift;
+            __syncthreads();
+        }
+        thr = prefix;
+    }
+    // order-preserving in-place compaction of the kept entries
+    uint32_t out_base = 0;
+    for (int t0 = 0; t0 < n; t0 += NTH) {
+        const int i = t0 + tid;
+        int32_t pos = 0;
+        float cv = 0.0f;
+        uint32_t keep = 0;
+        if (i < n) {
+            pos = ret[i];
+            cv = cum[i];
+            keep = is_protected(pos) || evict_key(cv, pos) > thr;
+        }
+        uint32_t tile_total;
+        // exclusive scan of `keep` over the CTA
+        const int lane = tid & 31, warp = tid >> 5;
+        uint32_t x = keep;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        __syncthreads();
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t w = lane < NTH / 32 ? wsum[lane] : 0u;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            wsum[lane] = w;
+        }
+        __syncthreads();
+        tile_total = wsum[NTH / 32 - 1];
+        const uint32_t before = x - keep + (warp > 0 ? wsum[warp - 1] : 0u);
+        if (keep) {
+            ret[out_base + before] = pos;
+            cum[out_base + before] = cv;
+        }
+        out_base += tile_total;
+        __syncthreads();
+    }
+    return (int)out_base;
+}
+
+__global__ void __launch_bounds__(HA_NT) h2o_kernel(H2OArgs a) {
+    __shared__ unsigned long long redk[HA_NT / 32];
     const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int Hq = a.H * a.GQ;
     const int64_t base = ((int64_t)b * a.H + g) * a.cap;
@@ -153,105 +251,9 @@ __global__ void __launch_bounds__(HA_NT) h2o_kernel(H2OArgs a) {
             }
         }
     } else if (excess > 1) {
-        uint32_t n_un = 0;
-        for (int i = tid; i < n; i += HA_NT) n_un += !is_protected(ret[i]);
-        const uint32_t U = block_sum_u32(n_un, red);
-        unsigned long long thr;
-        if (U <= (uint32_t)excess) {
-            thr = ~0ull;  // every unprotected token goes
-        } else {
-            // radix select of the excess-th smallest 64-bit key among unprotected tokens
-            unsigned long long prefix = 0ull, mask = 0ull;
-            uint32_t remaining = (uint32_t)excess;
-            for (int pass = 0; pass < 8; ++pass) {
-                const int shift = 56 - 8 * pass;
-                for (int i = tid; i < 256; i += HA_NT) hist[i] = 0u;
-                __syncthreads();
-                for (int i = tid; i < n; i += HA_NT) {
-                    const int32_t pos = ret[i];
-                    if (is_protected(pos)) continue;
-                    const unsigned long long k = evict_key(cum[i], pos);
-                    if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255ull], 1u);
-                }
-                __syncthreads();
-                if (tid < 32) {
-                    // lane l owns bins [8l, 8l + 7]; lane 0 the smallest
-                    uint32_t ls = 0;
-                    for (int j = 0; j < 8; ++j) ls += hist[8 * tid + j];
-                    uint32_t incl = ls;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (tid >= o) incl += y;
-                    }
-                    const uint32_t ballot = __ballot_sync(0xffffffffu, incl >= remaining);
-                    const int l = __ffs(ballot) - 1;
-                    if (tid == l) {
-                        uint32_t run = incl - ls;
-                        for (int j = 0; j < 8; ++j) {
-                            const int bin = 8 * tid + j;
-                            if (run + hist[bin] >= remaining) {
-                                s_bin = (uint32_t)bin;
-                                s_below = run;
-                                break;
-                            }
-                            run += hist[bin];
-                        }
-                    }
-                }
-                __syncthreads();
-                remaining -= s_below;
-                prefix |= (unsigned long long)s_bin << shift;
-                mask |= 255ull << shift;
-                __syncthreads();
-            }
-            thr = prefix;
-        }
-        // order-preserving in-place compaction of the kept entries
-        uint32_t out_base = 0;
-        for (int t0 = 0; t0 < n; t0 += HA_NT) {
-            const int i = t0 + tid;
-            int32_t pos = 0;
-            float cv = 0.0f;
-            uint32_t keep = 0;
-            if (i < n) {
-                pos = ret[i];
-                cv = cum[i];
-                keep = is_protected(pos) || evict_key(cv, pos) > thr;
-            }
-            uint32_t tile_total;
-            // exclusive scan of `keep` over the CTA
-            const int lane = tid & 31, warp = tid >> 5;
-            uint32_t x = keep;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            __syncthreads();
-            if (lane == 31) wsum[warp] = x;
-            __syncthreads();
-            if (warp == 0) {
-                uint32_t w = wsum[lane];
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
-                    if (lane >= o) w += y;
-                }
-                wsum[lane] = w;
-            }
-            __syncthreads();
-            tile_total = wsum[HA_NT / 32 - 1];
-            const uint32_t before = x - keep + (warp > 0 ? wsum[warp - 1] : 0u);
-            if (keep) {
-                ret[out_base + before] = pos;
-                cum[out_base + before] = cv;
-            }
-            out_base += tile_total;
-            __syncthreads();
-        }
-        evicted = n - (int)out_base;
-        n = (int)out_base;
+        const int kept = h2o_evict_many<HA_NT>(ret, cum, n, excess, a.n_sink, a.window, next_len);
+        evicted = n - kept;
+        n = kept;
     }
     // 3. admit the next token with score 0
     if (tid == 0) {
@@ -669,7 +671,7 @@ extern "C" int kv_h2o_accumulate(const kvq_layout* L, const kvq_seqs* S, const f
     KVQ_REQUIRE(cap > 0 && budget >= 1 && budget <= cap && n_sink >= 0 && window >= 0, KVQ_ERR_INVALID_ARG,
                 "kv_h2o_accumulate: need 1 <= budget <= cap, n_sink >= 0, window >= 0");
     if (S->batch == 0) return KVQ_OK;
-    H2OArgs a;
+    H2OArgs a{};
     a.probs = probs;
     a.retained = retained;
     a.count = retained_count;
