@@ -20,8 +20,6 @@
 // FMA per pair, against p_t in fp16.  The group's codes and scales are staged per warp with cp.async, one
 // group ahead.  An unfinished K group reads its keys from the fp16 tail buffer.
 #include <algorithm>
-#include <map>
-#include <mutex>
 
 #include "kvq_internal.cuh"
 
@@ -1188,24 +1186,14 @@ extern "C" int kv_decode_attn_quant_outlier(const kvq_layout* L, const kvq_pool*
 
 static __device__ __align__(256) unsigned char g_qattn_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_qattn_scratch for the current device, looked up once per
-// device (the host-side name of the array is not a device address).
+// Device address of g_qattn_scratch in the current context, looked up on every call (a host-side
+// lookup; a cached address would go stale if the context were reset and the module reloaded).
 static int qattn_scratch(void** out) {
-    static std::mutex mu;
-    static std::map<int, void*> addr;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant_noalloc: %s", cudaGetErrorString(e));
-    std::lock_guard<std::mutex> lk(mu);
-    auto it = addr.find(dev);
-    if (it == addr.end()) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_qattn_scratch);
-        if (e != cudaSuccess || p == nullptr)
-            return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant_noalloc: scratch address: %s", cudaGetErrorString(e));
-        it = addr.emplace(dev, p).first;
-    }
-    *out = it->second;
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_qattn_scratch);
+    if (e != cudaSuccess || p == nullptr)
+        return kvq_fail(KVQ_ERR_CUDA, "kv_decode_attn_quant_noalloc: scratch address: %s", cudaGetErrorString(e));
+    *out = p;
     return KVQ_OK;
 }
 

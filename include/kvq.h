@@ -262,12 +262,10 @@ size_t kv_decode_attn_quant_ws(const kvq_layout* layout, const kvq_seqs* seqs);
  * is one fixed 8 MiB array inside the library (kv_decode_attn_quant_noalloc_
  * max_scratch() bytes), which every GPU that loads the library keeps until
  * the process exits.  No call allocates or frees memory.
- *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before any
- *     stream capture.  The address stays cached for the life of the process:
- *     after cudaDeviceReset (or anything else that destroys the device's
- *     primary context) the library must be unloaded and loaded again before
- *     this entry point is called on that device.
+ *   - Every call looks up the array's device address in the current context
+ *     (a host-side lookup, so a context reset leaves no stale address); the
+ *     first call on a device loads the array's module, so make it before any
+ *     stream capture.
  *   - A batch whose scratch (kv_decode_attn_quant_ws) exceeds the array is
  *     rejected with KVQ_ERR_NO_SPACE before anything is launched.
  *   - All calls share the array and each clears the parts that must start at
