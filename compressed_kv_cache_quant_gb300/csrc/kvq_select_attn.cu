@@ -381,12 +381,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         s.n_s = 0;
         s.n_c = 0;
     }
-    // the first-digit histograms of the cluster's CTAs are summed into every CTA's copy
+    // the first-digit histograms of the cluster's CTAs are summed into every CTA's copy; the copy is
+    // zeroed and the cluster barrier's arrive released where this CTA has no load in flight (a
+    // release waits for them), the matching wait precedes the first remote add
     const bool exchange = !keep_all && k > 0 && (fused || a.hist == nullptr);
-    if (exchange) {
-        for (int i = tid; i < H1; i += NT) s.v.gh[i] = 0u;
-        cluster_arrive();  // the matching wait precedes the first remote add
-    }
 
     uint32_t kth = 0xffffffffu;  // kept: key > kth, or key == kth and position <= cut
     int32_t cut = -1;
@@ -466,6 +464,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         __syncthreads();
         // ---- approximate scores a_t = sum over the channels, ascending, of q_c K[t][c] (fp32 from
         // +0), their keys, and the local histogram of candidate keys (a dense head has none)
+        if (exchange) {
+            for (int i = tid; i < H1; i += NT) s.v.gh[i] = 0u;
+            cluster_arrive();
+        }
         const uint16_t* kbase = a.kT + kvrow * D * a.t_cap;
         float* srow_out = a.scores_out != nullptr ? a.scores_out + row * a.score_stride : nullptr;
         if (dense) {
@@ -523,6 +525,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     }
     if (!keep_all) {
         if (!fused) {
+            if (exchange) {
+                for (int i = tid; i < H1; i += NT) s.v.gh[i] = 0u;
+                cluster_arrive();
+            }
             // ---- the chunk's keys (16-byte loads, eight in flight per thread)
             for (int p0 = lo + 4 * tid; p0 < hi; p0 += 4 * NT * 8) {
                 float4 v[8];
