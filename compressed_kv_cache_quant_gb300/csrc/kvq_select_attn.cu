@@ -339,6 +339,10 @@ __device__ __forceinline__ bool warp_append(bool f, V v, V* list, int32_t* n, in
     return base + __popc(m) <= cap;
 }
 
+// LEAN: the instance for the fused decode without optional outputs (kT given, no sel, scores_out,
+// hist or dense flags, at most 8 critical channels): the paths it never takes are not compiled in,
+// so that the instructions a CTA runs once, phase after phase, are fetched from fewer lines.
+template <bool LEAN>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_kernel(SXArgs a, int chunk_cap) {
     extern __shared__ __align__(16) uint32_t keys[];  // the chunk's keys; later its kept positions
     SXSmem& s = *reinterpret_cast<SXSmem*>(reinterpret_cast<char*>(keys) +
@@ -349,7 +353,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t row = (int64_t)b * a.n_heads + h;
     kvq_pdl_begin();
-    const bool fused = a.kT != nullptr;
+    const bool fused = LEAN || a.kT != nullptr;
     // the fused path's per-channel inputs are requested together with the length
     uint16_t pre_q = 0, pre_kn = 0;
     float pre_am = 0.0f;
@@ -370,7 +374,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     const int n = hi - lo;
     // a dense head (head-level classification: quantization-friendly) attends every token: no
     // critical scores, no selection -- the same launch, dispatched by the head's class
-    const bool dense = a.dense != nullptr && a.dense[(int64_t)b * a.H + h / a.GQ] != 0;
+    const bool dense = !LEAN && a.dense != nullptr && a.dense[(int64_t)b * a.H + h / a.GQ] != 0;
     const bool keep_all = dense || (int64_t)T <= (int64_t)a.n_sink + a.window + k;
     const int cand_lo = a.n_sink, cand_hi = T - a.window;
     const float* srow = a.scores + row * a.score_stride;
@@ -385,6 +389,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     // zeroed and the cluster barrier's arrive released where this CTA has no load in flight (a
     // release waits for them), the matching wait precedes the first remote add
     const bool exchange = !keep_all && k > 0 && (fused || a.hist == nullptr);
+    const bool has_sel = !LEAN && a.sel != nullptr;
+    const bool has_hist = !LEAN && a.hist != nullptr;
 
     uint32_t kth = 0xffffffffu;  // kept: key > kth, or key == kth and position <= cut
     int32_t cut = -1;
@@ -427,7 +433,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         if (dense && a.dense_elsewhere) {
             // a dense kv head of a mixed layer: appended above; its attention is the second launch.
             // The ordered selection lists every token: position p at entry p (this CTA's chunk)
-            if (a.sel != nullptr) {
+            if (has_sel) {
                 int32_t* outl = a.sel + row * a.sel_cap;
                 for (int p = lo + tid; p < hi; p += NT) {
                     if (p < a.sel_cap) outl[p] = p;
@@ -469,9 +475,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
             cluster_arrive();
         }
         const uint16_t* kbase = a.kT + kvrow * D * a.t_cap;
-        float* srow_out = a.scores_out != nullptr ? a.scores_out + row * a.score_stride : nullptr;
+        float* srow_out = (!LEAN && a.scores_out != nullptr) ? a.scores_out + row * a.score_stride : nullptr;
         if (dense) {
-        } else if (a.n_crit <= 8) {
+        } else if (LEAN || a.n_crit <= 8) {
             // one 16-byte load per channel and 8 positions; a channel's registers are refilled
             // with the next group's load as soon as they are consumed, so loads stay in flight
             // channel row offsets: c * t_cap < 128 * 360448 fits in 32 bits
@@ -561,7 +567,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         }
         if (k > 0) {
             // ---- digit 1 (key bits 31..20): from the score kernel's histogram, or this cluster's
-            if (!exchange) {
+            if (!LEAN && !exchange) {
                 const uint4* gh = reinterpret_cast<const uint4*>(a.hist + row * H1);
                 for (int i = tid; i < H1 / 4; i += NT) reinterpret_cast<uint4*>(s.v.gh)[i] = __ldcg(gh + i);
                 __syncthreads();
@@ -634,7 +640,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
             // the candidates are exchanged and the last two digits found, so that the row traffic
             // overlaps the rest of the selection (one-pass list path only)
             static_assert(CAP_S == 2 * NT, "two early list entries per thread");
-            n_early = (a.q != nullptr && a.sel == nullptr) ? min(n_s0, CAP_S) : 0;
+            n_early = (a.q != nullptr && !has_sel) ? min(n_s0, CAP_S) : 0;
             uint32_t e_pos[2];
             int32_t e_pg[2];
 #pragma unroll
@@ -681,7 +687,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                 }
             }
             cluster_wait();
-            if (a.hist != nullptr && rank == 0)  // read by all: clear it for the next layer
+            if (has_hist && rank == 0)  // read by all: clear it for the next layer
                 for (int i = tid; i < H1; i += NT) a.hist[row * H1 + i] = 0u;
             bool ovf_c = false;
             for (int r = 0; r < CL; ++r) ovf_c |= s.ncand[r] > (uint32_t)CAP_C;
@@ -801,7 +807,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
                     warp_append<uint32_t>(f, p, s.list, &s.n_s, CAP_S, lane);
                 }
                 __syncthreads();
-                listed = s.n_s <= CAP_S && a.sel == nullptr;
+                listed = s.n_s <= CAP_S && !has_sel;
             } else {
                 // ---- fallback (many candidates share digit 1, e.g. heavy ties): distributed passes
                 if (tid == 0 && rank == 0) kvq_dev_count(a.hdr, KVQ_PATH_RADIX_PASSES);
@@ -888,7 +894,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         }
     }
     // the histogram was not needed (everything kept, or k == 0): clear it for the next layer
-    if (a.hist != nullptr && rank == 0 && (keep_all || k == 0))
+    if (has_hist && rank == 0 && (keep_all || k == 0))
         for (int i = tid; i < H1; i += NT) a.hist[row * H1 + i] = 0u;
 
     const uint32_t* plist;  // kept positions of this CTA
@@ -932,7 +938,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     }
     __syncthreads();
 
-    if (a.sel != nullptr) {
+    if (has_sel) {
         // the ordered selection: this CTA's positions follow those of the lower ranks
         cluster.sync();
         uint32_t off = 0;
@@ -1094,11 +1100,14 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
 }
 
 int launch(const SXArgs& a, int batch, cudaStream_t st) {
-    const int r = kvq_prepare_kernel((const void*)select_attn_kernel, (int)smem_bytes(MAX_CHUNK));
+    const bool lean = a.kT != nullptr && a.sel == nullptr && a.scores_out == nullptr && a.hist == nullptr &&
+                      a.dense == nullptr && a.q != nullptr && a.n_crit <= 8;
+    auto kernel = lean ? select_attn_kernel<true> : select_attn_kernel<false>;
+    const int r = kvq_prepare_kernel((const void*)kernel, (int)smem_bytes(MAX_CHUNK));
     if (r) return r;
     const int chunk_cap = chunk_of(a.max_len);
     const cudaError_t e =
-        kvq_launch_pdl(select_attn_kernel, dim3(CL, a.n_heads, batch), dim3(NT), smem_bytes(chunk_cap), st, a, chunk_cap);
+        kvq_launch_pdl(kernel, dim3(CL, a.n_heads, batch), dim3(NT), smem_bytes(chunk_cap), st, a, chunk_cap);
     if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "select kernel launch: %s", cudaGetErrorString(e));
     return KVQ_OK;
 }
