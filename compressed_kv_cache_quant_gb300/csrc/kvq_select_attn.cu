@@ -339,9 +339,9 @@ __device__ __forceinline__ bool warp_append(bool f, V v, V* list, int32_t* n, in
     return base + __popc(m) <= cap;
 }
 
-// LEAN: the instance for the fused decode without optional outputs (kT given, no sel, scores_out,
-// hist or dense flags, at most 8 critical channels): the paths it never takes are not compiled in,
-// so that the instructions a CTA runs once, phase after phase, are fetched from fewer lines.
+// LEAN: the instance for the fused decode without optional outputs (kT given, no sel, scores_out or
+// hist, at most 8 critical channels; dense flags allowed): the paths it never takes are not compiled
+// in, so that the instructions a CTA runs once, phase after phase, are fetched from fewer lines.
 template <bool LEAN>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_kernel(SXArgs a, int chunk_cap) {
     extern __shared__ __align__(16) uint32_t keys[];  // the chunk's keys; later its kept positions
@@ -374,7 +374,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     const int n = hi - lo;
     // a dense head (head-level classification: quantization-friendly) attends every token: no
     // critical scores, no selection -- the same launch, dispatched by the head's class
-    const bool dense = !LEAN && a.dense != nullptr && a.dense[(int64_t)b * a.H + h / a.GQ] != 0;
+    const bool dense = a.dense != nullptr && a.dense[(int64_t)b * a.H + h / a.GQ] != 0;
     const bool keep_all = dense || (int64_t)T <= (int64_t)a.n_sink + a.window + k;
     const int cand_lo = a.n_sink, cand_hi = T - a.window;
     const float* srow = a.scores + row * a.score_stride;
@@ -1101,7 +1101,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
 
 int launch(const SXArgs& a, int batch, cudaStream_t st) {
     const bool lean = a.kT != nullptr && a.sel == nullptr && a.scores_out == nullptr && a.hist == nullptr &&
-                      a.dense == nullptr && a.q != nullptr && a.n_crit <= 8;
+                      a.q != nullptr && a.n_crit <= 8;
     auto kernel = lean ? select_attn_kernel<true> : select_attn_kernel<false>;
     const int r = kvq_prepare_kernel((const void*)kernel, (int)smem_bytes(MAX_CHUNK));
     if (r) return r;
