@@ -339,11 +339,14 @@ __device__ __forceinline__ bool warp_append(bool f, V v, V* list, int32_t* n, in
     return base + __popc(m) <= cap;
 }
 
-// LEAN: the instance for the fused decode without optional outputs (kT given, no sel, scores_out or
-// hist, at most 8 critical channels; dense flags allowed): the paths it never takes are not compiled
-// in, so that the instructions a CTA runs once, phase after phase, are fetched from fewer lines.
-template <bool LEAN>
+// MODE 1 (lean): the instance for the fused decode without optional outputs (kT given, no sel,
+// scores_out or hist, at most 8 critical channels; dense flags allowed).  MODE 2: selection only
+// (scores read from memory, no attention, no dense flags).  MODE 0: every option.  The paths an
+// instance never takes are not compiled in, so that the instructions a CTA runs once, phase after
+// phase, are fetched from fewer lines.
+template <int MODE>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_kernel(SXArgs a, int chunk_cap) {
+    constexpr bool LEAN = MODE == 1, SEL_ONLY = MODE == 2;
     extern __shared__ __align__(16) uint32_t keys[];  // the chunk's keys; later its kept positions
     SXSmem& s = *reinterpret_cast<SXSmem*>(reinterpret_cast<char*>(keys) +
                                            kvq_round_up((size_t)max(chunk_cap, 1) * sizeof(uint32_t), 16));
@@ -353,7 +356,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t row = (int64_t)b * a.n_heads + h;
     kvq_pdl_begin();
-    const bool fused = LEAN || a.kT != nullptr;
+    const bool fused = LEAN || (!SEL_ONLY && a.kT != nullptr);
     // the fused path's per-channel inputs are requested together with the length
     uint16_t pre_q = 0, pre_kn = 0;
     float pre_am = 0.0f;
@@ -374,7 +377,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     const int n = hi - lo;
     // a dense head (head-level classification: quantization-friendly) attends every token: no
     // critical scores, no selection -- the same launch, dispatched by the head's class
-    const bool dense = a.dense != nullptr && a.dense[(int64_t)b * a.H + h / a.GQ] != 0;
+    const bool dense = !SEL_ONLY && a.dense != nullptr && a.dense[(int64_t)b * a.H + h / a.GQ] != 0;
     const bool keep_all = dense || (int64_t)T <= (int64_t)a.n_sink + a.window + k;
     const int cand_lo = a.n_sink, cand_hi = T - a.window;
     const float* srow = a.scores + row * a.score_stride;
@@ -956,7 +959,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
         }
         cluster.sync();  // remote counts read before any CTA moves on or leaves
     }
-    if (a.q == nullptr) return;
+    if (SEL_ONLY || a.q == nullptr) return;
 
     // ---- attention over this CTA's kept rows
     const int g = gkv;
@@ -1102,7 +1105,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
 int launch(const SXArgs& a, int batch, cudaStream_t st) {
     const bool lean = a.kT != nullptr && a.sel == nullptr && a.scores_out == nullptr && a.hist == nullptr &&
                       a.q != nullptr && a.n_crit <= 8;
-    auto kernel = lean ? select_attn_kernel<true> : select_attn_kernel<false>;
+    const bool sel_only = a.kT == nullptr && a.q == nullptr && a.dense == nullptr;
+    auto kernel = lean ? select_attn_kernel<1> : sel_only ? select_attn_kernel<2> : select_attn_kernel<0>;
     const int r = kvq_prepare_kernel((const void*)kernel, (int)smem_bytes(MAX_CHUNK));
     if (r) return r;
     const int chunk_cap = chunk_of(a.max_len);
