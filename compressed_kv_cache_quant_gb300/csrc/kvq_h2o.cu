@@ -528,17 +528,25 @@ __global__ void __launch_bounds__(DP_NT) dp_row_kernel(DPArgs a) {
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
             if (t4 < L4) x = src[t4];
             const float v[4] = {x.x, x.y, x.z, x.w};
+            bool cf[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const bool ok = 4 * t4 + e < L;
                 const uint32_t bin = ok ? kvq_float_key(v[e]) >> 21 : 0u;
                 if (ok && bin > b1) top += exp2f(v[e] - M);
-                const bool c = ok && bin == b1;
-                const uint32_t bal = __ballot_sync(0xffffffffu, c);
-                uint32_t base = 0;
-                if (lane == 0 && bal != 0u) base = atomicAdd(&n_cand, (uint32_t)__popc(bal));
-                base = __shfl_sync(0xffffffffu, base, 0) + (uint32_t)__popc(bal & ((1u << lane) - 1u));
-                if (c && base < (uint32_t)DP_CAND) cand[base] = v[e];
+                cf[e] = ok && bin == b1;
+            }
+            // candidates are rare (one bin of 2048): one vote per group of four, the slots only
+            // when a lane of the warp has one
+            if (__any_sync(0xffffffffu, cf[0] || cf[1] || cf[2] || cf[3])) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t bal = __ballot_sync(0xffffffffu, cf[e]);
+                    uint32_t base = 0;
+                    if (lane == 0 && bal != 0u) base = atomicAdd(&n_cand, (uint32_t)__popc(bal));
+                    base = __shfl_sync(0xffffffffu, base, 0) + (uint32_t)__popc(bal & ((1u << lane) - 1u));
+                    if (cf[e] && base < (uint32_t)DP_CAND) cand[base] = v[e];
+                }
             }
         }
         for (int j = tid; j < DP_H1; j += DP_NT) hist[j] = 0u;
