@@ -160,6 +160,7 @@ __device__ int h2o_evict_many(int32_t* ret, float* cum, int n, int excess, int n
 __global__ void __launch_bounds__(HA_NT) h2o_kernel(H2OArgs a) {
     __shared__ unsigned long long redk[HA_NT / 32];
     const int g = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    kvq_pdl_begin();
     const int Hq = a.H * a.GQ;
     const int64_t base = ((int64_t)b * a.H + g) * a.cap;
     int32_t* ret = a.retained + base;
@@ -694,7 +695,8 @@ extern "C" int kv_h2o_accumulate(const kvq_layout* L, const kvq_seqs* S, const f
     a.H = L->n_kv_heads;
     a.GQ = L->n_q_heads / L->n_kv_heads;
     a.hdr = static_cast<KvqWsHeader*>(ws);
-    h2o_kernel<<<dim3(L->n_kv_heads, S->batch), HA_NT, 0, kvq_stream(stream)>>>(a);
+    const cudaError_t e = kvq_launch_pdl(h2o_kernel, dim3(L->n_kv_heads, S->batch), dim3(HA_NT), 0, kvq_stream(stream), a);
+    if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_h2o_accumulate launch: %s", cudaGetErrorString(e));
     return kvq_launch_status("kv_h2o_accumulate");
 }
 

@@ -355,7 +355,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 2) select_attn_
     const int h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t row = (int64_t)b * a.n_heads + h;
-    kvq_pdl_begin();
+    if constexpr (SEL_ONLY) {
+        // wait for the previous kernel; the next one (an attention over the selection) is scheduled
+        // when this grid exits: an early trigger would let its CTAs hold SMs beside these clusters
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    } else {
+        kvq_pdl_begin();
+    }
     const bool fused = LEAN || (!SEL_ONLY && a.kT != nullptr);
     // the fused path's per-channel inputs are requested together with the length
     uint16_t pre_q = 0, pre_kn = 0;

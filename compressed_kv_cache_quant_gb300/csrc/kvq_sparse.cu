@@ -367,6 +367,10 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
     // whatever the lists' lengths, are scheduled first
     const int list = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x;
+    // dependent launch: wait for the previous kernel here; let the next one be scheduled only once
+    // this CTA's rows are done (an earlier trigger lets a cluster kernel that follows place its
+    // CTAs piecemeal while these still hold the SMs)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n_lists = a.per_kv ? a.H : a.H * a.GQ;
     const int Hq = a.H * a.GQ;
     const int g = a.per_kv ? list : list / a.GQ;
@@ -515,6 +519,7 @@ __global__ void __launch_bounds__(SA_NT) sparse_attn_kernel(SAArgs a) {
         stage(t + SA_STAGES * SA_NW, buf);
     }
     sa_wait<0>();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
     // ---- merge the warp states of the CTA (the records reuse the tile buffers)
@@ -701,7 +706,7 @@ size_t sa_ws_layout(const kvq_layout* L, const kvq_seqs* S, int32_t sel_cap, siz
 }
 
 template <int NH>
-int launch_sa(const SAArgs& a, dim3 grid, cudaStream_t s) {
+int launch_sa(const SAArgs& a, dim3 grid, cudaStream_t s, bool pdl = true) {
     static_assert((size_t)SA_NW * 8 * SA_REC * sizeof(float) <= (size_t)SA_TILES, "the warp states fit the tiles");
     const size_t smem = (size_t)sa_tiles(NH) + (size_t)a.rps * sizeof(uint32_t);
     const int st = kvq_prepare_kernel((const void*)sparse_attn_kernel<NH>,
@@ -713,7 +718,14 @@ int launch_sa(const SAArgs& a, dim3 grid, cudaStream_t s) {
     SAArgs b = a;
     const int64_t units = (int64_t)grid.x * grid.z;
     b.k_target = (int)std::max<int64_t>(1, (int64_t)std::max(occ, 1) * kvq_num_sms() / std::max<int64_t>(units, 1));
-    sparse_attn_kernel<NH><<<grid, SA_NT, smem, s>>>(b);
+    // a dependent launch (it may be scheduled while the previous kernel finishes), except after the
+    // mixed layer's cluster kernel, whose early trigger would only queue these CTAs behind it
+    if (!pdl) {
+        sparse_attn_kernel<NH><<<grid, SA_NT, smem, s>>>(b);
+        return kvq_launch_status("kv_sparse_attn");
+    }
+    const cudaError_t e = kvq_launch_pdl(sparse_attn_kernel<NH>, grid, dim3(SA_NT), smem, s, b);
+    if (e != cudaSuccess) return kvq_fail(KVQ_ERR_CUDA, "kv_sparse_attn launch: %s", cudaGetErrorString(e));
     return kvq_launch_status("kv_sparse_attn");
 }
 
@@ -903,10 +915,10 @@ int kvq_dense_heads_attn(const kvq_layout* L, const kvq_pool* P, const kvq_seqs*
     a.all_tokens = 1;
     const dim3 grid(L->n_kv_heads, p.n_splits, S->batch);
     switch (a.GQ) {
-        case 1: return launch_sa<1>(a, grid, s);
-        case 2: return launch_sa<2>(a, grid, s);
-        case 4: return launch_sa<4>(a, grid, s);
-        default: return launch_sa<8>(a, grid, s);
+        case 1: return launch_sa<1>(a, grid, s, false);
+        case 2: return launch_sa<2>(a, grid, s, false);
+        case 4: return launch_sa<4>(a, grid, s, false);
+        default: return launch_sa<8>(a, grid, s, false);
     }
 }
 
