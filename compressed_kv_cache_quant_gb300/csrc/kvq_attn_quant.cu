@@ -15,9 +15,13 @@
 // afterwards); the bias sum_c q_c scale_c 2^b joins the zero-point term.  With V = vscale_t
 // code + vzero_t per token and V group,
 //   o[d] = sum_t p_t (vscale_t code_t[d] + vzero_t)
-// is a [128 x tokens] x [tokens x heads] product: the V codes (stored
-// channel-major per page, kvq_v_code_pos) dequantized into fp16 by one fp16
-// FMA per pair, against p_t in fp16.  The group's codes and scales are staged per warp with cp.async, one
+// is a [128 x tokens] x [tokens x columns] product whose A operand is the V codes (stored
+// channel-major per page, kvq_v_code_pos) made exact fp16 numbers.  When the heads times the V
+// groups per token fit the product's eight columns (all but 4 heads with 32-dim V groups), column
+// NGV h + j holds fp16(2^8 p_t vscale_t) of head h and V group j (the softmax weights taken as
+// 2^8 p, which the normalisation cancels), the zero points join as an fp32 sum of p_t vzero_t per column, and a channel's output is read from its group's column; otherwise
+// the A operand is fp16(vscale_t code + vzero_t), one more fp16 FMA per pair, against p_t in fp16
+// (column 2h).  The group's codes and scales are staged per warp with cp.async, one
 // group ahead.  An unfinished K group reads its keys from the fp16 tail buffer.
 #include <algorithm>
 
@@ -304,7 +308,14 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), OUT && BITS == 4 ? 6 : 
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[mt][i] = 0.0f;
     float mrun = -INFINITY, lrun = 0.0f;
-    const int hs = g8 >> 1;  // the head of this lane's score rows (slot g8 = 2 hs + hi/lo)
+    [[maybe_unused]] const int hs = g8 >> 1;  // the head of this lane's score rows (slot g8 = 2 hs + hi/lo)
+    // With GQ NGV <= 8 the value product's eight B columns hold one (head, V group) each: column
+    // g8 = NGV h + j, so that the V scales go into B and the codes enter the A operand as they are
+    constexpr bool VCOL = GQ * NGV <= 8;
+    [[maybe_unused]] const int jn = g8 % NGV;                 // this lane's B column: V group jn
+    [[maybe_unused]] const bool vcol = g8 / NGV < GQ;         //   of head g8 / NGV, if present
+    [[maybe_unused]] const int vsrc = min(g8 / NGV, GQ - 1);  // (clamped: a lane to read from)
+    float zacc = 0.0f;  // sum_t p_t vzero_t of column g8 over this lane's tokens
     // outlier form: the score product gets one more k-step per m-tile whose k slots are the
     // outlier channels j < n_out (k = 2 q4, 2 q4 + 1 in this lane's registers): B column 2h holds
     // q of head h at channel c_j (fp16, exact), A the staged fp16 outlier keys of the tokens
@@ -456,57 +467,135 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), OUT && BITS == 4 ? 6 : 
         gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 16));
         const float mn = fmaxf(mrun, gm);
         const float alpha = mn == -INFINITY ? 1.0f : exp2f(mrun - mn);
+        // with the V scales in B the weights are taken as 2^8 p (l and o scale alike, o / l does
+        // not change), so that fp16(2^8 p vscale) stays normal down to p vscale = 2^-22
+        const float mp = VCOL ? mn - 8.0f : mn;
         float ls = 0.0f;
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const float p = mn == -INFINITY ? 0.0f : exp2f(sc[mt][e] - mn);
+                const float p = mn == -INFINITY ? 0.0f : exp2f(sc[mt][e] - mp);
                 sc[mt][e] = p;
                 ls += p;
             }
         mrun = mn;
         lrun = fmaf(lrun, alpha, ls);
-        // the accumulator columns belong to head q4 too
+        if constexpr (VCOL) {
+            // accumulator column n = 2 q4 + c is (head n / NGV, V group n % NGV); only the m-tiles
+            // of that group are read at the end
+            float al0 = alpha, al1 = alpha;
+            if constexpr (NGV != 2) {
+                al0 = __shfl_sync(0xffffffffu, alpha, min((2 * q4) / NGV, GQ - 1));
+                al1 = __shfl_sync(0xffffffffu, alpha, min((2 * q4 + 1) / NGV, GQ - 1));
+            }
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            acc[mt][0] *= alpha;
-            acc[mt][2] *= alpha;
+            for (int mt = 0; mt < 8; ++mt) {
+                const int j = (mt * NGV) >> 3;  // resolved at compile time
+                if (NGV == 1 || (j & 1) == 0) {
+                    acc[mt][0] *= al0;
+                    acc[mt][2] *= al0;
+                }
+                if (NGV == 1 || (j & 1) == 1) {
+                    acc[mt][1] *= al1;
+                    acc[mt][3] *= al1;
+                }
+            }
+            zacc *= __shfl_sync(0xffffffffu, alpha, vsrc);  // column g8's head
+        } else {
+            // the accumulator columns belong to head q4 too
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                acc[mt][0] *= alpha;
+                acc[mt][2] *= alpha;
+            }
         }
 
-        // ---- values, page by page: the A operand is the dequantized V, fp16(vscale code + vzero)
-        // (the codes' pair at tokens 2q4, 2q4 + 1 and 2q4 + 8, 2q4 + 9 of the page, channels g8 and
-        // g8 + 8 of the m-tile); the B column g8 = 2h carries fp16(p) of head h, odd columns 0
-        const bool even = (g8 & 1) == 0 && hs < GQ;
+        if constexpr (VCOL) {
+            // ---- values: the A operand is the codes themselves (exact in fp16: the pair at tokens
+            // 2q4, 2q4 + 1 and 2q4 + 8, 2q4 + 9 of page ks, channels g8 and g8 + 8 of the m-tile); B
+            // column g8 = NGV h + j carries fp16(2^8 p_t vscale_t) of head h and V group j, and the
+            // zero points join as sum_t p_t vzero_t per column, in fp32.  The code and zero-point
+            // sums are of similar size and opposite sign, so the tensor cores sum one group at a
+            // time from zero and the group's sums join the running ones by fp32 additions.
+            uint32_t bb[4][2];
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            // p of head hs at the page's tokens 2q4, 2q4 + 1, 2q4 + 8, 2q4 + 9: token y sits in lane
-            // 4 (y mod 8) + hs, register e = y / 8 of m-tile ks
-            const float p0 = __shfl_sync(0xffffffffu, sc[ks][0], 8 * q4 + hs);
-            const float p1 = __shfl_sync(0xffffffffu, sc[ks][0], 8 * q4 + 4 + hs);
-            const float p2 = __shfl_sync(0xffffffffu, sc[ks][1], 8 * q4 + hs);
-            const float p3 = __shfl_sync(0xffffffffu, sc[ks][1], 8 * q4 + 4 + hs);
-            const uint32_t b0 = even ? pack_h2(p0, p1) : 0u;
-            const uint32_t b1 = even ? pack_h2(p2, p3) : 0u;
-            const int tb = 16 * ks + 2 * q4;  // the lane's first token in the group
-            const int nv = T - t0 - tb;       // tokens tb, tb + 1 valid if > 0, > 1; tb + 8, + 9 if > 8, > 9
-            const uint32_t* vblk = st.v + ks * 64 * BITS;
+            for (int ks = 0; ks < 4; ++ks) {
+                // p of head vsrc at the page's tokens 2q4, 2q4 + 1, 2q4 + 8, 2q4 + 9: token y sits
+                // in lane 4 (y mod 8) + vsrc, register e = y / 8 of m-tile ks
+                const float p0 = __shfl_sync(0xffffffffu, sc[ks][0], 8 * q4 + vsrc);
+                const float p1 = __shfl_sync(0xffffffffu, sc[ks][0], 8 * q4 + 4 + vsrc);
+                const float p2 = __shfl_sync(0xffffffffu, sc[ks][1], 8 * q4 + vsrc);
+                const float p3 = __shfl_sync(0xffffffffu, sc[ks][1], 8 * q4 + 4 + vsrc);
+                const int tb = 16 * ks + 2 * q4;             // the lane's first token in the group
+                const int nv = vcol ? T - t0 - tb : 0;       // tokens tb, tb + 1 valid if > 0, > 1; tb + 8, + 9 if > 8, > 9
+                const uint32_t* vz = st.vsz + tb * NGV + jn;  // (scale, zero) of V group jn per token
+                // masked tokens and absent columns: scale and zero 0 (their staged words may hold anything)
+                const float2 u0 = unpack_h2(nv > 0 ? vz[0] : 0u);
+                const float2 u1 = unpack_h2(nv > 1 ? vz[NGV] : 0u);
+                const float2 u2 = unpack_h2(nv > 8 ? vz[8 * NGV] : 0u);
+                const float2 u3 = unpack_h2(nv > 9 ? vz[9 * NGV] : 0u);
+                // 2^8 p vscale must stay finite in fp16: |vscale| < 256
+                if (!(fmaxf(fmaxf(fabsf(u0.x), fabsf(u1.x)), fmaxf(fabsf(u2.x), fabsf(u3.x))) < 256.0f))
+                    kvq_dev_flag(a.hdr, KVQ_DEV_RANGE, b);
+                bb[ks][0] = pack_h2(p0 * u0.x, p1 * u1.x);
+                bb[ks][1] = pack_h2(p2 * u2.x, p3 * u3.x);
+                zacc = fmaf(p0, u0.y, fmaf(p1, u1.y, fmaf(p2, u2.y, fmaf(p3, u3.y, zacc))));
+            }
 #pragma unroll
-            for (int j = 0; j < NGV; ++j) {  // V group j: m-tiles [8j / NGV, 8(j + 1) / NGV)
-                // (scale, zero) words of the lane's tokens; masked tokens may hold anything: zero them
-                const uint32_t w0 = nv > 0 ? st.vsz[tb * NGV + j] : 0u;
-                const uint32_t w1 = nv > 1 ? st.vsz[(tb + 1) * NGV + j] : 0u;
-                const uint32_t w2 = nv > 8 ? st.vsz[(tb + 8) * NGV + j] : 0u;
-                const uint32_t w3 = nv > 9 ? st.vsz[(tb + 9) * NGV + j] : 0u;
-                const uint32_t s01 = prmt(w0, w1, 0x5410u), z01 = prmt(w0, w1, 0x7632u);
-                const uint32_t s23 = prmt(w2, w3, 0x5410u), z23 = prmt(w2, w3, 0x7632u);
+            for (int mt = 0; mt < 8; ++mt) {
+                float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    if (((mt * NGV) >> 3) != j) continue;  // resolved at compile time
+                for (int ks = 0; ks < 4; ++ks) {
                     uint32_t A[4];
-                    v_pairs<BITS>(vblk + (8 * mt + g8) * BITS, q4, A);
-                    mma16816(acc[mt], hfma2(A[0], s01, z01), hfma2(A[1], s01, z01), hfma2(A[2], s23, z23),
-                             hfma2(A[3], s23, z23), b0, b1);
+                    v_pairs<BITS>(st.v + ks * 64 * BITS + (8 * mt + g8) * BITS, q4, A);
+                    mma16816(d, A[0], A[1], A[2], A[3], bb[ks][0], bb[ks][1]);
+                }
+                const int j = (mt * NGV) >> 3;  // resolved at compile time: the columns read at the end
+                if (NGV == 1 || (j & 1) == 0) {
+                    acc[mt][0] += d[0];
+                    acc[mt][2] += d[2];
+                }
+                if (NGV == 1 || (j & 1) == 1) {
+                    acc[mt][1] += d[1];
+                    acc[mt][3] += d[3];
+                }
+            }
+        } else {
+            // ---- values, page by page: the A operand is the dequantized V, fp16(vscale code + vzero)
+            // (the codes' pair at tokens 2q4, 2q4 + 1 and 2q4 + 8, 2q4 + 9 of the page, channels g8 and
+            // g8 + 8 of the m-tile); the B column g8 = 2h carries fp16(p) of head h, odd columns 0
+            const bool even = (g8 & 1) == 0 && hs < GQ;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                // p of head hs at the page's tokens 2q4, 2q4 + 1, 2q4 + 8, 2q4 + 9: token y sits in lane
+                // 4 (y mod 8) + hs, register e = y / 8 of m-tile ks
+                const float p0 = __shfl_sync(0xffffffffu, sc[ks][0], 8 * q4 + hs);
+                const float p1 = __shfl_sync(0xffffffffu, sc[ks][0], 8 * q4 + 4 + hs);
+                const float p2 = __shfl_sync(0xffffffffu, sc[ks][1], 8 * q4 + hs);
+                const float p3 = __shfl_sync(0xffffffffu, sc[ks][1], 8 * q4 + 4 + hs);
+                const uint32_t b0 = even ? pack_h2(p0, p1) : 0u;
+                const uint32_t b1 = even ? pack_h2(p2, p3) : 0u;
+                const int tb = 16 * ks + 2 * q4;  // the lane's first token in the group
+                const int nv = T - t0 - tb;       // tokens tb, tb + 1 valid if > 0, > 1; tb + 8, + 9 if > 8, > 9
+                const uint32_t* vblk = st.v + ks * 64 * BITS;
+#pragma unroll
+                for (int j = 0; j < NGV; ++j) {  // V group j: m-tiles [8j / NGV, 8(j + 1) / NGV)
+                    // (scale, zero) words of the lane's tokens; masked tokens may hold anything: zero them
+                    const uint32_t w0 = nv > 0 ? st.vsz[tb * NGV + j] : 0u;
+                    const uint32_t w1 = nv > 1 ? st.vsz[(tb + 1) * NGV + j] : 0u;
+                    const uint32_t w2 = nv > 8 ? st.vsz[(tb + 8) * NGV + j] : 0u;
+                    const uint32_t w3 = nv > 9 ? st.vsz[(tb + 9) * NGV + j] : 0u;
+                    const uint32_t s01 = prmt(w0, w1, 0x5410u), z01 = prmt(w0, w1, 0x7632u);
+                    const uint32_t s23 = prmt(w2, w3, 0x5410u), z23 = prmt(w2, w3, 0x7632u);
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        if (((mt * NGV) >> 3) != j) continue;  // resolved at compile time
+                        uint32_t A[4];
+                        v_pairs<BITS>(vblk + (8 * mt + g8) * BITS, q4, A);
+                        mma16816(acc[mt], hfma2(A[0], s01, z01), hfma2(A[1], s01, z01), hfma2(A[2], s23, z23),
+                                 hfma2(A[3], s23, z23), b0, b1);
+                    }
                 }
             }
         }
@@ -519,12 +608,36 @@ __global__ void __launch_bounds__(32 * nwarp_of<BITS>(), OUT && BITS == 4 ? 6 : 
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 4);
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 8);
     lrun += __shfl_xor_sync(0xffffffffu, lrun, 16);
-    __syncthreads();  // every warp is done with its stages: the union now holds the outputs
-    if (q4 < GQ) {
+    if constexpr (VCOL) {
+        // the zero-point sums of the columns: column n is summed over its four lanes 4n .. 4n + 3;
+        // this lane's accumulator columns are 2 q4 and 2 q4 + 1
+        zacc += __shfl_xor_sync(0xffffffffu, zacc, 1);
+        zacc += __shfl_xor_sync(0xffffffffu, zacc, 2);
+        const float z0 = __shfl_sync(0xffffffffu, zacc, 8 * q4);
+        const float z1 = __shfl_sync(0xffffffffu, zacc, 8 * q4 + 4);
+        __syncthreads();  // every warp is done with its stages: the union now holds the outputs
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            S.u.ro[warp][q4][16 * mt + g8] = acc[mt][0];
-            S.u.ro[warp][q4][16 * mt + g8 + 8] = acc[mt][2];
+        for (int c = 0; c < 2; ++c) {
+            const int n = 2 * q4 + c, h = n / NGV;
+            const int jc = NGV == 2 ? c : n % NGV;  // the column's V group
+            const float z = c ? z1 : z0;
+            if (h < GQ) {
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    if (((mt * NGV) >> 3) != jc) continue;
+                    S.u.ro[warp][h][16 * mt + g8] = acc[mt][c] + z;
+                    S.u.ro[warp][h][16 * mt + g8 + 8] = acc[mt][2 + c] + z;
+                }
+            }
+        }
+    } else {
+        __syncthreads();  // every warp is done with its stages: the union now holds the outputs
+        if (q4 < GQ) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                S.u.ro[warp][q4][16 * mt + g8] = acc[mt][0];
+                S.u.ro[warp][q4][16 * mt + g8 + 8] = acc[mt][2];
+            }
         }
     }
     if (g8 == 0 && q4 < GQ) {

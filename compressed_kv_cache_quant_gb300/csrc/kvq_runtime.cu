@@ -150,7 +150,7 @@ extern "C" int kvq_check(void* ws, void* stream) {
     if (hdr[0] != 0) {
         static const char* names[] = {"ok", "page id outside the pool", "token id outside the sequence",
                                       "sequence length outside its bounds", "list capacity exceeded",
-                                      "query times K scale beyond the fp16 range",
+                                      "an operand beyond the fp16 range (query times K scale, or a V scale)",
                                       "a bounded wait for an asynchronous copy gave up"};
         const char* nm = (hdr[0] > 0 && hdr[0] <= 6) ? names[hdr[0]] : "unknown";
         int32_t zero[2] = {0, 0};

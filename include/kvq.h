@@ -233,11 +233,14 @@ size_t kv_page_append_ws(void);
  * Packed tokens use dequantized K (zero + code*scale with the stored fp16
  * scale/zero); tail tokens use their fp16 keys exactly; V is dequantized.
  * Both products run on the tensor cores with fp32 accumulation: q*scale
- * enters as two fp16 halves (about 22 bits), the dequantized V rows and the
- * softmax weights as fp16 (relative rounding 2^-11 per element, averaging
- * out over the tokens).  |q_c * scale_c| * 2^bits must stay below 32768 (the
- * fp16 operand range); otherwise the status word reports a range error and
- * the output is not valid.  The context is split across CTAs and the
+ * enters as two fp16 halves (about 22 bits); for the values, either (heads
+ * per kv head times V groups per token <= 8) the V codes enter exactly against
+ * fp16(2^8 p * vscale) per token, with the zero points summed in fp32, or (4
+ * heads with 32-dim V groups) the dequantized V rows against the softmax
+ * weights, both fp16 (relative rounding 2^-11 per element, averaging out over
+ * the tokens).  |q_c * scale_c| * 2^bits must stay below 32768 and, on the
+ * first form, |vscale| below 256 (the fp16 operand range); otherwise the
+ * status word reports a range error and the output is not valid.  The context is split across CTAs and the
  * partial softmax states are merged by log-sum-exp.  An empty sequence gives 0.
  * An FP8 E4M3 layer (bits == KVQ_BITS_E4M3) is attended the same way: its
  * pages are staged into shared memory by bulk asynchronous copies, keys and

@@ -77,7 +77,30 @@ def test_mha_int4_shared_prefix():
     _run(4, 32, 8, 8, lengths, synth.mix(synth.BASE_SEED + 2, 3), share=(256, [0, 1, 2]))
 
 
-@pytest.mark.parametrize("gq", [1, 2, 8])
-def test_gqa_widths(gq):
+@pytest.mark.parametrize("gq,G", [(1, 64), (2, 64), (8, 64), (2, 32), (1, 128)])
+def test_gqa_widths(gq, G):
+    """Query heads per kv head against V groups per token: the value product gives each
+    (head, V group) a column of its own when they fit (2 heads x 4 groups fill all eight)."""
     require_gpu()
-    _run(2, 64, 2 * gq, 2, [333, 900], synth.mix(synth.BASE_SEED, 4, gq))
+    seed = synth.mix(synth.BASE_SEED, 4, gq) if G == 64 else synth.mix(synth.BASE_SEED, 4, gq, G)
+    _run(2, G, 2 * gq, 2, [333, 900], seed)
+
+
+def test_v_scale_beyond_fp16_range_is_flagged():
+    """With the V scales in the value product's B operand as fp16(2^8 p vscale), a V group
+    whose scale reaches 256 (1-bit codes of values up to about +-1000) is reported as a
+    range error by the status word rather than giving an invalid output silently."""
+    require_gpu()
+    T, Hq, Hkv = 256, 8, 2
+    K, V = synth.kv_rows(T, Hkv, synth.mix(synth.BASE_SEED, 5))
+    V = (V.float() * 300.0).to(torch.float16)
+    alloc = kvq.Allocator(T // 16 + 4, seed=5)
+    batch, bt = paged_batch([T], alloc, lengths=[T])
+    cache = kvq.LayerCache(Hq, Hkv, 1, T // 16 + 4, 1, v_group_dims=64)
+    kvq.kv_quant_pack(cache, batch, 0, 0, T, K.cuda(), V.cuda())
+    q = synth.queries((1, Hq, 128), synth.mix(synth.BASE_SEED, 6))
+    out = torch.empty((1, Hq, 128), device="cuda")
+    w = ws(kvq.kv_decode_attn_quant_ws(cache, batch))
+    kvq.kv_decode_attn_quant(cache, batch, q.cuda(), out, w)
+    with pytest.raises(kvq.KvqError, match="fp16 range"):
+        kvq.kvq_check(w)
