@@ -229,3 +229,36 @@ def test_outlier_and_dense_pref_validation(lib):
     nw = lib.kv_dense_pref_score_ws(by(Lw), by(S2), 64)
     assert lib.kv_dense_pref_score(by(Lw), by(Pk), by(S2), fake, 64, 8, fake, fake, nw, None) \
         == _abi.KVQ_ERR_UNSUPPORTED
+
+
+def _plan(lib, L, S, noalloc=0):
+    n, g = ctypes.c_int32(), ctypes.c_int32()
+    st = lib.kv_decode_attn_quant_plan(ctypes.byref(L), ctypes.byref(S), noalloc, ctypes.byref(n), ctypes.byref(g))
+    assert st == _abi.KVQ_OK, _abi.last_error()
+    return n.value, g.value
+
+
+def test_quant_attention_split_plans(lib):
+    """The context split of the quantized attention (a host-only query) covers every 64-token
+    group exactly once, (n - 1) cps < groups <= n cps, in its three regimes: one long sequence
+    (splits fill one wave of resident CTAs: the 1-bit 128K layer takes more than 16 groups a
+    split, so each of a CTA's 16 warps loops through its double buffer), a batch of many units
+    (a fixed 32 groups a split) and a short sequence (one split); the allocation-free plan never
+    takes more splits than the workspace plan."""
+    cases = [  # (layout, batch, longest sequence)
+        (kvq.make_layout(32, 8, 1, 64), 1, 131072 + 37),
+        (kvq.make_layout(32, 32, 4, 32), 16, 32768),
+        (kvq.make_layout(8, 2, 1, 64), 1, 100),
+    ]
+    plans = []
+    for L, B, T in cases:
+        S = _abi.Seqs(None, None, B, (T + 15) // 16, T, 0)
+        groups = (T + 63) // 64
+        n, cps = _plan(lib, L, S)
+        assert n >= 1 and cps >= 1 and (n - 1) * cps < groups <= n * cps, (n, cps, groups)
+        n2, cps2 = _plan(lib, L, S, 1)
+        assert 1 <= n2 <= n and (n2 - 1) * cps2 < groups <= n2 * cps2, (n2, cps2, groups)
+        plans.append((n, cps))
+    assert plans[0][1] > 16
+    assert plans[1][1] == 32
+    assert plans[2] == (1, 2)
